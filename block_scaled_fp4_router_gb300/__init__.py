@@ -1,0 +1,203 @@
+"""Python binding of libmoefp4 (C ABI in include/moefp4.h).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls, takes torch tensors (device memory) or raw integer pointers,
+passes the current torch CUDA stream unless one is given, and raises
+MoeError on a non-OK status.  Every step of the layer runs in the library's
+own CUDA kernels; there is no fallback: if the library is not built, loading
+it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoefp4.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_TIMEOUT = 4
+MOE_ERR_WORKSPACE = 5
+MOE_W_MXFP4 = 1
+MOE_W_NVFP4 = 2
+
+EXPORTED = [
+    "moe_status_string", "moe_workspace_size", "moe_get_status", "moe_router_topk",
+    "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
+    "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
+]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s returned %s" % (where, _status_name(status)))
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "top_k", "renormalize", "act_quant")]
+
+
+class Experts(ctypes.Structure):
+    _fields_ = [
+        ("fmt", ctypes.c_int),
+        ("w13", ctypes.c_void_p),
+        ("w13_scale", ctypes.c_void_p),
+        ("w2", ctypes.c_void_p),
+        ("w2_scale", ctypes.c_void_p),
+        ("tensor_scale", ctypes.c_void_p),
+    ]
+
+
+class SharedBF16(ctypes.Structure):
+    _fields_ = [("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoefp4.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "libmoefp4.so is not built (expected at %s); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+    lib = ctypes.CDLL(path)
+    P, S, I32, U64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_uint64
+    sig = {
+        "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "moe_workspace_size": ([P, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+        "moe_get_status": ([P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+        "moe_router_topk": ([P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
+        "moe_quant_act_mxfp4": ([I32, I32, P, P, P, P], ctypes.c_int),
+        "moe_permute": ([P, P, P, P, P, P, P, S, P], ctypes.c_int),
+        "moe_expert_ffn_fp4": ([P, P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
+        "moe_combine": ([P, P, P, P, P, P, P], ctypes.c_int),
+        "moe_layer_decode": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
+        "moe_layer_forward": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
+        "moe_set_wait_limit_ns": ([U64], None),
+        "moe_debug_wait_probe": ([P, S, U64, P], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _status_name(st: int) -> str:
+    try:
+        return load().moe_status_string(st).decode()
+    except Exception:  # library not loadable: report the number
+        return "status %d" % st
+
+
+def _p(t):
+    """Device pointer of a tensor, an int pointer, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != MOE_OK:
+        raise MoeError(st, where)
+
+
+def desc(T, H, I, E, top_k) -> LayerDesc:
+    return LayerDesc(T, H, I, E, top_k, 1, 1)
+
+
+def experts(fmt, w13, w13_scale, w2, w2_scale, tensor_scale=None) -> Experts:
+    return Experts(fmt, _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(tensor_scale))
+
+
+def shared_bf16(w13=None, w2=None) -> SharedBF16:
+    return SharedBF16(_p(w13), _p(w2))
+
+
+# ---------------------------------------------------------------- entry points
+
+
+def moe_status_string(st: int) -> str:
+    return load().moe_status_string(st).decode()
+
+
+def moe_workspace_size(d: LayerDesc) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().moe_workspace_size(ctypes.byref(d), ctypes.byref(out)), "moe_workspace_size")
+    return out.value
+
+
+def moe_get_status(ws) -> int:
+    st = ctypes.c_int(0)
+    _check(load().moe_get_status(_p(ws), ctypes.byref(st)), "moe_get_status")
+    return st.value
+
+
+def moe_set_wait_limit_ns(ns: int) -> None:
+    load().moe_set_wait_limit_ns(int(ns))
+
+
+def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
+    _check(load().moe_debug_wait_probe(_p(ws), _nbytes(ws), int(limit_ns), _stream(stream)),
+           "moe_debug_wait_probe")
+
+
+def moe_router_topk(d, x, w_router, bias, topk_ids, topk_w, logits, ws, stream=None):
+    _check(load().moe_router_topk(ctypes.byref(d), _p(x), _p(w_router), _p(bias), _p(topk_ids), _p(topk_w),
+                                  _p(logits), _p(ws), _nbytes(ws), _stream(stream)), "moe_router_topk")
+
+
+def moe_quant_act_mxfp4(rows, K, x, codes, scales, stream=None):
+    _check(load().moe_quant_act_mxfp4(int(rows), int(K), _p(x), _p(codes), _p(scales), _stream(stream)),
+           "moe_quant_act_mxfp4")
+
+
+def moe_permute(d, topk_ids, counts, offsets, perm, inv_perm, ws, stream=None):
+    _check(load().moe_permute(ctypes.byref(d), _p(topk_ids), _p(counts), _p(offsets), _p(perm), _p(inv_perm),
+                              _p(ws), _nbytes(ws), _stream(stream)), "moe_permute")
+
+
+def moe_expert_ffn_fp4(d, ex, sh, x, xq, xs, offsets, perm, y_assign, y_shared, ws, stream=None):
+    _check(load().moe_expert_ffn_fp4(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh), _p(x), _p(xq), _p(xs),
+                                     _p(offsets), _p(perm), _p(y_assign), _p(y_shared), _p(ws), _nbytes(ws),
+                                     _stream(stream)), "moe_expert_ffn_fp4")
+
+
+def moe_combine(d, y_assign, inv_perm, topk_w, y_shared, out, stream=None):
+    _check(load().moe_combine(ctypes.byref(d), _p(y_assign), _p(inv_perm), _p(topk_w), _p(y_shared), _p(out),
+                              _stream(stream)), "moe_combine")
+
+
+def moe_layer_decode(d, ex, sh, w_router, bias, x, out, topk_ids, topk_w, ws, stream=None):
+    _check(load().moe_layer_decode(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh), _p(w_router), _p(bias),
+                                   _p(x), _p(out), _p(topk_ids), _p(topk_w), _p(ws), _nbytes(ws),
+                                   _stream(stream)), "moe_layer_decode")
+
+
+def moe_layer_forward(d, ex, sh, w_router, bias, x, out, topk_ids, topk_w, ws, stream=None):
+    _check(load().moe_layer_forward(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh), _p(w_router), _p(bias),
+                                    _p(x), _p(out), _p(topk_ids), _p(topk_w), _p(ws), _nbytes(ws),
+                                    _stream(stream)), "moe_layer_forward")

@@ -1,0 +1,242 @@
+// The C ABI of libmoefp4 (declared in include/moefp4.h): argument validation
+// on the host, workspace carving, and the launch sequences of the unfused and
+// fused layer paths.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "../../include/moefp4.h"
+#include "kernels.h"
+#include "layout.h"
+
+using namespace moefp4;
+
+namespace {
+
+std::atomic<uint64_t> g_wait_limit_ns{500ull * 1000 * 1000};
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status_t check_desc(const moe_layer_desc_t* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->H % 128 || d->I % 128) return MOE_ERR_INVALID_ARG;
+  if (d->top_k < 1 || d->top_k > MAX_TOPK || d->E < d->top_k || d->E > MAX_E) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)d->T * d->top_k > (int64_t)1 << 30) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)d->H > (1 << 20) || (int64_t)d->I > (1 << 20)) return MOE_ERR_INVALID_ARG;
+  if (d->renormalize != 1 || d->act_quant != 1) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_layer_desc_t* d, void* ws, size_t ws_bytes) {
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(d->T, d->H, d->I, d->E, d->top_k).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status_t check_experts(const moe_layer_desc_t* d, const moe_experts_t* ex, ExpertsDev* out) {
+  if (!ex) return MOE_ERR_INVALID_ARG;
+  if (ex->fmt != MOE_W_MXFP4 && ex->fmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
+  const bool nv = ex->fmt == MOE_W_NVFP4;
+  if (!ex->w13 || !ex->w13_scale || !ex->w2 || !ex->w2_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ex->w13, 16) || !aligned(ex->w2, 16)) return MOE_ERR_INVALID_ARG;
+  if (nv) {
+    if (!ex->tensor_scale || !aligned(ex->w13_scale, 2) || !aligned(ex->w2_scale, 2)) return MOE_ERR_INVALID_ARG;
+  } else if (ex->tensor_scale) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  *out = ExpertsDev{nv ? 1 : 0, ex->w13, ex->w13_scale, ex->w2, ex->w2_scale, ex->tensor_scale};
+  return MOE_OK;
+}
+
+moe_status_t check_shared(const moe_shared_bf16_t* sh, SharedDev* out) {
+  *out = SharedDev{nullptr, nullptr};
+  if (!sh || (!sh->w13 && !sh->w2)) return MOE_OK;
+  if (!sh->w13 || !sh->w2 || !aligned(sh->w13, 16) || !aligned(sh->w2, 16)) return MOE_ERR_INVALID_ARG;
+  *out = SharedDev{static_cast<const uint16_t*>(sh->w13), static_cast<const uint16_t*>(sh->w2)};
+  return MOE_OK;
+}
+
+inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                   \
+  do {                                  \
+    const moe_status_t st_ = (expr);    \
+    if (st_ != MOE_OK) return st_;      \
+  } while (0)
+
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+Shape shape_of(const moe_layer_desc_t* d) { return Shape{d->T, d->H, d->I, d->E, d->top_k}; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* bytes) {
+  MOE_TRY(check_desc(desc));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_get_status(void* ws, moe_status_t* st) {
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  if (!st) return MOE_ERR_INVALID_ARG;
+  int v = 0;
+  int* word = reinterpret_cast<int*>(ws) + C_STATUS;
+  MOE_CUDA(cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost));
+  if (v != 0) MOE_CUDA(cudaMemset(word, 0, sizeof(int)));
+  *st = static_cast<moe_status_t>(v);
+  return MOE_OK;
+}
+
+void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+moe_status_t moe_debug_wait_probe(void* ws, size_t ws_bytes, uint64_t limit_ns, moe_stream_t stream) {
+  if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(int) * N_COUNTERS) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_wait_probe(ws, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quant_act_mxfp4(int32_t rows, int32_t K, const void* x, uint8_t* codes, uint8_t* scales,
+                                 moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quant_mxfp4(static_cast<const uint16_t*>(x), rows, K, codes, scales,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const float* w_router,
+                             const float* bias, int32_t* topk_ids, float* topk_w, float* logits,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_ws(desc, ws, ws_bytes));
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !w_router || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16)) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
+  float* lg = logits ? logits : at<float>(ws, L.logits);
+  MOE_CUDA(launch_router_logits(static_cast<const uint16_t*>(x), w_router, bias, lg, desc->T, desc->H,
+                                desc->E, s));
+  return cuda_status(launch_topk(lg, desc->T, desc->E, desc->top_k, topk_ids, topk_w, s));
+}
+
+moe_status_t moe_permute(const moe_layer_desc_t* desc, const int32_t* topk_ids, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_ws(desc, ws, ws_bytes));
+  if (!counts || !offsets || (desc->T > 0 && (!topk_ids || !perm || !inv_perm))) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
+  return cuda_status(launch_permute(topk_ids, desc->T, desc->top_k, desc->E, counts, offsets, perm, inv_perm,
+                                    at<int>(ws, L.rank), at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base),
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                const moe_shared_bf16_t* shared, const void* x, const uint8_t* xq,
+                                const uint8_t* xs, const int32_t* offsets, const int32_t* perm,
+                                float* y_assign, float* y_shared, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_ws(desc, ws, ws_bytes));
+  ExpertsDev ex;
+  SharedDev shd;
+  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_shared(shared, &shd));
+  if (desc->T == 0) return MOE_OK;
+  if (!xq || !xs || !offsets || !perm || !y_assign) return MOE_ERR_INVALID_ARG;
+  if (!aligned(xq, 16) || !aligned(y_assign, 16)) return MOE_ERR_INVALID_ARG;
+  if (shd.w13 && (!x || !y_shared || !aligned(x, 16) || !aligned(y_shared, 16))) return MOE_ERR_INVALID_ARG;
+  if (!shd.w13 && y_shared) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
+  return cuda_status(launch_expert_ffn(shape_of(desc), ex, shd, static_cast<const uint16_t*>(x), xq, xs,
+                                       offsets, perm, at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs),
+                                       at<uint16_t>(ws, L.h_shared), y_assign, y_shared,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_assign, const int32_t* inv_perm,
+                         const float* topk_w, const float* y_shared, void* out, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  if (desc->T == 0) return MOE_OK;
+  if (!y_assign || !inv_perm || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y_assign, 16) || !aligned(out, 16) || (y_shared && !aligned(y_shared, 16)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(shape_of(desc), y_assign, inv_perm, topk_w, y_shared,
+                                    static_cast<uint16_t*>(out), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                               const moe_shared_bf16_t* shared, const float* w_router, const float* bias,
+                               const void* x, void* out, int32_t* topk_ids, float* topk_w, void* ws,
+                               size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_ws(desc, ws, ws_bytes));
+  ExpertsDev ex;
+  SharedDev shd;
+  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_shared(shared, &shd));
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !out || !w_router || !aligned(x, 16) || !aligned(out, 16) || !aligned(w_router, 16))
+    return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
+  const Shape sh = shape_of(desc);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  int* ids = topk_ids ? topk_ids : at<int>(ws, L.ids);
+  float* w = topk_w ? topk_w : at<float>(ws, L.wts);
+  MOE_CUDA(launch_router_logits(xb, w_router, bias, at<float>(ws, L.logits), sh.T, sh.H, sh.E, s));
+  MOE_CUDA(launch_topk(at<float>(ws, L.logits), sh.T, sh.E, sh.k, ids, w, s));
+  MOE_CUDA(launch_quant_mxfp4(xb, sh.T, sh.H, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), s));
+  MOE_CUDA(launch_permute(ids, sh.T, sh.k, sh.E, at<int>(ws, L.counts), at<int>(ws, L.offsets),
+                          at<int>(ws, L.perm), at<int>(ws, L.inv_perm), at<int>(ws, L.rank),
+                          at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base), s));
+  float* ysh = shd.w13 ? at<float>(ws, L.y_shared) : nullptr;
+  MOE_CUDA(launch_expert_ffn(sh, ex, shd, xb, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs),
+                             at<int>(ws, L.offsets), at<int>(ws, L.perm), at<uint8_t>(ws, L.hq),
+                             at<uint8_t>(ws, L.hs), at<uint16_t>(ws, L.h_shared), at<float>(ws, L.y_assign),
+                             ysh, s));
+  return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh,
+                                    static_cast<uint16_t*>(out), s));
+}
+
+moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                              const moe_shared_bf16_t* shared, const float* w_router, const float* bias,
+                              const void* x, void* out, int32_t* topk_ids, float* topk_w, void* ws,
+                              size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  if (desc->T > MAX_DECODE_T) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_ws(desc, ws, ws_bytes));
+  ExpertsDev ex;
+  SharedDev shd;
+  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_shared(shared, &shd));
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !out || !w_router || !aligned(x, 16) || !aligned(out, 16) || !aligned(w_router, 16))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_fused_decode(shape_of(desc), ex, shd, w_router, bias, static_cast<const uint16_t*>(x),
+                                         static_cast<uint16_t*>(out), topk_ids, topk_w, ws,
+                                         g_wait_limit_ns.load(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

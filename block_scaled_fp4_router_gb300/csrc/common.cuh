@@ -1,0 +1,190 @@
+// Device helpers shared by the kernels of libmoefp4 (sm_103a).
+//
+// Number formats (model card "amd/MiniMax-M3.1-Flash-Quark-MXFP4", section
+// "Model Overview": OCP MXFP4 weights and activations; AMD technical article
+// "MiniMax-M3.1 on AMD Instinct GPUs", section "MiniMax-M3.1 at a glance":
+// NVFP4 experts):
+//   E2M1  1 sign, 2 exponent (bias 1), 1 mantissa bit: +-{0,.5,1,1.5,2,3,4,6}
+//   E8M0  2^(b-127)
+//   E4M3  OCP FP8 e4m3 ("fn")
+// Element pairs are decoded with the sm_100-family conversion instructions
+// (cvt.rn.f16x2.e2m1x2 / .e4m3x2), which are exact for these formats.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "layout.h"
+
+namespace moefp4 {
+
+constexpr uint32_t FULL = 0xffffffffu;
+
+// ------------------------------------------------------------------ BF16
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// ------------------------------------------------------------ scale bytes
+
+// E8M0 byte -> float 2^(b-127).  b = 0 is 2^-127 (an FP32 subnormal); 0xFF
+// (NaN in E8M0) is outside what the library produces or accepts.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+  return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
+// Two E4M3 bytes (low byte first) -> two floats.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)two_bytes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+
+// -------------------------------------------------------------- E2M1 pairs
+
+// One 32-bit word of packed E2M1 codes (8 elements) -> four f16x2 holding the
+// exact element values; f16x2 i holds the two elements of byte i.
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ float h2sum(uint32_t a) {
+  float2 f = __half22float2(*reinterpret_cast<__half2*>(&a));
+  return f.x + f.y;
+}
+
+// ------------------------------------------------------ MXFP4 quantisation
+
+// Exponent of the OCP MX shared scale for a block with maximum magnitude amax:
+// floor(log2(amax)) - 2, clamped to [-127, 127]; amax = 0 (or subnormal, whose
+// floor(log2) is below -126) gives -127.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  const int ef = (int)((__float_as_uint(amax) >> 23) & 0xff);
+  return ef == 0 ? -127 : max(ef - 127 - 2, -127);
+}
+
+// 2^-e for e in [-127, 125], exactly.
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+
+// E2M1 code of s (already divided by the block scale): nearest magnitude, ties
+// to the even mantissa, clamped to 6; a zero result is the +0 code.
+__device__ __forceinline__ uint32_t e2m1_rne(float s) {
+  const float a = fabsf(s);
+  uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+               (a >= 3.5f) + (a > 5.0f);
+  return m | ((s < 0.0f && m) ? 8u : 0u);
+}
+
+// One thread quantises 8 consecutive BF16 values x[8g .. 8g+7]; the 4 threads
+// of a 32-element block (consecutive lanes, g = 4j .. 4j+3) share their maxima
+// with two shuffles.  All 32 lanes of the warp must call it together; lanes
+// with valid == false only join the shuffles.  Writes 4 code bytes and, from
+// the first lane of the block, the E8M0 scale byte.
+__device__ __forceinline__ void quant8_group(const uint16_t* __restrict__ x, size_t g, bool valid,
+                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  float v[8];
+  float amax = 0.0f;
+  if (valid) {
+    const uint4 q = *reinterpret_cast<const uint4*>(x + g * 8);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  if (!valid) return;
+  const int e = mx_scale_exp(amax);
+  const float inv = pow2_neg(e);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) packed |= e2m1_rne(v[i] * inv) << (4 * i);
+  reinterpret_cast<uint32_t*>(codes)[g] = packed;
+  if ((g & 3) == 0) scales[g >> 2] = (uint8_t)(e + 127);
+}
+
+// -------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// ------------------------------------------------------------- memory ops
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait until *p >= target.  Bounded twice over: by limit_ns of wall-clock time
+// and by an iteration cap; on expiry it records MOE_DEV_TIMEOUT in *status
+// (first error wins) and returns false.  Also returns false at once when an
+// earlier wait of the same launch already timed out.
+__device__ __forceinline__ bool wait_at_least(const int* p, int target, int* status,
+                                              uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  unsigned ns = 32;
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    if (ld_acquire(p) >= target) return true;
+    if (ld_acquire(status) == (int)MOE_DEV_TIMEOUT) return false;
+    if (globaltimer_ns() - t0 > limit_ns) break;
+    __nanosleep(ns);
+    if (ns < 256) ns <<= 1;
+  }
+  atomicCAS(status, 0, (int)MOE_DEV_TIMEOUT);
+  return false;
+}
+
+}  // namespace moefp4

@@ -1,0 +1,56 @@
+// Host-side launchers of libmoefp4's kernels (C++ linkage, internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "layout.h"
+
+namespace moefp4 {
+
+struct ExpertsDev {
+  int nv;  // 0 = MXFP4, 1 = NVFP4
+  const uint8_t* w13;
+  const uint8_t* w13s;
+  const uint8_t* w2;
+  const uint8_t* w2s;
+  const float* tscale;  // NVFP4 [E, 3]
+};
+
+struct SharedDev {
+  const uint16_t* w13;  // BF16 [2I, H] or null
+  const uint16_t* w2;   // BF16 [H, I]
+};
+
+struct Shape {
+  int T, H, I, E, k;
+};
+
+// A4
+cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t s);
+// A1
+cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
+                                 int T, int H, int E, cudaStream_t s);
+// A2
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s);
+// A3
+cudaError_t launch_permute(const int* ids, int T, int k, int E, int* counts, int* offsets, int* perm,
+                           int* inv_perm, int* rank, int* chunk_cnt, int* chunk_base, cudaStream_t s);
+// A5 - A8 (unfused)
+cudaError_t launch_expert_ffn(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd,
+                              const uint16_t* x, const uint8_t* xq, const uint8_t* xs,
+                              const int* offsets, const int* perm, uint8_t* hq, uint8_t* hs,
+                              uint16_t* h_shared, float* y_assign, float* y_shared, cudaStream_t s);
+// A9
+cudaError_t launch_combine(const Shape& sh, const float* y_assign, const int* inv_perm, const float* w,
+                           const float* y_shared, uint16_t* out, cudaStream_t s);
+// A10
+cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd,
+                                const float* wr, const float* bias, const uint16_t* x, uint16_t* out,
+                                int* ids_out, float* w_out, void* ws, uint64_t wait_limit_ns,
+                                cudaStream_t s);
+// A bounded wait on a counter nothing ever advances (exercises the timeout path).
+cudaError_t launch_wait_probe(void* ws, uint64_t wait_limit_ns, cudaStream_t s);
+
+}  // namespace moefp4

@@ -1,0 +1,93 @@
+// Workspace layout and limits of libmoefp4, shared by host and device code.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define MOE_HD __host__ __device__
+#else
+#define MOE_HD
+#endif
+
+namespace moefp4 {
+
+constexpr int MAX_TOPK = 8;
+constexpr int MAX_E = 256;
+constexpr int MAX_DECODE_T = 16;   // fused single-launch decode range
+constexpr int PERM_CHUNK = 1024;   // assignments ranked per block in the permutation
+
+// Device status word values (mirror moe_status_t).
+constexpr int MOE_DEV_OK = 0;
+constexpr int MOE_DEV_TIMEOUT = 4;
+
+// Counters of the fused decode launch (ints at the start of the workspace).
+enum Counter : int {
+  C_STATUS = 0,    // device status word
+  C_QUEUE = 1,     // next work unit to hand out
+  C_ROUTER = 2,    // router rows finished
+  C_QUANT = 3,     // token rows quantised
+  C_GU = 4,        // gate/up units finished (shared + routed)
+  C_EXIT = 5,      // blocks finished (the last one resets the counters)
+  C_TEST = 6,      // never written by the library: a wait on it always times out
+  N_COUNTERS = 16
+};
+
+MOE_HD inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Byte offsets of every workspace region for one layer shape.
+struct WsLayout {
+  size_t counters;     // int [N_COUNTERS]
+  size_t logits;       // float [T, E]
+  size_t ids;          // int [T, k]       (when the caller passes no output)
+  size_t wts;          // float [T, k]
+  size_t xq;           // uint8 [T, H/2]
+  size_t xs;           // uint8 [T, H/32]
+  size_t counts;       // int [E]
+  size_t offsets;      // int [E+1]
+  size_t perm;         // int [T*k]
+  size_t inv_perm;     // int [T*k]
+  size_t rank;         // int [T*k]        permutation scratch
+  size_t chunk_cnt;    // int [nchunks, E]
+  size_t chunk_base;   // int [nchunks, E]
+  size_t hq;           // uint8 [T*k, I/2]
+  size_t hs;           // uint8 [T*k, I/32]
+  size_t h_shared;     // bf16 [T, I]
+  size_t y_assign;     // float [T*k, H]   (layer_forward only)
+  size_t y_shared;     // float [T, H]     (layer_forward only)
+  size_t total;
+};
+
+MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
+  WsLayout L{};
+  const size_t n = (size_t)T * k;
+  const size_t nchunks = (n + PERM_CHUNK - 1) / PERM_CHUNK;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + (bytes ? bytes : 1));
+    return at;
+  };
+  L.counters = take(sizeof(int) * N_COUNTERS);
+  L.logits = take(sizeof(float) * (size_t)T * E);
+  L.ids = take(sizeof(int) * n);
+  L.wts = take(sizeof(float) * n);
+  L.xq = take((size_t)T * H / 2);
+  L.xs = take((size_t)T * H / 32);
+  L.counts = take(sizeof(int) * E);
+  L.offsets = take(sizeof(int) * (E + 1));
+  L.perm = take(sizeof(int) * n);
+  L.inv_perm = take(sizeof(int) * n);
+  L.rank = take(sizeof(int) * n);
+  L.chunk_cnt = take(sizeof(int) * nchunks * E);
+  L.chunk_base = take(sizeof(int) * nchunks * E);
+  L.hq = take(n * I / 2);
+  L.hs = take(n * I / 32);
+  L.h_shared = take((size_t)2 * T * I);
+  L.y_assign = take(sizeof(float) * n * H);
+  L.y_shared = take(sizeof(float) * (size_t)T * H);
+  L.total = o;
+  return L;
+}
+
+}  // namespace moefp4

@@ -1,0 +1,76 @@
+"""Device-resident layer: the arrays of one MoE layer as torch CUDA tensors,
+the C structs that point at them, and a workspace, for calling the C ABI.
+
+Marshalling only -- no layer arithmetic happens here.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (MOE_W_MXFP4, MOE_W_NVFP4, desc, experts, moe_layer_decode, moe_layer_forward,
+               moe_workspace_size, shared_bf16)
+
+
+def _to_dev(a, device, dtype=None):
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        return a.to(device).contiguous()
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(device)
+
+
+class DeviceLayer:
+    """One layer's weights on the GPU plus a workspace sized for up to T_max tokens."""
+
+    def __init__(self, arrays: dict, H: int, I: int, E: int, top_k: int, fmt: str, T_max: int,
+                 device="cuda", shared: bool = True):
+        self.H, self.I, self.E, self.k, self.fmt = H, I, E, top_k, fmt
+        self.device = torch.device(device)
+        d = self.device
+        self.w_router = _to_dev(arrays["w_router"], d)
+        self.bias = _to_dev(arrays.get("bias"), d)
+        self.w13 = _to_dev(arrays["w13"], d)
+        self.w13_scale = _to_dev(arrays["w13_scale"], d)
+        self.w2 = _to_dev(arrays["w2"], d)
+        self.w2_scale = _to_dev(arrays["w2_scale"], d)
+        self.tensor_scale = _to_dev(arrays.get("tensor_scale"), d)
+        use_shared = shared and arrays.get("ws13") is not None
+        self.ws13 = _to_dev(arrays["ws13"], d, torch.int16) if use_shared else None
+        self.ws2 = _to_dev(arrays["ws2"], d, torch.int16) if use_shared else None
+        self.ex = experts(MOE_W_MXFP4 if fmt == "mxfp4" else MOE_W_NVFP4, self.w13, self.w13_scale,
+                          self.w2, self.w2_scale, self.tensor_scale)
+        self.sh = shared_bf16(self.ws13, self.ws2)
+        self.T_max = T_max
+        nbytes = moe_workspace_size(desc(T_max, H, I, E, top_k))
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=d)
+
+    def desc(self, T: int):
+        if T > self.T_max:
+            raise ValueError("T=%d exceeds the workspace's T_max=%d" % (T, self.T_max))
+        return desc(T, self.H, self.I, self.E, self.k)
+
+    def outputs(self, T: int):
+        d = self.device
+        return (torch.empty((T, self.H), dtype=torch.int16, device=d),
+                torch.empty((T, self.k), dtype=torch.int32, device=d),
+                torch.empty((T, self.k), dtype=torch.float32, device=d))
+
+    def decode(self, x: torch.Tensor, out=None, ids=None, w=None, stream=None):
+        T = x.shape[0]
+        if out is None:
+            out, ids, w = self.outputs(T)
+        moe_layer_decode(self.desc(T), self.ex, self.sh, self.w_router, self.bias, x, out, ids, w, self.ws,
+                         stream)
+        return out, ids, w
+
+    def forward(self, x: torch.Tensor, out=None, ids=None, w=None, stream=None):
+        T = x.shape[0]
+        if out is None:
+            out, ids, w = self.outputs(T)
+        moe_layer_forward(self.desc(T), self.ex, self.sh, self.w_router, self.bias, x, out, ids, w, self.ws,
+                          stream)
+        return out, ids, w

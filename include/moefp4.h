@@ -1,0 +1,221 @@
+/*
+ * moefp4.h -- C ABI of libmoefp4, a block-scaled FP4 sparse MoE FFN layer for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer (AMD technical article "MiniMax-M3.1 on AMD Instinct GPUs: Day-0
+ * support and optimization", section "MiniMax-M3.1 at a glance"): a
+ * high-precision router over E routed experts with top-k selection, an
+ * always-on shared expert, routed SwiGLU experts whose gate/up and down
+ * projections are block-scaled FP4, and a weighted combine.  Routed-expert
+ * weights are OCP MXFP4 (E2M1 codes + one E8M0 scale per 32) or NVFP4 (E2M1 +
+ * one E4M3 scale per 16 + an FP32 tensor scale); routed-expert activations are
+ * quantised to OCP MXFP4 at run time (model card
+ * "amd/MiniMax-M3.1-Flash-Quark-MXFP4", section "Model Overview").
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_h or documented "host" are host memory; every other
+ *     pointer is device memory owned by the caller.  The library never keeps a
+ *     pointer beyond the call.
+ *   - Work is enqueued on the caller's stream; no entry point synchronises the
+ *     host or allocates device memory, except moe_get_status (which copies one
+ *     word device-to-host and therefore waits for that copy).
+ *   - Scratch memory comes from a caller-provided workspace (ws, ws_bytes) of
+ *     at least moe_workspace_size() bytes, 256-byte aligned, zero-filled once
+ *     before its first use (the library leaves it ready for the next call).
+ *     Calls that share one workspace must not overlap on the device.
+ *   - Device pointers to weights, activations and outputs must be 16-byte
+ *     aligned (MOE_ERR_INVALID_ARG otherwise).
+ *   - Arguments are validated on the host before anything is enqueued; an
+ *     invalid call returns an error and enqueues nothing.
+ *   - Device-side failures (a dependency wait that exceeded its bound) are
+ *     recorded in a status word inside the workspace; read it with
+ *     moe_get_status() after the stream has been synchronised.
+ *
+ * Layouts (row-major, C order, little-endian):
+ *   x         BF16 [T, H]
+ *   codes     E2M1, two per byte, the low nibble holds the even element
+ *   w13       [E, 2I, H/2] codes; rows [0, I) are gate, rows [I, 2I) are up
+ *   w13_scale MXFP4: E8M0 [E, 2I, H/32];  NVFP4: E4M3 [E, 2I, H/16]
+ *   w2        [E, H, I/2] codes
+ *   w2_scale  MXFP4: E8M0 [E, H, I/32];   NVFP4: E4M3 [E, H, I/16]
+ *   tensor_scale  NVFP4 only: FP32 [E, 3] = (gate, up, down) per expert
+ *   shared w13    BF16 [2I, H] (gate rows then up rows); shared w2 BF16 [H, I]
+ *   w_router  FP32 [E, H]; router bias FP32 [E] (optional)
+ *
+ * Arithmetic of every entry point (and of the layer as a whole):
+ *   logits = x . Wr^T + bias                       (FP32 accumulation)
+ *   p = softmax(logits); ids = top-k by logit (ties: lower expert index),
+ *   weights = p[ids] / sum p[ids]
+ *   xq = MXFP4(x): per 32 along H, X = 2^(floor(log2 amax) - 2) clamped to
+ *        [2^-127, 2^127], codes = E2M1 nearest-even of v / X, clamped to 6,
+ *        a zero result is code 0
+ *   routed expert e on xq:  G, U = deq(xq) . deq(Wgate/up[e])^T  (FP32)
+ *        h = SiLU(G) * U; hq = MXFP4(h) per 32 along I;  y = deq(hq) . deq(W2[e])^T
+ *   shared expert on x:     G, U = x . Ws_gate/up^T (FP32); h = BF16(SiLU(G) * U);
+ *        ys = h . Ws2^T
+ *   out = BF16(ys + sum_j weights_j * y_j)
+ */
+#ifndef MOEFP4_H
+#define MOEFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* An opaque CUDA stream (the runtime's cudaStream_t); NULL = legacy stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* bad pointer, shape, alignment or format    */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but outside this entry point's range */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime call failed                 */
+  MOE_ERR_TIMEOUT = 4,      /* a device-side wait exceeded its bound      */
+  MOE_ERR_WORKSPACE = 5     /* workspace missing, too small or misaligned */
+} moe_status_t;
+
+typedef enum { MOE_W_MXFP4 = 1, MOE_W_NVFP4 = 2 } moe_wfmt_t;
+
+/* Shape of one MoE layer call.
+ * T tokens (>= 0), hidden size H, intermediate size I, E routed experts,
+ * top_k experts per token.  Requirements: H and I multiples of 128 (NVFP4:
+ * also of 16), 1 <= top_k <= 8, top_k <= E <= 256.  renormalize must be 1
+ * (weights renormalised over the selected experts) and act_quant must be 1
+ * (routed-expert activations quantised to MXFP4); other values return
+ * MOE_ERR_UNSUPPORTED. */
+typedef struct {
+  int32_t T, H, I, E, top_k;
+  int32_t renormalize;
+  int32_t act_quant;
+} moe_layer_desc_t;
+
+/* Routed-expert weights (device pointers, layouts above). */
+typedef struct {
+  moe_wfmt_t fmt;
+  const uint8_t* w13;
+  const uint8_t* w13_scale;
+  const uint8_t* w2;
+  const uint8_t* w2_scale;
+  const float* tensor_scale;   /* NVFP4: [E, 3]; MXFP4: must be NULL */
+} moe_experts_t;
+
+/* The BF16 shared expert; both NULL = the layer has no shared expert. */
+typedef struct {
+  const void* w13;  /* BF16 [2I, H] */
+  const void* w2;   /* BF16 [H, I]  */
+} moe_shared_bf16_t;
+
+/* Human-readable name of a status code (static storage). */
+MOE_API const char* moe_status_string(moe_status_t st);
+
+/* Bytes of workspace any entry point below needs for this layer shape
+ * (the maximum over all of them).  desc must be valid. */
+MOE_API moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* bytes);
+
+/* Reads (and clears) the device status word of a workspace into *st.  Call
+ * after synchronising the stream the workspace was used on.  This is the one
+ * entry point that waits: it copies 4 bytes device-to-host. */
+MOE_API moe_status_t moe_get_status(void* ws, moe_status_t* st);
+
+/* A1 + A2: router logits, softmax, top-k, renormalisation.
+ * The router is "high precision" and "stacked" (AMD article, sections
+ * "MiniMax-M3.1 at a glance" and "What we Optimized"): FP32 weights, FP32
+ * accumulation.
+ *   x         BF16 [T, H]
+ *   w_router  FP32 [E, H];  bias FP32 [E] or NULL
+ *   topk_ids  int32 [T, top_k] out, descending logit, ties to lower index
+ *   topk_w    FP32 [T, top_k] out, softmax over the selected logits
+ *   logits    FP32 [T, E] out, or NULL
+ * ws: workspace for desc. */
+MOE_API moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const float* w_router,
+                             const float* bias, int32_t* topk_ids, float* topk_w, float* logits,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* A4: dynamic OCP MXFP4 quantisation of BF16 rows (model card, section
+ * "Model Overview": routed-expert activations "OCP MXFP4, Dynamic").
+ *   x      BF16 [rows, K], K a multiple of 32, row pitch K elements
+ *   codes  uint8 [rows, K/2] out;  scales  uint8 E8M0 [rows, K/32] out
+ * Non-finite inputs give unspecified codes. */
+MOE_API moe_status_t moe_quant_act_mxfp4(int32_t rows, int32_t K, const void* x, uint8_t* codes,
+                                 uint8_t* scales, moe_stream_t stream);
+
+/* A3: stable counting sort of the T*top_k (token, slot) assignments by
+ * expert.  Bit-exact and deterministic.
+ *   topk_ids  int32 [T, top_k]  (every id in [0, E))
+ *   counts    int32 [E] out;  offsets int32 [E+1] out (exclusive prefix sum)
+ *   perm      int32 [T*top_k] out: sorted position -> t*top_k + j, ordered by
+ *             expert, then token, then slot
+ *   inv_perm  int32 [T*top_k] out: t*top_k + j -> sorted position
+ * ws: workspace for desc.  Out-of-range ids give unspecified results. */
+MOE_API moe_status_t moe_permute(const moe_layer_desc_t* desc, const int32_t* topk_ids, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws,
+                         size_t ws_bytes, moe_stream_t stream);
+
+/* A5 - A8: routed expert FFNs on the permuted MXFP4 activations plus the BF16
+ * shared expert (AMD article, section "What we Optimized": the MXFP4 fused MoE
+ * with the shared expert).
+ *   x         BF16 [T, H]   (shared expert input; may be NULL if no shared)
+ *   xq, xs    MXFP4 of x in token order: uint8 [T, H/2], E8M0 [T, H/32]
+ *   offsets   int32 [E+1], perm int32 [T*top_k]  (from moe_permute)
+ *   y_assign  FP32 [T*top_k, H] out, row p = expert output of sorted
+ *             assignment p (unweighted)
+ *   y_shared  FP32 [T, H] out (NULL iff the layer has no shared expert)
+ * ws: workspace for desc. */
+MOE_API moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                const moe_shared_bf16_t* shared, const void* x,
+                                const uint8_t* xq, const uint8_t* xs, const int32_t* offsets,
+                                const int32_t* perm, float* y_assign, float* y_shared, void* ws,
+                                size_t ws_bytes, moe_stream_t stream);
+
+/* A9: weighted combine (vLLM PR #64273 commit list: "MoE finalize").
+ *   out[t] = BF16(y_shared[t] + sum_j topk_w[t, j] * y_assign[inv_perm[t*k + j]])
+ *   y_shared may be NULL (treated as 0).  out BF16 [T, H]. */
+MOE_API moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_assign,
+                         const int32_t* inv_perm, const float* topk_w, const float* y_shared,
+                         void* out, moe_stream_t stream);
+
+/* A10: the whole layer in one launch for decode steps of 1 to 16 tokens
+ * (AMD article, section "What we Optimized": one fused launch per MoE layer
+ * for pure decode steps of at most 16 tokens).  T > 16 returns
+ * MOE_ERR_UNSUPPORTED (use moe_layer_forward).
+ *   x          BF16 [T, H];  out BF16 [T, H]
+ *   topk_ids   int32 [T, top_k] out or NULL;  topk_w FP32 [T, top_k] out or NULL
+ * The launch is persistent (one block per SM slot); its dependency waits are
+ * bounded and report MOE_ERR_TIMEOUT through moe_get_status. */
+MOE_API moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                              const moe_shared_bf16_t* shared, const float* w_router,
+                              const float* bias, const void* x, void* out, int32_t* topk_ids,
+                              float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole layer for any T, as the unfused sequence router -> quantise ->
+ * permute -> expert FFNs -> combine (the pages' standard, non-fused path). */
+MOE_API moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                               const moe_shared_bf16_t* shared, const float* w_router,
+                               const float* bias, const void* x, void* out, int32_t* topk_ids,
+                               float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Upper bound, in nanoseconds, of every device-side dependency wait of later
+ * launches in this process (default 500 ms).  A wait that runs out records
+ * MOE_ERR_TIMEOUT in the workspace status word and the launch returns without
+ * finishing its work; the workspace must then be zero-filled again. */
+MOE_API void moe_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook for the failure path: launches one bounded wait on a workspace
+ * counter that nothing ever advances, with the given limit.  Afterwards
+ * moe_get_status reports MOE_ERR_TIMEOUT; the GPU context stays usable. */
+MOE_API moe_status_t moe_debug_wait_probe(void* ws, size_t ws_bytes, uint64_t limit_ns, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEFP4_H */

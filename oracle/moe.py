@@ -177,12 +177,14 @@ def shared_expert(x: np.ndarray, ws13_bits: np.ndarray, ws2_bits: np.ndarray):
 
 
 def layer_forward(layer: dict, top_k: int, fmt: str, tokens=None, forced_ids=None,
-                  keep=False) -> dict:
+                  keep=False, cache=None) -> dict:
     """The whole layer for the token rows ``tokens`` (default: all rows of x).
 
     ``layer`` holds the arrays described in the workload module (x as BF16
     bits, weights as codes / scale bytes).  ``forced_ids`` [len(tokens), k]
-    overrides the top-k selection.  Returns float64 arrays holding exact
+    overrides the top-k selection.  ``cache`` (a dict owned by the caller, one
+    per layer) memoises the dequantised expert matrices across calls.  Returns
+    float64 arrays holding exact
     float32 / BF16 values: logits, ids, weights, ys (or None), y [n, k, H],
     out [n, H] (BF16 values) and out_bits (uint16); with ``keep`` also the
     per-assignment intermediates.
@@ -205,7 +207,12 @@ def layer_forward(layer: dict, top_k: int, fmt: str, tokens=None, forced_ids=Non
     inter = {}
     for e in np.unique(ids):
         rows, slots = np.nonzero(ids == e)
-        wg, wu, wd = expert_matrices(layer, int(e), fmt)
+        if cache is not None:
+            if int(e) not in cache:
+                cache[int(e)] = expert_matrices(layer, int(e), fmt)
+            wg, wu, wd = cache[int(e)]
+        else:
+            wg, wu, wd = expert_matrices(layer, int(e), fmt)
         r = routed_expert(xq_deq[rows], wg, wu, wd)
         y[rows, slots] = r["y"]
         if keep:

@@ -1,0 +1,381 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle.
+
+Bars (the layer's stated tolerances):
+* bit-exact: MXFP4 activation codes and scales, routing ids (on logits with
+  an unambiguous top-k), the permutation;
+* max normwise relative error <= 1e-3 for single contractions (router
+  logits, routed expert outputs, shared expert outputs);
+* <= 2e-2 for the whole layer output.
+A token whose k-th and (k+1)-th oracle logits lie within 1e-5 (relative) is
+"ambiguous": either choice is correct, so its ids are only checked to be a
+valid top-k and its output is left out of the element-wise comparison.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp4_router_gb300 as M
+from block_scaled_fp4_router_gb300 import workloads as W
+from block_scaled_fp4_router_gb300.device import DeviceLayer
+from oracle import formats as F
+from oracle import moe as O
+
+pytestmark = pytest.mark.gpu
+
+LAYER_TOL = 2e-2
+CONTRACTION_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from block_scaled_fp4_router_gb300 import build as B
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    B.build()
+    M.load()
+
+
+def normwise(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def bf16_tensor(bits_np):
+    return torch.from_numpy(np.ascontiguousarray(bits_np)).view(torch.int16).cuda()
+
+
+def bits_to_float(t):
+    return F.bf16_bits_to_float(t.cpu().numpy().view(np.uint16))
+
+
+def ambiguous(logits, k, rel=1e-5):
+    s = -np.sort(-np.asarray(logits, np.float64), axis=1)
+    gap = s[:, k - 1] - s[:, k] if s.shape[1] > k else np.full(s.shape[0], np.inf)
+    return gap <= rel * np.maximum(1.0, np.abs(s[:, 0]))
+
+
+# ----------------------------------------------------------------- A4 quant
+
+
+def _quant_gpu(x_bits):
+    rows, K = x_bits.shape
+    x = bf16_tensor(x_bits)
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((rows, K // 32), dtype=torch.uint8, device="cuda")
+    M.moe_quant_act_mxfp4(rows, K, x, codes, scales)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy()
+
+
+def test_quant_bitexact_random_rows():
+    rng = np.random.default_rng(10)
+    x = rng.normal(0, 1, (37, 4096)) * np.exp2(rng.integers(-30, 30, (37, 1)))
+    x[3, :64] = 0.0                        # all-zero blocks
+    x[5, 32:64] = 1e-40                    # subnormal block
+    xb = F.bf16_value_to_bits(F.round_to_bf16(x))
+    codes, scales = _quant_gpu(xb)
+    rc, rs = F.quantize_mxfp4(F.bf16_bits_to_float(xb))
+    assert np.array_equal(scales, rs)
+    assert np.array_equal(codes, F.pack_e2m1(rc))
+
+
+def test_quant_bitexact_at_every_rounding_midpoint():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    mids = [(a + b) / 2 for a, b in zip(mags[:-1], mags[1:])]
+    rows = []
+    for scale_exp in (-20, -3, 0, 7):
+        for sign in (1, -1):
+            blk = np.zeros(32)
+            blk[0] = 4.0  # amax 4 -> X = 1 relative to the block's own scale
+            blk[1:1 + len(mids)] = sign * np.array(mids)
+            blk[10:17] = sign * np.array(mags[1:])
+            blk[20] = 7.0 * sign / 8 * 4  # 3.5
+            blk[21] = 5.999
+            rows.append(blk * 2.0 ** scale_exp)
+    x = np.stack(rows).reshape(-1, 128)  # 4 blocks per row
+    xb = F.bf16_value_to_bits(F.round_to_bf16(x))
+    codes, scales = _quant_gpu(xb)
+    rc, rs = F.quantize_mxfp4(F.bf16_bits_to_float(xb))
+    assert np.array_equal(scales, rs) and np.array_equal(codes, F.pack_e2m1(rc))
+
+
+def test_quant_ragged_rows_and_small_K():
+    rng = np.random.default_rng(11)
+    for rows, K in [(1, 32), (3, 96), (5, 160)]:
+        xb = F.bf16_value_to_bits(F.round_to_bf16(rng.normal(0, 3, (rows, K))))
+        codes, scales = _quant_gpu(xb)
+        rc, rs = F.quantize_mxfp4(F.bf16_bits_to_float(xb))
+        assert np.array_equal(scales, rs) and np.array_equal(codes, F.pack_e2m1(rc))
+
+
+# ------------------------------------------------------------ A1 + A2 router
+
+
+def _router_gpu(x_bits, wr, bias, k, H, E):
+    T = x_bits.shape[0]
+    d = M.desc(T, H, 128, E, k)
+    ws = torch.zeros(M.moe_workspace_size(d), dtype=torch.uint8, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    lg = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    b = None if bias is None else torch.from_numpy(bias).cuda()
+    M.moe_router_topk(d, bf16_tensor(x_bits), torch.from_numpy(wr).cuda(), b, ids, w, lg, ws)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy(), lg.cpu().numpy()
+
+
+@pytest.mark.parametrize("T", [5, 100])  # decode GEMV path and batched GEMM path
+def test_topk_bitexact_on_exactly_computed_logits(T):
+    """x rows are one-hot (1.0 at h_t), so logits[t, e] = Wr[e, h_t] exactly on
+    any summation order; the logits include exact ties."""
+    rng = np.random.default_rng(12)
+    H, E, k = 128, 64, 4
+    h_t = rng.integers(0, H, T)
+    x = np.zeros((T, H))
+    x[np.arange(T), h_t] = 1.0
+    wr = rng.normal(0, 1, (E, H)).astype(np.float32)
+    wr[:8, :] = wr[8:16, :]          # duplicated rows -> tied logits
+    wr[20:24, 5] = wr[3, 5]
+    xb = F.bf16_value_to_bits(x)
+    ids, w, lg = _router_gpu(xb, wr, None, k, H, E)
+    ref_logits = O.router_logits(F.bf16_bits_to_float(xb), wr)
+    assert np.array_equal(lg, ref_logits.astype(np.float32))
+    rid, rw = O.route(ref_logits, k)
+    assert np.array_equal(ids, rid)
+    assert np.allclose(w, rw, rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("wl_name,T", [("tiny", 16), ("decode1", 1), ("decode16z", 16), ("prefill8k", 300)])
+def test_router_topk_random(wl_name, T):
+    wl = W.WORKLOADS[wl_name]
+    lay = W.generate(wl, tokens=T)
+    ids, w, lg = _router_gpu(lay["x"], lay["w_router"], lay["bias"], wl.top_k, wl.H, wl.E)
+    ref = O.router_logits(F.bf16_bits_to_float(lay["x"]), lay["w_router"], lay["bias"])
+    assert normwise(lg, ref) <= 1e-5
+    rid, rw = O.route(ref, wl.top_k)
+    amb = ambiguous(ref, wl.top_k)
+    assert np.array_equal(ids[~amb], rid[~amb])
+    assert np.allclose(w[~amb], rw[~amb], rtol=1e-5, atol=1e-7)
+    assert amb.sum() <= max(1, T // 100)
+
+
+# ------------------------------------------------------------- A3 permute
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 4, 128), (16, 4, 16), (700, 4, 128), (8192, 4, 128), (33, 8, 256),
+                                   (5, 1, 4)])
+def test_permute_bitexact(T, k, E):
+    rng = np.random.default_rng(T * 7 + E)
+    # Zipf-skewed ids with repeats allowed: exercises several blocks and ragged tails
+    p = 1.0 / np.arange(1, E + 1) ** 1.1
+    ids_np = rng.choice(E, size=(T, k), p=p / p.sum()).astype(np.int32)
+    d = M.desc(T, 128, 128, E, k)
+    ws = torch.zeros(M.moe_workspace_size(d), dtype=torch.uint8, device="cuda")
+    n = T * k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(n, dtype=torch.int32, device="cuda")
+    inv = torch.empty(n, dtype=torch.int32, device="cuda")
+    M.moe_permute(d, torch.from_numpy(ids_np).cuda(), counts, offsets, perm, inv, ws)
+    torch.cuda.synchronize()
+    rc, ro, rp, ri = O.permute(ids_np, E)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(perm.cpu().numpy(), rp)
+    assert np.array_equal(inv.cpu().numpy(), ri)
+
+
+# ------------------------------------------------------------ layer fixtures
+
+_CACHE = {}
+
+
+def _workload(name, T=None):
+    """(workload, host arrays, device layer, oracle expert cache), cached."""
+    key = (name, T)
+    if key not in _CACHE:
+        wl = W.WORKLOADS[name]
+        if T is not None:
+            wl = wl.with_tokens(T)
+        lay = W.generate(wl)
+        dev = DeviceLayer(lay, wl.H, wl.I, wl.E, wl.top_k, wl.fmt, T_max=wl.T)
+        _CACHE.clear()  # keep at most one large layer resident
+        _CACHE[key] = (wl, lay, dev, {})
+    return _CACHE[key]
+
+
+def _compare_layer(wl, lay, cache, out, ids, tokens=None, tol=LAYER_TOL):
+    r = O.layer_forward(lay, wl.top_k, wl.fmt, tokens=tokens, cache=cache)
+    amb = ambiguous(r["logits"], wl.top_k)
+    tok = r["tokens"]
+    g_ids = ids.cpu().numpy()[tok]
+    assert np.array_equal(g_ids[~amb], r["ids"][~amb])
+    g_out = bits_to_float(out)[tok]
+    assert np.all(np.isfinite(g_out))
+    err = normwise(g_out[~amb], r["out"][~amb])
+    assert err <= tol, err
+    return err
+
+
+# ------------------------------------------------------ A5 - A8 expert FFNs
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16"])
+def test_expert_ffn_contractions(name):
+    """Routed expert outputs y (per sorted assignment) and the shared expert
+    output ys against the oracle, on the same MXFP4 activations (the GPU's own
+    quantiser output, bit-identical to the oracle's by the tests above)."""
+    wl, lay, dev, cache = _workload(name)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    x = F.bf16_bits_to_float(lay["x"])
+    ref = O.layer_forward(lay, k, wl.fmt, cache=cache, keep=True)
+    ids_np = ref["ids"]
+    counts, offsets, perm, inv = O.permute(ids_np, E)
+    d = dev.desc(T)
+    xt = bf16_tensor(lay["x"])
+    xq = torch.empty((T, H // 2), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((T, H // 32), dtype=torch.uint8, device="cuda")
+    M.moe_quant_act_mxfp4(T, H, xt, xq, xs)
+    g_off = torch.from_numpy(offsets).cuda()
+    g_perm = torch.from_numpy(perm).cuda()
+    y_assign = torch.empty((T * k, H), dtype=torch.float32, device="cuda")
+    y_shared = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    M.moe_expert_ffn_fp4(d, dev.ex, dev.sh, xt, xq, xs, g_off, g_perm, y_assign, y_shared, dev.ws)
+    torch.cuda.synchronize()
+    y_ref = ref["y"].reshape(T * k, H)[perm]  # oracle y in sorted-assignment order
+    assert normwise(y_assign.cpu().numpy(), y_ref) <= CONTRACTION_TOL
+    assert normwise(y_shared.cpu().numpy(), ref["ys"]) <= CONTRACTION_TOL
+    # combine alone on the oracle's expert outputs: out = BF16(ys + sum w y)
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    M.moe_combine(d, torch.from_numpy(y_ref.astype(np.float32)).cuda(), torch.from_numpy(inv).cuda(),
+                  torch.from_numpy(ref["weights"].astype(np.float32)).cuda(),
+                  torch.from_numpy(ref["ys"].astype(np.float32)).cuda(), out)
+    torch.cuda.synchronize()
+    g = bits_to_float(out)
+    ulp = np.abs(ref["out"]) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(g - ref["out"]) <= ulp)
+
+
+# ----------------------------------------------------------- whole layer
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode16z"])
+def test_layer_decode_fused(name):
+    wl, lay, dev, cache = _workload(name)
+    out, ids, w = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, cache, out, ids)
+    # the fused launch is deterministic and leaves the workspace reusable
+    out2, ids2, _ = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(ids, ids2)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16"])
+def test_layer_forward_matches_decode(name):
+    wl, lay, dev, cache = _workload(name)
+    out_f, ids_f, w_f = dev.forward(bf16_tensor(lay["x"]))
+    out_d, ids_d, w_d = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    _compare_layer(wl, lay, cache, out_f, ids_f)
+    assert torch.equal(ids_f, ids_d)
+    assert normwise(bits_to_float(out_f), bits_to_float(out_d)) <= 1e-2
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 13, 16])
+def test_decode_token_counts(T):
+    wl, lay, dev, cache = _workload("tiny")
+    sub = dict(lay)
+    sub["x"] = lay["x"][:T]
+    out, ids, _ = dev.decode(bf16_tensor(sub["x"]))
+    torch.cuda.synchronize()
+    _compare_layer(wl.with_tokens(T), sub, cache, out, ids)
+    # 17 tokens is past the fused decode range: rejected before any launch
+    d17 = M.desc(17, wl.H, wl.I, wl.E, wl.top_k)
+    ws17 = torch.zeros(M.moe_workspace_size(d17), dtype=torch.uint8, device="cuda")
+    x17 = bf16_tensor(np.zeros((17, wl.H), np.uint16))
+    o17 = torch.empty((17, wl.H), dtype=torch.int16, device="cuda")
+    with pytest.raises(M.MoeError) as e:
+        M.moe_layer_decode(d17, dev.ex, dev.sh, dev.w_router, dev.bias, x17, o17, None, None, ws17)
+    assert e.value.status == M.MOE_ERR_UNSUPPORTED
+
+
+def test_batch128_forward_sampled():
+    wl, lay, dev, cache = _workload("batch128")
+    out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(13)
+    tokens = np.sort(np.concatenate([rng.choice(wl.T - 1, 23, replace=False), [wl.T - 1]]))
+    _compare_layer(wl, lay, cache, out, ids, tokens=tokens)
+
+
+def test_prefill8k_forward_sampled():
+    wl, lay, dev, cache = _workload("prefill8k")
+    out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    g = bits_to_float(out)
+    assert np.all(np.isfinite(g))
+    # Zipf(1.1) load: the realised per-expert histogram is skewed
+    counts = np.bincount(ids.cpu().numpy().ravel(), minlength=wl.E)
+    assert counts.sum() == wl.T * wl.top_k and counts.max() > 4 * counts.mean()
+    rng = np.random.default_rng(14)
+    tokens = np.sort(np.concatenate([rng.choice(wl.T - 1, 15, replace=False), [0, wl.T - 1]]))
+    _compare_layer(wl, lay, cache, out, ids, tokens=tokens)
+
+
+# --------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("shape", [(4, 128, 128, 4, 4), (9, 256, 128, 8, 2), (3, 128, 256, 256, 8)])
+def test_small_and_degenerate_shapes(shape):
+    """Dense mixture (E == k), minimal H and I, E = 256 with k = 8."""
+    T, H, I, E, k = shape
+    wl = W.Workload("edge", T, H, I, E, k, W.MXFP4, 21, 0.5)
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, H, I, E, k, wl.fmt, T_max=T)
+    cache = {}
+    out, ids, _ = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    _compare_layer(wl, lay, cache, out, ids)
+    out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    _compare_layer(wl, lay, cache, out, ids)
+
+
+def test_layer_without_shared_expert():
+    wl = W.Workload("noshared", 6, 512, 256, 16, 4, W.NVFP4, 22, 0.05, shared=False)
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, wl.H, wl.I, wl.E, wl.top_k, wl.fmt, T_max=wl.T)
+    cache = {}
+    for fn in (dev.decode, dev.forward):
+        out, ids, _ = fn(bf16_tensor(lay["x"]))
+        torch.cuda.synchronize()
+        _compare_layer(wl, lay, cache, out, ids)
+
+
+def test_zero_tokens_is_a_no_op():
+    wl, lay, dev, cache = _workload("tiny")
+    x = torch.empty((0, wl.H), dtype=torch.int16, device="cuda")
+    out, ids, w = dev.decode(x)
+    out, ids, w = dev.forward(x)
+    torch.cuda.synchronize()
+    assert out.shape == (0, wl.H)
+
+
+# ------------------------------------------------------------ failure path
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait on a counter nothing advances runs out after ~2 ms, records
+    MOE_ERR_TIMEOUT in the workspace status word, and the GPU stays usable."""
+    wl, lay, dev, cache = _workload("tiny")
+    ws = torch.zeros(M.moe_workspace_size(dev.desc(wl.T)), dtype=torch.uint8, device="cuda")
+    M.moe_debug_wait_probe(ws, 2_000_000)
+    torch.cuda.synchronize()
+    assert M.moe_get_status(ws) == M.MOE_ERR_TIMEOUT
+    assert M.moe_get_status(ws) == M.MOE_OK  # reading clears it
+    out, ids, _ = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    _compare_layer(wl, lay, cache, out, ids)
