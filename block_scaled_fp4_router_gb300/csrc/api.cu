@@ -5,7 +5,7 @@
 
 #include <atomic>
 
-#include "../../include/moefp4.h"
+#include "moefp4.h"
 #include "kernels.h"
 #include "layout.h"
 

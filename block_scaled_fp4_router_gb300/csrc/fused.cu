@@ -156,18 +156,19 @@ __device__ void build_routing(const FusedArgs& a, Routing& R) {
   __syncthreads();
 }
 
-// Router row e for all tokens: the block's 512 threads stride over H eight
-// elements at a time, then a fixed-order reduction.
+// Router row e for all tokens: the block's threads stride over H eight
+// elements at a time, then a fixed-order reduction over lanes and warps.
+template <int MAXT>
 __device__ void unit_router(const FusedArgs& a, int e, float* red_s) {
   const int T = a.sh.T, H = a.sh.H;
-  float acc[MAX_DECODE_T];
+  float acc[MAXT];
 #pragma unroll
-  for (int t = 0; t < MAX_DECODE_T; ++t) acc[t] = 0.0f;
+  for (int t = 0; t < MAXT; ++t) acc[t] = 0.0f;
   const float* wrow = a.wr + (size_t)e * H;
   for (int k = threadIdx.x * 8; k < H; k += FT * 8) {
     const uint4 wa = ldg_stream(wrow + k), wb = ldg_stream(wrow + k + 4);
 #pragma unroll
-    for (int t = 0; t < MAX_DECODE_T; ++t) {
+    for (int t = 0; t < MAXT; ++t) {
       if (t < T) {
         const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H + k));
         float s = acc[t];
@@ -185,14 +186,14 @@ __device__ void unit_router(const FusedArgs& a, int e, float* red_s) {
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int t = 0; t < MAX_DECODE_T; ++t) {
+  for (int t = 0; t < MAXT; ++t) {
     const float v = warp_sum(acc[t]);
-    if (lane == 0) red_s[warp * MAX_DECODE_T + t] = v;
+    if (lane == 0) red_s[warp * MAXT + t] = v;
   }
   __syncthreads();
   if (threadIdx.x < T) {
     float s = 0.0f;
-    for (int w = 0; w < FW; ++w) s += red_s[w * MAX_DECODE_T + threadIdx.x];
+    for (int w = 0; w < FW; ++w) s += red_s[w * MAXT + threadIdx.x];
     if (a.bias) s += a.bias[e];
     a.logits[(size_t)threadIdx.x * a.sh.E + e] = s;
   }
@@ -208,32 +209,32 @@ __device__ void unit_quant(const FusedArgs& a) {
   }
 }
 
-// Shared-expert gate rows 8u..8u+7 and up rows I+8u.. (one per warp).
+// Shared-expert gate rows 8u..8u+7 and up rows I+8u.. (one per warp), then
+// h = BF16(SiLU(G) U) for the 8 columns.
+template <int MAXT>
 __device__ void unit_shared_gate_up(const FusedArgs& a, int u, const uint16_t* x_s, float* gu_s) {
   const int T = a.sh.T, H = a.sh.H, I = a.sh.I;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = warp < 8 ? 8 * u + warp : I + 8 * u + (warp - 8);
-  float acc[MAX_DECODE_T];
+  stream_bf16_rows<MAXT, 1, 4>(
+      1, H, [&](int) { return a.shd.w13 + (size_t)row * H; }, x_s, H, T,
+      [&](int, const float(&acc)[MAXT]) {
 #pragma unroll
-  for (int t = 0; t < MAX_DECODE_T; ++t) acc[t] = 0.0f;
-  bf16_row_dot<MAX_DECODE_T>(a.shd.w13 + (size_t)row * H, H, x_s, H, T, acc);
-#pragma unroll
-  for (int t = 0; t < MAX_DECODE_T; ++t) {
-    const float v = warp_sum(acc[t]);
-    if (lane == 0) gu_s[warp * MAX_DECODE_T + t] = v;
-  }
+        for (int t = 0; t < MAXT; ++t)
+          if (lane == 0) gu_s[warp * MAXT + t] = acc[t];
+      });
   __syncthreads();
   if (threadIdx.x < T * 8) {
     const int t = threadIdx.x >> 3, j = threadIdx.x & 7;
-    const float h = silu(gu_s[j * MAX_DECODE_T + t]) * gu_s[(8 + j) * MAX_DECODE_T + t];
+    const float h = silu(gu_s[j * MAXT + t]) * gu_s[(8 + j) * MAXT + t];
     a.h_shared[(size_t)t * I + 8 * u + j] = f32_to_bf16_rn(h);
   }
 }
 
-// Routed gate/up of distinct-expert slot s, columns 32b..32b+31, for every
-// assignment routed to it, then SwiGLU + MXFP4 requantisation into hq/hs
-// (rows in sorted-assignment order).
-template <bool NV>
+// Routed gate/up of distinct-expert slot s, columns 32b..32b+31 (warp w takes
+// rows w, w+16 of the gate block and the same of the up block), then SwiGLU +
+// MXFP4 requantisation into hq/hs (rows in sorted-assignment order).
+template <int MAXT, bool NV>
 __device__ void unit_routed_gate_up(const FusedArgs& a, const Routing& R, int s, int b,
                                     const uint8_t* xq_s, const float* xsc_s, float* gu_s) {
   const int H = a.sh.H, I = a.sh.I;
@@ -243,78 +244,124 @@ __device__ void unit_routed_gate_up(const FusedArgs& a, const Routing& R, int s,
   const uint8_t* w13 = a.ex.w13 + (size_t)e * 2 * I * rb;
   const uint8_t* s13 = a.ex.w13s + (size_t)e * 2 * I * sb;
   const float tg = NV ? a.ex.tscale[e * 3 + 0] : 1.0f, tu = NV ? a.ex.tscale[e * 3 + 1] : 1.0f;
-  for (int r = warp; r < 64; r += FW) {
-    const int row = r < 32 ? 32 * b + r : I + 32 * b + (r - 32);
-    float acc[MAX_DECODE_T];
+  auto local_row = [&](int i) { return warp + FW * i; };  // 0..63: gate 0..31, up 32..63
+  auto global_row = [&](int r) { return r < 32 ? 32 * b + r : I + 32 * b + (r - 32); };
+  stream_fp4_rows<MAXT, NV, 2, 2>(
+      64 / FW, H,
+      [&](int i) {
+        const int g = global_row(local_row(i));
+        return Fp4Src{w13 + g * rb, s13 + g * sb};
+      },
+      [&](int) { return Fp4Tok{&R.tok[beg], 0, nt}; }, xq_s, H / 2, xsc_s, H / 32,
+      [&](int i, const Fp4Tok&, const float(&acc)[MAXT]) {
+        const int r = local_row(i);
+        const float ts = r < 32 ? tg : tu;
+        if (lane == 0) {
 #pragma unroll
-    for (int t = 0; t < MAX_DECODE_T; ++t) acc[t] = 0.0f;
-    fp4_row_dot<MAX_DECODE_T, NV>(w13 + row * rb, s13 + row * sb, H, xq_s, H / 2, xsc_s, H / 32,
-                                  &R.tok[beg], nt, acc);
-    const float ts = r < 32 ? tg : tu;
-#pragma unroll
-    for (int t = 0; t < MAX_DECODE_T; ++t) {
-      const float v = warp_sum(acc[t]);
-      if (lane == 0) gu_s[r * MAX_DECODE_T + t] = v * ts;
-    }
-  }
+          for (int t = 0; t < MAXT; ++t) gu_s[r * MAXT + t] = acc[t] * ts;
+        }
+      });
   __syncthreads();
   for (int t = warp; t < nt; t += FW) {
     const size_t p = (size_t)beg + t;
-    swiglu_quant_block(gu_s[lane * MAX_DECODE_T + t], gu_s[(32 + lane) * MAX_DECODE_T + t],
-                       a.hq + p * (I / 2) + b * 16, a.hs + p * (I / 32) + b);
+    swiglu_quant_block(gu_s[lane * MAXT + t], gu_s[(32 + lane) * MAXT + t], a.hq + p * (I / 2) + b * 16,
+                       a.hs + p * (I / 32) + b);
   }
 }
 
-// Rows 32g..32g+31 of H: the shared-expert down rows and every touched
-// expert's down rows, then out = BF16(ys + sum_j w_j y_j) in a fixed order.
-template <bool NV>
+// Rows 32g..32g+31 of H (warp w takes rows w and w+16): the shared-expert
+// down rows and every touched expert's down rows, then
+// out = BF16(ys + sum_j w_j y_j) in a fixed order.
+template <int MAXT, bool NV>
 __device__ void unit_down(const FusedArgs& a, const Routing& R, int g, const uint8_t* hq_s,
                           const float* hsc_s, const uint16_t* hsh_s, float* y_s) {
   const int T = a.sh.T, H = a.sh.H, I = a.sh.I, k = a.sh.k, n = T * k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nsh = a.shd.w13 ? 1 : 0;
-  const int items = (nsh + R.n_slots) * 32;
   const size_t rb = (size_t)I / 2, sb = NV ? I / 16 : I / 32;
-  for (int it = warp; it < items; it += FW) {
-    const int c = it >> 5, r = it & 31, row = 32 * g + r;
-    float acc[MAX_DECODE_T];
+  if (a.shd.w13) {
+    stream_bf16_rows<MAXT, 1, 3>(
+        32 / FW, I, [&](int i) { return a.shd.w2 + (size_t)(32 * g + warp + FW * i) * I; }, hsh_s, I, T,
+        [&](int i, const float(&acc)[MAXT]) {
+          if (lane == 0) {
 #pragma unroll
-    for (int t = 0; t < MAX_DECODE_T; ++t) acc[t] = 0.0f;
-    if (c < nsh) {
-      bf16_row_dot<MAX_DECODE_T>(a.shd.w2 + (size_t)row * I, I, hsh_s, I, T, acc);
-#pragma unroll
-      for (int t = 0; t < MAX_DECODE_T; ++t) {
-        const float v = warp_sum(acc[t]);
-        if (lane == 0 && t < T) y_s[(n + t) * 32 + r] = v;
-      }
-    } else {
-      const int s = c - nsh, e = R.slot_e[s], beg = R.slot_beg[s], nt = R.slot_beg[s + 1] - beg;
-      const uint8_t* w2 = a.ex.w2 + (size_t)e * H * rb;
-      const uint8_t* s2 = a.ex.w2s + (size_t)e * H * sb;
-      fp4_row_dot<MAX_DECODE_T, NV>(w2 + row * rb, s2 + row * sb, I, hq_s + (size_t)beg * (I / 2), I / 2,
-                                    hsc_s + beg * (I / 32), I / 32, nullptr, nt, acc);
-      const float td = NV ? a.ex.tscale[e * 3 + 2] : 1.0f;
-#pragma unroll
-      for (int t = 0; t < MAX_DECODE_T; ++t) {
-        const float v = warp_sum(acc[t]);
-        if (lane == 0 && t < nt) y_s[(beg + t) * 32 + r] = v * td;
-      }
-    }
+            for (int t = 0; t < MAXT; ++t)
+              if (t < T) y_s[(n + t) * 32 + warp + FW * i] = acc[t];
+          }
+        });
   }
+  constexpr int RPW = 32 / FW;  // rows per warp
+  stream_fp4_rows<MAXT, NV, 4, 1>(
+      RPW * R.n_slots, I,
+      [&](int i) {
+        const int s = i / RPW, row = 32 * g + warp + FW * (i % RPW);
+        const int e = R.slot_e[s];
+        return Fp4Src{a.ex.w2 + (size_t)e * H * rb + row * rb, a.ex.w2s + (size_t)e * H * sb + row * sb};
+      },
+      [&](int i) {
+        const int s = i / RPW;
+        return Fp4Tok{nullptr, R.slot_beg[s], R.slot_beg[s + 1] - R.slot_beg[s]};
+      },
+      hq_s, I / 2, hsc_s, I / 32,
+      [&](int i, const Fp4Tok& rr, const float(&acc)[MAXT]) {
+        const int s = i / RPW, r = warp + FW * (i % RPW);
+        const float td = NV ? a.ex.tscale[R.slot_e[s] * 3 + 2] : 1.0f;
+        if (lane == 0) {
+#pragma unroll
+          for (int t = 0; t < MAXT; ++t)
+            if (t < rr.nt) y_s[(rr.tbase + t) * 32 + r] = acc[t] * td;
+        }
+      });
   __syncthreads();
   if (threadIdx.x < T * 32) {
     const int t = threadIdx.x >> 5, r = threadIdx.x & 31;
-    float acc = nsh ? y_s[(n + t) * 32 + r] : 0.0f;
+    float acc = a.shd.w13 ? y_s[(n + t) * 32 + r] : 0.0f;
     for (int j = 0; j < k; ++j) acc = fmaf(R.w[t * k + j], y_s[R.inv[t * k + j] * 32 + r], acc);
     a.out[(size_t)t * H + 32 * g + r] = f32_to_bf16_rn(acc);
   }
 }
 
-template <bool NV>
+// Thread 0: bulk-prefetch into L2 the weight bytes unit u will stream, so
+// that its loads hit L2 while this block still computes the current unit.
+// Routed units are prefetched only once this block knows the routing.
+__device__ void prefetch_unit(const FusedArgs& a, const Routing& R, bool routed_known, int u) {
+  const int H = a.sh.H, I = a.sh.I, nb = I / 32;
+  const bool nv = a.ex.nv != 0;
+  if (u < a.u_quant) {
+    prefetch_l2_bulk(a.wr + (size_t)u * H, 4u * H);
+  } else if (u < a.u_sgu) {
+  } else if (u < a.u_rgu) {
+    const int c = u - a.u_sgu;
+    prefetch_l2_bulk(a.shd.w13 + (size_t)8 * c * H, 16u * H);
+    prefetch_l2_bulk(a.shd.w13 + (size_t)(I + 8 * c) * H, 16u * H);
+  } else if (!routed_known) {
+  } else if (u < a.u_down) {
+    const int s = (u - a.u_rgu) / nb, b = (u - a.u_rgu) % nb;
+    if (s >= R.n_slots) return;
+    const int e = R.slot_e[s];
+    const size_t rb = (size_t)H / 2, sb = nv ? H / 16 : H / 32;
+    const uint8_t* w13 = a.ex.w13 + (size_t)e * 2 * I * rb;
+    const uint8_t* s13 = a.ex.w13s + (size_t)e * 2 * I * sb;
+    prefetch_l2_bulk(w13 + (size_t)32 * b * rb, (uint32_t)(32 * rb));
+    prefetch_l2_bulk(w13 + (size_t)(I + 32 * b) * rb, (uint32_t)(32 * rb));
+    prefetch_l2_bulk(s13 + (size_t)32 * b * sb, (uint32_t)(32 * sb));
+    prefetch_l2_bulk(s13 + (size_t)(I + 32 * b) * sb, (uint32_t)(32 * sb));
+  } else if (u < a.u_end) {
+    const int g = u - a.u_down;
+    const size_t rb = (size_t)I / 2, sb = nv ? I / 16 : I / 32;
+    if (a.shd.w2) prefetch_l2_bulk(a.shd.w2 + (size_t)32 * g * I, 64u * I);
+    for (int s = 0; s < R.n_slots; ++s) {
+      const int e = R.slot_e[s];
+      prefetch_l2_bulk(a.ex.w2 + (size_t)e * H * rb + (size_t)32 * g * rb, (uint32_t)(32 * rb));
+      prefetch_l2_bulk(a.ex.w2s + (size_t)e * H * sb + (size_t)32 * g * sb, (uint32_t)(32 * sb));
+    }
+  }
+}
+
+template <int MAXT, bool NV>
 __global__ void __launch_bounds__(FT, 1) k_fused_decode(FusedArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ Routing R;
-  __shared__ float red_s[FW * MAX_DECODE_T];
+  __shared__ float red_s[FW * MAXT];
   __shared__ int s_unit, s_next, s_flag;
   const int T = a.sh.T, H = a.sh.H, I = a.sh.I, E = a.sh.E, n = T * a.sh.k;
   const int nb = I / 32;
@@ -334,9 +381,13 @@ __global__ void __launch_bounds__(FT, 1) k_fused_decode(FusedArgs a) {
   int u = s_unit;
   while (u < a.u_end) {
     __syncthreads();
-    if (threadIdx.x == 0) s_next = atomicAdd(a.ctr + C_QUEUE, 1);
+    if (threadIdx.x == 0) {
+      const int nx = atomicAdd(a.ctr + C_QUEUE, 1);
+      s_next = nx;
+      prefetch_unit(a, R, have_routing > 0, nx);
+    }
     if (u < a.u_quant) {
-      unit_router(a, u, red_s);
+      unit_router<MAXT>(a, u, red_s);
       publish(a.ctr + C_ROUTER);
     } else if (u < a.u_sgu) {
       unit_quant(a);
@@ -349,7 +400,7 @@ __global__ void __launch_bounds__(FT, 1) k_fused_decode(FusedArgs a) {
         __syncthreads();
         have_x = 1;
       }
-      unit_shared_gate_up(a, u - a.u_sgu, x_s, gu_s);
+      unit_shared_gate_up<MAXT>(a, u - a.u_sgu, x_s, gu_s);
       publish(a.ctr + C_GU);
     } else {
       if (!have_routing) {
@@ -369,7 +420,7 @@ __global__ void __launch_bounds__(FT, 1) k_fused_decode(FusedArgs a) {
               __syncthreads();
             }
           }
-          if (have_xq > 0) unit_routed_gate_up<NV>(a, R, s, b, xq_s, xsc_s, gu_s);
+          if (have_xq > 0) unit_routed_gate_up<MAXT, NV>(a, R, s, b, xq_s, xsc_s, gu_s);
         }
         publish(a.ctr + C_GU);
       } else if (have_routing > 0) {
@@ -388,7 +439,7 @@ __global__ void __launch_bounds__(FT, 1) k_fused_decode(FusedArgs a) {
         }
         if (have_down > 0) {
           const int g = u - a.u_down;
-          unit_down<NV>(a, R, g, hq_s, hsc_s, hsh_s, y_s);
+          unit_down<MAXT, NV>(a, R, g, hq_s, hsc_s, hsh_s, y_s);
           if (g == 0 && threadIdx.x < n) {
             if (a.ids_out) a.ids_out[threadIdx.x] = R.ids[threadIdx.x];
             if (a.w_out) a.w_out[threadIdx.x] = R.w[threadIdx.x];
@@ -435,6 +486,21 @@ SmemPlan plan_smem(const Shape& sh, bool shared) {
   return p;
 }
 
+template <int MAXT>
+const void* fused_kernel_t(bool nv) {
+  return nv ? (const void*)k_fused_decode<MAXT, true> : (const void*)k_fused_decode<MAXT, false>;
+}
+
+const void* fused_kernel(int maxt, bool nv) {
+  switch (maxt) {
+    case 1: return fused_kernel_t<1>(nv);
+    case 2: return fused_kernel_t<2>(nv);
+    case 4: return fused_kernel_t<4>(nv);
+    case 8: return fused_kernel_t<8>(nv);
+    default: return fused_kernel_t<16>(nv);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd,
@@ -478,7 +544,8 @@ cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const Sha
   a.off_hsh = sp.off_hsh;
   a.off_y = sp.off_y;
 
-  const void* fn = ex.nv ? (const void*)k_fused_decode<true> : (const void*)k_fused_decode<false>;
+  const int maxt = sh.T <= 1 ? 1 : sh.T <= 2 ? 2 : sh.T <= 4 ? 4 : sh.T <= 8 ? 8 : 16;
+  const void* fn = fused_kernel(maxt, ex.nv != 0);
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, sp.bytes);
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 0, per_sm = 0;
@@ -489,11 +556,8 @@ cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const Sha
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int grid = sms * per_sm;
   if (grid > a.u_end) grid = a.u_end;
-  if (ex.nv)
-    k_fused_decode<true><<<grid, FT, sp.bytes, s>>>(a);
-  else
-    k_fused_decode<false><<<grid, FT, sp.bytes, s>>>(a);
-  return cudaGetLastError();
+  void* args[] = {&a};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(FT), args, sp.bytes, s);
 }
 
 cudaError_t launch_wait_probe(void* ws, uint64_t wait_limit_ns, cudaStream_t s) {
