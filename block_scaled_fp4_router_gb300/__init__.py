@@ -28,7 +28,9 @@ EXPORTED = [
     "moe_status_string", "moe_workspace_size", "moe_get_status", "moe_router_topk",
     "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
+    "moe_layer_decode_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class MoeError(RuntimeError):
@@ -83,6 +85,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_forward": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
         "moe_set_wait_limit_ns": ([U64], None),
         "moe_debug_wait_probe": ([P, S, U64, P], ctypes.c_int),
+        "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -201,3 +204,11 @@ def moe_layer_forward(d, ex, sh, w_router, bias, x, out, topk_ids, topk_w, ws, s
     _check(load().moe_layer_forward(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh), _p(w_router), _p(bias),
                                     _p(x), _p(out), _p(topk_ids), _p(topk_w), _p(ws), _nbytes(ws),
                                     _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_decode_noalloc(d, ex, sh, w_router, bias, x, out, topk_ids, topk_w, stream=None):
+    """moe_layer_decode with the library's built-in scratch instead of a caller
+    workspace, for callers that cannot allocate device memory (see the header)."""
+    _check(load().moe_layer_decode_noalloc(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh), _p(w_router),
+                                           _p(bias), _p(x), _p(out), _p(topk_ids), _p(topk_w), _stream(stream)),
+           "moe_layer_decode_noalloc")

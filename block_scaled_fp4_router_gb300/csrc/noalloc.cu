@@ -1,0 +1,71 @@
+// moe_layer_decode_noalloc: the single-launch decode with its scratch memory
+// built into the library instead of passed in by the caller.
+//
+// Some callers cannot hand the library a workspace: a plain C host program
+// that links only this library and the CUDA runtime and has no device-memory
+// manager of its own, or a plugin running inside a host framework whose
+// memory pool does not let outside code allocate device memory.  For them this
+// entry point uses a fixed scratch array that lives in the library itself; it
+// allocates nothing per call.
+//
+// The scratch is a file-scope device array of MOE_NOALLOC_SCRATCH_BYTES
+// (8 MiB).  Every GPU that loads the library holds it until the process
+// exits.  In host code the array's name is only a stand-in, not a device
+// address, so the real address is looked up once per device with
+// cudaGetSymbolAddress (on the first call made on that device, with that
+// device current) and then handed to the kernel.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "layout.h"
+#include "moefp4.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of this device's copy of the scratch array (set-up on the
+// first call per device).
+moe_status_t scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_layer_decode_noalloc(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                                 const moe_shared_bf16_t* shared, const float* w_router,
+                                                 const float* bias, const void* x, void* out, int32_t* topk_ids,
+                                                 float* topk_w, moe_stream_t stream) {
+  size_t need = 0;
+  const moe_status_t st = moe_workspace_size(desc, &need);
+  if (st != MOE_OK) return st;
+  if (desc->T > moefp4::MAX_DECODE_T) return MOE_ERR_UNSUPPORTED;
+  if (need > kScratchBytes) return MOE_ERR_UNSUPPORTED;  // shape too large for the built-in scratch
+  if (desc->T == 0) return MOE_OK;
+  void* ws = nullptr;
+  const moe_status_t sst = scratch_for_current_device(&ws);
+  if (sst != MOE_OK) return sst;
+  // The scratch keeps whatever the previous call left in it; the launch needs
+  // its counters and status word at zero.
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(int) * moefp4::N_COUNTERS, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return moe_layer_decode(desc, experts, shared, w_router, bias, x, out, topk_ids, topk_w, ws, kScratchBytes,
+                          stream);
+}

@@ -203,6 +203,34 @@ MOE_API moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_e
                                const float* bias, const void* x, void* out, int32_t* topk_ids,
                                float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Size of the scratch array built into the library for
+ * moe_layer_decode_noalloc (8 MiB, held on every GPU that loads the library
+ * until the process exits). */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* moe_layer_decode without a caller workspace.  The paper has no counterpart
+ * to this entry point; it exists for callers that cannot hand the library
+ * device memory: a plain C host program that links only this library and the
+ * CUDA runtime and keeps no device allocator of its own, or a plugin inside a
+ * host framework whose memory pool does not allow outside device
+ * allocations.  It allocates nothing: its scratch is a fixed array inside the
+ * library (MOE_NOALLOC_SCRATCH_BYTES).  Inputs, outputs and results are
+ * exactly those of moe_layer_decode.
+ *   - Shapes whose moe_workspace_size exceeds MOE_NOALLOC_SCRATCH_BYTES, and
+ *     T > 16, return MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up that device's scratch address (with
+ *     the device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps what the
+ *     previous call left; each call clears the part that must start at zero
+ *     (an extra memset on the stream).  Calls whose launches may overlap on
+ *     the GPU (different streams, no ordering between them) race on it.
+ *   - A device-side wait that runs out is not reported (there is no workspace
+ *     to read a status word from); the next call clears it. */
+MOE_API moe_status_t moe_layer_decode_noalloc(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                              const moe_shared_bf16_t* shared, const float* w_router,
+                                              const float* bias, const void* x, void* out, int32_t* topk_ids,
+                                              float* topk_w, moe_stream_t stream);
+
 /* Upper bound, in nanoseconds, of every device-side dependency wait of later
  * launches in this process (default 500 ms).  A wait that runs out records
  * MOE_ERR_TIMEOUT in the workspace status word and the launch returns without
