@@ -28,7 +28,7 @@ EXPORTED = [
     "moe_status_string", "moe_workspace_size", "moe_get_status", "moe_router_topk",
     "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
-    "moe_layer_decode_noalloc",
+    "moe_layer_decode_noalloc", "moe_debug_requantized_h",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_set_wait_limit_ns": ([U64], None),
         "moe_debug_wait_probe": ([P, S, U64, P], ctypes.c_int),
         "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
+        "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -166,6 +167,11 @@ def moe_set_wait_limit_ns(ns: int) -> None:
 def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
     _check(load().moe_debug_wait_probe(_p(ws), _nbytes(ws), int(limit_ns), _stream(stream)),
            "moe_debug_wait_probe")
+
+
+def moe_debug_requantized_h(d, ws, hq, hs, stream=None):
+    _check(load().moe_debug_requantized_h(ctypes.byref(d), _p(ws), _nbytes(ws), _p(hq), _p(hs), _stream(stream)),
+           "moe_debug_requantized_h")
 
 
 def moe_router_topk(d, x, w_router, bias, topk_ids, topk_w, logits, ws, stream=None):

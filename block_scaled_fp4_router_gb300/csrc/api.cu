@@ -74,6 +74,40 @@ T* at(void* ws, size_t off) {
 
 Shape shape_of(const moe_layer_desc_t* d) { return Shape{d->T, d->H, d->I, d->E, d->top_k}; }
 
+// A5 - A8: the routed experts on tensor cores when the batch is large enough
+// and the weights are MXFP4 (kind::mxf4 takes E8M0 scales), otherwise on CUDA
+// cores; the shared expert likewise from TC_MIN_T_SHARED tokens.
+moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, const SharedDev& shd,
+                            const uint16_t* x, const uint8_t* xq, const uint8_t* xs, const int* offsets,
+                            const int* perm, float* y_assign, float* y_shared, void* ws, cudaStream_t s) {
+  const WsLayout L = ws_layout(d->T, d->H, d->I, d->E, d->top_k);
+  const Shape sh = shape_of(d);
+  const uint64_t limit = g_wait_limit_ns.load();
+  int* status = at<int>(ws, L.counters) + C_STATUS;
+  const bool tc = !ex.nv && tc_routed_enabled(d->T * d->top_k) && d->H % 256 == 0 && d->I % 256 == 0 &&
+                  aligned(ex.w13s, 4) &&
+                  aligned(ex.w2s, 4);
+  // record which layout h is left in (read by moe_debug_requantized_h)
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.counters) + C_HPATH, tc ? 1 : 0, sizeof(int), s));
+  if (tc) {
+    TcWorkspace w{at<int>(ws, L.tc_poff), at<uint8_t>(ws, L.tc_mtiles), at<int>(ws, L.tc_num_mt),
+                  at<uint8_t>(ws, L.tc_xq), at<uint8_t>(ws, L.tc_xs), at<uint8_t>(ws, L.tc_hq),
+                  at<uint8_t>(ws, L.tc_hs), at<uint8_t>(ws, L.tc_w13s), at<uint8_t>(ws, L.tc_w2s)};
+    MOE_CUDA(launch_expert_ffn_tc(sh, ex, w, xq, xs, offsets, perm, y_assign, status, limit, s));
+  } else {
+    MOE_CUDA(launch_routed_simt(sh, ex, xq, xs, offsets, perm, at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs),
+                                y_assign, s));
+  }
+  if (shd.w13) {
+    uint16_t* h = at<uint16_t>(ws, L.h_shared);
+    if (d->T >= TC_MIN_T_SHARED && d->H % 256 == 0)
+      MOE_CUDA(launch_shared_tc(sh, shd, x, h, y_shared, status, limit, s));
+    else
+      MOE_CUDA(launch_shared_simt(sh, shd, x, h, y_shared, s));
+  }
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -106,6 +140,21 @@ moe_status_t moe_get_status(void* ws, moe_status_t* st) {
   if (v != 0) MOE_CUDA(cudaMemset(word, 0, sizeof(int)));
   *st = static_cast<moe_status_t>(v);
   return MOE_OK;
+}
+
+moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes, uint8_t* hq,
+                                     uint8_t* hs, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_ws(desc, const_cast<void*>(ws), ws_bytes));
+  if (desc->T == 0) return MOE_OK;
+  if (!hq || !hs || !aligned(hq, 16)) return MOE_ERR_INVALID_ARG;
+  void* w = const_cast<void*>(ws);
+  const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
+  TcWorkspace tw{at<int>(w, L.tc_poff), at<uint8_t>(w, L.tc_mtiles), at<int>(w, L.tc_num_mt), at<uint8_t>(w, L.tc_xq),
+                 at<uint8_t>(w, L.tc_xs), at<uint8_t>(w, L.tc_hq), at<uint8_t>(w, L.tc_hs), at<uint8_t>(w, L.tc_w13s),
+                 at<uint8_t>(w, L.tc_w2s)};
+  return cuda_status(launch_copy_h(shape_of(desc), at<int>(w, L.counters) + C_HPATH, at<uint8_t>(w, L.hq),
+                                   at<uint8_t>(w, L.hs), tw, hq, hs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
@@ -168,11 +217,8 @@ moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_
   if (!aligned(xq, 16) || !aligned(y_assign, 16)) return MOE_ERR_INVALID_ARG;
   if (shd.w13 && (!x || !y_shared || !aligned(x, 16) || !aligned(y_shared, 16))) return MOE_ERR_INVALID_ARG;
   if (!shd.w13 && y_shared) return MOE_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
-  return cuda_status(launch_expert_ffn(shape_of(desc), ex, shd, static_cast<const uint16_t*>(x), xq, xs,
-                                       offsets, perm, at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs),
-                                       at<uint16_t>(ws, L.h_shared), y_assign, y_shared,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+  return run_expert_ffn(desc, ex, shd, static_cast<const uint16_t*>(x), xq, xs, offsets, perm, y_assign, y_shared,
+                        ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_assign, const int32_t* inv_perm,
@@ -212,10 +258,8 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_experts_t
                           at<int>(ws, L.perm), at<int>(ws, L.inv_perm), at<int>(ws, L.rank),
                           at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base), s));
   float* ysh = shd.w13 ? at<float>(ws, L.y_shared) : nullptr;
-  MOE_CUDA(launch_expert_ffn(sh, ex, shd, xb, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs),
-                             at<int>(ws, L.offsets), at<int>(ws, L.perm), at<uint8_t>(ws, L.hq),
-                             at<uint8_t>(ws, L.hs), at<uint16_t>(ws, L.h_shared), at<float>(ws, L.y_assign),
-                             ysh, s));
+  MOE_TRY(run_expert_ffn(desc, ex, shd, xb, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), at<int>(ws, L.offsets),
+                         at<int>(ws, L.perm), at<float>(ws, L.y_assign), ysh, ws, s));
   return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh,
                                     static_cast<uint16_t*>(out), s));
 }

@@ -240,14 +240,12 @@ static cudaError_t set_smem(const void* fn, size_t bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-cudaError_t launch_expert_ffn(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd,
-                              const uint16_t* x, const uint8_t* xq, const uint8_t* xs,
-                              const int* offsets, const int* perm, uint8_t* hq, uint8_t* hs,
-                              uint16_t* h_shared, float* y_assign, float* y_shared, cudaStream_t s) {
+cudaError_t launch_routed_simt(const Shape& sh, const ExpertsDev& ex, const uint8_t* xq, const uint8_t* xs,
+                               const int* offsets, const int* perm, uint8_t* hq, uint8_t* hs, float* y_assign,
+                               cudaStream_t s) {
   if (sh.T == 0) return cudaSuccess;
   cudaError_t err;
   const int H = sh.H, I = sh.I;
-  // routed gate/up + SwiGLU + requantise
   {
     const size_t smem = (size_t)NT * (H / 2) + sizeof(float) * NT * (H / 32) + sizeof(float) * 64 * NT +
                         sizeof(int) * NT;
@@ -260,14 +258,6 @@ cudaError_t launch_expert_ffn(const Shape& sh, const ExpertsDev& ex, const Share
       k_routed_gate_up<false><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  // shared gate/up
-  if (shd.w13) {
-    const size_t smem = (size_t)NT_SH * H * 2 + sizeof(float) * 16 * NT_SH;
-    if ((err = set_smem((const void*)k_shared_gate_up, smem)) != cudaSuccess) return err;
-    k_shared_gate_up<<<I / 8, THREADS, smem, s>>>(sh, shd, x, h_shared);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  }
-  // routed down
   {
     const size_t smem = (size_t)NT * (I / 2) + sizeof(float) * NT * (I / 32) + sizeof(int) * NT;
     const void* fn = ex.nv ? (const void*)k_routed_down<true> : (const void*)k_routed_down<false>;
@@ -279,8 +269,21 @@ cudaError_t launch_expert_ffn(const Shape& sh, const ExpertsDev& ex, const Share
       k_routed_down<false><<<grid, THREADS, smem, s>>>(sh, ex, hq, hs, offsets, y_assign);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  // shared down
-  if (shd.w13) {
+  return cudaSuccess;
+}
+
+cudaError_t launch_shared_simt(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
+                               float* y_shared, cudaStream_t s) {
+  if (sh.T == 0 || !shd.w13) return cudaSuccess;
+  cudaError_t err;
+  const int H = sh.H, I = sh.I;
+  {
+    const size_t smem = (size_t)NT_SH * H * 2 + sizeof(float) * 16 * NT_SH;
+    if ((err = set_smem((const void*)k_shared_gate_up, smem)) != cudaSuccess) return err;
+    k_shared_gate_up<<<I / 8, THREADS, smem, s>>>(sh, shd, x, h_shared);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  {
     const size_t smem = (size_t)NT * I * 2;
     if ((err = set_smem((const void*)k_shared_down, smem)) != cudaSuccess) return err;
     k_shared_down<<<H / 16, THREADS, smem, s>>>(sh, shd, h_shared, y_shared);

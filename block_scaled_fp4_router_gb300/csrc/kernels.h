@@ -37,11 +37,36 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, floa
 // A3
 cudaError_t launch_permute(const int* ids, int T, int k, int E, int* counts, int* offsets, int* perm,
                            int* inv_perm, int* rank, int* chunk_cnt, int* chunk_base, cudaStream_t s);
-// A5 - A8 (unfused)
-cudaError_t launch_expert_ffn(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd,
-                              const uint16_t* x, const uint8_t* xq, const uint8_t* xs,
-                              const int* offsets, const int* perm, uint8_t* hq, uint8_t* hs,
-                              uint16_t* h_shared, float* y_assign, float* y_shared, cudaStream_t s);
+// A5 - A7 on CUDA cores (any T; the decode-sized path)
+cudaError_t launch_routed_simt(const Shape& sh, const ExpertsDev& ex, const uint8_t* xq, const uint8_t* xs,
+                               const int* offsets, const int* perm, uint8_t* hq, uint8_t* hs, float* y_assign,
+                               cudaStream_t s);
+// A8 on CUDA cores
+cudaError_t launch_shared_simt(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
+                               float* y_shared, cudaStream_t s);
+
+// Workspace regions of the tensor-core path.
+struct TcWorkspace {
+  int* poff;
+  void* mtiles;
+  int* num_mt;
+  uint8_t* xq_perm;
+  uint8_t* xs_mma;
+  uint8_t* hq_perm;
+  uint8_t* hs_mma;
+  uint8_t* w13s_mma;
+  uint8_t* w2s_mma;
+};
+// A5 - A7 on tensor cores (MXFP4 weights)
+cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const TcWorkspace& w, const uint8_t* xq,
+                                 const uint8_t* xs, const int* offsets, const int* perm, float* y_assign,
+                                 int* status, uint64_t limit_ns, cudaStream_t s);
+// A8 on tensor cores
+cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
+                             float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s);
+// Copies the requantised h to sorted-assignment order (either layout).
+cudaError_t launch_copy_h(const Shape& sh, const int* hpath, const uint8_t* hq_sorted, const uint8_t* hs_sorted,
+                          const TcWorkspace& w, uint8_t* hq_out, uint8_t* hs_out, cudaStream_t s);
 // A9
 cudaError_t launch_combine(const Shape& sh, const float* y_assign, const int* inv_perm, const float* w,
                            const float* y_shared, uint16_t* out, cudaStream_t s);

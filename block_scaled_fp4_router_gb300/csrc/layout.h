@@ -16,6 +16,12 @@ constexpr int MAX_TOPK = 8;
 constexpr int MAX_E = 256;
 constexpr int MAX_DECODE_T = 16;   // fused single-launch decode range
 constexpr int PERM_CHUNK = 1024;   // assignments ranked per block in the permutation
+constexpr int TC_MIN_ASSIGN = 256; // routed experts on tensor cores from this many assignments
+constexpr int TC_MIN_T_SHARED = 128; // shared expert on tensor cores from this many tokens
+
+// Rows of the per-expert padded order (each expert's rows rounded up to 128).
+MOE_HD inline int tc_padded_rows(int n, int E) { return ((n + E * 127) + 127) / 128 * 128; }
+MOE_HD inline bool tc_routed_enabled(int n) { return n >= TC_MIN_ASSIGN; }
 
 // Device status word values (mirror moe_status_t).
 constexpr int MOE_DEV_OK = 0;
@@ -30,6 +36,7 @@ enum Counter : int {
   C_GU = 4,        // gate/up units finished (shared + routed)
   C_EXIT = 5,      // blocks finished (the last one resets the counters)
   C_TEST = 6,      // never written by the library: a wait on it always times out
+  C_HPATH = 7,     // which layout the last expert FFN left h in (0: sorted rows, else padded tiles)
   N_COUNTERS = 16
 };
 
@@ -55,6 +62,16 @@ struct WsLayout {
   size_t h_shared;     // bf16 [T, I]
   size_t y_assign;     // float [T*k, H]   (layer_forward only)
   size_t y_shared;     // float [T, H]     (layer_forward only)
+  // tensor-core path (present when the routed experts run on tensor cores)
+  size_t tc_poff;      // int [E+1]
+  size_t tc_mtiles;    // 16-byte tile descriptors [padded rows / 128]
+  size_t tc_num_mt;    // int
+  size_t tc_xq;        // uint8 [padded rows, H/2]
+  size_t tc_xs;        // scale blocks [padded rows/128][H/128][512 B]
+  size_t tc_hq;        // uint8 [padded rows, I/2]
+  size_t tc_hs;        // scale blocks [padded rows/128][I/128][512 B]
+  size_t tc_w13s;      // weight scale blocks [E][2I/128][H/128][512 B]
+  size_t tc_w2s;       // weight scale blocks [E][H/128][I/128][512 B]
   size_t total;
 };
 
@@ -86,6 +103,17 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.h_shared = take((size_t)2 * T * I);
   L.y_assign = take(sizeof(float) * n * H);
   L.y_shared = take(sizeof(float) * (size_t)T * H);
+  const bool tc = tc_routed_enabled((int)n);
+  const size_t R = tc ? (size_t)tc_padded_rows((int)n, E) : 0;
+  L.tc_poff = take(tc ? sizeof(int) * (E + 1) : 0);
+  L.tc_mtiles = take(16 * (R / 128));
+  L.tc_num_mt = take(tc ? sizeof(int) : 0);
+  L.tc_xq = take(R * H / 2);
+  L.tc_xs = take(R * H / 32);
+  L.tc_hq = take(R * I / 2);
+  L.tc_hs = take(R * I / 32);
+  L.tc_w13s = take(tc ? (size_t)E * 2 * I * H / 32 : 0);
+  L.tc_w2s = take(tc ? (size_t)E * H * I / 32 : 0);
   L.total = o;
   return L;
 }

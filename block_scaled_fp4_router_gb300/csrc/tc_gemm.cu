@@ -1,0 +1,572 @@
+// Tensor-core (tcgen05) GEMMs of the batched path: the routed expert
+// gate/up and down projections on block-scaled FP4 (kind::mxf4, E8M0 scales
+// per 32) and the BF16 shared expert (kind::f16), with the SwiGLU + MXFP4
+// requantise epilogue fused into the gate/up GEMM (AMD technical article
+// "MiniMax-M3.1 on AMD Instinct GPUs", section "What we Optimized": the
+// MXFP4 fused MoE; model card "amd/MiniMax-M3.1-Flash-Quark-MXFP4", section
+// "Model Overview": MXFP4 weights and activations).
+//
+// One persistent kernel per GEMM, warp-specialised (192 threads):
+//   warp 0      TMA producer: 2D swizzled tiles of A and B and 1D bulk copies
+//               of their scale blocks into a 4-stage shared-memory ring;
+//   warp 1      MMA issuer: copies the stage's scale blocks into TMEM with
+//               tcgen05.cp and issues 4 MMAs per 256-element (FP4) / 64-element
+//               (BF16) K stage into a 128 x 256 FP32 accumulator in TMEM;
+//               tcgen05.commit frees the stage and signals the epilogue;
+//   warps 2-5   epilogue: one TMEM lane (one output row) per thread.
+// Tiles are 128 rows of A (tokens) x 256 rows of B (weight rows); for the
+// gate/up GEMMs the 256 B rows are 128 gate rows and the 128 matching up rows,
+// so each thread holds G and U of the same 128 columns.
+//
+// Grouped (routed) GEMMs run on a per-expert padded row order: expert e's
+// assignments occupy rows [poff[e], poff[e] + count[e]) of a buffer whose
+// expert blocks start at multiples of 128, so a tile never spans experts.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moefp4 {
+
+namespace {
+
+constexpr int BM = 128;           // A rows per tile
+constexpr int BN = 256;           // B rows per tile (accumulator columns)
+constexpr int STAGES = 4;
+constexpr int TC_THREADS = 192;
+constexpr uint32_t A_BYTES = BM * 128;       // 16 KB: 128 rows x 128 B
+constexpr uint32_t B_BYTES = BN * 128;       // 32 KB
+constexpr uint32_t SFA_BYTES = 2 * 512;      // two K groups of 128 elements
+constexpr uint32_t SFB_BYTES = 2 * 2 * 512;  // two 128-row B blocks x two K groups
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_TMEM_BASE = 256;       // scale slots after the 256 accumulator columns
+
+enum Kind { KIND_FP4 = 0, KIND_BF16 = 1 };
+enum Epi { EPI_SWIGLU_MX = 0, EPI_STORE_F32 = 1, EPI_SWIGLU_BF16 = 2 };
+
+__host__ __device__ constexpr uint32_t stage_bytes(int kind) {
+  return kind == KIND_FP4 ? A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES : A_BYTES + B_BYTES;
+}
+
+}  // namespace
+
+// One 128-row tile of A: which expert, its first row in the padded order and
+// in the sorted-assignment order, and how many of its rows are real.
+struct MTile {
+  int e;
+  int prow0;
+  int srow0;
+  int rows;
+};
+
+// --------------------------------------------------------------- tile list
+
+// One block: padded expert offsets and the list of 128-row tiles.
+__global__ void __launch_bounds__(256) k_build_mtiles(const int* __restrict__ offsets, int E, int* __restrict__ poff,
+                                                      MTile* __restrict__ tiles, int* __restrict__ num_tiles) {
+  __shared__ int s_poff[MAX_E + 1];
+  if (threadIdx.x == 0) {
+    int p = 0;
+    for (int e = 0; e < E; ++e) {
+      s_poff[e] = p;
+      const int cnt = offsets[e + 1] - offsets[e];
+      p += (cnt + BM - 1) / BM * BM;
+    }
+    s_poff[E] = p;
+    *num_tiles = p / BM;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) poff[e] = s_poff[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int cnt = offsets[e + 1] - offsets[e];
+    for (int m = 0; m * BM < cnt; ++m) {
+      MTile t;
+      t.e = e;
+      t.prow0 = s_poff[e] + m * BM;
+      t.srow0 = offsets[e] + m * BM;
+      t.rows = min(BM, cnt - m * BM);
+      tiles[t.prow0 / BM] = t;
+    }
+  }
+}
+
+// One block per padded row: copy the MXFP4 activation row of the assignment
+// there (zeros for padding rows) and scatter its scale bytes into the MMA
+// scale layout.  Scale layout of a matrix with R rows (R a multiple of 128)
+// and K elements: block (R/128 row tile, K/128 group) of 512 bytes, word
+// (i, j) at byte 16 i + 4 j holding the 4 scale bytes of row 32 j + i.
+__global__ void __launch_bounds__(128) k_gather_mx_rows(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
+                                                        int K, int k_top, const int* __restrict__ perm,
+                                                        const MTile* __restrict__ tiles, const int* __restrict__ num_tiles,
+                                                        uint8_t* __restrict__ q_out, uint32_t* __restrict__ sf_out) {
+  const int r = blockIdx.x;
+  if (r >= *num_tiles * BM) return;
+  const MTile t = tiles[r / BM];
+  const int m = r % BM;
+  const bool real = m < t.rows;
+  const int src = real ? perm[t.srow0 + m] / k_top : 0;
+  const int cpr = K / 32;  // 16-byte chunks per row
+  for (int c = threadIdx.x; c < cpr; c += blockDim.x) {
+    const uint4 v = real ? __ldg(reinterpret_cast<const uint4*>(q + (size_t)src * (K / 2)) + c) : make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(q_out + (size_t)r * (K / 2))[c] = v;
+  }
+  const int groups = K / 128;
+  const int i = m % 32, j = m / 32;
+  for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+    const uint32_t w = real ? __ldg(reinterpret_cast<const uint32_t*>(s + (size_t)src * (K / 32)) + g) : 0u;
+    sf_out[((size_t)(r / BM) * groups + g) * 128 + i * 4 + j] = w;
+  }
+}
+
+// Re-lays canonical scale bytes [E][R][K/32] into the MMA scale layout
+// [E][R/128][K/128][512 B].  One thread per 4-byte word.
+__global__ void __launch_bounds__(256) k_relayout_weight_sf(const uint8_t* __restrict__ s, int E, int R, int K,
+                                                            uint32_t* __restrict__ out) {
+  const size_t words = (size_t)E * R * (K / 128);
+  const size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= words) return;
+  const int groups = K / 128;
+  const size_t row = w / groups;  // global row (e * R + r)
+  const int g = (int)(w % groups);
+  const int m = (int)(row % BM);
+  const size_t tile = row / BM;   // (e * R + r) / 128: R is a multiple of 128
+  const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(s + row * (K / 32)) + g);
+  out[(tile * groups + g) * 128 + (m % 32) * 4 + (m / 32)] = v;
+}
+
+// ------------------------------------------------------------------ GEMM
+
+namespace {
+
+struct GemmArgs {
+  int K;                   // reduction length in elements
+  int n_tiles;             // B tiles per A tile
+  const int* num_mt;       // grouped: device count of A tiles
+  int num_mt_dense;        // dense: count of A tiles
+  int rows_dense;          // dense: rows of A
+  const MTile* mt;         // grouped: A tiles
+  int b_rows_per_expert;   // grouped: rows of B per expert (0 for dense)
+  int b_up_off;            // gate/up GEMMs: row offset of the up block (I)
+  const uint8_t* sfa;      // FP4: A scales, MMA layout
+  const uint8_t* sfb;      // FP4: B scales, MMA layout [E][R/128][K/128][512]
+  int sfb_rtiles;          // FP4: R/128 of B per expert
+  // epilogue outputs
+  uint8_t* hq;             // EPI_SWIGLU_MX: codes [padded rows][I/2]
+  uint32_t* hs;            // EPI_SWIGLU_MX: scales, MMA layout over I
+  int h_cols;              // I (SwiGLU epilogues)
+  uint16_t* h_bf16;        // EPI_SWIGLU_BF16: [rows][I]
+  float* out;              // EPI_STORE_F32: [rows][ldo]
+  int ldo;
+  int* status;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& g, bool grouped, int t, int& a_row, int& e, int& rows,
+                                            int& srow0, int& nt, int& mti) {
+  mti = t / g.n_tiles;
+  nt = t % g.n_tiles;
+  if (grouped) {
+    const MTile m = g.mt[mti];
+    a_row = m.prow0;
+    e = m.e;
+    rows = m.rows;
+    srow0 = m.srow0;
+  } else {
+    a_row = mti * BM;
+    e = 0;
+    rows = min(BM, g.rows_dense - a_row);
+    srow0 = a_row;
+  }
+}
+
+template <int KIND, int EPI, bool GROUPED>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, GemmArgs g) {
+  extern __shared__ __align__(1024) uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[STAGES], empty[STAGES], acc_full, acc_empty, drain;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  constexpr uint32_t SB = stage_bytes(KIND);
+  constexpr bool SWIGLU = EPI == EPI_SWIGLU_MX || EPI == EPI_SWIGLU_BF16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(&acc_full, 1);
+    tc::mbar_init(&acc_empty, 128);
+    tc::mbar_init(&drain, 1);
+    tc::mbar_fence_init();
+    abort_flag = 0;
+    tc::prefetch_tensormap(&mapA);
+    tc::prefetch_tensormap(&mapB);
+  }
+  if (warp == 1) tc::tmem_alloc(&tmem_base, TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const int num_mt = GROUPED ? *g.num_mt : g.num_mt_dense;
+  const int total = num_mt * g.n_tiles;
+  const int nks = g.K / (KIND == KIND_FP4 ? 256 : 64);
+  const int kgroups = g.K / 128;  // FP4 scale groups per row
+
+  auto fail = [&]() {
+    atomicCAS(g.status, 0, (int)MOE_DEV_TIMEOUT);
+    atomicExch(&abort_flag, 1);
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer
+    uint32_t stage = 0, phase = 0;
+    for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
+      int a_row, e, rows, srow0, nt, mti;
+      tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti);
+      const int b_base = e * g.b_rows_per_expert;
+      const int b0 = SWIGLU ? b_base + nt * (BN / 2) : b_base + nt * BN;
+      const int b1 = SWIGLU ? b0 + g.b_up_off : b0 + BN / 2;
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
+        uint8_t* sa = dsm + stage * SB;
+        uint8_t* sb = sa + A_BYTES;
+        tc::mbar_expect_tx(&full[stage], SB);
+        tc::tma_load_2d(sa, &mapA, ks * 128, a_row, &full[stage]);
+        tc::tma_load_2d(sb, &mapB, ks * 128, b0, &full[stage]);
+        tc::tma_load_2d(sb + B_BYTES / 2, &mapB, ks * 128, b1, &full[stage]);
+        if (KIND == KIND_FP4) {
+          uint8_t* ssa = sb + B_BYTES;
+          uint8_t* ssb = ssa + SFA_BYTES;
+          const int a_tile = a_row / BM;
+          tc::bulk_load(ssa, g.sfa + ((size_t)a_tile * kgroups + 2 * ks) * 512, 1024, &full[stage]);
+          const size_t rt0 = (size_t)e * g.sfb_rtiles + (b0 - b_base) / BM;
+          const size_t rt1 = (size_t)e * g.sfb_rtiles + (b1 - b_base) / BM;
+          tc::bulk_load(ssb, g.sfb + (rt0 * kgroups + 2 * ks) * 512, 1024, &full[stage]);
+          tc::bulk_load(ssb + 1024, g.sfb + (rt1 * kgroups + 2 * ks) * 512, 1024, &full[stage]);
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    const uint32_t idesc_bf = tc::idesc_bf16(BM, BN);
+    for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
+      if (!tc::mbar_wait(&acc_empty, acc_phase ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
+      tc::fence_after_sync();
+      bool ok = true;
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!tc::mbar_wait(&full[stage], phase, g.limit_ns, &abort_flag)) { fail(); ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t sa = tc::smem_u32(dsm + stage * SB);
+        const uint32_t sb = sa + A_BYTES;
+        if (KIND == KIND_FP4) {
+          const uint32_t ssa = sb + B_BYTES, ssb = ssa + SFA_BYTES;
+          const uint32_t ta = tmem + SF_TMEM_BASE + stage * 24;  // 8 columns of A scales, 16 of B
+          const uint32_t tb = ta + 8;
+          tc::sf_copy(ta + 0, tc::desc_sf(ssa));
+          tc::sf_copy(ta + 4, tc::desc_sf(ssa + 512));
+          tc::sf_copy(tb + 0, tc::desc_sf(ssb));            // B rows 0..127, group 0
+          tc::sf_copy(tb + 4, tc::desc_sf(ssb + 1024));     // B rows 128..255, group 0
+          tc::sf_copy(tb + 8, tc::desc_sf(ssb + 512));      // B rows 0..127, group 1
+          tc::sf_copy(tb + 12, tc::desc_sf(ssb + 1536));    // B rows 128..255, group 1
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int grp = kk >> 1, id = (kk & 1) * 2;
+            tc::mma_mxf4(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32),
+                         tc::idesc_mxf4(BM, BN, id, id), ta + 4 * grp, tb + 8 * grp, (ks | kk) != 0);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32), idesc_bf, (ks | kk) != 0);
+        }
+        tc::mma_commit(&empty[stage]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      tc::mma_commit(&acc_full);
+      acc_phase ^= 1;
+    }
+    // wait (bounded) for every MMA this thread issued before TMEM is released
+    tc::mma_commit(&drain);
+    if (!tc::mbar_wait(&drain, 0, g.limit_ns, &abort_flag)) fail();
+  } else if (warp >= 2) {
+    // ---------------- epilogue: thread <-> accumulator row
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
+      int a_row, e, rows, srow0, nt, mti;
+      tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti);
+      if (!tc::mbar_wait(&acc_full, acc_phase, g.limit_ns, &abort_flag)) { fail(); break; }
+      tc::fence_after_sync();
+      if (EPI == EPI_SWIGLU_MX) {
+        // h = SiLU(G) U for 128 columns, requantised to MXFP4 per 32; every
+        // padded row is written (padding rows quantise zeros).
+        uint32_t sw = 0;
+        const int r = a_row + m;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float gv[32], uv[32];
+          tc::tmem_ld32(trow + c * 32, gv);
+          tc::tmem_ld32(trow + 128 + c * 32, uv);
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            gv[i] = silu(gv[i]) * uv[i];
+            amax = fmaxf(amax, fabsf(gv[i]));
+          }
+          const int ex = mx_scale_exp(amax);
+          const float inv = pow2_neg(ex);
+          uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i >> 3] |= e2m1_rne(gv[i] * inv) << (4 * (i & 7));
+          *reinterpret_cast<uint4*>(g.hq + (size_t)r * (g.h_cols / 2) + (nt * 128 + c * 32) / 2) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+          sw |= (uint32_t)(ex + 127) << (8 * c);
+        }
+        const int hgroups = g.h_cols / 128;
+        g.hs[((size_t)(r / BM) * hgroups + nt) * 128 + (m % 32) * 4 + (m / 32)] = sw;
+      } else if (EPI == EPI_SWIGLU_BF16) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float gv[32], uv[32];
+          tc::tmem_ld32(trow + c * 32, gv);
+          tc::tmem_ld32(trow + 128 + c * 32, uv);
+          if (m < rows) {
+            uint16_t* dst = g.h_bf16 + (size_t)(srow0 + m) * g.h_cols + nt * 128 + c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 o;
+              o.x = f32_to_bf16_rn(silu(gv[i + 0]) * uv[i + 0]) | ((uint32_t)f32_to_bf16_rn(silu(gv[i + 1]) * uv[i + 1]) << 16);
+              o.y = f32_to_bf16_rn(silu(gv[i + 2]) * uv[i + 2]) | ((uint32_t)f32_to_bf16_rn(silu(gv[i + 3]) * uv[i + 3]) << 16);
+              o.z = f32_to_bf16_rn(silu(gv[i + 4]) * uv[i + 4]) | ((uint32_t)f32_to_bf16_rn(silu(gv[i + 5]) * uv[i + 5]) << 16);
+              o.w = f32_to_bf16_rn(silu(gv[i + 6]) * uv[i + 6]) | ((uint32_t)f32_to_bf16_rn(silu(gv[i + 7]) * uv[i + 7]) << 16);
+              *reinterpret_cast<uint4*>(dst + i) = o;
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tc::tmem_ld32(trow + c * 32, v);
+          if (m < rows) {
+            float* dst = g.out + (size_t)(srow0 + m) * g.ldo + nt * BN + c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          }
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&acc_empty);
+      acc_phase ^= 1;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+// --------------------------------------------------------- h inspection
+
+// One block per (padded tile, 128 rows): the requantised h of each real row,
+// codes and unscrambled scales, to its sorted-assignment position; or, when
+// h was left in sorted order, a plain copy.
+__global__ void __launch_bounds__(128) k_copy_h(int n, int I, const int* __restrict__ hpath,
+                                                const uint8_t* __restrict__ hq_sorted, const uint8_t* __restrict__ hs_sorted,
+                                                const MTile* __restrict__ tiles, const int* __restrict__ num_tiles,
+                                                const uint8_t* __restrict__ hq_perm, const uint32_t* __restrict__ hs_mma,
+                                                uint8_t* __restrict__ hq_out, uint8_t* __restrict__ hs_out) {
+  const int m = threadIdx.x;
+  const int groups = I / 128;
+  if (*hpath == 0) {
+    const int p = blockIdx.x * 128 + m;
+    if (p >= n) return;
+    for (int c = 0; c < I / 32; ++c)
+      reinterpret_cast<uint4*>(hq_out + (size_t)p * (I / 2))[c] = reinterpret_cast<const uint4*>(hq_sorted + (size_t)p * (I / 2))[c];
+    for (int c = 0; c < I / 32; ++c) hs_out[(size_t)p * (I / 32) + c] = hs_sorted[(size_t)p * (I / 32) + c];
+    return;
+  }
+  if ((int)blockIdx.x >= *num_tiles) return;
+  const MTile t = tiles[blockIdx.x];
+  if (m >= t.rows) return;
+  const int r = t.prow0 + m, p = t.srow0 + m;
+  for (int c = 0; c < I / 32; ++c)
+    reinterpret_cast<uint4*>(hq_out + (size_t)p * (I / 2))[c] = reinterpret_cast<const uint4*>(hq_perm + (size_t)r * (I / 2))[c];
+  for (int g = 0; g < groups; ++g) {
+    const uint32_t w = hs_mma[((size_t)(r / BM) * groups + g) * 128 + (m % 32) * 4 + (m / 32)];
+    for (int b = 0; b < 4; ++b) hs_out[(size_t)p * (I / 32) + 4 * g + b] = (uint8_t)(w >> (8 * b));
+  }
+}
+
+cudaError_t launch_copy_h(const Shape& sh, const int* hpath, const uint8_t* hq_sorted, const uint8_t* hs_sorted,
+                          const TcWorkspace& w, uint8_t* hq_out, uint8_t* hs_out, cudaStream_t s) {
+  const int n = sh.T * sh.k;
+  if (n == 0) return cudaSuccess;
+  const int blocks = tc_routed_enabled(n) ? max(tc_padded_rows(n, sh.E) / BM, (n + 127) / 128) : (n + 127) / 128;
+  k_copy_h<<<blocks, 128, 0, s>>>(n, sh.I, hpath, hq_sorted, hs_sorted, reinterpret_cast<const MTile*>(w.mtiles),
+                                  w.num_mt, w.hq_perm, reinterpret_cast<const uint32_t*>(w.hs_mma), hq_out, hs_out);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ host
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D byte tensor [rows][row_bytes], tiles of 128 rows x 128 bytes, 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int KIND, int EPI, bool GROUPED>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int max_tiles, cudaStream_t s) {
+  const size_t smem = (size_t)STAGES * stage_bytes(KIND) + 1024;
+  const void* fn = (const void*)k_tc_gemm<KIND, EPI, GROUPED>;
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int grid = max(1, min(max_tiles, sm_count()));
+  k_tc_gemm<KIND, EPI, GROUPED><<<grid, TC_THREADS, smem, s>>>(a, b, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const TcWorkspace& w, const uint8_t* xq,
+                                 const uint8_t* xs, const int* offsets, const int* perm, float* y_assign,
+                                 int* status, uint64_t limit_ns, cudaStream_t s) {
+  const int H = sh.H, I = sh.I, E = sh.E;
+  const int n = sh.T * sh.k;
+  if (n == 0) return cudaSuccess;
+  const int rmax = tc_padded_rows(n, E);
+  cudaError_t err;
+  k_build_mtiles<<<1, 256, 0, s>>>(offsets, E, w.poff, reinterpret_cast<MTile*>(w.mtiles), w.num_mt);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  k_gather_mx_rows<<<rmax, 128, 0, s>>>(xq, xs, H, sh.k, perm, reinterpret_cast<const MTile*>(w.mtiles), w.num_mt,
+                                        w.xq_perm, reinterpret_cast<uint32_t*>(w.xs_mma));
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  {
+    const size_t words13 = (size_t)E * 2 * I * (H / 128), words2 = (size_t)E * H * (I / 128);
+    k_relayout_weight_sf<<<(unsigned)((words13 + 255) / 256), 256, 0, s>>>(ex.w13s, E, 2 * I, H,
+                                                                          reinterpret_cast<uint32_t*>(w.w13s_mma));
+    k_relayout_weight_sf<<<(unsigned)((words2 + 255) / 256), 256, 0, s>>>(ex.w2s, E, H, I,
+                                                                         reinterpret_cast<uint32_t*>(w.w2s_mma));
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  const int max_mt = rmax / BM;
+  CUtensorMap ma, mb;
+  // gate/up: A = gathered activations [rmax][H/2], B = W13 [E*2I][H/2]
+  if ((err = make_map(&ma, w.xq_perm, rmax, H / 2)) != cudaSuccess) return err;
+  if ((err = make_map(&mb, ex.w13, (uint64_t)E * 2 * I, H / 2)) != cudaSuccess) return err;
+  GemmArgs g1{};
+  g1.K = H;
+  g1.n_tiles = I / 128;
+  g1.num_mt = w.num_mt;
+  g1.mt = reinterpret_cast<const MTile*>(w.mtiles);
+  g1.b_rows_per_expert = 2 * I;
+  g1.b_up_off = I;
+  g1.sfa = w.xs_mma;
+  g1.sfb = w.w13s_mma;
+  g1.sfb_rtiles = 2 * I / 128;
+  g1.hq = w.hq_perm;
+  g1.hs = reinterpret_cast<uint32_t*>(w.hs_mma);
+  g1.h_cols = I;
+  g1.status = status;
+  g1.limit_ns = limit_ns;
+  if ((err = launch_gemm<KIND_FP4, EPI_SWIGLU_MX, true>(ma, mb, g1, max_mt * g1.n_tiles, s)) != cudaSuccess) return err;
+  // down: A = requantised h [rmax][I/2], B = W2 [E*H][I/2]
+  if ((err = make_map(&ma, w.hq_perm, rmax, I / 2)) != cudaSuccess) return err;
+  if ((err = make_map(&mb, ex.w2, (uint64_t)E * H, I / 2)) != cudaSuccess) return err;
+  GemmArgs g2{};
+  g2.K = I;
+  g2.n_tiles = H / BN;
+  g2.num_mt = w.num_mt;
+  g2.mt = reinterpret_cast<const MTile*>(w.mtiles);
+  g2.b_rows_per_expert = H;
+  g2.sfa = w.hs_mma;
+  g2.sfb = w.w2s_mma;
+  g2.sfb_rtiles = H / 128;
+  g2.out = y_assign;
+  g2.ldo = H;
+  g2.status = status;
+  g2.limit_ns = limit_ns;
+  return launch_gemm<KIND_FP4, EPI_STORE_F32, true>(ma, mb, g2, max_mt * g2.n_tiles, s);
+}
+
+cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
+                             float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s) {
+  const int T = sh.T, H = sh.H, I = sh.I;
+  if (T == 0) return cudaSuccess;
+  const int mt = (T + BM - 1) / BM;
+  CUtensorMap ma, mb;
+  cudaError_t err;
+  if ((err = make_map(&ma, x, T, (uint64_t)H * 2)) != cudaSuccess) return err;
+  if ((err = make_map(&mb, shd.w13, (uint64_t)2 * I, (uint64_t)H * 2)) != cudaSuccess) return err;
+  GemmArgs g1{};
+  g1.K = H;
+  g1.n_tiles = I / 128;
+  g1.num_mt_dense = mt;
+  g1.rows_dense = T;
+  g1.b_up_off = I;
+  g1.h_bf16 = h_shared;
+  g1.h_cols = I;
+  g1.status = status;
+  g1.limit_ns = limit_ns;
+  if ((err = launch_gemm<KIND_BF16, EPI_SWIGLU_BF16, false>(ma, mb, g1, mt * g1.n_tiles, s)) != cudaSuccess) return err;
+  if ((err = make_map(&ma, h_shared, T, (uint64_t)I * 2)) != cudaSuccess) return err;
+  if ((err = make_map(&mb, shd.w2, H, (uint64_t)I * 2)) != cudaSuccess) return err;
+  GemmArgs g2{};
+  g2.K = I;
+  g2.n_tiles = H / BN;
+  g2.num_mt_dense = mt;
+  g2.rows_dense = T;
+  g2.out = y_shared;
+  g2.ldo = H;
+  g2.status = status;
+  g2.limit_ns = limit_ns;
+  return launch_gemm<KIND_BF16, EPI_STORE_F32, false>(ma, mb, g2, mt * g2.n_tiles, s);
+}
+
+}  // namespace moefp4

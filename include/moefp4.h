@@ -237,6 +237,14 @@ MOE_API moe_status_t moe_layer_decode_noalloc(const moe_layer_desc_t* desc, cons
  * finishing its work; the workspace must then be zero-filled again. */
 MOE_API void moe_set_wait_limit_ns(uint64_t ns);
 
+/* Test hook: copies the MXFP4-requantised intermediate h of the last
+ * moe_expert_ffn_fp4 / moe_layer_forward call made with this workspace (A6)
+ * into caller buffers in sorted-assignment order: codes [T*top_k, I/2] and
+ * E8M0 scales [T*top_k, I/32].  Enqueued on the stream; needs nothing but the
+ * workspace of that call. */
+MOE_API moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes,
+                                             uint8_t* hq, uint8_t* hs, moe_stream_t stream);
+
 /* Test hook for the failure path: launches one bounded wait on a workspace
  * counter that nothing ever advances, with the given limit.  Afterwards
  * moe_get_status reports MOE_ERR_TIMEOUT; the GPU context stays usable. */

@@ -220,8 +220,55 @@ def _compare_layer(wl, lay, cache, out, ids, tokens=None, tol=LAYER_TOL):
 
 # ------------------------------------------------------ A5 - A8 expert FFNs
 
+_E2M1_THRESHOLDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
 
-@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16"])
+
+def _oracle_h_sorted(ref, inv, T, k, I):
+    """Oracle's h (float32 values), requantised codes and scales, in sorted order."""
+    n = T * k
+    h = np.zeros((n, I))
+    hq = np.zeros((n, I), np.uint8)
+    hs = np.zeros((n, I // 32), np.uint8)
+    for e, r in ref["experts"].items():
+        p = inv[r["rows"] * k + r["slots"]]
+        h[p], hq[p], hs[p] = r["h"], r["hq"], r["hs"]
+    return h, hq, hs
+
+
+def _check_requant_and_down(dev, d, ref, inv, y_assign, T, k, I, H):
+    """A6 + A7 on identically quantised inputs.  The GPU's MXFP4 h must equal
+    the oracle's block for block, except blocks where the oracle's h lies
+    within 1e-5 (relative) of a rounding threshold or of a change of the
+    block exponent (G and U are FP32 sums whose order differs).  Rows whose h
+    is identical feed the down projection identical inputs: there y must agree
+    within the contraction tolerance."""
+    n = T * k
+    ghq = torch.empty((n, I // 2), dtype=torch.uint8, device="cuda")
+    ghs = torch.empty((n, I // 32), dtype=torch.uint8, device="cuda")
+    M.moe_debug_requantized_h(d, dev.ws, ghq, ghs)
+    torch.cuda.synchronize()
+    gq = F.unpack_e2m1(ghq.cpu().numpy()).reshape(n, I // 32, 32)
+    gs = ghs.cpu().numpy()
+    h, oq, os_ = _oracle_h_sorted(ref, inv, T, k, I)
+    oq = oq.reshape(n, I // 32, 32)
+    same = np.all(gq == oq, axis=2) & (gs == os_)
+    hb = h.reshape(n, I // 32, 32)
+    amax = np.abs(hb).max(2)
+    X = F.E8M0_TABLE[os_]
+    near_scale = np.abs(amax / 2.0 ** np.floor(np.log2(np.maximum(amax, 1e-300))) - 1) < 1e-5
+    sv = np.abs(hb) / X[..., None]
+    near_code = np.any(np.min(np.abs(sv[..., None] / _E2M1_THRESHOLDS - 1), axis=-1) < 1e-5, axis=2)
+    assert np.all(same | near_scale | near_code), "requantised h differs away from a rounding boundary"
+    assert same.mean() >= 0.999, same.mean()
+    rows = np.all(same, axis=1)
+    y_ref = ref["y"].reshape(n, H)[np.argsort(inv)]
+    ya = y_assign.cpu().numpy()
+    assert rows.mean() >= 0.9
+    assert normwise(ya[rows], y_ref[rows]) <= CONTRACTION_TOL
+    assert normwise(ya, y_ref) <= LAYER_TOL
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "batch128"])
 def test_expert_ffn_contractions(name):
     """Routed expert outputs y (per sorted assignment) and the shared expert
     output ys against the oracle, on the same MXFP4 activations (the GPU's own
@@ -244,7 +291,9 @@ def test_expert_ffn_contractions(name):
     M.moe_expert_ffn_fp4(d, dev.ex, dev.sh, xt, xq, xs, g_off, g_perm, y_assign, y_shared, dev.ws)
     torch.cuda.synchronize()
     y_ref = ref["y"].reshape(T * k, H)[perm]  # oracle y in sorted-assignment order
-    assert normwise(y_assign.cpu().numpy(), y_ref) <= CONTRACTION_TOL
+    if T * k >= 256:  # the tensor-core path: check that its tiles cover every row
+        assert np.all(np.abs(y_assign.cpu().numpy()).max(1) > 0)
+    _check_requant_and_down(dev, d, ref, inv, y_assign, T, k, I, H)
     assert normwise(y_shared.cpu().numpy(), ref["ys"]) <= CONTRACTION_TOL
     # combine alone on the oracle's expert outputs: out = BF16(ys + sum w y)
     out = torch.empty((T, H), dtype=torch.int16, device="cuda")
@@ -323,6 +372,42 @@ def test_prefill8k_forward_sampled():
     rng = np.random.default_rng(14)
     tokens = np.sort(np.concatenate([rng.choice(wl.T - 1, 15, replace=False), [0, wl.T - 1]]))
     _compare_layer(wl, lay, cache, out, ids, tokens=tokens)
+
+
+# ---------------------------------------------------- tensor-core path shapes
+
+
+@pytest.mark.parametrize("shape", [(64, 256, 256, 8, 4), (160, 512, 256, 16, 4), (130, 256, 512, 4, 2),
+                                   (300, 512, 512, 32, 8)])
+def test_tensor_core_path_shapes(shape):
+    """From 256 assignments the MXFP4 experts run on tcgen05 tensor cores
+    (and the shared expert from 128 tokens): ragged per-expert tiles, several
+    K stages, both entry points."""
+    T, H, I, E, k = shape
+    wl = W.Workload("tc", T, H, I, E, k, W.MXFP4, 23, 0.05)
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, H, I, E, k, wl.fmt, T_max=T)
+    cache = {}
+    out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, cache, out, ids)
+    ref = O.layer_forward(lay, k, wl.fmt, cache=cache, keep=True)
+    counts, offsets, perm, inv = O.permute(ref["ids"], E)
+    d = dev.desc(T)
+    xt = bf16_tensor(lay["x"])
+    xq = torch.empty((T, H // 2), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((T, H // 32), dtype=torch.uint8, device="cuda")
+    M.moe_quant_act_mxfp4(T, H, xt, xq, xs)
+    y_assign = torch.full((T * k, H), float("nan"), dtype=torch.float32, device="cuda")
+    y_shared = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    M.moe_expert_ffn_fp4(d, dev.ex, dev.sh, xt, xq, xs, torch.from_numpy(offsets).cuda(),
+                         torch.from_numpy(perm).cuda(), y_assign, y_shared, dev.ws)
+    torch.cuda.synchronize()
+    ya = y_assign.cpu().numpy()
+    assert np.all(np.isfinite(ya)) and np.all(np.isfinite(y_shared.cpu().numpy()))
+    _check_requant_and_down(dev, d, ref, inv, y_assign, T, k, I, H)
+    assert normwise(y_shared.cpu().numpy(), ref["ys"]) <= CONTRACTION_TOL
 
 
 # --------------------------------------------------------------- edge cases
