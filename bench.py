@@ -330,7 +330,8 @@ def run_ours(args):
                    "graph": "%d replays of a %d-step CUDA graph" % (R, S), "parallelism": "replicas"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "k_fused_decode" if fused else "unfused sequence",
+                     "kernel": ("k_decode_tc" if layers[0].prepared and wl.H % 256 == 0 and wl.I % 256 == 0
+                                else "k_fused_decode") if fused else "unfused sequence",
                      "kernel_us": float(durs.mean() * 1e6),
                      "bytes_per_step": float(byts.mean()), "distinct_experts_per_step": float(distinct.mean())},
         "e2e": {"value": T * n_e2e / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * wl.H * 2,

@@ -28,7 +28,7 @@ EXPORTED = [
     "moe_status_string", "moe_workspace_size", "moe_get_status", "moe_router_topk",
     "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
-    "moe_layer_decode_noalloc", "moe_debug_requantized_h",
+    "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -51,6 +51,8 @@ class Experts(ctypes.Structure):
         ("w2", ctypes.c_void_p),
         ("w2_scale", ctypes.c_void_p),
         ("tensor_scale", ctypes.c_void_p),
+        ("w13_scale_mma", ctypes.c_void_p),
+        ("w2_scale_mma", ctypes.c_void_p),
     ]
 
 
@@ -87,6 +89,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_debug_wait_probe": ([P, S, U64, P], ctypes.c_int),
         "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
+        "moe_prepare_weights": ([P, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -133,8 +136,9 @@ def desc(T, H, I, E, top_k) -> LayerDesc:
     return LayerDesc(T, H, I, E, top_k, 1, 1)
 
 
-def experts(fmt, w13, w13_scale, w2, w2_scale, tensor_scale=None) -> Experts:
-    return Experts(fmt, _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(tensor_scale))
+def experts(fmt, w13, w13_scale, w2, w2_scale, tensor_scale=None, w13_scale_mma=None, w2_scale_mma=None) -> Experts:
+    return Experts(fmt, _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(tensor_scale), _p(w13_scale_mma),
+                   _p(w2_scale_mma))
 
 
 def shared_bf16(w13=None, w2=None) -> SharedBF16:
@@ -167,6 +171,11 @@ def moe_set_wait_limit_ns(ns: int) -> None:
 def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
     _check(load().moe_debug_wait_probe(_p(ws), _nbytes(ws), int(limit_ns), _stream(stream)),
            "moe_debug_wait_probe")
+
+
+def moe_prepare_weights(d, ex, w13_scale_mma, w2_scale_mma, stream=None):
+    _check(load().moe_prepare_weights(ctypes.byref(d), ctypes.byref(ex), _p(w13_scale_mma), _p(w2_scale_mma),
+                                      _stream(stream)), "moe_prepare_weights")
 
 
 def moe_debug_requantized_h(d, ws, hq, hs, stream=None):

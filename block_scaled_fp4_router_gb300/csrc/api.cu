@@ -45,7 +45,11 @@ moe_status_t check_experts(const moe_layer_desc_t* d, const moe_experts_t* ex, E
   } else if (ex->tensor_scale) {
     return MOE_ERR_INVALID_ARG;
   }
-  *out = ExpertsDev{nv ? 1 : 0, ex->w13, ex->w13_scale, ex->w2, ex->w2_scale, ex->tensor_scale};
+  if ((ex->w13_scale_mma && !aligned(ex->w13_scale_mma, 16)) || (ex->w2_scale_mma && !aligned(ex->w2_scale_mma, 16)))
+    return MOE_ERR_INVALID_ARG;
+  const bool prepared = !nv && ex->w13_scale_mma && ex->w2_scale_mma;
+  *out = ExpertsDev{nv ? 1 : 0, ex->w13, ex->w13_scale, ex->w2, ex->w2_scale, ex->tensor_scale,
+                    prepared ? ex->w13_scale_mma : nullptr, prepared ? ex->w2_scale_mma : nullptr};
   return MOE_OK;
 }
 
@@ -140,6 +144,20 @@ moe_status_t moe_get_status(void* ws, moe_status_t* st) {
   if (v != 0) MOE_CUDA(cudaMemset(word, 0, sizeof(int)));
   *st = static_cast<moe_status_t>(v);
   return MOE_OK;
+}
+
+moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts_t* experts, uint8_t* w13_scale_mma,
+                                 uint8_t* w2_scale_mma, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  ExpertsDev ex;
+  MOE_TRY(check_experts(desc, experts, &ex));
+  if (ex.nv) return MOE_ERR_UNSUPPORTED;
+  if (!w13_scale_mma || !w2_scale_mma || !aligned(w13_scale_mma, 16) || !aligned(w2_scale_mma, 16) ||
+      !aligned(ex.w13s, 4) || !aligned(ex.w2s, 4))
+    return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_relayout_weight_sf(ex.w13s, desc->E, 2 * desc->I, desc->H, w13_scale_mma, s));
+  return cuda_status(launch_relayout_weight_sf(ex.w2s, desc->E, desc->H, desc->I, w2_scale_mma, s));
 }
 
 moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes, uint8_t* hq,
@@ -278,9 +296,11 @@ moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t*
   if (desc->T == 0) return MOE_OK;
   if (!x || !out || !w_router || !aligned(x, 16) || !aligned(out, 16) || !aligned(w_router, 16))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_fused_decode(shape_of(desc), ex, shd, w_router, bias, static_cast<const uint16_t*>(x),
-                                         static_cast<uint16_t*>(out), topk_ids, topk_w, ws,
-                                         g_wait_limit_ns.load(), reinterpret_cast<cudaStream_t>(stream)));
+  const Shape sh = shape_of(desc);
+  // Prepared MXFP4 scales (moe_prepare_weights) select the tensor-core launch.
+  auto launch = fused_decode_tc_supported(sh, ex) ? launch_fused_decode_tc : launch_fused_decode;
+  return cuda_status(launch(sh, ex, shd, w_router, bias, static_cast<const uint16_t*>(x), static_cast<uint16_t*>(out),
+                            topk_ids, topk_w, ws, g_wait_limit_ns.load(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,0 +1,885 @@
+// A10 on tensor cores: the whole MoE layer for decode steps of 1-16 tokens in
+// one launch, every contraction on tcgen05 (AMD technical article
+// "MiniMax-M3.1 on AMD Instinct GPUs", section "What we Optimized": the "mono
+// decode" path runs a pure decode step of at most 16 tokens as one fused MoE
+// launch).
+//
+// A decode step streams every touched weight byte once, so the layer is
+// bound by HBM.  The weights are the MMA's A operand (128 weight rows per
+// MMA, moved by TMA through a 5-stage shared-memory ring) and the 1-16 token
+// rows are a 16-row B operand, so one block keeps ~200 KB of weights in
+// flight without spending CUDA-core issue slots on FP4 decoding.
+//
+// Work units (one block per SM, cooperative launch, the same static
+// round-robin list in every block):
+//   SGU  shared gate/up:  128 gate + 128 up rows x a K part (BF16, kind::f16)
+//   RGU  routed gate/up:  expert slot x 128 gate + 128 up rows x a K part (MXFP4)
+//   SDN  shared down:     128 rows of H x a K part (BF16)
+//   RDN  routed down:     128 rows of H x one expert slot (MXFP4, whole K)
+// Split-K parts write FP32 partial sums; the block that delivers the last
+// part of a tile (an atomic ticket) sums the parts in a fixed order and runs
+// the tile's epilogue: SwiGLU to BF16 h (shared), SwiGLU + MXFP4 requantise
+// (routed), or the weighted combine out = BF16(ys + sum_j w_j y_j) (down).
+// Results are therefore bit-reproducible run to run.
+//
+// Warp roles: warp 0 issues TMA, warp 1 issues tcgen05.cp / tcgen05.mma,
+// warps 2-5 are the epilogue (one TMEM lane = one weight row each).  Before
+// their first unit the epilogue warps compute this block's router rows and
+// its slice of the MXFP4 quantisation of x; once every block has done so they
+// build the routing (top-k, sort by expert) in shared memory and release the
+// producer and MMA warps onto the routed units.  While the routing is not yet
+// known the producers pull the shared down-projection weights into L2, and
+// once it is known the routed down-projection weights, so that HBM keeps
+// streaming across the dependencies between the steps.
+//
+// Every wait is bounded (MOE_DEV_TIMEOUT in the status word); the last block
+// out resets the counters, and each finishing block resets its ticket.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "routing.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.h"
+
+namespace moefp4 {
+namespace {
+
+constexpr int DT = 192;                 // threads: TMA warp, MMA warp, 4 epilogue warps
+constexpr int EPI_THREADS = 128;
+constexpr int DSTAGES = 5;
+// byte offsets inside one stage (swizzled tiles on 1024-byte boundaries)
+constexpr uint32_t ST_A0 = 0, ST_A1 = 16384;       // 128 rows x 128 B each
+constexpr uint32_t ST_B0 = 32768, ST_B1 = 34816;   // 16 rows x 128 B each
+constexpr uint32_t ST_SFA = 36864;                 // A0 scales (2 x 512 B), A1 scales (2 x 512 B)
+constexpr uint32_t ST_SFB = 38912;                 // B0 scales, B1 scales
+constexpr uint32_t STAGE_BYTES = 40960;
+constexpr uint32_t A_TILE = 16384, B_TILE = 2048;
+constexpr uint32_t DC_TMEM_COLS = 256;
+constexpr uint32_t TM_SF = 64;          // scale columns of stage s: TM_SF + 32 s (+0 A0, +8 A1, +16 B0, +24 B1)
+constexpr int MAXN = MAX_DECODE_T * MAX_TOPK;
+
+enum UnitKind { U_SGU = 0, U_RGU = 1, U_SDN = 2, U_RDN = 3 };
+
+struct DcArgs {
+  int T, H, I, E, k;
+  int G;                     // blocks in the launch
+  int s_sgu, s_rgu, s_sdn;   // split-K parts
+  int n_sgu, n_sdn;          // unit counts that do not depend on the routing
+  int nslot_max;             // min(T k, E): ticket slots
+  int shared;
+  const uint8_t* w13s_mma;   // prepared routed weight scales
+  const uint8_t* w2s_mma;
+  const float* wr;
+  const float* bias;
+  const uint16_t* x;
+  uint16_t* out;
+  int* ids_out;
+  float* w_out;
+  int* ctr;
+  int* tickets;
+  float* logits;             // [T, E]
+  uint8_t* xq;               // [T, H/2]
+  uint8_t* xs_mma;           // [H/128][512]
+  uint8_t* hq;               // [T k, I/2] sorted-assignment rows
+  uint8_t* hs_mma;           // [slots][I/128][512]
+  uint16_t* h_shared;        // [T, I]
+  float* gu_sh;              // [s_sgu][T][2I]
+  float* gu_r;               // [s_rgu][T k][2I]
+  float* ys;                 // [s_sdn][T][H]
+  float* y_assign;           // [T k][H]
+  uint64_t limit_ns;
+};
+
+struct DcMaps {
+  CUtensorMap w13r, w2r, w13s, w2s;  // weights: boxes of 128 rows x 128 B
+  CUtensorMap xq, x, hsh, hq;        // activations: boxes of 16 rows x 128 B
+};
+
+// Routing of the step, built by the epilogue warps of every block.
+struct DcRouting {
+  int ids[MAXN];
+  float w[MAXN];
+  int inv[MAXN];          // assignment t*k+j -> sorted position
+  int tok[MAXN];          // sorted position -> token
+  int slot_e[MAXN];       // slot -> expert (distinct experts, ascending)
+  int slot_beg[MAXN + 1]; // slot -> first sorted position
+  int cnt[MAX_E];
+  int eoff[MAX_E];
+  int eslot[MAX_E];
+  int n_slots;
+};
+
+struct Unit {
+  int kind;
+  int tile;   // 128-row tile: of I (gate/up) or of H (down)
+  int part;   // split-K part
+  int slot;   // routed units
+  int st0, st1;
+};
+
+__device__ __forceinline__ int units_total(const DcArgs& a, int n_slots) {
+  return a.n_sgu + n_slots * (a.I / 128) * a.s_rgu + a.n_sdn + n_slots * (a.H / 128);
+}
+
+// Part p of `stages` stages split into s near-equal parts.
+__device__ __forceinline__ void part_range(int stages, int s, int p, int& st0, int& st1) {
+  st0 = p * stages / s;
+  st1 = (p + 1) * stages / s;
+}
+
+// v-th shared down unit: 128-row tile of H, K part over stages of two chunks.
+__device__ __forceinline__ Unit sdn_unit(const DcArgs& a, int v) {
+  Unit U{};
+  U.kind = U_SDN;
+  U.tile = v / a.s_sdn;
+  U.part = v % a.s_sdn;
+  part_range((a.I / 64 + 1) / 2, a.s_sdn, U.part, U.st0, U.st1);
+  return U;
+}
+
+// v-th routed down unit: 128-row tile of H x expert slot, whole K.
+__device__ __forceinline__ Unit rdn_unit(const DcArgs& a, int n_slots, int v) {
+  Unit U{};
+  U.kind = U_RDN;
+  U.tile = v / n_slots;
+  U.slot = v % n_slots;
+  U.st0 = 0;
+  U.st1 = (a.I / 256 + 1) / 2;
+  return U;
+}
+
+__device__ Unit unit_at(const DcArgs& a, int n_slots, int u) {
+  Unit U{};
+  const int nbI = a.I / 128;
+  if (u < a.n_sgu) {
+    U.kind = U_SGU;
+    U.tile = u / a.s_sgu;
+    U.part = u % a.s_sgu;
+    part_range(a.H / 64, a.s_sgu, U.part, U.st0, U.st1);
+    return U;
+  }
+  u -= a.n_sgu;
+  const int n_rgu = n_slots * nbI * a.s_rgu;
+  if (u < n_rgu) {
+    U.kind = U_RGU;
+    U.slot = u / (nbI * a.s_rgu);
+    U.tile = (u / a.s_rgu) % nbI;
+    U.part = u % a.s_rgu;
+    part_range(a.H / 256, a.s_rgu, U.part, U.st0, U.st1);
+    return U;
+  }
+  u -= n_rgu;
+  if (u < a.n_sdn) return sdn_unit(a, u);
+  return rdn_unit(a, n_slots, u - a.n_sdn);
+}
+
+__device__ __forceinline__ void epi_sync() { tc::named_sync(1, EPI_THREADS); }
+
+// sum over p < S of src[p * stride], in ascending p, every load issued first.
+__device__ __forceinline__ float sum_parts(const float* src, size_t stride, int S) {
+  float v[DC_MAX_SPLIT];
+#pragma unroll
+  for (int p = 0; p < DC_MAX_SPLIT; ++p) v[p] = p < S ? __ldcg(src + p * stride) : 0.0f;
+  float s = 0.0f;
+#pragma unroll
+  for (int p = 0; p < DC_MAX_SPLIT; ++p)
+    if (p < S) s += v[p];
+  return s;
+}
+
+// v[base + t] for a runtime t < 16 without indexing registers dynamically.
+__device__ __forceinline__ float pick16(const float (&v)[32], int base, int t) {
+  float r = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r = i == t ? v[base + i] : r;
+  return r;
+}
+
+// ----------------------------------------------------- epilogue-warp prologue
+
+// Router row e for all tokens (FP32 weights and accumulation), 128 threads.
+// Tokens go in groups of 4; within a group every load of a pass (4 x 8
+// elements per thread) is in flight before the FMAs, since these loads
+// compete with the weight streams for HBM.
+__device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DECODE_T]) {
+  const int T = a.T, H = a.H;
+  const int w = et >> 5, lane = et & 31;
+  constexpr int PASS = EPI_THREADS * 8;
+  const float* wrow = a.wr + (size_t)e * H;
+  for (int t0 = 0; t0 < T; t0 += 4) {
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int k0 = et * 8; k0 < H; k0 += 4 * PASS) {
+      uint4 wv[8];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int kk = k0 + c * PASS;
+        wv[2 * c] = kk < H ? __ldg(reinterpret_cast<const uint4*>(wrow + kk)) : make_uint4(0, 0, 0, 0);
+        wv[2 * c + 1] = kk < H ? __ldg(reinterpret_cast<const uint4*>(wrow + kk + 4)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) {
+        if (t0 + tt < T) {
+          const uint16_t* xr = a.x + (size_t)(t0 + tt) * H;
+          uint4 xv[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int kk = k0 + c * PASS;
+            xv[c] = kk < H ? __ldg(reinterpret_cast<const uint4*>(xr + kk)) : make_uint4(0, 0, 0, 0);
+          }
+          float s = acc[tt];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 q = xv[c], wa = wv[2 * c], wb = wv[2 * c + 1];
+            s = fmaf(bf16_lo(q.x), __uint_as_float(wa.x), s);
+            s = fmaf(bf16_hi(q.x), __uint_as_float(wa.y), s);
+            s = fmaf(bf16_lo(q.y), __uint_as_float(wa.z), s);
+            s = fmaf(bf16_hi(q.y), __uint_as_float(wa.w), s);
+            s = fmaf(bf16_lo(q.z), __uint_as_float(wb.x), s);
+            s = fmaf(bf16_hi(q.z), __uint_as_float(wb.y), s);
+            s = fmaf(bf16_lo(q.w), __uint_as_float(wb.z), s);
+            s = fmaf(bf16_hi(q.w), __uint_as_float(wb.w), s);
+          }
+          acc[tt] = s;
+        }
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt) {
+      const float v = warp_sum(acc[tt]);
+      if (lane == 0 && t0 + tt < T) red_s[w][t0 + tt] = v;
+    }
+  }
+  epi_sync();
+  if (et < T) {
+    float s = red_s[0][et];
+    for (int ww = 1; ww < EPI_THREADS / 32; ++ww) s += red_s[ww][et];
+    if (a.bias) s += a.bias[e];
+    a.logits[(size_t)et * a.E + e] = s;
+  }
+  epi_sync();
+}
+
+// MXFP4 quantisation of one 32-element block i = (token row t < 16, block b
+// of H/32): 16 code bytes of xq and byte b % 4 of the MMA-layout scale word
+// of row t in group b / 4 (word 4t of that group's 512-byte block).  Rows
+// t >= T get a zero scale byte.  Same arithmetic as the standalone quantiser.
+__device__ void quant_block(const DcArgs& a, int i) {
+  const int nb = a.H / 32;
+  const int t = i / nb, b = i % nb;
+  uint8_t sb = 0;
+  if (t < a.T) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + b * 32);
+    uint4 raw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) raw[j] = __ldg(src + j);
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+    }
+    const int ex = mx_scale_exp(amax);
+    const float inv = pow2_neg(ex);
+    uint32_t c[4];
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+      uint32_t word = 0;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        word |= e2m1_rne(bf16_lo(w4[h]) * inv) << (8 * h);
+        word |= e2m1_rne(bf16_hi(w4[h]) * inv) << (8 * h + 4);
+      }
+      c[j] = word;
+    }
+    *reinterpret_cast<uint4*>(a.xq + (size_t)t * (a.H / 2) + b * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+    sb = (uint8_t)(ex + 127);
+  }
+  a.xs_mma[(size_t)(b / 4) * 512 + t * 16 + (b % 4)] = sb;
+}
+
+// Top-k of every token (one epilogue warp per token), then the stable
+// counting sort of the T*k assignments by expert and the distinct-expert
+// slots.  128 epilogue threads, et = 0..127.
+__device__ void build_routing(const DcArgs& a, DcRouting& R, int et) {
+  const int T = a.T, E = a.E, k = a.k, n = T * k;
+  const int w = et >> 5, lane = et & 31;
+  for (int e = et; e < E; e += EPI_THREADS) R.cnt[e] = 0;
+  for (int t = w; t < T; t += EPI_THREADS / 32) {
+    float v[8];
+    load_logit_row(a.logits + (size_t)t * E, E, v, true);
+    int sel[MAX_TOPK];
+    float vals[MAX_TOPK], wt[MAX_TOPK];
+    warp_topk(v, E, k, sel, vals);
+    topk_weights(vals, k, wt);
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j == lane && j < k) {
+        R.ids[t * k + j] = sel[j];
+        R.w[t * k + j] = wt[j];
+      }
+  }
+  epi_sync();
+  int e = -1, rank = 0;
+  if (et < n) {
+    e = R.ids[et];
+    for (int b = 0; b < et; ++b) rank += R.ids[b] == e;
+    atomicAdd(&R.cnt[e], 1);
+  }
+  epi_sync();
+  if (w == 0) {
+    int run_c = 0, run_p = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int ex = base + lane;
+      const int c = ex < E ? R.cnt[ex] : 0;
+      int ic = c, ip = c > 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yc = __shfl_up_sync(FULL, ic, o), yp = __shfl_up_sync(FULL, ip, o);
+        if (lane >= o) {
+          ic += yc;
+          ip += yp;
+        }
+      }
+      if (ex < E) {
+        R.eoff[ex] = run_c + ic - c;
+        R.eslot[ex] = run_p + ip - (c > 0);
+      }
+      run_c += __shfl_sync(FULL, ic, 31);
+      run_p += __shfl_sync(FULL, ip, 31);
+    }
+    if (lane == 0) {
+      R.n_slots = run_p;
+      R.slot_beg[run_p] = n;
+    }
+  }
+  epi_sync();
+  if (et < n) {
+    R.inv[et] = R.eoff[e] + rank;
+    R.tok[R.eoff[e] + rank] = et / k;
+  }
+  for (int ex = et; ex < E; ex += EPI_THREADS) {
+    if (R.cnt[ex] > 0) {
+      R.slot_e[R.eslot[ex]] = ex;
+      R.slot_beg[R.eslot[ex]] = R.eoff[ex];
+    }
+  }
+  epi_sync();
+}
+
+// L2 prefetch of the weight boxes (A operand) of a down unit.
+__device__ void prefetch_down_unit(const DcArgs& a, const DcMaps& m, const Unit& U, int e) {
+  if (U.kind == U_SDN) {
+    for (int st = U.st0; st < U.st1; ++st)
+      for (int h = 0; h < 2 && 2 * st + h < a.I / 64; ++h)
+        tc::tma_prefetch_2d(&m.w2s, (2 * st + h) * 128, 128 * U.tile);
+  } else {
+    for (int st = U.st0; st < U.st1; ++st)
+      for (int h = 0; h < 2 && 2 * st + h < a.I / 256; ++h)
+        tc::tma_prefetch_2d(&m.w2r, (2 * st + h) * 128, e * a.H + 128 * U.tile);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcMaps maps, const DcArgs a) {
+  extern __shared__ __align__(1024) uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[DSTAGES], empty[DSTAGES], acc_full[2], acc_empty[2], drain, routing_ready;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag, s_ok, s_last;
+  __shared__ DcRouting R;
+  __shared__ float red_s[EPI_THREADS / 32][MAX_DECODE_T];
+  __shared__ __align__(4) uint8_t s_hsb[MAX_DECODE_T * 4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nbI = a.I / 128, nbH = a.H / 128;
+  int* status = a.ctr + C_STATUS;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < DSTAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&acc_full[b], 1);
+      tc::mbar_init(&acc_empty[b], EPI_THREADS);
+    }
+    tc::mbar_init(&drain, 1);
+    tc::mbar_init(&routing_ready, 1);
+    tc::mbar_fence_init();
+    abort_flag = 0;
+  }
+  if (warp == 1) tc::tmem_alloc(&tmem_base, DC_TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  auto fail = [&]() {
+    atomicCAS(status, 0, (int)MOE_DEV_TIMEOUT);
+    atomicExch(&abort_flag, 1);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      const int never = 0;
+      uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
+      int n_slots = -1;
+      bool hsh_ok = false, hr_ok = false;
+      tc::prefetch_tensormap(&maps.w13r);
+      tc::prefetch_tensormap(&maps.w2r);
+      tc::prefetch_tensormap(&maps.xq);
+      tc::prefetch_tensormap(&maps.hq);
+      if (a.shared) {
+        tc::prefetch_tensormap(&maps.w13s);
+        tc::prefetch_tensormap(&maps.w2s);
+        tc::prefetch_tensormap(&maps.x);
+        tc::prefetch_tensormap(&maps.hsh);
+      }
+      for (int u = blockIdx.x;; u += a.G) {
+        if (u >= a.n_sgu && n_slots < 0) {
+          // Until the routing is known, pull shared down weights into L2
+          // (unit v by block v mod G, whichever block computes it later).
+          for (int v = blockIdx.x; v < a.n_sdn; v += a.G) prefetch_down_unit(a, maps, sdn_unit(a, v), 0);
+          if (!tc::mbar_wait(&routing_ready, 0, a.limit_ns, &abort_flag)) { fail(); break; }
+          n_slots = R.n_slots;
+          tc::fence_proxy_async_global();  // x was quantised by plain stores of other blocks
+          // The routed down weights are known now: into L2 while the gate/up streams run.
+          const int n_rdn = n_slots * nbH;
+          for (int v = blockIdx.x; v < n_rdn; v += a.G) {
+            const Unit D = rdn_unit(a, n_slots, v);
+            prefetch_down_unit(a, maps, D, R.slot_e[D.slot]);
+          }
+        }
+        if (u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
+        const Unit U = unit_at(a, n_slots < 0 ? 0 : n_slots, u);
+        int e = 0, beg = 0;
+        if (U.kind == U_RGU || U.kind == U_RDN) {
+          e = R.slot_e[U.slot];
+          beg = R.slot_beg[U.slot];
+        }
+        // The down units read h written by other blocks.
+        if (U.kind == U_SDN && !hsh_ok) {
+          if (!wait_at_least(a.ctr + C_DC_HSH, nbI, status, a.limit_ns)) { fail(); break; }
+          hsh_ok = true;
+          tc::fence_proxy_async_global();
+        }
+        if (U.kind == U_RDN && !hr_ok) {
+          if (!wait_at_least(a.ctr + C_DC_HR, n_slots * nbI, status, a.limit_ns)) { fail(); break; }
+          hr_ok = true;
+          tc::fence_proxy_async_global();
+        }
+        bool ok = true;
+        for (int st = U.st0; st < U.st1; ++st) {
+          if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
+          uint8_t* sp = dsm + stage * STAGE_BYTES;
+          uint64_t* fb = &full[stage];
+          if (U.kind == U_SGU) {
+            const int xc = st * 128;
+            tc::mbar_expect_tx(fb, 2 * A_TILE + B_TILE);
+            tc::tma_load_2d(sp + ST_A0, &maps.w13s, xc, 128 * U.tile, fb);
+            tc::tma_load_2d(sp + ST_A1, &maps.w13s, xc, a.I + 128 * U.tile, fb);
+            tc::tma_load_2d(sp + ST_B0, &maps.x, xc, 0, fb);
+          } else if (U.kind == U_RGU) {
+            const int xc = st * 128;
+            const int row = e * 2 * a.I + 128 * U.tile;
+            const size_t hg = a.H / 128;
+            const size_t rt = (size_t)e * (2 * nbI) + U.tile;  // gate row tile; the up tile is nbI further
+            tc::mbar_expect_tx(fb, 2 * A_TILE + B_TILE + 3 * 1024);
+            tc::tma_load_2d(sp + ST_A0, &maps.w13r, xc, row, fb);
+            tc::tma_load_2d(sp + ST_A1, &maps.w13r, xc, row + a.I, fb);
+            tc::tma_load_2d(sp + ST_B0, &maps.xq, xc, 0, fb);
+            tc::bulk_load(sp + ST_SFA, a.w13s_mma + (rt * hg + 2 * st) * 512, 1024, fb);
+            tc::bulk_load(sp + ST_SFA + 1024, a.w13s_mma + ((rt + nbI) * hg + 2 * st) * 512, 1024, fb);
+            tc::bulk_load(sp + ST_SFB, a.xs_mma + (size_t)2 * st * 512, 1024, fb);
+          } else if (U.kind == U_SDN) {
+            const int halves = 2 * st + 1 < a.I / 64 ? 2 : 1;
+            tc::mbar_expect_tx(fb, halves * (A_TILE + B_TILE));
+            for (int h = 0; h < halves; ++h) {
+              const int xc = (2 * st + h) * 128;
+              tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &maps.w2s, xc, 128 * U.tile, fb);
+              tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &maps.hsh, xc, 0, fb);
+            }
+          } else {
+            const int halves = 2 * st + 1 < a.I / 256 ? 2 : 1;
+            const size_t ig = a.I / 128;
+            tc::mbar_expect_tx(fb, halves * (A_TILE + B_TILE + 2048));
+            for (int h = 0; h < halves; ++h) {
+              const int xc = (2 * st + h) * 128;
+              tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &maps.w2r, xc, e * a.H + 128 * U.tile, fb);
+              tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &maps.hq, xc, beg, fb);
+            }
+            tc::bulk_load(sp + ST_SFA, a.w2s_mma + (((size_t)e * nbH + U.tile) * ig + 4 * st) * 512, halves * 1024, fb);
+            tc::bulk_load(sp + ST_SFB, a.hs_mma + ((size_t)U.slot * ig + 4 * st) * 512, halves * 1024, fb);
+          }
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == DSTAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      // copies still in flight must land before the block's shared memory goes away
+      for (int s = 0; s < DSTAGES; ++s)
+        if ((issued >> s & 1) && !tc::mbar_wait(&full[s], last_parity >> s & 1, a.limit_ns, &never)) fail();
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const int never = 0;
+      const uint32_t id_bf = tc::idesc_bf16(128, 16);
+      uint32_t stage = 0, phase = 0;
+      int n_slots = -1, i = 0;
+      for (int u = blockIdx.x;; u += a.G, ++i) {
+        if (u >= a.n_sgu && n_slots < 0) {
+          if (!tc::mbar_wait(&routing_ready, 0, a.limit_ns, &abort_flag)) { fail(); break; }
+          n_slots = R.n_slots;
+        }
+        if (u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
+        const Unit U = unit_at(a, n_slots < 0 ? 0 : n_slots, u);
+        const int buf = i & 1;
+        const uint32_t use = (uint32_t)(i >> 1);
+        if (!tc::mbar_wait(&acc_empty[buf], (use & 1) ^ 1, a.limit_ns, &abort_flag)) { fail(); break; }
+        tc::fence_after_sync();
+        const uint32_t acc = tmem + 32 * buf;
+        bool ok = true;
+        for (int st = U.st0; st < U.st1; ++st) {
+          if (!tc::mbar_wait(&full[stage], phase, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t sa = tc::smem_u32(dsm + stage * STAGE_BYTES);
+          const uint32_t tsf = tmem + TM_SF + 32 * stage;
+          const bool first = st == U.st0;
+          if (U.kind == U_SGU) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = tc::desc_sw128(sa + ST_B0 + 32 * kk);
+              const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+              tc::mma_bf16(acc, tc::desc_sw128(sa + ST_A0 + 32 * kk), bd, id_bf, accum);
+              tc::mma_bf16(acc + 16, tc::desc_sw128(sa + ST_A1 + 32 * kk), bd, id_bf, accum);
+            }
+          } else if (U.kind == U_RGU) {
+            tc::sf_copy(tsf + 0, tc::desc_sf(sa + ST_SFA));
+            tc::sf_copy(tsf + 4, tc::desc_sf(sa + ST_SFA + 512));
+            tc::sf_copy(tsf + 8, tc::desc_sf(sa + ST_SFA + 1024));
+            tc::sf_copy(tsf + 12, tc::desc_sf(sa + ST_SFA + 1536));
+            tc::sf_copy(tsf + 16, tc::desc_sf(sa + ST_SFB));
+            tc::sf_copy(tsf + 20, tc::desc_sf(sa + ST_SFB + 512));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int grp = kk >> 1, id = (kk & 1) * 2;
+              const uint32_t idesc = tc::idesc_mxf4(128, 16, id, id);
+              const uint64_t bd = tc::desc_sw128(sa + ST_B0 + 32 * kk);
+              const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+              tc::mma_mxf4(acc, tc::desc_sw128(sa + ST_A0 + 32 * kk), bd, idesc, tsf + 4 * grp, tsf + 16 + 4 * grp, accum);
+              tc::mma_mxf4(acc + 16, tc::desc_sw128(sa + ST_A1 + 32 * kk), bd, idesc, tsf + 8 + 4 * grp,
+                           tsf + 16 + 4 * grp, accum);
+            }
+          } else if (U.kind == U_SDN) {
+            const int halves = 2 * st + 1 < a.I / 64 ? 2 : 1;
+            for (int h = 0; h < halves; ++h) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t accum = (first && h == 0 && kk == 0) ? 0u : 1u;
+                tc::mma_bf16(acc, tc::desc_sw128(sa + (h ? ST_A1 : ST_A0) + 32 * kk),
+                             tc::desc_sw128(sa + (h ? ST_B1 : ST_B0) + 32 * kk), id_bf, accum);
+              }
+            }
+          } else {
+            const int halves = 2 * st + 1 < a.I / 256 ? 2 : 1;
+            for (int h = 0; h < halves; ++h) {
+              tc::sf_copy(tsf + 8 * h, tc::desc_sf(sa + ST_SFA + 1024 * h));
+              tc::sf_copy(tsf + 8 * h + 4, tc::desc_sf(sa + ST_SFA + 1024 * h + 512));
+              tc::sf_copy(tsf + 16 + 8 * h, tc::desc_sf(sa + ST_SFB + 1024 * h));
+              tc::sf_copy(tsf + 16 + 8 * h + 4, tc::desc_sf(sa + ST_SFB + 1024 * h + 512));
+            }
+            for (int h = 0; h < halves; ++h) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const int grp = kk >> 1, id = (kk & 1) * 2;
+                const uint32_t accum = (first && h == 0 && kk == 0) ? 0u : 1u;
+                tc::mma_mxf4(acc, tc::desc_sw128(sa + (h ? ST_A1 : ST_A0) + 32 * kk),
+                             tc::desc_sw128(sa + (h ? ST_B1 : ST_B0) + 32 * kk), tc::idesc_mxf4(128, 16, id, id),
+                             tsf + 8 * h + 4 * grp, tsf + 16 + 8 * h + 4 * grp, accum);
+              }
+            }
+          }
+          tc::mma_commit(&empty[stage]);
+          if (++stage == DSTAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&acc_full[buf]);
+      }
+      // every MMA issued must finish before TMEM is released
+      tc::mma_commit(&drain);
+      if (!tc::mbar_wait(&drain, 0, a.limit_ns, &never)) fail();
+    }
+  } else {
+    // -------------------------------------------------- epilogue warps
+    const int et = threadIdx.x - 64;
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may read
+    const int m = q * 32 + lane;            // weight row within the 128-row tile
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    const int T = a.T, H = a.H, I = a.I, k = a.k, n = T * k;
+
+    for (int e = blockIdx.x; e < a.E; e += a.G) router_row(a, e, et, red_s);
+    const int nqb = MAX_DECODE_T * (H / 32);
+    for (int i = blockIdx.x * EPI_THREADS + et; i < nqb; i += a.G * EPI_THREADS) quant_block(a, i);
+    tc::fence_proxy_async_global();
+    __threadfence();
+    epi_sync();
+    if (et == 0) {
+      red_release_add(a.ctr + C_DC_READY, 1);
+      s_ok = wait_at_least(a.ctr + C_DC_READY, a.G, status, a.limit_ns);
+      if (!s_ok) fail();
+    }
+    epi_sync();
+    if (s_ok) {
+      build_routing(a, R, et);
+      if (et == 0) tc::mbar_arrive(&routing_ready);
+      if (blockIdx.x == 0 && et < n) {
+        if (a.ids_out) a.ids_out[et] = R.ids[et];
+        if (a.w_out) a.w_out[et] = R.w[et];
+      }
+      const int n_slots = R.n_slots;
+      const int total = units_total(a, n_slots);
+      const int dn_target = (a.shared ? a.s_sdn : 0) + n_slots;
+      int i = 0;
+      for (int u = blockIdx.x; u < total; u += a.G, ++i) {
+        const Unit U = unit_at(a, n_slots, u);
+        const int buf = i & 1;
+        const uint32_t use = (uint32_t)(i >> 1);
+        if (et == 0) {
+          s_ok = tc::mbar_wait(&acc_full[buf], use & 1, a.limit_ns, &abort_flag);
+          if (!s_ok) fail();
+        }
+        epi_sync();
+        if (!s_ok) break;
+        tc::fence_after_sync();
+        float v[32];
+        tc::tmem_ld32(trow + 32 * buf, v);
+        tc::fence_before_sync();
+        tc::mbar_arrive(&acc_empty[buf]);
+
+        int beg = 0, cnt = 0;
+        if (U.kind == U_RGU || U.kind == U_RDN) {
+          beg = R.slot_beg[U.slot];
+          cnt = R.slot_beg[U.slot + 1] - beg;
+        }
+        int ticket, target;
+        if (U.kind == U_SGU) {
+          float* dst = a.gu_sh + (size_t)U.part * T * 2 * I + 128 * U.tile + m;
+#pragma unroll
+          for (int t = 0; t < MAX_DECODE_T; ++t)
+            if (t < T) {
+              dst[(size_t)t * 2 * I] = v[t];
+              dst[(size_t)t * 2 * I + I] = v[16 + t];
+            }
+          ticket = U.tile;
+          target = a.s_sgu;
+        } else if (U.kind == U_RGU) {
+          // B held every token row: slot row c is the column of its token
+          float* dst = a.gu_r + ((size_t)U.part * n + beg) * 2 * I + 128 * U.tile + m;
+          for (int c = 0; c < cnt; ++c) {
+            const int t = R.tok[beg + c];
+            dst[(size_t)c * 2 * I] = pick16(v, 0, t);
+            dst[(size_t)c * 2 * I + I] = pick16(v, 16, t);
+          }
+          ticket = nbI + U.slot * nbI + U.tile;
+          target = a.s_rgu;
+        } else if (U.kind == U_SDN) {
+          float* dst = a.ys + (size_t)U.part * T * H + 128 * U.tile + m;
+#pragma unroll
+          for (int t = 0; t < MAX_DECODE_T; ++t)
+            if (t < T) dst[(size_t)t * H] = v[t];
+          ticket = nbI * (1 + a.nslot_max) + U.tile;
+          target = dn_target;
+        } else {
+          // B held the slot's sorted rows: column c is sorted position beg + c
+          float* dst = a.y_assign + (size_t)beg * H + 128 * U.tile + m;
+#pragma unroll
+          for (int c = 0; c < MAX_DECODE_T; ++c)
+            if (c < cnt) dst[(size_t)c * H] = v[c];
+          ticket = nbI * (1 + a.nslot_max) + U.tile;
+          target = dn_target;
+        }
+        // split-K arrival: the block that brings the last part finishes the tile
+        __threadfence();
+        epi_sync();
+        if (et == 0) {
+          const int old = atomicAdd(a.tickets + ticket, 1);
+          s_last = old == target - 1;
+          if (s_last) a.tickets[ticket] = 0;
+        }
+        epi_sync();
+        if (!s_last) continue;
+        __threadfence();
+        if (U.kind == U_SGU) {
+          const float* src = a.gu_sh + 128 * U.tile + m;
+          const size_t stride = (size_t)T * 2 * I;
+          for (int t = 0; t < T; ++t) {
+            const float g = sum_parts(src + (size_t)t * 2 * I, stride, a.s_sgu);
+            const float up = sum_parts(src + (size_t)t * 2 * I + I, stride, a.s_sgu);
+            a.h_shared[(size_t)t * I + 128 * U.tile + m] = f32_to_bf16_rn(silu(g) * up);
+          }
+          tc::fence_proxy_async_global();
+          __threadfence();
+          epi_sync();
+          if (et == 0) red_release_add(a.ctr + C_DC_HSH, 1);
+        } else if (U.kind == U_RGU) {
+          // h = SiLU(G) U requantised to MXFP4: warp q holds one 32-column block
+          const float* src = a.gu_r + (size_t)beg * 2 * I + 128 * U.tile + m;
+          const size_t stride = (size_t)n * 2 * I;
+          for (int c = 0; c < cnt; ++c) {
+            const float g = sum_parts(src + (size_t)c * 2 * I, stride, a.s_rgu);
+            const float up = sum_parts(src + (size_t)c * 2 * I + I, stride, a.s_rgu);
+            const float h = silu(g) * up;
+            const int ex = mx_scale_exp(warp_max(fabsf(h)));
+            uint32_t wv = e2m1_rne(h * pow2_neg(ex)) << (4 * (lane & 7));
+            wv |= __shfl_xor_sync(FULL, wv, 1);
+            wv |= __shfl_xor_sync(FULL, wv, 2);
+            wv |= __shfl_xor_sync(FULL, wv, 4);
+            if ((lane & 7) == 0)
+              *reinterpret_cast<uint32_t*>(a.hq + (size_t)(beg + c) * (I / 2) + 64 * U.tile + 16 * q + 4 * (lane >> 3)) = wv;
+            if (lane == 0) s_hsb[c * 4 + q] = (uint8_t)(ex + 127);
+          }
+          epi_sync();
+          // the slot's scale block for this 128-column group: word 4c holds row c
+          const uint32_t word = ((et & 3) == 0 && (et >> 2) < cnt) ? reinterpret_cast<const uint32_t*>(s_hsb)[et >> 2] : 0u;
+          reinterpret_cast<uint32_t*>(a.hs_mma)[((size_t)U.slot * nbI + U.tile) * 128 + et] = word;
+          tc::fence_proxy_async_global();
+          __threadfence();
+          epi_sync();
+          if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
+        } else {
+          // out = BF16(ys + sum_j w_j y_j), summed in a fixed order
+          const int col = 128 * U.tile + m;
+          for (int t = 0; t < T; ++t) {
+            float y[MAX_TOPK];
+#pragma unroll
+            for (int j = 0; j < MAX_TOPK; ++j)
+              y[j] = j < k ? __ldcg(a.y_assign + (size_t)R.inv[t * k + j] * H + col) : 0.0f;
+            float acc = a.shared ? sum_parts(a.ys + (size_t)t * H + col, (size_t)T * H, a.s_sdn) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < MAX_TOPK; ++j)
+              if (j < k) acc = fmaf(R.w[t * k + j], y[j], acc);
+            a.out[(size_t)t * H + col] = f32_to_bf16_rn(acc);
+          }
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, DC_TMEM_COLS);
+  }
+  // The last block out resets the launch's counters for the next call.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.ctr + C_DC_EXIT, 1) == a.G - 1) {
+      a.ctr[C_DC_READY] = 0;
+      a.ctr[C_DC_HSH] = 0;
+      a.ctr[C_DC_HR] = 0;
+      a.ctr[C_DC_EXIT] = 0;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex) {
+  return !ex.nv && ex.w13s_mma && ex.w2s_mma && sh.T >= 1 && sh.T <= MAX_DECODE_T && sh.H % 256 == 0 &&
+         sh.I % 256 == 0;
+}
+
+cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
+                                   const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
+                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s) {
+  if (sh.T == 0) return cudaSuccess;
+  if (!fused_decode_tc_supported(sh, ex)) return cudaErrorInvalidValue;
+  const int T = sh.T, H = sh.H, I = sh.I, E = sh.E, k = sh.k, n = T * k;
+  const WsLayout L = ws_layout(T, H, I, E, k);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const size_t smem = (size_t)DSTAGES * STAGE_BYTES + 1024;
+  cudaError_t err = cudaFuncSetAttribute((const void*)k_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0;
+  if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_tc, DT, smem)) != cudaSuccess) return err;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // one block per SM: every block holds a 200 KB stage ring and a TMEM allocation
+  const int G = imin(sm_count(), DC_MAX_GRID);
+  const bool shared = shd.w13 != nullptr;
+  const DcSplits sp = dc_splits(T, H, I, E, k, G);
+
+  DcArgs a{};
+  a.T = T;
+  a.H = H;
+  a.I = I;
+  a.E = E;
+  a.k = k;
+  a.G = G;
+  a.s_sgu = sp.sgu;
+  a.s_rgu = sp.rgu;
+  a.s_sdn = sp.sdn;
+  a.n_sgu = shared ? (I / 128) * sp.sgu : 0;
+  a.n_sdn = shared ? (H / 128) * sp.sdn : 0;
+  a.nslot_max = imin(n, E);
+  a.shared = shared ? 1 : 0;
+  a.w13s_mma = ex.w13s_mma;
+  a.w2s_mma = ex.w2s_mma;
+  a.wr = wr;
+  a.bias = bias;
+  a.x = x;
+  a.out = out;
+  a.ids_out = ids_out;
+  a.w_out = w_out;
+  a.ctr = reinterpret_cast<int*>(base + L.counters);
+  a.tickets = reinterpret_cast<int*>(base + L.dc_tickets);
+  a.logits = reinterpret_cast<float*>(base + L.logits);
+  a.xq = base + L.xq;
+  a.xs_mma = base + L.dc_xs;
+  a.hq = base + L.hq;
+  a.hs_mma = base + L.dc_hs;
+  a.h_shared = reinterpret_cast<uint16_t*>(base + L.h_shared);
+  a.gu_sh = reinterpret_cast<float*>(base + L.dc_gu_sh);
+  a.gu_r = reinterpret_cast<float*>(base + L.dc_gu_r);
+  a.ys = reinterpret_cast<float*>(base + L.dc_ys);
+  a.y_assign = reinterpret_cast<float*>(base + L.y_assign);
+  a.limit_ns = wait_limit_ns;
+
+  DcMaps m;
+  memset(&m, 0, sizeof(m));
+  if ((err = make_map(&m.w13r, ex.w13, (uint64_t)E * 2 * I, H / 2)) != cudaSuccess) return err;
+  if ((err = make_map(&m.w2r, ex.w2, (uint64_t)E * H, I / 2)) != cudaSuccess) return err;
+  if ((err = make_map(&m.xq, a.xq, T, H / 2, 16)) != cudaSuccess) return err;
+  if ((err = make_map(&m.hq, a.hq, n, I / 2, 16)) != cudaSuccess) return err;
+  if (shared) {
+    if ((err = make_map(&m.w13s, shd.w13, (uint64_t)2 * I, (uint64_t)2 * H)) != cudaSuccess) return err;
+    if ((err = make_map(&m.w2s, shd.w2, H, (uint64_t)2 * I)) != cudaSuccess) return err;
+    if ((err = make_map(&m.x, x, T, (uint64_t)2 * H, 16)) != cudaSuccess) return err;
+    if ((err = make_map(&m.hsh, a.h_shared, T, (uint64_t)2 * I, 16)) != cudaSuccess) return err;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(DT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // blocks wait on one another: all must be resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_decode_tc, m, a);
+}
+
+}  // namespace moefp4

@@ -15,6 +15,8 @@ struct ExpertsDev {
   const uint8_t* w2;
   const uint8_t* w2s;
   const float* tscale;  // NVFP4 [E, 3]
+  const uint8_t* w13s_mma;  // prepared tensor-core scale layout, or null
+  const uint8_t* w2s_mma;
 };
 
 struct SharedDev {
@@ -26,6 +28,8 @@ struct Shape {
   int T, H, I, E, k;
 };
 
+// Canonical scale bytes [E][R][K/32] -> tensor-core layout [E][R/128][K/128][512 B].
+cudaError_t launch_relayout_weight_sf(const uint8_t* s, int E, int R, int K, uint8_t* out, cudaStream_t st);
 // A4
 cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t s);
@@ -75,6 +79,11 @@ cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const Sha
                                 const float* wr, const float* bias, const uint16_t* x, uint16_t* out,
                                 int* ids_out, float* w_out, void* ws, uint64_t wait_limit_ns,
                                 cudaStream_t s);
+// A10 on tensor cores (MXFP4 weights with prepared scales, H and I multiples of 256).
+bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex);
+cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
+                                   const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
+                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s);
 // A bounded wait on a counter nothing ever advances (exercises the timeout path).
 cudaError_t launch_wait_probe(void* ws, uint64_t wait_limit_ns, cudaStream_t s);
 

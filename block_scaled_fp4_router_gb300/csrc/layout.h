@@ -19,6 +19,36 @@ constexpr int PERM_CHUNK = 1024;   // assignments ranked per block in the permut
 constexpr int TC_MIN_ASSIGN = 256; // routed experts on tensor cores from this many assignments
 constexpr int TC_MIN_T_SHARED = 128; // shared expert on tensor cores from this many tokens
 
+// Tensor-core decode (T <= MAX_DECODE_T): one block per SM, at most this many.
+constexpr int DC_MAX_GRID = 256;
+constexpr int DC_MAX_SPLIT = 16;
+
+MOE_HD inline int imin(int a, int b) { return a < b ? a : b; }
+
+// Split-K factor: as many parts as keep `tiles` output tiles within one work
+// unit per block of a `grid`-block launch, at most one part per K stage.
+MOE_HD inline int dc_split(int tiles, int stages, int grid) {
+  int s = grid / tiles;
+  s = imin(imin(s, stages), DC_MAX_SPLIT);
+  return s < 1 ? 1 : s;
+}
+
+// Split factors of the tensor-core decode: shared gate/up (K = H in 64-element
+// BF16 stages), routed gate/up (K = H in 256-element FP4 stages) and shared
+// down (K = I in stages of two 64-element chunks; four parts make a part the
+// size of one routed down unit).
+struct DcSplits {
+  int sgu, rgu, sdn;
+};
+MOE_HD inline DcSplits dc_splits(int T, int H, int I, int E, int k, int grid) {
+  const int nslot = imin(T * k, E);
+  DcSplits d;
+  d.sgu = dc_split(I / 128, H / 64, grid);
+  d.rgu = dc_split((nslot > 0 ? nslot : 1) * (I / 128), H / 256 > 0 ? H / 256 : 1, grid);
+  d.sdn = imin(4, (I / 64 + 1) / 2);
+  return d;
+}
+
 // Rows of the per-expert padded order (each expert's rows rounded up to 128).
 MOE_HD inline int tc_padded_rows(int n, int E) { return ((n + E * 127) + 127) / 128 * 128; }
 MOE_HD inline bool tc_routed_enabled(int n) { return n >= TC_MIN_ASSIGN; }
@@ -37,6 +67,10 @@ enum Counter : int {
   C_EXIT = 5,      // blocks finished (the last one resets the counters)
   C_TEST = 6,      // never written by the library: a wait on it always times out
   C_HPATH = 7,     // which layout the last expert FFN left h in (0: sorted rows, else padded tiles)
+  C_DC_READY = 8,  // tensor-core decode: blocks done with their router rows and quantisation slice
+  C_DC_HSH = 9,    // tensor-core decode: shared-expert h tiles finished
+  C_DC_HR = 10,    // tensor-core decode: routed h tiles finished
+  C_DC_EXIT = 11,  // tensor-core decode: blocks finished
   N_COUNTERS = 16
 };
 
@@ -45,6 +79,8 @@ MOE_HD inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Byte offsets of every workspace region for one layer shape.
 struct WsLayout {
   size_t counters;     // int [N_COUNTERS]
+  size_t dc_tickets;   // int: split-K arrival tickets of the tensor-core decode
+  size_t zero_end;     // end of the part that must start zero-filled
   size_t logits;       // float [T, E]
   size_t ids;          // int [T, k]       (when the caller passes no output)
   size_t wts;          // float [T, k]
@@ -72,6 +108,12 @@ struct WsLayout {
   size_t tc_hs;        // scale blocks [padded rows/128][I/128][512 B]
   size_t tc_w13s;      // weight scale blocks [E][2I/128][H/128][512 B]
   size_t tc_w2s;       // weight scale blocks [E][H/128][I/128][512 B]
+  // tensor-core decode (T <= MAX_DECODE_T)
+  size_t dc_xs;        // x scales, MMA layout [H/128][512 B] (16 token rows)
+  size_t dc_hs;        // routed h scales, MMA layout [slots][I/128][512 B]
+  size_t dc_gu_sh;     // float [splits][T][2I]  shared gate/up partial sums
+  size_t dc_gu_r;      // float [splits][T*k][2I] routed gate/up partial sums
+  size_t dc_ys;        // float [splits][T][H]   shared down partial sums
   size_t total;
 };
 
@@ -85,7 +127,12 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
     o = align256(o + (bytes ? bytes : 1));
     return at;
   };
+  const bool dc = T <= MAX_DECODE_T;
+  const int nslot = imin(T * k, E);
+  const DcSplits sp = dc_splits(T, H, I, E, k, DC_MAX_GRID);
   L.counters = take(sizeof(int) * N_COUNTERS);
+  L.dc_tickets = take(dc ? sizeof(int) * ((size_t)(1 + nslot) * (I / 128) + H / 128) : 0);
+  L.zero_end = o;
   L.logits = take(sizeof(float) * (size_t)T * E);
   L.ids = take(sizeof(int) * n);
   L.wts = take(sizeof(float) * n);
@@ -114,6 +161,11 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.tc_hs = take(R * I / 32);
   L.tc_w13s = take(tc ? (size_t)E * 2 * I * H / 32 : 0);
   L.tc_w2s = take(tc ? (size_t)E * H * I / 32 : 0);
+  L.dc_xs = take(dc ? (size_t)H / 128 * 512 : 0);
+  L.dc_hs = take(dc ? (size_t)nslot * (I / 128) * 512 : 0);
+  L.dc_gu_sh = take(dc ? sizeof(float) * sp.sgu * T * 2 * (size_t)I : 0);
+  L.dc_gu_r = take(dc ? sizeof(float) * sp.rgu * n * 2 * (size_t)I : 0);
+  L.dc_ys = take(dc ? sizeof(float) * sp.sdn * T * (size_t)H : 0);
   L.total = o;
   return L;
 }

@@ -63,9 +63,10 @@ extern "C" moe_status_t moe_layer_decode_noalloc(const moe_layer_desc_t* desc, c
   const moe_status_t sst = scratch_for_current_device(&ws);
   if (sst != MOE_OK) return sst;
   // The scratch keeps whatever the previous call left in it; the launch needs
-  // its counters and status word at zero.
+  // its counters, status word and split-K tickets at zero.
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(int) * moefp4::N_COUNTERS, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const size_t zero_bytes = moefp4::ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k).zero_end;
+  if (cudaMemsetAsync(ws, 0, zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
   return moe_layer_decode(desc, experts, shared, w_router, bias, x, out, topk_ids, topk_w, ws, kScratchBytes,
                           stream);
 }

@@ -29,6 +29,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace moefp4 {
 
@@ -136,6 +137,13 @@ __global__ void __launch_bounds__(256) k_relayout_weight_sf(const uint8_t* __res
   const size_t tile = row / BM;   // (e * R + r) / 128: R is a multiple of 128
   const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(s + row * (K / 32)) + g);
   out[(tile * groups + g) * 128 + (m % 32) * 4 + (m / 32)] = v;
+}
+
+cudaError_t launch_relayout_weight_sf(const uint8_t* s, int E, int R, int K, uint8_t* out, cudaStream_t st) {
+  const size_t words = (size_t)E * R * (K / 128);
+  if (words == 0) return cudaSuccess;
+  k_relayout_weight_sf<<<(unsigned)((words + 255) / 256), 256, 0, st>>>(s, E, R, K, reinterpret_cast<uint32_t*>(out));
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -440,13 +448,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2D byte tensor [rows][row_bytes], tiles of 128 rows x 128 bytes, 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes) {
+}  // namespace
+
+cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -460,6 +469,8 @@ int sm_count() {
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 1;
 }
+
+namespace {
 
 template <int KIND, int EPI, bool GROUPED>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int max_tiles, cudaStream_t s) {
@@ -487,13 +498,13 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   k_gather_mx_rows<<<rmax, 128, 0, s>>>(xq, xs, H, sh.k, perm, reinterpret_cast<const MTile*>(w.mtiles), w.num_mt,
                                         w.xq_perm, reinterpret_cast<uint32_t*>(w.xs_mma));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  {
-    const size_t words13 = (size_t)E * 2 * I * (H / 128), words2 = (size_t)E * H * (I / 128);
-    k_relayout_weight_sf<<<(unsigned)((words13 + 255) / 256), 256, 0, s>>>(ex.w13s, E, 2 * I, H,
-                                                                          reinterpret_cast<uint32_t*>(w.w13s_mma));
-    k_relayout_weight_sf<<<(unsigned)((words2 + 255) / 256), 256, 0, s>>>(ex.w2s, E, H, I,
-                                                                         reinterpret_cast<uint32_t*>(w.w2s_mma));
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const uint8_t* w13s_mma = ex.w13s_mma;
+  const uint8_t* w2s_mma = ex.w2s_mma;
+  if (!w13s_mma || !w2s_mma) {  // not prepared at load time: re-lay the scales for this call
+    if ((err = launch_relayout_weight_sf(ex.w13s, E, 2 * I, H, w.w13s_mma, s)) != cudaSuccess) return err;
+    if ((err = launch_relayout_weight_sf(ex.w2s, E, H, I, w.w2s_mma, s)) != cudaSuccess) return err;
+    w13s_mma = w.w13s_mma;
+    w2s_mma = w.w2s_mma;
   }
   const int max_mt = rmax / BM;
   CUtensorMap ma, mb;
@@ -508,7 +519,7 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   g1.b_rows_per_expert = 2 * I;
   g1.b_up_off = I;
   g1.sfa = w.xs_mma;
-  g1.sfb = w.w13s_mma;
+  g1.sfb = w13s_mma;
   g1.sfb_rtiles = 2 * I / 128;
   g1.hq = w.hq_perm;
   g1.hs = reinterpret_cast<uint32_t*>(w.hs_mma);
@@ -526,7 +537,7 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   g2.mt = reinterpret_cast<const MTile*>(w.mtiles);
   g2.b_rows_per_expert = H;
   g2.sfa = w.hs_mma;
-  g2.sfb = w.w2s_mma;
+  g2.sfb = w2s_mma;
   g2.sfb_rtiles = H / 128;
   g2.out = y_assign;
   g2.ldo = H;

@@ -9,7 +9,7 @@ import numpy as np
 import torch
 
 from . import (MOE_W_MXFP4, MOE_W_NVFP4, desc, experts, moe_layer_decode, moe_layer_forward,
-               moe_workspace_size, shared_bf16)
+               moe_prepare_weights, moe_workspace_size, shared_bf16)
 
 
 def _to_dev(a, device, dtype=None):
@@ -24,10 +24,14 @@ def _to_dev(a, device, dtype=None):
 
 
 class DeviceLayer:
-    """One layer's weights on the GPU plus a workspace sized for up to T_max tokens."""
+    """One layer's weights on the GPU plus a workspace sized for up to T_max tokens.
+
+    MXFP4 layers also get the tensor-core copy of their scales
+    (moe_prepare_weights) unless prepare=False; set_prepared() switches
+    between the two descriptions of the same weights."""
 
     def __init__(self, arrays: dict, H: int, I: int, E: int, top_k: int, fmt: str, T_max: int,
-                 device="cuda", shared: bool = True):
+                 device="cuda", shared: bool = True, prepare: bool = True):
         self.H, self.I, self.E, self.k, self.fmt = H, I, E, top_k, fmt
         self.device = torch.device(device)
         d = self.device
@@ -41,12 +45,30 @@ class DeviceLayer:
         use_shared = shared and arrays.get("ws13") is not None
         self.ws13 = _to_dev(arrays["ws13"], d, torch.int16) if use_shared else None
         self.ws2 = _to_dev(arrays["ws2"], d, torch.int16) if use_shared else None
-        self.ex = experts(MOE_W_MXFP4 if fmt == "mxfp4" else MOE_W_NVFP4, self.w13, self.w13_scale,
-                          self.w2, self.w2_scale, self.tensor_scale)
+        wfmt = MOE_W_MXFP4 if fmt == "mxfp4" else MOE_W_NVFP4
+        self.ex_plain = experts(wfmt, self.w13, self.w13_scale, self.w2, self.w2_scale, self.tensor_scale)
+        self.ex_prepared = None
+        if prepare and fmt == "mxfp4":
+            self.w13_scale_mma = torch.empty_like(self.w13_scale)
+            self.w2_scale_mma = torch.empty_like(self.w2_scale)
+            moe_prepare_weights(desc(0, H, I, E, top_k), self.ex_plain, self.w13_scale_mma, self.w2_scale_mma)
+            self.ex_prepared = experts(wfmt, self.w13, self.w13_scale, self.w2, self.w2_scale, self.tensor_scale,
+                                       self.w13_scale_mma, self.w2_scale_mma)
+        self.ex = self.ex_prepared if self.ex_prepared is not None else self.ex_plain
         self.sh = shared_bf16(self.ws13, self.ws2)
         self.T_max = T_max
         nbytes = moe_workspace_size(desc(T_max, H, I, E, top_k))
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=d)
+
+    @property
+    def prepared(self) -> bool:
+        return self.ex_prepared is not None and self.ex is self.ex_prepared
+
+    def set_prepared(self, on: bool):
+        """Use the prepared scales (tensor-core decode) or only the canonical ones."""
+        if on and self.ex_prepared is None:
+            raise ValueError("this layer has no prepared scales (NVFP4, or prepare=False)")
+        self.ex = self.ex_prepared if on else self.ex_plain
 
     def desc(self, T: int):
         if T > self.T_max:

@@ -98,7 +98,9 @@ typedef struct {
   int32_t act_quant;
 } moe_layer_desc_t;
 
-/* Routed-expert weights (device pointers, layouts above). */
+/* Routed-expert weights (device pointers, layouts above).  The two *_mma
+ * fields are optional copies of the scale bytes in the tensor-core layout
+ * written by moe_prepare_weights (MXFP4 only; NULL = not prepared). */
 typedef struct {
   moe_wfmt_t fmt;
   const uint8_t* w13;
@@ -106,6 +108,8 @@ typedef struct {
   const uint8_t* w2;
   const uint8_t* w2_scale;
   const float* tensor_scale;   /* NVFP4: [E, 3]; MXFP4: must be NULL */
+  const uint8_t* w13_scale_mma;
+  const uint8_t* w2_scale_mma;
 } moe_experts_t;
 
 /* The BF16 shared expert; both NULL = the layer has no shared expert. */
@@ -120,6 +124,20 @@ MOE_API const char* moe_status_string(moe_status_t st);
 /* Bytes of workspace any entry point below needs for this layer shape
  * (the maximum over all of them).  desc must be valid. */
 MOE_API moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* bytes);
+
+/* Load-time re-layout of MXFP4 expert scales for the tensor-core paths (the
+ * pages convert expert weights at load time: AMD article, section "Enabling
+ * the MXFP4 checkpoint with the AMD Quark"; vLLM PR #64273, section
+ * "Purpose").  Writes the E8M0 scale bytes of W13 and W2 again, in blocks of
+ * 128 rows x 128 K elements (512 bytes each, word (i, j) at byte 16 i + 4 j
+ * holding the 4 scales of row 32 j + i), block order [E][rows/128][K/128]:
+ *   w13_scale_mma  out, E * 2I * H/32 bytes;  w2_scale_mma  out, E * H * I/32 bytes
+ * (16-byte aligned).  Point experts->w13_scale_mma / w2_scale_mma at them
+ * afterwards: moe_layer_decode then runs its contractions on tensor cores
+ * (when H and I are multiples of 256), and the batched path skips its
+ * per-call re-layout.  NVFP4 returns MOE_ERR_UNSUPPORTED. */
+MOE_API moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                         uint8_t* w13_scale_mma, uint8_t* w2_scale_mma, moe_stream_t stream);
 
 /* Reads (and clears) the device status word of a workspace into *st.  Call
  * after synchronising the stream the workspace was used on.  This is the one

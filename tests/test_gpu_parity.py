@@ -309,9 +309,18 @@ def test_expert_ffn_contractions(name):
 # ----------------------------------------------------------- whole layer
 
 
+def _use_prepared(dev, prepared):
+    """Selects the tensor-core decode (prepared MXFP4 scales) or the CUDA-core one."""
+    if prepared and dev.ex_prepared is None:
+        pytest.skip("NVFP4 experts have no tensor-core decode")
+    dev.set_prepared(prepared)
+
+
+@pytest.mark.parametrize("prepared", [True, False], ids=["tcgen05", "cudacore"])
 @pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode16z"])
-def test_layer_decode_fused(name):
+def test_layer_decode_fused(name, prepared):
     wl, lay, dev, cache = _workload(name)
+    _use_prepared(dev, prepared)
     out, ids, w = dev.decode(bf16_tensor(lay["x"]))
     torch.cuda.synchronize()
     assert M.moe_get_status(dev.ws) == M.MOE_OK
@@ -320,7 +329,22 @@ def test_layer_decode_fused(name):
     out2, ids2, _ = dev.decode(bf16_tensor(lay["x"]))
     torch.cuda.synchronize()
     assert torch.equal(out, out2) and torch.equal(ids, ids2)
+    dev.set_prepared(dev.ex_prepared is not None)
 
+
+def test_prepared_scales_are_the_tensor_core_layout():
+    """moe_prepare_weights writes each 128-row x 128-element scale block as
+    512 bytes, word 4i + j (little-endian bytes) holding the four scales of
+    row 32j + i, blocks ordered [expert][row tile][K group]."""
+    wl, lay, dev, cache = _workload("tiny")
+    E, H, I = wl.E, wl.H, wl.I
+
+    def relayout(s, R, K):
+        s = s.reshape(E, R // 128, 4, 32, K // 128, 4)        # e, rt, j, i, g, byte
+        return s.transpose(0, 1, 4, 3, 2, 5).reshape(-1)       # e, rt, g, i, j, byte
+
+    assert np.array_equal(dev.w13_scale_mma.cpu().numpy().reshape(-1), relayout(lay["w13_scale"], 2 * I, H))
+    assert np.array_equal(dev.w2_scale_mma.cpu().numpy().reshape(-1), relayout(lay["w2_scale"], H, I))
 
 @pytest.mark.parametrize("name", ["tiny", "decode1", "decode16"])
 def test_layer_forward_matches_decode(name):
@@ -333,9 +357,11 @@ def test_layer_forward_matches_decode(name):
     assert normwise(bits_to_float(out_f), bits_to_float(out_d)) <= 1e-2
 
 
+@pytest.mark.parametrize("prepared", [True, False], ids=["tcgen05", "cudacore"])
 @pytest.mark.parametrize("T", [1, 2, 7, 13, 16])
-def test_decode_token_counts(T):
+def test_decode_token_counts(T, prepared):
     wl, lay, dev, cache = _workload("tiny")
+    _use_prepared(dev, prepared)
     sub = dict(lay)
     sub["x"] = lay["x"][:T]
     out, ids, _ = dev.decode(bf16_tensor(sub["x"]))
@@ -349,6 +375,7 @@ def test_decode_token_counts(T):
     with pytest.raises(M.MoeError) as e:
         M.moe_layer_decode(d17, dev.ex, dev.sh, dev.w_router, dev.bias, x17, o17, None, None, ws17)
     assert e.value.status == M.MOE_ERR_UNSUPPORTED
+    dev.set_prepared(True)
 
 
 def test_batch128_forward_sampled():
@@ -427,6 +454,39 @@ def test_small_and_degenerate_shapes(shape):
     out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
     torch.cuda.synchronize()
     _compare_layer(wl, lay, cache, out, ids)
+
+
+@pytest.mark.parametrize("shape", [(5, 256, 256, 256, 8), (16, 256, 512, 4, 4), (1, 768, 768, 8, 2),
+                                   (11, 1024, 256, 64, 6)])
+def test_tensor_core_decode_shapes(shape):
+    """The tcgen05 decode on E = 256 with k = 8, a dense mixture (E == k) at
+    16 tokens, odd numbers of K chunks (H = I = 768) and a mid-size case;
+    the CUDA-core decode on the same layer agrees."""
+    T, H, I, E, k = shape
+    wl = W.Workload("dcedge", T, H, I, E, k, W.MXFP4, 24, 0.5)
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, H, I, E, k, wl.fmt, T_max=T)
+    cache = {}
+    out, ids, _ = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, cache, out, ids)
+    dev.set_prepared(False)
+    out_c, ids_c, _ = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_c)
+    assert normwise(bits_to_float(out), bits_to_float(out_c)) <= 1e-2
+
+
+def test_tensor_core_decode_without_shared_expert():
+    wl = W.Workload("noshared_mx", 3, 512, 512, 16, 4, W.MXFP4, 25, 0.05, shared=False)
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, wl.H, wl.I, wl.E, wl.top_k, wl.fmt, T_max=wl.T)
+    assert dev.prepared
+    out, ids, _ = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, {}, out, ids)
 
 
 def test_layer_without_shared_expert():
