@@ -6,9 +6,9 @@
 //
 // A decode step streams every touched weight byte once, so the layer is
 // bound by HBM.  The weights are the MMA's A operand (128 weight rows per
-// MMA, moved by TMA through a 5-stage shared-memory ring) and the 1-16 token
-// rows are a 16-row B operand, so one block keeps ~200 KB of weights in
-// flight without spending CUDA-core issue slots on FP4 decoding.
+// MMA, moved by TMA through a shared-memory ring) and the 1-16 token rows are
+// a 16-row B operand, so every SM keeps weights in flight without spending
+// CUDA-core issue slots on FP4 decoding.
 //
 // Work units (one block per SM, cooperative launch, the same static
 // round-robin list in every block):
@@ -47,7 +47,10 @@ namespace {
 
 constexpr int DT = 192;                 // threads: TMA warp, MMA warp, 4 epilogue warps
 constexpr int EPI_THREADS = 128;
-constexpr int DSTAGES = 5;
+// Two stages (~68 KB in flight per SM, ~10 MB over the GPU) already cover
+// HBM's bandwidth-latency product; a deeper ring only lengthens the queues
+// that the latency-bound hand-offs between the steps wait in.
+constexpr int DSTAGES = 2;
 // byte offsets inside one stage (swizzled tiles on 1024-byte boundaries)
 constexpr uint32_t ST_A0 = 0, ST_A1 = 16384;       // 128 rows x 128 B each
 constexpr uint32_t ST_B0 = 32768, ST_B1 = 34816;   // 16 rows x 128 B each
@@ -78,7 +81,7 @@ struct DcArgs {
   float* w_out;
   int* ctr;
   int* tickets;
-  float* logits;             // [T, E]
+  unsigned long long* logit64;  // [T, E]: (launch number << 32) | FP32 bits
   uint8_t* xq;               // [T, H/2]
   uint8_t* xs_mma;           // [H/128][512]
   uint8_t* hq;               // [T k, I/2] sorted-assignment rows
@@ -176,14 +179,15 @@ __device__ Unit unit_at(const DcArgs& a, int n_slots, int u) {
 
 __device__ __forceinline__ void epi_sync() { tc::named_sync(1, EPI_THREADS); }
 
-// sum over p < S of src[p * stride], in ascending p, every load issued first.
+// sum over p < S <= MAXS of src[p * stride], in ascending p, every load issued first.
+template <int MAXS = DC_MAX_SPLIT>
 __device__ __forceinline__ float sum_parts(const float* src, size_t stride, int S) {
-  float v[DC_MAX_SPLIT];
+  float v[MAXS];
 #pragma unroll
-  for (int p = 0; p < DC_MAX_SPLIT; ++p) v[p] = p < S ? __ldcg(src + p * stride) : 0.0f;
+  for (int p = 0; p < MAXS; ++p) v[p] = p < S ? __ldcg(src + p * stride) : 0.0f;
   float s = 0.0f;
 #pragma unroll
-  for (int p = 0; p < DC_MAX_SPLIT; ++p)
+  for (int p = 0; p < MAXS; ++p)
     if (p < S) s += v[p];
   return s;
 }
@@ -198,11 +202,21 @@ __device__ __forceinline__ float pick16(const float (&v)[32], int base, int t) {
 
 // ----------------------------------------------------- epilogue-warp prologue
 
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Router row e for all tokens (FP32 weights and accumulation), 128 threads.
 // Tokens go in groups of 4; within a group every load of a pass (4 x 8
 // elements per thread) is in flight before the FMAs, since these loads
 // compete with the weight streams for HBM.
-__device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DECODE_T]) {
+__device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DECODE_T], uint32_t epoch) {
   const int T = a.T, H = a.H;
   const int w = et >> 5, lane = et & 31;
   constexpr int PASS = EPI_THREADS * 8;
@@ -255,7 +269,9 @@ __device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DE
     float s = red_s[0][et];
     for (int ww = 1; ww < EPI_THREADS / 32; ++ww) s += red_s[ww][et];
     if (a.bias) s += a.bias[e];
-    a.logits[(size_t)et * a.E + e] = s;
+    // one 64-bit store carries the value and this launch's number: a reader
+    // that sees the number has the value, with no fence or counter between
+    st_relaxed_u64(a.logit64 + (size_t)et * a.E + e, ((unsigned long long)epoch << 32) | __float_as_uint(s));
   }
   epi_sync();
 }
@@ -300,16 +316,44 @@ __device__ void quant_block(const DcArgs& a, int i) {
   a.xs_mma[(size_t)(b / 4) * 512 + t * 16 + (b % 4)] = sb;
 }
 
+// One warp reads token t's E logits once every one carries this launch's
+// number (bounded wait; false on timeout).  Lane l gets experts l, l+32, ...
+__device__ bool wait_logit_row(const DcArgs& a, int t, uint32_t epoch, float (&v)[8]) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long* row = a.logit64 + (size_t)t * a.E;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    bool mine = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = 0.0f;
+      if (e < a.E) {
+        const unsigned long long w = ld_relaxed_u64(row + e);
+        mine &= (uint32_t)(w >> 32) == epoch;
+        v[i] = __uint_as_float((uint32_t)w);
+      }
+    }
+    if (__all_sync(FULL, mine)) return true;
+    if (__shfl_sync(FULL, (int)(globaltimer_ns() - t0 > a.limit_ns), 0)) return false;
+    __nanosleep(32);
+  }
+}
+
 // Top-k of every token (one epilogue warp per token), then the stable
 // counting sort of the T*k assignments by expert and the distinct-expert
-// slots.  128 epilogue threads, et = 0..127.
-__device__ void build_routing(const DcArgs& a, DcRouting& R, int et) {
+// slots.  128 epilogue threads, et = 0..127.  *failed is set (by some
+// thread) when a logit row never arrived.
+__device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t epoch, int* failed) {
   const int T = a.T, E = a.E, k = a.k, n = T * k;
   const int w = et >> 5, lane = et & 31;
   for (int e = et; e < E; e += EPI_THREADS) R.cnt[e] = 0;
   for (int t = w; t < T; t += EPI_THREADS / 32) {
     float v[8];
-    load_logit_row(a.logits + (size_t)t * E, E, v, true);
+    if (!wait_logit_row(a, t, epoch, v)) {
+      if (lane == 0) *failed = 1;
+      continue;
+    }
     int sel[MAX_TOPK];
     float vals[MAX_TOPK], wt[MAX_TOPK];
     warp_topk(v, E, k, sel, vals);
@@ -322,6 +366,7 @@ __device__ void build_routing(const DcArgs& a, DcRouting& R, int et) {
       }
   }
   epi_sync();
+  if (*failed) return;  // the same answer in every thread after the barrier
   int e = -1, rank = 0;
   if (et < n) {
     e = R.ids[et];
@@ -382,6 +427,71 @@ __device__ void prefetch_down_unit(const DcArgs& a, const DcMaps& m, const Unit&
   }
 }
 
+// Halves of a stage that a unit uses: gate/up units one K chunk (two weight
+// tiles, one activation tile), down units two K chunks (the second may be
+// past the end of K).
+__device__ __forceinline__ int stage_halves(const DcArgs& a, const Unit& U, int st) {
+  if (U.kind == U_SDN) return 2 * st + 1 < a.I / 64 ? 2 : 1;
+  if (U.kind == U_RDN) return 2 * st + 1 < a.I / 256 ? 2 : 1;
+  return 2;
+}
+
+// Bytes one stage of a unit brings in (the mbarrier transaction count).
+__device__ __forceinline__ uint32_t stage_tx(const DcArgs& a, const Unit& U, int st) {
+  const uint32_t h = stage_halves(a, U, st);
+  switch (U.kind) {
+    case U_SGU: return 2 * A_TILE + B_TILE;
+    case U_RGU: return 2 * A_TILE + B_TILE + 3 * 1024;
+    case U_SDN: return h * (A_TILE + B_TILE);
+    default: return h * (A_TILE + B_TILE + 2048);
+  }
+}
+
+// TMA / bulk copies of the weight tiles (and their scales) of stage st.
+__device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, const Unit& U, int st, int e,
+                                              uint8_t* sp, uint64_t* fb) {
+  const int nbI = a.I / 128, nbH = a.H / 128;
+  if (U.kind == U_SGU) {
+    tc::tma_load_2d(sp + ST_A0, &m.w13s, st * 128, 128 * U.tile, fb);
+    tc::tma_load_2d(sp + ST_A1, &m.w13s, st * 128, a.I + 128 * U.tile, fb);
+  } else if (U.kind == U_RGU) {
+    const int row = e * 2 * a.I + 128 * U.tile;
+    const size_t hg = a.H / 128;
+    const size_t rt = (size_t)e * (2 * nbI) + U.tile;  // gate row tile; the up tile is nbI further
+    tc::tma_load_2d(sp + ST_A0, &m.w13r, st * 128, row, fb);
+    tc::tma_load_2d(sp + ST_A1, &m.w13r, st * 128, row + a.I, fb);
+    tc::bulk_load(sp + ST_SFA, a.w13s_mma + (rt * hg + 2 * st) * 512, 1024, fb);
+    tc::bulk_load(sp + ST_SFA + 1024, a.w13s_mma + ((rt + nbI) * hg + 2 * st) * 512, 1024, fb);
+  } else if (U.kind == U_SDN) {
+    for (int h = 0; h < stage_halves(a, U, st); ++h)
+      tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &m.w2s, (2 * st + h) * 128, 128 * U.tile, fb);
+  } else {
+    const int halves = stage_halves(a, U, st);
+    for (int h = 0; h < halves; ++h)
+      tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &m.w2r, (2 * st + h) * 128, e * a.H + 128 * U.tile, fb);
+    tc::bulk_load(sp + ST_SFA, a.w2s_mma + (((size_t)e * nbH + U.tile) * (a.I / 128) + 4 * st) * 512, halves * 1024, fb);
+  }
+}
+
+// TMA / bulk copies of the activation tiles (and their scales) of stage st.
+__device__ __forceinline__ void issue_acts(const DcArgs& a, const DcMaps& m, const Unit& U, int st, int beg,
+                                           uint8_t* sp, uint64_t* fb) {
+  if (U.kind == U_SGU) {
+    tc::tma_load_2d(sp + ST_B0, &m.x, st * 128, 0, fb);
+  } else if (U.kind == U_RGU) {
+    tc::tma_load_2d(sp + ST_B0, &m.xq, st * 128, 0, fb);
+    tc::bulk_load(sp + ST_SFB, a.xs_mma + (size_t)2 * st * 512, 1024, fb);
+  } else if (U.kind == U_SDN) {
+    for (int h = 0; h < stage_halves(a, U, st); ++h)
+      tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hsh, (2 * st + h) * 128, 0, fb);
+  } else {
+    const int halves = stage_halves(a, U, st);
+    for (int h = 0; h < halves; ++h)
+      tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hq, (2 * st + h) * 128, beg, fb);
+    tc::bulk_load(sp + ST_SFB, a.hs_mma + ((size_t)U.slot * (a.I / 128) + 4 * st) * 512, halves * 1024, fb);
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
 __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcMaps maps, const DcArgs a) {
@@ -389,7 +499,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[DSTAGES], empty[DSTAGES], acc_full[2], acc_empty[2], drain, routing_ready;
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag, s_ok, s_last;
+  __shared__ int abort_flag, s_ok, s_last, s_fail;
+  __shared__ uint32_t s_epoch;
   __shared__ DcRouting R;
   __shared__ float red_s[EPI_THREADS / 32][MAX_DECODE_T];
   __shared__ __align__(4) uint8_t s_hsb[MAX_DECODE_T * 4];
@@ -410,6 +521,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     tc::mbar_init(&routing_ready, 1);
     tc::mbar_fence_init();
     abort_flag = 0;
+    s_fail = 0;
+    s_epoch = (uint32_t)ld_acquire(a.ctr + C_DC_EPOCH) + 1u;
   }
   if (warp == 1) tc::tmem_alloc(&tmem_base, DC_TMEM_COLS);
   tc::fence_before_sync();
@@ -445,7 +558,9 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           for (int v = blockIdx.x; v < a.n_sdn; v += a.G) prefetch_down_unit(a, maps, sdn_unit(a, v), 0);
           if (!tc::mbar_wait(&routing_ready, 0, a.limit_ns, &abort_flag)) { fail(); break; }
           n_slots = R.n_slots;
-          tc::fence_proxy_async_global();  // x was quantised by plain stores of other blocks
+          // x was quantised by plain stores of other blocks
+          if (!wait_at_least(a.ctr + C_DC_READY, a.G, status, a.limit_ns)) { fail(); break; }
+          tc::fence_proxy_async_global();
           // The routed down weights are known now: into L2 while the gate/up streams run.
           const int n_rdn = n_slots * nbH;
           for (int v = blockIdx.x; v < n_rdn; v += a.G) {
@@ -460,60 +575,45 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           e = R.slot_e[U.slot];
           beg = R.slot_beg[U.slot];
         }
-        // The down units read h written by other blocks.
-        if (U.kind == U_SDN && !hsh_ok) {
-          if (!wait_at_least(a.ctr + C_DC_HSH, nbI, status, a.limit_ns)) { fail(); break; }
-          hsh_ok = true;
+        // Down units read h that other blocks write.  While it is not there
+        // yet, the unit's weight tiles already go into the ring (up to its
+        // depth); their h tiles follow once the dependency is met.
+        int npre = 0;
+        uint32_t pre_stage[DSTAGES];
+        const bool dep_sdn = U.kind == U_SDN && !hsh_ok, dep_rdn = U.kind == U_RDN && !hr_ok;
+        if (dep_sdn || dep_rdn) {
+          int* cnt = a.ctr + (dep_sdn ? C_DC_HSH : C_DC_HR);
+          const int target = dep_sdn ? nbI : n_slots * nbI;
+          if (ld_acquire(cnt) < target) {
+            npre = imin(U.st1 - U.st0, DSTAGES);
+            bool ok = true;
+            for (int j = 0; j < npre; ++j) {
+              if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
+              tc::mbar_expect_tx(&full[stage], stage_tx(a, U, U.st0 + j));
+              issue_weights(a, maps, U, U.st0 + j, e, dsm + stage * STAGE_BYTES, &full[stage]);
+              pre_stage[j] = stage;
+              issued |= 1u << stage;
+              last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+              if (++stage == DSTAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+            if (!ok) break;
+            if (!wait_at_least(cnt, target, status, a.limit_ns)) { fail(); break; }
+          }
+          if (dep_sdn) hsh_ok = true; else hr_ok = true;
           tc::fence_proxy_async_global();
-        }
-        if (U.kind == U_RDN && !hr_ok) {
-          if (!wait_at_least(a.ctr + C_DC_HR, n_slots * nbI, status, a.limit_ns)) { fail(); break; }
-          hr_ok = true;
-          tc::fence_proxy_async_global();
+          for (int j = 0; j < npre; ++j)
+            issue_acts(a, maps, U, U.st0 + j, beg, dsm + pre_stage[j] * STAGE_BYTES, &full[pre_stage[j]]);
         }
         bool ok = true;
-        for (int st = U.st0; st < U.st1; ++st) {
+        for (int st = U.st0 + npre; st < U.st1; ++st) {
           if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
           uint8_t* sp = dsm + stage * STAGE_BYTES;
-          uint64_t* fb = &full[stage];
-          if (U.kind == U_SGU) {
-            const int xc = st * 128;
-            tc::mbar_expect_tx(fb, 2 * A_TILE + B_TILE);
-            tc::tma_load_2d(sp + ST_A0, &maps.w13s, xc, 128 * U.tile, fb);
-            tc::tma_load_2d(sp + ST_A1, &maps.w13s, xc, a.I + 128 * U.tile, fb);
-            tc::tma_load_2d(sp + ST_B0, &maps.x, xc, 0, fb);
-          } else if (U.kind == U_RGU) {
-            const int xc = st * 128;
-            const int row = e * 2 * a.I + 128 * U.tile;
-            const size_t hg = a.H / 128;
-            const size_t rt = (size_t)e * (2 * nbI) + U.tile;  // gate row tile; the up tile is nbI further
-            tc::mbar_expect_tx(fb, 2 * A_TILE + B_TILE + 3 * 1024);
-            tc::tma_load_2d(sp + ST_A0, &maps.w13r, xc, row, fb);
-            tc::tma_load_2d(sp + ST_A1, &maps.w13r, xc, row + a.I, fb);
-            tc::tma_load_2d(sp + ST_B0, &maps.xq, xc, 0, fb);
-            tc::bulk_load(sp + ST_SFA, a.w13s_mma + (rt * hg + 2 * st) * 512, 1024, fb);
-            tc::bulk_load(sp + ST_SFA + 1024, a.w13s_mma + ((rt + nbI) * hg + 2 * st) * 512, 1024, fb);
-            tc::bulk_load(sp + ST_SFB, a.xs_mma + (size_t)2 * st * 512, 1024, fb);
-          } else if (U.kind == U_SDN) {
-            const int halves = 2 * st + 1 < a.I / 64 ? 2 : 1;
-            tc::mbar_expect_tx(fb, halves * (A_TILE + B_TILE));
-            for (int h = 0; h < halves; ++h) {
-              const int xc = (2 * st + h) * 128;
-              tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &maps.w2s, xc, 128 * U.tile, fb);
-              tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &maps.hsh, xc, 0, fb);
-            }
-          } else {
-            const int halves = 2 * st + 1 < a.I / 256 ? 2 : 1;
-            const size_t ig = a.I / 128;
-            tc::mbar_expect_tx(fb, halves * (A_TILE + B_TILE + 2048));
-            for (int h = 0; h < halves; ++h) {
-              const int xc = (2 * st + h) * 128;
-              tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &maps.w2r, xc, e * a.H + 128 * U.tile, fb);
-              tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &maps.hq, xc, beg, fb);
-            }
-            tc::bulk_load(sp + ST_SFA, a.w2s_mma + (((size_t)e * nbH + U.tile) * ig + 4 * st) * 512, halves * 1024, fb);
-            tc::bulk_load(sp + ST_SFB, a.hs_mma + ((size_t)U.slot * ig + 4 * st) * 512, halves * 1024, fb);
-          }
+          tc::mbar_expect_tx(&full[stage], stage_tx(a, U, st));
+          issue_weights(a, maps, U, st, e, sp, &full[stage]);
+          issue_acts(a, maps, U, st, beg, sp, &full[stage]);
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == DSTAGES) {
@@ -579,7 +679,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
                            tsf + 16 + 4 * grp, accum);
             }
           } else if (U.kind == U_SDN) {
-            const int halves = 2 * st + 1 < a.I / 64 ? 2 : 1;
+            const int halves = stage_halves(a, U, st);
             for (int h = 0; h < halves; ++h) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
@@ -589,7 +689,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               }
             }
           } else {
-            const int halves = 2 * st + 1 < a.I / 256 ? 2 : 1;
+            const int halves = stage_halves(a, U, st);
             for (int h = 0; h < halves; ++h) {
               tc::sf_copy(tsf + 8 * h, tc::desc_sf(sa + ST_SFA + 1024 * h));
               tc::sf_copy(tsf + 8 * h + 4, tc::desc_sf(sa + ST_SFA + 1024 * h + 512));
@@ -628,20 +728,18 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     const int T = a.T, H = a.H, I = a.I, k = a.k, n = T * k;
 
-    for (int e = blockIdx.x; e < a.E; e += a.G) router_row(a, e, et, red_s);
+    const uint32_t epoch = s_epoch;
+    for (int e = blockIdx.x; e < a.E; e += a.G) router_row(a, e, et, red_s, epoch);
     const int nqb = MAX_DECODE_T * (H / 32);
-    for (int i = blockIdx.x * EPI_THREADS + et; i < nqb; i += a.G * EPI_THREADS) quant_block(a, i);
+    // the router rows go to the first E blocks, the quantisation to the last ones
+    for (int i = (a.G - 1 - blockIdx.x) * EPI_THREADS + et; i < nqb; i += a.G * EPI_THREADS) quant_block(a, i);
     tc::fence_proxy_async_global();
-    __threadfence();
-    epi_sync();
-    if (et == 0) {
-      red_release_add(a.ctr + C_DC_READY, 1);
-      s_ok = wait_at_least(a.ctr + C_DC_READY, a.G, status, a.limit_ns);
-      if (!s_ok) fail();
-    }
-    epi_sync();
-    if (s_ok) {
-      build_routing(a, R, et);
+    epi_sync();  // orders every thread's stores before thread 0's release
+    if (et == 0) red_release_add(a.ctr + C_DC_READY, 1);
+    build_routing(a, R, et, epoch, &s_fail);
+    if (s_fail) {
+      if (et == 0) fail();
+    } else {
       if (et == 0) tc::mbar_arrive(&routing_ready);
       if (blockIdx.x == 0 && et < n) {
         if (a.ids_out) a.ids_out[et] = R.ids[et];
@@ -710,26 +808,34 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           target = dn_target;
         }
         // split-K arrival: the block that brings the last part finishes the tile
-        __threadfence();
         epi_sync();
         if (et == 0) {
+          __threadfence();
           const int old = atomicAdd(a.tickets + ticket, 1);
           s_last = old == target - 1;
-          if (s_last) a.tickets[ticket] = 0;
+          if (s_last) {
+            a.tickets[ticket] = 0;
+            __threadfence();
+          }
         }
         epi_sync();
         if (!s_last) continue;
-        __threadfence();
         if (U.kind == U_SGU) {
           const float* src = a.gu_sh + 128 * U.tile + m;
           const size_t stride = (size_t)T * 2 * I;
-          for (int t = 0; t < T; ++t) {
-            const float g = sum_parts(src + (size_t)t * 2 * I, stride, a.s_sgu);
-            const float up = sum_parts(src + (size_t)t * 2 * I + I, stride, a.s_sgu);
-            a.h_shared[(size_t)t * I + 128 * U.tile + m] = f32_to_bf16_rn(silu(g) * up);
+          for (int t0 = 0; t0 < T; t0 += 2) {  // two tokens' loads in flight together
+            float g[2], up[2];
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+              const int t = imin(t0 + tt, T - 1);
+              g[tt] = sum_parts(src + (size_t)t * 2 * I, stride, a.s_sgu);
+              up[tt] = sum_parts(src + (size_t)t * 2 * I + I, stride, a.s_sgu);
+            }
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+              if (t0 + tt < T) a.h_shared[(size_t)(t0 + tt) * I + 128 * U.tile + m] = f32_to_bf16_rn(silu(g[tt]) * up[tt]);
           }
           tc::fence_proxy_async_global();
-          __threadfence();
           epi_sync();
           if (et == 0) red_release_add(a.ctr + C_DC_HSH, 1);
         } else if (U.kind == U_RGU) {
@@ -754,22 +860,32 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           const uint32_t word = ((et & 3) == 0 && (et >> 2) < cnt) ? reinterpret_cast<const uint32_t*>(s_hsb)[et >> 2] : 0u;
           reinterpret_cast<uint32_t*>(a.hs_mma)[((size_t)U.slot * nbI + U.tile) * 128 + et] = word;
           tc::fence_proxy_async_global();
-          __threadfence();
           epi_sync();
           if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
         } else {
           // out = BF16(ys + sum_j w_j y_j), summed in a fixed order
           const int col = 128 * U.tile + m;
-          for (int t = 0; t < T; ++t) {
-            float y[MAX_TOPK];
+          for (int t0 = 0; t0 < T; t0 += 4) {  // four tokens' loads in flight together
+            float y[4][MAX_TOPK], ysh[4];
 #pragma unroll
-            for (int j = 0; j < MAX_TOPK; ++j)
-              y[j] = j < k ? __ldcg(a.y_assign + (size_t)R.inv[t * k + j] * H + col) : 0.0f;
-            float acc = a.shared ? sum_parts(a.ys + (size_t)t * H + col, (size_t)T * H, a.s_sdn) : 0.0f;
+            for (int tt = 0; tt < 4; ++tt) {
+              const int t = imin(t0 + tt, T - 1);
 #pragma unroll
-            for (int j = 0; j < MAX_TOPK; ++j)
-              if (j < k) acc = fmaf(R.w[t * k + j], y[j], acc);
-            a.out[(size_t)t * H + col] = f32_to_bf16_rn(acc);
+              for (int j = 0; j < MAX_TOPK; ++j)
+                y[tt][j] = j < k ? __ldcg(a.y_assign + (size_t)R.inv[t * k + j] * H + col) : 0.0f;
+              ysh[tt] = a.shared ? sum_parts<4>(a.ys + (size_t)t * H + col, (size_t)T * H, a.s_sdn) : 0.0f;
+            }
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+              const int t = t0 + tt;
+              if (t < T) {
+                float acc = ysh[tt];
+#pragma unroll
+                for (int j = 0; j < MAX_TOPK; ++j)
+                  if (j < k) acc = fmaf(R.w[t * k + j], y[tt][j], acc);
+                a.out[(size_t)t * H + col] = f32_to_bf16_rn(acc);
+              }
+            }
           }
         }
       }
@@ -790,6 +906,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       a.ctr[C_DC_HSH] = 0;
       a.ctr[C_DC_HR] = 0;
       a.ctr[C_DC_EXIT] = 0;
+      a.ctr[C_DC_EPOCH] = (int)s_epoch;
       __threadfence();
     }
   }
@@ -845,7 +962,7 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.w_out = w_out;
   a.ctr = reinterpret_cast<int*>(base + L.counters);
   a.tickets = reinterpret_cast<int*>(base + L.dc_tickets);
-  a.logits = reinterpret_cast<float*>(base + L.logits);
+  a.logit64 = reinterpret_cast<unsigned long long*>(base + L.dc_logit64);
   a.xq = base + L.xq;
   a.xs_mma = base + L.dc_xs;
   a.hq = base + L.hq;

@@ -67,10 +67,11 @@ enum Counter : int {
   C_EXIT = 5,      // blocks finished (the last one resets the counters)
   C_TEST = 6,      // never written by the library: a wait on it always times out
   C_HPATH = 7,     // which layout the last expert FFN left h in (0: sorted rows, else padded tiles)
-  C_DC_READY = 8,  // tensor-core decode: blocks done with their router rows and quantisation slice
+  C_DC_READY = 8,  // tensor-core decode: blocks done with their quantisation slice
   C_DC_HSH = 9,    // tensor-core decode: shared-expert h tiles finished
   C_DC_HR = 10,    // tensor-core decode: routed h tiles finished
   C_DC_EXIT = 11,  // tensor-core decode: blocks finished
+  C_DC_EPOCH = 12, // tensor-core decode: launches completed on this workspace (tags the logits)
   N_COUNTERS = 16
 };
 
@@ -80,6 +81,7 @@ MOE_HD inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct WsLayout {
   size_t counters;     // int [N_COUNTERS]
   size_t dc_tickets;   // int: split-K arrival tickets of the tensor-core decode
+  size_t dc_logit64;   // uint64 [T, E]: tensor-core decode logits tagged with the launch number
   size_t zero_end;     // end of the part that must start zero-filled
   size_t logits;       // float [T, E]
   size_t ids;          // int [T, k]       (when the caller passes no output)
@@ -130,8 +132,13 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   const bool dc = T <= MAX_DECODE_T;
   const int nslot = imin(T * k, E);
   const DcSplits sp = dc_splits(T, H, I, E, k, DC_MAX_GRID);
+  // The regions the tensor-core decode needs zeroed (or tagged) across calls
+  // sit at the same offsets, sized for the whole decode range, in the layout
+  // of every T: no call of any size writes anything else there.
+  const int nslot_cap = imin(MAX_DECODE_T * k, E);
   L.counters = take(sizeof(int) * N_COUNTERS);
-  L.dc_tickets = take(dc ? sizeof(int) * ((size_t)(1 + nslot) * (I / 128) + H / 128) : 0);
+  L.dc_tickets = take(sizeof(int) * ((size_t)(1 + nslot_cap) * (I / 128) + H / 128));
+  L.dc_logit64 = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * E);
   L.zero_end = o;
   L.logits = take(sizeof(float) * (size_t)T * E);
   L.ids = take(sizeof(int) * n);

@@ -478,6 +478,27 @@ def test_tensor_core_decode_shapes(shape):
     assert normwise(bits_to_float(out), bits_to_float(out_c)) <= 1e-2
 
 
+def test_decode_after_large_forward_on_one_workspace():
+    """A workspace sized for a 300-token forward also serves decode steps:
+    the forward's scratch never lands where the decode expects its zeroed
+    tickets and launch-tagged logits."""
+    H, I, E, k = 512, 256, 16, 4
+    wl = W.Workload("mixed", 300, H, I, E, k, W.MXFP4, 26, 0.05)
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, H, I, E, k, wl.fmt, T_max=300)
+    cache = {}
+    for _ in range(2):
+        out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
+        torch.cuda.synchronize()
+        for T in (1, 5, 16):
+            sub = dict(lay)
+            sub["x"] = lay["x"][:T]
+            o, i, _ = dev.decode(bf16_tensor(sub["x"]))
+            torch.cuda.synchronize()
+            assert M.moe_get_status(dev.ws) == M.MOE_OK
+            _compare_layer(wl.with_tokens(T), sub, cache, o, i)
+
+
 def test_tensor_core_decode_without_shared_expert():
     wl = W.Workload("noshared_mx", 3, 512, 512, 16, 4, W.MXFP4, 25, 0.05, shared=False)
     lay = W.generate(wl)
