@@ -105,11 +105,10 @@ struct DcRouting {
   float w[MAXN];
   int inv[MAXN];          // assignment t*k+j -> sorted position
   int tok[MAXN];          // sorted position -> token
+  int sorted_e[MAXN];     // sorted position -> expert
   int slot_e[MAXN];       // slot -> expert (distinct experts, ascending)
   int slot_beg[MAXN + 1]; // slot -> first sorted position
-  int cnt[MAX_E];
-  int eoff[MAX_E];
-  int eslot[MAX_E];
+  int wcount[EPI_THREADS / 32];
   int n_slots;
 };
 
@@ -340,14 +339,14 @@ __device__ bool wait_logit_row(const DcArgs& a, int t, uint32_t epoch, float (&v
   }
 }
 
-// Top-k of every token (one epilogue warp per token), then the stable
-// counting sort of the T*k assignments by expert and the distinct-expert
-// slots.  128 epilogue threads, et = 0..127.  *failed is set (by some
-// thread) when a logit row never arrived.
+// Top-k of every token (one epilogue warp per token), then the stable sort
+// of the T*k <= 128 assignments by expert (each assignment counts the ones
+// that precede it) and the distinct-expert slots (runs of one expert in the
+// sorted order, numbered with a ballot).  128 epilogue threads, et = 0..127.
+// *failed is set (by some thread) when a logit row never arrived.
 __device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t epoch, int* failed) {
   const int T = a.T, E = a.E, k = a.k, n = T * k;
   const int w = et >> 5, lane = et & 31;
-  for (int e = et; e < E; e += EPI_THREADS) R.cnt[e] = 0;
   for (int t = w; t < T; t += EPI_THREADS / 32) {
     float v[8];
     if (!wait_logit_row(a, t, epoch, v)) {
@@ -367,49 +366,34 @@ __device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t ep
   }
   epi_sync();
   if (*failed) return;  // the same answer in every thread after the barrier
-  int e = -1, rank = 0;
   if (et < n) {
-    e = R.ids[et];
-    for (int b = 0; b < et; ++b) rank += R.ids[b] == e;
-    atomicAdd(&R.cnt[e], 1);
+    const int e = R.ids[et];
+    int pos = 0;
+    for (int b = 0; b < n; ++b) {
+      const int eb = R.ids[b];
+      pos += (eb < e) | ((eb == e) & (b < et));
+    }
+    R.inv[et] = pos;
+    R.tok[pos] = et / k;
+    R.sorted_e[pos] = e;
   }
   epi_sync();
-  if (w == 0) {
-    int run_c = 0, run_p = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int ex = base + lane;
-      const int c = ex < E ? R.cnt[ex] : 0;
-      int ic = c, ip = c > 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int yc = __shfl_up_sync(FULL, ic, o), yp = __shfl_up_sync(FULL, ip, o);
-        if (lane >= o) {
-          ic += yc;
-          ip += yp;
-        }
-      }
-      if (ex < E) {
-        R.eoff[ex] = run_c + ic - c;
-        R.eslot[ex] = run_p + ip - (c > 0);
-      }
-      run_c += __shfl_sync(FULL, ic, 31);
-      run_p += __shfl_sync(FULL, ip, 31);
-    }
-    if (lane == 0) {
-      R.n_slots = run_p;
-      R.slot_beg[run_p] = n;
-    }
-  }
+  const bool start = et < n && (et == 0 || R.sorted_e[et] != R.sorted_e[et - 1]);
+  const unsigned mask = __ballot_sync(FULL, start);
+  if (lane == 0) R.wcount[w] = __popc(mask);
   epi_sync();
-  if (et < n) {
-    R.inv[et] = R.eoff[e] + rank;
-    R.tok[R.eoff[e] + rank] = et / k;
+  int base = 0;
+  for (int ww = 0; ww < w; ++ww) base += R.wcount[ww];
+  if (start) {
+    const int slot = base + __popc(mask & ((1u << lane) - 1u));
+    R.slot_e[slot] = R.sorted_e[et];
+    R.slot_beg[slot] = et;
   }
-  for (int ex = et; ex < E; ex += EPI_THREADS) {
-    if (R.cnt[ex] > 0) {
-      R.slot_e[R.eslot[ex]] = ex;
-      R.slot_beg[R.eslot[ex]] = R.eoff[ex];
-    }
+  if (et == 0) {
+    int total = 0;
+    for (int ww = 0; ww < EPI_THREADS / 32; ++ww) total += R.wcount[ww];
+    R.n_slots = total;
+    R.slot_beg[total] = n;
   }
   epi_sync();
 }

@@ -34,7 +34,7 @@ cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* code
 
 // ------------------------------------------------------------------ A1
 
-// Decode-sized router: one block per (expert row, tile of 16 tokens); the 256
+// Router up to a few hundred tokens: one block per (expert row, tile of 16 tokens); the 256
 // threads stride over H eight elements at a time (two float4 of Wr, one uint4
 // of x per token), then reduce over lanes and warps in a fixed order.
 __global__ void __launch_bounds__(256) k_router_gemv(const uint16_t* __restrict__ x,
@@ -148,7 +148,9 @@ __global__ void __launch_bounds__(256) k_router_gemm(const uint16_t* __restrict_
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  if (T <= 64) {
+  // Up to a few hundred tokens one block per (expert row, 16 tokens) keeps
+  // every SM busy (the x re-reads hit L2); beyond that the tiled GEMM.
+  if (T <= 512) {
     dim3 grid(E, (T + 15) / 16);
     k_router_gemv<<<grid, 256, 0, s>>>(x, wr, bias, logits, T, H, E);
   } else {

@@ -125,7 +125,7 @@ def _router_gpu(x_bits, wr, bias, k, H, E):
     return ids.cpu().numpy(), w.cpu().numpy(), lg.cpu().numpy()
 
 
-@pytest.mark.parametrize("T", [5, 100])  # decode GEMV path and batched GEMM path
+@pytest.mark.parametrize("T", [5, 100, 700])  # per-row router (up to 512 tokens) and tiled GEMM
 def test_topk_bitexact_on_exactly_computed_logits(T):
     """x rows are one-hot (1.0 at h_t), so logits[t, e] = Wr[e, h_t] exactly on
     any summation order; the logits include exact ties."""
@@ -146,7 +146,7 @@ def test_topk_bitexact_on_exactly_computed_logits(T):
     assert np.allclose(w, rw, rtol=1e-6, atol=0)
 
 
-@pytest.mark.parametrize("wl_name,T", [("tiny", 16), ("decode1", 1), ("decode16z", 16), ("prefill8k", 300)])
+@pytest.mark.parametrize("wl_name,T", [("tiny", 16), ("decode1", 1), ("decode16z", 16), ("prefill8k", 300), ("prefill8k", 600)])
 def test_router_topk_random(wl_name, T):
     wl = W.WORKLOADS[wl_name]
     lay = W.generate(wl, tokens=T)
