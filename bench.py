@@ -233,6 +233,9 @@ def run_ours(args):
         else:
             lay.forward(xs[i], *outs[i])
 
+    # layers, inputs and outputs were made on the default stream
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         for i in range(Wm):  # untimed warm-up steps
             step(i % S)

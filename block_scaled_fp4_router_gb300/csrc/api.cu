@@ -47,7 +47,7 @@ moe_status_t check_experts(const moe_layer_desc_t* d, const moe_experts_t* ex, E
   }
   if ((ex->w13_scale_mma && !aligned(ex->w13_scale_mma, 16)) || (ex->w2_scale_mma && !aligned(ex->w2_scale_mma, 16)))
     return MOE_ERR_INVALID_ARG;
-  const bool prepared = !nv && ex->w13_scale_mma && ex->w2_scale_mma;
+  const bool prepared = ex->w13_scale_mma && ex->w2_scale_mma;
   *out = ExpertsDev{nv ? 1 : 0, ex->w13, ex->w13_scale, ex->w2, ex->w2_scale, ex->tensor_scale,
                     prepared ? ex->w13_scale_mma : nullptr, prepared ? ex->w2_scale_mma : nullptr};
   return MOE_OK;
@@ -151,13 +151,15 @@ moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts
   MOE_TRY(check_desc(desc));
   ExpertsDev ex;
   MOE_TRY(check_experts(desc, experts, &ex));
-  if (ex.nv) return MOE_ERR_UNSUPPORTED;
   if (!w13_scale_mma || !w2_scale_mma || !aligned(w13_scale_mma, 16) || !aligned(w2_scale_mma, 16) ||
       !aligned(ex.w13s, 4) || !aligned(ex.w2s, 4))
     return MOE_ERR_INVALID_ARG;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MOE_CUDA(launch_relayout_weight_sf(ex.w13s, desc->E, 2 * desc->I, desc->H, w13_scale_mma, s));
-  return cuda_status(launch_relayout_weight_sf(ex.w2s, desc->E, desc->H, desc->I, w2_scale_mma, s));
+  // Both formats keep 4 scale bytes per row per block column (128 elements of
+  // MXFP4, 64 of NVFP4): the NVFP4 re-layout is the MXFP4 one over 2K.
+  const int kf = ex.nv ? 2 : 1;
+  MOE_CUDA(launch_relayout_weight_sf(ex.w13s, desc->E, 2 * desc->I, kf * desc->H, w13_scale_mma, s));
+  return cuda_status(launch_relayout_weight_sf(ex.w2s, desc->E, desc->H, kf * desc->I, w2_scale_mma, s));
 }
 
 moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes, uint8_t* hq,

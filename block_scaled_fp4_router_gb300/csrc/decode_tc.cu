@@ -54,12 +54,18 @@ constexpr int DSTAGES = 2;
 // byte offsets inside one stage (swizzled tiles on 1024-byte boundaries)
 constexpr uint32_t ST_A0 = 0, ST_A1 = 16384;       // 128 rows x 128 B each
 constexpr uint32_t ST_B0 = 32768, ST_B1 = 34816;   // 16 rows x 128 B each
-constexpr uint32_t ST_SFA = 36864;                 // A0 scales (2 x 512 B), A1 scales (2 x 512 B)
-constexpr uint32_t ST_SFB = 38912;                 // B0 scales, B1 scales
-constexpr uint32_t STAGE_BYTES = 40960;
+// Scale blocks (512 B each): per 256-element K chunk and 128 rows, NBLK = 2
+// for MXFP4 (E8M0 per 32) or 4 for NVFP4 (UE4M3 per 16).  Tile / half h of a
+// stage keeps its blocks at ST_SFA / ST_SFB + h * NBLK * 512, and their TMEM
+// copies at columns +4 NBLK h (A) and +4 NBLK (2 + h) (B) of the stage's
+// 16 NBLK scale columns (stage s from column TM_SF + 16 NBLK s).
+constexpr uint32_t ST_SFA = 36864;
+template <bool NV> __host__ __device__ constexpr int nblk() { return NV ? 4 : 2; }
+template <bool NV> __host__ __device__ constexpr uint32_t st_sfb() { return ST_SFA + 2 * 512 * nblk<NV>(); }
+template <bool NV> __host__ __device__ constexpr uint32_t stage_bytes() { return st_sfb<NV>() + 2 * 512 * nblk<NV>(); }
 constexpr uint32_t A_TILE = 16384, B_TILE = 2048;
 constexpr uint32_t DC_TMEM_COLS = 256;
-constexpr uint32_t TM_SF = 64;          // scale columns of stage s: TM_SF + 32 s (+0 A0, +8 A1, +16 B0, +24 B1)
+constexpr uint32_t TM_SF = 64;
 constexpr int MAXN = MAX_DECODE_T * MAX_TOPK;
 
 enum UnitKind { U_SGU = 0, U_RGU = 1, U_SDN = 2, U_RDN = 3 };
@@ -71,8 +77,10 @@ struct DcArgs {
   int n_sgu, n_sdn;          // unit counts that do not depend on the routing
   int nslot_max;             // min(T k, E): ticket slots
   int shared;
+  int nv;                    // NVFP4 experts (UE4M3 scales per 16, FP32 tensor scales)
   const uint8_t* w13s_mma;   // prepared routed weight scales
   const uint8_t* w2s_mma;
+  const float* tscale;       // NVFP4: [E, 3] (gate, up, down)
   const float* wr;
   const float* bias;
   const uint16_t* x;
@@ -83,9 +91,11 @@ struct DcArgs {
   int* tickets;
   unsigned long long* logit64;  // [T, E]: (launch number << 32) | FP32 bits
   uint8_t* xq;               // [T, H/2]
-  uint8_t* xs_mma;           // [H/128][512]
+  uint8_t* xs_mma;           // [H/128][512] E8M0 (MXFP4) or [H/64][512] UE4M3 (NVFP4)
+  int* xshift;               // NVFP4: [16] per-row power of two of the UE4M3 x scales
+  unsigned long long* rowmax;  // NVFP4: [T k] (launch << 32) | (largest h scale exponent + 256)
   uint8_t* hq;               // [T k, I/2] sorted-assignment rows
-  uint8_t* hs_mma;           // [slots][I/128][512]
+  uint8_t* hs_mma;           // MXFP4: [slots][I/128][512]; NVFP4: E8M0 bytes [T k][I/32]
   uint16_t* h_shared;        // [T, I]
   float* gu_sh;              // [s_sgu][T][2I]
   float* gu_r;               // [s_rgu][T k][2I]
@@ -339,6 +349,82 @@ __device__ bool wait_logit_row(const DcArgs& a, int t, uint32_t epoch, float (&v
   }
 }
 
+// 2^p as a UE4M3 byte: normal for p >= -6, subnormal down to 2^-9, 0 below
+// (p <= 8 always: the row shift puts the largest block scale at 2^8).
+__device__ __forceinline__ uint32_t ue4m3_pow2(int p) {
+  if (p < -9) return 0u;
+  if (p < -6) return 1u << (p + 9);
+  return (uint32_t)(p + 7) << 3;
+}
+
+// 2^c as a float (c >= -149).
+__device__ __forceinline__ float pow2f(int c) {
+  return c >= -126 ? __uint_as_float((uint32_t)(c + 127) << 23) : __uint_as_float(1u << (c + 149));
+}
+
+// NVFP4 experts: one warp quantises token row t < 16 to MXFP4 (the same codes
+// and E8M0 exponents as the standalone quantiser) and writes the scales for
+// the UE4M3 MMA: each 32-block's 2^e twice (two 16-blocks) as 2^(e - c_t),
+// c_t = (largest e of the row) - 8, and c_t to xshift[t]; the epilogue
+// multiplies the row's products by 2^c_t.  A block more than 2^17 below the
+// row's largest block scale falls under UE4M3's range and is dropped.  Rows
+// t >= T get zero scale words.
+__device__ void quant_row_nv(const DcArgs& a, int t) {
+  const int lane = threadIdx.x & 31, nb = a.H / 32;
+  if (t >= a.T) {
+    for (int kb = lane; kb < a.H / 64; kb += 32) *reinterpret_cast<uint32_t*>(a.xs_mma + (size_t)kb * 512 + t * 16) = 0u;
+    return;
+  }
+  const uint16_t* xr = a.x + (size_t)t * a.H;
+  int emax = -127;
+  for (int b = lane; b < nb; b += 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(xr + b * 32);
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 w = __ldg(src + j);
+      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+    }
+    emax = max(emax, mx_scale_exp(amax));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) emax = max(emax, __shfl_xor_sync(FULL, emax, o));
+  const int c = emax - 8;
+  if (lane == 0) a.xshift[t] = c;
+  for (int b = lane; b < nb; b += 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(xr + b * 32);
+    uint4 raw[4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      raw[j] = __ldg(src + j);
+      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+    }
+    const int ex = mx_scale_exp(amax);
+    const float inv = pow2_neg(ex);
+    uint32_t cw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+      uint32_t word = 0;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        word |= e2m1_rne(bf16_lo(w4[h]) * inv) << (8 * h);
+        word |= e2m1_rne(bf16_hi(w4[h]) * inv) << (8 * h + 4);
+      }
+      cw[j] = word;
+    }
+    *reinterpret_cast<uint4*>(a.xq + (size_t)t * (a.H / 2) + b * 16) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    const uint32_t u = ue4m3_pow2(ex - c);
+    // bytes 2(b&1), 2(b&1)+1 of the word of row t in 64-element chunk b/2
+    *reinterpret_cast<uint16_t*>(a.xs_mma + (size_t)(b / 2) * 512 + t * 16 + 2 * (b & 1)) = (uint16_t)(u | (u << 8));
+  }
+}
+
 // Top-k of every token (one epilogue warp per token), then the stable sort
 // of the T*k <= 128 assignments by expert (each assignment counts the ones
 // that precede it) and the distinct-expert slots (runs of one expert in the
@@ -420,18 +506,24 @@ __device__ __forceinline__ int stage_halves(const DcArgs& a, const Unit& U, int 
   return 2;
 }
 
-// Bytes one stage of a unit brings in (the mbarrier transaction count).
+// Scale bytes per 128 rows and 256-element K chunk.
+template <bool NV> __device__ __forceinline__ constexpr uint32_t sf_chunk() { return 512u * nblk<NV>(); }
+
+// Bytes one stage of a unit brings in (the mbarrier transaction count); the
+// NVFP4 routed down unit's h scales are written by the producer thread, not copied.
+template <bool NV>
 __device__ __forceinline__ uint32_t stage_tx(const DcArgs& a, const Unit& U, int st) {
   const uint32_t h = stage_halves(a, U, st);
   switch (U.kind) {
     case U_SGU: return 2 * A_TILE + B_TILE;
-    case U_RGU: return 2 * A_TILE + B_TILE + 3 * 1024;
+    case U_RGU: return 2 * A_TILE + B_TILE + 3 * sf_chunk<NV>();
     case U_SDN: return h * (A_TILE + B_TILE);
-    default: return h * (A_TILE + B_TILE + 2048);
+    default: return h * (A_TILE + B_TILE + (NV ? 1u : 2u) * sf_chunk<NV>());
   }
 }
 
 // TMA / bulk copies of the weight tiles (and their scales) of stage st.
+template <bool NV>
 __device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, const Unit& U, int st, int e,
                                               uint8_t* sp, uint64_t* fb) {
   const int nbI = a.I / 128, nbH = a.H / 128;
@@ -440,12 +532,13 @@ __device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, 
     tc::tma_load_2d(sp + ST_A1, &m.w13s, st * 128, a.I + 128 * U.tile, fb);
   } else if (U.kind == U_RGU) {
     const int row = e * 2 * a.I + 128 * U.tile;
-    const size_t hg = a.H / 128;
-    const size_t rt = (size_t)e * (2 * nbI) + U.tile;  // gate row tile; the up tile is nbI further
+    const uint32_t sfc = sf_chunk<NV>();
+    const size_t bpr = (size_t)a.H / 256 * (sfc / 512);  // scale blocks per 128-row tile
+    const size_t rt = (size_t)e * (2 * nbI) + U.tile;    // gate row tile; the up tile is nbI further
     tc::tma_load_2d(sp + ST_A0, &m.w13r, st * 128, row, fb);
     tc::tma_load_2d(sp + ST_A1, &m.w13r, st * 128, row + a.I, fb);
-    tc::bulk_load(sp + ST_SFA, a.w13s_mma + (rt * hg + 2 * st) * 512, 1024, fb);
-    tc::bulk_load(sp + ST_SFA + 1024, a.w13s_mma + ((rt + nbI) * hg + 2 * st) * 512, 1024, fb);
+    tc::bulk_load(sp + ST_SFA, a.w13s_mma + rt * bpr * 512 + (size_t)st * sfc, sfc, fb);
+    tc::bulk_load(sp + ST_SFA + sfc, a.w13s_mma + (rt + nbI) * bpr * 512 + (size_t)st * sfc, sfc, fb);
   } else if (U.kind == U_SDN) {
     for (int h = 0; h < stage_halves(a, U, st); ++h)
       tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &m.w2s, (2 * st + h) * 128, 128 * U.tile, fb);
@@ -453,18 +546,21 @@ __device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, 
     const int halves = stage_halves(a, U, st);
     for (int h = 0; h < halves; ++h)
       tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &m.w2r, (2 * st + h) * 128, e * a.H + 128 * U.tile, fb);
-    tc::bulk_load(sp + ST_SFA, a.w2s_mma + (((size_t)e * nbH + U.tile) * (a.I / 128) + 4 * st) * 512, halves * 1024, fb);
+    const uint32_t sfc = sf_chunk<NV>();
+    const size_t bpr = (size_t)a.I / 256 * (sfc / 512);
+    tc::bulk_load(sp + ST_SFA, a.w2s_mma + ((size_t)e * nbH + U.tile) * bpr * 512 + (size_t)2 * st * sfc, halves * sfc, fb);
   }
 }
 
 // TMA / bulk copies of the activation tiles (and their scales) of stage st.
+template <bool NV>
 __device__ __forceinline__ void issue_acts(const DcArgs& a, const DcMaps& m, const Unit& U, int st, int beg,
                                            uint8_t* sp, uint64_t* fb) {
   if (U.kind == U_SGU) {
     tc::tma_load_2d(sp + ST_B0, &m.x, st * 128, 0, fb);
   } else if (U.kind == U_RGU) {
     tc::tma_load_2d(sp + ST_B0, &m.xq, st * 128, 0, fb);
-    tc::bulk_load(sp + ST_SFB, a.xs_mma + (size_t)2 * st * 512, 1024, fb);
+    tc::bulk_load(sp + st_sfb<NV>(), a.xs_mma + (size_t)st * sf_chunk<NV>(), sf_chunk<NV>(), fb);
   } else if (U.kind == U_SDN) {
     for (int h = 0; h < stage_halves(a, U, st); ++h)
       tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hsh, (2 * st + h) * 128, 0, fb);
@@ -472,13 +568,65 @@ __device__ __forceinline__ void issue_acts(const DcArgs& a, const DcMaps& m, con
     const int halves = stage_halves(a, U, st);
     for (int h = 0; h < halves; ++h)
       tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hq, (2 * st + h) * 128, beg, fb);
-    tc::bulk_load(sp + ST_SFB, a.hs_mma + ((size_t)U.slot * (a.I / 128) + 4 * st) * 512, halves * 1024, fb);
+    if (!NV)
+      tc::bulk_load(sp + st_sfb<NV>(), a.hs_mma + ((size_t)U.slot * (a.I / 128) + 4 * st) * 512, halves * 1024, fb);
+  }
+}
+
+// NVFP4 routed down, stage st: the UE4M3 scale blocks of the slot's h rows
+// (sorted positions beg .. beg+cnt-1), from their E8M0 bytes and the row
+// shift 2^c (c = largest exponent of the row - 8), written into the stage by
+// the producer thread before the stage's copies are issued.
+__device__ void build_h_scales_nv(const DcArgs& a, int st, int beg, int cnt, const int* cshift, uint8_t* sp) {
+  const int nb = a.I / 32;
+  const int halves = 2 * st + 1 < a.I / 256 ? 2 : 1;
+  for (int h = 0; h < halves; ++h)
+    for (int kb = 0; kb < 4; ++kb) {
+      const int g = 4 * (2 * st + h) + kb;  // 64-element chunk of I: 32-blocks 2g, 2g+1
+      uint8_t* blk = sp + st_sfb<true>() + h * 2048 + kb * 512;
+      for (int r = 0; r < 16; ++r) {
+        uint32_t word = 0;
+        if (r < cnt) {
+          const uint8_t* hsr = a.hs_mma + (size_t)(beg + r) * nb;
+          const uint32_t u0 = ue4m3_pow2((int)__ldcg(hsr + 2 * g) - 127 - cshift[r]);
+          const uint32_t u1 = ue4m3_pow2((int)__ldcg(hsr + 2 * g + 1) - 127 - cshift[r]);
+          word = u0 | (u0 << 8) | (u1 << 16) | (u1 << 24);
+        }
+        *reinterpret_cast<uint32_t*>(blk + r * 16) = word;
+      }
+    }
+  tc::fence_proxy_async_shared();
+}
+
+// Row shift c of sorted h row p (NVFP4), final once every routed h tile is done.
+__device__ __forceinline__ int h_row_shift(const DcArgs& a, int p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(a.rowmax + p) : "memory");
+  return (int)(uint32_t)v - 256 - 8;
+}
+
+// One FP4 MMA (M = 128, N = 16, K = 64, the kk-th of a 256-element chunk)
+// with the chunk's A / B scale tiles at TMEM columns sfa / sfb: MXFP4 reads
+// byte pair (kk & 1) of the 128-element group kk / 2, NVFP4 the whole word of
+// 64-element chunk kk.
+template <bool NV>
+__device__ __forceinline__ void fp4_mma(uint32_t d, uint64_t ad, uint64_t bd, int kk, uint32_t sfa, uint32_t sfb,
+                                        uint32_t accum) {
+  if (NV) {
+    tc::mma_nvf4(d, ad, bd, tc::idesc_nvf4(128, 16), sfa + 4 * kk, sfb + 4 * kk, accum);
+  } else {
+    const int grp = kk >> 1, id = (kk & 1) * 2;
+    tc::mma_mxf4(d, ad, bd, tc::idesc_mxf4(128, 16, id, id), sfa + 4 * grp, sfb + 4 * grp, accum);
   }
 }
 
 // ------------------------------------------------------------------ kernel
 
+template <bool NV>
 __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcMaps maps, const DcArgs a) {
+  constexpr uint32_t STAGE_BYTES = stage_bytes<NV>();
+  constexpr uint32_t ST_SFB = st_sfb<NV>();
+  constexpr int NB = nblk<NV>();
   extern __shared__ __align__(1024) uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[DSTAGES], empty[DSTAGES], acc_full[2], acc_empty[2], drain, routing_ready;
@@ -573,8 +721,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             bool ok = true;
             for (int j = 0; j < npre; ++j) {
               if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
-              tc::mbar_expect_tx(&full[stage], stage_tx(a, U, U.st0 + j));
-              issue_weights(a, maps, U, U.st0 + j, e, dsm + stage * STAGE_BYTES, &full[stage]);
+              tc::mbar_expect_tx(&full[stage], stage_tx<NV>(a, U, U.st0 + j));
+              issue_weights<NV>(a, maps, U, U.st0 + j, e, dsm + stage * STAGE_BYTES, &full[stage]);
               pre_stage[j] = stage;
               issued |= 1u << stage;
               last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -588,16 +736,26 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           }
           if (dep_sdn) hsh_ok = true; else hr_ok = true;
           tc::fence_proxy_async_global();
-          for (int j = 0; j < npre; ++j)
-            issue_acts(a, maps, U, U.st0 + j, beg, dsm + pre_stage[j] * STAGE_BYTES, &full[pre_stage[j]]);
+        }
+        int cnt = 0, cshift[MAX_DECODE_T];
+        const bool build_sfb = NV && U.kind == U_RDN;
+        if (build_sfb) {
+          cnt = R.slot_beg[U.slot + 1] - beg;
+          for (int r = 0; r < MAX_DECODE_T; ++r) cshift[r] = r < cnt ? h_row_shift(a, beg + r) : 0;
+        }
+        for (int j = 0; j < npre; ++j) {
+          uint8_t* sp = dsm + pre_stage[j] * STAGE_BYTES;
+          if (build_sfb) build_h_scales_nv(a, U.st0 + j, beg, cnt, cshift, sp);
+          issue_acts<NV>(a, maps, U, U.st0 + j, beg, sp, &full[pre_stage[j]]);
         }
         bool ok = true;
         for (int st = U.st0 + npre; st < U.st1; ++st) {
           if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
           uint8_t* sp = dsm + stage * STAGE_BYTES;
-          tc::mbar_expect_tx(&full[stage], stage_tx(a, U, st));
-          issue_weights(a, maps, U, st, e, sp, &full[stage]);
-          issue_acts(a, maps, U, st, beg, sp, &full[stage]);
+          if (build_sfb) build_h_scales_nv(a, st, beg, cnt, cshift, sp);
+          tc::mbar_expect_tx(&full[stage], stage_tx<NV>(a, U, st));
+          issue_weights<NV>(a, maps, U, st, e, sp, &full[stage]);
+          issue_acts<NV>(a, maps, U, st, beg, sp, &full[stage]);
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == DSTAGES) {
@@ -635,7 +793,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           if (!tc::mbar_wait(&full[stage], phase, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
           tc::fence_after_sync();
           const uint32_t sa = tc::smem_u32(dsm + stage * STAGE_BYTES);
-          const uint32_t tsf = tmem + TM_SF + 32 * stage;
+          const uint32_t tsf = tmem + TM_SF + 16 * NB * stage;
           const bool first = st == U.st0;
           if (U.kind == U_SGU) {
 #pragma unroll
@@ -646,21 +804,18 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               tc::mma_bf16(acc + 16, tc::desc_sw128(sa + ST_A1 + 32 * kk), bd, id_bf, accum);
             }
           } else if (U.kind == U_RGU) {
-            tc::sf_copy(tsf + 0, tc::desc_sf(sa + ST_SFA));
-            tc::sf_copy(tsf + 4, tc::desc_sf(sa + ST_SFA + 512));
-            tc::sf_copy(tsf + 8, tc::desc_sf(sa + ST_SFA + 1024));
-            tc::sf_copy(tsf + 12, tc::desc_sf(sa + ST_SFA + 1536));
-            tc::sf_copy(tsf + 16, tc::desc_sf(sa + ST_SFB));
-            tc::sf_copy(tsf + 20, tc::desc_sf(sa + ST_SFB + 512));
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              tc::sf_copy(tsf + 4 * b, tc::desc_sf(sa + ST_SFA + 512 * b));
+              tc::sf_copy(tsf + 4 * NB + 4 * b, tc::desc_sf(sa + ST_SFA + 512 * (NB + b)));
+              tc::sf_copy(tsf + 8 * NB + 4 * b, tc::desc_sf(sa + ST_SFB + 512 * b));
+            }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const int grp = kk >> 1, id = (kk & 1) * 2;
-              const uint32_t idesc = tc::idesc_mxf4(128, 16, id, id);
               const uint64_t bd = tc::desc_sw128(sa + ST_B0 + 32 * kk);
               const uint32_t accum = (first && kk == 0) ? 0u : 1u;
-              tc::mma_mxf4(acc, tc::desc_sw128(sa + ST_A0 + 32 * kk), bd, idesc, tsf + 4 * grp, tsf + 16 + 4 * grp, accum);
-              tc::mma_mxf4(acc + 16, tc::desc_sw128(sa + ST_A1 + 32 * kk), bd, idesc, tsf + 8 + 4 * grp,
-                           tsf + 16 + 4 * grp, accum);
+              fp4_mma<NV>(acc, tc::desc_sw128(sa + ST_A0 + 32 * kk), bd, kk, tsf, tsf + 8 * NB, accum);
+              fp4_mma<NV>(acc + 16, tc::desc_sw128(sa + ST_A1 + 32 * kk), bd, kk, tsf + 4 * NB, tsf + 8 * NB, accum);
             }
           } else if (U.kind == U_SDN) {
             const int halves = stage_halves(a, U, st);
@@ -674,20 +829,19 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             }
           } else {
             const int halves = stage_halves(a, U, st);
-            for (int h = 0; h < halves; ++h) {
-              tc::sf_copy(tsf + 8 * h, tc::desc_sf(sa + ST_SFA + 1024 * h));
-              tc::sf_copy(tsf + 8 * h + 4, tc::desc_sf(sa + ST_SFA + 1024 * h + 512));
-              tc::sf_copy(tsf + 16 + 8 * h, tc::desc_sf(sa + ST_SFB + 1024 * h));
-              tc::sf_copy(tsf + 16 + 8 * h + 4, tc::desc_sf(sa + ST_SFB + 1024 * h + 512));
-            }
+            for (int h = 0; h < halves; ++h)
+#pragma unroll
+              for (int b = 0; b < NB; ++b) {
+                tc::sf_copy(tsf + 4 * NB * h + 4 * b, tc::desc_sf(sa + ST_SFA + 512 * (NB * h + b)));
+                tc::sf_copy(tsf + 4 * NB * (2 + h) + 4 * b, tc::desc_sf(sa + ST_SFB + 512 * (NB * h + b)));
+              }
             for (int h = 0; h < halves; ++h) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const int grp = kk >> 1, id = (kk & 1) * 2;
                 const uint32_t accum = (first && h == 0 && kk == 0) ? 0u : 1u;
-                tc::mma_mxf4(acc, tc::desc_sw128(sa + (h ? ST_A1 : ST_A0) + 32 * kk),
-                             tc::desc_sw128(sa + (h ? ST_B1 : ST_B0) + 32 * kk), tc::idesc_mxf4(128, 16, id, id),
-                             tsf + 8 * h + 4 * grp, tsf + 16 + 8 * h + 4 * grp, accum);
+                fp4_mma<NV>(acc, tc::desc_sw128(sa + (h ? ST_A1 : ST_A0) + 32 * kk),
+                            tc::desc_sw128(sa + (h ? ST_B1 : ST_B0) + 32 * kk), kk, tsf + 4 * NB * h,
+                            tsf + 4 * NB * (2 + h), accum);
               }
             }
           }
@@ -714,9 +868,14 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
 
     const uint32_t epoch = s_epoch;
     for (int e = blockIdx.x; e < a.E; e += a.G) router_row(a, e, et, red_s, epoch);
-    const int nqb = MAX_DECODE_T * (H / 32);
     // the router rows go to the first E blocks, the quantisation to the last ones
-    for (int i = (a.G - 1 - blockIdx.x) * EPI_THREADS + et; i < nqb; i += a.G * EPI_THREADS) quant_block(a, i);
+    if (NV) {
+      const int t = (a.G - 1 - blockIdx.x) * (EPI_THREADS / 32) + (et >> 5);
+      if (t < MAX_DECODE_T) quant_row_nv(a, t);
+    } else {
+      const int nqb = MAX_DECODE_T * (H / 32);
+      for (int i = (a.G - 1 - blockIdx.x) * EPI_THREADS + et; i < nqb; i += a.G * EPI_THREADS) quant_block(a, i);
+    }
     tc::fence_proxy_async_global();
     epi_sync();  // orders every thread's stores before thread 0's release
     if (et == 0) red_release_add(a.ctr + C_DC_READY, 1);
@@ -767,11 +926,19 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           target = a.s_sgu;
         } else if (U.kind == U_RGU) {
           // B held every token row: slot row c is the column of its token
+          // (NVFP4: times the expert's gate / up tensor scale and 2^c_t)
           float* dst = a.gu_r + ((size_t)U.part * n + beg) * 2 * I + 128 * U.tile + m;
+          float sg = 1.0f, su = 1.0f;
+          if (NV) {
+            const int e = R.slot_e[U.slot];
+            sg = __ldg(a.tscale + 3 * e);
+            su = __ldg(a.tscale + 3 * e + 1);
+          }
           for (int c = 0; c < cnt; ++c) {
             const int t = R.tok[beg + c];
-            dst[(size_t)c * 2 * I] = pick16(v, 0, t);
-            dst[(size_t)c * 2 * I + I] = pick16(v, 16, t);
+            const float f = NV ? pow2f(__ldcg(a.xshift + t)) : 1.0f;
+            dst[(size_t)c * 2 * I] = pick16(v, 0, t) * (sg * f);
+            dst[(size_t)c * 2 * I + I] = pick16(v, 16, t) * (su * f);
           }
           ticket = nbI + U.slot * nbI + U.tile;
           target = a.s_rgu;
@@ -784,10 +951,12 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           target = dn_target;
         } else {
           // B held the slot's sorted rows: column c is sorted position beg + c
+          // (NVFP4: times the expert's down tensor scale and 2^c of the h row)
           float* dst = a.y_assign + (size_t)beg * H + 128 * U.tile + m;
+          const float sd = NV ? __ldg(a.tscale + 3 * R.slot_e[U.slot] + 2) : 1.0f;
 #pragma unroll
           for (int c = 0; c < MAX_DECODE_T; ++c)
-            if (c < cnt) dst[(size_t)c * H] = v[c];
+            if (c < cnt) dst[(size_t)c * H] = NV ? v[c] * (sd * pow2f(h_row_shift(a, beg + c))) : v[c];
           ticket = nbI * (1 + a.nslot_max) + U.tile;
           target = dn_target;
         }
@@ -837,12 +1006,23 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             wv |= __shfl_xor_sync(FULL, wv, 4);
             if ((lane & 7) == 0)
               *reinterpret_cast<uint32_t*>(a.hq + (size_t)(beg + c) * (I / 2) + 64 * U.tile + 16 * q + 4 * (lane >> 3)) = wv;
-            if (lane == 0) s_hsb[c * 4 + q] = (uint8_t)(ex + 127);
+            if (lane == 0) {
+              if (NV) {
+                // E8M0 byte of the block and the row's largest exponent so far
+                a.hs_mma[(size_t)(beg + c) * (I / 32) + 4 * U.tile + q] = (uint8_t)(ex + 127);
+                atomicMax(a.rowmax + beg + c, ((unsigned long long)epoch << 32) | (unsigned long long)(ex + 256));
+              } else {
+                s_hsb[c * 4 + q] = (uint8_t)(ex + 127);
+              }
+            }
           }
           epi_sync();
-          // the slot's scale block for this 128-column group: word 4c holds row c
-          const uint32_t word = ((et & 3) == 0 && (et >> 2) < cnt) ? reinterpret_cast<const uint32_t*>(s_hsb)[et >> 2] : 0u;
-          reinterpret_cast<uint32_t*>(a.hs_mma)[((size_t)U.slot * nbI + U.tile) * 128 + et] = word;
+          if (!NV) {
+            // the slot's scale block for this 128-column group: word 4c holds row c
+            const uint32_t word =
+                ((et & 3) == 0 && (et >> 2) < cnt) ? reinterpret_cast<const uint32_t*>(s_hsb)[et >> 2] : 0u;
+            reinterpret_cast<uint32_t*>(a.hs_mma)[((size_t)U.slot * nbI + U.tile) * 128 + et] = word;
+          }
           tc::fence_proxy_async_global();
           epi_sync();
           if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
@@ -899,8 +1079,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
 }  // namespace
 
 bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex) {
-  return !ex.nv && ex.w13s_mma && ex.w2s_mma && sh.T >= 1 && sh.T <= MAX_DECODE_T && sh.H % 256 == 0 &&
-         sh.I % 256 == 0;
+  return ex.w13s_mma && ex.w2s_mma && sh.T >= 1 && sh.T <= MAX_DECODE_T && sh.H % 256 == 0 && sh.I % 256 == 0;
 }
 
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
@@ -911,11 +1090,16 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   const int T = sh.T, H = sh.H, I = sh.I, E = sh.E, k = sh.k, n = T * k;
   const WsLayout L = ws_layout(T, H, I, E, k);
   uint8_t* base = static_cast<uint8_t*>(ws);
-  const size_t smem = (size_t)DSTAGES * STAGE_BYTES + 1024;
-  cudaError_t err = cudaFuncSetAttribute((const void*)k_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const bool nv = ex.nv != 0;
+  // One block per SM: the request covers the stage ring and leaves no room
+  // for a second block, whose TMA stream would share the SM's copy engine.
+  const size_t smem = 120 * 1024;
+  static_assert(DSTAGES * stage_bytes<true>() + 1024 <= 120 * 1024, "stage ring exceeds the shared-memory request");
+  auto kern = nv ? k_decode_tc<true> : k_decode_tc<false>;
+  cudaError_t err = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int per_sm = 0;
-  if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_tc, DT, smem)) != cudaSuccess) return err;
+  if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DT, smem)) != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // one block per SM: every block holds a 200 KB stage ring and a TMEM allocation
   const int G = imin(sm_count(), DC_MAX_GRID);
@@ -936,8 +1120,10 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.n_sdn = shared ? (H / 128) * sp.sdn : 0;
   a.nslot_max = imin(n, E);
   a.shared = shared ? 1 : 0;
+  a.nv = ex.nv;
   a.w13s_mma = ex.w13s_mma;
   a.w2s_mma = ex.w2s_mma;
+  a.tscale = ex.tscale;
   a.wr = wr;
   a.bias = bias;
   a.x = x;
@@ -949,6 +1135,8 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.logit64 = reinterpret_cast<unsigned long long*>(base + L.dc_logit64);
   a.xq = base + L.xq;
   a.xs_mma = base + L.dc_xs;
+  a.xshift = reinterpret_cast<int*>(base + L.dc_xshift);
+  a.rowmax = reinterpret_cast<unsigned long long*>(base + L.dc_rowmax);
   a.hq = base + L.hq;
   a.hs_mma = base + L.dc_hs;
   a.h_shared = reinterpret_cast<uint16_t*>(base + L.h_shared);
@@ -980,7 +1168,7 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode_tc, m, a);
+  return cudaLaunchKernelEx(&cfg, kern, m, a);
 }
 
 }  // namespace moefp4

@@ -82,6 +82,7 @@ struct WsLayout {
   size_t counters;     // int [N_COUNTERS]
   size_t dc_tickets;   // int: split-K arrival tickets of the tensor-core decode
   size_t dc_logit64;   // uint64 [T, E]: tensor-core decode logits tagged with the launch number
+  size_t dc_rowmax;    // uint64 [T*k]: NVFP4 h row exponents tagged with the launch number
   size_t zero_end;     // end of the part that must start zero-filled
   size_t logits;       // float [T, E]
   size_t ids;          // int [T, k]       (when the caller passes no output)
@@ -111,7 +112,8 @@ struct WsLayout {
   size_t tc_w13s;      // weight scale blocks [E][2I/128][H/128][512 B]
   size_t tc_w2s;       // weight scale blocks [E][H/128][I/128][512 B]
   // tensor-core decode (T <= MAX_DECODE_T)
-  size_t dc_xs;        // x scales, MMA layout [H/128][512 B] (16 token rows)
+  size_t dc_xs;        // x scales, MMA layout [H/128][512 B] (E8M0) or [H/64][512 B] (UE4M3), 16 token rows
+  size_t dc_xshift;    // int [16]: NVFP4 per-row power of two of the x scales
   size_t dc_hs;        // routed h scales, MMA layout [slots][I/128][512 B]
   size_t dc_gu_sh;     // float [splits][T][2I]  shared gate/up partial sums
   size_t dc_gu_r;      // float [splits][T*k][2I] routed gate/up partial sums
@@ -139,6 +141,7 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.counters = take(sizeof(int) * N_COUNTERS);
   L.dc_tickets = take(sizeof(int) * ((size_t)(1 + nslot_cap) * (I / 128) + H / 128));
   L.dc_logit64 = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * E);
+  L.dc_rowmax = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * MAX_TOPK);
   L.zero_end = o;
   L.logits = take(sizeof(float) * (size_t)T * E);
   L.ids = take(sizeof(int) * n);
@@ -168,7 +171,8 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.tc_hs = take(R * I / 32);
   L.tc_w13s = take(tc ? (size_t)E * 2 * I * H / 32 : 0);
   L.tc_w2s = take(tc ? (size_t)E * H * I / 32 : 0);
-  L.dc_xs = take(dc ? (size_t)H / 128 * 512 : 0);
+  L.dc_xs = take(dc ? (size_t)H / 64 * 512 : 0);
+  L.dc_xshift = take(dc ? sizeof(int) * MAX_DECODE_T : 0);
   L.dc_hs = take(dc ? (size_t)nslot * (I / 128) * 512 : 0);
   L.dc_gu_sh = take(dc ? sizeof(float) * sp.sgu * T * 2 * (size_t)I : 0);
   L.dc_gu_r = take(dc ? sizeof(float) * sp.rgu * n * 2 * (size_t)I : 0);

@@ -18,7 +18,10 @@
 //    .32x128b.warpx4 produces exactly this from a 512-byte block whose 16-byte
 //    row i is {word(row i), word(row 32+i), word(row 64+i), word(row 96+i)}.
 //    A tile's column address must be a multiple of 4; with .scale_vec::2X an
-//    MMA of K = 64 reads bytes (id, id+1), id = 0 or 2.
+//    MMA of K = 64 reads bytes (id, id+1), id = 0 or 2;
+//  * with kind::mxf4nvf4 .scale_vec::4X (UE4M3 scales per 16 elements, scale
+//    type bit 23 = 0) one 4-column tile serves one MMA of K = 64: lane i,
+//    column j holds the four scales of row 32j + i for that K chunk.
 #pragma once
 
 #include <cuda.h>
@@ -106,6 +109,11 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// The same for shared memory: plain stores a tcgen05 copy of this block reads.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -151,6 +159,10 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int sfa_id, int 
          ((uint32_t)(M >> 4) << 24) | ((uint32_t)(sfa_id & 3) << 29);
 }
 
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
@@ -162,6 +174,16 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint6
   asm volatile(
       "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
+// FP4 x FP4 with UE4M3 scales per 16 elements (NVFP4).
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
 }

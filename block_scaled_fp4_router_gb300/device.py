@@ -26,7 +26,7 @@ def _to_dev(a, device, dtype=None):
 class DeviceLayer:
     """One layer's weights on the GPU plus a workspace sized for up to T_max tokens.
 
-    MXFP4 layers also get the tensor-core copy of their scales
+    Layers also get the tensor-core copy of their scales
     (moe_prepare_weights) unless prepare=False; set_prepared() switches
     between the two descriptions of the same weights."""
 
@@ -48,7 +48,7 @@ class DeviceLayer:
         wfmt = MOE_W_MXFP4 if fmt == "mxfp4" else MOE_W_NVFP4
         self.ex_plain = experts(wfmt, self.w13, self.w13_scale, self.w2, self.w2_scale, self.tensor_scale)
         self.ex_prepared = None
-        if prepare and fmt == "mxfp4":
+        if prepare:
             self.w13_scale_mma = torch.empty_like(self.w13_scale)
             self.w2_scale_mma = torch.empty_like(self.w2_scale)
             moe_prepare_weights(desc(0, H, I, E, top_k), self.ex_plain, self.w13_scale_mma, self.w2_scale_mma)
@@ -59,6 +59,9 @@ class DeviceLayer:
         self.T_max = T_max
         nbytes = moe_workspace_size(desc(T_max, H, I, E, top_k))
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=d)
+        # The zero fill and the scale re-layout ran on the current stream: make
+        # them complete before a call on any other stream can read them.
+        torch.cuda.synchronize(d)
 
     @property
     def prepared(self) -> bool:
@@ -67,7 +70,7 @@ class DeviceLayer:
     def set_prepared(self, on: bool):
         """Use the prepared scales (tensor-core decode) or only the canonical ones."""
         if on and self.ex_prepared is None:
-            raise ValueError("this layer has no prepared scales (NVFP4, or prepare=False)")
+            raise ValueError("this layer has no prepared scales (prepare=False)")
         self.ex = self.ex_prepared if on else self.ex_plain
 
     def desc(self, T: int):

@@ -100,7 +100,7 @@ typedef struct {
 
 /* Routed-expert weights (device pointers, layouts above).  The two *_mma
  * fields are optional copies of the scale bytes in the tensor-core layout
- * written by moe_prepare_weights (MXFP4 only; NULL = not prepared). */
+ * written by moe_prepare_weights (NULL = not prepared). */
 typedef struct {
   moe_wfmt_t fmt;
   const uint8_t* w13;
@@ -125,17 +125,20 @@ MOE_API const char* moe_status_string(moe_status_t st);
  * (the maximum over all of them).  desc must be valid. */
 MOE_API moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* bytes);
 
-/* Load-time re-layout of MXFP4 expert scales for the tensor-core paths (the
- * pages convert expert weights at load time: AMD article, section "Enabling
- * the MXFP4 checkpoint with the AMD Quark"; vLLM PR #64273, section
- * "Purpose").  Writes the E8M0 scale bytes of W13 and W2 again, in blocks of
- * 128 rows x 128 K elements (512 bytes each, word (i, j) at byte 16 i + 4 j
- * holding the 4 scales of row 32 j + i), block order [E][rows/128][K/128]:
- *   w13_scale_mma  out, E * 2I * H/32 bytes;  w2_scale_mma  out, E * H * I/32 bytes
- * (16-byte aligned).  Point experts->w13_scale_mma / w2_scale_mma at them
- * afterwards: moe_layer_decode then runs its contractions on tensor cores
- * (when H and I are multiples of 256), and the batched path skips its
- * per-call re-layout.  NVFP4 returns MOE_ERR_UNSUPPORTED. */
+/* Load-time re-layout of expert scales for the tensor-core paths (the pages
+ * convert expert weights at load time: AMD article, section "Enabling the
+ * MXFP4 checkpoint with the AMD Quark"; vLLM PR #64273, section "Purpose").
+ * Writes the scale bytes of W13 and W2 again, in blocks of 128 rows x 128 K
+ * elements (MXFP4, E8M0 per 32) or 128 rows x 64 K elements (NVFP4, E4M3 per
+ * 16): 512 bytes each, word (i, j) at byte 16 i + 4 j holding the 4 scales of
+ * row 32 j + i, block order [E][rows/128][K blocks]; the same byte counts as
+ * the canonical scales:
+ *   w13_scale_mma  out, E * 2I * H/32 (MXFP4) or E * 2I * H/16 (NVFP4) bytes
+ *   w2_scale_mma   out, E * H * I/32 (MXFP4) or E * H * I/16 (NVFP4) bytes
+ * (16-byte aligned; the canonical scales 4-byte aligned).  Point
+ * experts->w13_scale_mma / w2_scale_mma at them afterwards: moe_layer_decode
+ * then runs its contractions on tensor cores (when H and I are multiples of
+ * 256), and the MXFP4 batched path skips its per-call re-layout. */
 MOE_API moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts_t* experts,
                                          uint8_t* w13_scale_mma, uint8_t* w2_scale_mma, moe_stream_t stream);
 

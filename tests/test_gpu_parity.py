@@ -310,9 +310,7 @@ def test_expert_ffn_contractions(name):
 
 
 def _use_prepared(dev, prepared):
-    """Selects the tensor-core decode (prepared MXFP4 scales) or the CUDA-core one."""
-    if prepared and dev.ex_prepared is None:
-        pytest.skip("NVFP4 experts have no tensor-core decode")
+    """Selects the tensor-core decode (prepared scales) or the CUDA-core one."""
     dev.set_prepared(prepared)
 
 
@@ -345,6 +343,10 @@ def test_prepared_scales_are_the_tensor_core_layout():
 
     assert np.array_equal(dev.w13_scale_mma.cpu().numpy().reshape(-1), relayout(lay["w13_scale"], 2 * I, H))
     assert np.array_equal(dev.w2_scale_mma.cpu().numpy().reshape(-1), relayout(lay["w2_scale"], H, I))
+    # NVFP4: E4M3 per 16, so 4 bytes of a row cover 64 elements (the same map over 2K)
+    wl16, lay16, dev16, _ = _workload("decode16")
+    E, H, I = wl16.E, wl16.H, wl16.I
+    assert np.array_equal(dev16.w2_scale_mma.cpu().numpy().reshape(-1), relayout(lay16["w2_scale"], H, 2 * I))
 
 @pytest.mark.parametrize("name", ["tiny", "decode1", "decode16"])
 def test_layer_forward_matches_decode(name):
@@ -456,14 +458,15 @@ def test_small_and_degenerate_shapes(shape):
     _compare_layer(wl, lay, cache, out, ids)
 
 
-@pytest.mark.parametrize("shape", [(5, 256, 256, 256, 8), (16, 256, 512, 4, 4), (1, 768, 768, 8, 2),
-                                   (11, 1024, 256, 64, 6)])
+@pytest.mark.parametrize("shape", [(5, 256, 256, 256, 8, W.MXFP4), (16, 256, 512, 4, 4, W.MXFP4),
+                                   (1, 768, 768, 8, 2, W.MXFP4), (11, 1024, 256, 64, 6, W.MXFP4),
+                                   (6, 768, 512, 24, 4, W.NVFP4), (16, 256, 256, 256, 8, W.NVFP4)])
 def test_tensor_core_decode_shapes(shape):
     """The tcgen05 decode on E = 256 with k = 8, a dense mixture (E == k) at
-    16 tokens, odd numbers of K chunks (H = I = 768) and a mid-size case;
-    the CUDA-core decode on the same layer agrees."""
-    T, H, I, E, k = shape
-    wl = W.Workload("dcedge", T, H, I, E, k, W.MXFP4, 24, 0.5)
+    16 tokens, odd numbers of K chunks (H = I = 768), a mid-size case and two
+    NVFP4 layers; the CUDA-core decode on the same layer agrees."""
+    T, H, I, E, k, fmt = shape
+    wl = W.Workload("dcedge", T, H, I, E, k, fmt, 24, 0.5)
     lay = W.generate(wl)
     dev = DeviceLayer(lay, H, I, E, k, wl.fmt, T_max=T)
     cache = {}
