@@ -29,8 +29,9 @@
 // build the routing (top-k, sort by expert) in shared memory and release the
 // producer and MMA warps onto the routed units.  While the routing is not yet
 // known the producers pull the shared down-projection weights into L2, and
-// once it is known the routed down-projection weights, so that HBM keeps
-// streaming across the dependencies between the steps.
+// once it is known the routed down-projection weights (up to a byte budget
+// well inside L2), so that HBM keeps streaming across the dependencies
+// between the steps.
 //
 // Every wait is bounded (MOE_DEV_TIMEOUT in the status word); the last block
 // out resets the counters, and each finishing block resets its ticket.
@@ -95,7 +96,9 @@ struct DcArgs {
   int* xshift;               // NVFP4: [16] per-row power of two of the UE4M3 x scales
   unsigned long long* rowmax;  // NVFP4: [T k] (launch << 32) | (largest h scale exponent + 256)
   uint8_t* hq;               // [T k, I/2] sorted-assignment rows
-  uint8_t* hs_mma;           // MXFP4: [slots][I/128][512]; NVFP4: E8M0 bytes [T k][I/32]
+  uint8_t* hs_mma;           // [slots][I/128][512] E8M0 (MXFP4) or [slots][I/64][512] UE4M3 (NVFP4)
+  uint8_t* hsc;              // NVFP4: E8M0 bytes of h [T k][I/32]
+  size_t rdn_prefetch_units; // routed down units whose weights go to L2 early (a byte budget)
   uint16_t* h_shared;        // [T, I]
   float* gu_sh;              // [s_sgu][T][2I]
   float* gu_r;               // [s_rgu][T k][2I]
@@ -222,7 +225,7 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 }
 
 // Router row e for all tokens (FP32 weights and accumulation), 128 threads.
-// Tokens go in groups of 4; within a group every load of a pass (4 x 8
+// Tokens go in groups of 8; within a group every load of a pass (4 x 8
 // elements per thread) is in flight before the FMAs, since these loads
 // compete with the weight streams for HBM.
 __device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DECODE_T], uint32_t epoch) {
@@ -230,8 +233,11 @@ __device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DE
   const int w = et >> 5, lane = et & 31;
   constexpr int PASS = EPI_THREADS * 8;
   const float* wrow = a.wr + (size_t)e * H;
-  for (int t0 = 0; t0 < T; t0 += 4) {
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  constexpr int TG = 8;
+  for (int t0 = 0; t0 < T; t0 += TG) {
+    float acc[TG];
+#pragma unroll
+    for (int tt = 0; tt < TG; ++tt) acc[tt] = 0.0f;
     for (int k0 = et * 8; k0 < H; k0 += 4 * PASS) {
       uint4 wv[8];
 #pragma unroll
@@ -241,7 +247,7 @@ __device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DE
         wv[2 * c + 1] = kk < H ? __ldg(reinterpret_cast<const uint4*>(wrow + kk + 4)) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int tt = 0; tt < 4; ++tt) {
+      for (int tt = 0; tt < TG; ++tt) {
         if (t0 + tt < T) {
           const uint16_t* xr = a.x + (size_t)(t0 + tt) * H;
           uint4 xv[4];
@@ -268,7 +274,7 @@ __device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DE
       }
     }
 #pragma unroll
-    for (int tt = 0; tt < 4; ++tt) {
+    for (int tt = 0; tt < TG; ++tt) {
       const float v = warp_sum(acc[tt]);
       if (lane == 0 && t0 + tt < T) red_s[w][t0 + tt] = v;
     }
@@ -368,8 +374,9 @@ __device__ __forceinline__ float pow2f(int c) {
 // c_t = (largest e of the row) - 8, and c_t to xshift[t]; the epilogue
 // multiplies the row's products by 2^c_t.  A block more than 2^17 below the
 // row's largest block scale falls under UE4M3's range and is dropped.  Rows
-// t >= T get zero scale words.
-__device__ void quant_row_nv(const DcArgs& a, int t) {
+// t >= T get zero scale words.  Lane l takes blocks l, l+32, ... in batches
+// of 4 with all their loads in flight; the exponents wait in e_s (H <= 8192).
+__device__ void quant_row_nv(const DcArgs& a, int t, uint8_t* e_s) {
   const int lane = threadIdx.x & 31, nb = a.H / 32;
   if (t >= a.T) {
     for (int kb = lane; kb < a.H / 64; kb += 32) *reinterpret_cast<uint32_t*>(a.xs_mma + (size_t)kb * 512 + t * 16) = 0u;
@@ -377,50 +384,54 @@ __device__ void quant_row_nv(const DcArgs& a, int t) {
   }
   const uint16_t* xr = a.x + (size_t)t * a.H;
   int emax = -127;
-  for (int b = lane; b < nb; b += 32) {
-    const uint4* src = reinterpret_cast<const uint4*>(xr + b * 32);
-    float amax = 0.0f;
+  for (int b0 = lane; b0 < nb; b0 += 4 * 32) {
+    uint4 raw[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4 w = __ldg(src + j);
-      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+      const int b = b0 + 32 * j;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+      for (int q = 0; q < 4; ++q)
+        raw[j][q] = b < nb ? __ldg(reinterpret_cast<const uint4*>(xr + b * 32) + q) : make_uint4(0, 0, 0, 0);
     }
-    emax = max(emax, mx_scale_exp(amax));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int b = b0 + 32 * j;
+      float amax = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w4[4] = {raw[j][q].x, raw[j][q].y, raw[j][q].z, raw[j][q].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+      }
+      const int ex = mx_scale_exp(amax);
+      const float inv = pow2_neg(ex);
+      uint32_t cw[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w4[4] = {raw[j][q].x, raw[j][q].y, raw[j][q].z, raw[j][q].w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          word |= e2m1_rne(bf16_lo(w4[h]) * inv) << (8 * h);
+          word |= e2m1_rne(bf16_hi(w4[h]) * inv) << (8 * h + 4);
+        }
+        cw[q] = word;
+      }
+      if (b < nb) {
+        *reinterpret_cast<uint4*>(a.xq + (size_t)t * (a.H / 2) + b * 16) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        e_s[b] = (uint8_t)(ex + 127);
+        emax = max(emax, ex);
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) emax = max(emax, __shfl_xor_sync(FULL, emax, o));
   const int c = emax - 8;
   if (lane == 0) a.xshift[t] = c;
+  __syncwarp();
+  // bytes 2(b&1), 2(b&1)+1 of the word of row t in 64-element chunk b/2
   for (int b = lane; b < nb; b += 32) {
-    const uint4* src = reinterpret_cast<const uint4*>(xr + b * 32);
-    uint4 raw[4];
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      raw[j] = __ldg(src + j);
-      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
-    }
-    const int ex = mx_scale_exp(amax);
-    const float inv = pow2_neg(ex);
-    uint32_t cw[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-      uint32_t word = 0;
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        word |= e2m1_rne(bf16_lo(w4[h]) * inv) << (8 * h);
-        word |= e2m1_rne(bf16_hi(w4[h]) * inv) << (8 * h + 4);
-      }
-      cw[j] = word;
-    }
-    *reinterpret_cast<uint4*>(a.xq + (size_t)t * (a.H / 2) + b * 16) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    const uint32_t u = ue4m3_pow2(ex - c);
-    // bytes 2(b&1), 2(b&1)+1 of the word of row t in 64-element chunk b/2
+    const uint32_t u = ue4m3_pow2((int)e_s[b] - 127 - c);
     *reinterpret_cast<uint16_t*>(a.xs_mma + (size_t)(b / 2) * 512 + t * 16 + 2 * (b & 1)) = (uint16_t)(u | (u << 8));
   }
 }
@@ -509,8 +520,7 @@ __device__ __forceinline__ int stage_halves(const DcArgs& a, const Unit& U, int 
 // Scale bytes per 128 rows and 256-element K chunk.
 template <bool NV> __device__ __forceinline__ constexpr uint32_t sf_chunk() { return 512u * nblk<NV>(); }
 
-// Bytes one stage of a unit brings in (the mbarrier transaction count); the
-// NVFP4 routed down unit's h scales are written by the producer thread, not copied.
+// Bytes one stage of a unit brings in (the mbarrier transaction count).
 template <bool NV>
 __device__ __forceinline__ uint32_t stage_tx(const DcArgs& a, const Unit& U, int st) {
   const uint32_t h = stage_halves(a, U, st);
@@ -518,7 +528,7 @@ __device__ __forceinline__ uint32_t stage_tx(const DcArgs& a, const Unit& U, int
     case U_SGU: return 2 * A_TILE + B_TILE;
     case U_RGU: return 2 * A_TILE + B_TILE + 3 * sf_chunk<NV>();
     case U_SDN: return h * (A_TILE + B_TILE);
-    default: return h * (A_TILE + B_TILE + (NV ? 1u : 2u) * sf_chunk<NV>());
+    default: return h * (A_TILE + B_TILE + 2 * sf_chunk<NV>());
   }
 }
 
@@ -568,37 +578,36 @@ __device__ __forceinline__ void issue_acts(const DcArgs& a, const DcMaps& m, con
     const int halves = stage_halves(a, U, st);
     for (int h = 0; h < halves; ++h)
       tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hq, (2 * st + h) * 128, beg, fb);
-    if (!NV)
-      tc::bulk_load(sp + st_sfb<NV>(), a.hs_mma + ((size_t)U.slot * (a.I / 128) + 4 * st) * 512, halves * 1024, fb);
+    const size_t bpr = (size_t)a.I / 256 * nblk<NV>();  // scale blocks of one slot
+    tc::bulk_load(sp + st_sfb<NV>(), a.hs_mma + (size_t)U.slot * bpr * 512 + (size_t)2 * st * sf_chunk<NV>(),
+                  halves * sf_chunk<NV>(), fb);
   }
 }
 
-// NVFP4 routed down, stage st: the UE4M3 scale blocks of the slot's h rows
-// (sorted positions beg .. beg+cnt-1), from their E8M0 bytes and the row
-// shift 2^c (c = largest exponent of the row - 8), written into the stage by
-// the producer thread before the stage's copies are issued.
-__device__ void build_h_scales_nv(const DcArgs& a, int st, int beg, int cnt, const int* cshift, uint8_t* sp) {
-  const int nb = a.I / 32;
-  const int halves = 2 * st + 1 < a.I / 256 ? 2 : 1;
-  for (int h = 0; h < halves; ++h)
-    for (int kb = 0; kb < 4; ++kb) {
-      const int g = 4 * (2 * st + h) + kb;  // 64-element chunk of I: 32-blocks 2g, 2g+1
-      uint8_t* blk = sp + st_sfb<true>() + h * 2048 + kb * 512;
-      for (int r = 0; r < 16; ++r) {
-        uint32_t word = 0;
-        if (r < cnt) {
-          const uint8_t* hsr = a.hs_mma + (size_t)(beg + r) * nb;
-          const uint32_t u0 = ue4m3_pow2((int)__ldcg(hsr + 2 * g) - 127 - cshift[r]);
-          const uint32_t u1 = ue4m3_pow2((int)__ldcg(hsr + 2 * g + 1) - 127 - cshift[r]);
-          word = u0 | (u0 << 8) | (u1 << 16) | (u1 << 24);
-        }
-        *reinterpret_cast<uint32_t*>(blk + r * 16) = word;
-      }
+// Row shift c of sorted h row p (NVFP4), final once every routed h tile is done.
+__device__ __forceinline__ int h_row_shift(const DcArgs& a, int p);
+
+// NVFP4: the UE4M3 scale blocks of slot s's h rows (sorted positions beg ..
+// beg+cnt-1) for the down MMA, [I/64][512 B], from their E8M0 bytes and the
+// row shift 2^c (c = the row's largest exponent - 8).  128 threads; thread
+// et writes word et of every block (row et/4 when et % 4 == 0, else zero).
+__device__ void convert_h_scales_nv(const DcArgs& a, int slot, int beg, int cnt, int et) {
+  const int nb = a.I / 32, r = et >> 2;
+  const bool real = (et & 3) == 0 && r < cnt;
+  const int c = real ? h_row_shift(a, beg + r) : 0;
+  const uint8_t* hsr = a.hsc + (size_t)(beg + (real ? r : 0)) * nb;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(a.hs_mma) + (size_t)slot * (a.I / 64) * 128 + et;
+  for (int g = 0; g < a.I / 64; ++g) {
+    uint32_t word = 0;
+    if (real) {
+      const uint32_t u0 = ue4m3_pow2((int)__ldcg(hsr + 2 * g) - 127 - c);
+      const uint32_t u1 = ue4m3_pow2((int)__ldcg(hsr + 2 * g + 1) - 127 - c);
+      word = u0 | (u0 << 8) | (u1 << 16) | (u1 << 24);
     }
-  tc::fence_proxy_async_shared();
+    dst[(size_t)g * 128] = word;
+  }
 }
 
-// Row shift c of sorted h row p (NVFP4), final once every routed h tile is done.
 __device__ __forceinline__ int h_row_shift(const DcArgs& a, int p) {
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(a.rowmax + p) : "memory");
@@ -636,6 +645,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
   __shared__ DcRouting R;
   __shared__ float red_s[EPI_THREADS / 32][MAX_DECODE_T];
   __shared__ __align__(4) uint8_t s_hsb[MAX_DECODE_T * 4];
+  __shared__ uint8_t s_qe[EPI_THREADS / 32][256];  // NVFP4 quantiser: a row's block exponents
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nbI = a.I / 128, nbH = a.H / 128;
   int* status = a.ctr + C_STATUS;
@@ -694,7 +704,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           if (!wait_at_least(a.ctr + C_DC_READY, a.G, status, a.limit_ns)) { fail(); break; }
           tc::fence_proxy_async_global();
           // The routed down weights are known now: into L2 while the gate/up streams run.
-          const int n_rdn = n_slots * nbH;
+          const int n_rdn = imin(n_slots * nbH, (int)a.rdn_prefetch_units);
           for (int v = blockIdx.x; v < n_rdn; v += a.G) {
             const Unit D = rdn_unit(a, n_slots, v);
             prefetch_down_unit(a, maps, D, R.slot_e[D.slot]);
@@ -715,7 +725,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         const bool dep_sdn = U.kind == U_SDN && !hsh_ok, dep_rdn = U.kind == U_RDN && !hr_ok;
         if (dep_sdn || dep_rdn) {
           int* cnt = a.ctr + (dep_sdn ? C_DC_HSH : C_DC_HR);
-          const int target = dep_sdn ? nbI : n_slots * nbI;
+          const int target = dep_sdn ? nbI : (NV ? n_slots : n_slots * nbI);
           if (ld_acquire(cnt) < target) {
             npre = imin(U.st1 - U.st0, DSTAGES);
             bool ok = true;
@@ -737,22 +747,12 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           if (dep_sdn) hsh_ok = true; else hr_ok = true;
           tc::fence_proxy_async_global();
         }
-        int cnt = 0, cshift[MAX_DECODE_T];
-        const bool build_sfb = NV && U.kind == U_RDN;
-        if (build_sfb) {
-          cnt = R.slot_beg[U.slot + 1] - beg;
-          for (int r = 0; r < MAX_DECODE_T; ++r) cshift[r] = r < cnt ? h_row_shift(a, beg + r) : 0;
-        }
-        for (int j = 0; j < npre; ++j) {
-          uint8_t* sp = dsm + pre_stage[j] * STAGE_BYTES;
-          if (build_sfb) build_h_scales_nv(a, U.st0 + j, beg, cnt, cshift, sp);
-          issue_acts<NV>(a, maps, U, U.st0 + j, beg, sp, &full[pre_stage[j]]);
-        }
+        for (int j = 0; j < npre; ++j)
+          issue_acts<NV>(a, maps, U, U.st0 + j, beg, dsm + pre_stage[j] * STAGE_BYTES, &full[pre_stage[j]]);
         bool ok = true;
         for (int st = U.st0 + npre; st < U.st1; ++st) {
           if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
           uint8_t* sp = dsm + stage * STAGE_BYTES;
-          if (build_sfb) build_h_scales_nv(a, st, beg, cnt, cshift, sp);
           tc::mbar_expect_tx(&full[stage], stage_tx<NV>(a, U, st));
           issue_weights<NV>(a, maps, U, st, e, sp, &full[stage]);
           issue_acts<NV>(a, maps, U, st, beg, sp, &full[stage]);
@@ -871,7 +871,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     // the router rows go to the first E blocks, the quantisation to the last ones
     if (NV) {
       const int t = (a.G - 1 - blockIdx.x) * (EPI_THREADS / 32) + (et >> 5);
-      if (t < MAX_DECODE_T) quant_row_nv(a, t);
+      if (t < MAX_DECODE_T) quant_row_nv(a, t, s_qe[et >> 5]);
     } else {
       const int nqb = MAX_DECODE_T * (H / 32);
       for (int i = (a.G - 1 - blockIdx.x) * EPI_THREADS + et; i < nqb; i += a.G * EPI_THREADS) quant_block(a, i);
@@ -1009,7 +1009,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             if (lane == 0) {
               if (NV) {
                 // E8M0 byte of the block and the row's largest exponent so far
-                a.hs_mma[(size_t)(beg + c) * (I / 32) + 4 * U.tile + q] = (uint8_t)(ex + 127);
+                a.hsc[(size_t)(beg + c) * (I / 32) + 4 * U.tile + q] = (uint8_t)(ex + 127);
                 atomicMax(a.rowmax + beg + c, ((unsigned long long)epoch << 32) | (unsigned long long)(ex + 256));
               } else {
                 s_hsb[c * 4 + q] = (uint8_t)(ex + 127);
@@ -1022,10 +1022,29 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             const uint32_t word =
                 ((et & 3) == 0 && (et >> 2) < cnt) ? reinterpret_cast<const uint32_t*>(s_hsb)[et >> 2] : 0u;
             reinterpret_cast<uint32_t*>(a.hs_mma)[((size_t)U.slot * nbI + U.tile) * 128 + et] = word;
+            tc::fence_proxy_async_global();
+            epi_sync();
+            if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
+          } else {
+            // NVFP4: the slot's last finished tile knows every row's largest
+            // exponent and writes the slot's UE4M3 scale blocks for the down MMA
+            if (et == 0) {
+              __threadfence();
+              const int old = atomicAdd(a.tickets + nbI * (1 + a.nslot_max) + nbH + U.slot, 1);
+              s_last = old == nbI - 1;
+              if (s_last) {
+                a.tickets[nbI * (1 + a.nslot_max) + nbH + U.slot] = 0;
+                __threadfence();
+              }
+            }
+            epi_sync();
+            if (s_last) {
+              convert_h_scales_nv(a, U.slot, beg, cnt, et);
+              tc::fence_proxy_async_global();
+              epi_sync();
+              if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
+            }
           }
-          tc::fence_proxy_async_global();
-          epi_sync();
-          if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
         } else {
           // out = BF16(ys + sum_j w_j y_j), summed in a fixed order
           const int col = 128 * U.tile + m;
@@ -1079,7 +1098,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
 }  // namespace
 
 bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex) {
-  return ex.w13s_mma && ex.w2s_mma && sh.T >= 1 && sh.T <= MAX_DECODE_T && sh.H % 256 == 0 && sh.I % 256 == 0;
+  return ex.w13s_mma && ex.w2s_mma && sh.T >= 1 && sh.T <= MAX_DECODE_T && sh.H % 256 == 0 && sh.I % 256 == 0 &&
+         (!ex.nv || sh.H <= 8192);  // the NVFP4 quantiser keeps a row's 32-block exponents in shared memory
 }
 
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
@@ -1136,6 +1156,10 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.xq = base + L.xq;
   a.xs_mma = base + L.dc_xs;
   a.xshift = reinterpret_cast<int*>(base + L.dc_xshift);
+  a.hsc = base + L.dc_hsc;
+  // routed down weights pulled into L2 ahead of use: at most 48 MB
+  const size_t rdn_unit_bytes = (size_t)128 * I / 2 + (size_t)128 * I / (ex.nv ? 16 : 32);
+  a.rdn_prefetch_units = ((size_t)48 << 20) / rdn_unit_bytes;
   a.rowmax = reinterpret_cast<unsigned long long*>(base + L.dc_rowmax);
   a.hq = base + L.hq;
   a.hs_mma = base + L.dc_hs;

@@ -114,7 +114,8 @@ struct WsLayout {
   // tensor-core decode (T <= MAX_DECODE_T)
   size_t dc_xs;        // x scales, MMA layout [H/128][512 B] (E8M0) or [H/64][512 B] (UE4M3), 16 token rows
   size_t dc_xshift;    // int [16]: NVFP4 per-row power of two of the x scales
-  size_t dc_hs;        // routed h scales, MMA layout [slots][I/128][512 B]
+  size_t dc_hs;        // routed h scales, MMA layout [slots][I/128][512 B] (E8M0) or [slots][I/64][512 B] (UE4M3)
+  size_t dc_hsc;       // NVFP4: E8M0 bytes of h [T*k][I/32] before the per-row UE4M3 conversion
   size_t dc_gu_sh;     // float [splits][T][2I]  shared gate/up partial sums
   size_t dc_gu_r;      // float [splits][T*k][2I] routed gate/up partial sums
   size_t dc_ys;        // float [splits][T][H]   shared down partial sums
@@ -139,7 +140,7 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   // of every T: no call of any size writes anything else there.
   const int nslot_cap = imin(MAX_DECODE_T * k, E);
   L.counters = take(sizeof(int) * N_COUNTERS);
-  L.dc_tickets = take(sizeof(int) * ((size_t)(1 + nslot_cap) * (I / 128) + H / 128));
+  L.dc_tickets = take(sizeof(int) * ((size_t)(1 + nslot_cap) * (I / 128) + H / 128 + nslot_cap));
   L.dc_logit64 = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * E);
   L.dc_rowmax = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * MAX_TOPK);
   L.zero_end = o;
@@ -173,7 +174,8 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.tc_w2s = take(tc ? (size_t)E * H * I / 32 : 0);
   L.dc_xs = take(dc ? (size_t)H / 64 * 512 : 0);
   L.dc_xshift = take(dc ? sizeof(int) * MAX_DECODE_T : 0);
-  L.dc_hs = take(dc ? (size_t)nslot * (I / 128) * 512 : 0);
+  L.dc_hs = take(dc ? (size_t)nslot * (I / 64) * 512 : 0);
+  L.dc_hsc = take(dc ? n * (I / 32) : 0);
   L.dc_gu_sh = take(dc ? sizeof(float) * sp.sgu * T * 2 * (size_t)I : 0);
   L.dc_gu_r = take(dc ? sizeof(float) * sp.rgu * n * 2 * (size_t)I : 0);
   L.dc_ys = take(dc ? sizeof(float) * sp.sdn * T * (size_t)H : 0);
