@@ -48,10 +48,12 @@ namespace {
 
 constexpr int DT = 192;                 // threads: TMA warp, MMA warp, 4 epilogue warps
 constexpr int EPI_THREADS = 128;
-// Two stages (~68 KB in flight per SM, ~10 MB over the GPU) already cover
-// HBM's bandwidth-latency product; a deeper ring only lengthens the queues
-// that the latency-bound hand-offs between the steps wait in.
-constexpr int DSTAGES = 2;
+// A 4-stage ring, of which the host lets `depth` stages be in flight: two
+// (~70-90 KB per SM, ~10-13 MB over the GPU) cover HBM's bandwidth-latency
+// product for a 1-4 token step, where a deeper queue would only slow the
+// latency-bound hand-offs between the steps; four for the larger steps,
+// which stream hundreds of MB.
+constexpr int DSTAGES = 4;
 // byte offsets inside one stage (swizzled tiles on 1024-byte boundaries)
 constexpr uint32_t ST_A0 = 0, ST_A1 = 16384;       // 128 rows x 128 B each
 constexpr uint32_t ST_B0 = 32768, ST_B1 = 34816;   // 16 rows x 128 B each
@@ -65,8 +67,11 @@ template <bool NV> __host__ __device__ constexpr int nblk() { return NV ? 4 : 2;
 template <bool NV> __host__ __device__ constexpr uint32_t st_sfb() { return ST_SFA + 2 * 512 * nblk<NV>(); }
 template <bool NV> __host__ __device__ constexpr uint32_t stage_bytes() { return st_sfb<NV>() + 2 * 512 * nblk<NV>(); }
 constexpr uint32_t A_TILE = 16384, B_TILE = 2048;
-constexpr uint32_t DC_TMEM_COLS = 256;
-constexpr uint32_t TM_SF = 64;
+// TMEM: NACC 32-column accumulators (the MMA runs up to NACC units ahead of
+// the epilogue), then 16 NBLK scale columns per stage.
+constexpr int NACC = 4;
+template <bool NV> __host__ __device__ constexpr uint32_t tmem_cols() { return NV ? 512u : 256u; }
+constexpr uint32_t TM_SF = 32 * NACC;
 constexpr int MAXN = MAX_DECODE_T * MAX_TOPK;
 
 enum UnitKind { U_SGU = 0, U_RGU = 1, U_SDN = 2, U_RDN = 3 };
@@ -99,6 +104,7 @@ struct DcArgs {
   uint8_t* hs_mma;           // [slots][I/128][512] E8M0 (MXFP4) or [slots][I/64][512] UE4M3 (NVFP4)
   uint8_t* hsc;              // NVFP4: E8M0 bytes of h [T k][I/32]
   size_t rdn_prefetch_units; // routed down units whose weights go to L2 early (a byte budget)
+  int depth;                 // stages in flight (<= DSTAGES)
   uint16_t* h_shared;        // [T, I]
   float* gu_sh;              // [s_sgu][T][2I]
   float* gu_r;               // [s_rgu][T k][2I]
@@ -385,43 +391,41 @@ __device__ void quant_row_nv(const DcArgs& a, int t, uint8_t* e_s) {
   const uint16_t* xr = a.x + (size_t)t * a.H;
   int emax = -127;
   for (int b0 = lane; b0 < nb; b0 += 4 * 32) {
-    uint4 raw[4][4];
+    uint4 raw[16];  // 4 blocks: every load issued before any is used
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int b = b0 + 32 * j;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        raw[j][q] = b < nb ? __ldg(reinterpret_cast<const uint4*>(xr + b * 32) + q) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 16; ++i) {
+      const int b = b0 + 32 * (i >> 2);
+      raw[i] = b < nb ? __ldg(reinterpret_cast<const uint4*>(xr + b * 32) + (i & 3)) : make_uint4(0, 0, 0, 0);
     }
-#pragma unroll
+    // compact loops: this runs once per launch, where instruction fetch is slow
+#pragma unroll 1
     for (int j = 0; j < 4; ++j) {
       const int b = b0 + 32 * j;
+      if (b >= nb) break;
       float amax = 0.0f;
-#pragma unroll
+#pragma unroll 1
       for (int q = 0; q < 4; ++q) {
-        const uint32_t w4[4] = {raw[j][q].x, raw[j][q].y, raw[j][q].z, raw[j][q].w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+        const uint4 w = raw[4 * j + q];
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))), fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))), fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w)))));
       }
       const int ex = mx_scale_exp(amax);
       const float inv = pow2_neg(ex);
-      uint32_t cw[4];
-#pragma unroll
+      uint32_t* dst = reinterpret_cast<uint32_t*>(a.xq + (size_t)t * (a.H / 2) + b * 16);
+#pragma unroll 1
       for (int q = 0; q < 4; ++q) {
-        const uint32_t w4[4] = {raw[j][q].x, raw[j][q].y, raw[j][q].z, raw[j][q].w};
+        const uint4 w = raw[4 * j + q];
+        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
         uint32_t word = 0;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           word |= e2m1_rne(bf16_lo(w4[h]) * inv) << (8 * h);
           word |= e2m1_rne(bf16_hi(w4[h]) * inv) << (8 * h + 4);
         }
-        cw[q] = word;
+        dst[q] = word;
       }
-      if (b < nb) {
-        *reinterpret_cast<uint4*>(a.xq + (size_t)t * (a.H / 2) + b * 16) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        e_s[b] = (uint8_t)(ex + 127);
-        emax = max(emax, ex);
-      }
+      e_s[b] = (uint8_t)(ex + 127);
+      emax = max(emax, ex);
     }
   }
 #pragma unroll
@@ -638,7 +642,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
   constexpr int NB = nblk<NV>();
   extern __shared__ __align__(1024) uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full[DSTAGES], empty[DSTAGES], acc_full[2], acc_empty[2], drain, routing_ready;
+  __shared__ uint64_t full[DSTAGES], empty[DSTAGES], acc_full[NACC], acc_empty[NACC], drain, routing_ready;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag, s_ok, s_last, s_fail;
   __shared__ uint32_t s_epoch;
@@ -655,7 +659,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NACC; ++b) {
       tc::mbar_init(&acc_full[b], 1);
       tc::mbar_init(&acc_empty[b], EPI_THREADS);
     }
@@ -666,7 +670,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     s_fail = 0;
     s_epoch = (uint32_t)ld_acquire(a.ctr + C_DC_EPOCH) + 1u;
   }
-  if (warp == 1) tc::tmem_alloc(&tmem_base, DC_TMEM_COLS);
+  if (warp == 1) tc::tmem_alloc(&tmem_base, tmem_cols<NV>());
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -680,7 +684,14 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
       const int never = 0;
-      uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
+      uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0, gi = 0;
+      // Stage gi may be issued once stage gi - depth has been consumed (which
+      // also frees slot gi % DSTAGES: depth <= DSTAGES, consumption in order).
+      auto claim = [&]() -> bool {
+        if (gi < (uint32_t)a.depth) return true;
+        const uint32_t j = gi - (uint32_t)a.depth;
+        return tc::mbar_wait(&empty[j % DSTAGES], (j / DSTAGES) & 1, a.limit_ns, &abort_flag);
+      };
       int n_slots = -1;
       bool hsh_ok = false, hr_ok = false;
       tc::prefetch_tensormap(&maps.w13r);
@@ -727,15 +738,16 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           int* cnt = a.ctr + (dep_sdn ? C_DC_HSH : C_DC_HR);
           const int target = dep_sdn ? nbI : (NV ? n_slots : n_slots * nbI);
           if (ld_acquire(cnt) < target) {
-            npre = imin(U.st1 - U.st0, DSTAGES);
+            npre = imin(U.st1 - U.st0, a.depth);
             bool ok = true;
             for (int j = 0; j < npre; ++j) {
-              if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
+              if (!claim()) { fail(); ok = false; break; }
               tc::mbar_expect_tx(&full[stage], stage_tx<NV>(a, U, U.st0 + j));
               issue_weights<NV>(a, maps, U, U.st0 + j, e, dsm + stage * STAGE_BYTES, &full[stage]);
               pre_stage[j] = stage;
               issued |= 1u << stage;
               last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+              ++gi;
               if (++stage == DSTAGES) {
                 stage = 0;
                 phase ^= 1;
@@ -751,13 +763,14 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           issue_acts<NV>(a, maps, U, U.st0 + j, beg, dsm + pre_stage[j] * STAGE_BYTES, &full[pre_stage[j]]);
         bool ok = true;
         for (int st = U.st0 + npre; st < U.st1; ++st) {
-          if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.limit_ns, &abort_flag)) { fail(); ok = false; break; }
+          if (!claim()) { fail(); ok = false; break; }
           uint8_t* sp = dsm + stage * STAGE_BYTES;
           tc::mbar_expect_tx(&full[stage], stage_tx<NV>(a, U, st));
           issue_weights<NV>(a, maps, U, st, e, sp, &full[stage]);
           issue_acts<NV>(a, maps, U, st, beg, sp, &full[stage]);
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          ++gi;
           if (++stage == DSTAGES) {
             stage = 0;
             phase ^= 1;
@@ -783,8 +796,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         }
         if (u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
         const Unit U = unit_at(a, n_slots < 0 ? 0 : n_slots, u);
-        const int buf = i & 1;
-        const uint32_t use = (uint32_t)(i >> 1);
+        const int buf = i % NACC;
+        const uint32_t use = (uint32_t)(i / NACC);
         if (!tc::mbar_wait(&acc_empty[buf], (use & 1) ^ 1, a.limit_ns, &abort_flag)) { fail(); break; }
         tc::fence_after_sync();
         const uint32_t acc = tmem + 32 * buf;
@@ -890,12 +903,12 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       }
       const int n_slots = R.n_slots;
       const int total = units_total(a, n_slots);
-      const int dn_target = (a.shared ? a.s_sdn : 0) + n_slots;
+      const int dn_total = nbH * ((a.shared ? a.s_sdn : 0) + n_slots);  // down parts over all tiles
       int i = 0;
       for (int u = blockIdx.x; u < total; u += a.G, ++i) {
         const Unit U = unit_at(a, n_slots, u);
-        const int buf = i & 1;
-        const uint32_t use = (uint32_t)(i >> 1);
+        const int buf = i % NACC;
+        const uint32_t use = (uint32_t)(i / NACC);
         if (et == 0) {
           s_ok = tc::mbar_wait(&acc_full[buf], use & 1, a.limit_ns, &abort_flag);
           if (!s_ok) fail();
@@ -947,8 +960,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
 #pragma unroll
           for (int t = 0; t < MAX_DECODE_T; ++t)
             if (t < T) dst[(size_t)t * H] = v[t];
-          ticket = nbI * (1 + a.nslot_max) + U.tile;
-          target = dn_target;
+          ticket = -1;
+          target = 0;
         } else {
           // B held the slot's sorted rows: column c is sorted position beg + c
           // (NVFP4: times the expert's down tensor scale and 2^c of the h row)
@@ -957,22 +970,31 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
 #pragma unroll
           for (int c = 0; c < MAX_DECODE_T; ++c)
             if (c < cnt) dst[(size_t)c * H] = NV ? v[c] * (sd * pow2f(h_row_shift(a, beg + c))) : v[c];
-          ticket = nbI * (1 + a.nslot_max) + U.tile;
-          target = dn_target;
+          ticket = -1;
+          target = 0;
         }
-        // split-K arrival: the block that brings the last part finishes the tile
-        epi_sync();
-        if (et == 0) {
-          __threadfence();
-          const int old = atomicAdd(a.tickets + ticket, 1);
-          s_last = old == target - 1;
-          if (s_last) {
-            a.tickets[ticket] = 0;
+        if (ticket < 0) {
+          // a down part: counted without waiting; the combine runs after the unit list
+          epi_sync();
+          if (et == 0) red_release_add(a.ctr + C_DC_DN, 1);
+          continue;
+        }
+        // split-K arrival: the block that brings the last part finishes the
+        // tile (a tile of one part needs no ticket: its own stores precede)
+        if (target > 1) {
+          epi_sync();
+          if (et == 0) {
             __threadfence();
+            const int old = atomicAdd(a.tickets + ticket, 1);
+            s_last = old == target - 1;
+            if (s_last) {
+              a.tickets[ticket] = 0;
+              __threadfence();
+            }
           }
+          epi_sync();
+          if (!s_last) continue;
         }
-        epi_sync();
-        if (!s_last) continue;
         if (U.kind == U_SGU) {
           const float* src = a.gu_sh + 128 * U.tile + m;
           const size_t stride = (size_t)T * 2 * I;
@@ -1045,29 +1067,39 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
             }
           }
-        } else {
-          // out = BF16(ys + sum_j w_j y_j), summed in a fixed order
-          const int col = 128 * U.tile + m;
-          for (int t0 = 0; t0 < T; t0 += 4) {  // four tokens' loads in flight together
-            float y[4][MAX_TOPK], ysh[4];
+        }
+      }
+      // out = BF16(ys + sum_j w_j y_j), summed in a fixed order, for the
+      // 128-row tiles of H this block owns, once every down part is stored
+      for (int tile = blockIdx.x; tile < nbH; tile += a.G) {
+        if (et == 0) {
+          s_ok = wait_at_least(a.ctr + C_DC_DN, dn_total, status, a.limit_ns);
+          if (!s_ok) fail();
+        }
+        epi_sync();
+        const bool ok = s_ok;
+        epi_sync();  // every thread has read s_ok before thread 0 writes it again
+        if (!ok) break;
+        const int col = 128 * tile + m;
+        for (int t0 = 0; t0 < T; t0 += 4) {  // four tokens' loads in flight together
+          float y[4][MAX_TOPK], ysh[4];
 #pragma unroll
-            for (int tt = 0; tt < 4; ++tt) {
-              const int t = imin(t0 + tt, T - 1);
+          for (int tt = 0; tt < 4; ++tt) {
+            const int t = imin(t0 + tt, T - 1);
+#pragma unroll
+            for (int j = 0; j < MAX_TOPK; ++j)
+              y[tt][j] = j < k ? __ldcg(a.y_assign + (size_t)R.inv[t * k + j] * H + col) : 0.0f;
+            ysh[tt] = a.shared ? sum_parts<4>(a.ys + (size_t)t * H + col, (size_t)T * H, a.s_sdn) : 0.0f;
+          }
+#pragma unroll
+          for (int tt = 0; tt < 4; ++tt) {
+            const int t = t0 + tt;
+            if (t < T) {
+              float acc = ysh[tt];
 #pragma unroll
               for (int j = 0; j < MAX_TOPK; ++j)
-                y[tt][j] = j < k ? __ldcg(a.y_assign + (size_t)R.inv[t * k + j] * H + col) : 0.0f;
-              ysh[tt] = a.shared ? sum_parts<4>(a.ys + (size_t)t * H + col, (size_t)T * H, a.s_sdn) : 0.0f;
-            }
-#pragma unroll
-            for (int tt = 0; tt < 4; ++tt) {
-              const int t = t0 + tt;
-              if (t < T) {
-                float acc = ysh[tt];
-#pragma unroll
-                for (int j = 0; j < MAX_TOPK; ++j)
-                  if (j < k) acc = fmaf(R.w[t * k + j], y[tt][j], acc);
-                a.out[(size_t)t * H + col] = f32_to_bf16_rn(acc);
-              }
+                if (j < k) acc = fmaf(R.w[t * k + j], y[tt][j], acc);
+              a.out[(size_t)t * H + col] = f32_to_bf16_rn(acc);
             }
           }
         }
@@ -1079,7 +1111,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, DC_TMEM_COLS);
+    tc::tmem_dealloc(tmem, tmem_cols<NV>());
   }
   // The last block out resets the launch's counters for the next call.
   if (threadIdx.x == 0) {
@@ -1089,6 +1121,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       a.ctr[C_DC_HSH] = 0;
       a.ctr[C_DC_HR] = 0;
       a.ctr[C_DC_EXIT] = 0;
+      a.ctr[C_DC_DN] = 0;
       a.ctr[C_DC_EPOCH] = (int)s_epoch;
       __threadfence();
     }
@@ -1111,10 +1144,10 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   const WsLayout L = ws_layout(T, H, I, E, k);
   uint8_t* base = static_cast<uint8_t*>(ws);
   const bool nv = ex.nv != 0;
-  // One block per SM: the request covers the stage ring and leaves no room
-  // for a second block, whose TMA stream would share the SM's copy engine.
-  const size_t smem = 120 * 1024;
-  static_assert(DSTAGES * stage_bytes<true>() + 1024 <= 120 * 1024, "stage ring exceeds the shared-memory request");
+  // One block per SM: the stage ring leaves no room for a second block,
+  // whose TMA stream would share the SM's copy engine.
+  const size_t smem = (size_t)DSTAGES * (nv ? stage_bytes<true>() : stage_bytes<false>()) + 1024;
+  static_assert(DSTAGES * stage_bytes<false>() + 1024 > 114 * 1024, "the ring must keep one block per SM");
   auto kern = nv ? k_decode_tc<true> : k_decode_tc<false>;
   cudaError_t err = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
@@ -1160,6 +1193,7 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   // routed down weights pulled into L2 ahead of use: at most 48 MB
   const size_t rdn_unit_bytes = (size_t)128 * I / 2 + (size_t)128 * I / (ex.nv ? 16 : 32);
   a.rdn_prefetch_units = ((size_t)48 << 20) / rdn_unit_bytes;
+  a.depth = a.nslot_max >= 16 ? 4 : 2;
   a.rowmax = reinterpret_cast<unsigned long long*>(base + L.dc_rowmax);
   a.hq = base + L.hq;
   a.hs_mma = base + L.dc_hs;

@@ -72,6 +72,7 @@ enum Counter : int {
   C_DC_HR = 10,    // tensor-core decode: routed h tiles finished
   C_DC_EXIT = 11,  // tensor-core decode: blocks finished
   C_DC_EPOCH = 12, // tensor-core decode: launches completed on this workspace (tags the logits)
+  C_DC_DN = 13,    // tensor-core decode: down-projection parts stored
   N_COUNTERS = 16
 };
 
