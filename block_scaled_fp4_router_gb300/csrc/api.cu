@@ -205,7 +205,7 @@ moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const 
   const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
   float* lg = logits ? logits : at<float>(ws, L.logits);
   MOE_CUDA(launch_router_logits(static_cast<const uint16_t*>(x), w_router, bias, lg, desc->T, desc->H,
-                                desc->E, s));
+                                desc->E, at<float>(ws, L.rt_part), s));
   return cuda_status(launch_topk(lg, desc->T, desc->E, desc->top_k, topk_ids, topk_w, s));
 }
 
@@ -271,7 +271,8 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_experts_t
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   int* ids = topk_ids ? topk_ids : at<int>(ws, L.ids);
   float* w = topk_w ? topk_w : at<float>(ws, L.wts);
-  MOE_CUDA(launch_router_logits(xb, w_router, bias, at<float>(ws, L.logits), sh.T, sh.H, sh.E, s));
+  MOE_CUDA(launch_router_logits(xb, w_router, bias, at<float>(ws, L.logits), sh.T, sh.H, sh.E,
+                                at<float>(ws, L.rt_part), s));
   MOE_CUDA(launch_topk(at<float>(ws, L.logits), sh.T, sh.E, sh.k, ids, w, s));
   MOE_CUDA(launch_quant_mxfp4(xb, sh.T, sh.H, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), s));
   MOE_CUDA(launch_permute(ids, sh.T, sh.k, sh.E, at<int>(ws, L.counts), at<int>(ws, L.offsets),

@@ -35,7 +35,7 @@ cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* code
                                cudaStream_t s);
 // A1
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
-                                 int T, int H, int E, cudaStream_t s);
+                                 int T, int H, int E, float* part, cudaStream_t s);  // part: [router_splits][T][E]
 // A2
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s);
 // A3

@@ -49,6 +49,15 @@ MOE_HD inline DcSplits dc_splits(int T, int H, int I, int E, int k, int grid) {
   return d;
 }
 
+// Split-K parts of the batched router (T > 512): enough 128 x 128 tiles for
+// two blocks per SM of a 152-SM GPU, at most 8.
+MOE_HD inline int router_splits(int T, int E) {
+  if (T <= 512) return 1;
+  const int tiles = ((T + 127) / 128) * ((E + 127) / 128);
+  int s = (304 + tiles - 1) / tiles;
+  return s < 1 ? 1 : (s > 8 ? 8 : s);
+}
+
 // Rows of the per-expert padded order (each expert's rows rounded up to 128).
 MOE_HD inline int tc_padded_rows(int n, int E) { return ((n + E * 127) + 127) / 128 * 128; }
 MOE_HD inline bool tc_routed_enabled(int n) { return n >= TC_MIN_ASSIGN; }
@@ -86,6 +95,7 @@ struct WsLayout {
   size_t dc_rowmax;    // uint64 [T*k]: NVFP4 h row exponents tagged with the launch number
   size_t zero_end;     // end of the part that must start zero-filled
   size_t logits;       // float [T, E]
+  size_t rt_part;      // float [splits, T, E]: split-K parts of the batched router
   size_t ids;          // int [T, k]       (when the caller passes no output)
   size_t wts;          // float [T, k]
   size_t xq;           // uint8 [T, H/2]
@@ -146,6 +156,8 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.dc_rowmax = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * MAX_TOPK);
   L.zero_end = o;
   L.logits = take(sizeof(float) * (size_t)T * E);
+  const int rs = router_splits(T, E);
+  L.rt_part = take(rs > 1 ? sizeof(float) * rs * (size_t)T * E : 0);
   L.ids = take(sizeof(int) * n);
   L.wts = take(sizeof(float) * n);
   L.xq = take((size_t)T * H / 2);

@@ -85,78 +85,116 @@ __global__ void __launch_bounds__(256) k_router_gemv(const uint16_t* __restrict_
   }
 }
 
-// Batched router: a 64-token x 64-expert tile per block, K staged 32 at a
-// time through shared memory, 4x4 outputs per thread, FP32 FMA in k order.
-constexpr int RBM = 64, RBN = 64, RBK = 32;
-__global__ void __launch_bounds__(256) k_router_gemm(const uint16_t* __restrict__ x,
-                                                     const float* __restrict__ wr,
-                                                     const float* __restrict__ bias,
-                                                     float* __restrict__ logits, int T, int H, int E) {
-  __shared__ float xs_[RBK][RBM + 4];
-  __shared__ float ws_[RBK][RBN + 4];
-  const int m0 = blockIdx.x * RBM, n0 = blockIdx.y * RBN;
-  const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;  // 16 x 16 threads, 4x4 outputs each
-  float acc[4][4] = {};
-  // loaders: x tile 64 rows x 32 bf16 -> thread loads 8 bf16 (row tid/4, cols (tid%4)*8)
-  const int lr = tid >> 2, lc = (tid & 3) * 8;
-  for (int k0 = 0; k0 < H; k0 += RBK) {
-    {
-      const int m = m0 + lr;
-      uint4 q = make_uint4(0, 0, 0, 0);
-      if (m < T) q = __ldg(reinterpret_cast<const uint4*>(x + (size_t)m * H + k0 + lc));
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// Batched router: a 128-token x 128-expert tile per block, 256 threads with
+// 8 x 8 outputs each, K staged 8 at a time through double-buffered shared
+// memory (the next slice is loaded into registers while the current one is
+// used), FP32 FMA in k order.  Split-K part p covers k-steps
+// [p*nk/S, (p+1)*nk/S) and writes out[p] ([S][T][E]); with S == 1 out is the
+// logits and the bias is added here.
+constexpr int RBM = 128, RBN = 128, RBK = 8;
+__global__ void __launch_bounds__(256) k_router_sgemm(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                                                      const float* __restrict__ bias, float* __restrict__ out, int T,
+                                                      int H, int E, int S) {
+  __shared__ __align__(16) float As[2][RBK][RBM + 4];
+  __shared__ __align__(16) float Bs[2][RBK][RBN + 4];
+  const int m0 = blockIdx.x * RBM, n0 = blockIdx.y * RBN, p = blockIdx.z;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int nk = H / RBK;
+  const int ks0 = p * nk / S, ks1 = (p + 1) * nk / S;
+  // loader: row tid/2 of each tile, 4 consecutive k
+  const int lr = tid >> 1, lc = (tid & 1) * 4;
+  const bool xa = m0 + lr < T, wa = n0 + lr < E;
+  const uint16_t* xrow = x + (size_t)(xa ? m0 + lr : 0) * H + lc;
+  const float* wrow = wr + (size_t)(wa ? n0 + lr : 0) * H + lc;
+  auto load = [&](int ks, uint2& xv, float4& wv) {
+    xv = xa ? __ldg(reinterpret_cast<const uint2*>(xrow + ks * RBK)) : make_uint2(0, 0);
+    wv = wa ? __ldg(reinterpret_cast<const float4*>(wrow + ks * RBK)) : make_float4(0, 0, 0, 0);
+  };
+  auto store = [&](int buf, const uint2& xv, const float4& wv) {
+    As[buf][lc + 0][lr] = bf16_lo(xv.x);
+    As[buf][lc + 1][lr] = bf16_hi(xv.x);
+    As[buf][lc + 2][lr] = bf16_lo(xv.y);
+    As[buf][lc + 3][lr] = bf16_hi(xv.y);
+    Bs[buf][lc + 0][lr] = wv.x;
+    Bs[buf][lc + 1][lr] = wv.y;
+    Bs[buf][lc + 2][lr] = wv.z;
+    Bs[buf][lc + 3][lr] = wv.w;
+  };
+  float acc[8][8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        xs_[lc + 2 * i][lr] = bf16_lo(w[i]);
-        xs_[lc + 2 * i + 1][lr] = bf16_hi(w[i]);
-      }
-      const int n = n0 + lr;
-      float4 a = make_float4(0, 0, 0, 0), b = a;
-      if (n < E) {
-        a = __ldg(reinterpret_cast<const float4*>(wr + (size_t)n * H + k0 + lc));
-        b = __ldg(reinterpret_cast<const float4*>(wr + (size_t)n * H + k0 + lc + 4));
-      }
-      ws_[lc + 0][lr] = a.x; ws_[lc + 1][lr] = a.y; ws_[lc + 2][lr] = a.z; ws_[lc + 3][lr] = a.w;
-      ws_[lc + 4][lr] = b.x; ws_[lc + 5][lr] = b.y; ws_[lc + 6][lr] = b.z; ws_[lc + 7][lr] = b.w;
-    }
-    __syncthreads();
-#pragma unroll 8
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+  uint2 xv;
+  float4 wv;
+  if (ks0 < ks1) {
+    load(ks0, xv, wv);
+    store(0, xv, wv);
+  }
+  __syncthreads();
+  for (int ks = ks0; ks < ks1; ++ks) {
+    const int buf = (ks - ks0) & 1;
+    if (ks + 1 < ks1) load(ks + 1, xv, wv);
+#pragma unroll
     for (int kk = 0; kk < RBK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&xs_[kk][ty * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&ws_[kk][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 8 + 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
+    if (ks + 1 < ks1) store(buf ^ 1, xv, wv);
     __syncthreads();
   }
+  float* o = out + (size_t)p * T * E;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + ty * 8 + i;
     if (m >= T) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
-      if (n < E) logits[(size_t)m * E + n] = acc[i][j] + (bias ? bias[n] : 0.0f);
+    for (int j = 0; j < 8; ++j) {
+      const int n = n0 + tx * 8 + j;
+      if (n < E) o[(size_t)m * E + n] = acc[i][j] + ((S == 1 && bias) ? bias[n] : 0.0f);
     }
   }
 }
 
+// logits = sum over the S split-K parts in ascending order, + bias.
+__global__ void __launch_bounds__(256) k_router_sum(const float* __restrict__ part, const float* __restrict__ bias,
+                                                    float* __restrict__ logits, int T, int E, int S) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)T * E) return;
+  float v = part[i];
+  for (int p = 1; p < S; ++p) v += part[(size_t)p * T * E + i];
+  if (bias) v += bias[i % E];
+  logits[i] = v;
+}
+
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
-                                 int T, int H, int E, cudaStream_t s) {
+                                 int T, int H, int E, float* part, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   // Up to a few hundred tokens one block per (expert row, 16 tokens) keeps
-  // every SM busy (the x re-reads hit L2); beyond that the tiled GEMM.
+  // every SM busy (the x re-reads hit L2); beyond that the tiled GEMM, split
+  // along K until the grid covers the GPU twice.
   if (T <= 512) {
     dim3 grid(E, (T + 15) / 16);
     k_router_gemv<<<grid, 256, 0, s>>>(x, wr, bias, logits, T, H, E);
-  } else {
-    dim3 grid((T + RBM - 1) / RBM, (E + RBN - 1) / RBN);
-    k_router_gemm<<<grid, 256, 0, s>>>(x, wr, bias, logits, T, H, E);
+    return cudaGetLastError();
   }
+  const int tiles = ((T + RBM - 1) / RBM) * ((E + RBN - 1) / RBN);
+  const int S = router_splits(T, E);
+  dim3 grid((T + RBM - 1) / RBM, (E + RBN - 1) / RBN, S);
+  (void)tiles;
+  k_router_sgemm<<<grid, 256, 0, s>>>(x, wr, bias, S == 1 ? logits : part, T, H, E, S);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || S == 1) return err;
+  const size_t n = (size_t)T * E;
+  k_router_sum<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, bias, logits, T, E, S);
   return cudaGetLastError();
 }
 

@@ -125,12 +125,13 @@ def _router_gpu(x_bits, wr, bias, k, H, E):
     return ids.cpu().numpy(), w.cpu().numpy(), lg.cpu().numpy()
 
 
-@pytest.mark.parametrize("T", [5, 100, 700])  # per-row router (up to 512 tokens) and tiled GEMM
-def test_topk_bitexact_on_exactly_computed_logits(T):
+@pytest.mark.parametrize("T,H", [(5, 128), (100, 128), (700, 128), (700, 256)])
+def test_topk_bitexact_on_exactly_computed_logits(T, H):
     """x rows are one-hot (1.0 at h_t), so logits[t, e] = Wr[e, h_t] exactly on
-    any summation order; the logits include exact ties."""
+    any summation order; the logits include exact ties.  Covers the per-row
+    router (up to 512 tokens) and the tiled GEMM."""
     rng = np.random.default_rng(12)
-    H, E, k = 128, 64, 4
+    E, k = 64, 4
     h_t = rng.integers(0, H, T)
     x = np.zeros((T, H))
     x[np.arange(T), h_t] = 1.0
@@ -153,6 +154,11 @@ def test_router_topk_random(wl_name, T):
     ids, w, lg = _router_gpu(lay["x"], lay["w_router"], lay["bias"], wl.top_k, wl.H, wl.E)
     ref = O.router_logits(F.bf16_bits_to_float(lay["x"]), lay["w_router"], lay["bias"])
     assert normwise(lg, ref) <= 1e-5
+    # element-wise: an FP32-accurate dot product (error within 1e-7 of sum |x w|;
+    # a BF16 rounding of the weights, or tensor-core accumulation over H, exceeds it)
+    mag = np.abs(F.bf16_bits_to_float(lay["x"])) @ np.abs(lay["w_router"].astype(np.float64)).T
+    ratio = np.max(np.abs(lg - ref) / (mag + 1e-30))
+    assert ratio <= 1e-7, ratio
     rid, rw = O.route(ref, wl.top_k)
     amb = ambiguous(ref, wl.top_k)
     assert np.array_equal(ids[~amb], rid[~amb])
