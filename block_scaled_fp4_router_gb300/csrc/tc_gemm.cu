@@ -13,7 +13,11 @@
 //               tcgen05.cp and issues 4 MMAs per 256-element (FP4) / 64-element
 //               (BF16) K stage into a 128 x 256 FP32 accumulator in TMEM;
 //               tcgen05.commit frees the stage and signals the epilogue;
-//   warps 2-5   epilogue: one TMEM lane (one output row) per thread.
+//   warps 2-17  epilogue: four warps per TMEM lane quadrant, each taking one
+//               quarter of the tile's columns; a warp copies its columns from
+//               TMEM to registers and frees the accumulator before the
+//               SwiGLU / requantise arithmetic and the stores, so the next
+//               tile's MMAs overlap them.
 // Tiles are 128 rows of A (tokens) x 256 rows of B (weight rows); for the
 // gate/up GEMMs the 256 B rows are 128 gate rows and the 128 matching up rows,
 // so each thread holds G and U of the same 128 columns.
@@ -38,7 +42,8 @@ namespace {
 constexpr int BM = 128;           // A rows per tile
 constexpr int BN = 256;           // B rows per tile (accumulator columns)
 constexpr int STAGES = 4;
-constexpr int TC_THREADS = 192;
+constexpr int EPI_WARPS = 16;
+constexpr int TC_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t A_BYTES = BM * 128;       // 16 KB: 128 rows x 128 B
 constexpr uint32_t B_BYTES = BN * 128;       // 32 KB
 constexpr uint32_t SFA_BYTES = 2 * 512;      // two K groups of 128 elements
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc::mbar_init(&empty[s], 1);
     }
     tc::mbar_init(&acc_full, 1);
-    tc::mbar_init(&acc_empty, 128);
+    tc::mbar_init(&acc_empty, 32 * EPI_WARPS);
     tc::mbar_init(&drain, 1);
     tc::mbar_fence_init();
     abort_flag = 0;
@@ -306,8 +311,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc::mma_commit(&drain);
     if (!tc::mbar_wait(&drain, 0, g.limit_ns, &abort_flag)) fail();
   } else if (warp >= 2) {
-    // ---------------- epilogue: thread <-> accumulator row
-    const int q = warp & 3;
+    // ---------------- epilogue: thread <-> accumulator row m, column quarter cq
+    const int q = warp & 3;          // TMEM lane quadrant this warp may read
+    const int cq = (warp - 2) >> 2;  // column quarter: 32 h columns, or 64 output columns
     const int m = q * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t acc_phase = 0;
@@ -316,67 +322,61 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti);
       if (!tc::mbar_wait(&acc_full, acc_phase, g.limit_ns, &abort_flag)) { fail(); break; }
       tc::fence_after_sync();
+      float va[32], vb[32];
+      if (SWIGLU) {
+        tc::tmem_ld32(trow + cq * 32, va);        // G, h columns 32cq ..
+        tc::tmem_ld32(trow + 128 + cq * 32, vb);  // U, the same columns
+      } else {
+        tc::tmem_ld32(trow + cq * 64, va);
+        tc::tmem_ld32(trow + cq * 64 + 32, vb);
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&acc_empty);  // the accumulator is free for the next tile
+      acc_phase ^= 1;
       if (EPI == EPI_SWIGLU_MX) {
-        // h = SiLU(G) U for 128 columns, requantised to MXFP4 per 32; every
+        // h = SiLU(G) U for 32 columns, requantised to MXFP4 (one block); every
         // padded row is written (padding rows quantise zeros).
-        uint32_t sw = 0;
         const int r = a_row + m;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float gv[32], uv[32];
-          tc::tmem_ld32(trow + c * 32, gv);
-          tc::tmem_ld32(trow + 128 + c * 32, uv);
-          float amax = 0.0f;
+        float amax = 0.0f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            gv[i] = silu(gv[i]) * uv[i];
-            amax = fmaxf(amax, fabsf(gv[i]));
-          }
-          const int ex = mx_scale_exp(amax);
-          const float inv = pow2_neg(ex);
-          uint32_t w[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i >> 3] |= e2m1_rne(gv[i] * inv) << (4 * (i & 7));
-          *reinterpret_cast<uint4*>(g.hq + (size_t)r * (g.h_cols / 2) + (nt * 128 + c * 32) / 2) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-          sw |= (uint32_t)(ex + 127) << (8 * c);
+        for (int i = 0; i < 32; ++i) {
+          va[i] = silu(va[i]) * vb[i];
+          amax = fmaxf(amax, fabsf(va[i]));
         }
-        const int hgroups = g.h_cols / 128;
-        g.hs[((size_t)(r / BM) * hgroups + nt) * 128 + (m % 32) * 4 + (m / 32)] = sw;
-      } else if (EPI == EPI_SWIGLU_BF16) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float gv[32], uv[32];
-          tc::tmem_ld32(trow + c * 32, gv);
-          tc::tmem_ld32(trow + 128 + c * 32, uv);
-          if (m < rows) {
-            uint16_t* dst = g.h_bf16 + (size_t)(srow0 + m) * g.h_cols + nt * 128 + c * 32;
+        const int ex = mx_scale_exp(amax);
+        const float inv = pow2_neg(ex);
+        uint32_t w[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 o;
-              o.x = f32_to_bf16_rn(silu(gv[i + 0]) * uv[i + 0]) | ((uint32_t)f32_to_bf16_rn(silu(gv[i + 1]) * uv[i + 1]) << 16);
-              o.y = f32_to_bf16_rn(silu(gv[i + 2]) * uv[i + 2]) | ((uint32_t)f32_to_bf16_rn(silu(gv[i + 3]) * uv[i + 3]) << 16);
-              o.z = f32_to_bf16_rn(silu(gv[i + 4]) * uv[i + 4]) | ((uint32_t)f32_to_bf16_rn(silu(gv[i + 5]) * uv[i + 5]) << 16);
-              o.w = f32_to_bf16_rn(silu(gv[i + 6]) * uv[i + 6]) | ((uint32_t)f32_to_bf16_rn(silu(gv[i + 7]) * uv[i + 7]) << 16);
-              *reinterpret_cast<uint4*>(dst + i) = o;
-            }
+        for (int i = 0; i < 32; ++i) w[i >> 3] |= e2m1_rne(va[i] * inv) << (4 * (i & 7));
+        *reinterpret_cast<uint4*>(g.hq + (size_t)r * (g.h_cols / 2) + (nt * 128 + cq * 32) / 2) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+        const int hgroups = g.h_cols / 128;
+        // byte cq of the MMA-layout scale word of row m in group nt
+        reinterpret_cast<uint8_t*>(g.hs)[(((size_t)(r / BM) * hgroups + nt) * 128 + (m % 32) * 4 + (m / 32)) * 4 + cq] =
+            (uint8_t)(ex + 127);
+      } else if (EPI == EPI_SWIGLU_BF16) {
+        if (m < rows) {
+          uint16_t* dst = g.h_bf16 + (size_t)(srow0 + m) * g.h_cols + nt * 128 + cq * 32;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 o;
+            o.x = f32_to_bf16_rn(silu(va[i + 0]) * vb[i + 0]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 1]) * vb[i + 1]) << 16);
+            o.y = f32_to_bf16_rn(silu(va[i + 2]) * vb[i + 2]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 3]) * vb[i + 3]) << 16);
+            o.z = f32_to_bf16_rn(silu(va[i + 4]) * vb[i + 4]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 5]) * vb[i + 5]) << 16);
+            o.w = f32_to_bf16_rn(silu(va[i + 6]) * vb[i + 6]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 7]) * vb[i + 7]) << 16);
+            *reinterpret_cast<uint4*>(dst + i) = o;
           }
         }
       } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tc::tmem_ld32(trow + c * 32, v);
-          if (m < rows) {
-            float* dst = g.out + (size_t)(srow0 + m) * g.ldo + nt * BN + c * 32;
+        if (m < rows) {
+          float* dst = g.out + (size_t)(srow0 + m) * g.ldo + nt * BN + cq * 64;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-          }
+          for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(va[i], va[i + 1], va[i + 2], va[i + 3]);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + 32 + i) = make_float4(vb[i], vb[i + 1], vb[i + 2], vb[i + 3]);
         }
       }
-      tc::fence_before_sync();
-      tc::mbar_arrive(&acc_empty);
-      acc_phase ^= 1;
     }
   }
   tc::fence_before_sync();
