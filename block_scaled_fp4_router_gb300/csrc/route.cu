@@ -86,12 +86,13 @@ __global__ void __launch_bounds__(256) k_router_gemv(const uint16_t* __restrict_
 }
 
 // Batched router: a 128-token x 128-expert tile per block, 256 threads with
-// 8 x 8 outputs each, K staged 8 at a time through double-buffered shared
-// memory (the next slice is loaded into registers while the current one is
-// used), FP32 FMA in k order.  Split-K part p covers k-steps
-// [p*nk/S, (p+1)*nk/S) and writes out[p] ([S][T][E]); with S == 1 out is the
-// logits and the bias is added here.
-constexpr int RBM = 128, RBN = 128, RBK = 8;
+// 8 x 8 outputs each (rows 4ty..4ty+3 and 64+4ty.., columns 4tx.. and
+// 64+4tx.., so the shared-memory reads are conflict-free), K staged 16 at a
+// time through double-buffered shared memory (the next slice is loaded into
+// registers while the current one is used), FP32 FMA in k order.  Split-K
+// part p covers k-steps [p*nk/S, (p+1)*nk/S) and writes out[p] ([S][T][E]);
+// with S == 1 out is the logits and the bias is added here.
+constexpr int RBM = 128, RBN = 128, RBK = 16;
 __global__ void __launch_bounds__(256) k_router_sgemm(const uint16_t* __restrict__ x, const float* __restrict__ wr,
                                                       const float* __restrict__ bias, float* __restrict__ out, int T,
                                                       int H, int E, int S) {
@@ -101,46 +102,53 @@ __global__ void __launch_bounds__(256) k_router_sgemm(const uint16_t* __restrict
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int nk = H / RBK;
   const int ks0 = p * nk / S, ks1 = (p + 1) * nk / S;
-  // loader: row tid/2 of each tile, 4 consecutive k
-  const int lr = tid >> 1, lc = (tid & 1) * 4;
+  // loader: row tid/2 of each tile, 8 consecutive k
+  const int lr = tid >> 1, lc = (tid & 1) * 8;
   const bool xa = m0 + lr < T, wa = n0 + lr < E;
   const uint16_t* xrow = x + (size_t)(xa ? m0 + lr : 0) * H + lc;
   const float* wrow = wr + (size_t)(wa ? n0 + lr : 0) * H + lc;
-  auto load = [&](int ks, uint2& xv, float4& wv) {
-    xv = xa ? __ldg(reinterpret_cast<const uint2*>(xrow + ks * RBK)) : make_uint2(0, 0);
-    wv = wa ? __ldg(reinterpret_cast<const float4*>(wrow + ks * RBK)) : make_float4(0, 0, 0, 0);
+  auto load = [&](int ks, uint4& xv, float4& w0, float4& w1) {
+    xv = xa ? __ldg(reinterpret_cast<const uint4*>(xrow + ks * RBK)) : make_uint4(0, 0, 0, 0);
+    w0 = wa ? __ldg(reinterpret_cast<const float4*>(wrow + ks * RBK)) : make_float4(0, 0, 0, 0);
+    w1 = wa ? __ldg(reinterpret_cast<const float4*>(wrow + ks * RBK + 4)) : make_float4(0, 0, 0, 0);
   };
-  auto store = [&](int buf, const uint2& xv, const float4& wv) {
-    As[buf][lc + 0][lr] = bf16_lo(xv.x);
-    As[buf][lc + 1][lr] = bf16_hi(xv.x);
-    As[buf][lc + 2][lr] = bf16_lo(xv.y);
-    As[buf][lc + 3][lr] = bf16_hi(xv.y);
-    Bs[buf][lc + 0][lr] = wv.x;
-    Bs[buf][lc + 1][lr] = wv.y;
-    Bs[buf][lc + 2][lr] = wv.z;
-    Bs[buf][lc + 3][lr] = wv.w;
+  auto store = [&](int buf, const uint4& xv, const float4& w0, const float4& w1) {
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      As[buf][lc + 2 * i][lr] = bf16_lo(xw[i]);
+      As[buf][lc + 2 * i + 1][lr] = bf16_hi(xw[i]);
+    }
+    Bs[buf][lc + 0][lr] = w0.x;
+    Bs[buf][lc + 1][lr] = w0.y;
+    Bs[buf][lc + 2][lr] = w0.z;
+    Bs[buf][lc + 3][lr] = w0.w;
+    Bs[buf][lc + 4][lr] = w1.x;
+    Bs[buf][lc + 5][lr] = w1.y;
+    Bs[buf][lc + 6][lr] = w1.z;
+    Bs[buf][lc + 7][lr] = w1.w;
   };
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-  uint2 xv;
-  float4 wv;
+  uint4 xv;
+  float4 w0, w1;
   if (ks0 < ks1) {
-    load(ks0, xv, wv);
-    store(0, xv, wv);
+    load(ks0, xv, w0, w1);
+    store(0, xv, w0, w1);
   }
   __syncthreads();
   for (int ks = ks0; ks < ks1; ++ks) {
     const int buf = (ks - ks0) & 1;
-    if (ks + 1 < ks1) load(ks + 1, xv, wv);
+    if (ks + 1 < ks1) load(ks + 1, xv, w0, w1);
 #pragma unroll
     for (int kk = 0; kk < RBK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8 + 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 8]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 8 + 4]);
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -148,17 +156,17 @@ __global__ void __launch_bounds__(256) k_router_sgemm(const uint16_t* __restrict
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
-    if (ks + 1 < ks1) store(buf ^ 1, xv, wv);
+    if (ks + 1 < ks1) store(buf ^ 1, xv, w0, w1);
     __syncthreads();
   }
   float* o = out + (size_t)p * T * E;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int m = m0 + ty * 8 + i;
+    const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
     if (m >= T) continue;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int n = n0 + tx * 8 + j;
+      const int n = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
       if (n < E) o[(size_t)m * E + n] = acc[i][j] + ((S == 1 && bias) ? bias[n] : 0.0f);
     }
   }
