@@ -28,7 +28,7 @@ EXPORTED = [
     "moe_status_string", "moe_workspace_size", "moe_get_status", "moe_router_topk",
     "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
-    "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights",
+    "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -90,6 +90,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
         "moe_prepare_weights": ([P, P, P, P, P], ctypes.c_int),
+        "moe_convert_nvfp4_to_mxfp4": ([P, P, P, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -176,6 +177,12 @@ def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:
 def moe_prepare_weights(d, ex, w13_scale_mma, w2_scale_mma, stream=None):
     _check(load().moe_prepare_weights(ctypes.byref(d), ctypes.byref(ex), _p(w13_scale_mma), _p(w2_scale_mma),
                                       _stream(stream)), "moe_prepare_weights")
+
+
+def moe_convert_nvfp4_to_mxfp4(d, ex, w13_out, w13_scale_out, w2_out, w2_scale_out, stream=None):
+    _check(load().moe_convert_nvfp4_to_mxfp4(ctypes.byref(d), ctypes.byref(ex), _p(w13_out), _p(w13_scale_out),
+                                             _p(w2_out), _p(w2_scale_out), _stream(stream)),
+           "moe_convert_nvfp4_to_mxfp4")
 
 
 def moe_debug_requantized_h(d, ws, hq, hs, stream=None):

@@ -162,6 +162,19 @@ moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts
   return cuda_status(launch_relayout_weight_sf(ex.w2s, desc->E, desc->H, kf * desc->I, w2_scale_mma, s));
 }
 
+moe_status_t moe_convert_nvfp4_to_mxfp4(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                        uint8_t* w13_out, uint8_t* w13_scale_out, uint8_t* w2_out,
+                                        uint8_t* w2_scale_out, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  ExpertsDev ex;
+  MOE_TRY(check_experts(desc, experts, &ex));
+  if (!ex.nv) return MOE_ERR_INVALID_ARG;
+  if (!w13_out || !w13_scale_out || !w2_out || !w2_scale_out || !aligned(w13_out, 16) || !aligned(w2_out, 16))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_nvfp4_to_mxfp4(shape_of(desc), ex, w13_out, w13_scale_out, w2_out, w2_scale_out,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes, uint8_t* hq,
                                      uint8_t* hs, moe_stream_t stream) {
   MOE_TRY(check_desc(desc));

@@ -142,6 +142,20 @@ MOE_API moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* by
 MOE_API moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts_t* experts,
                                          uint8_t* w13_scale_mma, uint8_t* w2_scale_mma, moe_stream_t stream);
 
+/* Load-time conversion of NVFP4 routed experts to OCP MXFP4 (the pages convert
+ * NVFP4 checkpoints to MXFP4 before serving: AMD article, section "Enabling
+ * the MXFP4 checkpoint with the AMD Quark"; vLLM PR #64273, section
+ * "Purpose").  Per 32-element block the exact values code x E4M3 scale x FP32
+ * tensor scale (gate, up and down scales of experts->tensor_scale [E, 3]) are
+ * requantised with the MXFP4 rule of moe_quant_act_mxfp4; every decision is
+ * taken in exact arithmetic.  experts must be NVFP4 (else
+ * MOE_ERR_INVALID_ARG).  Outputs, caller-allocated (codes 16-byte aligned):
+ *   w13_out [E, 2I, H/2], w13_scale_out [E, 2I, H/32],
+ *   w2_out  [E, H, I/2],  w2_scale_out  [E, H, I/32]. */
+MOE_API moe_status_t moe_convert_nvfp4_to_mxfp4(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                                uint8_t* w13_out, uint8_t* w13_scale_out, uint8_t* w2_out,
+                                                uint8_t* w2_scale_out, moe_stream_t stream);
+
 /* Reads (and clears) the device status word of a workspace into *st.  Call
  * after synchronising the stream the workspace was used on.  This is the one
  * entry point that waits: it copies 4 bytes device-to-host. */

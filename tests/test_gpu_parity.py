@@ -445,6 +445,78 @@ def test_tensor_core_path_shapes(shape):
     assert normwise(y_shared.cpu().numpy(), ref["ys"]) <= CONTRACTION_TOL
 
 
+# ------------------------------------------------- NVFP4 -> MXFP4 conversion
+
+
+def _random_nvfp4_layer(rng, E, H, I, scale_codes):
+    def mat(R, K):
+        codes = rng.integers(0, 16, (E, R, K)).astype(np.uint8)
+        return F.pack_e2m1(codes), codes, rng.choice(scale_codes, (E, R, K // 16)).astype(np.uint8)
+    w13p, w13c, w13s = mat(2 * I, H)
+    w2p, w2c, w2s = mat(H, I)
+    # non-power-of-two FP32 tensor scales, one per (expert, gate / up / down)
+    ts = rng.uniform(1e-3, 3e-2, (E, 3)).astype(np.float32)
+    return w13p, w13c, w13s, w2p, w2c, w2s, ts
+
+
+def test_nvfp4_to_mxfp4_conversion_bitexact():
+    """Every code and scale byte equals the oracle's exact requantisation,
+    for random codes, E4M3 scales over normal and subnormal encodings, and
+    non-power-of-two tensor scales."""
+    rng = np.random.default_rng(31)
+    E, H, I = 6, 512, 256
+    scale_codes = np.concatenate([np.arange(0x01, 0x08), np.arange(0x20, 0x60)])
+    w13p, w13c, w13s, w2p, w2c, w2s, ts = _random_nvfp4_layer(rng, E, H, I, scale_codes)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    d13p, d13s, d2p, d2s, dts = dev(w13p), dev(w13s), dev(w2p), dev(w2s), dev(ts)
+    ex = M.experts(M.MOE_W_NVFP4, d13p, d13s, d2p, d2s, dts)
+    o13 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device="cuda")
+    o13s = torch.empty((E, 2 * I, H // 32), dtype=torch.uint8, device="cuda")
+    o2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device="cuda")
+    o2s = torch.empty((E, H, I // 32), dtype=torch.uint8, device="cuda")
+    M.moe_convert_nvfp4_to_mxfp4(M.desc(1, H, I, E, 4), ex, o13, o13s, o2, o2s)
+    torch.cuda.synchronize()
+    for e in range(E):
+        tsr = np.where(np.arange(2 * I) < I, ts[e, 0], ts[e, 1])  # per row: gate, then up
+        rc, rs = F.requantize_nvfp4_to_mxfp4(w13c[e], w13s[e], tsr)
+        assert np.array_equal(o13[e].cpu().numpy(), F.pack_e2m1(rc))
+        assert np.array_equal(o13s[e].cpu().numpy(), rs)
+        rc, rs = F.requantize_nvfp4_to_mxfp4(w2c[e], w2s[e], ts[e, 2])
+        assert np.array_equal(o2[e].cpu().numpy(), F.pack_e2m1(rc))
+        assert np.array_equal(o2s[e].cpu().numpy(), rs)
+    with pytest.raises(M.MoeError):  # the source must be NVFP4
+        M.moe_convert_nvfp4_to_mxfp4(M.desc(1, H, I, E, 4), M.experts(M.MOE_W_MXFP4, d13p, o13s, d2p, o2s), o13,
+                                     o13s, o2, o2s)
+
+
+def test_decode_on_converted_weights():
+    """An NVFP4 layer converted on the GPU runs as an MXFP4 layer: the decode
+    matches the oracle on the oracle's own conversion of the same weights."""
+    wl = W.WORKLOADS["tiny"]
+    nv = W.Workload("tiny_nv", wl.T, wl.H, wl.I, wl.E, wl.top_k, W.NVFP4, 27, wl.wr_std)
+    lay = W.generate(nv)
+    E, H, I = nv.E, nv.H, nv.I
+    src = DeviceLayer(lay, H, I, E, nv.top_k, nv.fmt, T_max=nv.T, prepare=False)
+    o13 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device="cuda")
+    o13s = torch.empty((E, 2 * I, H // 32), dtype=torch.uint8, device="cuda")
+    o2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device="cuda")
+    o2s = torch.empty((E, H, I // 32), dtype=torch.uint8, device="cuda")
+    M.moe_convert_nvfp4_to_mxfp4(src.desc(nv.T), src.ex, o13, o13s, o2, o2s)
+    torch.cuda.synchronize()
+    mx = dict(lay)
+    ts = lay["tensor_scale"]
+    ts13 = np.where(np.arange(2 * I)[None, :] < I, ts[:, 0:1], ts[:, 1:2])  # [E, 2I]: gate rows, up rows
+    c13, s13 = F.requantize_nvfp4_to_mxfp4(F.unpack_e2m1(lay["w13"]), lay["w13_scale"], ts13)
+    c2, s2 = F.requantize_nvfp4_to_mxfp4(F.unpack_e2m1(lay["w2"]), lay["w2_scale"], ts[:, 2:3])
+    mx.update(w13=F.pack_e2m1(c13), w13_scale=s13, w2=F.pack_e2m1(c2), w2_scale=s2, tensor_scale=None)
+    assert np.array_equal(o13.cpu().numpy(), mx["w13"]) and np.array_equal(o2s.cpu().numpy(), mx["w2_scale"])
+    mxw = W.Workload("tiny_conv", nv.T, H, I, E, nv.top_k, W.MXFP4, 27, wl.wr_std)
+    dev = DeviceLayer(mx, H, I, E, nv.top_k, W.MXFP4, T_max=nv.T)
+    out, ids, _ = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    _compare_layer(mxw, mx, {}, out, ids)
+
+
 # --------------------------------------------------------------- edge cases
 
 
