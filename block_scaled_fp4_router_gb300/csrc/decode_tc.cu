@@ -27,11 +27,9 @@
 // their first unit the epilogue warps compute this block's router rows and
 // its slice of the MXFP4 quantisation of x; once every block has done so they
 // build the routing (top-k, sort by expert) in shared memory and release the
-// producer and MMA warps onto the routed units.  While the routing is not yet
-// known the producers pull the shared down-projection weights into L2, and
-// once it is known the routed down-projection weights (up to a byte budget
-// well inside L2), so that HBM keeps streaming across the dependencies
-// between the steps.
+// producer and MMA warps onto the routed units.  There is no L2 prefetch
+// beyond the stage ring: extra traffic measurably slows the latency-bound
+// hand-offs more than it saves in streaming.
 //
 // Every wait is bounded (MOE_DEV_TIMEOUT in the status word); the last block
 // out resets the counters, and each finishing block resets its ticket.
@@ -103,7 +101,6 @@ struct DcArgs {
   uint8_t* hq;               // [T k, I/2] sorted-assignment rows
   uint8_t* hs_mma;           // [slots][I/128][512] E8M0 (MXFP4) or [slots][I/64][512] UE4M3 (NVFP4)
   uint8_t* hsc;              // NVFP4: E8M0 bytes of h [T k][I/32]
-  size_t rdn_prefetch_units; // routed down units whose weights go to L2 early (a byte budget)
   int depth;                 // stages in flight (<= DSTAGES)
   uint16_t* h_shared;        // [T, I]
   float* gu_sh;              // [s_sgu][T][2I]
@@ -499,19 +496,6 @@ __device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t ep
   epi_sync();
 }
 
-// L2 prefetch of the weight boxes (A operand) of a down unit.
-__device__ void prefetch_down_unit(const DcArgs& a, const DcMaps& m, const Unit& U, int e) {
-  if (U.kind == U_SDN) {
-    for (int st = U.st0; st < U.st1; ++st)
-      for (int h = 0; h < 2 && 2 * st + h < a.I / 64; ++h)
-        tc::tma_prefetch_2d(&m.w2s, (2 * st + h) * 128, 128 * U.tile);
-  } else {
-    for (int st = U.st0; st < U.st1; ++st)
-      for (int h = 0; h < 2 && 2 * st + h < a.I / 256; ++h)
-        tc::tma_prefetch_2d(&m.w2r, (2 * st + h) * 128, e * a.H + 128 * U.tile);
-  }
-}
-
 // Halves of a stage that a unit uses: gate/up units one K chunk (two weight
 // tiles, one activation tile), down units two K chunks (the second may be
 // past the end of K).
@@ -706,20 +690,11 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       }
       for (int u = blockIdx.x;; u += a.G) {
         if (u >= a.n_sgu && n_slots < 0) {
-          // Until the routing is known, pull shared down weights into L2
-          // (unit v by block v mod G, whichever block computes it later).
-          for (int v = blockIdx.x; v < a.n_sdn; v += a.G) prefetch_down_unit(a, maps, sdn_unit(a, v), 0);
           if (!tc::mbar_wait(&routing_ready, 0, a.limit_ns, &abort_flag)) { fail(); break; }
           n_slots = R.n_slots;
           // x was quantised by plain stores of other blocks
           if (!wait_at_least(a.ctr + C_DC_READY, a.G, status, a.limit_ns)) { fail(); break; }
           tc::fence_proxy_async_global();
-          // The routed down weights are known now: into L2 while the gate/up streams run.
-          const int n_rdn = imin(n_slots * nbH, (int)a.rdn_prefetch_units);
-          for (int v = blockIdx.x; v < n_rdn; v += a.G) {
-            const Unit D = rdn_unit(a, n_slots, v);
-            prefetch_down_unit(a, maps, D, R.slot_e[D.slot]);
-          }
         }
         if (u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
         const Unit U = unit_at(a, n_slots < 0 ? 0 : n_slots, u);
@@ -1190,9 +1165,6 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.xs_mma = base + L.dc_xs;
   a.xshift = reinterpret_cast<int*>(base + L.dc_xshift);
   a.hsc = base + L.dc_hsc;
-  // routed down weights pulled into L2 ahead of use: at most 48 MB
-  const size_t rdn_unit_bytes = (size_t)128 * I / 2 + (size_t)128 * I / (ex.nv ? 16 : 32);
-  a.rdn_prefetch_units = ((size_t)48 << 20) / rdn_unit_bytes;
   a.depth = a.nslot_max >= 16 ? 4 : 2;
   a.rowmax = reinterpret_cast<unsigned long long*>(base + L.dc_rowmax);
   a.hq = base + L.hq;
