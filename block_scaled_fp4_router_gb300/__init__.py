@@ -29,6 +29,7 @@ EXPORTED = [
     "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
+    "moe_set_routed_gemm",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -86,6 +87,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_decode": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
         "moe_layer_forward": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
         "moe_set_wait_limit_ns": ([U64], None),
+        "moe_set_routed_gemm": ([ctypes.c_int32], ctypes.c_int),
         "moe_debug_wait_probe": ([P, S, U64, P], ctypes.c_int),
         "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
@@ -167,6 +169,13 @@ def moe_get_status(ws) -> int:
 
 def moe_set_wait_limit_ns(ns: int) -> None:
     load().moe_set_wait_limit_ns(int(ns))
+
+
+ROUTED_GEMM_AUTO, ROUTED_GEMM_TOKENS_AS_A, ROUTED_GEMM_WEIGHTS_AS_A = 0, 1, 2
+
+
+def moe_set_routed_gemm(mode: int) -> None:
+    _check(load().moe_set_routed_gemm(int(mode)), "moe_set_routed_gemm")
 
 
 def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:

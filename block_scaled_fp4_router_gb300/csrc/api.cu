@@ -14,6 +14,7 @@ using namespace moefp4;
 namespace {
 
 std::atomic<uint64_t> g_wait_limit_ns{500ull * 1000 * 1000};
+std::atomic<int> g_routed_gemm{TC_GEMM_AUTO};
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -91,13 +92,14 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
   const bool tc = !ex.nv && tc_routed_enabled(d->T * d->top_k) && d->H % 256 == 0 && d->I % 256 == 0 &&
                   aligned(ex.w13s, 4) &&
                   aligned(ex.w2s, 4);
+  const bool wa = tc && tc_weights_as_a(d->T * d->top_k, d->E, g_routed_gemm.load());
   // record which layout h is left in (read by moe_debug_requantized_h)
-  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.counters) + C_HPATH, tc ? 1 : 0, sizeof(int), s));
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.counters) + C_HPATH, tc ? (wa ? 2 : 1) : 0, sizeof(int), s));
   if (tc) {
     TcWorkspace w{at<int>(ws, L.tc_poff), at<uint8_t>(ws, L.tc_mtiles), at<int>(ws, L.tc_num_mt),
                   at<uint8_t>(ws, L.tc_xq), at<uint8_t>(ws, L.tc_xs), at<uint8_t>(ws, L.tc_hq),
                   at<uint8_t>(ws, L.tc_hs), at<uint8_t>(ws, L.tc_w13s), at<uint8_t>(ws, L.tc_w2s)};
-    MOE_CUDA(launch_expert_ffn_tc(sh, ex, w, xq, xs, offsets, perm, y_assign, status, limit, s));
+    MOE_CUDA(launch_expert_ffn_tc(sh, ex, w, xq, xs, offsets, perm, y_assign, status, limit, wa, s));
   } else {
     MOE_CUDA(launch_routed_simt(sh, ex, xq, xs, offsets, perm, at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs),
                                 y_assign, s));
@@ -191,6 +193,12 @@ moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* w
 }
 
 void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+moe_status_t moe_set_routed_gemm(int32_t mode) {
+  if (mode < TC_GEMM_AUTO || mode > TC_GEMM_WEIGHTS_AS_A) return MOE_ERR_INVALID_ARG;
+  g_routed_gemm.store(mode);
+  return MOE_OK;
+}
 
 moe_status_t moe_debug_wait_probe(void* ws, size_t ws_bytes, uint64_t limit_ns, moe_stream_t stream) {
   if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(int) * N_COUNTERS) return MOE_ERR_WORKSPACE;

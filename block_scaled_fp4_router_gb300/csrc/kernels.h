@@ -62,9 +62,14 @@ struct TcWorkspace {
   uint8_t* w2s_mma;
 };
 // A5 - A7 on tensor cores (MXFP4 weights)
+// wa: weights as the MMA's A operand and 64-row token windows as B (small
+// per-expert batches); otherwise 128-token tiles as A.
 cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const TcWorkspace& w, const uint8_t* xq,
                                  const uint8_t* xs, const int* offsets, const int* perm, float* y_assign,
-                                 int* status, uint64_t limit_ns, cudaStream_t s);
+                                 int* status, uint64_t limit_ns, bool wa, cudaStream_t s);
+// Whether n assignments over E experts take the weights-as-A GEMMs under an
+// orientation mode (TC_GEMM_*).
+bool tc_weights_as_a(int n, int E, int mode);
 // A8 on tensor cores
 cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
                              float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s);

@@ -18,6 +18,7 @@ constexpr int MAX_DECODE_T = 16;   // fused single-launch decode range
 constexpr int PERM_CHUNK = 1024;   // assignments ranked per block in the permutation
 constexpr int TC_MIN_ASSIGN = 256; // routed experts on tensor cores from this many assignments
 constexpr int TC_MIN_T_SHARED = 128; // shared expert on tensor cores from this many tokens
+constexpr int ROUTER_SMS = 152;       // SMs the batched router's split-K is balanced for
 
 // Tensor-core decode (T <= MAX_DECODE_T): one block per SM, at most this many.
 constexpr int DC_MAX_GRID = 256;
@@ -51,15 +52,31 @@ MOE_HD inline DcSplits dc_splits(int T, int H, int I, int E, int k, int grid) {
 
 // Split-K parts of the batched router (T > 512): enough 128 x 128 tiles for
 // two blocks per SM of a 152-SM GPU, at most 8.
+// The batched router runs two 256-thread blocks per SM; the split count S
+// (1..8) minimises the busiest SM's share of the work, ceil(tiles S / SMs) / S
+// blocks of 1/S of a tile each (the smallest S on ties).
 MOE_HD inline int router_splits(int T, int E) {
   if (T <= 512) return 1;
   const int tiles = ((T + 127) / 128) * ((E + 127) / 128);
-  int s = (304 + tiles - 1) / tiles;
-  return s < 1 ? 1 : (s > 8 ? 8 : s);
+  int best = 1;
+  for (int s = 2; s <= 8; ++s)
+    if ((int64_t)((tiles * s + ROUTER_SMS - 1) / ROUTER_SMS) * best <
+        (int64_t)((tiles * best + ROUTER_SMS - 1) / ROUTER_SMS) * s)
+      best = s;
+  return best;
 }
 
 // Rows of the per-expert padded order (each expert's rows rounded up to 128).
 MOE_HD inline int tc_padded_rows(int n, int E) { return ((n + E * 127) + 127) / 128 * 128; }
+// The same with windows of `win` rows (128, or 64 for the weights-as-A GEMMs).
+MOE_HD inline int tc_padded_rows_win(int n, int E, int win) {
+  return ((n + E * (win - 1)) + win - 1) / win * win;
+}
+// Routed tensor-core GEMM orientation: tokens as the MMA's A operand
+// (128-token tiles), or weights as A with up to 64 tokens as B, chosen when
+// the average expert has at most WA_MAX_AVG_ROWS assignments.
+enum { TC_GEMM_AUTO = 0, TC_GEMM_TOKENS_AS_A = 1, TC_GEMM_WEIGHTS_AS_A = 2 };
+constexpr int WA_MAX_AVG_ROWS = 32;
 MOE_HD inline bool tc_routed_enabled(int n) { return n >= TC_MIN_ASSIGN; }
 
 // Device status word values (mirror moe_status_t).
@@ -75,7 +92,7 @@ enum Counter : int {
   C_GU = 4,        // gate/up units finished (shared + routed)
   C_EXIT = 5,      // blocks finished (the last one resets the counters)
   C_TEST = 6,      // never written by the library: a wait on it always times out
-  C_HPATH = 7,     // which layout the last expert FFN left h in (0: sorted rows, else padded tiles)
+  C_HPATH = 7,     // low byte: layout the last expert FFN left h in (0 sorted, 1 / 2 windows of 128 / 64)
   C_DC_READY = 8,  // tensor-core decode: blocks done with their quantisation slice
   C_DC_HSH = 9,    // tensor-core decode: shared-expert h tiles finished
   C_DC_HR = 10,    // tensor-core decode: routed h tiles finished
@@ -176,13 +193,17 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.y_shared = take(sizeof(float) * (size_t)T * H);
   const bool tc = tc_routed_enabled((int)n);
   const size_t R = tc ? (size_t)tc_padded_rows((int)n, E) : 0;
+  // 64-row windows (weights-as-A GEMMs): no more rows, up to twice the tiles
+  // and scale blocks per row
+  const size_t R64 = tc ? (size_t)tc_padded_rows_win((int)n, E, 64) : 0;
+  const size_t tiles = R / 128 > R64 / 64 ? R / 128 : R64 / 64;
   L.tc_poff = take(tc ? sizeof(int) * (E + 1) : 0);
-  L.tc_mtiles = take(16 * (R / 128));
+  L.tc_mtiles = take(16 * tiles);
   L.tc_num_mt = take(tc ? sizeof(int) : 0);
   L.tc_xq = take(R * H / 2);
-  L.tc_xs = take(R * H / 32);
+  L.tc_xs = take(tiles * (H / 128) * 512);
   L.tc_hq = take(R * I / 2);
-  L.tc_hs = take(R * I / 32);
+  L.tc_hs = take(tiles * (I / 128) * 512);
   L.tc_w13s = take(tc ? (size_t)E * 2 * I * H / 32 : 0);
   L.tc_w2s = take(tc ? (size_t)E * H * I / 32 : 0);
   L.dc_xs = take(dc ? (size_t)H / 64 * 512 : 0);

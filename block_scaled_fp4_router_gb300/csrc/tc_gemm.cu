@@ -71,48 +71,54 @@ struct MTile {
 
 // --------------------------------------------------------------- tile list
 
-// One block: padded expert offsets and the list of 128-row tiles.
-__global__ void __launch_bounds__(256) k_build_mtiles(const int* __restrict__ offsets, int E, int* __restrict__ poff,
-                                                      MTile* __restrict__ tiles, int* __restrict__ num_tiles) {
+// One block: padded expert offsets and the list of row windows (tiles of
+// `win` = 128 or 64 rows; each expert's rows are rounded up to `win`).
+__global__ void __launch_bounds__(256) k_build_mtiles(const int* __restrict__ offsets, int E, int win,
+                                                      int* __restrict__ poff, MTile* __restrict__ tiles,
+                                                      int* __restrict__ num_tiles) {
   __shared__ int s_poff[MAX_E + 1];
   if (threadIdx.x == 0) {
     int p = 0;
     for (int e = 0; e < E; ++e) {
       s_poff[e] = p;
       const int cnt = offsets[e + 1] - offsets[e];
-      p += (cnt + BM - 1) / BM * BM;
+      p += (cnt + win - 1) / win * win;
     }
     s_poff[E] = p;
-    *num_tiles = p / BM;
+    *num_tiles = p / win;
   }
   __syncthreads();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) poff[e] = s_poff[e];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int cnt = offsets[e + 1] - offsets[e];
-    for (int m = 0; m * BM < cnt; ++m) {
+    for (int m = 0; m * win < cnt; ++m) {
       MTile t;
       t.e = e;
-      t.prow0 = s_poff[e] + m * BM;
-      t.srow0 = offsets[e] + m * BM;
-      t.rows = min(BM, cnt - m * BM);
-      tiles[t.prow0 / BM] = t;
+      t.prow0 = s_poff[e] + m * win;
+      t.srow0 = offsets[e] + m * win;
+      t.rows = min(win, cnt - m * win);
+      tiles[t.prow0 / win] = t;
     }
   }
 }
 
 // One block per padded row: copy the MXFP4 activation row of the assignment
 // there (zeros for padding rows) and scatter its scale bytes into the MMA
-// scale layout.  Scale layout of a matrix with R rows (R a multiple of 128)
-// and K elements: block (R/128 row tile, K/128 group) of 512 bytes, word
-// (i, j) at byte 16 i + 4 j holding the 4 scale bytes of row 32 j + i.
+// scale layout.  Scale layout of a matrix of windows of `win` rows and K
+// elements: block (window, K/128 group) of 512 bytes, word (i, j) at byte
+// 16 i + 4 j holding the 4 scale bytes of window row 32 j + i (with 64-row
+// windows words j = 2, 3 are unused).  With rows16 set, rows past the
+// window's real rows rounded up to 16 are skipped (nothing reads them).
 __global__ void __launch_bounds__(128) k_gather_mx_rows(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
                                                         int K, int k_top, const int* __restrict__ perm,
                                                         const MTile* __restrict__ tiles, const int* __restrict__ num_tiles,
-                                                        uint8_t* __restrict__ q_out, uint32_t* __restrict__ sf_out) {
+                                                        int win, int rows16, uint8_t* __restrict__ q_out,
+                                                        uint32_t* __restrict__ sf_out) {
   const int r = blockIdx.x;
-  if (r >= *num_tiles * BM) return;
-  const MTile t = tiles[r / BM];
-  const int m = r % BM;
+  if (r >= *num_tiles * win) return;
+  const MTile t = tiles[r / win];
+  const int m = r % win;
+  if (rows16 && m >= ((t.rows + 15) & ~15)) return;
   const bool real = m < t.rows;
   const int src = real ? perm[t.srow0 + m] / k_top : 0;
   const int cpr = K / 32;  // 16-byte chunks per row
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(128) k_gather_mx_rows(const uint8_t* __restric
   const int i = m % 32, j = m / 32;
   for (int g = threadIdx.x; g < groups; g += blockDim.x) {
     const uint32_t w = real ? __ldg(reinterpret_cast<const uint32_t*>(s + (size_t)src * (K / 32)) + g) : 0u;
-    sf_out[((size_t)(r / BM) * groups + g) * 128 + i * 4 + j] = w;
+    sf_out[((size_t)(r / win) * groups + g) * 128 + i * 4 + j] = w;
   }
 }
 
@@ -327,8 +333,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc::tmem_ld32(trow + cq * 32, va);        // G, h columns 32cq ..
         tc::tmem_ld32(trow + 128 + cq * 32, vb);  // U, the same columns
       } else {
-        tc::tmem_ld32(trow + cq * 64, va);
-        tc::tmem_ld32(trow + cq * 64 + 32, vb);
+        // rows 32q + {0..15} and 32q + {16..31}, columns 64cq .. 64cq + 63
+        tc::tmem_ld16x256_x8(trow + cq * 64, va);
+        tc::tmem_ld16x256_x8(trow + (16u << 16) + cq * 64, vb);
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&acc_empty);  // the accumulator is free for the next tile
@@ -368,14 +375,230 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
       } else {
-        if (m < rows) {
-          float* dst = g.out + (size_t)(srow0 + m) * g.ldo + nt * BN + cq * 64;
+        // Four threads share a row, so each warp store fills eight whole
+        // 32-byte sectors (a row-per-thread store fills 32 half sectors).
+        const int r0 = q * 32 + (lane >> 2);
+        float* base = g.out + (size_t)srow0 * g.ldo + nt * BN + cq * 64 + 2 * (lane & 3);
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(va[i], va[i + 1], va[i + 2], va[i + 3]);
+        for (int hh = 0; hh < 4; ++hh) {
+          const int r = r0 + 8 * hh;  // hh: lanes +0, +8 (first load), +16, +24 (second)
+          if (r < rows) {
+            float* dst = base + (size_t)r * g.ldo;
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + 32 + i) = make_float4(vb[i], vb[i + 1], vb[i + 2], vb[i + 3]);
+            for (int j = 0; j < 8; ++j) {
+              const float* v = hh < 2 ? va : vb;
+              const int o = 4 * j + 2 * (hh & 1);
+              *reinterpret_cast<float2*>(dst + 8 * j) = make_float2(v[o], v[o + 1]);
+            }
+          }
         }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------- weights-as-A grouped GEMM
+//
+// With a few tokens per expert (batched decode) the routed GEMMs above would
+// carry up to 127 padding rows in every 128-row token tile.  This variant
+// swaps the operands: 128 weight rows are the MMA's A (M = 128) and the
+// expert's tokens are B, a window of up to WA_WIN rows of the per-expert
+// padded order (N = the window's real rows rounded up to 16, moved as 16-row
+// TMA boxes), so an SM streams weights and little else.  TMEM lane = weight
+// row, column = token.  Two accumulator buffers of 128 columns (gate 0..63
+// and up 64..127, or down 0..63) let the next tile's MMAs overlap the
+// epilogue.  Epilogues:
+//   EPI_SWIGLU_MX  lane = h column; the 32 lanes of a warp are one MXFP4
+//                  block of h for each token: amax and the packed codes by
+//                  warp shuffles, h rows written in the padded window order
+//                  with their scales in the MMA layout of 64-row windows;
+//   EPI_STORE_F32  lane = output column; each warp store writes one token's
+//                  32 consecutive FP32 outputs (a whole 128-byte line).
+// GemmArgs here: sfa = the token operand's scale blocks (per window), sfb =
+// the weights' ([E][R/128][K/128][512]), b_rows_per_expert / sfb_rtiles /
+// b_up_off describe the weights, n_tiles = 128-row weight tiles per window.
+
+constexpr int WA_WIN = 64;
+constexpr uint32_t WA_B_BYTES = WA_WIN * 128;
+constexpr uint32_t WA_ACC_COLS = 128;
+constexpr uint32_t WA_SF_BASE = 2 * WA_ACC_COLS;
+template <int NA> __host__ __device__ constexpr uint32_t wa_stage_bytes() {
+  return NA * A_BYTES + WA_B_BYTES + NA * 1024 + 1024;
+}
+template <int NA> __host__ __device__ constexpr int wa_stages() { return NA == 2 ? 4 : 6; }
+
+template <int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    k_tc_gemm_wa(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX, GemmArgs g) {
+  constexpr bool SWIGLU = EPI == EPI_SWIGLU_MX;
+  constexpr int NA = SWIGLU ? 2 : 1;  // weight tiles per stage: gate + up, or down
+  constexpr int NS = wa_stages<NA>();
+  constexpr uint32_t SB = wa_stage_bytes<NA>();
+  constexpr uint32_t OFF_B = NA * A_BYTES, OFF_SFA = OFF_B + WA_B_BYTES, OFF_SFB = OFF_SFA + NA * 1024;
+  constexpr uint32_t SF_COLS = 8 * NA + 8;  // TMEM scale columns per stage
+  static_assert(WA_SF_BASE + NS * SF_COLS <= TMEM_COLS, "TMEM columns");
+  extern __shared__ __align__(1024) uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[NS], empty[NS], acc_full[2], acc_empty[2], drain;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&acc_full[b], 1);
+      tc::mbar_init(&acc_empty[b], 32 * EPI_WARPS);
+    }
+    tc::mbar_init(&drain, 1);
+    tc::mbar_fence_init();
+    abort_flag = 0;
+    tc::prefetch_tensormap(&mapW);
+    tc::prefetch_tensormap(&mapX);
+  }
+  if (warp == 1) tc::tmem_alloc(&tmem_base, TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const int total = *g.num_mt * g.n_tiles;
+  const int nks = g.K / 256;
+  const int kgroups = g.K / 128;
+
+  auto fail = [&]() {
+    atomicCAS(g.status, 0, (int)MOE_DEV_TIMEOUT);
+    atomicExch(&abort_flag, 1);
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer
+    uint32_t stage = 0, phase = 0;
+    for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
+      const int nt = t % g.n_tiles;
+      const MTile m = g.mt[t / g.n_tiles];
+      const int nb = (m.rows + 15) >> 4;  // 16-row token boxes
+      const int wr0 = m.e * g.b_rows_per_expert + nt * BM;
+      const size_t rt0 = (size_t)m.e * g.sfb_rtiles + nt;
+      const size_t rt1 = rt0 + g.b_up_off / BM;
+      const size_t win = (size_t)(m.prow0 / WA_WIN);
+      const uint32_t bytes = NA * (A_BYTES + 1024) + (uint32_t)nb * 2048 + 1024;
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
+        uint8_t* st = dsm + stage * SB;
+        tc::mbar_expect_tx(&full[stage], bytes);
+        tc::tma_load_2d(st, &mapW, ks * 128, wr0, &full[stage]);
+        if (SWIGLU) tc::tma_load_2d(st + A_BYTES, &mapW, ks * 128, wr0 + g.b_up_off, &full[stage]);
+        for (int b = 0; b < nb; ++b)
+          tc::tma_load_2d(st + OFF_B + b * 2048, &mapX, ks * 128, m.prow0 + 16 * b, &full[stage]);
+        tc::bulk_load(st + OFF_SFA, g.sfb + (rt0 * kgroups + 2 * ks) * 512, 1024, &full[stage]);
+        if (SWIGLU) tc::bulk_load(st + OFF_SFA + 1024, g.sfb + (rt1 * kgroups + 2 * ks) * 512, 1024, &full[stage]);
+        tc::bulk_load(st + OFF_SFB, g.sfa + (win * kgroups + 2 * ks) * 512, 1024, &full[stage]);
+        if (++stage == NS) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    uint32_t stage = 0, phase = 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x, ++it) {
+      const int buf = it & 1;
+      if (!tc::mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
+      tc::fence_after_sync();
+      const MTile m = g.mt[t / g.n_tiles];
+      const int N = (m.rows + 15) & ~15;
+      const uint32_t acc = tmem + buf * WA_ACC_COLS;
+      bool ok = true;
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!tc::mbar_wait(&full[stage], phase, g.limit_ns, &abort_flag)) { fail(); ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t sa = tc::smem_u32(dsm + stage * SB);
+        const uint32_t sb = sa + OFF_B, ssa = sa + OFF_SFA, ssb = sa + OFF_SFB;
+        // weight tile a's scales at columns tsf + 8a (+4 for the second K group), the tokens' at tsf + 8 NA
+        const uint32_t tsf = tmem + WA_SF_BASE + stage * SF_COLS;
+        tc::sf_copy(tsf + 0, tc::desc_sf(ssa));
+        tc::sf_copy(tsf + 4, tc::desc_sf(ssa + 512));
+        if (SWIGLU) {
+          tc::sf_copy(tsf + 8, tc::desc_sf(ssa + 1024));
+          tc::sf_copy(tsf + 12, tc::desc_sf(ssa + 1536));
+        }
+        tc::sf_copy(tsf + 8 * NA, tc::desc_sf(ssb));
+        tc::sf_copy(tsf + 8 * NA + 4, tc::desc_sf(ssb + 512));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int grp = kk >> 1, id = (kk & 1) * 2;
+          const uint32_t idesc = tc::idesc_mxf4(BM, N, id, id);
+          const uint64_t bdesc = tc::desc_sw128(sb + kk * 32);
+          tc::mma_mxf4(acc, tc::desc_sw128(sa + kk * 32), bdesc, idesc, tsf + 4 * grp, tsf + 8 * NA + 4 * grp,
+                       (ks | kk) != 0);
+          if (SWIGLU)
+            tc::mma_mxf4(acc + 64, tc::desc_sw128(sa + A_BYTES + kk * 32), bdesc, idesc, tsf + 8 + 4 * grp,
+                         tsf + 8 * NA + 4 * grp, (ks | kk) != 0);
+        }
+        tc::mma_commit(&empty[stage]);
+        if (++stage == NS) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      tc::mma_commit(&acc_full[buf]);
+    }
+    tc::mma_commit(&drain);
+    if (!tc::mbar_wait(&drain, 0, g.limit_ns, &abort_flag)) fail();
+  } else if (warp >= 2) {
+    // ---------------- epilogue: lane <-> weight row 32q + lane, token columns 16cq .. 16cq + 15
+    const int q = warp & 3;
+    const int cq = (warp - 2) >> 2;
+    const int j0 = 16 * cq;
+    const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16);
+    int it = 0;
+    for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const int nt = t % g.n_tiles;
+      const MTile m = g.mt[t / g.n_tiles];
+      if (!tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, g.limit_ns, &abort_flag)) { fail(); break; }
+      tc::fence_after_sync();
+      const bool active = j0 < ((m.rows + 15) & ~15);  // the same in the whole warp
+      float va[16], vb[16];
+      if (active) {
+        tc::tmem_ld16(tlane + buf * WA_ACC_COLS + j0, va);
+        if (SWIGLU) tc::tmem_ld16(tlane + buf * WA_ACC_COLS + 64 + j0, vb);
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&acc_empty[buf]);  // the accumulator is free for the tile after next
+      if (!active) continue;
+      if (EPI == EPI_SWIGLU_MX) {
+        const int c0 = nt * BM + q * 32;  // this warp's MXFP4 block of h columns
+        const int hgroups = g.h_cols / 128;
+        uint8_t* hs = reinterpret_cast<uint8_t*>(g.hs) + ((size_t)(m.prow0 / WA_WIN) * hgroups + nt) * 512;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float h = silu(va[j]) * vb[j];
+          float amax = fabsf(h);
+#pragma unroll
+          for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const int ex = mx_scale_exp(amax);
+          uint32_t v = e2m1_rne(h * pow2_neg(ex)) << (4 * (lane & 7));
+          v |= __shfl_xor_sync(0xffffffffu, v, 1);
+          v |= __shfl_xor_sync(0xffffffffu, v, 2);
+          v |= __shfl_xor_sync(0xffffffffu, v, 4);
+          const int r = j0 + j;  // window row
+          if ((lane & 7) == 0)
+            *reinterpret_cast<uint32_t*>(g.hq + (size_t)(m.prow0 + r) * (g.h_cols / 2) + c0 / 2 + lane / 2) = v;
+          if (lane == 0) hs[((r % 32) * 4 + r / 32) * 4 + q] = (uint8_t)(ex + 127);
+        }
+      } else {
+        float* dst = g.out + (size_t)(m.srow0 + j0) * g.ldo + nt * BM + q * 32 + lane;
+        const int nj = min(16, m.rows - j0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < nj) dst[(size_t)j * g.ldo] = va[j];
       }
     }
   }
@@ -401,7 +624,8 @@ __global__ void __launch_bounds__(128) k_copy_h(int n, int I, const int* __restr
                                                 uint8_t* __restrict__ hq_out, uint8_t* __restrict__ hs_out) {
   const int m = threadIdx.x;
   const int groups = I / 128;
-  if (*hpath == 0) {
+  const int path = *hpath & 0xff;  // written by a byte-wise memset
+  if (path == 0) {
     const int p = blockIdx.x * 128 + m;
     if (p >= n) return;
     for (int c = 0; c < I / 32; ++c)
@@ -409,6 +633,8 @@ __global__ void __launch_bounds__(128) k_copy_h(int n, int I, const int* __restr
     for (int c = 0; c < I / 32; ++c) hs_out[(size_t)p * (I / 32) + c] = hs_sorted[(size_t)p * (I / 32) + c];
     return;
   }
+  // h in the padded order: windows of 128 rows (hpath 1) or 64 (hpath 2)
+  const int win = path == 2 ? 64 : 128;
   if ((int)blockIdx.x >= *num_tiles) return;
   const MTile t = tiles[blockIdx.x];
   if (m >= t.rows) return;
@@ -416,7 +642,7 @@ __global__ void __launch_bounds__(128) k_copy_h(int n, int I, const int* __restr
   for (int c = 0; c < I / 32; ++c)
     reinterpret_cast<uint4*>(hq_out + (size_t)p * (I / 2))[c] = reinterpret_cast<const uint4*>(hq_perm + (size_t)r * (I / 2))[c];
   for (int g = 0; g < groups; ++g) {
-    const uint32_t w = hs_mma[((size_t)(r / BM) * groups + g) * 128 + (m % 32) * 4 + (m / 32)];
+    const uint32_t w = hs_mma[((size_t)(r / win) * groups + g) * 128 + (m % 32) * 4 + (m / 32)];
     for (int b = 0; b < 4; ++b) hs_out[(size_t)p * (I / 32) + 4 * g + b] = (uint8_t)(w >> (8 * b));
   }
 }
@@ -425,7 +651,9 @@ cudaError_t launch_copy_h(const Shape& sh, const int* hpath, const uint8_t* hq_s
                           const TcWorkspace& w, uint8_t* hq_out, uint8_t* hs_out, cudaStream_t s) {
   const int n = sh.T * sh.k;
   if (n == 0) return cudaSuccess;
-  const int blocks = tc_routed_enabled(n) ? max(tc_padded_rows(n, sh.E) / BM, (n + 127) / 128) : (n + 127) / 128;
+  const int blocks = tc_routed_enabled(n) ? max(max(tc_padded_rows(n, sh.E) / BM, tc_padded_rows_win(n, sh.E, 64) / 64),
+                                                (n + 127) / 128)
+                                          : (n + 127) / 128;
   k_copy_h<<<blocks, 128, 0, s>>>(n, sh.I, hpath, hq_sorted, hs_sorted, reinterpret_cast<const MTile*>(w.mtiles),
                                   w.num_mt, w.hq_perm, reinterpret_cast<const uint32_t*>(w.hs_mma), hq_out, hs_out);
   return cudaGetLastError();
@@ -483,20 +711,38 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
   return cudaGetLastError();
 }
 
+template <int EPI>
+cudaError_t launch_gemm_wa(const CUtensorMap& w, const CUtensorMap& x, const GemmArgs& g, int max_tiles,
+                           cudaStream_t s) {
+  constexpr int NA = EPI == EPI_SWIGLU_MX ? 2 : 1;
+  const size_t smem = (size_t)wa_stages<NA>() * wa_stage_bytes<NA>() + 1024;
+  const void* fn = (const void*)k_tc_gemm_wa<EPI>;
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int grid = max(1, min(max_tiles, sm_count()));
+  k_tc_gemm_wa<EPI><<<grid, TC_THREADS, smem, s>>>(w, x, g);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+bool tc_weights_as_a(int n, int E, int mode) {
+  return mode == TC_GEMM_WEIGHTS_AS_A || (mode == TC_GEMM_AUTO && n <= WA_MAX_AVG_ROWS * E);
+}
 
 cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const TcWorkspace& w, const uint8_t* xq,
                                  const uint8_t* xs, const int* offsets, const int* perm, float* y_assign,
-                                 int* status, uint64_t limit_ns, cudaStream_t s) {
+                                 int* status, uint64_t limit_ns, bool wa, cudaStream_t s) {
   const int H = sh.H, I = sh.I, E = sh.E;
   const int n = sh.T * sh.k;
   if (n == 0) return cudaSuccess;
-  const int rmax = tc_padded_rows(n, E);
+  const int win = wa ? WA_WIN : BM;
+  const int rmax = tc_padded_rows_win(n, E, win);
   cudaError_t err;
-  k_build_mtiles<<<1, 256, 0, s>>>(offsets, E, w.poff, reinterpret_cast<MTile*>(w.mtiles), w.num_mt);
+  k_build_mtiles<<<1, 256, 0, s>>>(offsets, E, win, w.poff, reinterpret_cast<MTile*>(w.mtiles), w.num_mt);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   k_gather_mx_rows<<<rmax, 128, 0, s>>>(xq, xs, H, sh.k, perm, reinterpret_cast<const MTile*>(w.mtiles), w.num_mt,
-                                        w.xq_perm, reinterpret_cast<uint32_t*>(w.xs_mma));
+                                        win, wa ? 1 : 0, w.xq_perm, reinterpret_cast<uint32_t*>(w.xs_mma));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const uint8_t* w13s_mma = ex.w13s_mma;
   const uint8_t* w2s_mma = ex.w2s_mma;
@@ -506,8 +752,46 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
     w13s_mma = w.w13s_mma;
     w2s_mma = w.w2s_mma;
   }
-  const int max_mt = rmax / BM;
+  const int max_mt = rmax / win;
   CUtensorMap ma, mb;
+  if (wa) {
+    // gate/up: A = W13 [E*2I][H/2], B = gathered activations [rmax][H/2] in 16-row boxes
+    if ((err = make_map(&ma, ex.w13, (uint64_t)E * 2 * I, H / 2)) != cudaSuccess) return err;
+    if ((err = make_map(&mb, w.xq_perm, rmax, H / 2, 16)) != cudaSuccess) return err;
+    GemmArgs g1{};
+    g1.K = H;
+    g1.n_tiles = I / BM;
+    g1.num_mt = w.num_mt;
+    g1.mt = reinterpret_cast<const MTile*>(w.mtiles);
+    g1.b_rows_per_expert = 2 * I;
+    g1.b_up_off = I;
+    g1.sfa = w.xs_mma;
+    g1.sfb = w13s_mma;
+    g1.sfb_rtiles = 2 * I / BM;
+    g1.hq = w.hq_perm;
+    g1.hs = reinterpret_cast<uint32_t*>(w.hs_mma);
+    g1.h_cols = I;
+    g1.status = status;
+    g1.limit_ns = limit_ns;
+    if ((err = launch_gemm_wa<EPI_SWIGLU_MX>(ma, mb, g1, max_mt * g1.n_tiles, s)) != cudaSuccess) return err;
+    // down: A = W2 [E*H][I/2], B = requantised h [rmax][I/2]
+    if ((err = make_map(&ma, ex.w2, (uint64_t)E * H, I / 2)) != cudaSuccess) return err;
+    if ((err = make_map(&mb, w.hq_perm, rmax, I / 2, 16)) != cudaSuccess) return err;
+    GemmArgs g2{};
+    g2.K = I;
+    g2.n_tiles = H / BM;
+    g2.num_mt = w.num_mt;
+    g2.mt = reinterpret_cast<const MTile*>(w.mtiles);
+    g2.b_rows_per_expert = H;
+    g2.sfa = w.hs_mma;
+    g2.sfb = w2s_mma;
+    g2.sfb_rtiles = H / BM;
+    g2.out = y_assign;
+    g2.ldo = H;
+    g2.status = status;
+    g2.limit_ns = limit_ns;
+    return launch_gemm_wa<EPI_STORE_F32>(ma, mb, g2, max_mt * g2.n_tiles, s);
+  }
   // gate/up: A = gathered activations [rmax][H/2], B = W13 [E*2I][H/2]
   if ((err = make_map(&ma, w.xq_perm, rmax, H / 2)) != cudaSuccess) return err;
   if ((err = make_map(&mb, ex.w13, (uint64_t)E * 2 * I, H / 2)) != cudaSuccess) return err;

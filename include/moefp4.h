@@ -272,6 +272,15 @@ MOE_API moe_status_t moe_layer_decode_noalloc(const moe_layer_desc_t* desc, cons
  * finishing its work; the workspace must then be zero-filled again. */
 MOE_API void moe_set_wait_limit_ns(uint64_t ns);
 
+/* Orientation of the routed-expert tensor-core GEMMs of later
+ * moe_expert_ffn_fp4 / moe_layer_forward calls in this process (MXFP4
+ * experts, from 256 assignments): 0 = automatic (the default: weights as A
+ * when the average expert has at most 32 assignments), 1 = 128-token tiles as
+ * the MMA's A operand, 2 = 128 weight rows as A and up to 64 of an expert's
+ * tokens as B.  Results agree within rounding; the choice only moves time.
+ * Other values return MOE_ERR_INVALID_ARG and change nothing. */
+MOE_API moe_status_t moe_set_routed_gemm(int32_t mode);
+
 /* Test hook: copies the MXFP4-requantised intermediate h of the last
  * moe_expert_ffn_fp4 / moe_layer_forward call made with this workspace (A6)
  * into caller buffers in sorted-assignment order: codes [T*top_k, I/2] and

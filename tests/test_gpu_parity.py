@@ -386,7 +386,16 @@ def test_decode_token_counts(T, prepared):
     dev.set_prepared(True)
 
 
-def test_batch128_forward_sampled():
+@pytest.fixture
+def routed_gemm():
+    """Sets the routed GEMM orientation for one test, automatic afterwards."""
+    yield M.moe_set_routed_gemm
+    M.moe_set_routed_gemm(M.ROUTED_GEMM_AUTO)
+
+
+@pytest.mark.parametrize("gemm", [M.ROUTED_GEMM_AUTO, M.ROUTED_GEMM_TOKENS_AS_A], ids=["auto", "tokens_as_A"])
+def test_batch128_forward_sampled(gemm, routed_gemm):
+    routed_gemm(gemm)
     wl, lay, dev, cache = _workload("batch128")
     out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
     torch.cuda.synchronize()
@@ -412,13 +421,18 @@ def test_prefill8k_forward_sampled():
 # ---------------------------------------------------- tensor-core path shapes
 
 
+@pytest.mark.parametrize("gemm", [M.ROUTED_GEMM_TOKENS_AS_A, M.ROUTED_GEMM_WEIGHTS_AS_A],
+                         ids=["tokens_as_A", "weights_as_A"])
 @pytest.mark.parametrize("shape", [(64, 256, 256, 8, 4), (160, 512, 256, 16, 4), (130, 256, 512, 4, 2),
-                                   (300, 512, 512, 32, 8)])
-def test_tensor_core_path_shapes(shape):
+                                   (300, 512, 512, 32, 8), (90, 256, 256, 64, 3)])
+def test_tensor_core_path_shapes(shape, gemm, routed_gemm):
     """From 256 assignments the MXFP4 experts run on tcgen05 tensor cores
-    (and the shared expert from 128 tokens): ragged per-expert tiles, several
-    K stages, both entry points."""
+    (and the shared expert from 128 tokens), in either orientation of the
+    routed GEMMs: ragged per-expert tiles and token windows (experts with
+    1-15, 16-64 and more than 64 assignments), several K stages, both entry
+    points."""
     T, H, I, E, k = shape
+    routed_gemm(gemm)
     wl = W.Workload("tc", T, H, I, E, k, W.MXFP4, 23, 0.05)
     lay = W.generate(wl)
     dev = DeviceLayer(lay, H, I, E, k, wl.fmt, T_max=T)
