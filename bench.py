@@ -344,7 +344,8 @@ def run_ours(args):
                        nl, nl * (wl.E * expert_bytes(wl) + 3 * wl.H * wl.I * 2) / 1e9),
                    "graph": "%d replays of a %d-step CUDA graph" % (R, S), "parallelism": "replicas"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": peak_kind,
+                     "traffic": NCU_TRAFFIC.get((wl.name, "k_decode_tc")) if fused and layers[0].prepared else None,
+                     "peak_kind": peak_kind,
                      "kernel": ("k_decode_tc" if layers[0].prepared and wl.H % 256 == 0 and wl.I % 256 == 0
                                 else "k_fused_decode") if fused else "unfused sequence",
                      "kernel_us": float(durs.mean() * 1e6),
@@ -356,6 +357,11 @@ def run_ours(args):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
+
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the ncu
+# capture summarised in profiles/k_decode_tc_decode1.md (same kernel source).
+NCU_TRAFFIC = {("decode1", "k_decode_tc"): 82.10e6}
 
 
 def main():
