@@ -107,7 +107,7 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
   if (shd.w13) {
     uint16_t* h = at<uint16_t>(ws, L.h_shared);
     if (d->T >= TC_MIN_T_SHARED && d->H % 256 == 0)
-      MOE_CUDA(launch_shared_tc(sh, shd, x, h, y_shared, status, limit, s));
+      MOE_CUDA(launch_shared_tc(sh, shd, x, h, y_shared, at<float>(ws, L.sh_part), status, limit, s));
     else
       MOE_CUDA(launch_shared_simt(sh, shd, x, h, y_shared, s));
   }

@@ -71,8 +71,9 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
 // orientation mode (TC_GEMM_*).
 bool tc_weights_as_a(int n, int E, int mode);
 // A8 on tensor cores
+// parts: split-K scratch, float [max(s1 * T * 2I, s2 * T * H)] (see shared_ksplit)
 cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
-                             float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s);
+                             float* y_shared, float* parts, int* status, uint64_t limit_ns, cudaStream_t s);
 // Copies the requantised h to sorted-assignment order (either layout).
 cudaError_t launch_copy_h(const Shape& sh, const int* hpath, const uint8_t* hq_sorted, const uint8_t* hs_sorted,
                           const TcWorkspace& w, uint8_t* hq_out, uint8_t* hs_out, cudaStream_t s);

@@ -18,7 +18,7 @@ constexpr int MAX_DECODE_T = 16;   // fused single-launch decode range
 constexpr int PERM_CHUNK = 1024;   // assignments ranked per block in the permutation
 constexpr int TC_MIN_ASSIGN = 256; // routed experts on tensor cores from this many assignments
 constexpr int TC_MIN_T_SHARED = 128; // shared expert on tensor cores from this many tokens
-constexpr int ROUTER_SMS = 152;       // SMs the batched router's split-K is balanced for
+constexpr int SPLIT_SMS = 152;        // SMs the split-K counts are balanced for
 
 // Tensor-core decode (T <= MAX_DECODE_T): one block per SM, at most this many.
 constexpr int DC_MAX_GRID = 256;
@@ -52,19 +52,44 @@ MOE_HD inline DcSplits dc_splits(int T, int H, int I, int E, int k, int grid) {
 
 // Split-K parts of the batched router (T > 512): enough 128 x 128 tiles for
 // two blocks per SM of a 152-SM GPU, at most 8.
-// The batched router runs two 256-thread blocks per SM; the split count S
-// (1..8) minimises the busiest SM's share of the work, ceil(tiles S / SMs) / S
-// blocks of 1/S of a tile each (the smallest S on ties).
-MOE_HD inline int router_splits(int T, int E) {
-  if (T <= 512) return 1;
+// Split-K count of the router.  T <= 16: one pass per expert row, no split.
+// 16 < T <= 512 (64 x 64 tiles): the largest power of two that keeps K parts
+// a multiple of 32 elements, at least 64 long, and the grid within 608
+// blocks.  Larger T (128 x 128 tiles, two 256-thread blocks per SM): S in
+// 1..8 minimising the busiest SM's share, ceil(tiles S / SMs) / S (the
+// smallest S on ties).
+MOE_HD inline int router_splits(int T, int E, int H) {
+  if (T <= 16) return 1;
+  if (T <= 512) {
+    const int tiles = ((T + 63) / 64) * ((E + 63) / 64);
+    int s = 1;
+    while (H % (2 * s * 32) == 0 && H / (2 * s) >= 64 && tiles * 2 * s <= 608) s *= 2;
+    return s;
+  }
   const int tiles = ((T + 127) / 128) * ((E + 127) / 128);
   int best = 1;
   for (int s = 2; s <= 8; ++s)
-    if ((int64_t)((tiles * s + ROUTER_SMS - 1) / ROUTER_SMS) * best <
-        (int64_t)((tiles * best + ROUTER_SMS - 1) / ROUTER_SMS) * s)
+    if ((int64_t)((tiles * s + SPLIT_SMS - 1) / SPLIT_SMS) * best <
+        (int64_t)((tiles * best + SPLIT_SMS - 1) / SPLIT_SMS) * s)
       best = s;
   return best;
 }
+
+// Split-K count of a dense tensor-core GEMM of the shared expert with `tiles`
+// output tiles and `nks` K stages: enough parts to give every SM a unit when
+// the tiles alone do not (1 from SPLIT_SMS / 2 tiles up), at most 16 and
+// at most the stages.
+MOE_HD inline int shared_ksplit(int tiles, int nks) {
+  if (2 * tiles >= SPLIT_SMS) return 1;
+  int s = SPLIT_SMS / tiles;
+  if (s > 16) s = 16;
+  if (s > nks) s = nks;
+  return s < 1 ? 1 : s;
+}
+// Output tiles of the shared expert's gate/up (first) and down GEMMs on
+// tensor cores: 128 tokens x 256 weight rows.
+MOE_HD inline int shared_tiles_gu(int T, int I) { return (T + 127) / 128 * (2 * I / 256); }
+MOE_HD inline int shared_tiles_dn(int T, int H) { return (T + 127) / 128 * (H / 256); }
 
 // Rows of the per-expert padded order (each expert's rows rounded up to 128).
 MOE_HD inline int tc_padded_rows(int n, int E) { return ((n + E * 127) + 127) / 128 * 128; }
@@ -129,6 +154,7 @@ struct WsLayout {
   size_t h_shared;     // bf16 [T, I]
   size_t y_assign;     // float [T*k, H]   (layer_forward only)
   size_t y_shared;     // float [T, H]     (layer_forward only)
+  size_t sh_part;      // float split-K parts of the shared expert's GEMMs
   // tensor-core path (present when the routed experts run on tensor cores)
   size_t tc_poff;      // int [E+1]
   size_t tc_mtiles;    // 16-byte tile descriptors [padded rows / 128]
@@ -173,8 +199,8 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.dc_rowmax = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * MAX_TOPK);
   L.zero_end = o;
   L.logits = take(sizeof(float) * (size_t)T * E);
-  const int rs = router_splits(T, E);
-  L.rt_part = take(rs > 1 ? sizeof(float) * rs * (size_t)T * E : 0);
+  const int rs = router_splits(T, E, H);
+  L.rt_part = take(rs > 1 || (T > 16 && T <= 512) ? sizeof(float) * rs * (size_t)T * E : 0);
   L.ids = take(sizeof(int) * n);
   L.wts = take(sizeof(float) * n);
   L.xq = take((size_t)T * H / 2);
@@ -191,6 +217,13 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.h_shared = take((size_t)2 * T * I);
   L.y_assign = take(sizeof(float) * n * H);
   L.y_shared = take(sizeof(float) * (size_t)T * H);
+  {  // split-K partial sums of the shared expert's tensor-core GEMMs
+    const bool shtc = T >= TC_MIN_T_SHARED && H % 256 == 0;
+    const size_t s1 = shtc ? shared_ksplit(shared_tiles_gu(T, I), H / 64) : 1;
+    const size_t s2 = shtc ? shared_ksplit(shared_tiles_dn(T, H), I / 64) : 1;
+    const size_t a = s1 > 1 ? s1 * T * 2 * (size_t)I : 0, b = s2 > 1 ? s2 * T * (size_t)H : 0;
+    L.sh_part = take(sizeof(float) * (a > b ? a : b));
+  }
   const bool tc = tc_routed_enabled((int)n);
   const size_t R = tc ? (size_t)tc_padded_rows((int)n, E) : 0;
   // 64-row windows (weights-as-A GEMMs): no more rows, up to twice the tiles

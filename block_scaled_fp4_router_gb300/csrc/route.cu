@@ -34,7 +34,7 @@ cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* code
 
 // ------------------------------------------------------------------ A1
 
-// Router up to a few hundred tokens: one block per (expert row, tile of 16 tokens); the 256
+// Router up to 16 tokens: one block per (expert row, tile of 16 tokens); the 256
 // threads stride over H eight elements at a time (two float4 of Wr, one uint4
 // of x per token), then reduce over lanes and warps in a fixed order.
 __global__ void __launch_bounds__(256) k_router_gemv(const uint16_t* __restrict__ x,
@@ -172,6 +172,75 @@ __global__ void __launch_bounds__(256) k_router_sgemm(const uint16_t* __restrict
   }
 }
 
+// Router for 16 < T <= 512: a 64-token x 64-expert tile and one K part of
+// H / S elements per block (256 threads, 4 x 4 outputs each at rows 4ty..
+// and columns 4tx..), K staged 32 at a time through shared memory, FP32 FMA
+// in k order.  Part p writes out[p] ([S][T][E]); k_router_sum adds the parts
+// in ascending order.  Enough blocks to cover the GPU where a per-row pass
+// would re-read x once per expert.
+constexpr int RSM = 64, RSK = 32;
+__global__ void __launch_bounds__(256) k_router_splitk(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                                                       float* __restrict__ out, int T, int H, int E, int S) {
+  __shared__ __align__(16) float As[RSK][RSM + 4];
+  __shared__ __align__(16) float Bs[RSK][RSM + 4];
+  const int m0 = blockIdx.x * RSM, n0 = blockIdx.y * RSM, p = blockIdx.z;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int kc = H / S, kb = p * kc;
+  // loader: row tid / 4 of each tile, 8 consecutive k at 8 (tid % 4)
+  const int lr = tid >> 2, lc = (tid & 3) * 8;
+  const bool xa = m0 + lr < T, wa = n0 + lr < E;
+  const uint16_t* xrow = x + (size_t)(xa ? m0 + lr : 0) * H + kb + lc;
+  const float* wrow = wr + (size_t)(wa ? n0 + lr : 0) * H + kb + lc;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  for (int k0 = 0; k0 < kc; k0 += RSK) {
+    const uint4 xv = xa ? __ldg(reinterpret_cast<const uint4*>(xrow + k0)) : make_uint4(0, 0, 0, 0);
+    const float4 w0 = wa ? __ldg(reinterpret_cast<const float4*>(wrow + k0)) : make_float4(0, 0, 0, 0);
+    const float4 w1 = wa ? __ldg(reinterpret_cast<const float4*>(wrow + k0 + 4)) : make_float4(0, 0, 0, 0);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      As[lc + 2 * i][lr] = bf16_lo(xw[i]);
+      As[lc + 2 * i + 1][lr] = bf16_hi(xw[i]);
+    }
+    Bs[lc + 0][lr] = w0.x;
+    Bs[lc + 1][lr] = w0.y;
+    Bs[lc + 2][lr] = w0.z;
+    Bs[lc + 3][lr] = w0.w;
+    Bs[lc + 4][lr] = w1.x;
+    Bs[lc + 5][lr] = w1.y;
+    Bs[lc + 6][lr] = w1.z;
+    Bs[lc + 7][lr] = w1.w;
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < RSK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  float* o = out + (size_t)p * T * E;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n < E) o[(size_t)m * E + n] = acc[i][j];
+    }
+  }
+}
+
 // logits = sum over the S split-K parts in ascending order, + bias.
 __global__ void __launch_bounds__(256) k_router_sum(const float* __restrict__ part, const float* __restrict__ bias,
                                                     float* __restrict__ logits, int T, int E, int S) {
@@ -186,21 +255,25 @@ __global__ void __launch_bounds__(256) k_router_sum(const float* __restrict__ pa
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, float* part, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  // Up to a few hundred tokens one block per (expert row, 16 tokens) keeps
-  // every SM busy (the x re-reads hit L2); beyond that the tiled GEMM, split
-  // along K until the grid covers the GPU twice.
-  if (T <= 512) {
+  // Up to 16 tokens one block per expert row; up to 512 split-K 64 x 64
+  // tiles; beyond that the 128 x 128 tiled GEMM, split along K to balance
+  // the SMs.
+  const int S = router_splits(T, E, H);
+  cudaError_t err;
+  if (T <= 16) {
     dim3 grid(E, (T + 15) / 16);
     k_router_gemv<<<grid, 256, 0, s>>>(x, wr, bias, logits, T, H, E);
     return cudaGetLastError();
   }
-  const int tiles = ((T + RBM - 1) / RBM) * ((E + RBN - 1) / RBN);
-  const int S = router_splits(T, E);
-  dim3 grid((T + RBM - 1) / RBM, (E + RBN - 1) / RBN, S);
-  (void)tiles;
-  k_router_sgemm<<<grid, 256, 0, s>>>(x, wr, bias, S == 1 ? logits : part, T, H, E, S);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess || S == 1) return err;
+  if (T <= 512) {
+    dim3 grid((T + RSM - 1) / RSM, (E + RSM - 1) / RSM, S);
+    k_router_splitk<<<grid, 256, 0, s>>>(x, wr, part, T, H, E, S);
+  } else {
+    dim3 grid((T + RBM - 1) / RBM, (E + RBN - 1) / RBN, S);
+    k_router_sgemm<<<grid, 256, 0, s>>>(x, wr, bias, S == 1 ? logits : part, T, H, E, S);
+  }
+  err = cudaGetLastError();
+  if (err != cudaSuccess || (S == 1 && T > 512)) return err;
   const size_t n = (size_t)T * E;
   k_router_sum<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, bias, logits, T, E, S);
   return cudaGetLastError();

@@ -77,12 +77,17 @@ __global__ void __launch_bounds__(256) k_build_mtiles(const int* __restrict__ of
                                                       int* __restrict__ poff, MTile* __restrict__ tiles,
                                                       int* __restrict__ num_tiles) {
   __shared__ int s_poff[MAX_E + 1];
+  __shared__ int s_pad[MAX_E];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {  // the offsets are read in parallel
+    const int cnt = offsets[e + 1] - offsets[e];
+    s_pad[e] = (cnt + win - 1) / win * win;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     int p = 0;
     for (int e = 0; e < E; ++e) {
       s_poff[e] = p;
-      const int cnt = offsets[e + 1] - offsets[e];
-      p += (cnt + win - 1) / win * win;
+      p += s_pad[e];
     }
     s_poff[E] = p;
     *num_tiles = p / win;
@@ -178,18 +183,26 @@ struct GemmArgs {
   uint32_t* hs;            // EPI_SWIGLU_MX: scales, MMA layout over I
   int h_cols;              // I (SwiGLU epilogues)
   uint16_t* h_bf16;        // EPI_SWIGLU_BF16: [rows][I]
-  float* out;              // EPI_STORE_F32: [rows][ldo]
+  float* out;              // EPI_STORE_F32: [rows][ldo] (split-K: part p at out + p * part_stride)
   int ldo;
+  int ksplit;              // dense: K parts per output tile (0 or 1: none)
+  size_t part_stride;
   int* status;
   uint64_t limit_ns;
 };
 
+__device__ __forceinline__ int ksplit_of(const GemmArgs& g) { return g.ksplit > 1 ? g.ksplit : 1; }
+
+// Tile t: A tile mti, B tile nt and K part kp (split-K dense GEMMs).
+// A grouped caller may pass the tile's MTile, loaded ahead (pre).
 __device__ __forceinline__ void tile_coords(const GemmArgs& g, bool grouped, int t, int& a_row, int& e, int& rows,
-                                            int& srow0, int& nt, int& mti) {
+                                            int& srow0, int& nt, int& mti, int& kp, const MTile* pre = nullptr) {
+  kp = t % ksplit_of(g);
+  t /= ksplit_of(g);
   mti = t / g.n_tiles;
   nt = t % g.n_tiles;
   if (grouped) {
-    const MTile m = g.mt[mti];
+    const MTile m = pre ? *pre : g.mt[mti];
     a_row = m.prow0;
     e = m.e;
     rows = m.rows;
@@ -233,7 +246,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
   const int num_mt = GROUPED ? *g.num_mt : g.num_mt_dense;
-  const int total = num_mt * g.n_tiles;
+  const int total = num_mt * g.n_tiles * ksplit_of(g);
   const int nks = g.K / (KIND == KIND_FP4 ? 256 : 64);
   const int kgroups = g.K / 128;  // FP4 scale groups per row
 
@@ -245,13 +258,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 0 && lane == 0) {
     // ---------------- producer
     uint32_t stage = 0, phase = 0;
+    // grouped: each tile's MTile is loaded a tile ahead, off the stream's critical path
+    auto mt_of = [&](int t) { return GROUPED && t < total ? g.mt[(t / ksplit_of(g)) / g.n_tiles] : MTile{}; };
+    MTile mn = mt_of(blockIdx.x);
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
-      int a_row, e, rows, srow0, nt, mti;
-      tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti);
+      int a_row, e, rows, srow0, nt, mti, kp;
+      const MTile m = mn;
+      tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti, kp, &m);
+      mn = mt_of(t + gridDim.x);
       const int b_base = e * g.b_rows_per_expert;
       const int b0 = SWIGLU ? b_base + nt * (BN / 2) : b_base + nt * BN;
       const int b1 = SWIGLU ? b0 + g.b_up_off : b0 + BN / 2;
-      for (int ks = 0; ks < nks; ++ks) {
+      const int ks1 = (kp + 1) * nks / ksplit_of(g);
+      for (int ks = kp * nks / ksplit_of(g); ks < ks1; ++ks) {
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
         uint8_t* sa = dsm + stage * SB;
         uint8_t* sb = sa + A_BYTES;
@@ -280,7 +299,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (!tc::mbar_wait(&acc_empty, acc_phase ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
       tc::fence_after_sync();
       bool ok = true;
-      for (int ks = 0; ks < nks; ++ks) {
+      const int kp = t % ksplit_of(g);
+      const int ks0 = kp * nks / ksplit_of(g), ks1 = (kp + 1) * nks / ksplit_of(g);
+      for (int ks = ks0; ks < ks1; ++ks) {
         if (!tc::mbar_wait(&full[stage], phase, g.limit_ns, &abort_flag)) { fail(); ok = false; break; }
         tc::fence_after_sync();
         const uint32_t sa = tc::smem_u32(dsm + stage * SB);
@@ -299,12 +320,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const int grp = kk >> 1, id = (kk & 1) * 2;
             tc::mma_mxf4(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32),
-                         tc::idesc_mxf4(BM, BN, id, id), ta + 4 * grp, tb + 8 * grp, (ks | kk) != 0);
+                         tc::idesc_mxf4(BM, BN, id, id), ta + 4 * grp, tb + 8 * grp, (ks != ks0) | (kk != 0));
           }
         } else {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32), idesc_bf, (ks | kk) != 0);
+            tc::mma_bf16(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32), idesc_bf,
+                         (ks != ks0) | (kk != 0));
         }
         tc::mma_commit(&empty[stage]);
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -324,8 +346,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
-      int a_row, e, rows, srow0, nt, mti;
-      tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti);
+      int a_row, e, rows, srow0, nt, mti, kp;
+      tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti, kp);
       if (!tc::mbar_wait(&acc_full, acc_phase, g.limit_ns, &abort_flag)) { fail(); break; }
       tc::fence_after_sync();
       float va[32], vb[32];
@@ -378,7 +400,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // Four threads share a row, so each warp store fills eight whole
         // 32-byte sectors (a row-per-thread store fills 32 half sectors).
         const int r0 = q * 32 + (lane >> 2);
-        float* base = g.out + (size_t)srow0 * g.ldo + nt * BN + cq * 64 + 2 * (lane & 3);
+        float* base = g.out + kp * g.part_stride + (size_t)srow0 * g.ldo + nt * BN + cq * 64 + 2 * (lane & 3);
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {
           const int r = r0 + 8 * hh;  // hh: lanes +0, +8 (first load), +16, +24 (second)
@@ -482,9 +504,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 0 && lane == 0) {
     // ---------------- producer
     uint32_t stage = 0, phase = 0;
+    MTile mn = (int)blockIdx.x < total ? g.mt[blockIdx.x / g.n_tiles] : MTile{};
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
       const int nt = t % g.n_tiles;
-      const MTile m = g.mt[t / g.n_tiles];
+      const MTile m = mn;
+      // the next tile's window, loaded a tile ahead so its latency overlaps the stream
+      if (t + (int)gridDim.x < total) mn = g.mt[(t + gridDim.x) / g.n_tiles];
       const int nb = (m.rows + 15) >> 4;  // 16-row token boxes
       const int wr0 = m.e * g.b_rows_per_expert + nt * BM;
       const size_t rt0 = (size_t)m.e * g.sfb_rtiles + nt;
@@ -509,12 +534,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ---------------- MMA issuer
     uint32_t stage = 0, phase = 0;
     int it = 0;
+    int rows_n = (int)blockIdx.x < total ? g.mt[blockIdx.x / g.n_tiles].rows : 0;
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x, ++it) {
       const int buf = it & 1;
+      const int N = (rows_n + 15) & ~15;
+      if (t + (int)gridDim.x < total) rows_n = g.mt[(t + gridDim.x) / g.n_tiles].rows;  // a tile ahead
       if (!tc::mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
       tc::fence_after_sync();
-      const MTile m = g.mt[t / g.n_tiles];
-      const int N = (m.rows + 15) & ~15;
       const uint32_t acc = tmem + buf * WA_ACC_COLS;
       bool ok = true;
       for (int ks = 0; ks < nks; ++ks) {
@@ -558,10 +584,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int j0 = 16 * cq;
     const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16);
     int it = 0;
+    MTile mn = (int)blockIdx.x < total ? g.mt[blockIdx.x / g.n_tiles] : MTile{};
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x, ++it) {
       const int buf = it & 1;
       const int nt = t % g.n_tiles;
-      const MTile m = g.mt[t / g.n_tiles];
+      const MTile m = mn;
+      if (t + (int)gridDim.x < total) mn = g.mt[(t + gridDim.x) / g.n_tiles];  // a tile ahead
       if (!tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, g.limit_ns, &abort_flag)) { fail(); break; }
       tc::fence_after_sync();
       const bool active = j0 < ((m.rows + 15) & ~15);  // the same in the whole warp
@@ -830,26 +858,93 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   return launch_gemm<KIND_FP4, EPI_STORE_F32, true>(ma, mb, g2, max_mt * g2.n_tiles, s);
 }
 
+namespace {
+
+// Split-K finishers of the shared expert (parts summed in ascending order).
+// h[t][c] = BF16(SiLU(G) U), G and U the sums of parts [S][T][2I] at columns
+// c and I + c; four columns per thread.
+__global__ void __launch_bounds__(256) k_swiglu_parts(const float* __restrict__ parts, int S, int T, int I,
+                                                      uint16_t* __restrict__ h) {
+  const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i >= (size_t)T * I) return;
+  const size_t t = i / I, c = i % I;
+  const size_t stride = (size_t)T * 2 * I;
+  const float* pg = parts + t * 2 * I + c;
+  float4 gs = *reinterpret_cast<const float4*>(pg), us = *reinterpret_cast<const float4*>(pg + I);
+  for (int p = 1; p < S; ++p) {
+    const float4 a = *reinterpret_cast<const float4*>(pg + p * stride);
+    const float4 b = *reinterpret_cast<const float4*>(pg + p * stride + I);
+    gs.x += a.x; gs.y += a.y; gs.z += a.z; gs.w += a.w;
+    us.x += b.x; us.y += b.y; us.z += b.z; us.w += b.w;
+  }
+  uint2 o;
+  o.x = f32_to_bf16_rn(silu(gs.x) * us.x) | ((uint32_t)f32_to_bf16_rn(silu(gs.y) * us.y) << 16);
+  o.y = f32_to_bf16_rn(silu(gs.z) * us.z) | ((uint32_t)f32_to_bf16_rn(silu(gs.w) * us.w) << 16);
+  *reinterpret_cast<uint2*>(h + i) = o;
+}
+
+// out[i] = sum of parts [S][n] at i, four elements per thread.
+__global__ void __launch_bounds__(256) k_sum_parts(const float* __restrict__ parts, int S, size_t n,
+                                                   float* __restrict__ out) {
+  const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i >= n) return;
+  float4 v = *reinterpret_cast<const float4*>(parts + i);
+  for (int p = 1; p < S; ++p) {
+    const float4 a = *reinterpret_cast<const float4*>(parts + p * n + i);
+    v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+  }
+  *reinterpret_cast<float4*>(out + i) = v;
+}
+
+}  // namespace
+
 cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
-                             float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s) {
+                             float* y_shared, float* parts, int* status, uint64_t limit_ns, cudaStream_t s) {
   const int T = sh.T, H = sh.H, I = sh.I;
   if (T == 0) return cudaSuccess;
   const int mt = (T + BM - 1) / BM;
   CUtensorMap ma, mb;
   cudaError_t err;
-  if ((err = make_map(&ma, x, T, (uint64_t)H * 2)) != cudaSuccess) return err;
-  if ((err = make_map(&mb, shd.w13, (uint64_t)2 * I, (uint64_t)H * 2)) != cudaSuccess) return err;
-  GemmArgs g1{};
-  g1.K = H;
-  g1.n_tiles = I / 128;
-  g1.num_mt_dense = mt;
-  g1.rows_dense = T;
-  g1.b_up_off = I;
-  g1.h_bf16 = h_shared;
-  g1.h_cols = I;
-  g1.status = status;
-  g1.limit_ns = limit_ns;
-  if ((err = launch_gemm<KIND_BF16, EPI_SWIGLU_BF16, false>(ma, mb, g1, mt * g1.n_tiles, s)) != cudaSuccess) return err;
+  // Few tokens: the 128 x 256 tiles alone would leave most SMs idle, so K is
+  // split and small kernels finish (the same parts for every T: the choice
+  // depends on the shape only).
+  const int s1 = shared_ksplit(shared_tiles_gu(T, I), H / 64);
+  const int s2 = shared_ksplit(shared_tiles_dn(T, H), I / 64);
+  if (s1 > 1) {
+    if ((err = make_map(&ma, x, T, (uint64_t)H * 2)) != cudaSuccess) return err;
+    if ((err = make_map(&mb, shd.w13, (uint64_t)2 * I, (uint64_t)H * 2)) != cudaSuccess) return err;
+    GemmArgs g1{};
+    g1.K = H;
+    g1.n_tiles = 2 * I / BN;
+    g1.num_mt_dense = mt;
+    g1.rows_dense = T;
+    g1.out = parts;
+    g1.ldo = 2 * I;
+    g1.ksplit = s1;
+    g1.part_stride = (size_t)T * 2 * I;
+    g1.status = status;
+    g1.limit_ns = limit_ns;
+    if ((err = launch_gemm<KIND_BF16, EPI_STORE_F32, false>(ma, mb, g1, mt * g1.n_tiles * s1, s)) != cudaSuccess)
+      return err;
+    const size_t n4 = (size_t)T * I / 4;
+    k_swiglu_parts<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(parts, s1, T, I, h_shared);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  } else {
+    if ((err = make_map(&ma, x, T, (uint64_t)H * 2)) != cudaSuccess) return err;
+    if ((err = make_map(&mb, shd.w13, (uint64_t)2 * I, (uint64_t)H * 2)) != cudaSuccess) return err;
+    GemmArgs g1{};
+    g1.K = H;
+    g1.n_tiles = I / 128;
+    g1.num_mt_dense = mt;
+    g1.rows_dense = T;
+    g1.b_up_off = I;
+    g1.h_bf16 = h_shared;
+    g1.h_cols = I;
+    g1.status = status;
+    g1.limit_ns = limit_ns;
+    if ((err = launch_gemm<KIND_BF16, EPI_SWIGLU_BF16, false>(ma, mb, g1, mt * g1.n_tiles, s)) != cudaSuccess)
+      return err;
+  }
   if ((err = make_map(&ma, h_shared, T, (uint64_t)I * 2)) != cudaSuccess) return err;
   if ((err = make_map(&mb, shd.w2, H, (uint64_t)I * 2)) != cudaSuccess) return err;
   GemmArgs g2{};
@@ -857,11 +952,20 @@ cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16
   g2.n_tiles = H / BN;
   g2.num_mt_dense = mt;
   g2.rows_dense = T;
-  g2.out = y_shared;
+  g2.out = s2 > 1 ? parts : y_shared;
   g2.ldo = H;
+  g2.ksplit = s2;
+  g2.part_stride = (size_t)T * H;
   g2.status = status;
   g2.limit_ns = limit_ns;
-  return launch_gemm<KIND_BF16, EPI_STORE_F32, false>(ma, mb, g2, mt * g2.n_tiles, s);
+  if ((err = launch_gemm<KIND_BF16, EPI_STORE_F32, false>(ma, mb, g2, mt * g2.n_tiles * s2, s)) != cudaSuccess)
+    return err;
+  if (s2 > 1) {
+    const size_t n = (size_t)T * H;
+    k_sum_parts<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(parts, s2, n, y_shared);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
 }
 
 }  // namespace moefp4
