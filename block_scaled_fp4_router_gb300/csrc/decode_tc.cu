@@ -1044,19 +1044,22 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           }
         }
       }
-      // out = BF16(ys + sum_j w_j y_j), summed in a fixed order, for the
-      // 128-row tiles of H this block owns, once every down part is stored
-      for (int tile = blockIdx.x; tile < nbH; tile += a.G) {
+      // out = BF16(ys + sum_j w_j y_j), summed in a fixed order, once every
+      // down part is stored.  Items (128 columns of H x 4 tokens) are spread
+      // over all blocks, so a block's items cost one load round trip each
+      // (on 32 blocks a 16-token step took four in a row).
+      const int n_items = nbH * ((T + 3) / 4);
+      if ((int)blockIdx.x < n_items) {
         if (et == 0) {
           s_ok = wait_at_least(a.ctr + C_DC_DN, dn_total, status, a.limit_ns);
           if (!s_ok) fail();
         }
         epi_sync();
-        const bool ok = s_ok;
-        epi_sync();  // every thread has read s_ok before thread 0 writes it again
-        if (!ok) break;
-        const int col = 128 * tile + m;
-        for (int t0 = 0; t0 < T; t0 += 4) {  // four tokens' loads in flight together
+      }
+      for (int item = blockIdx.x; item < n_items && s_ok; item += a.G) {
+        const int col = 128 * (item % nbH) + m;
+        {
+          const int t0 = 4 * (item / nbH);  // four tokens' loads in flight together
           float y[4][MAX_TOPK], ysh[4];
 #pragma unroll
           for (int tt = 0; tt < 4; ++tt) {
