@@ -17,7 +17,13 @@ Instinct GPUs", section "MiniMax-M3.1 at a glance"):
 * ``batch128``   T=128,  same shape, MXFP4, router logits ~ N(0,1), seed 3
 * ``prefill8k``  T=8192, same shape, MXFP4, Zipf(1.1)-skewed expert load, seed 4
 
-Every workload carries an always-on shared expert with BF16 weights.
+Every workload carries an always-on shared expert with BF16 weights, except
+the ``*_sfp4`` variants of tiny, decode1 and batch128, whose shared expert is
+an MXFP4 expert folded into the expert table as expert E, drawn like the
+routed experts (AMD technical article "MiniMax-M3.1 on AMD Instinct GPUs",
+section "Performance, mono decode on vs off": folding the shared expert into
+the expert table; model card "amd/MiniMax-M3.1-Flash-Quark-MXFP4", section
+"Experimental MXFP4 shared experts").
 
 Array conventions (all numpy, C-contiguous, little-endian):
 
@@ -35,6 +41,9 @@ Array conventions (all numpy, C-contiguous, little-endian):
                                           scale: gate, up, down
 * ``ws13``         uint16 [2I, H]         shared expert gate/up, BF16 bits
 * ``ws2``          uint16 [H, I]          shared expert down, BF16 bits
+* ``shared_in_table`` bool               the expert arrays hold E + 1 experts,
+                                          the last one the shared expert (then
+                                          ``ws13`` / ``ws2`` are None)
 """
 from __future__ import annotations
 
@@ -61,6 +70,7 @@ class Workload:
     zipf: float = 0.0        # 0 = no router bias
     shared: bool = True
     shared_std: float = 0.02
+    shared_fp4: bool = False  # the shared expert as expert E of the FP4 table
     # E8M0 block-scale exponents drawn uniformly from [lo, hi]
     mx_exp_lo: int = -8
     mx_exp_hi: int = -4
@@ -82,6 +92,9 @@ WORKLOADS = {
         Workload("decode16z", 16, 4096, 1536, 128, 4, NVFP4, 2, 0.02, zipf=1.2),
         Workload("batch128", 128, 4096, 1536, 128, 4, MXFP4, 3, 1.0 / 64.0),
         Workload("prefill8k", 8192, 4096, 1536, 128, 4, MXFP4, 4, 0.02, zipf=1.1),
+        Workload("tiny_sfp4", 16, 512, 256, 16, 4, MXFP4, 10, 0.02, shared=False, shared_fp4=True),
+        Workload("decode1_sfp4", 1, 4096, 1536, 128, 4, MXFP4, 11, 0.02, shared=False, shared_fp4=True),
+        Workload("batch128_sfp4", 128, 4096, 1536, 128, 4, MXFP4, 13, 1.0 / 64.0, shared=False, shared_fp4=True),
     ]
 }
 
@@ -119,18 +132,20 @@ def generate(w: Workload, layer: int = 0, tokens: Optional[int] = None) -> dict:
         out["bias"] = (-w.zipf * np.log(ranks)).astype(np.float32)
     else:
         out["bias"] = None
-    out["w13"] = rw.integers(0, 256, size=(E, 2 * I, H // 2), dtype=np.uint8)
-    out["w2"] = rw.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8)
+    Et = E + 1 if w.shared_fp4 else E  # experts in the table
+    out["shared_in_table"] = w.shared_fp4
+    out["w13"] = rw.integers(0, 256, size=(Et, 2 * I, H // 2), dtype=np.uint8)
+    out["w2"] = rw.integers(0, 256, size=(Et, H, I // 2), dtype=np.uint8)
     if w.fmt == MXFP4:
         lo, hi = 127 + w.mx_exp_lo, 127 + w.mx_exp_hi
-        out["w13_scale"] = rw.integers(lo, hi + 1, size=(E, 2 * I, H // 32), dtype=np.uint8)
-        out["w2_scale"] = rw.integers(lo, hi + 1, size=(E, H, I // 32), dtype=np.uint8)
+        out["w13_scale"] = rw.integers(lo, hi + 1, size=(Et, 2 * I, H // 32), dtype=np.uint8)
+        out["w2_scale"] = rw.integers(lo, hi + 1, size=(Et, H, I // 32), dtype=np.uint8)
         out["tensor_scale"] = None
     else:
         lo, hi = E4M3_CODE_LO, E4M3_CODE_HI
-        out["w13_scale"] = rw.integers(lo, hi + 1, size=(E, 2 * I, H // 16), dtype=np.uint8)
-        out["w2_scale"] = rw.integers(lo, hi + 1, size=(E, H, I // 16), dtype=np.uint8)
-        out["tensor_scale"] = np.full((E, 3), NVFP4_TENSOR_SCALE, dtype=np.float32)
+        out["w13_scale"] = rw.integers(lo, hi + 1, size=(Et, 2 * I, H // 16), dtype=np.uint8)
+        out["w2_scale"] = rw.integers(lo, hi + 1, size=(Et, H, I // 16), dtype=np.uint8)
+        out["tensor_scale"] = np.full((Et, 3), NVFP4_TENSOR_SCALE, dtype=np.float32)
     if w.shared:
         out["ws13"] = _to_bf16_bits(rw.normal(0.0, w.shared_std, size=(2 * I, H)))
         out["ws2"] = _to_bf16_bits(rw.normal(0.0, w.shared_std, size=(H, I)))
@@ -166,18 +181,20 @@ def generate_device(w: Workload, layer: int, device) -> dict:
         out["bias"] = -w.zipf * torch.log(ranks)
     else:
         out["bias"] = None
-    out["w13"] = torch.randint(0, 256, (E, 2 * I, H // 2), **u8)
-    out["w2"] = torch.randint(0, 256, (E, H, I // 2), **u8)
+    Et = E + 1 if w.shared_fp4 else E
+    out["shared_in_table"] = w.shared_fp4
+    out["w13"] = torch.randint(0, 256, (Et, 2 * I, H // 2), **u8)
+    out["w2"] = torch.randint(0, 256, (Et, H, I // 2), **u8)
     if w.fmt == MXFP4:
         lo, hi = 127 + w.mx_exp_lo, 127 + w.mx_exp_hi
-        out["w13_scale"] = torch.randint(lo, hi + 1, (E, 2 * I, H // 32), **u8)
-        out["w2_scale"] = torch.randint(lo, hi + 1, (E, H, I // 32), **u8)
+        out["w13_scale"] = torch.randint(lo, hi + 1, (Et, 2 * I, H // 32), **u8)
+        out["w2_scale"] = torch.randint(lo, hi + 1, (Et, H, I // 32), **u8)
         out["tensor_scale"] = None
     else:
         lo, hi = E4M3_CODE_LO, E4M3_CODE_HI
-        out["w13_scale"] = torch.randint(lo, hi + 1, (E, 2 * I, H // 16), **u8)
-        out["w2_scale"] = torch.randint(lo, hi + 1, (E, H, I // 16), **u8)
-        out["tensor_scale"] = torch.full((E, 3), NVFP4_TENSOR_SCALE, device=device)
+        out["w13_scale"] = torch.randint(lo, hi + 1, (Et, 2 * I, H // 16), **u8)
+        out["w2_scale"] = torch.randint(lo, hi + 1, (Et, H, I // 16), **u8)
+        out["tensor_scale"] = torch.full((Et, 3), NVFP4_TENSOR_SCALE, device=device)
     if w.shared:
         bf = torch.bfloat16
         out["ws13"] = (torch.randn((2 * I, H), device=device, generator=g) * w.shared_std).to(bf)

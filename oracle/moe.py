@@ -26,6 +26,11 @@ Readings where the pages are silent (each one also listed in the design doc):
 * the shared expert has BF16 weights, takes the BF16 token as is, and rounds
   its intermediate h to BF16 before its down projection; its weight in the
   combine is 1;
+* folded into the expert table (model card "amd/MiniMax-M3.1-Flash-Quark-MXFP4",
+  section "Experimental MXFP4 shared experts"; AMD article, section
+  "Performance, mono decode on vs off"), the shared expert is expert E of the
+  FP4 table (E = the router's rows): every token passes through it exactly
+  as through a routed expert (MXFP4 token, MXFP4-requantised h), weight 1;
 * out = BF16(ys + sum_j w_j * y_j), rounded once, to nearest-even.
 
 Precision: every contraction accumulates in float64 and is rounded to float32
@@ -219,7 +224,18 @@ def layer_forward(layer: dict, top_k: int, fmt: str, tokens=None, forced_ids=Non
             inter[int(e)] = dict(rows=rows, slots=slots, **r)
 
     ys = None
-    if layer.get("ws13") is not None:
+    if layer.get("shared_in_table"):
+        # the shared expert is table entry E, applied to every token like a
+        # routed expert
+        if cache is not None:
+            if E not in cache:
+                cache[E] = expert_matrices(layer, E, fmt)
+            wg, wu, wd = cache[E]
+        else:
+            wg, wu, wd = expert_matrices(layer, E, fmt)
+        sh = routed_expert(xq_deq, wg, wu, wd)
+        ys = sh["y"]
+    elif layer.get("ws13") is not None:
         sh = shared_expert(x, layer["ws13"], layer["ws2"])
         ys = sh["ys"]
     acc = np.einsum("nk,nkh->nh", w, y)

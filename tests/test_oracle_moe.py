@@ -193,6 +193,34 @@ def test_structured_layer_closed_form():
     assert np.all(r["out"] == 2.109375)
 
 
+def test_structured_layer_closed_form_shared_in_table():
+    """The same layer with the shared expert folded into the FP4 table as
+    expert E = 4 (gate codes 1.0, up codes 2.0 at 2^-6, down codes 1.0 at
+    2^-5, no BF16 shared weights).  It sees the MXFP4 token like a routed
+    expert: G = 1, U = 2, h = 2 SiLU(1) requantised to 1.5, y_E = 32 * 1.5 *
+    2^-5 = 1.5, weight 1.  out = BF16(1.5 + 0.75 w1 + 0.375 w2) =
+    BF16(2.1491470) = 2.15625 (138 * 2^-6; the midpoint below is 2.1484375)."""
+    lay = _structured_layer([1.0, 3.0, 2.0, 0.0])
+    E, H, I = 4, 64, 32
+    c13 = np.zeros((2 * I, H), np.uint8)
+    c13[:I] = 2
+    c13[I:] = 4
+    lay["w13"] = np.concatenate([lay["w13"], F.pack_e2m1(c13)[None]])
+    lay["w13_scale"] = np.concatenate([lay["w13_scale"], np.full((1, 2 * I, H // 32), 127 - 6, np.uint8)])
+    lay["w2"] = np.concatenate([lay["w2"], F.pack_e2m1(np.full((1, H, I), 2, np.uint8))])
+    lay["w2_scale"] = np.concatenate([lay["w2_scale"], np.full((1, H, I // 32), 127 - 5, np.uint8)])
+    lay["ws13"] = lay["ws2"] = None
+    lay["shared_in_table"] = True
+    r = M.layer_forward(lay, 2, "mxfp4", keep=True)
+    assert r["ids"].tolist() == [[1, 2]] and int(E) not in r["experts"]
+    assert np.all(r["shared"]["hq"] == 7) and np.all(r["shared"]["hs"] == 125)
+    assert np.all(r["ys"] == 1.5)
+    w1 = float(np.float32(1 / (1 + math.exp(-1))))
+    w2 = float(np.float32(1 / (1 + math.exp(1))))
+    assert abs(1.5 + 0.75 * w1 + 0.375 * w2 - 2.1491470) < 1e-6
+    assert np.all(r["out"] == 2.15625)
+
+
 def test_structured_layer_routing_ties():
     lay = _structured_layer([2.0, 2.0, 1.0, 2.0])
     r = M.layer_forward(lay, 2, "mxfp4")
@@ -232,6 +260,33 @@ def test_moe_identity_dense_gate_weighted_sum(tiny):
     diff = np.abs(ref - r["out"])
     ulp = np.abs(r["out"]) * 2 ** -7
     assert np.all(diff <= ulp)
+    assert np.mean(diff == 0) > 0.99
+
+
+def test_moe_identity_with_shared_expert_in_table():
+    """Folded shared expert: the layer equals the dense gate-weighted sum over
+    the E routed experts plus table entry E with gate 1 for every token, each
+    computed on the MXFP4 token."""
+    wl = W.WORKLOADS["tiny_sfp4"]
+    lay = W.generate(wl)
+    assert lay["w13"].shape[0] == wl.E + 1 and lay["ws13"] is None
+    r = M.layer_forward(lay, wl.top_k, wl.fmt)
+    x = F.bf16_bits_to_float(lay["x"])
+    xq, xs = M.quantize_activations(x)
+    xd = F.dequantize_mxfp4(xq, xs)
+    acc = np.zeros((x.shape[0], wl.H))
+    for e in range(wl.E + 1):
+        gate = np.ones(x.shape[0]) if e == wl.E else np.zeros(x.shape[0])
+        for t in range(x.shape[0]):
+            hit = np.nonzero(r["ids"][t] == e)[0]
+            if hit.size:
+                gate[t] = r["weights"][t, hit[0]]
+        wg, wu, wd = M.expert_matrices(lay, e, wl.fmt)
+        acc += gate[:, None] * M.routed_expert(xd, wg, wu, wd)["y"]
+    assert not np.any(r["ids"] == wl.E)  # the router never selects the shared expert
+    ref = F.round_to_bf16(acc)
+    diff = np.abs(ref - r["out"])
+    assert np.all(diff <= np.abs(r["out"]) * 2 ** -7)
     assert np.mean(diff == 0) > 0.99
 
 
