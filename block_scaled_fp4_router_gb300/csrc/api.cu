@@ -26,12 +26,30 @@ moe_status_t check_desc(const moe_layer_desc_t* d) {
   if ((int64_t)d->T * d->top_k > (int64_t)1 << 30) return MOE_ERR_INVALID_ARG;
   if ((int64_t)d->H > (1 << 20) || (int64_t)d->I > (1 << 20)) return MOE_ERR_INVALID_ARG;
   if (d->renormalize != 1 || d->act_quant != 1) return MOE_ERR_UNSUPPORTED;
+  if (d->shared_in_table != 0 && d->shared_in_table != 1) return MOE_ERR_INVALID_ARG;
+  if (d->shared_in_table && (d->top_k + 1 > MAX_TOPK || d->E + 1 > MAX_E)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
+}
+
+// The shape of the expert table and of the per-token assignments: with the
+// shared expert folded into the table, E + 1 experts and top_k + 1
+// assignments (the last one expert E with weight 1).
+moe_layer_desc_t table_desc(const moe_layer_desc_t* d) {
+  moe_layer_desc_t t = *d;
+  t.E += d->shared_in_table;
+  t.top_k += d->shared_in_table;
+  t.shared_in_table = 0;
+  return t;
+}
+
+WsLayout layout_of(const moe_layer_desc_t* d) {
+  const moe_layer_desc_t t = table_desc(d);
+  return ws_layout(t.T, t.H, t.I, t.E, t.top_k);
 }
 
 moe_status_t check_ws(const moe_layer_desc_t* d, void* ws, size_t ws_bytes) {
   if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
-  if (ws_bytes < ws_layout(d->T, d->H, d->I, d->E, d->top_k).total) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < layout_of(d).total) return MOE_ERR_WORKSPACE;
   return MOE_OK;
 }
 
@@ -114,6 +132,35 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
   return MOE_OK;
 }
 
+// The whole layer through the per-step kernels (any T).  With the shared
+// expert folded into the table, top-k also writes [T][k + 1] copies whose
+// last column is expert E with weight 1, and the rest runs on the table
+// shape with no BF16 shared expert.
+moe_status_t run_forward(const moe_layer_desc_t* desc, const ExpertsDev& ex, const SharedDev& shd,
+                         const float* w_router, const float* bias, const uint16_t* xb, uint16_t* out,
+                         int32_t* topk_ids, float* topk_w, void* ws, cudaStream_t s) {
+  const moe_layer_desc_t dt = table_desc(desc);
+  const int fold = desc->shared_in_table;
+  const WsLayout L = ws_layout(dt.T, dt.H, dt.I, dt.E, dt.top_k);
+  const Shape sh = shape_of(&dt);
+  int* ids_r = topk_ids ? topk_ids : at<int>(ws, fold ? L.ids_r : L.ids);
+  float* w_r = topk_w ? topk_w : at<float>(ws, fold ? L.wts_r : L.wts);
+  int* ids = fold ? at<int>(ws, L.ids) : ids_r;  // [T][table k]
+  float* w = fold ? at<float>(ws, L.wts) : w_r;
+  MOE_CUDA(launch_router_logits(xb, w_router, bias, at<float>(ws, L.logits), desc->T, desc->H, desc->E,
+                                at<float>(ws, L.rt_part), s));
+  MOE_CUDA(launch_topk(at<float>(ws, L.logits), desc->T, desc->E, desc->top_k, ids_r, w_r, s,
+                       fold ? ids : nullptr, fold ? w : nullptr));
+  MOE_CUDA(launch_quant_mxfp4(xb, sh.T, sh.H, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), s));
+  MOE_CUDA(launch_permute(ids, sh.T, sh.k, sh.E, at<int>(ws, L.counts), at<int>(ws, L.offsets),
+                          at<int>(ws, L.perm), at<int>(ws, L.inv_perm), at<int>(ws, L.rank),
+                          at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base), s));
+  float* ysh = shd.w13 ? at<float>(ws, L.y_shared) : nullptr;
+  MOE_TRY(run_expert_ffn(&dt, ex, shd, xb, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), at<int>(ws, L.offsets),
+                         at<int>(ws, L.perm), at<float>(ws, L.y_assign), ysh, ws, s));
+  return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh, out, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -133,7 +180,7 @@ const char* moe_status_string(moe_status_t st) {
 moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* bytes) {
   MOE_TRY(check_desc(desc));
   if (!bytes) return MOE_ERR_INVALID_ARG;
-  *bytes = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k).total;
+  *bytes = layout_of(desc).total;
   return MOE_OK;
 }
 
@@ -151,8 +198,9 @@ moe_status_t moe_get_status(void* ws, moe_status_t* st) {
 moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts_t* experts, uint8_t* w13_scale_mma,
                                  uint8_t* w2_scale_mma, moe_stream_t stream) {
   MOE_TRY(check_desc(desc));
+  const moe_layer_desc_t t = table_desc(desc);  // every expert of the table, a folded shared one included
   ExpertsDev ex;
-  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_experts(&t, experts, &ex));
   if (!w13_scale_mma || !w2_scale_mma || !aligned(w13_scale_mma, 16) || !aligned(w2_scale_mma, 16) ||
       !aligned(ex.w13s, 4) || !aligned(ex.w2s, 4))
     return MOE_ERR_INVALID_ARG;
@@ -160,26 +208,28 @@ moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts
   // Both formats keep 4 scale bytes per row per block column (128 elements of
   // MXFP4, 64 of NVFP4): the NVFP4 re-layout is the MXFP4 one over 2K.
   const int kf = ex.nv ? 2 : 1;
-  MOE_CUDA(launch_relayout_weight_sf(ex.w13s, desc->E, 2 * desc->I, kf * desc->H, w13_scale_mma, s));
-  return cuda_status(launch_relayout_weight_sf(ex.w2s, desc->E, desc->H, kf * desc->I, w2_scale_mma, s));
+  MOE_CUDA(launch_relayout_weight_sf(ex.w13s, t.E, 2 * t.I, kf * t.H, w13_scale_mma, s));
+  return cuda_status(launch_relayout_weight_sf(ex.w2s, t.E, t.H, kf * t.I, w2_scale_mma, s));
 }
 
 moe_status_t moe_convert_nvfp4_to_mxfp4(const moe_layer_desc_t* desc, const moe_experts_t* experts,
                                         uint8_t* w13_out, uint8_t* w13_scale_out, uint8_t* w2_out,
                                         uint8_t* w2_scale_out, moe_stream_t stream) {
   MOE_TRY(check_desc(desc));
+  const moe_layer_desc_t t = table_desc(desc);
   ExpertsDev ex;
-  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_experts(&t, experts, &ex));
   if (!ex.nv) return MOE_ERR_INVALID_ARG;
   if (!w13_out || !w13_scale_out || !w2_out || !w2_scale_out || !aligned(w13_out, 16) || !aligned(w2_out, 16))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_nvfp4_to_mxfp4(shape_of(desc), ex, w13_out, w13_scale_out, w2_out, w2_scale_out,
+  return cuda_status(launch_nvfp4_to_mxfp4(shape_of(&t), ex, w13_out, w13_scale_out, w2_out, w2_scale_out,
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes, uint8_t* hq,
                                      uint8_t* hs, moe_stream_t stream) {
   MOE_TRY(check_desc(desc));
+  if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, const_cast<void*>(ws), ws_bytes));
   if (desc->T == 0) return MOE_OK;
   if (!hq || !hs || !aligned(hq, 16)) return MOE_ERR_INVALID_ARG;
@@ -218,6 +268,7 @@ moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const 
                              const float* bias, int32_t* topk_ids, float* topk_w, float* logits,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_desc(desc));
+  if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));
   if (desc->T == 0) return MOE_OK;
   if (!x || !w_router || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -234,6 +285,7 @@ moe_status_t moe_permute(const moe_layer_desc_t* desc, const int32_t* topk_ids, 
                          int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes,
                          moe_stream_t stream) {
   MOE_TRY(check_desc(desc));
+  if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));
   if (!counts || !offsets || (desc->T > 0 && (!topk_ids || !perm || !inv_perm))) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
@@ -248,6 +300,7 @@ moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_
                                 float* y_assign, float* y_shared, void* ws, size_t ws_bytes,
                                 moe_stream_t stream) {
   MOE_TRY(check_desc(desc));
+  if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));
   ExpertsDev ex;
   SharedDev shd;
@@ -265,6 +318,7 @@ moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_
 moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_assign, const int32_t* inv_perm,
                          const float* topk_w, const float* y_shared, void* out, moe_stream_t stream) {
   MOE_TRY(check_desc(desc));
+  if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   if (desc->T == 0) return MOE_OK;
   if (!y_assign || !inv_perm || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned(y_assign, 16) || !aligned(out, 16) || (y_shared && !aligned(y_shared, 16)))
@@ -279,31 +333,17 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_experts_t
                                size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_desc(desc));
   MOE_TRY(check_ws(desc, ws, ws_bytes));
+  const moe_layer_desc_t dt = table_desc(desc);
   ExpertsDev ex;
   SharedDev shd;
-  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_experts(&dt, experts, &ex));
   MOE_TRY(check_shared(shared, &shd));
+  if (desc->shared_in_table && shd.w13) return MOE_ERR_INVALID_ARG;  // one shared expert, not two
   if (desc->T == 0) return MOE_OK;
   if (!x || !out || !w_router || !aligned(x, 16) || !aligned(out, 16) || !aligned(w_router, 16))
     return MOE_ERR_INVALID_ARG;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
-  const Shape sh = shape_of(desc);
-  const uint16_t* xb = static_cast<const uint16_t*>(x);
-  int* ids = topk_ids ? topk_ids : at<int>(ws, L.ids);
-  float* w = topk_w ? topk_w : at<float>(ws, L.wts);
-  MOE_CUDA(launch_router_logits(xb, w_router, bias, at<float>(ws, L.logits), sh.T, sh.H, sh.E,
-                                at<float>(ws, L.rt_part), s));
-  MOE_CUDA(launch_topk(at<float>(ws, L.logits), sh.T, sh.E, sh.k, ids, w, s));
-  MOE_CUDA(launch_quant_mxfp4(xb, sh.T, sh.H, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), s));
-  MOE_CUDA(launch_permute(ids, sh.T, sh.k, sh.E, at<int>(ws, L.counts), at<int>(ws, L.offsets),
-                          at<int>(ws, L.perm), at<int>(ws, L.inv_perm), at<int>(ws, L.rank),
-                          at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base), s));
-  float* ysh = shd.w13 ? at<float>(ws, L.y_shared) : nullptr;
-  MOE_TRY(run_expert_ffn(desc, ex, shd, xb, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), at<int>(ws, L.offsets),
-                         at<int>(ws, L.perm), at<float>(ws, L.y_assign), ysh, ws, s));
-  return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh,
-                                    static_cast<uint16_t*>(out), s));
+  return run_forward(desc, ex, shd, w_router, bias, static_cast<const uint16_t*>(x), static_cast<uint16_t*>(out),
+                     topk_ids, topk_w, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t* experts,
@@ -313,18 +353,27 @@ moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t*
   MOE_TRY(check_desc(desc));
   if (desc->T > MAX_DECODE_T) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));
+  const moe_layer_desc_t dt = table_desc(desc);
   ExpertsDev ex;
   SharedDev shd;
-  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_experts(&dt, experts, &ex));
   MOE_TRY(check_shared(shared, &shd));
+  if (desc->shared_in_table && shd.w13) return MOE_ERR_INVALID_ARG;
   if (desc->T == 0) return MOE_OK;
   if (!x || !out || !w_router || !aligned(x, 16) || !aligned(out, 16) || !aligned(w_router, 16))
     return MOE_ERR_INVALID_ARG;
-  const Shape sh = shape_of(desc);
-  // Prepared MXFP4 scales (moe_prepare_weights) select the tensor-core launch.
-  auto launch = fused_decode_tc_supported(sh, ex) ? launch_fused_decode_tc : launch_fused_decode;
-  return cuda_status(launch(sh, ex, shd, w_router, bias, static_cast<const uint16_t*>(x), static_cast<uint16_t*>(out),
-                            topk_ids, topk_w, ws, g_wait_limit_ns.load(), reinterpret_cast<cudaStream_t>(stream)));
+  const Shape sh = shape_of(&dt);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  uint16_t* ob = static_cast<uint16_t*>(out);
+  // Prepared scales (moe_prepare_weights) select the tensor-core launch; a
+  // folded shared expert without them takes the batched path.
+  if (fused_decode_tc_supported(sh, ex))
+    return cuda_status(launch_fused_decode_tc(sh, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws,
+                                              g_wait_limit_ns.load(), s, desc->shared_in_table));
+  if (desc->shared_in_table) return run_forward(desc, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws, s);
+  return cuda_status(launch_fused_decode(sh, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws,
+                                         g_wait_limit_ns.load(), s));
 }
 
 }  // extern "C"

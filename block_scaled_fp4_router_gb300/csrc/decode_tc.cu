@@ -75,7 +75,9 @@ constexpr int MAXN = MAX_DECODE_T * MAX_TOPK;
 enum UnitKind { U_SGU = 0, U_RGU = 1, U_SDN = 2, U_RDN = 3 };
 
 struct DcArgs {
-  int T, H, I, E, k;
+  int T, H, I, E, k;         // E experts in the table, k assignments per token
+  int Er, kr;                // the router's experts and top-k (E - 1, k - 1 with the
+                             // shared expert folded into the table as expert Er)
   int G;                     // blocks in the launch
   int s_sgu, s_rgu, s_sdn;   // split-K parts
   int n_sgu, n_sdn;          // unit counts that do not depend on the routing
@@ -289,7 +291,7 @@ __device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DE
     if (a.bias) s += a.bias[e];
     // one 64-bit store carries the value and this launch's number: a reader
     // that sees the number has the value, with no fence or counter between
-    st_relaxed_u64(a.logit64 + (size_t)et * a.E + e, ((unsigned long long)epoch << 32) | __float_as_uint(s));
+    st_relaxed_u64(a.logit64 + (size_t)et * a.Er + e, ((unsigned long long)epoch << 32) | __float_as_uint(s));
   }
   epi_sync();
 }
@@ -338,7 +340,7 @@ __device__ void quant_block(const DcArgs& a, int i) {
 // number (bounded wait; false on timeout).  Lane l gets experts l, l+32, ...
 __device__ bool wait_logit_row(const DcArgs& a, int t, uint32_t epoch, float (&v)[8]) {
   const int lane = threadIdx.x & 31;
-  const unsigned long long* row = a.logit64 + (size_t)t * a.E;
+  const unsigned long long* row = a.logit64 + (size_t)t * a.Er;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     bool mine = true;
@@ -346,7 +348,7 @@ __device__ bool wait_logit_row(const DcArgs& a, int t, uint32_t epoch, float (&v
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
       v[i] = 0.0f;
-      if (e < a.E) {
+      if (e < a.Er) {
         const unsigned long long w = ld_relaxed_u64(row + e);
         mine &= (uint32_t)(w >> 32) == epoch;
         v[i] = __uint_as_float((uint32_t)w);
@@ -443,7 +445,7 @@ __device__ void quant_row_nv(const DcArgs& a, int t, uint8_t* e_s) {
 // sorted order, numbered with a ballot).  128 epilogue threads, et = 0..127.
 // *failed is set (by some thread) when a logit row never arrived.
 __device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t epoch, int* failed) {
-  const int T = a.T, E = a.E, k = a.k, n = T * k;
+  const int T = a.T, k = a.k, kr = a.kr, n = T * k;
   const int w = et >> 5, lane = et & 31;
   for (int t = w; t < T; t += EPI_THREADS / 32) {
     float v[8];
@@ -453,14 +455,18 @@ __device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t ep
     }
     int sel[MAX_TOPK];
     float vals[MAX_TOPK], wt[MAX_TOPK];
-    warp_topk(v, E, k, sel, vals);
-    topk_weights(vals, k, wt);
+    warp_topk(v, a.Er, kr, sel, vals);
+    topk_weights(vals, kr, wt);
 #pragma unroll
     for (int j = 0; j < MAX_TOPK; ++j)
-      if (j == lane && j < k) {
+      if (j == lane && j < kr) {
         R.ids[t * k + j] = sel[j];
         R.w[t * k + j] = wt[j];
       }
+    if (lane == 0 && kr < k) {  // the shared expert folded into the table: expert Er, weight 1
+      R.ids[t * k + kr] = a.Er;
+      R.w[t * k + kr] = 1.0f;
+    }
   }
   epi_sync();
   if (*failed) return;  // the same answer in every thread after the barrier
@@ -855,7 +861,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     const int T = a.T, H = a.H, I = a.I, k = a.k, n = T * k;
 
     const uint32_t epoch = s_epoch;
-    for (int e = blockIdx.x; e < a.E; e += a.G) router_row(a, e, et, red_s, epoch);
+    for (int e = blockIdx.x; e < a.Er; e += a.G) router_row(a, e, et, red_s, epoch);
     // the router rows go to the first E blocks, the quantisation to the last ones
     if (NV) {
       const int t = (a.G - 1 - blockIdx.x) * (EPI_THREADS / 32) + (et >> 5);
@@ -872,9 +878,10 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       if (et == 0) fail();
     } else {
       if (et == 0) tc::mbar_arrive(&routing_ready);
-      if (blockIdx.x == 0 && et < n) {
-        if (a.ids_out) a.ids_out[et] = R.ids[et];
-        if (a.w_out) a.w_out[et] = R.w[et];
+      if (blockIdx.x == 0 && et < n && et % a.k < a.kr) {  // the router's top-k, [T][kr]
+        const int o = et / a.k * a.kr + et % a.k;
+        if (a.ids_out) a.ids_out[o] = R.ids[et];
+        if (a.w_out) a.w_out[o] = R.w[et];
       }
       const int n_slots = R.n_slots;
       const int total = units_total(a, n_slots);
@@ -1115,7 +1122,7 @@ bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex) {
 
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
                                    const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
-                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s) {
+                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold) {
   if (sh.T == 0) return cudaSuccess;
   if (!fused_decode_tc_supported(sh, ex)) return cudaErrorInvalidValue;
   const int T = sh.T, H = sh.H, I = sh.I, E = sh.E, k = sh.k, n = T * k;
@@ -1143,6 +1150,8 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.I = I;
   a.E = E;
   a.k = k;
+  a.Er = E - fold;
+  a.kr = k - fold;
   a.G = G;
   a.s_sgu = sp.sgu;
   a.s_rgu = sp.rgu;

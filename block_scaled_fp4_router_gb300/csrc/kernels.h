@@ -37,7 +37,10 @@ cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* code
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, float* part, cudaStream_t s);  // part: [router_splits][T][E]
 // A2
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s);
+// ids_ext / w_ext (optional): [T][k + 1], the last column the shared expert
+// folded into the table (id E, weight 1).
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s,
+                        int* ids_ext = nullptr, float* w_ext = nullptr);
 // A3
 cudaError_t launch_permute(const int* ids, int T, int k, int E, int* counts, int* offsets, int* perm,
                            int* inv_perm, int* rank, int* chunk_cnt, int* chunk_base, cudaStream_t s);
@@ -87,9 +90,12 @@ cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const Sha
                                 cudaStream_t s);
 // A10 on tensor cores (MXFP4 weights with prepared scales, H and I multiples of 256).
 bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex);
+// sh: the table shape (E experts, k assignments per token).  fold = 1: the
+// shared expert is table entry E - 1, the router has E - 1 rows and picks
+// k - 1 experts; ids_out / w_out are [T][k - fold].
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
                                    const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
-                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s);
+                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold = 0);
 // NVFP4 -> MXFP4 conversion of the routed experts (load time).
 cudaError_t launch_nvfp4_to_mxfp4(const Shape& sh, const ExpertsDev& ex, uint8_t* w13_out, uint8_t* w13s_out,
                                   uint8_t* w2_out, uint8_t* w2s_out, cudaStream_t s);

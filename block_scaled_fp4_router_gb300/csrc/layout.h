@@ -25,6 +25,7 @@ constexpr int DC_MAX_GRID = 256;
 constexpr int DC_MAX_SPLIT = 16;
 
 MOE_HD inline int imin(int a, int b) { return a < b ? a : b; }
+MOE_HD inline int imax(int a, int b) { return a > b ? a : b; }
 
 // Split-K factor: as many parts as keep `tiles` output tiles within one work
 // unit per block of a `grid`-block launch, at most one part per K stage.
@@ -140,6 +141,8 @@ struct WsLayout {
   size_t rt_part;      // float [splits, T, E]: split-K parts of the batched router
   size_t ids;          // int [T, k]       (when the caller passes no output)
   size_t wts;          // float [T, k]
+  size_t ids_r;        // int [T, k]: the router's top-k when the shared expert is folded into the table
+  size_t wts_r;        // float [T, k]
   size_t xq;           // uint8 [T, H/2]
   size_t xs;           // uint8 [T, H/32]
   size_t counts;       // int [E]
@@ -176,7 +179,12 @@ struct WsLayout {
   size_t total;
 };
 
+// E, k: experts in the table and assignments per token (with a shared expert
+// folded into the table: the router's E + 1 and top_k + 1).  The router's
+// regions fit a router over E or E - 1 experts, so the layout depends on the
+// table shape alone.
 MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
+  const int Er = E > 1 ? E - 1 : E;
   WsLayout L{};
   const size_t n = (size_t)T * k;
   const size_t nchunks = (n + PERM_CHUNK - 1) / PERM_CHUNK;
@@ -199,10 +207,12 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.dc_rowmax = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * MAX_TOPK);
   L.zero_end = o;
   L.logits = take(sizeof(float) * (size_t)T * E);
-  const int rs = router_splits(T, E, H);
-  L.rt_part = take(rs > 1 || (T > 16 && T <= 512) ? sizeof(float) * rs * (size_t)T * E : 0);
+  const size_t rparts = (size_t)imax(router_splits(T, E, H) * E, router_splits(T, Er, H) * Er);
+  L.rt_part = take(rparts > (size_t)E || (T > 16 && T <= 512) ? sizeof(float) * rparts * (size_t)T : 0);
   L.ids = take(sizeof(int) * n);
   L.wts = take(sizeof(float) * n);
+  L.ids_r = take(sizeof(int) * n);
+  L.wts_r = take(sizeof(float) * n);
   L.xq = take((size_t)T * H / 2);
   L.xs = take((size_t)T * H / 32);
   L.counts = take(sizeof(int) * E);

@@ -65,7 +65,9 @@ extern "C" moe_status_t moe_layer_decode_noalloc(const moe_layer_desc_t* desc, c
   // The scratch keeps whatever the previous call left in it; the launch needs
   // its counters, status word and split-K tickets at zero.
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t zero_bytes = moefp4::ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k).zero_end;
+  const int fold = desc->shared_in_table;  // the table shape: E + fold experts, top_k + fold per token
+  const size_t zero_bytes =
+      moefp4::ws_layout(desc->T, desc->H, desc->I, desc->E + fold, desc->top_k + fold).zero_end;
   if (cudaMemsetAsync(ws, 0, zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
   return moe_layer_decode(desc, experts, shared, w_router, bias, x, out, topk_ids, topk_w, ws, kScratchBytes,
                           stream);

@@ -281,8 +281,11 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float
 
 // ------------------------------------------------------------------ A2
 
+// ids / wts: [T][k].  With ids_ext set, also [T][k + 1] copies whose last
+// column is the shared expert folded into the table (expert E, weight 1).
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
-                                              int* __restrict__ ids, float* __restrict__ wts) {
+                                              int* __restrict__ ids, float* __restrict__ wts,
+                                              int* __restrict__ ids_ext, float* __restrict__ wts_ext) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   int sel[MAX_TOPK];
@@ -300,12 +303,21 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
       if (j == lane) { id = sel[j]; wv = w[j]; }
     ids[(size_t)t * k + lane] = id;
     wts[(size_t)t * k + lane] = wv;
+    if (ids_ext) {
+      ids_ext[(size_t)t * (k + 1) + lane] = id;
+      wts_ext[(size_t)t * (k + 1) + lane] = wv;
+    }
+  }
+  if (ids_ext && lane == k) {
+    ids_ext[(size_t)t * (k + 1) + k] = E;
+    wts_ext[(size_t)t * (k + 1) + k] = 1.0f;
   }
 }
 
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s) {
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s,
+                        int* ids_ext, float* w_ext) {
   if (T == 0) return cudaSuccess;
-  k_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, ids, w);
+  k_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, ids, w, ids_ext, w_ext);
   return cudaGetLastError();
 }
 

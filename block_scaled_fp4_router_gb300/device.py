@@ -33,6 +33,8 @@ class DeviceLayer:
     def __init__(self, arrays: dict, H: int, I: int, E: int, top_k: int, fmt: str, T_max: int,
                  device="cuda", shared: bool = True, prepare: bool = True):
         self.H, self.I, self.E, self.k, self.fmt = H, I, E, top_k, fmt
+        # the shared expert folded into the FP4 table as expert E (E + 1 experts)
+        self.fold = bool(arrays.get("shared_in_table", False))
         self.device = torch.device(device)
         d = self.device
         self.w_router = _to_dev(arrays["w_router"], d)
@@ -51,13 +53,14 @@ class DeviceLayer:
         if prepare:
             self.w13_scale_mma = torch.empty_like(self.w13_scale)
             self.w2_scale_mma = torch.empty_like(self.w2_scale)
-            moe_prepare_weights(desc(0, H, I, E, top_k), self.ex_plain, self.w13_scale_mma, self.w2_scale_mma)
+            moe_prepare_weights(desc(0, H, I, E, top_k, self.fold), self.ex_plain, self.w13_scale_mma,
+                                self.w2_scale_mma)
             self.ex_prepared = experts(wfmt, self.w13, self.w13_scale, self.w2, self.w2_scale, self.tensor_scale,
                                        self.w13_scale_mma, self.w2_scale_mma)
         self.ex = self.ex_prepared if self.ex_prepared is not None else self.ex_plain
         self.sh = shared_bf16(self.ws13, self.ws2)
         self.T_max = T_max
-        nbytes = moe_workspace_size(desc(T_max, H, I, E, top_k))
+        nbytes = moe_workspace_size(desc(T_max, H, I, E, top_k, self.fold))
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=d)
         # The zero fill and the scale re-layout ran on the current stream: make
         # them complete before a call on any other stream can read them.
@@ -76,7 +79,7 @@ class DeviceLayer:
     def desc(self, T: int):
         if T > self.T_max:
             raise ValueError("T=%d exceeds the workspace's T_max=%d" % (T, self.T_max))
-        return desc(T, self.H, self.I, self.E, self.k)
+        return desc(T, self.H, self.I, self.E, self.k, self.fold)
 
     def outputs(self, T: int):
         d = self.device

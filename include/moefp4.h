@@ -91,11 +91,26 @@ typedef enum { MOE_W_MXFP4 = 1, MOE_W_NVFP4 = 2 } moe_wfmt_t;
  * also of 16), 1 <= top_k <= 8, top_k <= E <= 256.  renormalize must be 1
  * (weights renormalised over the selected experts) and act_quant must be 1
  * (routed-expert activations quantised to MXFP4); other values return
- * MOE_ERR_UNSUPPORTED. */
+ * MOE_ERR_UNSUPPORTED.
+ *
+ * shared_in_table = 1 folds the shared expert into the routed-expert table
+ * (model card "amd/MiniMax-M3.1-Flash-Quark-MXFP4", section "Experimental
+ * MXFP4 shared experts"; AMD article, section "Performance, mono decode on vs
+ * off"): the expert arrays then hold E + 1 experts in the same FP4 format,
+ * and expert E is the shared expert, applied to every token with weight 1 on
+ * the same MXFP4 activations as a routed expert.  The router still has E
+ * rows and picks top_k of them (topk outputs stay [T, top_k]); the BF16
+ * shared expert must then be absent.  Needs top_k + 1 <= 8 and E + 1 <= 256.
+ * moe_layer_decode, moe_layer_decode_noalloc, moe_layer_forward,
+ * moe_workspace_size, moe_prepare_weights and moe_convert_nvfp4_to_mxfp4 take
+ * it (the last two act on all E + 1 experts); the per-step entry points
+ * return MOE_ERR_UNSUPPORTED (call them with the table shape, E + 1 experts
+ * and top_k + 1 assignments, instead).  0 = no folded shared expert. */
 typedef struct {
   int32_t T, H, I, E, top_k;
   int32_t renormalize;
   int32_t act_quant;
+  int32_t shared_in_table;
 } moe_layer_desc_t;
 
 /* Routed-expert weights (device pointers, layouts above).  The two *_mma

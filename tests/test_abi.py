@@ -105,6 +105,38 @@ def test_decode_range_and_workspace_checks(lib):
                                 4096, None, None, 4096, need, None) == M.MOE_OK
 
 
+def test_shared_in_table_descriptor_checks(lib):
+    """The folded shared expert: flag values, the top_k / E limits, the table
+    shape in the workspace size, the per-step entry points refusing it and a
+    BF16 shared expert given beside it (host checks only)."""
+    def dsc(**kw):
+        d = dict(T=4, H=512, I=256, E=16, top_k=4, renormalize=1, act_quant=1, shared_in_table=1)
+        d.update(kw)
+        return M.LayerDesc(*[d[k] for k in ("T", "H", "I", "E", "top_k", "renormalize", "act_quant",
+                                            "shared_in_table")])
+    out = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(dsc(shared_in_table=2)), ctypes.byref(out)) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_size(ctypes.byref(dsc(top_k=8)), ctypes.byref(out)) == M.MOE_ERR_UNSUPPORTED
+    assert lib.moe_workspace_size(ctypes.byref(dsc(E=256)), ctypes.byref(out)) == M.MOE_ERR_UNSUPPORTED
+    # the table shape: the same bytes as E + 1 experts and top_k + 1 assignments
+    assert M.moe_workspace_size(dsc()) == M.moe_workspace_size(M.desc(4, 512, 256, 17, 5))
+    d = dsc()
+    need = M.moe_workspace_size(d)
+    unsup = M.MOE_ERR_UNSUPPORTED
+    assert lib.moe_router_topk(ctypes.byref(d), 4096, 4096, None, 4096, 4096, None, 4096, need, None) == unsup
+    assert lib.moe_permute(ctypes.byref(d), 4096, 4096, 4096, 4096, 4096, 4096, need, None) == unsup
+    assert lib.moe_combine(ctypes.byref(d), 4096, 4096, 4096, None, 4096, None) == unsup
+    ex = M.Experts(M.MOE_W_MXFP4, 4096, 4096, 4096, 4096, None)
+    sh = M.SharedBF16(None, None)
+    assert lib.moe_expert_ffn_fp4(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh), 4096, 4096, 4096, 4096,
+                                  4096, 4096, None, 4096, need, None) == unsup
+    both = M.SharedBF16(4096, 4096)  # a BF16 shared expert beside the folded one
+    assert lib.moe_layer_decode(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(both), 4096, None, 4096,
+                                4096, None, None, 4096, need, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(both), 4096, None, 4096,
+                                 4096, None, None, 4096, need, None) == M.MOE_ERR_INVALID_ARG
+
+
 def test_quant_argument_checks(lib):
     assert lib.moe_quant_act_mxfp4(4, 33, 4096, 4096, 4096, None) == M.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_act_mxfp4(4, 64, 4096 + 2, 4096, 4096, None) == M.MOE_ERR_INVALID_ARG

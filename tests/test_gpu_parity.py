@@ -321,7 +321,7 @@ def _use_prepared(dev, prepared):
 
 
 @pytest.mark.parametrize("prepared", [True, False], ids=["tcgen05", "cudacore"])
-@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode16z"])
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode16z", "tiny_sfp4", "decode1_sfp4"])
 def test_layer_decode_fused(name, prepared):
     wl, lay, dev, cache = _workload(name)
     _use_prepared(dev, prepared)
@@ -354,7 +354,7 @@ def test_prepared_scales_are_the_tensor_core_layout():
     E, H, I = wl16.E, wl16.H, wl16.I
     assert np.array_equal(dev16.w2_scale_mma.cpu().numpy().reshape(-1), relayout(lay16["w2_scale"], H, 2 * I))
 
-@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16"])
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode1_sfp4"])
 def test_layer_forward_matches_decode(name):
     wl, lay, dev, cache = _workload(name)
     out_f, ids_f, w_f = dev.forward(bf16_tensor(lay["x"]))
@@ -401,6 +401,21 @@ def test_batch128_forward_sampled(gemm, routed_gemm):
     torch.cuda.synchronize()
     rng = np.random.default_rng(13)
     tokens = np.sort(np.concatenate([rng.choice(wl.T - 1, 23, replace=False), [wl.T - 1]]))
+    _compare_layer(wl, lay, cache, out, ids, tokens=tokens)
+
+
+@pytest.mark.parametrize("name,T", [("tiny_sfp4", 16), ("batch128_sfp4", 128), ("decode1_sfp4", 1)])
+def test_layer_forward_shared_in_table(name, T):
+    """The shared expert folded into the FP4 table (expert E, weight 1) through
+    the batched path: CUDA-core routed experts for a few assignments,
+    weights-as-A tensor-core GEMMs for batch128 (a 128-token window of the
+    shared expert next to ~4-token windows of the routed ones)."""
+    wl, lay, dev, cache = _workload(name, T if T != W.WORKLOADS[name].T else None)
+    out, ids, w = dev.forward(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    assert ids.shape == (T, wl.top_k) and int(ids.max()) < wl.E  # the router's top-k only
+    tokens = None if T <= 16 else np.sort(np.random.default_rng(15).choice(T, 24, replace=False))
     _compare_layer(wl, lay, cache, out, ids, tokens=tokens)
 
 
