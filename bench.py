@@ -76,7 +76,8 @@ def expert_bytes(wl) -> int:
 def step_bytes(wl, n_distinct: int) -> int:
     """Algorithmic bytes of one decode step: touched experts + shared expert +
     router (+ bias) + token rows in and out."""
-    shared = 3 * wl.H * wl.I * 2 if wl.shared else 0
+    # the shared expert: BF16, or one more FP4 expert when folded into the table
+    shared = expert_bytes(wl) if wl.shared_fp4 else (3 * wl.H * wl.I * 2 if wl.shared else 0)
     router = wl.E * wl.H * 4 + (wl.E * 4 if wl.zipf > 0 else 0)
     return n_distinct * expert_bytes(wl) + shared + router + 2 * wl.T * wl.H * 2
 
@@ -157,7 +158,8 @@ def oracle_rate(wl, budget_s: float, max_steps: int):
 def describe(wl):
     return ("%s: T=%d tokens/step, H=%d, I=%d, E=%d routed top-%d %s + %s, seed %d%s" % (
         wl.name, wl.T, wl.H, wl.I, wl.E, wl.top_k, wl.fmt.upper(),
-        "BF16 shared expert" if wl.shared else "no shared expert", wl.seed,
+        "%s shared expert folded into the table" % wl.fmt.upper() if wl.shared_fp4 else
+        ("BF16 shared expert" if wl.shared else "no shared expert"), wl.seed,
         ", Zipf(%.1f) router bias" % wl.zipf if wl.zipf else ""))
 
 
@@ -360,7 +362,7 @@ def run_ours(args):
         "config": {"workload": describe(wl), "entry_point": "moe_layer_decode" if fused else "moe_layer_forward",
                    "tokens_per_step": T, "layers_rotated": nl,
                    "l2": "inputs larger than L2: %d distinct layers (%.1f GB) rotated every step" % (
-                       nl, nl * (wl.E * expert_bytes(wl) + 3 * wl.H * wl.I * 2) / 1e9),
+                       nl, nl * step_bytes(wl, wl.E) / 1e9),
                    "graph": "%d replays of a %d-step CUDA graph" % (R, S), "parallelism": "replicas"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": NCU_TRAFFIC.get((wl.name, "k_decode_tc")) if fused and layers[0].prepared else None,
