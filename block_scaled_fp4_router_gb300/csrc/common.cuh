@@ -94,17 +94,38 @@ __device__ __forceinline__ uint32_t e2m1_rne(float s) {
   return m | ((s < 0.0f && m) ? 8u : 0u);
 }
 
+// Eight E2M1 codes of v[i] * inv packed low nibble first (element i in bits
+// 4i .. 4i+3), by the hardware's round-to-nearest-even, saturating E2M1
+// conversion (two values per cvt): the same codes as e2m1_rne, except that
+// the conversion keeps the sign of a value that rounds to zero, so those
+// nibbles are cleared to the +0 code afterwards.
+__device__ __forceinline__ uint32_t e2m1x8_rne(const float (&v)[8], float inv) {
+  uint32_t packed;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(packed)
+      : "f"(v[0] * inv), "f"(v[1] * inv), "f"(v[2] * inv), "f"(v[3] * inv), "f"(v[4] * inv), "f"(v[5] * inv),
+        "f"(v[6] * inv), "f"(v[7] * inv));
+  const uint32_t mag = packed & 0x77777777u;
+  const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;  // bit 3 of each nibble whose magnitude is not 0
+  return packed & (0x77777777u | nonzero);
+}
+
 // One thread quantises 8 consecutive BF16 values x[8g .. 8g+7]; the 4 threads
 // of a 32-element block (consecutive lanes, g = 4j .. 4j+3) share their maxima
 // with two shuffles.  All 32 lanes of the warp must call it together; lanes
 // with valid == false only join the shuffles.  Writes 4 code bytes and, from
 // the first lane of the block, the E8M0 scale byte.
-__device__ __forceinline__ void quant8_group(const uint16_t* __restrict__ x, size_t g, bool valid,
-                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+// quant8_values takes the 8 values already loaded (q = x[8g .. 8g+7]).
+__device__ __forceinline__ void quant8_values(const uint4 q, size_t g, bool valid, uint8_t* __restrict__ codes,
+                                              uint8_t* __restrict__ scales) {
   float v[8];
   float amax = 0.0f;
   if (valid) {
-    const uint4 q = *reinterpret_cast<const uint4*>(x + g * 8);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -118,12 +139,14 @@ __device__ __forceinline__ void quant8_group(const uint16_t* __restrict__ x, siz
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   if (!valid) return;
   const int e = mx_scale_exp(amax);
-  const float inv = pow2_neg(e);
-  uint32_t packed = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) packed |= e2m1_rne(v[i] * inv) << (4 * i);
-  reinterpret_cast<uint32_t*>(codes)[g] = packed;
+  reinterpret_cast<uint32_t*>(codes)[g] = e2m1x8_rne(v, pow2_neg(e));
   if ((g & 3) == 0) scales[g >> 2] = (uint8_t)(e + 127);
+}
+
+__device__ __forceinline__ void quant8_group(const uint16_t* __restrict__ x, size_t g, bool valid,
+                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const uint4 q = valid ? *reinterpret_cast<const uint4*>(x + g * 8) : make_uint4(0, 0, 0, 0);
+  quant8_values(q, g, valid, codes, scales);
 }
 
 // -------------------------------------------------------------- reductions

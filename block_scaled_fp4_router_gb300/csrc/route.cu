@@ -15,19 +15,30 @@ namespace moefp4 {
 
 // ------------------------------------------------------------------ A4
 
-// One thread per 8 elements (see quant8_group).  Requires K % 32 == 0.
+// Each thread quantises QG groups of 8 elements (see quant8_values), one per
+// grid-wide stride, with all QG loads issued before the arithmetic so each
+// thread keeps QG loads in flight.  Requires K % 32 == 0.
+constexpr int QG = 4;
 __global__ void __launch_bounds__(256) k_quant_mxfp4(const uint16_t* __restrict__ x, size_t ngroups,
                                                      uint8_t* __restrict__ codes,
                                                      uint8_t* __restrict__ scales) {
-  const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  quant8_group(x, g, g < ngroups, codes, scales);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t g0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint4 q[QG];
+#pragma unroll
+  for (int i = 0; i < QG; ++i) {
+    const size_t g = g0 + i * stride;
+    q[i] = g < ngroups ? __ldg(reinterpret_cast<const uint4*>(x + g * 8)) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < QG; ++i) quant8_values(q[i], g0 + i * stride, g0 + i * stride < ngroups, codes, scales);
 }
 
 cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t s) {
   const size_t ngroups = (size_t)rows * K / 8;
   if (ngroups == 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((ngroups + 255) / 256);
+  const unsigned blocks = (unsigned)((ngroups + 256 * QG - 1) / (256 * QG));
   k_quant_mxfp4<<<blocks, 256, 0, s>>>(x, ngroups, codes, scales);
   return cudaGetLastError();
 }

@@ -107,35 +107,49 @@ __global__ void __launch_bounds__(256) k_build_mtiles(const int* __restrict__ of
   }
 }
 
-// One block per padded row: copy the MXFP4 activation row of the assignment
-// there (zeros for padding rows) and scatter its scale bytes into the MMA
-// scale layout.  Scale layout of a matrix of windows of `win` rows and K
-// elements: block (window, K/128 group) of 512 bytes, word (i, j) at byte
-// 16 i + 4 j holding the 4 scale bytes of window row 32 j + i (with 64-row
-// windows words j = 2, 3 are unused).  With rows16 set, rows past the
-// window's real rows rounded up to 16 are skipped (nothing reads them).
+// One block per GR consecutive padded rows (one window: GR divides `win`):
+// copy the MXFP4 activation row of each row's assignment there (zeros for
+// padding rows) and scatter its scale bytes into the MMA scale layout.  The
+// GR rows' index and data loads are issued together.  Scale layout of a
+// matrix of windows of `win` rows and K elements: block (window, K/128 group)
+// of 512 bytes, word (i, j) at byte 16 i + 4 j holding the 4 scale bytes of
+// window row 32 j + i (with 64-row windows words j = 2, 3 are unused).  With
+// rows16 set, rows past the window's real rows rounded up to 16 are skipped
+// (nothing reads them).
+constexpr int GR = 4;
 __global__ void __launch_bounds__(128) k_gather_mx_rows(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
                                                         int K, int k_top, const int* __restrict__ perm,
                                                         const MTile* __restrict__ tiles, const int* __restrict__ num_tiles,
                                                         int win, int rows16, uint8_t* __restrict__ q_out,
                                                         uint32_t* __restrict__ sf_out) {
-  const int r = blockIdx.x;
-  if (r >= *num_tiles * win) return;
-  const MTile t = tiles[r / win];
-  const int m = r % win;
-  if (rows16 && m >= ((t.rows + 15) & ~15)) return;
-  const bool real = m < t.rows;
-  const int src = real ? perm[t.srow0 + m] / k_top : 0;
+  const int r0 = blockIdx.x * GR;
+  if (r0 >= *num_tiles * win) return;
+  const MTile t = tiles[r0 / win];
+  const int lim = rows16 ? ((t.rows + 15) & ~15) : win;  // rows of the window that are written
+  int src[GR];
+#pragma unroll
+  for (int i = 0; i < GR; ++i) {
+    const int m = r0 % win + i;
+    src[i] = m < t.rows ? perm[t.srow0 + m] / k_top : -1;
+  }
   const int cpr = K / 32;  // 16-byte chunks per row
   for (int c = threadIdx.x; c < cpr; c += blockDim.x) {
-    const uint4 v = real ? __ldg(reinterpret_cast<const uint4*>(q + (size_t)src * (K / 2)) + c) : make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(q_out + (size_t)r * (K / 2))[c] = v;
+    uint4 v[GR];
+#pragma unroll
+    for (int i = 0; i < GR; ++i)
+      v[i] = src[i] >= 0 ? __ldg(reinterpret_cast<const uint4*>(q + (size_t)src[i] * (K / 2)) + c)
+                         : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < GR; ++i)
+      if (r0 % win + i < lim) reinterpret_cast<uint4*>(q_out + (size_t)(r0 + i) * (K / 2))[c] = v[i];
   }
   const int groups = K / 128;
-  const int i = m % 32, j = m / 32;
-  for (int g = threadIdx.x; g < groups; g += blockDim.x) {
-    const uint32_t w = real ? __ldg(reinterpret_cast<const uint32_t*>(s + (size_t)src * (K / 32)) + g) : 0u;
-    sf_out[((size_t)(r / win) * groups + g) * 128 + i * 4 + j] = w;
+  for (int x = threadIdx.x; x < GR * groups; x += blockDim.x) {
+    const int i = x / groups, g = x % groups;
+    const int m = r0 % win + i;
+    if (m >= lim) continue;
+    const uint32_t w = src[i] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(s + (size_t)src[i] * (K / 32)) + g) : 0u;
+    sf_out[((size_t)((r0 + i) / win) * groups + g) * 128 + (m % 32) * 4 + m / 32] = w;
   }
 }
 
@@ -770,8 +784,9 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   cudaError_t err;
   k_build_mtiles<<<1, 256, 0, s>>>(offsets, E, win, w.poff, reinterpret_cast<MTile*>(w.mtiles), w.num_mt);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  k_gather_mx_rows<<<rmax, 128, 0, s>>>(xq, xs, H, sh.k, perm, reinterpret_cast<const MTile*>(w.mtiles), w.num_mt,
-                                        win, wa ? 1 : 0, w.xq_perm, reinterpret_cast<uint32_t*>(w.xs_mma));
+  k_gather_mx_rows<<<rmax / GR, 128, 0, s>>>(xq, xs, H, sh.k, perm, reinterpret_cast<const MTile*>(w.mtiles),
+                                             w.num_mt, win, wa ? 1 : 0, w.xq_perm,
+                                             reinterpret_cast<uint32_t*>(w.xs_mma));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const uint8_t* w13s_mma = ex.w13s_mma;
   const uint8_t* w2s_mma = ex.w2s_mma;
