@@ -252,13 +252,45 @@ __global__ void __launch_bounds__(256) k_router_splitk(const uint16_t* __restric
   }
 }
 
-// logits = sum over the S split-K parts in ascending order, + bias.
+// logits = sum over the S split-K parts in ascending order, + bias; four
+// consecutive logits per thread when E % 4 == 0 (all parts' loads issued
+// before the sums), else one.
 __global__ void __launch_bounds__(256) k_router_sum(const float* __restrict__ part, const float* __restrict__ bias,
                                                     float* __restrict__ logits, int T, int E, int S) {
+  const size_t n = (size_t)T * E;
+  if (E % 4 == 0) {
+    const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= n) return;
+    float4 v = *reinterpret_cast<const float4*>(part + i);
+    constexpr int B = 8;  // parts loaded together
+    for (int p0 = 1; p0 < S; p0 += B) {
+      float4 q[B];
+#pragma unroll
+      for (int j = 0; j < B; ++j)
+        q[j] = p0 + j < S ? *reinterpret_cast<const float4*>(part + (size_t)(p0 + j) * n + i) : make_float4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < B; ++j)
+        if (p0 + j < S) {
+          v.x += q[j].x;
+          v.y += q[j].y;
+          v.z += q[j].z;
+          v.w += q[j].w;
+        }
+    }
+    if (bias) {
+      const int e = (int)(i % E);
+      v.x += bias[e];
+      v.y += bias[e + 1];
+      v.z += bias[e + 2];
+      v.w += bias[e + 3];
+    }
+    *reinterpret_cast<float4*>(logits + i) = v;
+    return;
+  }
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (size_t)T * E) return;
+  if (i >= n) return;
   float v = part[i];
-  for (int p = 1; p < S; ++p) v += part[(size_t)p * T * E + i];
+  for (int p = 1; p < S; ++p) v += part[(size_t)p * n + i];
   if (bias) v += bias[i % E];
   logits[i] = v;
 }
@@ -286,7 +318,8 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float
   err = cudaGetLastError();
   if (err != cudaSuccess || (S == 1 && T > 512)) return err;
   const size_t n = (size_t)T * E;
-  k_router_sum<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, bias, logits, T, E, S);
+  const size_t threads = E % 4 == 0 ? n / 4 : n;
+  k_router_sum<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(part, bias, logits, T, E, S);
   return cudaGetLastError();
 }
 
