@@ -319,10 +319,11 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     def e2e_step(i):
-        x_dev.copy_(x_host[i], non_blocking=True)
+        # H2D and D2H through the library's SM copy (moe_copy_rows)
+        pkg.moe_copy_rows(x_dev, x_host[i])
         lay = layers[i % nl]
         (lay.decode if fused else lay.forward)(x_dev, o_dev, i_dev, w_dev)
-        out_host[i].copy_(o_dev, non_blocking=True)
+        pkg.moe_copy_rows(out_host[i], o_dev)
 
     with torch.cuda.stream(stream):
         for i in range(min(Wm, S_e)):
@@ -373,7 +374,8 @@ def run_ours(args):
                      "bytes_per_step": float(byts.mean()), "distinct_experts_per_step": float(distinct.mean())},
         "e2e": {"value": T * n_e2e / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * wl.H * 2,
                 "d2h_bytes_per_step": T * wl.H * 2, "steps": n_e2e,
-                "graph": "%d replays of a %d-step CUDA graph of (H2D x, layer, D2H out)" % (R_e, S_e)},
+                "graph": "%d replays of a %d-step CUDA graph of (H2D x, layer, D2H out), the copies by "
+                         "moe_copy_rows from / to pinned host memory" % (R_e, S_e)},
         "gpu_launches": K if fused else None,
         "clocks": clk,
         "cpu_baseline": cpu,

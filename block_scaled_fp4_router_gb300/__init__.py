@@ -29,7 +29,7 @@ EXPORTED = [
     "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
-    "moe_set_routed_gemm",
+    "moe_set_routed_gemm", "moe_copy_rows",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -89,6 +89,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_forward": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
         "moe_set_wait_limit_ns": ([U64], None),
         "moe_set_routed_gemm": ([ctypes.c_int32], ctypes.c_int),
+        "moe_copy_rows": ([P, P, S, P], ctypes.c_int),
         "moe_debug_wait_probe": ([P, S, U64, P], ctypes.c_int),
         "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
@@ -177,6 +178,15 @@ ROUTED_GEMM_AUTO, ROUTED_GEMM_TOKENS_AS_A, ROUTED_GEMM_WEIGHTS_AS_A = 0, 1, 2
 
 def moe_set_routed_gemm(mode: int) -> None:
     _check(load().moe_set_routed_gemm(int(mode)), "moe_set_routed_gemm")
+
+
+def moe_copy_rows(dst, src, stream=None) -> None:
+    """Copies src into dst (same byte size) with the GPU's SMs: device tensors
+    or pinned host tensors."""
+    nbytes = _nbytes(src)
+    if _nbytes(dst) != nbytes:
+        raise ValueError("moe_copy_rows: %d bytes into %d" % (nbytes, _nbytes(dst)))
+    _check(load().moe_copy_rows(_p(dst), _p(src), nbytes, _stream(stream)), "moe_copy_rows")
 
 
 def moe_debug_wait_probe(ws, limit_ns: int, stream=None) -> None:

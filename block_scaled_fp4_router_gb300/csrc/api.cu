@@ -242,6 +242,29 @@ moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* w
                                    at<uint8_t>(w, L.hs), tw, hq, hs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_copy_rows(void* dst, const void* src, size_t bytes, moe_stream_t stream) {
+  if (bytes == 0) return MOE_OK;
+  if (!dst || !src || bytes % 16 || !aligned(dst, 16) || !aligned(src, 16)) return MOE_ERR_INVALID_ARG;
+  // only memory the GPU addresses: device, managed, or pinned host memory
+  // mapped into the GPU's address space (its device address is used)
+  void* p[2] = {dst, const_cast<void*>(src)};
+  for (void*& q : p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_INVALID_ARG;
+    }
+    if (at.type == cudaMemoryTypeHost) {
+      if (!at.devicePointer) return MOE_ERR_INVALID_ARG;
+      q = at.devicePointer;
+    } else if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) {
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
+  if (!aligned(p[0], 16) || !aligned(p[1], 16)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_copy16(p[0], p[1], bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 
 moe_status_t moe_set_routed_gemm(int32_t mode) {

@@ -96,6 +96,9 @@ bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex);
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
                                    const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
                                    void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold = 0);
+// bytes (a multiple of 16) from src to dst, both 16-byte aligned, device or
+// GPU-addressable pinned host memory, by SM loads and stores.
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t s);
 // NVFP4 -> MXFP4 conversion of the routed experts (load time).
 cudaError_t launch_nvfp4_to_mxfp4(const Shape& sh, const ExpertsDev& ex, uint8_t* w13_out, uint8_t* w13s_out,
                                   uint8_t* w2_out, uint8_t* w2s_out, cudaStream_t s);

@@ -296,6 +296,17 @@ MOE_API void moe_set_wait_limit_ns(uint64_t ns);
  * Other values return MOE_ERR_INVALID_ARG and change nothing. */
 MOE_API moe_status_t moe_set_routed_gemm(int32_t mode);
 
+/* Copies bytes (a multiple of 16, both pointers 16-byte aligned) from src
+ * to dst on the stream, moved by the GPU's SMs rather than a copy engine.
+ * Each pointer is device memory or pinned host memory that the GPU can
+ * address (cudaHostAlloc / cudaHostRegister; on a Grace-Blackwell node the
+ * CPU-GPU link carries the loads and stores); the whole range must lie in one
+ * allocation.  Meant for a decode step's token rows and outputs, a few KB
+ * each way, captured in a CUDA graph with moe_layer_decode, where a kernel
+ * costs less than a copy-engine transfer.  Other memory kinds return
+ * MOE_ERR_INVALID_ARG. */
+MOE_API moe_status_t moe_copy_rows(void* dst, const void* src, size_t bytes, moe_stream_t stream);
+
 /* Test hook: copies the MXFP4-requantised intermediate h of the last
  * moe_expert_ffn_fp4 / moe_layer_forward call made with this workspace (A6)
  * into caller buffers in sorted-assignment order: codes [T*top_k, I/2] and

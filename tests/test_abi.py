@@ -137,6 +137,16 @@ def test_shared_in_table_descriptor_checks(lib):
                                  4096, None, None, 4096, need, None) == M.MOE_ERR_INVALID_ARG
 
 
+def test_copy_rows_argument_checks(lib):
+    inv = M.MOE_ERR_INVALID_ARG
+    assert lib.moe_copy_rows(None, 4096, 64, None) == inv
+    assert lib.moe_copy_rows(4096, None, 64, None) == inv
+    assert lib.moe_copy_rows(4096 + 8, 4096, 64, None) == inv   # misaligned destination
+    assert lib.moe_copy_rows(4096, 4096 + 4, 64, None) == inv   # misaligned source
+    assert lib.moe_copy_rows(4096, 8192, 40, None) == inv       # not a multiple of 16 bytes
+    assert lib.moe_copy_rows(None, None, 0, None) == M.MOE_OK   # nothing to copy
+
+
 def test_quant_argument_checks(lib):
     assert lib.moe_quant_act_mxfp4(4, 33, 4096, 4096, 4096, None) == M.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_act_mxfp4(4, 64, 4096 + 2, 4096, 4096, None) == M.MOE_ERR_INVALID_ARG

@@ -631,6 +631,35 @@ def test_layer_without_shared_expert():
         _compare_layer(wl, lay, cache, out, ids)
 
 
+@pytest.mark.parametrize("nbytes", [16, 8192, (1 << 20) + 16])
+def test_copy_rows_pinned_host_and_device(nbytes):
+    """moe_copy_rows moves bytes exactly: pinned host -> device -> pinned host,
+    eagerly and replayed from a CUDA graph; pageable host memory is refused."""
+    rng = np.random.default_rng(nbytes)
+    src = torch.from_numpy(rng.integers(0, 256, nbytes, dtype=np.uint8)).pin_memory()
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    M.moe_copy_rows(dev, src)
+    M.moe_copy_rows(back, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src) and torch.equal(dev.cpu(), src)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    back.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        M.moe_copy_rows(dev, src, stream=s)
+        M.moe_copy_rows(back, dev, stream=s)
+    src.copy_(torch.from_numpy(rng.integers(0, 256, nbytes, dtype=np.uint8)))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    pageable = torch.zeros(nbytes, dtype=torch.uint8)
+    with pytest.raises(M.MoeError) as e:
+        M.moe_copy_rows(dev, pageable)
+    assert e.value.status == M.MOE_ERR_INVALID_ARG
+
+
 def test_zero_tokens_is_a_no_op():
     wl, lay, dev, cache = _workload("tiny")
     x = torch.empty((0, wl.H), dtype=torch.int16, device="cuda")
