@@ -6,7 +6,7 @@
 // MXFP4 fused MoE; model card "amd/MiniMax-M3.1-Flash-Quark-MXFP4", section
 // "Model Overview": MXFP4 weights and activations).
 //
-// One persistent kernel per GEMM, warp-specialised (192 threads):
+// One persistent kernel per GEMM, warp-specialised (576 threads):
 //   warp 0      TMA producer: 2D swizzled tiles of A and B and 1D bulk copies
 //               of their scale blocks into a 4-stage shared-memory ring;
 //   warp 1      MMA issuer: copies the stage's scale blocks into TMEM with
@@ -25,6 +25,10 @@
 // Grouped (routed) GEMMs run on a per-expert padded row order: expert e's
 // assignments occupy rows [poff[e], poff[e] + count[e]) of a buffer whose
 // expert blocks start at multiples of 128, so a tile never spans experts.
+// Dense (shared-expert) GEMMs may split K into parts written to separate FP32
+// outputs that small kernels sum in order (few tokens: too few tiles for the
+// SMs).  With a few tokens per expert the routed GEMMs swap operands instead
+// (k_tc_gemm_wa below: weights as A, 64-row token windows as B).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -33,7 +33,7 @@ def lib():
     return M.load()
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16"])
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode1_sfp4"])
 def test_noalloc_matches_workspace_decode_twice(lib, name):
     wl = W.WORKLOADS[name]
     lay = W.generate(wl)
