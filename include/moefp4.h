@@ -14,8 +14,8 @@
  *
  * Conventions for every entry point:
  *   - Pointers named *_h or documented "host" are host memory; every other
- *     pointer is device memory owned by the caller.  The library never keeps a
- *     pointer beyond the call.
+ *     pointer is device memory owned by the caller (moe_copy_rows also takes
+ *     pinned host memory).  The library never keeps a pointer beyond the call.
  *   - Work is enqueued on the caller's stream; no entry point synchronises the
  *     host or allocates device memory, except moe_get_status (which copies one
  *     word device-to-host and therefore waits for that copy).
@@ -53,6 +53,8 @@
  *        h = SiLU(G) * U; hq = MXFP4(h) per 32 along I;  y = deq(hq) . deq(W2[e])^T
  *   shared expert on x:     G, U = x . Ws_gate/up^T (FP32); h = BF16(SiLU(G) * U);
  *        ys = h . Ws2^T
+ *        (folded into the table, shared_in_table = 1: ys = the routed-expert
+ *        arithmetic above with table entry E)
  *   out = BF16(ys + sum_j weights_j * y_j)
  */
 #ifndef MOEFP4_H
