@@ -19,6 +19,12 @@ Sources:
 * NVFP4 -> MXFP4 re-quantisation of the routed experts: same article,
   section "Enabling the MXFP4 checkpoint with the AMD Quark" (the rounding
   method itself is not given; the plain OCP rule above is used).
+* OCP MXFP8 (E4M3 elements, one E8M0 scale per 32): the format of the
+  shared expert in the pages' fused decode (same article, section "What we
+  Optimized": "the shared expert runs in MXFP8"; section "MiniMax-M3.1 at a
+  glance": the shared expert is MXFP8 in the checkpoint).  OCP MX v1.0 with
+  emax_elem = 8 for E4M3: X = 2^(floor(log2(amax)) - 8), elements rounded to
+  nearest-even E4M3 and saturated to +-448.
 """
 from __future__ import annotations
 
@@ -216,3 +222,66 @@ def dequantize_nvfp4(codes: np.ndarray, scales: np.ndarray, tensor_scale) -> np.
 def requantize_nvfp4_to_mxfp4(codes, scales, tensor_scale):
     """NVFP4 -> MXFP4: dequantise exactly, then the OCP MXFP4 rule per 32."""
     return quantize_mxfp4(dequantize_nvfp4(codes, scales, tensor_scale))
+
+
+# ------------------------------------------------------- MXFP8 quantisation
+
+E4M3_EMAX = 8  # largest E4M3 binade: 448 = 1.75 * 2^8
+# codes 0x00 .. 0x7E: every finite non-negative E4M3 magnitude, increasing
+_E4M3_MAGS = E4M3_TABLE[:0x7F]
+
+
+def round_to_e4m3(s: np.ndarray) -> np.ndarray:
+    """Round values (already divided by the block scale) to E4M3 codes.
+
+    Nearest E4M3 magnitude (subnormals included), ties to the code with an
+    even mantissa, magnitudes beyond 448 saturate to 448 (code 0x7E); the sign
+    goes to bit 7, and a result of magnitude zero is always the +0 code 0x00.
+    """
+    s = np.asarray(s, dtype=np.float64)
+    if not np.all(np.isfinite(s)):
+        raise ValueError("E4M3 quantisation of a non-finite value")
+    mag = np.minimum(np.abs(s), _E4M3_MAGS[-1])
+    dist = np.abs(mag[..., None] - _E4M3_MAGS)  # exact in float64
+    best = np.argmin(dist, axis=-1)  # first (lower) code on a tie
+    nxt = np.minimum(best + 1, 0x7E)
+    dbest = np.take_along_axis(dist, best[..., None], -1)[..., 0]
+    dnext = np.take_along_axis(dist, nxt[..., None], -1)[..., 0]
+    tie = (nxt != best) & (dnext == dbest)
+    best = np.where(tie & (best % 2 == 1), nxt, best)  # prefer the even mantissa
+    sign = (s < 0) & (best != 0)
+    return (best + 0x80 * sign).astype(np.uint8)
+
+
+def mx8_block_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """Shared-scale exponent floor(log2(amax)) - 8, clamped to E8M0 [-127, 127];
+    a block whose amax is 0 takes 2^-127."""
+    amax = np.asarray(amax, dtype=np.float64)
+    _, p = np.frexp(amax)
+    e = np.where(amax > 0, (p - 1) - E4M3_EMAX, -127)
+    return np.clip(e, -127, 127).astype(np.int64)
+
+
+def quantize_mxfp8(v: np.ndarray):
+    """OCP MXFP8 (E4M3) quantisation along the last axis (a multiple of 32).
+
+    Returns (codes uint8 [..., K], scale bytes uint8 [..., K/32])."""
+    v = np.asarray(v, dtype=np.float64)
+    K = v.shape[-1]
+    if K % 32:
+        raise ValueError("MXFP8 needs the quantised axis to be a multiple of 32")
+    blocks = v.reshape(v.shape[:-1] + (K // 32, 32))
+    e = mx8_block_scale_exponent(np.max(np.abs(blocks), axis=-1))
+    codes = round_to_e4m3(np.ldexp(blocks, -e[..., None])).reshape(v.shape)
+    return codes, (e + 127).astype(np.uint8)
+
+
+def dequantize_mxfp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """E4M3 codes [..., K] and E8M0 bytes [..., K/32] -> float64."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales)
+    K = codes.shape[-1]
+    if K % 32 or scales.shape != codes.shape[:-1] + (K // 32,):
+        raise ValueError("MXFP8 scales must be [..., K/32] for codes [..., K]")
+    vals = E4M3_TABLE[codes].reshape(codes.shape[:-1] + (K // 32, 32))
+    return (vals * E8M0_TABLE[scales][..., None]).reshape(codes.shape)

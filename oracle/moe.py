@@ -178,6 +178,29 @@ def shared_expert(x: np.ndarray, ws13_bits: np.ndarray, ws2_bits: np.ndarray):
     return dict(G=G, U=U, h=h, ys=ys)
 
 
+def shared_expert_mxfp8(x: np.ndarray, w13_codes, w13_scales, w2_codes, w2_scales):
+    """MXFP8 shared expert on token rows x [n, H] (float64 values).
+
+    The pages' fused decode runs the shared expert in MXFP8 (AMD article,
+    section "What we Optimized"); reading: the token is quantised to MXFP8 per
+    32 along H and the intermediate h re-quantised to MXFP8 per 32 along I,
+    as the routed experts do with MXFP4 (an MXFP8 datapath takes FP8 on both
+    operands).  Weights: E4M3 codes [2I, H] / [H, I] with E8M0 scales per 32.
+    Returns dict(xq, xs, G, U, h, hq, hs, ys): G, U, h, ys float32 values.
+    """
+    xq, xs = F.quantize_mxfp8(x)
+    xd = F.dequantize_mxfp8(xq, xs)
+    w13 = F.dequantize_mxfp8(w13_codes, w13_scales)
+    w2 = F.dequantize_mxfp8(w2_codes, w2_scales)
+    I = w13.shape[0] // 2
+    G = F.round_to_f32(xd @ w13[:I].T)
+    U = F.round_to_f32(xd @ w13[I:].T)
+    h = F.round_to_f32(swiglu(G, U))
+    hq, hs = F.quantize_mxfp8(h)
+    ys = F.round_to_f32(F.dequantize_mxfp8(hq, hs) @ w2.T)
+    return dict(xq=xq, xs=xs, G=G, U=U, h=h, hq=hq, hs=hs, ys=ys)
+
+
 # ------------------------------------------------------------------- layer
 
 

@@ -310,3 +310,96 @@ def test_e2m1_round_exhaustive_over_dyadic_grid():
         want = cands[0] if len(cands) == 1 else [i for i in cands if i % 2 == 0][0]
         want = want + (8 if (si < 0 and want != 0) else 0)
         assert c == want, (si, c, want)
+
+
+# ------------------------------------------------------------------ MXFP8
+
+
+def test_e4m3_rounding_matches_torch_float8():
+    """Nearest-even E4M3 against torch's float32 -> float8_e4m3fn cast on
+    in-range values of every binade (subnormals included); the only
+    difference allowed is the sign of zero (the oracle writes +0)."""
+    rng = np.random.default_rng(81)
+    mags = np.concatenate([rng.uniform(0, 2.0 ** -6, 4000), 2.0 ** rng.uniform(-9, np.log2(448.0), 20000),
+                           F.E4M3_TABLE[:0x7F]])
+    v = (mags * rng.choice([-1.0, 1.0], mags.size)).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref = np.where((ref & 0x7F) == 0, 0, ref)
+    got = F.round_to_e4m3(v.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_ties_at_every_midpoint_go_to_even_mantissa():
+    mags = F.E4M3_TABLE[:0x7F]
+    mid = (mags[:-1] + mags[1:]) / 2  # exact in float64
+    lo = np.arange(0x7E)
+    even = np.where(lo % 2 == 0, lo, lo + 1)  # of codes lo and lo + 1, the even one
+    assert np.array_equal(F.round_to_e4m3(mid), even)
+    assert np.array_equal(F.round_to_e4m3(-mid), np.where(even > 0, even | 0x80, 0))
+
+
+def test_e4m3_saturates_and_zero_is_positive():
+    assert F.round_to_e4m3(np.array([448.0, 449.0, 464.0, 511.0, 1e6])).tolist() == [0x7E] * 5
+    assert F.round_to_e4m3(np.array([-448.0, -500.0])).tolist() == [0xFE, 0xFE]
+    # below half the smallest subnormal (2^-10) the result is +0, whatever the sign
+    assert F.round_to_e4m3(np.array([-2.0 ** -11, 2.0 ** -11, -0.0])).tolist() == [0, 0, 0]
+
+
+def test_mxfp8_scale_rule_and_range():
+    """X = 2^(floor(log2 amax) - 8): a block whose amax is 2^k holds it as
+    code 0x78 (2^8); every scaled block lies in [-512, 512) and quantises
+    within E4M3's range; the error is at most half an E4M3 step of the value
+    (or the saturation gap above 448)."""
+    blk = np.zeros((1, 32))
+    blk[0, 5] = 2.0 ** 3
+    c, s = F.quantize_mxfp8(blk)
+    assert s[0] == 127 + 3 - 8 and c[0, 5] == 0x78
+    rng = np.random.default_rng(82)
+    v = rng.normal(0, 1, (64, 256)) * 2.0 ** rng.integers(-20, 20, (64, 1))
+    c, s = F.quantize_mxfp8(v)
+    X = F.E8M0_TABLE[s]
+    amax = np.abs(v.reshape(64, 8, 32)).max(-1)
+    assert np.all((amax / X >= 256) & (amax / X < 512))
+    d = F.dequantize_mxfp8(c, s).reshape(64, 8, 32)
+    sv = np.abs(v.reshape(64, 8, 32)) / X[..., None]
+    step = np.where(sv < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(sv, 2.0 ** -6))) - 3))
+    err = np.abs(d - v.reshape(64, 8, 32)) / X[..., None]
+    assert np.all((err <= step / 2 + 1e-12) | (sv > 448))
+
+
+def test_mxfp8_idempotent():
+    rng = np.random.default_rng(83)
+    v = rng.normal(0, 3, (16, 128))
+    c, s = F.quantize_mxfp8(v)
+    d = F.dequantize_mxfp8(c, s)
+    c2, s2 = F.quantize_mxfp8(d)
+    assert np.array_equal(F.dequantize_mxfp8(c2, s2), d)
+
+
+def test_shared_expert_mxfp8_exact_rational():
+    """Every contraction of the MXFP8 shared expert on a tiny case, against
+    exact rational sums of the dequantised operands rounded once to FP32."""
+    from fractions import Fraction
+    from oracle import moe as M
+
+    rng = np.random.default_rng(84)
+    H, I = 64, 32
+    x = F.bf16_bits_to_float(F.bf16_value_to_bits(F.round_to_bf16(rng.normal(0, 1, (1, H)))))
+    c13 = rng.integers(0, 0x7F, (2 * I, H)).astype(np.uint8) | (rng.integers(0, 2, (2 * I, H)) * 0x80).astype(np.uint8)
+    s13 = rng.integers(115, 119, (2 * I, H // 32)).astype(np.uint8)
+    c2 = rng.integers(0, 0x7F, (H, I)).astype(np.uint8)
+    s2 = rng.integers(115, 119, (H, I // 32)).astype(np.uint8)
+    r = M.shared_expert_mxfp8(x, c13, s13, c2, s2)
+
+    def val(code, sc):
+        return Fraction(F.E4M3_TABLE[code]) * Fraction(2) ** (int(sc) - 127)
+
+    xq, xs = r["xq"], r["xs"]
+    for i in range(I):
+        g = sum(val(xq[0, h], xs[0, h // 32]) * val(c13[i, h], s13[i, h // 32]) for h in range(H))
+        u = sum(val(xq[0, h], xs[0, h // 32]) * val(c13[I + i, h], s13[I + i, h // 32]) for h in range(H))
+        assert r["G"][0, i] == float(np.float32(float(g)))
+        assert r["U"][0, i] == float(np.float32(float(u)))
+    for o in range(H):
+        y = sum(val(r["hq"][0, i], r["hs"][0, i // 32]) * val(c2[o, i], s2[o, i // 32]) for i in range(I))
+        assert r["ys"][0, o] == float(np.float32(float(y)))
