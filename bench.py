@@ -190,6 +190,26 @@ def run_reference(args):
 # ------------------------------------------------------------- our kernels
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest replica's timed-region length: every rank calls this after
+    its own timing (a collective when world > 1)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(ms: float, world: int, T: int, K: int) -> float:
+    """Whole-job tokens/s of `world` independent replicas, each stepping T
+    tokens K times, over the slowest replica's time (weak scaling)."""
+    return world * T * K / (ms * 1e-3)
+
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -283,11 +303,7 @@ def run_ours(args):
     phys = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
     clk = clocks.stop(phys)
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     for lay in layers:
         st = pkg.moe_get_status(lay.ws)
         if st != pkg.MOE_OK:
@@ -355,7 +371,7 @@ def run_ours(args):
 
     if rank != 0:
         return
-    value = world * T * K / (ms * 1e-3)
+    value = replica_throughput(ms, world, T, K)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
