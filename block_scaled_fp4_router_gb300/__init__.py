@@ -29,7 +29,7 @@ EXPORTED = [
     "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
-    "moe_set_routed_gemm", "moe_copy_rows",
+    "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -82,6 +82,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_get_status": ([P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
         "moe_router_topk": ([P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
         "moe_quant_act_mxfp4": ([I32, I32, P, P, P, P], ctypes.c_int),
+        "moe_quant_act_mxfp8": ([I32, I32, P, P, P, P], ctypes.c_int),
         "moe_permute": ([P, P, P, P, P, P, P, S, P], ctypes.c_int),
         "moe_expert_ffn_fp4": ([P, P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
         "moe_combine": ([P, P, P, P, P, P, P], ctypes.c_int),
@@ -218,6 +219,11 @@ def moe_router_topk(d, x, w_router, bias, topk_ids, topk_w, logits, ws, stream=N
 def moe_quant_act_mxfp4(rows, K, x, codes, scales, stream=None):
     _check(load().moe_quant_act_mxfp4(int(rows), int(K), _p(x), _p(codes), _p(scales), _stream(stream)),
            "moe_quant_act_mxfp4")
+
+
+def moe_quant_act_mxfp8(rows, K, x, codes, scales, stream=None):
+    _check(load().moe_quant_act_mxfp8(int(rows), int(K), _p(x), _p(codes), _p(scales), _stream(stream)),
+           "moe_quant_act_mxfp8")
 
 
 def moe_permute(d, topk_ids, counts, offsets, perm, inv_perm, ws, stream=None):

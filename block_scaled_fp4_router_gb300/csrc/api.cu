@@ -287,6 +287,15 @@ moe_status_t moe_quant_act_mxfp4(int32_t rows, int32_t K, const void* x, uint8_t
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_quant_act_mxfp8(int32_t rows, int32_t K, const void* x, uint8_t* codes, uint8_t* scales,
+                                 moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 8)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quant_mxfp8(static_cast<const uint16_t*>(x), rows, K, codes, scales,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const float* w_router,
                              const float* bias, int32_t* topk_ids, float* topk_w, float* logits,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {

@@ -115,6 +115,54 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float (&v)[8], float inv) {
   return packed & (0x77777777u | nonzero);
 }
 
+// Eight E4M3 codes of v[i] * inv, element i in byte i of the pair (lo, hi),
+// by the hardware's round-to-nearest-even E4M3 conversion saturating at
+// +-448 (two values per cvt); codes of magnitude 0 are cleared to +0.
+__device__ __forceinline__ uint2 e4m3x8_rne(const float (&v)[8], float inv) {
+  uint32_t lo, hi;
+  asm("{\n\t.reg .b16 h0, h1, h2, h3;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h0, %3, %2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h1, %5, %4;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h2, %7, %6;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h3, %9, %8;\n\t"
+      "mov.b32 %0, {h0, h1};\n\t"
+      "mov.b32 %1, {h2, h3};\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "f"(v[0] * inv), "f"(v[1] * inv), "f"(v[2] * inv), "f"(v[3] * inv), "f"(v[4] * inv), "f"(v[5] * inv),
+        "f"(v[6] * inv), "f"(v[7] * inv));
+  auto clear_neg_zero = [](uint32_t w) {
+    const uint32_t nonzero = ((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;  // bit 7 of each nonzero byte
+    return w & (0x7F7F7F7Fu | nonzero);
+  };
+  return make_uint2(clear_neg_zero(lo), clear_neg_zero(hi));
+}
+
+// One thread quantises 8 consecutive BF16 values x[8g .. 8g+7] to MXFP8
+// (E4M3, one E8M0 scale per 32: X = 2^(floor(log2 amax) - 8)); the 4 threads
+// of a block share their maxima with two shuffles, as in quant8_values.
+__device__ __forceinline__ void quant8_values_mx8(const uint4 q, size_t g, bool valid, uint8_t* __restrict__ codes,
+                                                  uint8_t* __restrict__ scales) {
+  float v[8];
+  float amax = 0.0f;
+  if (valid) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  if (!valid) return;
+  const int ef = (int)((__float_as_uint(amax) >> 23) & 0xff);
+  const int e = ef == 0 ? -127 : max(ef - 127 - 8, -127);
+  reinterpret_cast<uint2*>(codes)[g] = e4m3x8_rne(v, pow2_neg(e));
+  if ((g & 3) == 0) scales[g >> 2] = (uint8_t)(e + 127);
+}
+
 // One thread quantises 8 consecutive BF16 values x[8g .. 8g+7]; the 4 threads
 // of a 32-element block (consecutive lanes, g = 4j .. 4j+3) share their maxima
 // with two shuffles.  All 32 lanes of the warp must call it together; lanes

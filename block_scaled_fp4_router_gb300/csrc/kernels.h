@@ -33,6 +33,9 @@ cudaError_t launch_relayout_weight_sf(const uint8_t* s, int E, int R, int K, uin
 // A4
 cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t s);
+// A4 for the MXFP8 shared expert: E4M3 codes [rows][K], E8M0 scales [rows][K/32].
+cudaError_t launch_quant_mxfp8(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t s);
 // A1
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, float* part, cudaStream_t s);  // part: [router_splits][T][E]

@@ -43,6 +43,32 @@ cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* code
   return cudaGetLastError();
 }
 
+// MXFP8 (E4M3 elements, E8M0 per 32) activation quantisation: the same
+// structure, QG groups of 8 per thread.
+__global__ void __launch_bounds__(256) k_quant_mxfp8(const uint16_t* __restrict__ x, size_t ngroups,
+                                                     uint8_t* __restrict__ codes,
+                                                     uint8_t* __restrict__ scales) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t g0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint4 q[QG];
+#pragma unroll
+  for (int i = 0; i < QG; ++i) {
+    const size_t g = g0 + i * stride;
+    q[i] = g < ngroups ? __ldg(reinterpret_cast<const uint4*>(x + g * 8)) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < QG; ++i) quant8_values_mx8(q[i], g0 + i * stride, g0 + i * stride < ngroups, codes, scales);
+}
+
+cudaError_t launch_quant_mxfp8(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t s) {
+  const size_t ngroups = (size_t)rows * K / 8;
+  if (ngroups == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((ngroups + 256 * QG - 1) / (256 * QG));
+  k_quant_mxfp8<<<blocks, 256, 0, s>>>(x, ngroups, codes, scales);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ A1
 
 // Router up to 16 tokens: one block per (expert row, tile of 16 tokens); the 256

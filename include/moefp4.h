@@ -200,6 +200,16 @@ MOE_API moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x
 MOE_API moe_status_t moe_quant_act_mxfp4(int32_t rows, int32_t K, const void* x, uint8_t* codes,
                                  uint8_t* scales, moe_stream_t stream);
 
+/* Dynamic OCP MXFP8 quantisation of BF16 rows: E4M3 elements with one E8M0
+ * scale per 32, X = 2^(floor(log2 amax) - 8), elements nearest-even E4M3
+ * saturated to +-448, a zero result +0 (the format of the pages' MXFP8
+ * shared expert: AMD article, section "What we Optimized").
+ *   x      BF16 [rows, K], K a multiple of 32
+ *   codes  uint8 E4M3 [rows, K] out (8-byte aligned);  scales  uint8 E8M0 [rows, K/32] out
+ * Non-finite inputs give unspecified codes. */
+MOE_API moe_status_t moe_quant_act_mxfp8(int32_t rows, int32_t K, const void* x, uint8_t* codes,
+                                         uint8_t* scales, moe_stream_t stream);
+
 /* A3: stable counting sort of the T*top_k (token, slot) assignments by
  * expert.  Bit-exact and deterministic.
  *   topk_ids  int32 [T, top_k]  (every id in [0, E))

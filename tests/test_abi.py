@@ -151,6 +151,9 @@ def test_quant_argument_checks(lib):
     assert lib.moe_quant_act_mxfp4(4, 33, 4096, 4096, 4096, None) == M.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_act_mxfp4(4, 64, 4096 + 2, 4096, 4096, None) == M.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_act_mxfp4(0, 64, None, None, None, None) == M.MOE_OK
+    assert lib.moe_quant_act_mxfp8(4, 48, 4096, 4096, 4096, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_act_mxfp8(4, 64, 4096, 4096 + 4, 4096, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_act_mxfp8(0, 64, None, None, None, None) == M.MOE_OK
 
 
 def test_binding_raises_on_error(lib):

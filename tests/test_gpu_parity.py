@@ -100,6 +100,41 @@ def test_quant_bitexact_at_every_rounding_midpoint():
     assert np.array_equal(scales, rs) and np.array_equal(codes, F.pack_e2m1(rc))
 
 
+def _quant8_gpu(x_bits):
+    rows, K = x_bits.shape
+    codes = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((rows, K // 32), dtype=torch.uint8, device="cuda")
+    M.moe_quant_act_mxfp8(rows, K, bf16_tensor(x_bits), codes, scales)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy()
+
+
+def test_mxfp8_quant_bitexact():
+    """MXFP8 (E4M3) codes and scales equal the oracle's bit for bit: random
+    rows over a wide range of magnitudes, every E4M3 rounding midpoint and
+    the saturation band (the block's largest element is scaled into
+    [256, 512), above E4M3's 448), and all-zero blocks."""
+    rng = np.random.default_rng(31)
+    x = rng.normal(0, 1, (37, 512)) * 2.0 ** rng.integers(-30, 30, (37, 1))
+    mags = F.E4M3_TABLE[:0x7F]
+    mid = (mags[:-1] + mags[1:]) / 2
+    blk = np.zeros((8, 512))
+    for r in range(8):  # each block: amax 2^8 (so X = 1) and 31 midpoints
+        vals = rng.choice(mid, (16, 31)) * rng.choice([-1.0, 1.0], (16, 31))
+        b = np.concatenate([np.full((16, 1), 256.0), vals], axis=1)
+        blk[r] = b.reshape(-1)
+    sat = np.zeros((2, 512))
+    sat[:, ::32] = 256.0
+    sat[:, 1::32] = rng.uniform(448.0, 511.0, (2, 16))
+    sat[0, 2::32] = -rng.uniform(448.0, 511.0, 16)
+    xb = F.bf16_value_to_bits(F.round_to_bf16(np.concatenate([x, blk, sat, np.zeros((1, 512))])))
+    xv = F.bf16_bits_to_float(xb)
+    gc, gs = _quant8_gpu(xb)
+    oc, os_ = F.quantize_mxfp8(xv)
+    assert np.array_equal(gs, os_)
+    assert np.array_equal(gc, oc)
+
+
 def test_quant_ragged_rows_and_small_K():
     rng = np.random.default_rng(11)
     for rows, K in [(1, 32), (3, 96), (5, 160)]:
