@@ -29,7 +29,7 @@ EXPORTED = [
     "moe_quant_act_mxfp4", "moe_permute", "moe_expert_ffn_fp4", "moe_combine",
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
-    "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8",
+    "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8", "moe_shared_expert_mxfp8",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -43,6 +43,11 @@ class MoeError(RuntimeError):
 class LayerDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "top_k", "renormalize", "act_quant",
                                               "shared_in_table")]
+
+
+class SharedMXFP8(ctypes.Structure):
+    _fields_ = [("w13", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p), ("w2", ctypes.c_void_p),
+                ("w2_scale", ctypes.c_void_p)]
 
 
 class Experts(ctypes.Structure):
@@ -91,6 +96,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_set_wait_limit_ns": ([U64], None),
         "moe_set_routed_gemm": ([ctypes.c_int32], ctypes.c_int),
         "moe_copy_rows": ([P, P, S, P], ctypes.c_int),
+        "moe_shared_expert_mxfp8": ([P, P, P, P, P, S, P], ctypes.c_int),
         "moe_debug_wait_probe": ([P, S, U64, P], ctypes.c_int),
         "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
@@ -219,6 +225,15 @@ def moe_router_topk(d, x, w_router, bias, topk_ids, topk_w, logits, ws, stream=N
 def moe_quant_act_mxfp4(rows, K, x, codes, scales, stream=None):
     _check(load().moe_quant_act_mxfp4(int(rows), int(K), _p(x), _p(codes), _p(scales), _stream(stream)),
            "moe_quant_act_mxfp4")
+
+
+def shared_mxfp8(w13, w13_scale, w2, w2_scale) -> SharedMXFP8:
+    return SharedMXFP8(_p(w13), _p(w13_scale), _p(w2), _p(w2_scale))
+
+
+def moe_shared_expert_mxfp8(d, sh8, x, y_shared, ws, stream=None):
+    _check(load().moe_shared_expert_mxfp8(ctypes.byref(d), ctypes.byref(sh8), _p(x), _p(y_shared), _p(ws),
+                                          _nbytes(ws), _stream(stream)), "moe_shared_expert_mxfp8")
 
 
 def moe_quant_act_mxfp8(rows, K, x, codes, scales, stream=None):

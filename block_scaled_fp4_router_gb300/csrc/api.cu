@@ -347,6 +347,28 @@ moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_
                         ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_shared_expert_mxfp8(const moe_layer_desc_t* desc, const moe_shared_mxfp8_t* shared,
+                                     const void* x, float* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
+  if (desc->H % 256 || desc->I % 256) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_ws(desc, ws, ws_bytes));
+  if (!shared || !shared->w13 || !shared->w13_scale || !shared->w2 || !shared->w2_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(shared->w13, 16) || !aligned(shared->w2, 16) || !aligned(shared->w13_scale, 4) ||
+      !aligned(shared->w2_scale, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !y_shared || !aligned(x, 16) || !aligned(y_shared, 16)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout_of(desc);
+  const Shared8Dev sh8{shared->w13, shared->w13_scale, shared->w2, shared->w2_scale};
+  const Shared8Ws w{at<uint8_t>(ws, L.s8_xq),  at<uint8_t>(ws, L.s8_xs),   at<uint8_t>(ws, L.s8_xs_mma),
+                    at<uint8_t>(ws, L.s8_hq),  at<uint8_t>(ws, L.s8_hs_mma), at<uint8_t>(ws, L.s8_w13s),
+                    at<uint8_t>(ws, L.s8_w2s)};
+  return cuda_status(launch_shared_mxfp8_tc(shape_of(desc), sh8, static_cast<const uint16_t*>(x), w, y_shared,
+                                            at<int>(ws, L.counters) + C_STATUS, g_wait_limit_ns.load(),
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_assign, const int32_t* inv_perm,
                          const float* topk_w, const float* y_shared, void* out, moe_stream_t stream) {
   MOE_TRY(check_desc(desc));

@@ -83,6 +83,26 @@ cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16
 // Copies the requantised h to sorted-assignment order (either layout).
 cudaError_t launch_copy_h(const Shape& sh, const int* hpath, const uint8_t* hq_sorted, const uint8_t* hs_sorted,
                           const TcWorkspace& w, uint8_t* hq_out, uint8_t* hs_out, cudaStream_t s);
+// The MXFP8 shared expert (E4M3 weights with E8M0 scales per 32) and its
+// scratch: xq [T_pad][H], xs [T_pad][H/32], the MMA-layout scales of x, h,
+// W13 and W2, and hq [T_pad][I] (T_pad = T rounded up to 128).
+struct Shared8Dev {
+  const uint8_t* w13;
+  const uint8_t* w13s;
+  const uint8_t* w2;
+  const uint8_t* w2s;
+};
+struct Shared8Ws {
+  uint8_t* xq;
+  uint8_t* xs;
+  uint8_t* xs_mma;
+  uint8_t* hq;
+  uint8_t* hs_mma;
+  uint8_t* w13s_mma;
+  uint8_t* w2s_mma;
+};
+cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const uint16_t* x, const Shared8Ws& w,
+                                   float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s);
 // A9
 cudaError_t launch_combine(const Shape& sh, const float* y_assign, const int* inv_perm, const float* w,
                            const float* y_shared, uint16_t* out, cudaStream_t s);

@@ -158,6 +158,7 @@ struct WsLayout {
   size_t y_assign;     // float [T*k, H]   (layer_forward only)
   size_t y_shared;     // float [T, H]     (layer_forward only)
   size_t sh_part;      // float split-K parts of the shared expert's GEMMs
+  size_t s8_xq, s8_xs, s8_xs_mma, s8_hq, s8_hs_mma, s8_w13s, s8_w2s;  // MXFP8 shared expert
   // tensor-core path (present when the routed experts run on tensor cores)
   size_t tc_poff;      // int [E+1]
   size_t tc_mtiles;    // 16-byte tile descriptors [padded rows / 128]
@@ -234,6 +235,7 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
     const size_t a = s1 > 1 ? s1 * T * 2 * (size_t)I : 0, b = s2 > 1 ? s2 * T * (size_t)H : 0;
     L.sh_part = take(sizeof(float) * (a > b ? a : b));
   }
+
   const bool tc = tc_routed_enabled((int)n);
   const size_t R = tc ? (size_t)tc_padded_rows((int)n, E) : 0;
   // 64-row windows (weights-as-A GEMMs): no more rows, up to twice the tiles
@@ -257,6 +259,24 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.dc_gu_r = take(dc ? sizeof(float) * sp.rgu * n * 2 * (size_t)I : 0);
   L.dc_ys = take(dc ? sizeof(float) * sp.sdn * T * (size_t)H : 0);
   L.total = o;
+  {  // MXFP8 shared expert (moe_shared_expert_mxfp8, T rounded up to 128 rows):
+     // it uses nothing else past zero_end, so its scratch overlays that part
+    size_t o8 = L.zero_end;
+    auto take8 = [&](size_t bytes) {
+      size_t at = o8;
+      o8 = align256(o8 + (bytes ? bytes : 1));
+      return at;
+    };
+    const size_t tp = ((size_t)T + 127) / 128 * 128;
+    L.s8_xq = take8(tp * H);
+    L.s8_xs = take8(tp * H / 32);
+    L.s8_xs_mma = take8(tp * H / 32);
+    L.s8_hq = take8(tp * I);
+    L.s8_hs_mma = take8(tp * I / 32);
+    L.s8_w13s = take8((size_t)2 * I * H / 32);
+    L.s8_w2s = take8((size_t)H * I / 32);
+    if (o8 > L.total) L.total = o8;
+  }
   return L;
 }
 

@@ -55,11 +55,17 @@ constexpr uint32_t SFB_BYTES = 2 * 2 * 512;  // two 128-row B blocks x two K gro
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_TMEM_BASE = 256;       // scale slots after the 256 accumulator columns
 
-enum Kind { KIND_FP4 = 0, KIND_BF16 = 1 };
-enum Epi { EPI_SWIGLU_MX = 0, EPI_STORE_F32 = 1, EPI_SWIGLU_BF16 = 2 };
+enum Kind { KIND_FP4 = 0, KIND_BF16 = 1, KIND_FP8 = 2 };
+enum Epi { EPI_SWIGLU_MX = 0, EPI_STORE_F32 = 1, EPI_SWIGLU_BF16 = 2, EPI_SWIGLU_MX8 = 3 };
 
+// Shared-memory stride of one stage (FP8 stages keep the FP4 layout and fill
+// half of each scale slot: one K group of 128 per stage).
 __host__ __device__ constexpr uint32_t stage_bytes(int kind) {
-  return kind == KIND_FP4 ? A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES : A_BYTES + B_BYTES;
+  return kind == KIND_BF16 ? A_BYTES + B_BYTES : A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+}
+// Bytes a stage's copies deliver (the mbarrier transaction count).
+__host__ __device__ constexpr uint32_t stage_tx(int kind) {
+  return kind == KIND_FP8 ? A_BYTES + B_BYTES + 512 + 1024 : stage_bytes(kind);
 }
 
 }  // namespace
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   constexpr uint32_t SB = stage_bytes(KIND);
-  constexpr bool SWIGLU = EPI == EPI_SWIGLU_MX || EPI == EPI_SWIGLU_BF16;
+  constexpr bool SWIGLU = EPI == EPI_SWIGLU_MX || EPI == EPI_SWIGLU_BF16 || EPI == EPI_SWIGLU_MX8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tmem = tmem_base;
   const int num_mt = GROUPED ? *g.num_mt : g.num_mt_dense;
   const int total = num_mt * g.n_tiles * ksplit_of(g);
-  const int nks = g.K / (KIND == KIND_FP4 ? 256 : 64);
+  const int nks = g.K / (KIND == KIND_FP4 ? 256 : KIND == KIND_FP8 ? 128 : 64);
   const int kgroups = g.K / 128;  // FP4 scale groups per row
 
   auto fail = [&]() {
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
         uint8_t* sa = dsm + stage * SB;
         uint8_t* sb = sa + A_BYTES;
-        tc::mbar_expect_tx(&full[stage], SB);
+        tc::mbar_expect_tx(&full[stage], stage_tx(KIND));
         tc::tma_load_2d(sa, &mapA, ks * 128, a_row, &full[stage]);
         tc::tma_load_2d(sb, &mapB, ks * 128, b0, &full[stage]);
         tc::tma_load_2d(sb + B_BYTES / 2, &mapB, ks * 128, b1, &full[stage]);
@@ -305,6 +311,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const size_t rt1 = (size_t)e * g.sfb_rtiles + (b1 - b_base) / BM;
           tc::bulk_load(ssb, g.sfb + (rt0 * kgroups + 2 * ks) * 512, 1024, &full[stage]);
           tc::bulk_load(ssb + 1024, g.sfb + (rt1 * kgroups + 2 * ks) * 512, 1024, &full[stage]);
+        } else if (KIND == KIND_FP8) {  // one K group (128 elements) per stage
+          uint8_t* ssa = sb + B_BYTES;
+          uint8_t* ssb = ssa + SFA_BYTES;
+          const int a_tile = a_row / BM;
+          tc::bulk_load(ssa, g.sfa + ((size_t)a_tile * kgroups + ks) * 512, 512, &full[stage]);
+          const size_t rt0 = (size_t)e * g.sfb_rtiles + (b0 - b_base) / BM;
+          const size_t rt1 = (size_t)e * g.sfb_rtiles + (b1 - b_base) / BM;
+          tc::bulk_load(ssb, g.sfb + (rt0 * kgroups + ks) * 512, 512, &full[stage]);
+          tc::bulk_load(ssb + 512, g.sfb + (rt1 * kgroups + ks) * 512, 512, &full[stage]);
         }
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
@@ -340,6 +355,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc::mma_mxf4(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32),
                          tc::idesc_mxf4(BM, BN, id, id), ta + 4 * grp, tb + 8 * grp, (ks != ks0) | (kk != 0));
           }
+        } else if (KIND == KIND_FP8) {
+          const uint32_t ssa = sb + B_BYTES, ssb = ssa + SFA_BYTES;
+          const uint32_t ta = tmem + SF_TMEM_BASE + stage * 24;  // 4 columns of A scales, 8 of B
+          const uint32_t tb = ta + 8;
+          tc::sf_copy(ta, tc::desc_sf(ssa));
+          tc::sf_copy(tb + 0, tc::desc_sf(ssb));        // B rows 0..127
+          tc::sf_copy(tb + 4, tc::desc_sf(ssb + 512));  // B rows 128..255
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 32 per MMA: scale byte kk of each row's word
+            tc::mma_mxf8(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32),
+                         tc::idesc_mxf8(BM, BN, kk, kk), ta, tb, (ks != ks0) | (kk != 0));
         } else {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -401,6 +427,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // byte cq of the MMA-layout scale word of row m in group nt
         reinterpret_cast<uint8_t*>(g.hs)[(((size_t)(r / BM) * hgroups + nt) * 128 + (m % 32) * 4 + (m / 32)) * 4 + cq] =
             (uint8_t)(ex + 127);
+      } else if (EPI == EPI_SWIGLU_MX8) {
+        // h = SiLU(G) U for 32 columns, requantised to MXFP8 (E4M3, one E8M0
+        // scale per 32); rows past the tile's real rows are not written.
+        if (m < rows) {
+          const int r = a_row + m;
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            va[i] = silu(va[i]) * vb[i];
+            amax = fmaxf(amax, fabsf(va[i]));
+          }
+          const int ef = (int)((__float_as_uint(amax) >> 23) & 0xff);
+          const int ex = ef == 0 ? -127 : max(ef - 127 - 8, -127);
+          const float inv = pow2_neg(ex);
+          uint8_t* dst = g.hq + (size_t)r * g.h_cols + nt * 128 + cq * 32;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            const float (&v8)[8] = *reinterpret_cast<const float(*)[8]>(&va[i]);
+            *reinterpret_cast<uint2*>(dst + i) = e4m3x8_rne(v8, inv);
+          }
+          const int hgroups = g.h_cols / 128;
+          reinterpret_cast<uint8_t*>(g.hs)[(((size_t)(r / BM) * hgroups + nt) * 128 + (m % 32) * 4 + (m / 32)) * 4 + cq] =
+              (uint8_t)(ex + 127);
+        }
       } else if (EPI == EPI_SWIGLU_BF16) {
         if (m < rows) {
           uint16_t* dst = g.h_bf16 + (size_t)(srow0 + m) * g.h_cols + nt * 128 + cq * 32;
@@ -917,6 +967,56 @@ __global__ void __launch_bounds__(256) k_sum_parts(const float* __restrict__ par
 }
 
 }  // namespace
+
+cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const uint16_t* x, const Shared8Ws& w,
+                                   float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s) {
+  const int T = sh.T, H = sh.H, I = sh.I;
+  if (T == 0) return cudaSuccess;
+  const int mt = (T + BM - 1) / BM;
+  const int tpad = mt * BM;
+  cudaError_t err;
+  // the token (MXFP8, scales into the MMA layout over 128-row tiles; padding
+  // rows' scales are never used) and the weights' scales in the MMA layout
+  if ((err = launch_quant_mxfp8(x, T, H, w.xq, w.xs, s)) != cudaSuccess) return err;
+  if ((err = launch_relayout_weight_sf(w.xs, 1, tpad, H, w.xs_mma, s)) != cudaSuccess) return err;
+  if ((err = launch_relayout_weight_sf(sh8.w13s, 1, 2 * I, H, w.w13s_mma, s)) != cudaSuccess) return err;
+  if ((err = launch_relayout_weight_sf(sh8.w2s, 1, H, I, w.w2s_mma, s)) != cudaSuccess) return err;
+  CUtensorMap ma, mb;
+  // gate/up: A = xq [T][H] E4M3, B = W13 [2I][H] E4M3; SwiGLU + MXFP8 requantise
+  if ((err = make_map(&ma, w.xq, T, H)) != cudaSuccess) return err;
+  if ((err = make_map(&mb, sh8.w13, (uint64_t)2 * I, H)) != cudaSuccess) return err;
+  GemmArgs g1{};
+  g1.K = H;
+  g1.n_tiles = I / 128;
+  g1.num_mt_dense = mt;
+  g1.rows_dense = T;
+  g1.b_up_off = I;
+  g1.sfa = w.xs_mma;
+  g1.sfb = w.w13s_mma;
+  g1.sfb_rtiles = 2 * I / BM;
+  g1.hq = w.hq;
+  g1.hs = reinterpret_cast<uint32_t*>(w.hs_mma);
+  g1.h_cols = I;
+  g1.status = status;
+  g1.limit_ns = limit_ns;
+  if ((err = launch_gemm<KIND_FP8, EPI_SWIGLU_MX8, false>(ma, mb, g1, mt * g1.n_tiles, s)) != cudaSuccess) return err;
+  // down: A = hq [T][I] E4M3, B = W2 [H][I] E4M3 -> y_shared FP32
+  if ((err = make_map(&ma, w.hq, T, I)) != cudaSuccess) return err;
+  if ((err = make_map(&mb, sh8.w2, H, I)) != cudaSuccess) return err;
+  GemmArgs g2{};
+  g2.K = I;
+  g2.n_tiles = H / BN;
+  g2.num_mt_dense = mt;
+  g2.rows_dense = T;
+  g2.sfa = w.hs_mma;
+  g2.sfb = w.w2s_mma;
+  g2.sfb_rtiles = H / BM;
+  g2.out = y_shared;
+  g2.ldo = H;
+  g2.status = status;
+  g2.limit_ns = limit_ns;
+  return launch_gemm<KIND_FP8, EPI_STORE_F32, false>(ma, mb, g2, mt * g2.n_tiles, s);
+}
 
 cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
                              float* y_shared, float* parts, int* status, uint64_t limit_ns, cudaStream_t s) {

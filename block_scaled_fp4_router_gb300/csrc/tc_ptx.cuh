@@ -19,6 +19,9 @@
 //    row i is {word(row i), word(row 32+i), word(row 64+i), word(row 96+i)}.
 //    A tile's column address must be a multiple of 4; with .scale_vec::2X an
 //    MMA of K = 64 reads bytes (id, id+1), id = 0 or 2;
+//  * kind::mxf8f6f4 .scale_vec::1X (E4M3 operands, type code 0, UE8M0 scales
+//    per 32): the same 4-column tile per 128 rows and 128 K elements; an MMA
+//    of K = 32 reads byte id (0..3) of each row's word;
 //  * with kind::mxf4nvf4 .scale_vec::4X (UE4M3 scales per 16 elements, scale
 //    type bit 23 = 0) one 4-column tile serves one MMA of K = 64: lane i,
 //    column j holds the four scales of row 32j + i for that K chunk.
@@ -159,6 +162,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int sfa_id, int 
          ((uint32_t)(M >> 4) << 24) | ((uint32_t)(sfa_id & 3) << 29);
 }
 
+// kind::mxf8f6f4 with E4M3 A and B (type code 0) and UE8M0 scales, one per
+// 32 elements (scale_vec::1X: an MMA of K = 32 reads byte id of each row's
+// scale word, id = 0..3).
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sfa_id, int sfb_id) {
+  return ((uint32_t)(sfb_id & 3) << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+         ((uint32_t)(sfa_id & 3) << 29);
+}
+
 __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
@@ -174,6 +185,16 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint6
   asm volatile(
       "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
+// E4M3 x E4M3 with UE8M0 scales per 32 elements (MXFP8).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
 }

@@ -156,6 +156,26 @@ def generate(w: Workload, layer: int = 0, tokens: Optional[int] = None) -> dict:
     return out
 
 
+def generate_shared_mxfp8(w: Workload, seed: int) -> dict:
+    """An MXFP8 shared expert for the workload's shape, from PCG64(seed):
+    E4M3 codes uniform over the 254 finite non-NaN encodings (either sign),
+    E8M0 scale exponents uniform in [-14, -10].  Arrays s8_w13 [2I, H],
+    s8_w13_scale [2I, H/32], s8_w2 [H, I], s8_w2_scale [H, I/32] (uint8)."""
+    r = np.random.Generator(np.random.PCG64(seed))
+    H, I = w.H, w.I
+
+    def codes(shape):
+        c = r.integers(0, 0x7F, size=shape, dtype=np.uint8)  # 0x00 .. 0x7E: finite magnitudes
+        return c | (r.integers(0, 2, size=shape, dtype=np.uint8) << 7)
+
+    return {
+        "s8_w13": codes((2 * I, H)),
+        "s8_w13_scale": r.integers(127 - 14, 127 - 10 + 1, size=(2 * I, H // 32), dtype=np.uint8),
+        "s8_w2": codes((H, I)),
+        "s8_w2_scale": r.integers(127 - 14, 127 - 10 + 1, size=(H, I // 32), dtype=np.uint8),
+    }
+
+
 def generate_tokens(w: Workload, seed: int, T: int) -> np.ndarray:
     """Fresh BF16 token rows ~ N(0, 1) from PCG64(seed): uint16 [T, H]."""
     r = np.random.Generator(np.random.PCG64(seed))

@@ -135,6 +135,15 @@ typedef struct {
   const void* w2;   /* BF16 [H, I]  */
 } moe_shared_bf16_t;
 
+/* An MXFP8 shared expert (OCP MX: E4M3 elements, one E8M0 scale per 32
+ * along K), the format the pages' fused decode runs the shared expert in. */
+typedef struct {
+  const uint8_t* w13;        /* E4M3 [2I, H] (gate rows then up rows), 16-byte aligned */
+  const uint8_t* w13_scale;  /* E8M0 [2I, H/32], 4-byte aligned */
+  const uint8_t* w2;         /* E4M3 [H, I], 16-byte aligned */
+  const uint8_t* w2_scale;   /* E8M0 [H, I/32], 4-byte aligned */
+} moe_shared_mxfp8_t;
+
 /* Human-readable name of a status code (static storage). */
 MOE_API const char* moe_status_string(moe_status_t st);
 
@@ -237,6 +246,20 @@ MOE_API moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_
                                 const uint8_t* xq, const uint8_t* xs, const int32_t* offsets,
                                 const int32_t* perm, float* y_assign, float* y_shared, void* ws,
                                 size_t ws_bytes, moe_stream_t stream);
+
+/* A8 with an MXFP8 shared expert (AMD article, section "What we Optimized":
+ * the fused decode runs the shared expert in MXFP8), on tcgen05
+ * kind::mxf8f6f4 tensor cores:
+ *   xq = MXFP8(x) per 32 along H (moe_quant_act_mxfp8's rule);
+ *   G, U = deq(xq) . deq(W13 gate / up)^T (FP32); h = SiLU(G) * U;
+ *   hq = MXFP8(h) per 32 along I;  y_shared = deq(hq) . deq(W2)^T (FP32 [T, H]).
+ * Needs H and I multiples of 256 (else MOE_ERR_UNSUPPORTED) and the
+ * workspace of desc (its per-call scratch, which the next call of any entry
+ * point may reuse); desc->shared_in_table must be 0.  The combine takes
+ * y_shared as for the BF16 shared expert. */
+MOE_API moe_status_t moe_shared_expert_mxfp8(const moe_layer_desc_t* desc, const moe_shared_mxfp8_t* shared,
+                                             const void* x, float* y_shared, void* ws, size_t ws_bytes,
+                                             moe_stream_t stream);
 
 /* A9: weighted combine (vLLM PR #64273 commit list: "MoE finalize").
  *   out[t] = BF16(y_shared[t] + sum_j topk_w[t, j] * y_assign[inv_perm[t*k + j]])

@@ -137,6 +137,21 @@ def test_shared_in_table_descriptor_checks(lib):
                                  4096, None, None, 4096, need, None) == M.MOE_ERR_INVALID_ARG
 
 
+def test_shared_expert_mxfp8_argument_checks(lib):
+    d = M.desc(4, 512, 256, 16, 4)
+    need = M.moe_workspace_size(d)
+    ok = M.SharedMXFP8(4096, 4096, 4096, 4096)
+    assert lib.moe_shared_expert_mxfp8(ctypes.byref(d), None, 4096, 4096, 4096, need, None) == M.MOE_ERR_INVALID_ARG
+    mis = M.SharedMXFP8(4096 + 8, 4096, 4096, 4096)
+    assert lib.moe_shared_expert_mxfp8(ctypes.byref(d), ctypes.byref(mis), 4096, 4096, 4096, need,
+                                       None) == M.MOE_ERR_INVALID_ARG
+    narrow = M.desc(4, 384, 256, 16, 4)  # H not a multiple of 256
+    assert lib.moe_shared_expert_mxfp8(ctypes.byref(narrow), ctypes.byref(ok), 4096, 4096, 4096, need,
+                                       None) == M.MOE_ERR_UNSUPPORTED
+    assert lib.moe_shared_expert_mxfp8(ctypes.byref(d), ctypes.byref(ok), 4096, 4096, 4096, need - 1,
+                                       None) == M.MOE_ERR_WORKSPACE
+
+
 def test_copy_rows_argument_checks(lib):
     inv = M.MOE_ERR_INVALID_ARG
     assert lib.moe_copy_rows(None, 4096, 64, None) == inv

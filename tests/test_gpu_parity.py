@@ -695,6 +695,29 @@ def test_copy_rows_pinned_host_and_device(nbytes):
     assert e.value.status == M.MOE_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("T,H,I", [(16, 512, 256), (130, 512, 512), (1, 4096, 1536)])
+def test_shared_expert_mxfp8(T, H, I):
+    """The MXFP8 shared expert on kind::mxf8f6f4 tensor cores against the
+    oracle: the same MXFP8 token (bit-exact quantiser), FP32 G / U, MXFP8 h;
+    ragged token tiles (130 = 128 + 2) and a decode shape (K = 4096)."""
+    wl = W.Workload("s8", T, H, I, 16, 4, W.MXFP4, 29, 0.02)
+    arr = W.generate_shared_mxfp8(wl, 29 + T)
+    xb = W.generate_tokens(wl, 31 + T, T)
+    d = M.desc(T, H, I, 16, 4)
+    ws = torch.zeros(M.moe_workspace_size(d), dtype=torch.uint8, device="cuda")
+    dev = {k: torch.from_numpy(v).cuda() for k, v in arr.items()}
+    sh8 = M.shared_mxfp8(dev["s8_w13"], dev["s8_w13_scale"], dev["s8_w2"], dev["s8_w2_scale"])
+    y = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    M.moe_shared_expert_mxfp8(d, sh8, bf16_tensor(xb), y, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_status(ws) == M.MOE_OK
+    ref = O.shared_expert_mxfp8(F.bf16_bits_to_float(xb), arr["s8_w13"], arr["s8_w13_scale"], arr["s8_w2"],
+                                arr["s8_w2_scale"])
+    got = y.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert normwise(got, ref["ys"]) <= CONTRACTION_TOL
+
+
 def test_zero_tokens_is_a_no_op():
     wl, lay, dev, cache = _workload("tiny")
     x = torch.empty((0, wl.H), dtype=torch.int16, device="cuda")
