@@ -13,14 +13,18 @@
 // Work units (one block per SM, cooperative launch, the same static
 // round-robin list in every block):
 //   SGU  shared gate/up:  128 gate + 128 up rows x a K part (BF16, kind::f16)
-//   RGU  routed gate/up:  expert slot x 128 gate + 128 up rows x a K part (MXFP4)
+//   RGU  routed gate/up:  expert slot x 128 gate + 128 up rows x a K part (FP4)
 //   SDN  shared down:     128 rows of H x a K part (BF16)
-//   RDN  routed down:     128 rows of H x one expert slot (MXFP4, whole K)
-// Split-K parts write FP32 partial sums; the block that delivers the last
-// part of a tile (an atomic ticket) sums the parts in a fixed order and runs
-// the tile's epilogue: SwiGLU to BF16 h (shared), SwiGLU + MXFP4 requantise
-// (routed), or the weighted combine out = BF16(ys + sum_j w_j y_j) (down).
-// Results are therefore bit-reproducible run to run.
+//   RDN  routed down:     128 rows of H x one expert slot (FP4, whole K)
+// Split-K gate/up parts write FP32 partial sums; the block that delivers the
+// last part of a tile (an atomic ticket) sums the parts in a fixed order and
+// runs the tile's epilogue: SwiGLU to BF16 h (shared) or SwiGLU + MXFP4
+// requantise (routed).  Down parts are counted; once all are stored, the
+// weighted combine out = BF16(ys + sum_j w_j y_j), summed in a fixed order,
+// runs as items of 128 columns x 4 tokens spread over all blocks.  Results
+// are therefore bit-reproducible run to run.  With the shared expert folded
+// into the FP4 table, every token has one more slot (the table's last
+// expert, weight 1) and there are no SGU / SDN units.
 //
 // Warp roles: warp 0 issues TMA, warp 1 issues tcgen05.cp / tcgen05.mma,
 // warps 2-5 are the epilogue (one TMEM lane = one weight row each).  Before
