@@ -103,8 +103,12 @@ WORKLOADS = {
 # mantissa, plus exponent field 10 with mantissa 0.
 E4M3_CODE_LO = 0x30
 E4M3_CODE_HI = 0x50
-# NVFP4 per-(expert, projection) FP32 tensor scale: a power of two.
+# NVFP4 per-(expert, projection) FP32 tensor scales: 2^-8 times a factor
+# drawn uniformly from [NVFP4_TS_LO, NVFP4_TS_HI), so gate, up and down of
+# every expert carry different scales that are (almost surely) not powers of
+# two, as the global scale of a real NVFP4 checkpoint (amax / (6 * 448)).
 NVFP4_TENSOR_SCALE = 2.0 ** -8
+NVFP4_TS_LO, NVFP4_TS_HI = 0.6, 1.7
 
 
 def _to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -123,7 +127,9 @@ def generate(w: Workload, layer: int = 0, tokens: Optional[int] = None) -> dict:
     """
     T = w.T if tokens is None else tokens
     ss = np.random.SeedSequence([w.seed, layer])
-    rw, rx = [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(2)]
+    # the third stream draws only the NVFP4 tensor scales, so the other
+    # arrays are the same draws as before those scales existed
+    rw, rx, rt = [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(3)]
     H, I, E = w.H, w.I, w.E
     out = {}
     out["w_router"] = rw.normal(0.0, w.wr_std, size=(E, H)).astype(np.float32)
@@ -145,7 +151,8 @@ def generate(w: Workload, layer: int = 0, tokens: Optional[int] = None) -> dict:
         lo, hi = E4M3_CODE_LO, E4M3_CODE_HI
         out["w13_scale"] = rw.integers(lo, hi + 1, size=(Et, 2 * I, H // 16), dtype=np.uint8)
         out["w2_scale"] = rw.integers(lo, hi + 1, size=(Et, H, I // 16), dtype=np.uint8)
-        out["tensor_scale"] = np.full((Et, 3), NVFP4_TENSOR_SCALE, dtype=np.float32)
+        out["tensor_scale"] = (NVFP4_TENSOR_SCALE * rt.uniform(NVFP4_TS_LO, NVFP4_TS_HI, size=(Et, 3))).astype(
+            np.float32)
     if w.shared:
         out["ws13"] = _to_bf16_bits(rw.normal(0.0, w.shared_std, size=(2 * I, H)))
         out["ws2"] = _to_bf16_bits(rw.normal(0.0, w.shared_std, size=(H, I)))
@@ -214,7 +221,8 @@ def generate_device(w: Workload, layer: int, device) -> dict:
         lo, hi = E4M3_CODE_LO, E4M3_CODE_HI
         out["w13_scale"] = torch.randint(lo, hi + 1, (Et, 2 * I, H // 16), **u8)
         out["w2_scale"] = torch.randint(lo, hi + 1, (Et, H, I // 16), **u8)
-        out["tensor_scale"] = torch.full((Et, 3), NVFP4_TENSOR_SCALE, device=device)
+        out["tensor_scale"] = NVFP4_TENSOR_SCALE * (
+            NVFP4_TS_LO + (NVFP4_TS_HI - NVFP4_TS_LO) * torch.rand((Et, 3), device=device, generator=g))
     if w.shared:
         bf = torch.bfloat16
         out["ws13"] = (torch.randn((2 * I, H), device=device, generator=g) * w.shared_std).to(bf)

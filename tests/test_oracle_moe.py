@@ -368,6 +368,58 @@ def test_nvfp4_with_power_of_two_scales_equals_mxfp4_layer():
     assert np.array_equal(a["out_bits"], b["out_bits"])
 
 
+def _e4m3_value(code):
+    """E4M3 normal encoding s eeee mmm -> 2^(e - 7) (1 + m / 8), written out."""
+    e, m = (code >> 3) & 0xF, code & 7
+    return 2.0 ** (e - 7) * (1 + m / 8)
+
+
+def test_nvfp4_per_projection_tensor_scales_closed_form():
+    """NVFP4 experts whose gate, up and down projections carry three
+    different FP32 tensor scales (one per (expert, projection), the [E, 3]
+    layout gate / up / down), some of them not powers of two, worked by hand.
+
+    The structured layer (x = 1, logits (1, 3, 2, 0), top-2 = experts 1, 2):
+    gate codes 1.0 with E4M3 block scale 2.0 (0x40), up codes 2.0 with block
+    scale 1.5 (0x3C), down codes 1.0 with block scale 0.75 (0x34).  With
+    tensor scales (g, u, d) of the expert, the MXFP4 token is exactly 1, so
+      G = 64 * 1.0 * 2.0 * g = 128 g,    U = 64 * 2.0 * 1.5 * u = 192 u,
+      h = SiLU(G) U, a constant block that requantises to hq = 4X or 6X with
+        X = 2^(floor(log2 h) - 2) (6X when h / X > 5),
+      y = 32 * hq * 1.0 * 0.75 * d = 24 hq d,
+    each rounded to FP32.  Expert 1 takes (3 * 2^-9, float32(0.0371),
+    5 * 2^-10), expert 2 takes (float32(0.0371), 3 * 2^-9, 7 * 2^-10): a
+    swapped gate / up index, one scale used for all three projections, or
+    another expert's scales change G, U or y."""
+    lay = _structured_layer([1.0, 3.0, 2.0, 0.0])
+    E, H, I = 4, 64, 32
+    lay["w13_scale"] = np.concatenate([np.full((E, I, H // 16), 0x40, np.uint8),
+                                       np.full((E, I, H // 16), 0x3C, np.uint8)], axis=1)
+    lay["w2_scale"] = np.full((E, H, I // 16), 0x34, np.uint8)
+    assert (_e4m3_value(0x40), _e4m3_value(0x3C), _e4m3_value(0x34)) == (2.0, 1.5, 0.75)
+    a = float(np.float32(0.0371))
+    ts = np.array([[1.0, 1.0, 1.0], [3 * 2.0 ** -9, a, 5 * 2.0 ** -10], [a, 3 * 2.0 ** -9, 7 * 2.0 ** -10],
+                   [1.0, 1.0, 1.0]], np.float32)
+    lay["tensor_scale"] = ts
+    r = M.layer_forward(lay, 2, "nvfp4", keep=True)
+    assert r["ids"].tolist() == [[1, 2]]
+    f32 = lambda v: float(np.float32(v))
+    for slot, e in enumerate((1, 2)):
+        g, u, d = (float(v) for v in ts[e])
+        G, U = f32(128 * g), f32(192 * u)
+        h = f32(G / (1 + math.exp(-G)) * U)
+        X = 2.0 ** (math.floor(math.log2(h)) - 2)
+        hq = (6 if h / X > 5 else 4) * X
+        y = f32(24 * hq * d)
+        ex = r["experts"][e]
+        assert np.all(ex["G"] == G) and np.all(ex["U"] == U), e
+        assert np.all(ex["h"] == h), e
+        assert np.all(F.dequantize_mxfp4(ex["hq"], ex["hs"]) == hq), e
+        assert np.all(r["y"][0, slot] == y), e
+    # the hand values differ between the experts and from a shared scale
+    assert f32(128 * ts[1, 0]) != f32(128 * ts[1, 1]) and f32(192 * ts[1, 1]) != f32(192 * ts[1, 0])
+
+
 def test_forced_routing_matches_free_routing_on_same_ids(tiny):
     wl = W.WORKLOADS["tiny"]
     a = M.layer_forward(tiny, wl.top_k, wl.fmt)
