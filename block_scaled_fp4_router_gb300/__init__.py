@@ -30,6 +30,7 @@ EXPORTED = [
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
     "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8", "moe_shared_expert_mxfp8",
+    "moe_noalloc_get_status", "moe_debug_wait_probe_noalloc",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -99,6 +100,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_shared_expert_mxfp8": ([P, P, P, P, P, S, P], ctypes.c_int),
         "moe_debug_wait_probe": ([P, S, U64, P], ctypes.c_int),
         "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
+        "moe_noalloc_get_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+        "moe_debug_wait_probe_noalloc": ([U64, P], ctypes.c_int),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
         "moe_prepare_weights": ([P, P, P, P, P], ctypes.c_int),
         "moe_convert_nvfp4_to_mxfp4": ([P, P, P, P, P, P, P], ctypes.c_int),
@@ -275,3 +278,15 @@ def moe_layer_decode_noalloc(d, ex, sh, w_router, bias, x, out, topk_ids, topk_w
     _check(load().moe_layer_decode_noalloc(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh), _p(w_router),
                                            _p(bias), _p(x), _p(out), _p(topk_ids), _p(topk_w), _stream(stream)),
            "moe_layer_decode_noalloc")
+
+
+def moe_noalloc_get_status() -> int:
+    """Reads and clears the status word of the built-in scratch of
+    moe_layer_decode_noalloc on the current device."""
+    st = ctypes.c_int(0)
+    _check(load().moe_noalloc_get_status(ctypes.byref(st)), "moe_noalloc_get_status")
+    return st.value
+
+
+def moe_debug_wait_probe_noalloc(limit_ns: int, stream=None) -> None:
+    _check(load().moe_debug_wait_probe_noalloc(int(limit_ns), _stream(stream)), "moe_debug_wait_probe_noalloc")

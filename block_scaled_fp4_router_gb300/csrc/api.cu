@@ -21,7 +21,7 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 moe_status_t check_desc(const moe_layer_desc_t* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0) return MOE_ERR_INVALID_ARG;
-  if (d->H % 128 || d->I % 128) return MOE_ERR_INVALID_ARG;
+  if (d->H % 32 || d->I % 32) return MOE_ERR_INVALID_ARG;  // whole MXFP4 blocks along H and I
   if (d->top_k < 1 || d->top_k > MAX_TOPK || d->E < d->top_k || d->E > MAX_E) return MOE_ERR_INVALID_ARG;
   if ((int64_t)d->T * d->top_k > (int64_t)1 << 30) return MOE_ERR_INVALID_ARG;
   if ((int64_t)d->H > (1 << 20) || (int64_t)d->I > (1 << 20)) return MOE_ERR_INVALID_ARG;
@@ -124,7 +124,7 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
   }
   if (shd.w13) {
     uint16_t* h = at<uint16_t>(ws, L.h_shared);
-    if (d->T >= TC_MIN_T_SHARED && d->H % 256 == 0)
+    if (shared_tc_path(d->T, d->H, d->I))
       MOE_CUDA(launch_shared_tc(sh, shd, x, h, y_shared, at<float>(ws, L.sh_part), status, limit, s));
     else
       MOE_CUDA(launch_shared_simt(sh, shd, x, h, y_shared, s));
@@ -204,6 +204,8 @@ moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts
   if (!w13_scale_mma || !w2_scale_mma || !aligned(w13_scale_mma, 16) || !aligned(w2_scale_mma, 16) ||
       !aligned(ex.w13s, 4) || !aligned(ex.w2s, 4))
     return MOE_ERR_INVALID_ARG;
+  // the tensor-core scale blocks are 128 rows x 128 (MXFP4) or 64 (NVFP4) K elements
+  if (t.H % 128 || t.I % 128) return MOE_ERR_UNSUPPORTED;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Both formats keep 4 scale bytes per row per block column (128 elements of
   // MXFP4, 64 of NVFP4): the NVFP4 re-layout is the MXFP4 one over 2K.

@@ -662,7 +662,10 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     tc::mbar_fence_init();
     abort_flag = 0;
     s_fail = 0;
-    s_epoch = (uint32_t)ld_acquire(a.ctr + C_DC_EPOCH) + 1u;
+    // Launch number: never 0 (the tag of zero-filled words), so after 2^32
+    // launches it skips from 0xFFFFFFFF to 1.
+    const uint32_t ep = (uint32_t)ld_acquire(a.ctr + C_DC_EPOCH) + 1u;
+    s_epoch = ep == 0u ? 1u : ep;
   }
   if (warp == 1) tc::tmem_alloc(&tmem_base, tmem_cols<NV>());
   tc::fence_before_sync();
@@ -1102,18 +1105,26 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, tmem_cols<NV>());
   }
-  // The last block out resets the launch's counters for the next call.
+  // The last block out resets the launch's counters for the next call and
+  // clears the NVFP4 row exponents (atomicMax words: a word tagged with an
+  // older launch number than the next launch's would otherwise win it).
   if (threadIdx.x == 0) {
     __threadfence();
-    if (atomicAdd(a.ctr + C_DC_EXIT, 1) == a.G - 1) {
+    s_last = atomicAdd(a.ctr + C_DC_EXIT, 1) == a.G - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    if (a.nv)
+      for (int i = threadIdx.x; i < MAXN; i += blockDim.x) a.rowmax[i] = 0ull;
+    if (threadIdx.x == 0) {
       a.ctr[C_DC_READY] = 0;
       a.ctr[C_DC_HSH] = 0;
       a.ctr[C_DC_HR] = 0;
       a.ctr[C_DC_EXIT] = 0;
       a.ctr[C_DC_DN] = 0;
       a.ctr[C_DC_EPOCH] = (int)s_epoch;
-      __threadfence();
     }
+    __threadfence();
   }
 }
 

@@ -30,7 +30,7 @@ MOE_HD inline int imax(int a, int b) { return a > b ? a : b; }
 // Split-K factor: as many parts as keep `tiles` output tiles within one work
 // unit per block of a `grid`-block launch, at most one part per K stage.
 MOE_HD inline int dc_split(int tiles, int stages, int grid) {
-  int s = grid / tiles;
+  int s = grid / (tiles > 0 ? tiles : 1);
   s = imin(imin(s, stages), DC_MAX_SPLIT);
   return s < 1 ? 1 : s;
 }
@@ -86,6 +86,11 @@ MOE_HD inline int shared_ksplit(int tiles, int nks) {
   if (s > 16) s = 16;
   if (s > nks) s = nks;
   return s < 1 ? 1 : s;
+}
+// The BF16 shared expert runs on tensor cores from TC_MIN_T_SHARED tokens when
+// its 128 x 256 tiles and 64-element K stages divide the shape.
+MOE_HD inline bool shared_tc_path(int T, int H, int I) {
+  return T >= TC_MIN_T_SHARED && H % 256 == 0 && I % 128 == 0;
 }
 // Output tiles of the shared expert's gate/up (first) and down GEMMs on
 // tensor cores: 128 tokens x 256 weight rows.
@@ -229,7 +234,7 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.y_assign = take(sizeof(float) * n * H);
   L.y_shared = take(sizeof(float) * (size_t)T * H);
   {  // split-K partial sums of the shared expert's tensor-core GEMMs
-    const bool shtc = T >= TC_MIN_T_SHARED && H % 256 == 0;
+    const bool shtc = shared_tc_path(T, H, I);
     const size_t s1 = shtc ? shared_ksplit(shared_tiles_gu(T, I), H / 64) : 1;
     const size_t s2 = shtc ? shared_ksplit(shared_tiles_dn(T, H), I / 64) : 1;
     const size_t a = s1 > 1 ? s1 * T * 2 * (size_t)I : 0, b = s2 > 1 ? s2 * T * (size_t)H : 0;

@@ -50,7 +50,8 @@ class DeviceLayer:
         wfmt = MOE_W_MXFP4 if fmt == "mxfp4" else MOE_W_NVFP4
         self.ex_plain = experts(wfmt, self.w13, self.w13_scale, self.w2, self.w2_scale, self.tensor_scale)
         self.ex_prepared = None
-        if prepare:
+        # the tensor-core scale layout exists for H and I multiples of 128
+        if prepare and H % 128 == 0 and I % 128 == 0:
             self.w13_scale_mma = torch.empty_like(self.w13_scale)
             self.w2_scale_mma = torch.empty_like(self.w2_scale)
             moe_prepare_weights(desc(0, H, I, E, top_k, self.fold), self.ex_plain, self.w13_scale_mma,

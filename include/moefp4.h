@@ -89,8 +89,12 @@ typedef enum { MOE_W_MXFP4 = 1, MOE_W_NVFP4 = 2 } moe_wfmt_t;
 
 /* Shape of one MoE layer call.
  * T tokens (>= 0), hidden size H, intermediate size I, E routed experts,
- * top_k experts per token.  Requirements: H and I multiples of 128 (NVFP4:
- * also of 16), 1 <= top_k <= 8, top_k <= E <= 256.  renormalize must be 1
+ * top_k experts per token.  Requirements: H and I multiples of 32 (whole
+ * MXFP4 activation blocks; NVFP4 weights then hold whole 16-element blocks
+ * too), 1 <= top_k <= 8, top_k <= E <= 256.  The tensor-core paths run where
+ * their tiles divide the shape (H and I multiples of 256 for the routed
+ * experts and the fused decode; moe_prepare_weights needs multiples of 128);
+ * every other shape runs on CUDA cores with the same arithmetic.  renormalize must be 1
  * (weights renormalised over the selected experts) and act_quant must be 1
  * (routed-expert activations quantised to MXFP4); other values return
  * MOE_ERR_UNSUPPORTED.
@@ -161,7 +165,8 @@ MOE_API moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* by
  * the canonical scales:
  *   w13_scale_mma  out, E * 2I * H/32 (MXFP4) or E * 2I * H/16 (NVFP4) bytes
  *   w2_scale_mma   out, E * H * I/32 (MXFP4) or E * H * I/16 (NVFP4) bytes
- * (16-byte aligned; the canonical scales 4-byte aligned).  Point
+ * (16-byte aligned; the canonical scales 4-byte aligned).  H and I must be
+ * multiples of 128 (else MOE_ERR_UNSUPPORTED).  Point
  * experts->w13_scale_mma / w2_scale_mma at them afterwards: moe_layer_decode
  * then runs its contractions on tensor cores (when H and I are multiples of
  * 256), and the MXFP4 batched path skips its per-call re-layout. */
@@ -220,7 +225,11 @@ MOE_API moe_status_t moe_quant_act_mxfp8(int32_t rows, int32_t K, const void* x,
                                          uint8_t* scales, moe_stream_t stream);
 
 /* A3: stable counting sort of the T*top_k (token, slot) assignments by
- * expert.  Bit-exact and deterministic.
+ * expert: the token-to-expert permutation and per-expert histogram by which
+ * a fused MoE groups its work, each expert running on the tokens routed to
+ * it (AMD article, section "What we Optimized": the MXFP4 fused MoE; section
+ * "MiniMax-M3.1 at a glance": 4 of 128 routed experts active per token).
+ * Bit-exact and deterministic.
  *   topk_ids  int32 [T, top_k]  (every id in [0, E))
  *   counts    int32 [E] out;  offsets int32 [E+1] out (exclusive prefix sum)
  *   perm      int32 [T*top_k] out: sorted position -> t*top_k + j, ordered by
@@ -281,8 +290,13 @@ MOE_API moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_ex
                               const float* bias, const void* x, void* out, int32_t* topk_ids,
                               float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* The whole layer for any T, as the unfused sequence router -> quantise ->
- * permute -> expert FFNs -> combine (the pages' standard, non-fused path). */
+/* The whole layer for any T, as the sequence router -> quantise -> permute ->
+ * expert FFNs -> combine: the standard path the pages run outside the fused
+ * decode range, i.e. prefill and decode steps of more than 16 tokens (AMD
+ * article, section "What we Optimized": the stacked router GEMM, then the
+ * MXFP4 fused MoE with the shared expert; the single fused launch is kept for
+ * pure decode steps of at most 16 tokens).  Arguments, layouts and results
+ * as for moe_layer_decode; every T >= 0 is accepted. */
 MOE_API moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_experts_t* experts,
                                const moe_shared_bf16_t* shared, const float* w_router,
                                const float* bias, const void* x, void* out, int32_t* topk_ids,
@@ -301,20 +315,33 @@ MOE_API moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_e
  * allocations.  It allocates nothing: its scratch is a fixed array inside the
  * library (MOE_NOALLOC_SCRATCH_BYTES).  Inputs, outputs and results are
  * exactly those of moe_layer_decode.
- *   - Shapes whose moe_workspace_size exceeds MOE_NOALLOC_SCRATCH_BYTES, and
- *     T > 16, return MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *   - Shapes whose moe_workspace_size exceeds MOE_NOALLOC_SCRATCH_BYTES - 256
+ *     (the array's last 256 bytes keep a sticky status word), and T > 16,
+ *     return MOE_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on a device looks up that device's scratch address (with
  *     the device current); make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps what the
  *     previous call left; each call clears the part that must start at zero
- *     (an extra memset on the stream).  Calls whose launches may overlap on
+ *     (one extra small kernel on the stream).  Calls whose launches may overlap on
  *     the GPU (different streams, no ordering between them) race on it.
- *   - A device-side wait that runs out is not reported (there is no workspace
- *     to read a status word from); the next call clears it. */
+ *   - A device-side wait that runs out records MOE_ERR_TIMEOUT (the call's
+ *     output is then unfinished).  Each call first moves a failure left by the
+ *     previous call into the sticky word, where it stays until
+ *     moe_noalloc_get_status reads it; call that after synchronising the
+ *     stream. */
 MOE_API moe_status_t moe_layer_decode_noalloc(const moe_layer_desc_t* desc, const moe_experts_t* experts,
                                               const moe_shared_bf16_t* shared, const float* w_router,
                                               const float* bias, const void* x, void* out, int32_t* topk_ids,
                                               float* topk_w, moe_stream_t stream);
+
+/* Reads (and clears) the device status word of the built-in scratch array of
+ * moe_layer_decode_noalloc on the current device into *st: MOE_OK, or
+ * MOE_ERR_TIMEOUT when a call since the last read had a device-side wait run
+ * out (its output is then unfinished); both the last call's word and the
+ * sticky word are read and cleared.  Call after synchronising the streams
+ * of those calls; like moe_get_status it waits for a 4-byte device-to-host
+ * copy.  The paper has no counterpart to this entry point either. */
+MOE_API moe_status_t moe_noalloc_get_status(moe_status_t* st);
 
 /* Upper bound, in nanoseconds, of every device-side dependency wait of later
  * launches in this process (default 500 ms).  A wait that runs out records
@@ -354,6 +381,11 @@ MOE_API moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const
  * counter that nothing ever advances, with the given limit.  Afterwards
  * moe_get_status reports MOE_ERR_TIMEOUT; the GPU context stays usable. */
 MOE_API moe_status_t moe_debug_wait_probe(void* ws, size_t ws_bytes, uint64_t limit_ns, moe_stream_t stream);
+
+/* The same probe on the built-in scratch array of moe_layer_decode_noalloc
+ * (current device): afterwards moe_noalloc_get_status reports
+ * MOE_ERR_TIMEOUT, also across moe_layer_decode_noalloc calls made in between. */
+MOE_API moe_status_t moe_debug_wait_probe_noalloc(uint64_t limit_ns, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

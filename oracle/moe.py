@@ -13,7 +13,7 @@ GPUs: Day-0 support and optimization"):
   routed-expert weights OCP MXFP4 (static), routed-expert activations OCP
   MXFP4 (dynamic).
 
-Readings where the pages are silent (each one also listed in the design doc):
+Readings where the pages are silent:
 * scores are softmax over the E router logits (the bias, when present, is
   part of the logit); the top-k experts are those with the k largest logits,
   ties to the lower expert index, emitted in that order; their probabilities

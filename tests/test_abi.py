@@ -54,7 +54,8 @@ def test_workspace_size_grows_with_tokens(lib):
 
 @pytest.mark.parametrize("bad,code", [
     (dict(H=100), M.MOE_ERR_INVALID_ARG),
-    (dict(I=96), M.MOE_ERR_INVALID_ARG),
+    (dict(I=80), M.MOE_ERR_INVALID_ARG),
+    (dict(H=48), M.MOE_ERR_INVALID_ARG),
     (dict(top_k=0), M.MOE_ERR_INVALID_ARG),
     (dict(top_k=9), M.MOE_ERR_INVALID_ARG),
     (dict(E=3), M.MOE_ERR_INVALID_ARG),
@@ -69,6 +70,17 @@ def test_invalid_descriptors_rejected(lib, bad, code):
     desc = M.LayerDesc(*[d[k] for k in ("T", "H", "I", "E", "top_k", "renormalize", "act_quant")])
     out = ctypes.c_size_t(0)
     assert lib.moe_workspace_size(ctypes.byref(desc), ctypes.byref(out)) == code
+
+
+@pytest.mark.parametrize("H,I", [(32, 32), (96, 160), (4096, 1536)])
+def test_shapes_in_whole_mxfp4_blocks_accepted(lib, H, I):
+    """H and I only need whole 32-element blocks (the single-block layer
+    H = I = 32 included); shapes the tensor-core tiles do not divide run on
+    CUDA cores."""
+    out = ctypes.c_size_t(0)
+    for T in (1, 16, 300):
+        assert lib.moe_workspace_size(ctypes.byref(M.desc(T, H, I, 8, 2)), ctypes.byref(out)) == M.MOE_OK
+        assert out.value > 0
 
 
 def test_decode_range_and_workspace_checks(lib):

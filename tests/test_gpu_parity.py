@@ -584,17 +584,24 @@ def test_decode_on_converted_weights():
 # --------------------------------------------------------------- edge cases
 
 
-@pytest.mark.parametrize("shape", [(4, 128, 128, 4, 4), (9, 256, 128, 8, 2), (3, 128, 256, 256, 8)])
+@pytest.mark.parametrize("shape", [(4, 128, 128, 4, 4, W.MXFP4), (9, 256, 128, 8, 2, W.MXFP4),
+                                   (3, 128, 256, 256, 8, W.MXFP4), (3, 32, 32, 4, 2, W.MXFP4),
+                                   (5, 32, 32, 4, 2, W.NVFP4), (13, 96, 160, 8, 4, W.MXFP4),
+                                   (70, 160, 96, 8, 4, W.NVFP4), (140, 96, 224, 16, 2, W.MXFP4)])
 def test_small_and_degenerate_shapes(shape):
-    """Dense mixture (E == k), minimal H and I, E = 256 with k = 8."""
-    T, H, I, E, k = shape
-    wl = W.Workload("edge", T, H, I, E, k, W.MXFP4, 21, 0.5)
+    """Dense mixture (E == k), E = 256 with k = 8, and H, I that only hold
+    whole 32-element blocks: the single-block layer H = I = 32 (one MXFP4
+    block along each), and shapes no tensor-core tile divides (CUDA-core
+    paths; 70 and 140 tokens take the batched path with >= 256 assignments)."""
+    T, H, I, E, k, fmt = shape
+    wl = W.Workload("edge", T, H, I, E, k, fmt, 21, 0.5)
     lay = W.generate(wl)
     dev = DeviceLayer(lay, H, I, E, k, wl.fmt, T_max=T)
     cache = {}
-    out, ids, _ = dev.decode(bf16_tensor(lay["x"]))
-    torch.cuda.synchronize()
-    _compare_layer(wl, lay, cache, out, ids)
+    if T <= 16:
+        out, ids, _ = dev.decode(bf16_tensor(lay["x"]))
+        torch.cuda.synchronize()
+        _compare_layer(wl, lay, cache, out, ids)
     out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
     torch.cuda.synchronize()
     _compare_layer(wl, lay, cache, out, ids)
@@ -642,6 +649,31 @@ def test_decode_after_large_forward_on_one_workspace():
             torch.cuda.synchronize()
             assert M.moe_get_status(dev.ws) == M.MOE_OK
             _compare_layer(wl.with_tokens(T), sub, cache, o, i)
+
+
+def test_nvfp4_decode_across_launch_number_wrap():
+    """The tensor-core NVFP4 decode tags its router logits and its per-row h
+    exponents (combined by atomicMax) with a 32-bit launch number kept in the
+    workspace.  Seeded two launches below the wrap, three launches whose
+    tokens differ in magnitude by 2^6 (so their h row exponents differ) each
+    match the oracle: nothing left by the launch before the wrap survives into
+    the launches after it."""
+    wl = W.Workload("wrap_nv", 16, 512, 256, 16, 4, W.NVFP4, 33, 0.05)
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, wl.H, wl.I, wl.E, wl.top_k, wl.fmt, T_max=wl.T)
+    assert dev.prepared
+    C_DC_EPOCH = 12
+    dev.ws[:64].view(torch.int32)[C_DC_EPOCH] = -2  # the next launch is number 0xFFFFFFFF
+    cache = {}
+    for i, mag in enumerate((2.0 ** 6, 1.0, 2.0 ** 3)):
+        x = F.bf16_bits_to_float(W.generate_tokens(wl, 40 + i, wl.T)) * mag
+        sub = dict(lay)
+        sub["x"] = F.bf16_value_to_bits(F.round_to_bf16(x))
+        out, ids, _ = dev.decode(bf16_tensor(sub["x"]))
+        torch.cuda.synchronize()
+        assert M.moe_get_status(dev.ws) == M.MOE_OK
+        _compare_layer(wl, sub, cache, out, ids)
+    assert int(dev.ws[:64].view(torch.int32)[C_DC_EPOCH]) == 2  # 0xFFFFFFFF, then 1 and 2 (0 is skipped)
 
 
 def test_tensor_core_decode_without_shared_expert():

@@ -51,6 +51,27 @@ def test_noalloc_matches_workspace_decode_twice(lib, name):
         assert err <= LAYER_TOL, err
         assert torch.equal(ids, ref_ids)
         assert torch.allclose(w, ref_w, rtol=1e-6, atol=0)
+    assert M.moe_noalloc_get_status() == M.MOE_OK
+
+
+def test_noalloc_keeps_a_recorded_timeout_until_read(lib):
+    """A device-side wait that ran out on the built-in scratch stays recorded
+    across later calls (whose per-call clear leaves the status word alone)
+    until moe_noalloc_get_status reads it; the timeout is made by the library's
+    wait probe (a bounded wait on a counter nothing advances), not by a
+    decode."""
+    wl = W.WORKLOADS["tiny"]
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, wl.H, wl.I, wl.E, wl.top_k, wl.fmt, T_max=wl.T)
+    x = torch.from_numpy(lay["x"]).view(torch.int16).cuda()
+    ref_out, _, _ = dev.decode(x)
+    M.moe_debug_wait_probe_noalloc(2_000_000)
+    out, ids, w = dev.outputs(wl.T)
+    M.moe_layer_decode_noalloc(dev.desc(wl.T), dev.ex, dev.sh, dev.w_router, dev.bias, x, out, ids, w)
+    torch.cuda.synchronize()
+    assert M.moe_noalloc_get_status() == M.MOE_ERR_TIMEOUT
+    assert M.moe_noalloc_get_status() == M.MOE_OK  # reading clears it
+    assert torch.equal(out, ref_out)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
