@@ -30,7 +30,7 @@ EXPORTED = [
     "moe_layer_decode", "moe_layer_forward", "moe_set_wait_limit_ns", "moe_debug_wait_probe",
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
     "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8", "moe_shared_expert_mxfp8",
-    "moe_noalloc_get_status", "moe_debug_wait_probe_noalloc",
+    "moe_noalloc_get_status", "moe_debug_wait_probe_noalloc", "moe_debug_launch_count", "moe_set_timing_events",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -102,6 +102,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_decode_noalloc": ([P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
         "moe_noalloc_get_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
         "moe_debug_wait_probe_noalloc": ([U64, P], ctypes.c_int),
+        "moe_debug_launch_count": ([ctypes.POINTER(ctypes.c_uint64)], None),
+        "moe_set_timing_events": ([P, P], None),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
         "moe_prepare_weights": ([P, P, P, P, P], ctypes.c_int),
         "moe_convert_nvfp4_to_mxfp4": ([P, P, P, P, P, P, P], ctypes.c_int),
@@ -290,3 +292,15 @@ def moe_noalloc_get_status() -> int:
 
 def moe_debug_wait_probe_noalloc(limit_ns: int, stream=None) -> None:
     _check(load().moe_debug_wait_probe_noalloc(int(limit_ns), _stream(stream)), "moe_debug_wait_probe_noalloc")
+
+
+def moe_debug_launch_count() -> int:
+    n = ctypes.c_uint64(0)
+    load().moe_debug_launch_count(ctypes.byref(n))
+    return n.value
+
+
+def moe_set_timing_events(begin=None, end=None) -> None:
+    """begin / end: torch.cuda.Event objects (or raw cudaEvent_t ints), None = off."""
+    h = lambda e: None if e is None else (e if isinstance(e, int) else e.cuda_event)
+    load().moe_set_timing_events(h(begin), h(end))

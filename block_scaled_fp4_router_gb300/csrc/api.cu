@@ -15,6 +15,8 @@ namespace {
 
 std::atomic<uint64_t> g_wait_limit_ns{500ull * 1000 * 1000};
 std::atomic<int> g_routed_gemm{TC_GEMM_AUTO};
+std::atomic<uint64_t> g_launches{0};
+std::atomic<cudaEvent_t> g_marks[2] = {{nullptr}, {nullptr}};
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -163,7 +165,33 @@ moe_status_t run_forward(const moe_layer_desc_t* desc, const ExpertsDev& ex, con
 
 }  // namespace
 
+namespace moefp4 {
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+void record_mark(TimingMark m, cudaStream_t s) {
+  cudaEvent_t ev = g_marks[m].load();
+  if (!ev) return;
+  // inside a stream capture the record must become an event node of the graph
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
+}
+
+}  // namespace moefp4
+
 extern "C" {
+
+void moe_debug_launch_count(uint64_t* n) {
+  if (n) *n = g_launches.load();
+}
+
+void moe_set_timing_events(void* routed_gemm_begin, void* routed_gemm_end) {
+  g_marks[MARK_ROUTED_GEMM_BEGIN].store(static_cast<cudaEvent_t>(routed_gemm_begin));
+  g_marks[MARK_ROUTED_GEMM_END].store(static_cast<cudaEvent_t>(routed_gemm_end));
+}
 
 const char* moe_status_string(moe_status_t st) {
   switch (st) {
@@ -427,7 +455,11 @@ moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t*
   if (fused_decode_tc_supported(sh, ex))
     return cuda_status(launch_fused_decode_tc(sh, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws,
                                               g_wait_limit_ns.load(), s, desc->shared_in_table));
-  if (desc->shared_in_table) return run_forward(desc, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws, s);
+  // The CUDA-core single launch streams weight rows in 64-element pairs (32-byte
+  // code loads, 2- or 4-byte scale loads): shapes with H or I not a multiple of
+  // 64 take the per-step kernels, which work in 32-element blocks.
+  if (desc->shared_in_table || !fused_decode_supported(sh))
+    return run_forward(desc, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws, s);
   return cuda_status(launch_fused_decode(sh, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws,
                                          g_wait_limit_ns.load(), s));
 }

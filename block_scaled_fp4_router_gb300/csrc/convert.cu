@@ -73,7 +73,7 @@ cudaError_t launch_one(const uint8_t* c, const uint8_t* s, const float* ts, int 
                        int p1, uint8_t* co, uint8_t* so, cudaStream_t st) {
   const size_t n = (size_t)E * R * (K / 32);
   if (n == 0) return cudaSuccess;
-  k_nv_to_mx<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(c, s, ts, E, R, K, split, p0, p1, co, so);
+  count_launch(), k_nv_to_mx<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(c, s, ts, E, R, K, split, p0, p1, co, so);
   return cudaGetLastError();
 }
 

@@ -36,7 +36,7 @@ cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t
   const size_t n = bytes / 16;
   if (n == 0) return cudaSuccess;
   const size_t blocks = (n + 256 * CP16 - 1) / (256 * CP16);
-  k_copy16<<<(unsigned)(blocks < 65535 ? blocks : 65535), 256, 0, s>>>(static_cast<uint4*>(dst),
+  count_launch(), k_copy16<<<(unsigned)(blocks < 65535 ? blocks : 65535), 256, 0, s>>>(static_cast<uint4*>(dst),
                                                                        static_cast<const uint4*>(src), n);
   return cudaGetLastError();
 }

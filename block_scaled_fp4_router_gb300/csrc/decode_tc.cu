@@ -1225,7 +1225,7 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, m, a);
+  return count_launch(), cudaLaunchKernelEx(&cfg, kern, m, a);
 }
 
 }  // namespace moefp4

@@ -230,7 +230,7 @@ cudaError_t launch_combine(const Shape& sh, const float* y_assign, const int* in
                            const float* y_shared, uint16_t* out, cudaStream_t s) {
   const size_t n = (size_t)sh.T * sh.H / 4;
   if (n == 0) return cudaSuccess;
-  k_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(sh, y_assign, inv_perm, w, y_shared, out);
+  count_launch(), k_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(sh, y_assign, inv_perm, w, y_shared, out);
   return cudaGetLastError();
 }
 
@@ -253,9 +253,9 @@ cudaError_t launch_routed_simt(const Shape& sh, const ExpertsDev& ex, const uint
     if ((err = set_smem(fn, smem)) != cudaSuccess) return err;
     dim3 grid(sh.E, I / 32);
     if (ex.nv)
-      k_routed_gate_up<true><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs);
+      count_launch(), k_routed_gate_up<true><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs);
     else
-      k_routed_gate_up<false><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs);
+      count_launch(), k_routed_gate_up<false><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   {
@@ -264,9 +264,9 @@ cudaError_t launch_routed_simt(const Shape& sh, const ExpertsDev& ex, const uint
     if ((err = set_smem(fn, smem)) != cudaSuccess) return err;
     dim3 grid(sh.E, H / 32);
     if (ex.nv)
-      k_routed_down<true><<<grid, THREADS, smem, s>>>(sh, ex, hq, hs, offsets, y_assign);
+      count_launch(), k_routed_down<true><<<grid, THREADS, smem, s>>>(sh, ex, hq, hs, offsets, y_assign);
     else
-      k_routed_down<false><<<grid, THREADS, smem, s>>>(sh, ex, hq, hs, offsets, y_assign);
+      count_launch(), k_routed_down<false><<<grid, THREADS, smem, s>>>(sh, ex, hq, hs, offsets, y_assign);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   return cudaSuccess;
@@ -280,13 +280,13 @@ cudaError_t launch_shared_simt(const Shape& sh, const SharedDev& shd, const uint
   {
     const size_t smem = (size_t)NT_SH * H * 2 + sizeof(float) * 16 * NT_SH;
     if ((err = set_smem((const void*)k_shared_gate_up, smem)) != cudaSuccess) return err;
-    k_shared_gate_up<<<I / 8, THREADS, smem, s>>>(sh, shd, x, h_shared);
+    count_launch(), k_shared_gate_up<<<I / 8, THREADS, smem, s>>>(sh, shd, x, h_shared);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   {
     const size_t smem = (size_t)NT * I * 2;
     if ((err = set_smem((const void*)k_shared_down, smem)) != cudaSuccess) return err;
-    k_shared_down<<<H / 16, THREADS, smem, s>>>(sh, shd, h_shared, y_shared);
+    count_launch(), k_shared_down<<<H / 16, THREADS, smem, s>>>(sh, shd, h_shared, y_shared);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   return cudaSuccess;

@@ -508,6 +508,7 @@ cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const Sha
                                 int* ids_out, float* w_out, void* ws, uint64_t wait_limit_ns,
                                 cudaStream_t s) {
   if (sh.T == 0) return cudaSuccess;
+  if (!fused_decode_supported(sh)) return cudaErrorInvalidValue;
   const WsLayout L = ws_layout(sh.T, sh.H, sh.I, sh.E, sh.k);
   uint8_t* base = static_cast<uint8_t*>(ws);
   const bool shared = shd.w13 != nullptr;
@@ -557,12 +558,12 @@ cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const Sha
   int grid = sms * per_sm;
   if (grid > a.u_end) grid = a.u_end;
   void* args[] = {&a};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(FT), args, sp.bytes, s);
+  return count_launch(), cudaLaunchKernel(fn, dim3(grid), dim3(FT), args, sp.bytes, s);
 }
 
 cudaError_t launch_wait_probe(void* ws, uint64_t wait_limit_ns, cudaStream_t s) {
   int* ctr = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ws_layout(0, 128, 128, 1, 1).counters);
-  k_wait_probe<<<1, 32, 0, s>>>(ctr, wait_limit_ns);
+  count_launch(), k_wait_probe<<<1, 32, 0, s>>>(ctr, wait_limit_ns);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,13 @@
 
 namespace moefp4 {
 
+// Instrumentation (defined in api.cu): every kernel launch of the library is
+// counted (moe_debug_launch_count), and the routed tensor-core GEMMs of the
+// batched path are bracketed by the events set with moe_set_timing_events.
+void count_launch();
+enum TimingMark { MARK_ROUTED_GEMM_BEGIN = 0, MARK_ROUTED_GEMM_END = 1 };
+void record_mark(TimingMark m, cudaStream_t s);
+
 struct ExpertsDev {
   int nv;  // 0 = MXFP4, 1 = NVFP4
   const uint8_t* w13;
@@ -106,7 +113,11 @@ cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const
 // A9
 cudaError_t launch_combine(const Shape& sh, const float* y_assign, const int* inv_perm, const float* w,
                            const float* y_shared, uint16_t* out, cudaStream_t s);
-// A10
+// A10 on CUDA cores: needs H and I multiples of 64 (rows streamed in
+// 64-element pairs by 32-byte loads).
+inline bool fused_decode_supported(const Shape& sh) {
+  return sh.T >= 1 && sh.T <= MAX_DECODE_T && sh.H % 64 == 0 && sh.I % 64 == 0;
+}
 cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd,
                                 const float* wr, const float* bias, const uint16_t* x, uint16_t* out,
                                 int* ids_out, float* w_out, void* ws, uint64_t wait_limit_ns,

@@ -96,7 +96,7 @@ extern "C" moe_status_t moe_layer_decode_noalloc(const moe_layer_desc_t* desc, c
   static_assert(moefp4::C_STATUS == 0, "the status word is the scratch's first int");
   const size_t n16 = zero_bytes / 16;  // zero_end is a multiple of 256
   uint8_t* base = static_cast<uint8_t*>(ws);
-  k_noalloc_begin<<<(unsigned)((n16 + 255) / 256), 256, 0, s>>>(reinterpret_cast<uint4*>(base), n16,
+  moefp4::count_launch(), k_noalloc_begin<<<(unsigned)((n16 + 255) / 256), 256, 0, s>>>(reinterpret_cast<uint4*>(base), n16,
                                                                  reinterpret_cast<int*>(base + kStickyOffset));
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   return moe_layer_decode(desc, experts, shared, w_router, bias, x, out, topk_ids, topk_w, ws, kStickyOffset,

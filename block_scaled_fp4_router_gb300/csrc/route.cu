@@ -39,7 +39,7 @@ cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* code
   const size_t ngroups = (size_t)rows * K / 8;
   if (ngroups == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((ngroups + 256 * QG - 1) / (256 * QG));
-  k_quant_mxfp4<<<blocks, 256, 0, s>>>(x, ngroups, codes, scales);
+  count_launch(), k_quant_mxfp4<<<blocks, 256, 0, s>>>(x, ngroups, codes, scales);
   return cudaGetLastError();
 }
 
@@ -65,7 +65,7 @@ cudaError_t launch_quant_mxfp8(const uint16_t* x, int rows, int K, uint8_t* code
   const size_t ngroups = (size_t)rows * K / 8;
   if (ngroups == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((ngroups + 256 * QG - 1) / (256 * QG));
-  k_quant_mxfp8<<<blocks, 256, 0, s>>>(x, ngroups, codes, scales);
+  count_launch(), k_quant_mxfp8<<<blocks, 256, 0, s>>>(x, ngroups, codes, scales);
   return cudaGetLastError();
 }
 
@@ -331,21 +331,21 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float
   cudaError_t err;
   if (T <= 16) {
     dim3 grid(E, (T + 15) / 16);
-    k_router_gemv<<<grid, 256, 0, s>>>(x, wr, bias, logits, T, H, E);
+    count_launch(), k_router_gemv<<<grid, 256, 0, s>>>(x, wr, bias, logits, T, H, E);
     return cudaGetLastError();
   }
   if (T <= 512) {
     dim3 grid((T + RSM - 1) / RSM, (E + RSM - 1) / RSM, S);
-    k_router_splitk<<<grid, 256, 0, s>>>(x, wr, part, T, H, E, S);
+    count_launch(), k_router_splitk<<<grid, 256, 0, s>>>(x, wr, part, T, H, E, S);
   } else {
     dim3 grid((T + RBM - 1) / RBM, (E + RBN - 1) / RBN, S);
-    k_router_sgemm<<<grid, 256, 0, s>>>(x, wr, bias, S == 1 ? logits : part, T, H, E, S);
+    count_launch(), k_router_sgemm<<<grid, 256, 0, s>>>(x, wr, bias, S == 1 ? logits : part, T, H, E, S);
   }
   err = cudaGetLastError();
   if (err != cudaSuccess || (S == 1 && T > 512)) return err;
   const size_t n = (size_t)T * E;
   const size_t threads = E % 4 == 0 ? n / 4 : n;
-  k_router_sum<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(part, bias, logits, T, E, S);
+  count_launch(), k_router_sum<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(part, bias, logits, T, E, S);
   return cudaGetLastError();
 }
 
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s,
                         int* ids_ext, float* w_ext) {
   if (T == 0) return cudaSuccess;
-  k_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, ids, w, ids_ext, w_ext);
+  count_launch(), k_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, ids, w, ids_ext, w_ext);
   return cudaGetLastError();
 }
 
@@ -474,10 +474,10 @@ cudaError_t launch_permute(const int* ids, int T, int k, int E, int* counts, int
   const int n = T * k;
   const int nchunks = (n + PERM_CHUNK - 1) / PERM_CHUNK;
   if (nchunks > 0) {
-    k_perm_rank<<<nchunks, PERM_CHUNK, 0, s>>>(ids, n, E, rank, chunk_cnt);
+    count_launch(), k_perm_rank<<<nchunks, PERM_CHUNK, 0, s>>>(ids, n, E, rank, chunk_cnt);
   }
-  k_perm_scan<<<1, MAX_E, 0, s>>>(chunk_cnt, nchunks, E, chunk_base, counts, offsets);
-  if (n > 0) k_perm_scatter<<<(n + 255) / 256, 256, 0, s>>>(ids, n, E, rank, chunk_base, offsets, perm, inv_perm);
+  count_launch(), k_perm_scan<<<1, MAX_E, 0, s>>>(chunk_cnt, nchunks, E, chunk_base, counts, offsets);
+  if (n > 0) count_launch(), k_perm_scatter<<<(n + 255) / 256, 256, 0, s>>>(ids, n, E, rank, chunk_base, offsets, perm, inv_perm);
   return cudaGetLastError();
 }
 

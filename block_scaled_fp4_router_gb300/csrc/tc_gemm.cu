@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(256) k_relayout_weight_sf(const uint8_t* __res
 cudaError_t launch_relayout_weight_sf(const uint8_t* s, int E, int R, int K, uint8_t* out, cudaStream_t st) {
   const size_t words = (size_t)E * R * (K / 128);
   if (words == 0) return cudaSuccess;
-  k_relayout_weight_sf<<<(unsigned)((words + 255) / 256), 256, 0, st>>>(s, E, R, K, reinterpret_cast<uint32_t*>(out));
+  count_launch(), k_relayout_weight_sf<<<(unsigned)((words + 255) / 256), 256, 0, st>>>(s, E, R, K, reinterpret_cast<uint32_t*>(out));
   return cudaGetLastError();
 }
 
@@ -751,7 +751,7 @@ cudaError_t launch_copy_h(const Shape& sh, const int* hpath, const uint8_t* hq_s
   const int blocks = tc_routed_enabled(n) ? max(max(tc_padded_rows(n, sh.E) / BM, tc_padded_rows_win(n, sh.E, 64) / 64),
                                                 (n + 127) / 128)
                                           : (n + 127) / 128;
-  k_copy_h<<<blocks, 128, 0, s>>>(n, sh.I, hpath, hq_sorted, hs_sorted, reinterpret_cast<const MTile*>(w.mtiles),
+  count_launch(), k_copy_h<<<blocks, 128, 0, s>>>(n, sh.I, hpath, hq_sorted, hs_sorted, reinterpret_cast<const MTile*>(w.mtiles),
                                   w.num_mt, w.hq_perm, reinterpret_cast<const uint32_t*>(w.hs_mma), hq_out, hs_out);
   return cudaGetLastError();
 }
@@ -804,7 +804,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int grid = max(1, min(max_tiles, sm_count()));
-  k_tc_gemm<KIND, EPI, GROUPED><<<grid, TC_THREADS, smem, s>>>(a, b, g);
+  count_launch(), k_tc_gemm<KIND, EPI, GROUPED><<<grid, TC_THREADS, smem, s>>>(a, b, g);
   return cudaGetLastError();
 }
 
@@ -817,7 +817,7 @@ cudaError_t launch_gemm_wa(const CUtensorMap& w, const CUtensorMap& x, const Gem
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int grid = max(1, min(max_tiles, sm_count()));
-  k_tc_gemm_wa<EPI><<<grid, TC_THREADS, smem, s>>>(w, x, g);
+  count_launch(), k_tc_gemm_wa<EPI><<<grid, TC_THREADS, smem, s>>>(w, x, g);
   return cudaGetLastError();
 }
 
@@ -836,9 +836,9 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   const int win = wa ? WA_WIN : BM;
   const int rmax = tc_padded_rows_win(n, E, win);
   cudaError_t err;
-  k_build_mtiles<<<1, 256, 0, s>>>(offsets, E, win, w.poff, reinterpret_cast<MTile*>(w.mtiles), w.num_mt);
+  count_launch(), k_build_mtiles<<<1, 256, 0, s>>>(offsets, E, win, w.poff, reinterpret_cast<MTile*>(w.mtiles), w.num_mt);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  k_gather_mx_rows<<<rmax / GR, 128, 0, s>>>(xq, xs, H, sh.k, perm, reinterpret_cast<const MTile*>(w.mtiles),
+  count_launch(), k_gather_mx_rows<<<rmax / GR, 128, 0, s>>>(xq, xs, H, sh.k, perm, reinterpret_cast<const MTile*>(w.mtiles),
                                              w.num_mt, win, wa ? 1 : 0, w.xq_perm,
                                              reinterpret_cast<uint32_t*>(w.xs_mma));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -852,6 +852,7 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   }
   const int max_mt = rmax / win;
   CUtensorMap ma, mb;
+  record_mark(MARK_ROUTED_GEMM_BEGIN, s);
   if (wa) {
     // gate/up: A = W13 [E*2I][H/2], B = gathered activations [rmax][H/2] in 16-row boxes
     if ((err = make_map(&ma, ex.w13, (uint64_t)E * 2 * I, H / 2)) != cudaSuccess) return err;
@@ -888,7 +889,9 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
     g2.ldo = H;
     g2.status = status;
     g2.limit_ns = limit_ns;
-    return launch_gemm_wa<EPI_STORE_F32>(ma, mb, g2, max_mt * g2.n_tiles, s);
+    if ((err = launch_gemm_wa<EPI_STORE_F32>(ma, mb, g2, max_mt * g2.n_tiles, s)) != cudaSuccess) return err;
+    record_mark(MARK_ROUTED_GEMM_END, s);
+    return cudaSuccess;
   }
   // gate/up: A = gathered activations [rmax][H/2], B = W13 [E*2I][H/2]
   if ((err = make_map(&ma, w.xq_perm, rmax, H / 2)) != cudaSuccess) return err;
@@ -925,7 +928,10 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   g2.ldo = H;
   g2.status = status;
   g2.limit_ns = limit_ns;
-  return launch_gemm<KIND_FP4, EPI_STORE_F32, true>(ma, mb, g2, max_mt * g2.n_tiles, s);
+  if ((err = launch_gemm<KIND_FP4, EPI_STORE_F32, true>(ma, mb, g2, max_mt * g2.n_tiles, s)) != cudaSuccess)
+    return err;
+  record_mark(MARK_ROUTED_GEMM_END, s);
+  return cudaSuccess;
 }
 
 namespace {
@@ -1047,7 +1053,7 @@ cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16
     if ((err = launch_gemm<KIND_BF16, EPI_STORE_F32, false>(ma, mb, g1, mt * g1.n_tiles * s1, s)) != cudaSuccess)
       return err;
     const size_t n4 = (size_t)T * I / 4;
-    k_swiglu_parts<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(parts, s1, T, I, h_shared);
+    count_launch(), k_swiglu_parts<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(parts, s1, T, I, h_shared);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   } else {
     if ((err = make_map(&ma, x, T, (uint64_t)H * 2)) != cudaSuccess) return err;
@@ -1082,7 +1088,7 @@ cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16
     return err;
   if (s2 > 1) {
     const size_t n = (size_t)T * H;
-    k_sum_parts<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(parts, s2, n, y_shared);
+    count_launch(), k_sum_parts<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(parts, s2, n, y_shared);
     return cudaGetLastError();
   }
   return cudaSuccess;

@@ -284,7 +284,9 @@ MOE_API moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_as
  *   x          BF16 [T, H];  out BF16 [T, H]
  *   topk_ids   int32 [T, top_k] out or NULL;  topk_w FP32 [T, top_k] out or NULL
  * The launch is persistent (one block per SM slot); its dependency waits are
- * bounded and report MOE_ERR_TIMEOUT through moe_get_status. */
+ * bounded and report MOE_ERR_TIMEOUT through moe_get_status.  Shapes whose H
+ * or I is not a multiple of 64 run as the per-step sequence of
+ * moe_layer_forward instead (same arithmetic, several launches). */
 MOE_API moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t* experts,
                               const moe_shared_bf16_t* shared, const float* w_router,
                               const float* bias, const void* x, void* out, int32_t* topk_ids,
@@ -386,6 +388,21 @@ MOE_API moe_status_t moe_debug_wait_probe(void* ws, size_t ws_bytes, uint64_t li
  * (current device): afterwards moe_noalloc_get_status reports
  * MOE_ERR_TIMEOUT, also across moe_layer_decode_noalloc calls made in between. */
 MOE_API moe_status_t moe_debug_wait_probe_noalloc(uint64_t limit_ns, moe_stream_t stream);
+
+/* Instrumentation: the number of kernels this library has enqueued in this
+ * process so far (launches captured into a CUDA graph count once, at
+ * capture).  No counterpart on the pages. */
+MOE_API void moe_debug_launch_count(uint64_t* n);
+
+/* Instrumentation: two CUDA events (cudaEvent_t, created by the caller; NULL
+ * = off) that later moe_expert_ffn_fp4 / moe_layer_forward calls whose routed
+ * experts run on tensor cores record on their stream right before the routed
+ * gate/up GEMM and right after the routed down GEMM, so the caller can time
+ * the two block-scaled FP4 contractions alone (the prefill FP4 tensor-core
+ * rate).  Inside a stream capture they become external event nodes of the
+ * graph.  Process-wide, like moe_set_routed_gemm.  No counterpart on the
+ * pages. */
+MOE_API void moe_set_timing_events(void* routed_gemm_begin, void* routed_gemm_end);
 
 #ifdef __cplusplus
 }
