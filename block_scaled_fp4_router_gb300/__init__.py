@@ -31,6 +31,7 @@ EXPORTED = [
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
     "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8", "moe_shared_expert_mxfp8",
     "moe_noalloc_get_status", "moe_debug_wait_probe_noalloc", "moe_debug_launch_count", "moe_set_timing_events",
+    "moe_dequant_mxfp8_to_bf16",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -103,6 +104,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_noalloc_get_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
         "moe_debug_wait_probe_noalloc": ([U64, P], ctypes.c_int),
         "moe_debug_launch_count": ([ctypes.POINTER(ctypes.c_uint64)], None),
+        "moe_dequant_mxfp8_to_bf16": ([I32, I32, P, P, P, P], ctypes.c_int),
         "moe_set_timing_events": ([P, P], None),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
         "moe_prepare_weights": ([P, P, P, P, P], ctypes.c_int),
@@ -304,3 +306,8 @@ def moe_set_timing_events(begin=None, end=None) -> None:
     """begin / end: torch.cuda.Event objects (or raw cudaEvent_t ints), None = off."""
     h = lambda e: None if e is None else (e if isinstance(e, int) else e.cuda_event)
     load().moe_set_timing_events(h(begin), h(end))
+
+
+def moe_dequant_mxfp8_to_bf16(rows, K, codes, scales, out, stream=None):
+    _check(load().moe_dequant_mxfp8_to_bf16(int(rows), int(K), _p(codes), _p(scales), _p(out), _stream(stream)),
+           "moe_dequant_mxfp8_to_bf16")

@@ -326,6 +326,15 @@ moe_status_t moe_quant_act_mxfp8(int32_t rows, int32_t K, const void* x, uint8_t
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_dequant_mxfp8_to_bf16(int32_t rows, int32_t K, const uint8_t* codes, const uint8_t* scales,
+                                       void* out, moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!codes || !scales || !out || !aligned(codes, 8) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_mxfp8_to_bf16(codes, scales, (size_t)rows * K, static_cast<uint16_t*>(out),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const float* w_router,
                              const float* bias, int32_t* topk_ids, float* topk_w, float* logits,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {

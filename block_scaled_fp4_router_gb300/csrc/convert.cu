@@ -79,6 +79,43 @@ cudaError_t launch_one(const uint8_t* c, const uint8_t* s, const float* ts, int 
 
 }  // namespace
 
+namespace {
+
+// MXFP8 -> BF16, one thread per 8 consecutive elements (their scale is the
+// E8M0 byte of the 32-element block g / 4).  The E4M3 value (at most four
+// significant bits, converted exactly through f16) times 2^(b - 127) is exact
+// in FP32 (down to its subnormals; at or above 2^128 it overflows to inf, as
+// BF16 would), so the one RNE conversion to BF16 is the only rounding, and
+// it is exact wherever the value lies in BF16's normal range.  A NaN code or
+// the E8M0 NaN byte 0xFF gives NaN.
+__global__ void __launch_bounds__(256) k_mxfp8_to_bf16(const uint8_t* __restrict__ codes,
+                                                       const uint8_t* __restrict__ scales, size_t ngroups,
+                                                       uint16_t* __restrict__ out) {
+  const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= ngroups) return;
+  const uint2 c = __ldg(reinterpret_cast<const uint2*>(codes) + g);
+  const uint32_t sb = __ldg(scales + g / 4);
+  const float sc = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : e8m0_to_f32(sb);
+  const uint32_t w[2] = {c.x, c.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = e4m3x2_to_f32x2(w[i >> 1] >> (16 * (i & 1)));
+    o[i] = (uint32_t)f32_to_bf16_rn(f.x * sc) | ((uint32_t)f32_to_bf16_rn(f.y * sc) << 16);
+  }
+  reinterpret_cast<uint4*>(out)[g] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp8_to_bf16(const uint8_t* codes, const uint8_t* scales, size_t n, uint16_t* out,
+                                 cudaStream_t s) {
+  const size_t ngroups = n / 8;
+  if (ngroups == 0) return cudaSuccess;
+  count_launch(), k_mxfp8_to_bf16<<<(unsigned)((ngroups + 255) / 256), 256, 0, s>>>(codes, scales, ngroups, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_nvfp4_to_mxfp4(const Shape& sh, const ExpertsDev& ex, uint8_t* w13_out, uint8_t* w13s_out,
                                   uint8_t* w2_out, uint8_t* w2s_out, cudaStream_t s) {
   const int H = sh.H, I = sh.I, E = sh.E;

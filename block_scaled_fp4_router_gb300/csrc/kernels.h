@@ -136,6 +136,9 @@ cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t
 // NVFP4 -> MXFP4 conversion of the routed experts (load time).
 cudaError_t launch_nvfp4_to_mxfp4(const Shape& sh, const ExpertsDev& ex, uint8_t* w13_out, uint8_t* w13s_out,
                                   uint8_t* w2_out, uint8_t* w2s_out, cudaStream_t s);
+// MXFP8 (E4M3 codes [n], E8M0 scales [n/32]) -> BF16 [n], n a multiple of 32.
+cudaError_t launch_mxfp8_to_bf16(const uint8_t* codes, const uint8_t* scales, size_t n, uint16_t* out,
+                                 cudaStream_t s);
 // A bounded wait on a counter nothing ever advances (exercises the timeout path).
 cudaError_t launch_wait_probe(void* ws, uint64_t wait_limit_ns, cudaStream_t s);
 

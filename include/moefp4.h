@@ -224,6 +224,21 @@ MOE_API moe_status_t moe_quant_act_mxfp4(int32_t rows, int32_t K, const void* x,
 MOE_API moe_status_t moe_quant_act_mxfp8(int32_t rows, int32_t K, const void* x, uint8_t* codes,
                                          uint8_t* scales, moe_stream_t stream);
 
+/* Lossless MXFP8 -> BF16 dequantising copy (vLLM PR #64273, section
+ * "Purpose": an E4M3 value times a power-of-two scale is exact in BF16, so an
+ * MXFP8 checkpoint tensor dequantises to BF16 without rounding):
+ *   out[r, c] = BF16(E4M3(codes[r, c]) * 2^(scales[r, c / 32] - 127))
+ * with one rounding, to nearest even, which changes nothing where the value
+ * lies in BF16's normal range (BF16 keeps 8 significant bits, E4M3 has at
+ * most 4); below it BF16 subnormals round, at or above 2^128 the result is
+ * +-inf, and a NaN code or the E8M0 NaN byte 0xFF gives NaN.
+ *   codes   uint8 E4M3 [rows, K] (8-byte aligned), K a multiple of 32
+ *   scales  uint8 E8M0 [rows, K/32]
+ *   out     BF16 [rows, K] (16-byte aligned)
+ * Meant for load time (for example an MXFP8 shared expert kept as BF16). */
+MOE_API moe_status_t moe_dequant_mxfp8_to_bf16(int32_t rows, int32_t K, const uint8_t* codes,
+                                               const uint8_t* scales, void* out, moe_stream_t stream);
+
 /* A3: stable counting sort of the T*top_k (token, slot) assignments by
  * expert: the token-to-expert permutation and per-expert histogram by which
  * a fused MoE groups its work, each expert running on the tokens routed to

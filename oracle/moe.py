@@ -18,6 +18,10 @@ Readings where the pages are silent:
   part of the logit); the top-k experts are those with the k largest logits,
   ties to the lower expert index, emitted in that order; their probabilities
   are renormalised to sum to 1;
+* the sigmoid variant (layer["score"] == "sigmoid"): scores are sigmoid of
+  the raw router logits, the bias only corrects the selection (the k largest
+  sigmoid + bias, ties to the lower index, in that order), and the weights
+  are the selected sigmoid scores renormalised to sum to 1;
 * an expert is a SwiGLU FFN: h = SiLU(x W_gate^T) * (x W_up^T), y = h W_down^T,
   with SiLU(g) = g / (1 + exp(-g));
 * a routed expert sees the token quantised to MXFP4 (per 32 along H), and its
@@ -76,17 +80,42 @@ def select_topk(logits: np.ndarray, k: int) -> np.ndarray:
     return ids
 
 
-def route(logits: np.ndarray, k: int, forced_ids=None):
-    """Softmax over all experts, top-k, renormalise over the selected k.
+def sigmoid(l: np.ndarray) -> np.ndarray:
+    """1 / (1 + exp(-l)) in float64."""
+    return 1.0 / (1.0 + np.exp(-np.asarray(l, dtype=np.float64)))
 
+
+def route(logits: np.ndarray, k: int, forced_ids=None, score: str = "softmax", bias=None):
+    """Scores, top-k and renormalisation over the selected k.
+
+    score "softmax": ``logits`` already hold the bias; p = softmax over all
+    experts, the top-k logits are selected, weights p_sel / sum p_sel.
+    score "sigmoid" (bias-corrected selection): ``logits`` are the raw router
+    products x . Wr^T; s = sigmoid(logits), the experts with the k largest
+    s_e + bias_e are selected (bias 0 when None), weights s_sel / sum s_sel.
     Returns (ids int32 [T, k], weights float64 [T, k] holding float32 values).
     ``forced_ids`` replaces the selection (weights still come from ``logits``).
     """
-    p = softmax(logits)
-    ids = select_topk(logits, k) if forced_ids is None else np.asarray(forced_ids, np.int32)
+    if score == "softmax":
+        p = softmax(logits)
+        key = logits
+    elif score == "sigmoid":
+        p = sigmoid(logits)
+        key = p + (0.0 if bias is None else np.asarray(bias, dtype=np.float64)[None, :])
+    else:
+        raise ValueError(score)
+    ids = select_topk(key, k) if forced_ids is None else np.asarray(forced_ids, np.int32)
     sel = np.take_along_axis(p, ids.astype(np.int64), axis=-1)
     w = sel / sel.sum(axis=-1, keepdims=True)
     return ids, F.round_to_f32(w)
+
+
+def selection_keys(logits: np.ndarray, score: str = "softmax", bias=None) -> np.ndarray:
+    """The values top-k selection ranks: the logits (softmax scoring) or
+    sigmoid(logits) + bias (bias-corrected sigmoid scoring), float64."""
+    if score == "softmax":
+        return np.asarray(logits, dtype=np.float64)
+    return sigmoid(logits) + (0.0 if bias is None else np.asarray(bias, dtype=np.float64)[None, :])
 
 
 # ------------------------------------------------------------- permutation
@@ -225,8 +254,13 @@ def layer_forward(layer: dict, top_k: int, fmt: str, tokens=None, forced_ids=Non
     n, H = x.shape
     E = layer["w_router"].shape[0]
 
-    logits = router_logits(x, layer["w_router"], layer.get("bias"))
-    ids, w = route(logits, top_k, forced_ids)
+    score = layer.get("score", "softmax")
+    if score == "softmax":  # the bias is part of the logit
+        logits = router_logits(x, layer["w_router"], layer.get("bias"))
+        ids, w = route(logits, top_k, forced_ids)
+    else:  # the bias only corrects the selection
+        logits = router_logits(x, layer["w_router"])
+        ids, w = route(logits, top_k, forced_ids, score, layer.get("bias"))
 
     xq, xs = quantize_activations(x)
     xq_deq = F.dequantize_mxfp4(xq, xs)

@@ -779,6 +779,40 @@ def test_shared_expert_mxfp8(T, H, I):
     assert normwise(got, ref["ys"]) <= CONTRACTION_TOL
 
 
+def test_mxfp8_to_bf16_dequant_bitexact():
+    """The MXFP8 -> BF16 copy against the oracle's exact dequantisation
+    rounded once to BF16: every E4M3 code under scales across the E8M0 range
+    (the BF16 subnormal band, overflow to inf and the NaN byte included), and
+    a random tensor.  Where the value lies in BF16's normal range the copy is
+    lossless: the BF16 result equals the exact product."""
+    codes = np.tile(np.arange(256, dtype=np.uint8), 32).reshape(-1, 256)       # 32 rows, every code 8 x per row
+    sexp = np.array([0, 1, 5, 9, 100, 118, 127, 135, 200, 247, 248, 253, 254, 255], dtype=np.uint8)
+    rng = np.random.default_rng(41)
+    scales = rng.choice(sexp, (32, 8)).astype(np.uint8)
+    scales[0] = sexp[:8]
+    scales[1] = sexp[6:]
+    rc = rng.integers(0, 256, (300, 1024), dtype=np.uint8)
+    rs = rng.integers(100, 150, (300, 32), dtype=np.uint8)
+    for c, sc in ((codes, scales), (rc, rs)):
+        rows, K = c.shape
+        out = torch.empty((rows, K), dtype=torch.int16, device="cuda")
+        M.moe_dequant_mxfp8_to_bf16(rows, K, torch.from_numpy(c).cuda(), torch.from_numpy(sc).cuda(), out)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy().view(np.uint16)
+        exact = F.dequantize_mxfp8(c, sc)
+        ref = F.round_to_bf16(exact)
+        nan = np.isnan(exact)
+        gv = F.bf16_bits_to_float(got)
+        assert np.array_equal(np.isnan(gv), nan)
+        want = F.bf16_value_to_bits(np.where(nan, 0.0, ref))
+        zero = exact == 0  # E4M3 -0 (0x80) times a scale is -0, kept as the BF16 sign bit
+        want[zero] = np.where(np.signbit(exact[zero]), 0x8000, 0)
+        assert np.array_equal(got[~nan], want[~nan])
+        normal = ~nan & (np.abs(exact) >= 2.0 ** -126) & (np.abs(exact) < 2.0 ** 128)
+        assert np.array_equal(gv[normal], exact[normal])  # lossless in BF16's normal range
+        assert normal.sum() > 0.5 * exact.size
+
+
 def test_zero_tokens_is_a_no_op():
     wl, lay, dev, cache = _workload("tiny")
     x = torch.empty((0, wl.H), dtype=torch.int16, device="cuda")

@@ -55,6 +55,56 @@ def test_topk_is_brute_force_best_subset(E, k):
         assert np.all(np.diff(logits[t, ids[t]]) <= 0)  # descending
 
 
+@pytest.mark.parametrize("E,k", [(8, 2), (8, 4), (16, 3)])
+def test_sigmoid_topk_is_brute_force_best_subset(E, k):
+    """Bias-corrected sigmoid scoring: the selected set maximises the sum of
+    sigmoid(l) + b over all C(E, k) subsets (the bias changes the choice), in
+    descending order of that key, and the weights are the selected sigmoid
+    values (without the bias) over their sum."""
+    rng = np.random.default_rng(E * 10 + k)
+    for _ in range(20):
+        l = rng.normal(0, 2, (1, E))
+        b = rng.normal(0, 0.3, E)
+        ids, w = M.route(l, k, score="sigmoid", bias=b)
+        sig = [1 / (1 + math.exp(-v)) for v in l[0]]
+        key = [sig[e] + b[e] for e in range(E)]
+        best = max(itertools.combinations(range(E), k), key=lambda c: sum(key[e] for e in c))
+        assert set(ids[0].tolist()) == set(best)
+        assert all(key[ids[0][j]] >= key[ids[0][j + 1]] for j in range(k - 1))
+        tot = sum(sig[e] for e in best)
+        for j, e in enumerate(ids[0]):
+            assert w[0, j] == float(np.float32(sig[e] / tot))
+
+
+def test_sigmoid_scoring_closed_form():
+    """Worked by hand on the structured layer (logits (1, 3, 2, 0), top-2).
+    Softmax picks experts 1, 2.  With sigmoid scoring and bias (0.6, 0, 0,
+    0.5) the keys are sigmoid(l) + b = (1.3311, 0.9526, 0.8808, 1.0): experts
+    0 and 3 are selected (the bias overrides the larger logits), weighted
+    sigmoid(1) / (sigmoid(1) + sigmoid(0)) = 0.5938 and 0.5 / 1.2311 = 0.4062,
+    not by their biased keys.  y_e = 1.5 * 2^-e (as in the softmax closed
+    form), so out = BF16(1.4609375 + 1.5 w0 + 0.1875 w3) = BF16(2.42786)
+    = 2.421875 (155 * 2^-6; the midpoint above it is 2.4296875)."""
+    lay = _structured_layer([1.0, 3.0, 2.0, 0.0])
+    lay["bias"] = np.array([0.6, 0.0, 0.0, 0.5], np.float32)
+    lay["score"] = "sigmoid"
+    r = M.layer_forward(lay, 2, "mxfp4", keep=True)
+    assert r["logits"].tolist() == [[1.0, 3.0, 2.0, 0.0]]  # raw: the bias stays out of the logits
+    assert r["ids"].tolist() == [[0, 3]]
+    s1 = 1 / (1 + math.exp(-1))
+    w0, w3 = float(np.float32(s1 / (s1 + 0.5))), float(np.float32(0.5 / (s1 + 0.5)))
+    assert r["weights"].tolist() == [[w0, w3]]
+    assert abs(w0 - 0.5938) < 1e-4 and abs(w3 - 0.4062) < 1e-4
+    assert np.all(r["y"][0, 0] == 1.5) and np.all(r["y"][0, 1] == 0.1875)
+    acc = 1.4609375 + 1.5 * w0 + 0.1875 * w3
+    assert abs(acc - 2.42786) < 1e-5
+    assert np.all(r["out"] == 2.421875)
+    # the same layer under softmax scoring adds the bias to the logits instead
+    lay["score"] = "softmax"
+    r2 = M.layer_forward(lay, 2, "mxfp4")
+    assert r2["ids"].tolist() == [[1, 2]]
+
+
 def test_topk_ties_go_to_lower_index():
     logits = np.array([[2.0, 2.0, 1.0, 2.0], [0.0, 0.0, 0.0, 0.0]])
     assert M.select_topk(logits, 2).tolist() == [[0, 1], [0, 1]]
