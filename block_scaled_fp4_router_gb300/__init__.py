@@ -44,7 +44,10 @@ class MoeError(RuntimeError):
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "top_k", "renormalize", "act_quant",
-                                              "shared_in_table")]
+                                              "shared_in_table", "score_func")]
+
+
+SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 
 
 class SharedMXFP8(ctypes.Structure):
@@ -151,8 +154,9 @@ def _check(st: int, where: str):
         raise MoeError(st, where)
 
 
-def desc(T, H, I, E, top_k, shared_in_table=False) -> LayerDesc:
-    return LayerDesc(T, H, I, E, top_k, 1, 1, 1 if shared_in_table else 0)
+def desc(T, H, I, E, top_k, shared_in_table=False, score="softmax") -> LayerDesc:
+    return LayerDesc(T, H, I, E, top_k, 1, 1, 1 if shared_in_table else 0,
+                     {"softmax": SCORE_SOFTMAX, "sigmoid": SCORE_SIGMOID}[score])
 
 
 def experts(fmt, w13, w13_scale, w2, w2_scale, tensor_scale=None, w13_scale_mma=None, w2_scale_mma=None) -> Experts:

@@ -8,6 +8,7 @@
 #include "moefp4.h"
 #include "kernels.h"
 #include "layout.h"
+#include "routing.cuh"
 
 using namespace moefp4;
 
@@ -30,7 +31,17 @@ moe_status_t check_desc(const moe_layer_desc_t* d) {
   if (d->renormalize != 1 || d->act_quant != 1) return MOE_ERR_UNSUPPORTED;
   if (d->shared_in_table != 0 && d->shared_in_table != 1) return MOE_ERR_INVALID_ARG;
   if (d->shared_in_table && (d->top_k + 1 > MAX_TOPK || d->E + 1 > MAX_E)) return MOE_ERR_UNSUPPORTED;
+  if (d->score_func != SCORE_SOFTMAX && d->score_func != SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
+}
+
+// The router bias goes into the logits (softmax scoring) or only into the
+// top-k choice (sigmoid scoring).
+inline const float* logit_bias(const moe_layer_desc_t* d, const float* bias) {
+  return d->score_func == SCORE_SOFTMAX ? bias : nullptr;
+}
+inline const float* select_bias(const moe_layer_desc_t* d, const float* bias) {
+  return d->score_func == SCORE_SIGMOID ? bias : nullptr;
 }
 
 // The shape of the expert table and of the per-token assignments: with the
@@ -102,9 +113,17 @@ Shape shape_of(const moe_layer_desc_t* d) { return Shape{d->T, d->H, d->I, d->E,
 // A5 - A8: the routed experts on tensor cores when the batch is large enough
 // and the weights are MXFP4 (kind::mxf4 takes E8M0 scales), otherwise on CUDA
 // cores; the shared expert likewise from TC_MIN_T_SHARED tokens.
+//
+// With fuse_w (the flat routing weights [T * k]) and the routed experts on
+// 128-token tensor-core tiles, the combine runs inside the routed down GEMM:
+// the shared expert first writes ys into acc (FP32 [T][H]; zero-filled
+// without a shared expert), the down GEMM adds every weighted expert output
+// into it, and *fused reports that acc then holds the layer output in FP32
+// (y_assign is not written).
 moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, const SharedDev& shd,
                             const uint16_t* x, const uint8_t* xq, const uint8_t* xs, const int* offsets,
-                            const int* perm, float* y_assign, float* y_shared, void* ws, cudaStream_t s) {
+                            const int* perm, float* y_assign, float* y_shared, void* ws, cudaStream_t s,
+                            const float* fuse_w = nullptr, float* acc = nullptr, bool* fused = nullptr) {
   const WsLayout L = ws_layout(d->T, d->H, d->I, d->E, d->top_k);
   const Shape sh = shape_of(d);
   const uint64_t limit = g_wait_limit_ns.load();
@@ -113,24 +132,34 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
                   aligned(ex.w13s, 4) &&
                   aligned(ex.w2s, 4);
   const bool wa = tc && tc_weights_as_a(d->T * d->top_k, d->E, g_routed_gemm.load());
+  const bool fuse = fuse_w && acc && tc && !wa;
+  if (fused) *fused = fuse;
   // record which layout h is left in (read by moe_debug_requantized_h)
   MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.counters) + C_HPATH, tc ? (wa ? 2 : 1) : 0, sizeof(int), s));
+  auto shared_expert = [&](float* ys) -> moe_status_t {
+    uint16_t* h = at<uint16_t>(ws, L.h_shared);
+    if (shared_tc_path(d->T, d->H, d->I))
+      return cuda_status(launch_shared_tc(sh, shd, x, h, ys, at<float>(ws, L.sh_part), status, limit, s));
+    return cuda_status(launch_shared_simt(sh, shd, x, h, ys, s));
+  };
+  if (fuse) {  // the accumulator starts as ys (or zero)
+    if (shd.w13)
+      MOE_TRY(shared_expert(acc));
+    else
+      MOE_CUDA(cudaMemsetAsync(acc, 0, sizeof(float) * (size_t)d->T * d->H, s));
+  }
   if (tc) {
     TcWorkspace w{at<int>(ws, L.tc_poff), at<uint8_t>(ws, L.tc_mtiles), at<int>(ws, L.tc_num_mt),
                   at<uint8_t>(ws, L.tc_xq), at<uint8_t>(ws, L.tc_xs), at<uint8_t>(ws, L.tc_hq),
                   at<uint8_t>(ws, L.tc_hs), at<uint8_t>(ws, L.tc_w13s), at<uint8_t>(ws, L.tc_w2s)};
-    MOE_CUDA(launch_expert_ffn_tc(sh, ex, w, xq, xs, offsets, perm, y_assign, status, limit, wa, s));
+    const CombineArgs comb{fuse_w, acc};
+    MOE_CUDA(launch_expert_ffn_tc(sh, ex, w, xq, xs, offsets, perm, y_assign, status, limit, wa, s,
+                                  fuse ? &comb : nullptr));
   } else {
     MOE_CUDA(launch_routed_simt(sh, ex, xq, xs, offsets, perm, at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs),
                                 y_assign, s));
   }
-  if (shd.w13) {
-    uint16_t* h = at<uint16_t>(ws, L.h_shared);
-    if (shared_tc_path(d->T, d->H, d->I))
-      MOE_CUDA(launch_shared_tc(sh, shd, x, h, y_shared, at<float>(ws, L.sh_part), status, limit, s));
-    else
-      MOE_CUDA(launch_shared_simt(sh, shd, x, h, y_shared, s));
-  }
+  if (shd.w13 && !fuse) MOE_TRY(shared_expert(y_shared));
   return MOE_OK;
 }
 
@@ -149,17 +178,21 @@ moe_status_t run_forward(const moe_layer_desc_t* desc, const ExpertsDev& ex, con
   float* w_r = topk_w ? topk_w : at<float>(ws, fold ? L.wts_r : L.wts);
   int* ids = fold ? at<int>(ws, L.ids) : ids_r;  // [T][table k]
   float* w = fold ? at<float>(ws, L.wts) : w_r;
-  MOE_CUDA(launch_router_logits(xb, w_router, bias, at<float>(ws, L.logits), desc->T, desc->H, desc->E,
-                                at<float>(ws, L.rt_part), s));
-  MOE_CUDA(launch_topk(at<float>(ws, L.logits), desc->T, desc->E, desc->top_k, ids_r, w_r, s,
-                       fold ? ids : nullptr, fold ? w : nullptr));
+  MOE_CUDA(launch_router_logits(xb, w_router, logit_bias(desc, bias), at<float>(ws, L.logits), desc->T, desc->H,
+                                desc->E, at<float>(ws, L.rt_part), s));
+  MOE_CUDA(launch_topk(at<float>(ws, L.logits), desc->T, desc->E, desc->top_k, desc->score_func,
+                       select_bias(desc, bias), ids_r, w_r, s, fold ? ids : nullptr, fold ? w : nullptr));
   MOE_CUDA(launch_quant_mxfp4(xb, sh.T, sh.H, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), s));
   MOE_CUDA(launch_permute(ids, sh.T, sh.k, sh.E, at<int>(ws, L.counts), at<int>(ws, L.offsets),
                           at<int>(ws, L.perm), at<int>(ws, L.inv_perm), at<int>(ws, L.rank),
                           at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base), s));
   float* ysh = shd.w13 ? at<float>(ws, L.y_shared) : nullptr;
+  bool fused = false;
   MOE_TRY(run_expert_ffn(&dt, ex, shd, xb, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), at<int>(ws, L.offsets),
-                         at<int>(ws, L.perm), at<float>(ws, L.y_assign), ysh, ws, s));
+                         at<int>(ws, L.perm), at<float>(ws, L.y_assign), ysh, ws, s, w, at<float>(ws, L.y_shared),
+                         &fused));
+  if (fused)  // the combine ran in the down GEMM: the FP32 output is rounded to BF16
+    return cuda_status(launch_acc_to_bf16(at<float>(ws, L.y_shared), (size_t)sh.T * sh.H, out, s));
   return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh, out, s));
 }
 
@@ -347,9 +380,10 @@ moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
   float* lg = logits ? logits : at<float>(ws, L.logits);
-  MOE_CUDA(launch_router_logits(static_cast<const uint16_t*>(x), w_router, bias, lg, desc->T, desc->H,
-                                desc->E, at<float>(ws, L.rt_part), s));
-  return cuda_status(launch_topk(lg, desc->T, desc->E, desc->top_k, topk_ids, topk_w, s));
+  MOE_CUDA(launch_router_logits(static_cast<const uint16_t*>(x), w_router, logit_bias(desc, bias), lg, desc->T,
+                                desc->H, desc->E, at<float>(ws, L.rt_part), s));
+  return cuda_status(launch_topk(lg, desc->T, desc->E, desc->top_k, desc->score_func, select_bias(desc, bias),
+                                 topk_ids, topk_w, s));
 }
 
 moe_status_t moe_permute(const moe_layer_desc_t* desc, const int32_t* topk_ids, int32_t* counts,
@@ -463,14 +497,14 @@ moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t*
   // folded shared expert without them takes the batched path.
   if (fused_decode_tc_supported(sh, ex))
     return cuda_status(launch_fused_decode_tc(sh, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws,
-                                              g_wait_limit_ns.load(), s, desc->shared_in_table));
+                                              g_wait_limit_ns.load(), s, desc->shared_in_table, desc->score_func));
   // The CUDA-core single launch streams weight rows in 64-element pairs (32-byte
   // code loads, 2- or 4-byte scale loads): shapes with H or I not a multiple of
   // 64 take the per-step kernels, which work in 32-element blocks.
   if (desc->shared_in_table || !fused_decode_supported(sh))
     return run_forward(desc, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws, s);
   return cuda_status(launch_fused_decode(sh, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws,
-                                         g_wait_limit_ns.load(), s));
+                                         g_wait_limit_ns.load(), s, desc->score_func));
 }
 
 }  // extern "C"

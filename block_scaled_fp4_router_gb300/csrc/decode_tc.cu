@@ -88,6 +88,7 @@ struct DcArgs {
   int nslot_max;             // min(T k, E): ticket slots
   int shared;
   int nv;                    // NVFP4 experts (UE4M3 scales per 16, FP32 tensor scales)
+  int score;                 // SCORE_SOFTMAX (the bias is part of the logit) or SCORE_SIGMOID
   const uint8_t* w13s_mma;   // prepared routed weight scales
   const uint8_t* w2s_mma;
   const float* tscale;       // NVFP4: [E, 3] (gate, up, down)
@@ -292,7 +293,7 @@ __device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DE
   if (et < T) {
     float s = red_s[0][et];
     for (int ww = 1; ww < EPI_THREADS / 32; ++ww) s += red_s[ww][et];
-    if (a.bias) s += a.bias[e];
+    if (a.bias && a.score == SCORE_SOFTMAX) s += a.bias[e];
     // one 64-bit store carries the value and this launch's number: a reader
     // that sees the number has the value, with no fence or counter between
     st_relaxed_u64(a.logit64 + (size_t)et * a.Er + e, ((unsigned long long)epoch << 32) | __float_as_uint(s));
@@ -458,9 +459,8 @@ __device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t ep
       continue;
     }
     int sel[MAX_TOPK];
-    float vals[MAX_TOPK], wt[MAX_TOPK];
-    warp_topk(v, a.Er, kr, sel, vals);
-    topk_weights(vals, kr, wt);
+    float wt[MAX_TOPK];
+    route_row(v, a.Er, kr, a.score, a.bias, sel, wt);
 #pragma unroll
     for (int j = 0; j < MAX_TOPK; ++j)
       if (j == lane && j < kr) {
@@ -1137,7 +1137,7 @@ bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex) {
 
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
                                    const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
-                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold) {
+                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold, int score) {
   if (sh.T == 0) return cudaSuccess;
   if (!fused_decode_tc_supported(sh, ex)) return cudaErrorInvalidValue;
   const int T = sh.T, H = sh.H, I = sh.I, E = sh.E, k = sh.k, n = T * k;
@@ -1176,6 +1176,7 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.nslot_max = imin(n, E);
   a.shared = shared ? 1 : 0;
   a.nv = ex.nv;
+  a.score = score;
   a.w13s_mma = ex.w13s_mma;
   a.w2s_mma = ex.w2s_mma;
   a.tscale = ex.tscale;

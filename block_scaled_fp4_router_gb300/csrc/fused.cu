@@ -51,6 +51,7 @@ struct FusedArgs {
   uint8_t* hs;
   uint16_t* h_shared;
   uint64_t wait_limit_ns;
+  int score;  // SCORE_SOFTMAX (the bias is part of the logit) or SCORE_SIGMOID
   // unit ranges
   int u_quant, u_sgu, u_rgu, u_down, u_end;
   // dynamic shared memory offsets
@@ -97,9 +98,8 @@ __device__ void build_routing(const FusedArgs& a, Routing& R) {
     float v[8];
     load_logit_row(a.logits + (size_t)warp * E, E, v, true);
     int sel[MAX_TOPK];
-    float vals[MAX_TOPK], w[MAX_TOPK];
-    warp_topk(v, E, k, sel, vals);
-    topk_weights(vals, k, w);
+    float w[MAX_TOPK];
+    route_row(v, E, k, a.score, a.bias, sel, w);
     if (lane < k) {
 #pragma unroll
       for (int j = 0; j < MAX_TOPK; ++j)
@@ -194,7 +194,7 @@ __device__ void unit_router(const FusedArgs& a, int e, float* red_s) {
   if (threadIdx.x < T) {
     float s = 0.0f;
     for (int w = 0; w < FW; ++w) s += red_s[w * MAXT + threadIdx.x];
-    if (a.bias) s += a.bias[e];
+    if (a.bias && a.score == SCORE_SOFTMAX) s += a.bias[e];
     a.logits[(size_t)threadIdx.x * a.sh.E + e] = s;
   }
 }
@@ -506,7 +506,7 @@ const void* fused_kernel(int maxt, bool nv) {
 cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd,
                                 const float* wr, const float* bias, const uint16_t* x, uint16_t* out,
                                 int* ids_out, float* w_out, void* ws, uint64_t wait_limit_ns,
-                                cudaStream_t s) {
+                                cudaStream_t s, int score) {
   if (sh.T == 0) return cudaSuccess;
   if (!fused_decode_supported(sh)) return cudaErrorInvalidValue;
   const WsLayout L = ws_layout(sh.T, sh.H, sh.I, sh.E, sh.k);
@@ -531,6 +531,7 @@ cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const Sha
   a.hs = base + L.hs;
   a.h_shared = reinterpret_cast<uint16_t*>(base + L.h_shared);
   a.wait_limit_ns = wait_limit_ns;
+  a.score = score;
   a.u_quant = sh.E;
   a.u_sgu = a.u_quant + 1;
   a.u_rgu = a.u_sgu + (shared ? sh.I / 8 : 0);

@@ -46,11 +46,12 @@ cudaError_t launch_quant_mxfp8(const uint16_t* x, int rows, int K, uint8_t* code
 // A1
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, float* part, cudaStream_t s);  // part: [router_splits][T][E]
-// A2
+// A2.  score: SCORE_SOFTMAX (logits hold the bias) or SCORE_SIGMOID (raw
+// logits; sel_bias, may be null, corrects the choice only).
 // ids_ext / w_ext (optional): [T][k + 1], the last column the shared expert
 // folded into the table (id E, weight 1).
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s,
-                        int* ids_ext = nullptr, float* w_ext = nullptr);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int score, const float* sel_bias, int* ids,
+                        float* w, cudaStream_t s, int* ids_ext = nullptr, float* w_ext = nullptr);
 // A3
 cudaError_t launch_permute(const int* ids, int T, int k, int E, int* counts, int* offsets, int* perm,
                            int* inv_perm, int* rank, int* chunk_cnt, int* chunk_base, cudaStream_t s);
@@ -74,12 +75,23 @@ struct TcWorkspace {
   uint8_t* w13s_mma;
   uint8_t* w2s_mma;
 };
+// The combine fused into the routed down GEMM (A9 in A7's epilogue): acc FP32
+// [T][H] += topk_w[a] * y of every assignment a (already holding the shared
+// expert's output, or zero).
+struct CombineArgs {
+  const float* topk_w;  // [T * k], flat assignment t * k + j
+  float* acc;
+};
 // A5 - A7 on tensor cores (MXFP4 weights)
 // wa: weights as the MMA's A operand and 64-row token windows as B (small
-// per-expert batches); otherwise 128-token tiles as A.
+// per-expert batches); otherwise 128-token tiles as A, where comb (optional)
+// replaces the y_assign store by the fused combine.
 cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const TcWorkspace& w, const uint8_t* xq,
                                  const uint8_t* xs, const int* offsets, const int* perm, float* y_assign,
-                                 int* status, uint64_t limit_ns, bool wa, cudaStream_t s);
+                                 int* status, uint64_t limit_ns, bool wa, cudaStream_t s,
+                                 const CombineArgs* comb = nullptr);
+// out BF16 [n] = acc FP32 [n] (n a multiple of 4).
+cudaError_t launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s);
 // Whether n assignments over E experts take the weights-as-A GEMMs under an
 // orientation mode (TC_GEMM_*).
 bool tc_weights_as_a(int n, int E, int mode);
@@ -121,7 +133,7 @@ inline bool fused_decode_supported(const Shape& sh) {
 cudaError_t launch_fused_decode(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd,
                                 const float* wr, const float* bias, const uint16_t* x, uint16_t* out,
                                 int* ids_out, float* w_out, void* ws, uint64_t wait_limit_ns,
-                                cudaStream_t s);
+                                cudaStream_t s, int score = 0);
 // A10 on tensor cores (MXFP4 weights with prepared scales, H and I multiples of 256).
 bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex);
 // sh: the table shape (E experts, k assignments per token).  fold = 1: the
@@ -129,7 +141,7 @@ bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex);
 // k - 1 experts; ids_out / w_out are [T][k - fold].
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
                                    const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
-                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold = 0);
+                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold = 0, int score = 0);
 // bytes (a multiple of 16) from src to dst, both 16-byte aligned, device or
 // GPU-addressable pinned host memory, by SM loads and stores.
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t s);

@@ -353,17 +353,17 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float
 
 // ids / wts: [T][k].  With ids_ext set, also [T][k + 1] copies whose last
 // column is the shared expert folded into the table (expert E, weight 1).
-__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
-                                              int* __restrict__ ids, float* __restrict__ wts,
-                                              int* __restrict__ ids_ext, float* __restrict__ wts_ext) {
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k, int score,
+                                              const float* __restrict__ sel_bias, int* __restrict__ ids,
+                                              float* __restrict__ wts, int* __restrict__ ids_ext,
+                                              float* __restrict__ wts_ext) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   int sel[MAX_TOPK];
-  float vals[MAX_TOPK], w[MAX_TOPK];
+  float w[MAX_TOPK];
   float v[8];
   load_logit_row(logits + (size_t)t * E, E, v, false);
-  warp_topk(v, E, k, sel, vals);
-  topk_weights(vals, k, w);
+  route_row(v, E, k, score, sel_bias, sel, w);
   const int lane = threadIdx.x & 31;
   if (lane < k) {
     int id = 0;
@@ -384,10 +384,10 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
   }
 }
 
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int* ids, float* w, cudaStream_t s,
-                        int* ids_ext, float* w_ext) {
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int score, const float* sel_bias, int* ids,
+                        float* w, cudaStream_t s, int* ids_ext, float* w_ext) {
   if (T == 0) return cudaSuccess;
-  count_launch(), k_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, ids, w, ids_ext, w_ext);
+  count_launch(), k_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, score, sel_bias, ids, w, ids_ext, w_ext);
   return cudaGetLastError();
 }
 

@@ -56,7 +56,12 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_TMEM_BASE = 256;       // scale slots after the 256 accumulator columns
 
 enum Kind { KIND_FP4 = 0, KIND_BF16 = 1, KIND_FP8 = 2 };
-enum Epi { EPI_SWIGLU_MX = 0, EPI_STORE_F32 = 1, EPI_SWIGLU_BF16 = 2, EPI_SWIGLU_MX8 = 3 };
+enum Epi { EPI_SWIGLU_MX = 0, EPI_STORE_F32 = 1, EPI_SWIGLU_BF16 = 2, EPI_SWIGLU_MX8 = 3, EPI_COMBINE_RED = 4 };
+
+// out[0..1] += {a, b}: one vector FP32 reduction at the L2 (8-byte aligned).
+__device__ __forceinline__ void red_add_f32x2(float* out, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(out), "f"(a), "f"(b) : "memory");
+}
 
 // Shared-memory stride of one stage (FP8 stages keep the FP4 layout and fill
 // half of each scale slot: one K group of 128 per stage).
@@ -211,20 +216,36 @@ struct GemmArgs {
   int ldo;
   int ksplit;              // dense: K parts per output tile (0 or 1: none)
   size_t part_stride;
+  // EPI_COMBINE_RED: out[token][col] += topk_w[a] * y for sorted row p with
+  // assignment a = perm[p], token a / k_top (out is FP32 [T][ldo])
+  const int* perm;
+  const float* topk_w;
+  int k_top;
+  int n_major;             // tiles ordered B tile first (every A tile of one output column slice in turn)
   int* status;
   uint64_t limit_ns;
 };
 
 __device__ __forceinline__ int ksplit_of(const GemmArgs& g) { return g.ksplit > 1 ? g.ksplit : 1; }
 
+// A tile / B tile of work item t (num_mt A tiles).
+__device__ __forceinline__ int mti_of(const GemmArgs& g, int t, int num_mt) {
+  t /= ksplit_of(g);
+  return g.n_major ? t % num_mt : t / g.n_tiles;
+}
+__device__ __forceinline__ int nt_of(const GemmArgs& g, int t, int num_mt) {
+  t /= ksplit_of(g);
+  return g.n_major ? t / num_mt : t % g.n_tiles;
+}
+
 // Tile t: A tile mti, B tile nt and K part kp (split-K dense GEMMs).
 // A grouped caller may pass the tile's MTile, loaded ahead (pre).
-__device__ __forceinline__ void tile_coords(const GemmArgs& g, bool grouped, int t, int& a_row, int& e, int& rows,
-                                            int& srow0, int& nt, int& mti, int& kp, const MTile* pre = nullptr) {
+__device__ __forceinline__ void tile_coords(const GemmArgs& g, bool grouped, int t, int num_mt, int& a_row, int& e,
+                                            int& rows, int& srow0, int& nt, int& mti, int& kp,
+                                            const MTile* pre = nullptr) {
   kp = t % ksplit_of(g);
-  t /= ksplit_of(g);
-  mti = t / g.n_tiles;
-  nt = t % g.n_tiles;
+  mti = mti_of(g, t, num_mt);
+  nt = nt_of(g, t, num_mt);
   if (grouped) {
     const MTile m = pre ? *pre : g.mt[mti];
     a_row = m.prow0;
@@ -249,6 +270,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __shared__ int abort_flag;
   constexpr uint32_t SB = stage_bytes(KIND);
   constexpr bool SWIGLU = EPI == EPI_SWIGLU_MX || EPI == EPI_SWIGLU_BF16 || EPI == EPI_SWIGLU_MX8;
+  static_assert(EPI != EPI_COMBINE_RED || GROUPED, "the combine epilogue needs the routed tile list");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -283,12 +305,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ---------------- producer
     uint32_t stage = 0, phase = 0;
     // grouped: each tile's MTile is loaded a tile ahead, off the stream's critical path
-    auto mt_of = [&](int t) { return GROUPED && t < total ? g.mt[(t / ksplit_of(g)) / g.n_tiles] : MTile{}; };
+    auto mt_of = [&](int t) { return GROUPED && t < total ? g.mt[mti_of(g, t, num_mt)] : MTile{}; };
     MTile mn = mt_of(blockIdx.x);
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
       int a_row, e, rows, srow0, nt, mti, kp;
       const MTile m = mn;
-      tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti, kp, &m);
+      tile_coords(g, GROUPED, t, num_mt, a_row, e, rows, srow0, nt, mti, kp, &m);
       mn = mt_of(t + gridDim.x);
       const int b_base = e * g.b_rows_per_expert;
       const int b0 = SWIGLU ? b_base + nt * (BN / 2) : b_base + nt * BN;
@@ -391,7 +413,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
       int a_row, e, rows, srow0, nt, mti, kp;
-      tile_coords(g, GROUPED, t, a_row, e, rows, srow0, nt, mti, kp);
+      tile_coords(g, GROUPED, t, num_mt, a_row, e, rows, srow0, nt, mti, kp);
       if (!tc::mbar_wait(&acc_full, acc_phase, g.limit_ns, &abort_flag)) { fail(); break; }
       tc::fence_after_sync();
       float va[32], vb[32];
@@ -462,6 +484,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             o.z = f32_to_bf16_rn(silu(va[i + 4]) * vb[i + 4]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 5]) * vb[i + 5]) << 16);
             o.w = f32_to_bf16_rn(silu(va[i + 6]) * vb[i + 6]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 7]) * vb[i + 7]) << 16);
             *reinterpret_cast<uint4*>(dst + i) = o;
+          }
+        }
+      } else if (EPI == EPI_COMBINE_RED) {
+        // A9 fused: each real row's 64 columns, times its routing weight, are
+        // added into its token's FP32 output row by vector reductions (four
+        // threads share a row: every warp reduction covers whole sectors)
+        const int r0 = q * 32 + (lane >> 2);
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          const int r = r0 + 8 * hh;  // hh: lanes +0, +8 (first load), +16, +24 (second)
+          if (r < rows) {
+            const int a = __ldg(g.perm + srow0 + r);
+            const float wgt = __ldg(g.topk_w + a);
+            float* dst = g.out + (size_t)(a / g.k_top) * g.ldo + nt * BN + cq * 64 + 2 * (lane & 3);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float* v = hh < 2 ? va : vb;
+              const int o = 4 * j + 2 * (hh & 1);
+              red_add_f32x2(dst + 8 * j, wgt * v[o], wgt * v[o + 1]);
+            }
           }
         }
       } else {
@@ -829,10 +871,11 @@ bool tc_weights_as_a(int n, int E, int mode) {
 
 cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const TcWorkspace& w, const uint8_t* xq,
                                  const uint8_t* xs, const int* offsets, const int* perm, float* y_assign,
-                                 int* status, uint64_t limit_ns, bool wa, cudaStream_t s) {
+                                 int* status, uint64_t limit_ns, bool wa, cudaStream_t s, const CombineArgs* comb) {
   const int H = sh.H, I = sh.I, E = sh.E;
   const int n = sh.T * sh.k;
   if (n == 0) return cudaSuccess;
+  if (comb && wa) return cudaErrorInvalidValue;  // the fused combine exists for 128-token tiles as A
   const int win = wa ? WA_WIN : BM;
   const int rmax = tc_padded_rows_win(n, E, win);
   cudaError_t err;
@@ -928,10 +971,45 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   g2.ldo = H;
   g2.status = status;
   g2.limit_ns = limit_ns;
-  if ((err = launch_gemm<KIND_FP4, EPI_STORE_F32, true>(ma, mb, g2, max_mt * g2.n_tiles, s)) != cudaSuccess)
-    return err;
+  if (comb) {
+    // the combine in the epilogue: tiles of one 256-column slice of the
+    // output in turn, so that slice of the FP32 accumulator (T x 1 KB) stays
+    // in L2 while every expert adds into it
+    g2.out = comb->acc;
+    g2.perm = perm;
+    g2.topk_w = comb->topk_w;
+    g2.k_top = sh.k;
+    g2.n_major = 1;
+    err = launch_gemm<KIND_FP4, EPI_COMBINE_RED, true>(ma, mb, g2, max_mt * g2.n_tiles, s);
+  } else {
+    err = launch_gemm<KIND_FP4, EPI_STORE_F32, true>(ma, mb, g2, max_mt * g2.n_tiles, s);
+  }
+  if (err != cudaSuccess) return err;
   record_mark(MARK_ROUTED_GEMM_END, s);
   return cudaSuccess;
+}
+
+namespace {
+
+// out[i] = BF16(acc[i]), four elements per thread.
+__global__ void __launch_bounds__(256) k_acc_to_bf16(const float* __restrict__ acc, size_t n4,
+                                                     uint16_t* __restrict__ out) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = __ldcs(reinterpret_cast<const float4*>(acc) + i);
+  uint2 o;
+  o.x = (uint32_t)f32_to_bf16_rn(v.x) | ((uint32_t)f32_to_bf16_rn(v.y) << 16);
+  o.y = (uint32_t)f32_to_bf16_rn(v.z) | ((uint32_t)f32_to_bf16_rn(v.w) << 16);
+  reinterpret_cast<uint2*>(out)[i] = o;
+}
+
+}  // namespace
+
+cudaError_t launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s) {
+  const size_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  count_launch(), k_acc_to_bf16<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(acc, n4, out);
+  return cudaGetLastError();
 }
 
 namespace {

@@ -35,6 +35,7 @@ class DeviceLayer:
         self.H, self.I, self.E, self.k, self.fmt = H, I, E, top_k, fmt
         # the shared expert folded into the FP4 table as expert E (E + 1 experts)
         self.fold = bool(arrays.get("shared_in_table", False))
+        self.score = arrays.get("score", "softmax")  # the router's score function
         self.device = torch.device(device)
         d = self.device
         self.w_router = _to_dev(arrays["w_router"], d)
@@ -80,7 +81,7 @@ class DeviceLayer:
     def desc(self, T: int):
         if T > self.T_max:
             raise ValueError("T=%d exceeds the workspace's T_max=%d" % (T, self.T_max))
-        return desc(T, self.H, self.I, self.E, self.k, self.fold)
+        return desc(T, self.H, self.I, self.E, self.k, self.fold, self.score)
 
     def outputs(self, T: int):
         d = self.device

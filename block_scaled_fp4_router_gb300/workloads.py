@@ -16,6 +16,8 @@ Instinct GPUs", section "MiniMax-M3.1 at a glance"):
 * ``decode16z``  T=16,   same shape, NVFP4, Zipf(1.2)-skewed router bias, seed 2
 * ``batch128``   T=128,  same shape, MXFP4, router logits ~ N(0,1), seed 3
 * ``prefill8k``  T=8192, same shape, MXFP4, Zipf(1.1)-skewed expert load, seed 4
+* ``*_sig``      tiny, 16-token NVFP4 decode and 128-token batch with sigmoid
+                 scoring and a Zipf(0.05) correction bias (seeds 14, 15, 16)
 
 Every workload carries an always-on shared expert with BF16 weights, except
 the ``*_sfp4`` variants of tiny, decode1 and batch128, whose shared expert is
@@ -41,6 +43,9 @@ Array conventions (all numpy, C-contiguous, little-endian):
                                           scale: gate, up, down
 * ``ws13``         uint16 [2I, H]         shared expert gate/up, BF16 bits
 * ``ws2``          uint16 [H, I]          shared expert down, BF16 bits
+* ``score``        str                    router scores: "softmax" (the bias is
+                                          part of the logit) or "sigmoid" (the
+                                          bias only corrects the top-k choice)
 * ``shared_in_table`` bool               the expert arrays hold E + 1 experts,
                                           the last one the shared expert (then
                                           ``ws13`` / ``ws2`` are None)
@@ -71,6 +76,7 @@ class Workload:
     shared: bool = True
     shared_std: float = 0.02
     shared_fp4: bool = False  # the shared expert as expert E of the FP4 table
+    score: str = "softmax"    # router scores: softmax, or sigmoid with a bias-corrected choice
     # E8M0 block-scale exponents drawn uniformly from [lo, hi]
     mx_exp_lo: int = -8
     mx_exp_hi: int = -4
@@ -95,6 +101,9 @@ WORKLOADS = {
         Workload("tiny_sfp4", 16, 512, 256, 16, 4, MXFP4, 10, 0.02, shared=False, shared_fp4=True),
         Workload("decode1_sfp4", 1, 4096, 1536, 128, 4, MXFP4, 11, 0.02, shared=False, shared_fp4=True),
         Workload("batch128_sfp4", 128, 4096, 1536, 128, 4, MXFP4, 13, 1.0 / 64.0, shared=False, shared_fp4=True),
+        Workload("tiny_sig", 16, 512, 256, 16, 4, MXFP4, 14, 0.02, zipf=0.05, score="sigmoid"),
+        Workload("decode16_sig", 16, 4096, 1536, 128, 4, NVFP4, 15, 0.02, zipf=0.05, score="sigmoid"),
+        Workload("batch128_sig", 128, 4096, 1536, 128, 4, MXFP4, 16, 1.0 / 64.0, zipf=0.05, score="sigmoid"),
     ]
 }
 
@@ -140,6 +149,7 @@ def generate(w: Workload, layer: int = 0, tokens: Optional[int] = None) -> dict:
         out["bias"] = None
     Et = E + 1 if w.shared_fp4 else E  # experts in the table
     out["shared_in_table"] = w.shared_fp4
+    out["score"] = w.score
     out["w13"] = rw.integers(0, 256, size=(Et, 2 * I, H // 2), dtype=np.uint8)
     out["w2"] = rw.integers(0, 256, size=(Et, H, I // 2), dtype=np.uint8)
     if w.fmt == MXFP4:
@@ -210,6 +220,7 @@ def generate_device(w: Workload, layer: int, device) -> dict:
         out["bias"] = None
     Et = E + 1 if w.shared_fp4 else E
     out["shared_in_table"] = w.shared_fp4
+    out["score"] = w.score
     out["w13"] = torch.randint(0, 256, (Et, 2 * I, H // 2), **u8)
     out["w2"] = torch.randint(0, 256, (Et, H, I // 2), **u8)
     if w.fmt == MXFP4:

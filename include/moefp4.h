@@ -111,12 +111,24 @@ typedef enum { MOE_W_MXFP4 = 1, MOE_W_NVFP4 = 2 } moe_wfmt_t;
  * moe_workspace_size, moe_prepare_weights and moe_convert_nvfp4_to_mxfp4 take
  * it (the last two act on all E + 1 experts); the per-step entry points
  * return MOE_ERR_UNSUPPORTED (call them with the table shape, E + 1 experts
- * and top_k + 1 assignments, instead).  0 = no folded shared expert. */
+ * and top_k + 1 assignments, instead).  0 = no folded shared expert.
+ *
+ * score_func picks the router's score function (the pages only call the
+ * router high precision: AMD article, section "MiniMax-M3.1 at a glance"):
+ *   0 = softmax: the bias, when given, is added to the logits; the top_k
+ *       largest logits are selected, weighted by their softmax probabilities
+ *       renormalised over the selection;
+ *   1 = sigmoid with a bias-corrected choice: scores s = sigmoid(x . Wr^T);
+ *       the top_k largest s + bias are selected (the bias only corrects the
+ *       choice), weighted by s_selected / sum s_selected.
+ * Ties go to the lower expert index in both.  Other values return
+ * MOE_ERR_INVALID_ARG. */
 typedef struct {
   int32_t T, H, I, E, top_k;
   int32_t renormalize;
   int32_t act_quant;
   int32_t shared_in_table;
+  int32_t score_func;
 } moe_layer_desc_t;
 
 /* Routed-expert weights (device pointers, layouts above).  The two *_mma
@@ -192,15 +204,16 @@ MOE_API moe_status_t moe_convert_nvfp4_to_mxfp4(const moe_layer_desc_t* desc, co
  * entry point that waits: it copies 4 bytes device-to-host. */
 MOE_API moe_status_t moe_get_status(void* ws, moe_status_t* st);
 
-/* A1 + A2: router logits, softmax, top-k, renormalisation.
+/* A1 + A2: router logits, scores, top-k, renormalisation (desc->score_func).
  * The router is "high precision" and "stacked" (AMD article, sections
  * "MiniMax-M3.1 at a glance" and "What we Optimized"): FP32 weights, FP32
  * accumulation.
  *   x         BF16 [T, H]
  *   w_router  FP32 [E, H];  bias FP32 [E] or NULL
  *   topk_ids  int32 [T, top_k] out, descending logit, ties to lower index
- *   topk_w    FP32 [T, top_k] out, softmax over the selected logits
- *   logits    FP32 [T, E] out, or NULL
+ *   topk_w    FP32 [T, top_k] out, the renormalised weights
+ *   logits    FP32 [T, E] out, or NULL: x . Wr^T + bias (softmax scoring) or
+ *             the raw x . Wr^T (sigmoid scoring)
  * ws: workspace for desc. */
 MOE_API moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const float* w_router,
                              const float* bias, int32_t* topk_ids, float* topk_w, float* logits,

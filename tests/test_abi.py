@@ -63,11 +63,14 @@ def test_workspace_size_grows_with_tokens(lib):
     (dict(T=-1), M.MOE_ERR_INVALID_ARG),
     (dict(renormalize=0), M.MOE_ERR_UNSUPPORTED),
     (dict(act_quant=0), M.MOE_ERR_UNSUPPORTED),
+    (dict(score_func=2), M.MOE_ERR_INVALID_ARG),
+    (dict(score_func=-1), M.MOE_ERR_INVALID_ARG),
 ])
 def test_invalid_descriptors_rejected(lib, bad, code):
-    d = dict(T=4, H=512, I=256, E=16, top_k=4, renormalize=1, act_quant=1)
+    d = dict(T=4, H=512, I=256, E=16, top_k=4, renormalize=1, act_quant=1, shared_in_table=0, score_func=0)
     d.update(bad)
-    desc = M.LayerDesc(*[d[k] for k in ("T", "H", "I", "E", "top_k", "renormalize", "act_quant")])
+    desc = M.LayerDesc(*[d[k] for k in ("T", "H", "I", "E", "top_k", "renormalize", "act_quant",
+                                        "shared_in_table", "score_func")])
     out = ctypes.c_size_t(0)
     assert lib.moe_workspace_size(ctypes.byref(desc), ctypes.byref(out)) == code
 

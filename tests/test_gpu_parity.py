@@ -248,7 +248,8 @@ def _workload(name, T=None):
 
 def _compare_layer(wl, lay, cache, out, ids, tokens=None, tol=LAYER_TOL, w=None):
     r = O.layer_forward(lay, wl.top_k, wl.fmt, tokens=tokens, cache=cache)
-    amb = ambiguous(r["logits"], wl.top_k)
+    # ambiguity on the values the selection ranks (logits, or sigmoid + bias)
+    amb = ambiguous(O.selection_keys(r["logits"], lay.get("score", "softmax"), lay.get("bias")), wl.top_k)
     tok = r["tokens"]
     g_ids = ids.cpu().numpy()[tok]
     assert np.array_equal(g_ids[~amb], r["ids"][~amb])
@@ -379,7 +380,8 @@ def _use_prepared(dev, prepared):
 
 
 @pytest.mark.parametrize("prepared", [True, False], ids=["tcgen05", "cudacore"])
-@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode16z", "tiny_sfp4", "decode1_sfp4"])
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode16z", "tiny_sfp4", "decode1_sfp4",
+                                  "tiny_sig", "decode16_sig"])
 def test_layer_decode_fused(name, prepared):
     wl, lay, dev, cache = _workload(name)
     _use_prepared(dev, prepared)
@@ -412,7 +414,7 @@ def test_prepared_scales_are_the_tensor_core_layout():
     E, H, I = wl16.E, wl16.H, wl16.I
     assert np.array_equal(dev16.w2_scale_mma.cpu().numpy().reshape(-1), relayout(lay16["w2_scale"], H, 2 * I))
 
-@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode1_sfp4"])
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode16", "decode1_sfp4", "tiny_sig", "decode16_sig"])
 def test_layer_forward_matches_decode(name):
     wl, lay, dev, cache = _workload(name)
     out_f, ids_f, w_f = dev.forward(bf16_tensor(lay["x"]))
@@ -477,6 +479,35 @@ def test_layer_forward_shared_in_table(name, T):
     assert ids.shape == (T, wl.top_k) and int(ids.max()) < wl.E  # the router's top-k only
     tokens = None if T <= 16 else np.sort(np.random.default_rng(15).choice(T, 24, replace=False))
     _compare_layer(wl, lay, cache, out, ids, tokens=tokens)
+
+
+def test_batch128_sigmoid_scoring_every_token():
+    """Sigmoid scores with a bias-corrected top-k choice (the bias moves the
+    choice, not the weights) through the batched path, every token against the
+    oracle (ids, weights, output), and the router entry point on the same
+    tokens: its logits are the raw products, without the bias."""
+    wl, lay, dev, cache = _workload("batch128_sig")
+    out, ids, w = dev.forward(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, cache, out, ids, w=w)
+    # the bias changes the choice for a good share of the tokens
+    x = F.bf16_bits_to_float(lay["x"])
+    raw = O.router_logits(x, lay["w_router"])
+    sel_sig, _ = O.route(raw, wl.top_k, score="sigmoid", bias=lay["bias"])
+    sel_nob, _ = O.route(raw, wl.top_k, score="sigmoid")
+    assert np.mean(np.any(sel_sig != sel_nob, axis=1)) > 0.2
+    d = dev.desc(wl.T)
+    g_ids = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device="cuda")
+    g_w = torch.empty((wl.T, wl.top_k), dtype=torch.float32, device="cuda")
+    g_lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    M.moe_router_topk(d, bf16_tensor(lay["x"]), dev.w_router, dev.bias, g_ids, g_w, g_lg, dev.ws)
+    torch.cuda.synchronize()
+    mag = np.abs(x) @ np.abs(lay["w_router"].astype(np.float64)).T
+    assert np.max(np.abs(g_lg.cpu().numpy() - raw) / (mag + 1e-30)) <= 1e-7
+    keys = O.selection_keys(raw, "sigmoid", lay["bias"])
+    amb = ambiguous(keys, wl.top_k)
+    assert np.array_equal(g_ids.cpu().numpy()[~amb], sel_sig[~amb])
 
 
 def test_prefill8k_forward_every_token():
