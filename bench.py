@@ -47,7 +47,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill FP4 TFLOPS vs peak"
 N_LAYERS = 8
-PER_CONFIG = ["tiny", "decode1", "decode16", "decode16z", "batch128"]
+PER_CONFIG = ["tiny", "decode1", "decode16", "decode16z", "batch128", "prefill8k_s8"]
 # nominal dense GB300 tensor rates (PFLOP/s): FP4 13.5, BF16 2.25
 FP4_PER_BF16 = 13.5 / 2.25
 MIN_REGION_S = 1.0

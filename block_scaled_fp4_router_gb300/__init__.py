@@ -31,7 +31,8 @@ EXPORTED = [
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
     "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8", "moe_shared_expert_mxfp8",
     "moe_noalloc_get_status", "moe_debug_wait_probe_noalloc", "moe_debug_launch_count", "moe_set_timing_events",
-    "moe_dequant_mxfp8_to_bf16",
+    "moe_dequant_mxfp8_to_bf16", "moe_prepare_shared_mxfp8", "moe_layer_forward_shared_mxfp8",
+    "moe_debug_shared_mxfp8_h",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -52,7 +53,7 @@ SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 
 class SharedMXFP8(ctypes.Structure):
     _fields_ = [("w13", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p), ("w2", ctypes.c_void_p),
-                ("w2_scale", ctypes.c_void_p)]
+                ("w2_scale", ctypes.c_void_p), ("w13_scale_mma", ctypes.c_void_p), ("w2_scale_mma", ctypes.c_void_p)]
 
 
 class Experts(ctypes.Structure):
@@ -108,6 +109,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_debug_wait_probe_noalloc": ([U64, P], ctypes.c_int),
         "moe_debug_launch_count": ([ctypes.POINTER(ctypes.c_uint64)], None),
         "moe_dequant_mxfp8_to_bf16": ([I32, I32, P, P, P, P], ctypes.c_int),
+        "moe_prepare_shared_mxfp8": ([P, P, P, P, P], ctypes.c_int),
+        "moe_layer_forward_shared_mxfp8": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
+        "moe_debug_shared_mxfp8_h": ([P, P, S, P, P, P], ctypes.c_int),
         "moe_set_timing_events": ([P, P], None),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
         "moe_prepare_weights": ([P, P, P, P, P], ctypes.c_int),
@@ -238,8 +242,24 @@ def moe_quant_act_mxfp4(rows, K, x, codes, scales, stream=None):
            "moe_quant_act_mxfp4")
 
 
-def shared_mxfp8(w13, w13_scale, w2, w2_scale) -> SharedMXFP8:
-    return SharedMXFP8(_p(w13), _p(w13_scale), _p(w2), _p(w2_scale))
+def shared_mxfp8(w13, w13_scale, w2, w2_scale, w13_scale_mma=None, w2_scale_mma=None) -> SharedMXFP8:
+    return SharedMXFP8(_p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(w13_scale_mma), _p(w2_scale_mma))
+
+
+def moe_prepare_shared_mxfp8(d, sh8, w13_scale_mma, w2_scale_mma, stream=None):
+    _check(load().moe_prepare_shared_mxfp8(ctypes.byref(d), ctypes.byref(sh8), _p(w13_scale_mma), _p(w2_scale_mma),
+                                           _stream(stream)), "moe_prepare_shared_mxfp8")
+
+
+def moe_layer_forward_shared_mxfp8(d, ex, sh8, w_router, bias, x, out, topk_ids, topk_w, ws, stream=None):
+    _check(load().moe_layer_forward_shared_mxfp8(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh8), _p(w_router),
+                                                 _p(bias), _p(x), _p(out), _p(topk_ids), _p(topk_w), _p(ws),
+                                                 _nbytes(ws), _stream(stream)), "moe_layer_forward_shared_mxfp8")
+
+
+def moe_debug_shared_mxfp8_h(d, ws, hq, hs, stream=None):
+    _check(load().moe_debug_shared_mxfp8_h(ctypes.byref(d), _p(ws), _nbytes(ws), _p(hq), _p(hs), _stream(stream)),
+           "moe_debug_shared_mxfp8_h")
 
 
 def moe_shared_expert_mxfp8(d, sh8, x, y_shared, ws, stream=None):

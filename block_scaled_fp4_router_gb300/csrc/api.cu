@@ -93,6 +93,20 @@ moe_status_t check_shared(const moe_shared_bf16_t* sh, SharedDev* out) {
   return MOE_OK;
 }
 
+moe_status_t check_shared8(const moe_layer_desc_t* d, const moe_shared_mxfp8_t* sh, Shared8Dev* out) {
+  if (d->shared_in_table) return MOE_ERR_INVALID_ARG;  // one shared expert, not two
+  if (d->H % 256 || d->I % 256) return MOE_ERR_UNSUPPORTED;
+  if (!sh || !sh->w13 || !sh->w13_scale || !sh->w2 || !sh->w2_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(sh->w13, 16) || !aligned(sh->w2, 16) || !aligned(sh->w13_scale, 4) || !aligned(sh->w2_scale, 4))
+    return MOE_ERR_INVALID_ARG;
+  if ((sh->w13_scale_mma && !aligned(sh->w13_scale_mma, 16)) || (sh->w2_scale_mma && !aligned(sh->w2_scale_mma, 16)))
+    return MOE_ERR_INVALID_ARG;
+  const bool prepared = sh->w13_scale_mma && sh->w2_scale_mma;
+  *out = Shared8Dev{sh->w13, sh->w13_scale, sh->w2, sh->w2_scale, prepared ? sh->w13_scale_mma : nullptr,
+                    prepared ? sh->w2_scale_mma : nullptr};
+  return MOE_OK;
+}
+
 inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 #define MOE_TRY(expr)                   \
@@ -123,7 +137,8 @@ Shape shape_of(const moe_layer_desc_t* d) { return Shape{d->T, d->H, d->I, d->E,
 moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, const SharedDev& shd,
                             const uint16_t* x, const uint8_t* xq, const uint8_t* xs, const int* offsets,
                             const int* perm, float* y_assign, float* y_shared, void* ws, cudaStream_t s,
-                            const float* fuse_w = nullptr, float* acc = nullptr, bool* fused = nullptr) {
+                            const float* fuse_w = nullptr, float* acc = nullptr, bool* fused = nullptr,
+                            const Shared8Dev* sh8 = nullptr) {
   const WsLayout L = ws_layout(d->T, d->H, d->I, d->E, d->top_k);
   const Shape sh = shape_of(d);
   const uint64_t limit = g_wait_limit_ns.load();
@@ -136,14 +151,21 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
   if (fused) *fused = fuse;
   // record which layout h is left in (read by moe_debug_requantized_h)
   MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.counters) + C_HPATH, tc ? (wa ? 2 : 1) : 0, sizeof(int), s));
+  const bool has_shared = shd.w13 || sh8;
   auto shared_expert = [&](float* ys) -> moe_status_t {
+    if (sh8) {  // MXFP8 on kind::mxf8f6f4 tensor cores
+      const Shared8Ws w8{at<uint8_t>(ws, L.s8_xq), at<uint8_t>(ws, L.s8_xs),     at<uint8_t>(ws, L.s8_xs_mma),
+                         at<uint8_t>(ws, L.s8_hq), at<uint8_t>(ws, L.s8_hs_mma), at<uint8_t>(ws, L.s8_w13s),
+                         at<uint8_t>(ws, L.s8_w2s)};
+      return cuda_status(launch_shared_mxfp8_tc(sh, *sh8, x, w8, ys, status, limit, s));
+    }
     uint16_t* h = at<uint16_t>(ws, L.h_shared);
     if (shared_tc_path(d->T, d->H, d->I))
       return cuda_status(launch_shared_tc(sh, shd, x, h, ys, at<float>(ws, L.sh_part), status, limit, s));
     return cuda_status(launch_shared_simt(sh, shd, x, h, ys, s));
   };
   if (fuse) {  // the accumulator starts as ys (or zero)
-    if (shd.w13)
+    if (has_shared)
       MOE_TRY(shared_expert(acc));
     else
       MOE_CUDA(cudaMemsetAsync(acc, 0, sizeof(float) * (size_t)d->T * d->H, s));
@@ -159,7 +181,7 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
     MOE_CUDA(launch_routed_simt(sh, ex, xq, xs, offsets, perm, at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs),
                                 y_assign, s));
   }
-  if (shd.w13 && !fuse) MOE_TRY(shared_expert(y_shared));
+  if (has_shared && !fuse) MOE_TRY(shared_expert(y_shared));
   return MOE_OK;
 }
 
@@ -169,7 +191,8 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
 // shape with no BF16 shared expert.
 moe_status_t run_forward(const moe_layer_desc_t* desc, const ExpertsDev& ex, const SharedDev& shd,
                          const float* w_router, const float* bias, const uint16_t* xb, uint16_t* out,
-                         int32_t* topk_ids, float* topk_w, void* ws, cudaStream_t s) {
+                         int32_t* topk_ids, float* topk_w, void* ws, cudaStream_t s,
+                         const Shared8Dev* sh8 = nullptr) {
   const moe_layer_desc_t dt = table_desc(desc);
   const int fold = desc->shared_in_table;
   const WsLayout L = ws_layout(dt.T, dt.H, dt.I, dt.E, dt.top_k);
@@ -186,11 +209,11 @@ moe_status_t run_forward(const moe_layer_desc_t* desc, const ExpertsDev& ex, con
   MOE_CUDA(launch_permute(ids, sh.T, sh.k, sh.E, at<int>(ws, L.counts), at<int>(ws, L.offsets),
                           at<int>(ws, L.perm), at<int>(ws, L.inv_perm), at<int>(ws, L.rank),
                           at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base), s));
-  float* ysh = shd.w13 ? at<float>(ws, L.y_shared) : nullptr;
+  float* ysh = (shd.w13 || sh8) ? at<float>(ws, L.y_shared) : nullptr;
   bool fused = false;
   MOE_TRY(run_expert_ffn(&dt, ex, shd, xb, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), at<int>(ws, L.offsets),
                          at<int>(ws, L.perm), at<float>(ws, L.y_assign), ysh, ws, s, w, at<float>(ws, L.y_shared),
-                         &fused));
+                         &fused, sh8));
   if (fused)  // the combine ran in the down GEMM: the FP32 output is rounded to BF16
     return cuda_status(launch_acc_to_bf16(at<float>(ws, L.y_shared), (size_t)sh.T * sh.H, out, s));
   return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh, out, s));
@@ -433,13 +456,57 @@ moe_status_t moe_shared_expert_mxfp8(const moe_layer_desc_t* desc, const moe_sha
   if (desc->T == 0) return MOE_OK;
   if (!x || !y_shared || !aligned(x, 16) || !aligned(y_shared, 16)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = layout_of(desc);
-  const Shared8Dev sh8{shared->w13, shared->w13_scale, shared->w2, shared->w2_scale};
+  Shared8Dev sh8;
+  MOE_TRY(check_shared8(desc, shared, &sh8));
   const Shared8Ws w{at<uint8_t>(ws, L.s8_xq),  at<uint8_t>(ws, L.s8_xs),   at<uint8_t>(ws, L.s8_xs_mma),
                     at<uint8_t>(ws, L.s8_hq),  at<uint8_t>(ws, L.s8_hs_mma), at<uint8_t>(ws, L.s8_w13s),
                     at<uint8_t>(ws, L.s8_w2s)};
   return cuda_status(launch_shared_mxfp8_tc(shape_of(desc), sh8, static_cast<const uint16_t*>(x), w, y_shared,
                                             at<int>(ws, L.counters) + C_STATUS, g_wait_limit_ns.load(),
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_prepare_shared_mxfp8(const moe_layer_desc_t* desc, const moe_shared_mxfp8_t* shared,
+                                      uint8_t* w13_scale_mma, uint8_t* w2_scale_mma, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  Shared8Dev sh8;
+  MOE_TRY(check_shared8(desc, shared, &sh8));
+  if (!w13_scale_mma || !w2_scale_mma || !aligned(w13_scale_mma, 16) || !aligned(w2_scale_mma, 16))
+    return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_relayout_weight_sf(sh8.w13s, 1, 2 * desc->I, desc->H, w13_scale_mma, s));
+  return cuda_status(launch_relayout_weight_sf(sh8.w2s, 1, desc->H, desc->I, w2_scale_mma, s));
+}
+
+moe_status_t moe_debug_shared_mxfp8_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes, uint8_t* hq,
+                                      uint8_t* hs, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_ws(desc, const_cast<void*>(ws), ws_bytes));
+  if (desc->T == 0) return MOE_OK;
+  if (!hq || !hs) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout_of(desc);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint8_t* base = static_cast<const uint8_t*>(ws);
+  const size_t tp = ((size_t)desc->T + 127) / 128 * 128;
+  MOE_CUDA(cudaMemcpyAsync(hq, base + L.s8_hq, (size_t)desc->T * desc->I, cudaMemcpyDeviceToDevice, s));
+  return cuda_status(cudaMemcpyAsync(hs, base + L.s8_hs_mma, tp * desc->I / 32, cudaMemcpyDeviceToDevice, s));
+}
+
+moe_status_t moe_layer_forward_shared_mxfp8(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                            const moe_shared_mxfp8_t* shared, const float* w_router,
+                                            const float* bias, const void* x, void* out, int32_t* topk_ids,
+                                            float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_ws(desc, ws, ws_bytes));
+  ExpertsDev ex;
+  Shared8Dev sh8;
+  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_shared8(desc, shared, &sh8));
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !out || !w_router || !aligned(x, 16) || !aligned(out, 16) || !aligned(w_router, 16))
+    return MOE_ERR_INVALID_ARG;
+  return run_forward(desc, ex, SharedDev{nullptr, nullptr}, w_router, bias, static_cast<const uint16_t*>(x),
+                     static_cast<uint16_t*>(out), topk_ids, topk_w, ws, reinterpret_cast<cudaStream_t>(stream), &sh8);
 }
 
 moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_assign, const int32_t* inv_perm,

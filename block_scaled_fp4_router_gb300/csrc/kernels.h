@@ -110,6 +110,8 @@ struct Shared8Dev {
   const uint8_t* w13s;
   const uint8_t* w2;
   const uint8_t* w2s;
+  const uint8_t* w13s_mma;  // prepared scale layout, or null (re-laid per call)
+  const uint8_t* w2s_mma;
 };
 struct Shared8Ws {
   uint8_t* xq;

@@ -264,9 +264,12 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.dc_gu_r = take(dc ? sizeof(float) * sp.rgu * n * 2 * (size_t)I : 0);
   L.dc_ys = take(dc ? sizeof(float) * sp.sdn * T * (size_t)H : 0);
   L.total = o;
-  {  // MXFP8 shared expert (moe_shared_expert_mxfp8, T rounded up to 128 rows):
-     // it uses nothing else past zero_end, so its scratch overlays that part
-    size_t o8 = L.zero_end;
+  {  // MXFP8 shared expert (T rounded up to 128 rows).  Inside a layer call it
+     // runs between the routing and the routed experts, so it keeps clear of
+     // every region above except the tensor-core decode's scratch (from dc_xs
+     // on), which only the single-launch decode uses and which holds nothing
+     // across calls.
+    size_t o8 = L.dc_xs;
     auto take8 = [&](size_t bytes) {
       size_t at = o8;
       o8 = align256(o8 + (bytes ? bytes : 1));

@@ -1063,8 +1063,15 @@ cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const
   // rows' scales are never used) and the weights' scales in the MMA layout
   if ((err = launch_quant_mxfp8(x, T, H, w.xq, w.xs, s)) != cudaSuccess) return err;
   if ((err = launch_relayout_weight_sf(w.xs, 1, tpad, H, w.xs_mma, s)) != cudaSuccess) return err;
-  if ((err = launch_relayout_weight_sf(sh8.w13s, 1, 2 * I, H, w.w13s_mma, s)) != cudaSuccess) return err;
-  if ((err = launch_relayout_weight_sf(sh8.w2s, 1, H, I, w.w2s_mma, s)) != cudaSuccess) return err;
+  // the weights' scales: prepared at load time, else re-laid for this call
+  const uint8_t* w13s_mma = sh8.w13s_mma;
+  const uint8_t* w2s_mma = sh8.w2s_mma;
+  if (!w13s_mma || !w2s_mma) {
+    if ((err = launch_relayout_weight_sf(sh8.w13s, 1, 2 * I, H, w.w13s_mma, s)) != cudaSuccess) return err;
+    if ((err = launch_relayout_weight_sf(sh8.w2s, 1, H, I, w.w2s_mma, s)) != cudaSuccess) return err;
+    w13s_mma = w.w13s_mma;
+    w2s_mma = w.w2s_mma;
+  }
   CUtensorMap ma, mb;
   // gate/up: A = xq [T][H] E4M3, B = W13 [2I][H] E4M3; SwiGLU + MXFP8 requantise
   if ((err = make_map(&ma, w.xq, T, H)) != cudaSuccess) return err;
@@ -1076,7 +1083,7 @@ cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const
   g1.rows_dense = T;
   g1.b_up_off = I;
   g1.sfa = w.xs_mma;
-  g1.sfb = w.w13s_mma;
+  g1.sfb = w13s_mma;
   g1.sfb_rtiles = 2 * I / BM;
   g1.hq = w.hq;
   g1.hs = reinterpret_cast<uint32_t*>(w.hs_mma);
@@ -1093,7 +1100,7 @@ cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const
   g2.num_mt_dense = mt;
   g2.rows_dense = T;
   g2.sfa = w.hs_mma;
-  g2.sfb = w.w2s_mma;
+  g2.sfb = w2s_mma;
   g2.sfb_rtiles = H / BM;
   g2.out = y_shared;
   g2.ldo = H;

@@ -9,7 +9,8 @@ import numpy as np
 import torch
 
 from . import (MOE_W_MXFP4, MOE_W_NVFP4, desc, experts, moe_layer_decode, moe_layer_forward,
-               moe_prepare_weights, moe_workspace_size, shared_bf16)
+               moe_layer_forward_shared_mxfp8, moe_prepare_shared_mxfp8, moe_prepare_weights, moe_workspace_size,
+               shared_bf16, shared_mxfp8)
 
 
 def _to_dev(a, device, dtype=None):
@@ -61,6 +62,16 @@ class DeviceLayer:
                                        self.w13_scale_mma, self.w2_scale_mma)
         self.ex = self.ex_prepared if self.ex_prepared is not None else self.ex_plain
         self.sh = shared_bf16(self.ws13, self.ws2)
+        # an MXFP8 shared expert (its scales prepared for the tensor cores)
+        self.sh8 = None
+        if shared and arrays.get("s8_w13") is not None:
+            self.s8 = {k: _to_dev(arrays[k], d) for k in ("s8_w13", "s8_w13_scale", "s8_w2", "s8_w2_scale")}
+            self.s8_w13_mma = torch.empty_like(self.s8["s8_w13_scale"])
+            self.s8_w2_mma = torch.empty_like(self.s8["s8_w2_scale"])
+            plain = shared_mxfp8(self.s8["s8_w13"], self.s8["s8_w13_scale"], self.s8["s8_w2"], self.s8["s8_w2_scale"])
+            moe_prepare_shared_mxfp8(desc(0, H, I, E, top_k), plain, self.s8_w13_mma, self.s8_w2_mma)
+            self.sh8 = shared_mxfp8(self.s8["s8_w13"], self.s8["s8_w13_scale"], self.s8["s8_w2"],
+                                    self.s8["s8_w2_scale"], self.s8_w13_mma, self.s8_w2_mma)
         self.T_max = T_max
         nbytes = moe_workspace_size(desc(T_max, H, I, E, top_k, self.fold))
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=d)
@@ -90,6 +101,8 @@ class DeviceLayer:
                 torch.empty((T, self.k), dtype=torch.float32, device=d))
 
     def decode(self, x: torch.Tensor, out=None, ids=None, w=None, stream=None):
+        if self.sh8 is not None:
+            raise NotImplementedError("the single-launch decode takes a BF16 or folded shared expert")
         T = x.shape[0]
         if out is None:
             out, ids, w = self.outputs(T)
@@ -101,6 +114,10 @@ class DeviceLayer:
         T = x.shape[0]
         if out is None:
             out, ids, w = self.outputs(T)
-        moe_layer_forward(self.desc(T), self.ex, self.sh, self.w_router, self.bias, x, out, ids, w, self.ws,
-                          stream)
+        if self.sh8 is not None:
+            moe_layer_forward_shared_mxfp8(self.desc(T), self.ex, self.sh8, self.w_router, self.bias, x, out, ids, w,
+                                           self.ws, stream)
+        else:
+            moe_layer_forward(self.desc(T), self.ex, self.sh, self.w_router, self.bias, x, out, ids, w, self.ws,
+                              stream)
         return out, ids, w

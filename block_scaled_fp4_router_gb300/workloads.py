@@ -16,6 +16,8 @@ Instinct GPUs", section "MiniMax-M3.1 at a glance"):
 * ``decode16z``  T=16,   same shape, NVFP4, Zipf(1.2)-skewed router bias, seed 2
 * ``batch128``   T=128,  same shape, MXFP4, router logits ~ N(0,1), seed 3
 * ``prefill8k``  T=8192, same shape, MXFP4, Zipf(1.1)-skewed expert load, seed 4
+* ``*_s8``       128-token batch and 8192-token prefill with the shared
+                 expert in MXFP8 (E4M3 + E8M0 per 32) instead of BF16
 * ``*_sig``      tiny, 16-token NVFP4 decode and 128-token batch with sigmoid
                  scoring and a Zipf(0.05) correction bias (seeds 14, 15, 16)
 
@@ -77,6 +79,7 @@ class Workload:
     shared_std: float = 0.02
     shared_fp4: bool = False  # the shared expert as expert E of the FP4 table
     score: str = "softmax"    # router scores: softmax, or sigmoid with a bias-corrected choice
+    shared_fmt: str = "bf16"  # the shared expert's weights: BF16, or MXFP8 (E4M3 + E8M0 per 32)
     # E8M0 block-scale exponents drawn uniformly from [lo, hi]
     mx_exp_lo: int = -8
     mx_exp_hi: int = -4
@@ -101,6 +104,8 @@ WORKLOADS = {
         Workload("tiny_sfp4", 16, 512, 256, 16, 4, MXFP4, 10, 0.02, shared=False, shared_fp4=True),
         Workload("decode1_sfp4", 1, 4096, 1536, 128, 4, MXFP4, 11, 0.02, shared=False, shared_fp4=True),
         Workload("batch128_sfp4", 128, 4096, 1536, 128, 4, MXFP4, 13, 1.0 / 64.0, shared=False, shared_fp4=True),
+        Workload("batch128_s8", 128, 4096, 1536, 128, 4, MXFP4, 3, 1.0 / 64.0, shared_fmt="mxfp8"),
+        Workload("prefill8k_s8", 8192, 4096, 1536, 128, 4, MXFP4, 4, 0.02, zipf=1.1, shared_fmt="mxfp8"),
         Workload("tiny_sig", 16, 512, 256, 16, 4, MXFP4, 14, 0.02, zipf=0.05, score="sigmoid"),
         Workload("decode16_sig", 16, 4096, 1536, 128, 4, NVFP4, 15, 0.02, zipf=0.05, score="sigmoid"),
         Workload("batch128_sig", 128, 4096, 1536, 128, 4, MXFP4, 16, 1.0 / 64.0, zipf=0.05, score="sigmoid"),
@@ -163,7 +168,11 @@ def generate(w: Workload, layer: int = 0, tokens: Optional[int] = None) -> dict:
         out["w2_scale"] = rw.integers(lo, hi + 1, size=(Et, H, I // 16), dtype=np.uint8)
         out["tensor_scale"] = (NVFP4_TENSOR_SCALE * rt.uniform(NVFP4_TS_LO, NVFP4_TS_HI, size=(Et, 3))).astype(
             np.float32)
-    if w.shared:
+    if w.shared and w.shared_fmt == "mxfp8":
+        out["ws13"] = None
+        out["ws2"] = None
+        out.update(generate_shared_mxfp8(w, 7919 * w.seed + layer))
+    elif w.shared:
         out["ws13"] = _to_bf16_bits(rw.normal(0.0, w.shared_std, size=(2 * I, H)))
         out["ws2"] = _to_bf16_bits(rw.normal(0.0, w.shared_std, size=(H, I)))
     else:
@@ -234,7 +243,16 @@ def generate_device(w: Workload, layer: int, device) -> dict:
         out["w2_scale"] = torch.randint(lo, hi + 1, (Et, H, I // 16), **u8)
         out["tensor_scale"] = NVFP4_TENSOR_SCALE * (
             NVFP4_TS_LO + (NVFP4_TS_HI - NVFP4_TS_LO) * torch.rand((Et, 3), device=device, generator=g))
-    if w.shared:
+    if w.shared and w.shared_fmt == "mxfp8":
+        out["ws13"] = None
+        out["ws2"] = None
+        # E4M3 codes over the finite encodings of either sign, E8M0 exponents in [-14, -10]
+        codes = lambda shape: (torch.randint(0, 0x7F, shape, **u8) | (torch.randint(0, 2, shape, **u8) << 7))
+        out["s8_w13"] = codes((2 * I, H))
+        out["s8_w13_scale"] = torch.randint(127 - 14, 127 - 10 + 1, (2 * I, H // 32), **u8)
+        out["s8_w2"] = codes((H, I))
+        out["s8_w2_scale"] = torch.randint(127 - 14, 127 - 10 + 1, (H, I // 32), **u8)
+    elif w.shared:
         bf = torch.bfloat16
         out["ws13"] = (torch.randn((2 * I, H), device=device, generator=g) * w.shared_std).to(bf)
         out["ws2"] = (torch.randn((H, I), device=device, generator=g) * w.shared_std).to(bf)

@@ -152,12 +152,16 @@ typedef struct {
 } moe_shared_bf16_t;
 
 /* An MXFP8 shared expert (OCP MX: E4M3 elements, one E8M0 scale per 32
- * along K), the format the pages' fused decode runs the shared expert in. */
+ * along K), the format the pages' fused decode runs the shared expert in.
+ * The two *_mma fields are optional copies of the scales in the tensor-core
+ * layout written by moe_prepare_shared_mxfp8 (NULL = re-laid on every call). */
 typedef struct {
   const uint8_t* w13;        /* E4M3 [2I, H] (gate rows then up rows), 16-byte aligned */
   const uint8_t* w13_scale;  /* E8M0 [2I, H/32], 4-byte aligned */
   const uint8_t* w2;         /* E4M3 [H, I], 16-byte aligned */
   const uint8_t* w2_scale;   /* E8M0 [H, I/32], 4-byte aligned */
+  const uint8_t* w13_scale_mma;
+  const uint8_t* w2_scale_mma;
 } moe_shared_mxfp8_t;
 
 /* Human-readable name of a status code (static storage). */
@@ -298,6 +302,15 @@ MOE_API moe_status_t moe_shared_expert_mxfp8(const moe_layer_desc_t* desc, const
                                              const void* x, float* y_shared, void* ws, size_t ws_bytes,
                                              moe_stream_t stream);
 
+/* Load-time re-layout of an MXFP8 shared expert's scales for the tensor
+ * cores (the same 512-byte blocks as moe_prepare_weights over 128 rows x 128
+ * K elements):
+ *   w13_scale_mma  out, 2I * H/32 bytes;  w2_scale_mma  out, H * I/32 bytes
+ * (16-byte aligned).  H and I multiples of 256 (else MOE_ERR_UNSUPPORTED).
+ * Point shared->w13_scale_mma / w2_scale_mma at them afterwards. */
+MOE_API moe_status_t moe_prepare_shared_mxfp8(const moe_layer_desc_t* desc, const moe_shared_mxfp8_t* shared,
+                                              uint8_t* w13_scale_mma, uint8_t* w2_scale_mma, moe_stream_t stream);
+
 /* A9: weighted combine (vLLM PR #64273 commit list: "MoE finalize").
  *   out[t] = BF16(y_shared[t] + sum_j topk_w[t, j] * y_assign[inv_perm[t*k + j]])
  *   y_shared may be NULL (treated as 0).  out BF16 [T, H]. */
@@ -331,6 +344,18 @@ MOE_API moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_e
                                const moe_shared_bf16_t* shared, const float* w_router,
                                const float* bias, const void* x, void* out, int32_t* topk_ids,
                                float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_layer_forward with the shared expert in MXFP8 (AMD article, section
+ * "What we Optimized": the shared expert runs in MXFP8), on kind::mxf8f6f4
+ * tensor cores with the arithmetic of moe_shared_expert_mxfp8 (the token and
+ * h quantised to MXFP8 per 32), weight 1 in the combine.  Needs H and I
+ * multiples of 256 and desc->shared_in_table = 0 (else MOE_ERR_UNSUPPORTED /
+ * MOE_ERR_INVALID_ARG); every other argument as for moe_layer_forward. */
+MOE_API moe_status_t moe_layer_forward_shared_mxfp8(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                                    const moe_shared_mxfp8_t* shared, const float* w_router,
+                                                    const float* bias, const void* x, void* out,
+                                                    int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                                                    moe_stream_t stream);
 
 /* Size of the scratch array built into the library for
  * moe_layer_decode_noalloc (8 MiB, held on every GPU that loads the library
@@ -406,6 +431,15 @@ MOE_API moe_status_t moe_copy_rows(void* dst, const void* src, size_t bytes, moe
  * workspace of that call. */
 MOE_API moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes,
                                              uint8_t* hq, uint8_t* hs, moe_stream_t stream);
+
+/* Test hook: copies the MXFP8 shared expert's requantised h of the last call
+ * that ran it with this workspace (moe_shared_expert_mxfp8 or
+ * moe_layer_forward_shared_mxfp8): E4M3 codes [T, I] into hq and the E8M0
+ * scales, in their tensor-core layout, [ceil(T/128)][I/128][512] bytes into
+ * hs (word (i, j) of a block at byte 16 i + 4 j holds the four scales of row
+ * 32 j + i for 128 consecutive columns).  Enqueued on the stream. */
+MOE_API moe_status_t moe_debug_shared_mxfp8_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes,
+                                              uint8_t* hq, uint8_t* hs, moe_stream_t stream);
 
 /* Test hook for the failure path: launches one bounded wait on a workspace
  * counter that nothing ever advances, with the given limit.  Afterwards

@@ -30,6 +30,8 @@ Readings where the pages are silent:
 * the shared expert has BF16 weights, takes the BF16 token as is, and rounds
   its intermediate h to BF16 before its down projection; its weight in the
   combine is 1;
+* an MXFP8 shared expert (layer["s8_w13"] ...) follows shared_expert_mxfp8:
+  the token and h quantised to MXFP8 per 32, weight 1;
 * folded into the expert table (model card "amd/MiniMax-M3.1-Flash-Quark-MXFP4",
   section "Experimental MXFP4 shared experts"; AMD article, section
   "Performance, mono decode on vs off"), the shared expert is expert E of the
@@ -292,6 +294,11 @@ def layer_forward(layer: dict, top_k: int, fmt: str, tokens=None, forced_ids=Non
             wg, wu, wd = expert_matrices(layer, E, fmt)
         sh = routed_expert(xq_deq, wg, wu, wd)
         ys = sh["y"]
+    elif layer.get("s8_w13") is not None:
+        # the MXFP8 shared expert the pages' fused decode runs (AMD article,
+        # section "What we Optimized")
+        sh = shared_expert_mxfp8(x, layer["s8_w13"], layer["s8_w13_scale"], layer["s8_w2"], layer["s8_w2_scale"])
+        ys = sh["ys"]
     elif layer.get("ws13") is not None:
         sh = shared_expert(x, layer["ws13"], layer["ws2"])
         ys = sh["ys"]

@@ -808,6 +808,70 @@ def test_shared_expert_mxfp8(T, H, I):
     got = y.cpu().numpy()
     assert np.all(np.isfinite(got))
     assert normwise(got, ref["ys"]) <= CONTRACTION_TOL
+    _check_mxfp8_h(d, ws, T, I, ref, F.dequantize_mxfp8(ref["xq"], ref["xs"]),
+                   F.dequantize_mxfp8(arr["s8_w13"], arr["s8_w13_scale"]))
+
+
+_E4M3_MIDS = (F.E4M3_TABLE[:0x7E] + F.E4M3_TABLE[1:0x7F]) / 2  # between neighbouring positive E4M3 values
+
+
+def _check_mxfp8_h(d, ws, T, I, ref, xq_deq, w13):
+    """The MXFP8-requantised h of the shared expert (codes and the E8M0 scale
+    bytes in their tensor-core layout) equals the oracle's block for block,
+    except blocks where the oracle's h lies within the FP32 contraction's
+    error of an E4M3 rounding midpoint or of a change of the block exponent.
+    G and U are FP32 tensor-core sums over K = H products: their error is
+    bounded here by 2^-19 sum |xq w| (an FP32 accumulation of K terms in any
+    order, with room), and carried to h through dh = |SiLU'(G) U| dG +
+    |SiLU(G)| dU; E4M3's midpoints are dense enough (every 1/16 of a binade)
+    that a fixed relative margin would not hold."""
+    tp = (T + 127) // 128 * 128
+    ghq = torch.empty((T, I), dtype=torch.uint8, device="cuda")
+    ghs = torch.empty(tp * I // 32, dtype=torch.uint8, device="cuda")
+    M.moe_debug_shared_mxfp8_h(d, ws, ghq, ghs)
+    torch.cuda.synchronize()
+    # word (i, j) of block (row tile, 128-column group) holds rows 32 j + i
+    raw = ghs.cpu().numpy().reshape(tp // 128, I // 128, 32, 4, 4)   # tile, group, i, j, byte
+    gs = raw.transpose(0, 3, 2, 1, 4).reshape(tp, I // 32)[:T]       # tile, j, i -> row; group, byte -> block
+    gq = ghq.cpu().numpy().reshape(T, I // 32, 32)
+    oq = ref["hq"].reshape(T, I // 32, 32)
+    same = np.all(gq == oq, axis=2) & (gs == ref["hs"])
+    G, U = ref["G"], ref["U"]
+    mag = np.abs(xq_deq) @ np.abs(w13).T                           # [T, 2I]: sum |xq w|
+    dG, dU = 2.0 ** -19 * mag[:, :I], 2.0 ** -19 * mag[:, I:]
+    sg = 1.0 / (1.0 + np.exp(-G))
+    dh = np.abs(sg * (1 + G * (1 - sg)) * U) * dG + np.abs(G * sg) * dU + 2.0 ** -23 * np.abs(ref["h"])
+    hb = ref["h"].reshape(T, I // 32, 32)
+    db = dh.reshape(T, I // 32, 32)
+    amax = np.abs(hb).max(2)
+    p2 = 2.0 ** np.floor(np.log2(np.maximum(amax, 1e-300)))
+    near_scale = (np.abs(amax - p2) <= db.max(2)) | (np.abs(amax - 2 * p2) <= db.max(2))
+    X = F.E8M0_TABLE[ref["hs"]][..., None]
+    sv, sd = np.abs(hb) / X, db / X
+    near_code = np.any(np.min(np.abs(sv[..., None] - _E4M3_MIDS), axis=-1) <= sd, axis=2)
+    assert np.all(same | near_scale | near_code), "MXFP8 h differs away from a rounding boundary"
+    assert same.mean() >= 0.99, same.mean()
+
+
+@pytest.mark.parametrize("name,T,gemm", [("batch128_s8", None, M.ROUTED_GEMM_AUTO),
+                                         ("batch128_s8", 300, M.ROUTED_GEMM_TOKENS_AS_A)])
+def test_layer_forward_with_mxfp8_shared_expert(name, T, gemm, routed_gemm):
+    """The layer with the shared expert in MXFP8 (moe_layer_forward_shared_mxfp8,
+    scales prepared at load time) against the oracle on every token: 128
+    tokens (weights-as-A routed GEMMs, separate combine) and 300 tokens
+    (128-token routed tiles, the combine fused into the down GEMM, the MXFP8
+    shared expert writing the accumulator first)."""
+    routed_gemm(gemm)
+    wl, lay, dev, cache = _workload(name, T)
+    assert dev.sh8 is not None
+    out, ids, w = dev.forward(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, cache, out, ids, w=w)
+    ref = O.shared_expert_mxfp8(F.bf16_bits_to_float(lay["x"]), lay["s8_w13"], lay["s8_w13_scale"], lay["s8_w2"],
+                                lay["s8_w2_scale"])
+    _check_mxfp8_h(dev.desc(wl.T), dev.ws, wl.T, wl.I, ref, F.dequantize_mxfp8(ref["xq"], ref["xs"]),
+                   F.dequantize_mxfp8(lay["s8_w13"], lay["s8_w13_scale"]))
 
 
 def test_mxfp8_to_bf16_dequant_bitexact():

@@ -271,6 +271,32 @@ def test_structured_layer_closed_form_shared_in_table():
     assert np.all(r["out"] == 2.15625)
 
 
+def test_structured_layer_closed_form_mxfp8_shared_expert():
+    """The structured layer with an MXFP8 shared expert (E4M3 gate codes 1.0,
+    up codes 2.0, down codes 1.0; E8M0 scales 2^-6, 2^-6, 2^-5) instead of
+    the BF16 one, worked by hand.  x = 1 quantises to MXFP8 exactly (amax 1,
+    X = 2^-8, 256 = E4M3 0x78): G = 64 * 2^-6 = 1, U = 64 * 2 * 2^-6 = 2,
+    h = 2 SiLU(1) = 1.4621172; h / 2^-8 = 374.30 rounds to the E4M3 value
+    384 (neighbours 352 and 384, step 32 in [256, 512)), so hq = 1.5 and
+    ys = 32 * 1.5 * 2^-5 = 1.5.  out = BF16(1.5 + 0.75 w1 + 0.375 w2) =
+    2.15625, as with the MXFP4 shared expert folded into the table."""
+    lay = _structured_layer([1.0, 3.0, 2.0, 0.0])
+    H, I = 64, 32
+    assert F.E4M3_TABLE[0x38] == 1.0 and F.E4M3_TABLE[0x40] == 2.0 and F.E4M3_TABLE[0x78] == 256.0
+    lay["ws13"] = lay["ws2"] = None
+    lay["s8_w13"] = np.concatenate([np.full((I, H), 0x38, np.uint8), np.full((I, H), 0x40, np.uint8)])
+    lay["s8_w13_scale"] = np.full((2 * I, H // 32), 127 - 6, np.uint8)
+    lay["s8_w2"] = np.full((H, I), 0x38, np.uint8)
+    lay["s8_w2_scale"] = np.full((H, I // 32), 127 - 5, np.uint8)
+    r = M.layer_forward(lay, 2, "mxfp4", keep=True)
+    sh = r["shared"]
+    assert np.all(sh["xq"] == 0x78) and np.all(sh["xs"] == 127 - 8)
+    assert np.all(sh["G"] == 1.0) and np.all(sh["U"] == 2.0)
+    assert np.all(F.dequantize_mxfp8(sh["hq"], sh["hs"]) == 1.5)
+    assert np.all(r["ys"] == 1.5)
+    assert np.all(r["out"] == 2.15625)
+
+
 def test_structured_layer_routing_ties():
     lay = _structured_layer([2.0, 2.0, 1.0, 2.0])
     r = M.layer_forward(lay, 2, "mxfp4")
