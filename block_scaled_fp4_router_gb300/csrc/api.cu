@@ -138,7 +138,7 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
                             const uint16_t* x, const uint8_t* xq, const uint8_t* xs, const int* offsets,
                             const int* perm, float* y_assign, float* y_shared, void* ws, cudaStream_t s,
                             const float* fuse_w = nullptr, float* acc = nullptr, bool* fused = nullptr,
-                            const Shared8Dev* sh8 = nullptr) {
+                            const Shared8Dev* sh8 = nullptr, int* slice_rows = nullptr) {
   const WsLayout L = ws_layout(d->T, d->H, d->I, d->E, d->top_k);
   const Shape sh = shape_of(d);
   const uint64_t limit = g_wait_limit_ns.load();
@@ -152,21 +152,26 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
   // record which layout h is left in (read by moe_debug_requantized_h)
   MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.counters) + C_HPATH, tc ? (wa ? 2 : 1) : 0, sizeof(int), s));
   const bool has_shared = shd.w13 || sh8;
-  auto shared_expert = [&](float* ys) -> moe_status_t {
+  // The fused combine keeps the accumulator by 256-column slices (each pass
+  // of the down GEMM then works on one contiguous T x 1 KB block) when its
+  // first writer, the shared expert, is a tensor-core GEMM or absent.
+  const int slice = fuse && (!has_shared || sh8 || shared_tc_path(d->T, d->H, d->I)) ? d->T : 0;
+  if (slice_rows) *slice_rows = slice;
+  auto shared_expert = [&](float* ys, int sl) -> moe_status_t {
     if (sh8) {  // MXFP8 on kind::mxf8f6f4 tensor cores
       const Shared8Ws w8{at<uint8_t>(ws, L.s8_xq), at<uint8_t>(ws, L.s8_xs),     at<uint8_t>(ws, L.s8_xs_mma),
                          at<uint8_t>(ws, L.s8_hq), at<uint8_t>(ws, L.s8_hs_mma), at<uint8_t>(ws, L.s8_w13s),
                          at<uint8_t>(ws, L.s8_w2s)};
-      return cuda_status(launch_shared_mxfp8_tc(sh, *sh8, x, w8, ys, status, limit, s));
+      return cuda_status(launch_shared_mxfp8_tc(sh, *sh8, x, w8, ys, status, limit, s, sl));
     }
     uint16_t* h = at<uint16_t>(ws, L.h_shared);
     if (shared_tc_path(d->T, d->H, d->I))
-      return cuda_status(launch_shared_tc(sh, shd, x, h, ys, at<float>(ws, L.sh_part), status, limit, s));
+      return cuda_status(launch_shared_tc(sh, shd, x, h, ys, at<float>(ws, L.sh_part), status, limit, s, sl));
     return cuda_status(launch_shared_simt(sh, shd, x, h, ys, s));
   };
   if (fuse) {  // the accumulator starts as ys (or zero)
     if (has_shared)
-      MOE_TRY(shared_expert(acc));
+      MOE_TRY(shared_expert(acc, slice));
     else
       MOE_CUDA(cudaMemsetAsync(acc, 0, sizeof(float) * (size_t)d->T * d->H, s));
   }
@@ -174,14 +179,14 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
     TcWorkspace w{at<int>(ws, L.tc_poff), at<uint8_t>(ws, L.tc_mtiles), at<int>(ws, L.tc_num_mt),
                   at<uint8_t>(ws, L.tc_xq), at<uint8_t>(ws, L.tc_xs), at<uint8_t>(ws, L.tc_hq),
                   at<uint8_t>(ws, L.tc_hs), at<uint8_t>(ws, L.tc_w13s), at<uint8_t>(ws, L.tc_w2s)};
-    const CombineArgs comb{fuse_w, acc};
+    const CombineArgs comb{fuse_w, acc, slice};
     MOE_CUDA(launch_expert_ffn_tc(sh, ex, w, xq, xs, offsets, perm, y_assign, status, limit, wa, s,
                                   fuse ? &comb : nullptr));
   } else {
     MOE_CUDA(launch_routed_simt(sh, ex, xq, xs, offsets, perm, at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs),
                                 y_assign, s));
   }
-  if (has_shared && !fuse) MOE_TRY(shared_expert(y_shared));
+  if (has_shared && !fuse) MOE_TRY(shared_expert(y_shared, 0));
   return MOE_OK;
 }
 
@@ -211,11 +216,12 @@ moe_status_t run_forward(const moe_layer_desc_t* desc, const ExpertsDev& ex, con
                           at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base), s));
   float* ysh = (shd.w13 || sh8) ? at<float>(ws, L.y_shared) : nullptr;
   bool fused = false;
+  int slice = 0;
   MOE_TRY(run_expert_ffn(&dt, ex, shd, xb, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), at<int>(ws, L.offsets),
                          at<int>(ws, L.perm), at<float>(ws, L.y_assign), ysh, ws, s, w, at<float>(ws, L.y_shared),
-                         &fused, sh8));
+                         &fused, sh8, &slice));
   if (fused)  // the combine ran in the down GEMM: the FP32 output is rounded to BF16
-    return cuda_status(launch_acc_to_bf16(at<float>(ws, L.y_shared), (size_t)sh.T * sh.H, out, s));
+    return cuda_status(launch_acc_to_bf16(at<float>(ws, L.y_shared), sh.T, sh.H, slice, out, s));
   return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh, out, s));
 }
 

@@ -213,6 +213,12 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// SiLU for the batched GEMM epilogues, where it runs on every element of the
+// accumulator: the fast exponential and division intrinsics, a few ulp from
+// silu() for |g| < 88 (where h is later requantised or rounded to BF16), and
+// 0 below (the approximate reciprocal of the infinite denominator is 0).
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
 // ------------------------------------------------------------- memory ops
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {

@@ -81,6 +81,7 @@ struct TcWorkspace {
 struct CombineArgs {
   const float* topk_w;  // [T * k], flat assignment t * k + j
   float* acc;
+  int slice_rows;       // acc laid out by 256-column slices [H/256][T][256] (slice_rows = T), or 0: [T][H]
 };
 // A5 - A7 on tensor cores (MXFP4 weights)
 // wa: weights as the MMA's A operand and 64-row token windows as B (small
@@ -90,15 +91,17 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
                                  const uint8_t* xs, const int* offsets, const int* perm, float* y_assign,
                                  int* status, uint64_t limit_ns, bool wa, cudaStream_t s,
                                  const CombineArgs* comb = nullptr);
-// out BF16 [n] = acc FP32 [n] (n a multiple of 4).
-cudaError_t launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s);
+// out BF16 [T][H] = acc FP32, laid out [T][H] or (slice_rows = T) [H/256][T][256].
+cudaError_t launch_acc_to_bf16(const float* acc, int T, int H, int slice_rows, uint16_t* out, cudaStream_t s);
 // Whether n assignments over E experts take the weights-as-A GEMMs under an
 // orientation mode (TC_GEMM_*).
 bool tc_weights_as_a(int n, int E, int mode);
 // A8 on tensor cores
 // parts: split-K scratch, float [max(s1 * T * 2I, s2 * T * H)] (see shared_ksplit)
+// slice_rows = T: y_shared written by 256-column slices [H/256][T][256]
 cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
-                             float* y_shared, float* parts, int* status, uint64_t limit_ns, cudaStream_t s);
+                             float* y_shared, float* parts, int* status, uint64_t limit_ns, cudaStream_t s,
+                             int slice_rows = 0);
 // Copies the requantised h to sorted-assignment order (either layout).
 cudaError_t launch_copy_h(const Shape& sh, const int* hpath, const uint8_t* hq_sorted, const uint8_t* hs_sorted,
                           const TcWorkspace& w, uint8_t* hq_out, uint8_t* hs_out, cudaStream_t s);
@@ -123,7 +126,8 @@ struct Shared8Ws {
   uint8_t* w2s_mma;
 };
 cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const uint16_t* x, const Shared8Ws& w,
-                                   float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s);
+                                   float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s,
+                                   int slice_rows = 0);
 // A9
 cudaError_t launch_combine(const Shape& sh, const float* y_assign, const int* inv_perm, const float* w,
                            const float* y_shared, uint16_t* out, cudaStream_t s);

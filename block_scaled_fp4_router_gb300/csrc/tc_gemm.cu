@@ -222,6 +222,9 @@ struct GemmArgs {
   const float* topk_w;
   int k_top;
   int n_major;             // tiles ordered B tile first (every A tile of one output column slice in turn)
+  // EPI_STORE_F32 (one K part) / EPI_COMBINE_RED: out laid out by 256-column
+  // slices, [ldo / 256][slice_rows][256], when slice_rows > 0
+  int slice_rows;
   int* status;
   uint64_t limit_ns;
 };
@@ -414,6 +417,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
       int a_row, e, rows, srow0, nt, mti, kp;
       tile_coords(g, GROUPED, t, num_mt, a_row, e, rows, srow0, nt, mti, kp);
+      // the combine's assignment and routing weight of this thread's four
+      // rows, loaded while the tile's MMAs still run
+      int ra[4] = {0, 0, 0, 0};
+      float rw[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (EPI == EPI_COMBINE_RED) {
+        const int r0 = q * 32 + (lane >> 2);
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+          if (r0 + 8 * hh < rows) ra[hh] = __ldg(g.perm + srow0 + r0 + 8 * hh);
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+          if (r0 + 8 * hh < rows) rw[hh] = __ldg(g.topk_w + ra[hh]);
+      }
       if (!tc::mbar_wait(&acc_full, acc_phase, g.limit_ns, &abort_flag)) { fail(); break; }
       tc::fence_after_sync();
       float va[32], vb[32];
@@ -435,14 +451,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          va[i] = silu(va[i]) * vb[i];
+          va[i] = silu_fast(va[i]) * vb[i];
           amax = fmaxf(amax, fabsf(va[i]));
         }
         const int ex = mx_scale_exp(amax);
         const float inv = pow2_neg(ex);
-        uint32_t w[4] = {0, 0, 0, 0};
+        uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i >> 3] |= e2m1_rne(va[i] * inv) << (4 * (i & 7));
+        for (int j = 0; j < 4; ++j) w[j] = e2m1x8_rne(*reinterpret_cast<const float(*)[8]>(&va[8 * j]), inv);
         *reinterpret_cast<uint4*>(g.hq + (size_t)r * (g.h_cols / 2) + (nt * 128 + cq * 32) / 2) =
             make_uint4(w[0], w[1], w[2], w[3]);
         const int hgroups = g.h_cols / 128;
@@ -457,7 +473,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           float amax = 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            va[i] = silu(va[i]) * vb[i];
+            va[i] = silu_fast(va[i]) * vb[i];
             amax = fmaxf(amax, fabsf(va[i]));
           }
           const int ef = (int)((__float_as_uint(amax) >> 23) & 0xff);
@@ -479,10 +495,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 o;
-            o.x = f32_to_bf16_rn(silu(va[i + 0]) * vb[i + 0]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 1]) * vb[i + 1]) << 16);
-            o.y = f32_to_bf16_rn(silu(va[i + 2]) * vb[i + 2]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 3]) * vb[i + 3]) << 16);
-            o.z = f32_to_bf16_rn(silu(va[i + 4]) * vb[i + 4]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 5]) * vb[i + 5]) << 16);
-            o.w = f32_to_bf16_rn(silu(va[i + 6]) * vb[i + 6]) | ((uint32_t)f32_to_bf16_rn(silu(va[i + 7]) * vb[i + 7]) << 16);
+            o.x = f32_to_bf16_rn(silu_fast(va[i + 0]) * vb[i + 0]) | ((uint32_t)f32_to_bf16_rn(silu_fast(va[i + 1]) * vb[i + 1]) << 16);
+            o.y = f32_to_bf16_rn(silu_fast(va[i + 2]) * vb[i + 2]) | ((uint32_t)f32_to_bf16_rn(silu_fast(va[i + 3]) * vb[i + 3]) << 16);
+            o.z = f32_to_bf16_rn(silu_fast(va[i + 4]) * vb[i + 4]) | ((uint32_t)f32_to_bf16_rn(silu_fast(va[i + 5]) * vb[i + 5]) << 16);
+            o.w = f32_to_bf16_rn(silu_fast(va[i + 6]) * vb[i + 6]) | ((uint32_t)f32_to_bf16_rn(silu_fast(va[i + 7]) * vb[i + 7]) << 16);
             *reinterpret_cast<uint4*>(dst + i) = o;
           }
         }
@@ -495,14 +511,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int hh = 0; hh < 4; ++hh) {
           const int r = r0 + 8 * hh;  // hh: lanes +0, +8 (first load), +16, +24 (second)
           if (r < rows) {
-            const int a = __ldg(g.perm + srow0 + r);
-            const float wgt = __ldg(g.topk_w + a);
-            float* dst = g.out + (size_t)(a / g.k_top) * g.ldo + nt * BN + cq * 64 + 2 * (lane & 3);
+            const size_t tok = (size_t)(ra[hh] / g.k_top);
+            float* dst = (g.slice_rows ? g.out + ((size_t)nt * g.slice_rows + tok) * BN
+                                       : g.out + tok * g.ldo + nt * BN) + cq * 64 + 2 * (lane & 3);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float* v = hh < 2 ? va : vb;
               const int o = 4 * j + 2 * (hh & 1);
-              red_add_f32x2(dst + 8 * j, wgt * v[o], wgt * v[o + 1]);
+              red_add_f32x2(dst + 8 * j, rw[hh] * v[o], rw[hh] * v[o + 1]);
             }
           }
         }
@@ -510,12 +526,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // Four threads share a row, so each warp store fills eight whole
         // 32-byte sectors (a row-per-thread store fills 32 half sectors).
         const int r0 = q * 32 + (lane >> 2);
-        float* base = g.out + kp * g.part_stride + (size_t)srow0 * g.ldo + nt * BN + cq * 64 + 2 * (lane & 3);
+        const bool sl = g.slice_rows > 0;
+        float* base = (sl ? g.out + ((size_t)nt * g.slice_rows + srow0) * BN
+                          : g.out + kp * g.part_stride + (size_t)srow0 * g.ldo + nt * BN) + cq * 64 + 2 * (lane & 3);
+        const size_t rstride = sl ? (size_t)BN : (size_t)g.ldo;
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {
           const int r = r0 + 8 * hh;  // hh: lanes +0, +8 (first load), +16, +24 (second)
           if (r < rows) {
-            float* dst = base + (size_t)r * g.ldo;
+            float* dst = base + (size_t)r * rstride;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float* v = hh < 2 ? va : vb;
@@ -718,7 +737,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint8_t* hs = reinterpret_cast<uint8_t*>(g.hs) + ((size_t)(m.prow0 / WA_WIN) * hgroups + nt) * 512;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float h = silu(va[j]) * vb[j];
+          const float h = silu_fast(va[j]) * vb[j];
           float amax = fabsf(h);
 #pragma unroll
           for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -980,6 +999,7 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
     g2.topk_w = comb->topk_w;
     g2.k_top = sh.k;
     g2.n_major = 1;
+    g2.slice_rows = comb->slice_rows;
     err = launch_gemm<KIND_FP4, EPI_COMBINE_RED, true>(ma, mb, g2, max_mt * g2.n_tiles, s);
   } else {
     err = launch_gemm<KIND_FP4, EPI_STORE_F32, true>(ma, mb, g2, max_mt * g2.n_tiles, s);
@@ -991,12 +1011,18 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
 
 namespace {
 
-// out[i] = BF16(acc[i]), four elements per thread.
-__global__ void __launch_bounds__(256) k_acc_to_bf16(const float* __restrict__ acc, size_t n4,
+// out[t][c] = BF16(acc at (t, c)), four consecutive columns per thread; acc
+// row-major [T][H] or (slice_rows = T) by 256-column slices [H/256][T][256].
+__global__ void __launch_bounds__(256) k_acc_to_bf16(const float* __restrict__ acc, size_t n4, int H, int slice_rows,
                                                      uint16_t* __restrict__ out) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n4) return;
-  const float4 v = __ldcs(reinterpret_cast<const float4*>(acc) + i);
+  size_t src = i;
+  if (slice_rows) {
+    const size_t t = i / (H / 4), c = (i % (H / 4)) * 4;
+    src = ((c / 256) * slice_rows + t) * 64 + (c % 256) / 4;
+  }
+  const float4 v = __ldcs(reinterpret_cast<const float4*>(acc) + src);
   uint2 o;
   o.x = (uint32_t)f32_to_bf16_rn(v.x) | ((uint32_t)f32_to_bf16_rn(v.y) << 16);
   o.y = (uint32_t)f32_to_bf16_rn(v.z) | ((uint32_t)f32_to_bf16_rn(v.w) << 16);
@@ -1005,10 +1031,10 @@ __global__ void __launch_bounds__(256) k_acc_to_bf16(const float* __restrict__ a
 
 }  // namespace
 
-cudaError_t launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s) {
-  const size_t n4 = n / 4;
+cudaError_t launch_acc_to_bf16(const float* acc, int T, int H, int slice_rows, uint16_t* out, cudaStream_t s) {
+  const size_t n4 = (size_t)T * H / 4;
   if (n4 == 0) return cudaSuccess;
-  count_launch(), k_acc_to_bf16<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(acc, n4, out);
+  count_launch(), k_acc_to_bf16<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(acc, n4, H, slice_rows, out);
   return cudaGetLastError();
 }
 
@@ -1037,9 +1063,11 @@ __global__ void __launch_bounds__(256) k_swiglu_parts(const float* __restrict__ 
   *reinterpret_cast<uint2*>(h + i) = o;
 }
 
-// out[i] = sum of parts [S][n] at i, four elements per thread.
-__global__ void __launch_bounds__(256) k_sum_parts(const float* __restrict__ parts, int S, size_t n,
-                                                   float* __restrict__ out) {
+// out[i] = sum of parts [S][n] at i, four elements per thread; with
+// slice_rows = T the parts are [S][T][H] and out is laid out by 256-column
+// slices, [H/256][T][256].
+__global__ void __launch_bounds__(256) k_sum_parts(const float* __restrict__ parts, int S, size_t n, int H,
+                                                   int slice_rows, float* __restrict__ out) {
   const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i >= n) return;
   float4 v = *reinterpret_cast<const float4*>(parts + i);
@@ -1047,13 +1075,18 @@ __global__ void __launch_bounds__(256) k_sum_parts(const float* __restrict__ par
     const float4 a = *reinterpret_cast<const float4*>(parts + p * n + i);
     v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
   }
-  *reinterpret_cast<float4*>(out + i) = v;
+  size_t dst = i;
+  if (slice_rows) {
+    const size_t t = i / H, c = i % H;
+    dst = ((c / 256) * slice_rows + t) * 256 + c % 256;
+  }
+  *reinterpret_cast<float4*>(out + dst) = v;
 }
 
 }  // namespace
 
 cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const uint16_t* x, const Shared8Ws& w,
-                                   float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s) {
+                                   float* y_shared, int* status, uint64_t limit_ns, cudaStream_t s, int slice_rows) {
   const int T = sh.T, H = sh.H, I = sh.I;
   if (T == 0) return cudaSuccess;
   const int mt = (T + BM - 1) / BM;
@@ -1104,13 +1137,15 @@ cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const
   g2.sfb_rtiles = H / BM;
   g2.out = y_shared;
   g2.ldo = H;
+  g2.slice_rows = slice_rows;
   g2.status = status;
   g2.limit_ns = limit_ns;
   return launch_gemm<KIND_FP8, EPI_STORE_F32, false>(ma, mb, g2, mt * g2.n_tiles, s);
 }
 
 cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
-                             float* y_shared, float* parts, int* status, uint64_t limit_ns, cudaStream_t s) {
+                             float* y_shared, float* parts, int* status, uint64_t limit_ns, cudaStream_t s,
+                             int slice_rows) {
   const int T = sh.T, H = sh.H, I = sh.I;
   if (T == 0) return cudaSuccess;
   const int mt = (T + BM - 1) / BM;
@@ -1165,6 +1200,7 @@ cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16
   g2.rows_dense = T;
   g2.out = s2 > 1 ? parts : y_shared;
   g2.ldo = H;
+  g2.slice_rows = s2 > 1 ? 0 : slice_rows;
   g2.ksplit = s2;
   g2.part_stride = (size_t)T * H;
   g2.status = status;
@@ -1173,7 +1209,8 @@ cudaError_t launch_shared_tc(const Shape& sh, const SharedDev& shd, const uint16
     return err;
   if (s2 > 1) {
     const size_t n = (size_t)T * H;
-    count_launch(), k_sum_parts<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(parts, s2, n, y_shared);
+    count_launch(), k_sum_parts<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(parts, s2, n, H, slice_rows,
+                                                                               y_shared);
     return cudaGetLastError();
   }
   return cudaSuccess;
