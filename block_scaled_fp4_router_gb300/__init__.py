@@ -14,6 +14,8 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoefp4.so")
+# the checked build (out-of-range caller indices recorded in the status word)
+CHECKED_LIB_PATH = os.path.join(_HERE, "libmoefp4_checked.so")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -76,11 +78,14 @@ class SharedBF16(ctypes.Structure):
 _lib = None
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libmoefp4.so (raises if it has not been built)."""
+def load(path: str = None) -> ctypes.CDLL:
+    """Load libmoefp4.so (raises if it has not been built); with
+    MOEFP4_CHECKED=1 in the environment, the checked build instead."""
     global _lib
     if _lib is not None:
         return _lib
+    if path is None:
+        path = CHECKED_LIB_PATH if os.environ.get("MOEFP4_CHECKED") == "1" else LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(
             "libmoefp4.so is not built (expected at %s); run "

@@ -2,6 +2,7 @@
 // on the host, workspace carving, and the launch sequences of the unfused and
 // fused layer paths.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 
@@ -13,6 +14,14 @@
 using namespace moefp4;
 
 namespace {
+
+// An NVTX range over one entry point (named after it in profiler timelines;
+// without an attached tool the push and pop do nothing).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+};
+#define MOE_RANGE() const Range moe_range_(__func__)
 
 std::atomic<uint64_t> g_wait_limit_ns{500ull * 1000 * 1000};
 std::atomic<int> g_routed_gemm{TC_GEMM_AUTO};
@@ -184,7 +193,7 @@ moe_status_t run_expert_ffn(const moe_layer_desc_t* d, const ExpertsDev& ex, con
                                   fuse ? &comb : nullptr));
   } else {
     MOE_CUDA(launch_routed_simt(sh, ex, xq, xs, offsets, perm, at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs),
-                                y_assign, s));
+                                y_assign, s, status));
   }
   if (has_shared && !fuse) MOE_TRY(shared_expert(y_shared, 0));
   return MOE_OK;
@@ -222,7 +231,8 @@ moe_status_t run_forward(const moe_layer_desc_t* desc, const ExpertsDev& ex, con
                          &fused, sh8, &slice));
   if (fused)  // the combine ran in the down GEMM: the FP32 output is rounded to BF16
     return cuda_status(launch_acc_to_bf16(at<float>(ws, L.y_shared), sh.T, sh.H, slice, out, s));
-  return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh, out, s));
+  return cuda_status(launch_combine(sh, at<float>(ws, L.y_assign), at<int>(ws, L.inv_perm), w, ysh, out, s,
+                                    at<int>(ws, L.counters) + C_STATUS));
 }
 
 }  // namespace
@@ -268,6 +278,7 @@ const char* moe_status_string(moe_status_t st) {
 }
 
 moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* bytes) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   if (!bytes) return MOE_ERR_INVALID_ARG;
   *bytes = layout_of(desc).total;
@@ -275,6 +286,7 @@ moe_status_t moe_workspace_size(const moe_layer_desc_t* desc, size_t* bytes) {
 }
 
 moe_status_t moe_get_status(void* ws, moe_status_t* st) {
+  MOE_RANGE();
   if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
   if (!st) return MOE_ERR_INVALID_ARG;
   int v = 0;
@@ -287,6 +299,7 @@ moe_status_t moe_get_status(void* ws, moe_status_t* st) {
 
 moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts_t* experts, uint8_t* w13_scale_mma,
                                  uint8_t* w2_scale_mma, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   const moe_layer_desc_t t = table_desc(desc);  // every expert of the table, a folded shared one included
   ExpertsDev ex;
@@ -307,6 +320,7 @@ moe_status_t moe_prepare_weights(const moe_layer_desc_t* desc, const moe_experts
 moe_status_t moe_convert_nvfp4_to_mxfp4(const moe_layer_desc_t* desc, const moe_experts_t* experts,
                                         uint8_t* w13_out, uint8_t* w13_scale_out, uint8_t* w2_out,
                                         uint8_t* w2_scale_out, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   const moe_layer_desc_t t = table_desc(desc);
   ExpertsDev ex;
@@ -320,6 +334,7 @@ moe_status_t moe_convert_nvfp4_to_mxfp4(const moe_layer_desc_t* desc, const moe_
 
 moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes, uint8_t* hq,
                                      uint8_t* hs, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, const_cast<void*>(ws), ws_bytes));
@@ -335,6 +350,7 @@ moe_status_t moe_debug_requantized_h(const moe_layer_desc_t* desc, const void* w
 }
 
 moe_status_t moe_copy_rows(void* dst, const void* src, size_t bytes, moe_stream_t stream) {
+  MOE_RANGE();
   if (bytes == 0) return MOE_OK;
   if (!dst || !src || bytes % 16 || !aligned(dst, 16) || !aligned(src, 16)) return MOE_ERR_INVALID_ARG;
   // only memory the GPU addresses: device, managed, or pinned host memory
@@ -360,18 +376,21 @@ moe_status_t moe_copy_rows(void* dst, const void* src, size_t bytes, moe_stream_
 void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 
 moe_status_t moe_set_routed_gemm(int32_t mode) {
+  MOE_RANGE();
   if (mode < TC_GEMM_AUTO || mode > TC_GEMM_WEIGHTS_AS_A) return MOE_ERR_INVALID_ARG;
   g_routed_gemm.store(mode);
   return MOE_OK;
 }
 
 moe_status_t moe_debug_wait_probe(void* ws, size_t ws_bytes, uint64_t limit_ns, moe_stream_t stream) {
+  MOE_RANGE();
   if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(int) * N_COUNTERS) return MOE_ERR_WORKSPACE;
   return cuda_status(launch_wait_probe(ws, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_quant_act_mxfp4(int32_t rows, int32_t K, const void* x, uint8_t* codes, uint8_t* scales,
                                  moe_stream_t stream) {
+  MOE_RANGE();
   if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4)) return MOE_ERR_INVALID_ARG;
@@ -381,6 +400,7 @@ moe_status_t moe_quant_act_mxfp4(int32_t rows, int32_t K, const void* x, uint8_t
 
 moe_status_t moe_quant_act_mxfp8(int32_t rows, int32_t K, const void* x, uint8_t* codes, uint8_t* scales,
                                  moe_stream_t stream) {
+  MOE_RANGE();
   if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 8)) return MOE_ERR_INVALID_ARG;
@@ -390,6 +410,7 @@ moe_status_t moe_quant_act_mxfp8(int32_t rows, int32_t K, const void* x, uint8_t
 
 moe_status_t moe_dequant_mxfp8_to_bf16(int32_t rows, int32_t K, const uint8_t* codes, const uint8_t* scales,
                                        void* out, moe_stream_t stream) {
+  MOE_RANGE();
   if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!codes || !scales || !out || !aligned(codes, 8) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
@@ -400,6 +421,7 @@ moe_status_t moe_dequant_mxfp8_to_bf16(int32_t rows, int32_t K, const uint8_t* c
 moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const float* w_router,
                              const float* bias, int32_t* topk_ids, float* topk_w, float* logits,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));
@@ -418,6 +440,7 @@ moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const 
 moe_status_t moe_permute(const moe_layer_desc_t* desc, const int32_t* topk_ids, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes,
                          moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));
@@ -425,7 +448,7 @@ moe_status_t moe_permute(const moe_layer_desc_t* desc, const int32_t* topk_ids, 
   const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
   return cuda_status(launch_permute(topk_ids, desc->T, desc->top_k, desc->E, counts, offsets, perm, inv_perm,
                                     at<int>(ws, L.rank), at<int>(ws, L.chunk_cnt), at<int>(ws, L.chunk_base),
-                                    reinterpret_cast<cudaStream_t>(stream)));
+                                    reinterpret_cast<cudaStream_t>(stream), at<int>(ws, L.counters) + C_STATUS));
 }
 
 moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_t* experts,
@@ -433,6 +456,7 @@ moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_
                                 const uint8_t* xs, const int32_t* offsets, const int32_t* perm,
                                 float* y_assign, float* y_shared, void* ws, size_t ws_bytes,
                                 moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));
@@ -451,6 +475,7 @@ moe_status_t moe_expert_ffn_fp4(const moe_layer_desc_t* desc, const moe_experts_
 
 moe_status_t moe_shared_expert_mxfp8(const moe_layer_desc_t* desc, const moe_shared_mxfp8_t* shared,
                                      const void* x, float* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   if (desc->H % 256 || desc->I % 256) return MOE_ERR_UNSUPPORTED;
@@ -474,6 +499,7 @@ moe_status_t moe_shared_expert_mxfp8(const moe_layer_desc_t* desc, const moe_sha
 
 moe_status_t moe_prepare_shared_mxfp8(const moe_layer_desc_t* desc, const moe_shared_mxfp8_t* shared,
                                       uint8_t* w13_scale_mma, uint8_t* w2_scale_mma, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   Shared8Dev sh8;
   MOE_TRY(check_shared8(desc, shared, &sh8));
@@ -486,6 +512,7 @@ moe_status_t moe_prepare_shared_mxfp8(const moe_layer_desc_t* desc, const moe_sh
 
 moe_status_t moe_debug_shared_mxfp8_h(const moe_layer_desc_t* desc, const void* ws, size_t ws_bytes, uint8_t* hq,
                                       uint8_t* hs, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   MOE_TRY(check_ws(desc, const_cast<void*>(ws), ws_bytes));
   if (desc->T == 0) return MOE_OK;
@@ -502,6 +529,7 @@ moe_status_t moe_layer_forward_shared_mxfp8(const moe_layer_desc_t* desc, const 
                                             const moe_shared_mxfp8_t* shared, const float* w_router,
                                             const float* bias, const void* x, void* out, int32_t* topk_ids,
                                             float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   MOE_TRY(check_ws(desc, ws, ws_bytes));
   ExpertsDev ex;
@@ -517,6 +545,7 @@ moe_status_t moe_layer_forward_shared_mxfp8(const moe_layer_desc_t* desc, const 
 
 moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_assign, const int32_t* inv_perm,
                          const float* topk_w, const float* y_shared, void* out, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   if (desc->shared_in_table) return MOE_ERR_UNSUPPORTED;
   if (desc->T == 0) return MOE_OK;
@@ -531,6 +560,7 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t* desc, const moe_experts_t
                                const moe_shared_bf16_t* shared, const float* w_router, const float* bias,
                                const void* x, void* out, int32_t* topk_ids, float* topk_w, void* ws,
                                size_t ws_bytes, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   MOE_TRY(check_ws(desc, ws, ws_bytes));
   const moe_layer_desc_t dt = table_desc(desc);
@@ -550,6 +580,7 @@ moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t*
                               const moe_shared_bf16_t* shared, const float* w_router, const float* bias,
                               const void* x, void* out, int32_t* topk_ids, float* topk_w, void* ws,
                               size_t ws_bytes, moe_stream_t stream) {
+  MOE_RANGE();
   MOE_TRY(check_desc(desc));
   if (desc->T > MAX_DECODE_T) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));

@@ -211,6 +211,16 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Checked builds (compiled with MOEFP4_CHECKED=1) record a caller-given index
+// that is out of range as MOE_ERR_INVALID_ARG in the status word; every build
+// leaves such an index out (no access through it).
+#ifndef MOEFP4_CHECKED
+#define MOEFP4_CHECKED 0
+#endif
+__device__ __forceinline__ void report_bad_index(int* status) {
+  if (MOEFP4_CHECKED && status) atomicCAS(status, 0, (int)MOE_DEV_INVALID);
+}
+
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 // SiLU for the batched GEMM epilogues, where it runs on every element of the

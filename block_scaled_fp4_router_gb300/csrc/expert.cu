@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(THREADS) k_routed_gate_up(Shape sh, ExpertsDev
                                                             const int* __restrict__ offsets,
                                                             const int* __restrict__ perm,
                                                             uint8_t* __restrict__ hq,
-                                                            uint8_t* __restrict__ hs) {
+                                                            uint8_t* __restrict__ hs, int* __restrict__ status) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int e = blockIdx.x, b = blockIdx.y;
   const int H = sh.H, I = sh.I, na = sh.T * sh.k;
@@ -48,8 +48,10 @@ __global__ void __launch_bounds__(THREADS) k_routed_gate_up(Shape sh, ExpertsDev
   for (int t0 = 0; t0 < n; t0 += NT) {
     const int nt = min(NT, n - t0);
     if (threadIdx.x < nt) {
-      const int tok = perm[p0 + t0 + threadIdx.x] / sh.k;
-      rows_s[threadIdx.x] = (tok >= 0 && tok < sh.T) ? tok : 0;
+      const int a = perm[p0 + t0 + threadIdx.x];
+      const bool ok = a >= 0 && a < na;
+      if (!ok) report_bad_index(status);
+      rows_s[threadIdx.x] = ok ? a / sh.k : 0;
     }
     __syncthreads();
     stage_mx_rows(xq, xs, H, rows_s, nt, xq_s, xsc_s, false);
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(256) k_combine(Shape sh, const float* __restri
                                                  const int* __restrict__ inv_perm,
                                                  const float* __restrict__ w,
                                                  const float* __restrict__ y_shared,
-                                                 uint16_t* __restrict__ out) {
+                                                 uint16_t* __restrict__ out, int* __restrict__ status) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t q = (size_t)sh.H / 4;
   if (i >= (size_t)sh.T * q) return;
@@ -213,7 +215,10 @@ __global__ void __launch_bounds__(256) k_combine(Shape sh, const float* __restri
   for (int j = 0; j < sh.k; ++j) {
     const float wj = w[(size_t)t * sh.k + j];
     int p = inv_perm[(size_t)t * sh.k + j];
-    p = (p >= 0 && p < sh.T * sh.k) ? p : 0;
+    if (p < 0 || p >= sh.T * sh.k) {
+      report_bad_index(status);
+      p = 0;
+    }
     const float4 y = *reinterpret_cast<const float4*>(y_assign + (size_t)p * sh.H + h);
     acc.x = fmaf(wj, y.x, acc.x);
     acc.y = fmaf(wj, y.y, acc.y);
@@ -227,10 +232,11 @@ __global__ void __launch_bounds__(256) k_combine(Shape sh, const float* __restri
 }
 
 cudaError_t launch_combine(const Shape& sh, const float* y_assign, const int* inv_perm, const float* w,
-                           const float* y_shared, uint16_t* out, cudaStream_t s) {
+                           const float* y_shared, uint16_t* out, cudaStream_t s, int* status) {
   const size_t n = (size_t)sh.T * sh.H / 4;
   if (n == 0) return cudaSuccess;
-  count_launch(), k_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(sh, y_assign, inv_perm, w, y_shared, out);
+  count_launch(), k_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(sh, y_assign, inv_perm, w, y_shared, out,
+                                                                        status);
   return cudaGetLastError();
 }
 
@@ -242,7 +248,7 @@ static cudaError_t set_smem(const void* fn, size_t bytes) {
 
 cudaError_t launch_routed_simt(const Shape& sh, const ExpertsDev& ex, const uint8_t* xq, const uint8_t* xs,
                                const int* offsets, const int* perm, uint8_t* hq, uint8_t* hs, float* y_assign,
-                               cudaStream_t s) {
+                               cudaStream_t s, int* status) {
   if (sh.T == 0) return cudaSuccess;
   cudaError_t err;
   const int H = sh.H, I = sh.I;
@@ -253,9 +259,10 @@ cudaError_t launch_routed_simt(const Shape& sh, const ExpertsDev& ex, const uint
     if ((err = set_smem(fn, smem)) != cudaSuccess) return err;
     dim3 grid(sh.E, I / 32);
     if (ex.nv)
-      count_launch(), k_routed_gate_up<true><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs);
+      count_launch(), k_routed_gate_up<true><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs, status);
     else
-      count_launch(), k_routed_gate_up<false><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs);
+      count_launch(), k_routed_gate_up<false><<<grid, THREADS, smem, s>>>(sh, ex, xq, xs, offsets, perm, hq, hs,
+                                                                          status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   {

@@ -53,12 +53,14 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int score, const float* sel_bias, int* ids,
                         float* w, cudaStream_t s, int* ids_ext = nullptr, float* w_ext = nullptr);
 // A3
+// status: where a checked build records an out-of-range id (may be null)
 cudaError_t launch_permute(const int* ids, int T, int k, int E, int* counts, int* offsets, int* perm,
-                           int* inv_perm, int* rank, int* chunk_cnt, int* chunk_base, cudaStream_t s);
+                           int* inv_perm, int* rank, int* chunk_cnt, int* chunk_base, cudaStream_t s,
+                           int* status = nullptr);
 // A5 - A7 on CUDA cores (any T; the decode-sized path)
 cudaError_t launch_routed_simt(const Shape& sh, const ExpertsDev& ex, const uint8_t* xq, const uint8_t* xs,
                                const int* offsets, const int* perm, uint8_t* hq, uint8_t* hs, float* y_assign,
-                               cudaStream_t s);
+                               cudaStream_t s, int* status = nullptr);
 // A8 on CUDA cores
 cudaError_t launch_shared_simt(const Shape& sh, const SharedDev& shd, const uint16_t* x, uint16_t* h_shared,
                                float* y_shared, cudaStream_t s);
@@ -130,7 +132,7 @@ cudaError_t launch_shared_mxfp8_tc(const Shape& sh, const Shared8Dev& sh8, const
                                    int slice_rows = 0);
 // A9
 cudaError_t launch_combine(const Shape& sh, const float* y_assign, const int* inv_perm, const float* w,
-                           const float* y_shared, uint16_t* out, cudaStream_t s);
+                           const float* y_shared, uint16_t* out, cudaStream_t s, int* status = nullptr);
 // A10 on CUDA cores: needs H and I multiples of 64 (rows streamed in
 // 64-element pairs by 32-byte loads).
 inline bool fused_decode_supported(const Shape& sh) {

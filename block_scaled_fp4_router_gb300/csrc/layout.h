@@ -112,6 +112,7 @@ MOE_HD inline bool tc_routed_enabled(int n) { return n >= TC_MIN_ASSIGN; }
 
 // Device status word values (mirror moe_status_t).
 constexpr int MOE_DEV_OK = 0;
+constexpr int MOE_DEV_INVALID = 1;  // a caller-given index out of range (checked builds)
 constexpr int MOE_DEV_TIMEOUT = 4;
 
 // Counters of the fused decode launch (ints at the start of the workspace).

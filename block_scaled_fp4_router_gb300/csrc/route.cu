@@ -399,7 +399,7 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int score, con
 // across warps a per-expert exclusive scan over the 32 warp counts.
 __global__ void __launch_bounds__(PERM_CHUNK) k_perm_rank(const int* __restrict__ ids, int n, int E,
                                                           int* __restrict__ rank,
-                                                          int* __restrict__ chunk_cnt) {
+                                                          int* __restrict__ chunk_cnt, int* __restrict__ status) {
   __shared__ int wc[32][MAX_E];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < 32 * MAX_E; i += blockDim.x) (&wc[0][0])[i] = 0;
@@ -407,6 +407,7 @@ __global__ void __launch_bounds__(PERM_CHUNK) k_perm_rank(const int* __restrict_
   const int a = blockIdx.x * PERM_CHUNK + threadIdx.x;
   const int e0 = a < n ? ids[a] : -1;
   const int e = (e0 >= 0 && e0 < E) ? e0 : -1;  // out-of-range ids are left out
+  if (a < n && e < 0) report_bad_index(status);
   const uint32_t peers = __match_any_sync(FULL, e);
   const int r = __popc(peers & ((1u << lane) - 1));
   if (e >= 0 && r == 0) wc[warp][e] = __popc(peers);
@@ -470,11 +471,11 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int* __restrict__ id
 }
 
 cudaError_t launch_permute(const int* ids, int T, int k, int E, int* counts, int* offsets, int* perm,
-                           int* inv_perm, int* rank, int* chunk_cnt, int* chunk_base, cudaStream_t s) {
+                           int* inv_perm, int* rank, int* chunk_cnt, int* chunk_base, cudaStream_t s, int* status) {
   const int n = T * k;
   const int nchunks = (n + PERM_CHUNK - 1) / PERM_CHUNK;
   if (nchunks > 0) {
-    count_launch(), k_perm_rank<<<nchunks, PERM_CHUNK, 0, s>>>(ids, n, E, rank, chunk_cnt);
+    count_launch(), k_perm_rank<<<nchunks, PERM_CHUNK, 0, s>>>(ids, n, E, rank, chunk_cnt, status);
   }
   count_launch(), k_perm_scan<<<1, MAX_E, 0, s>>>(chunk_cnt, nchunks, E, chunk_base, counts, offsets);
   if (n > 0) count_launch(), k_perm_scatter<<<(n + 255) / 256, 256, 0, s>>>(ids, n, E, rank, chunk_base, offsets, perm, inv_perm);

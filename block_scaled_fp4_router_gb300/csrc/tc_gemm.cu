@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(128) k_gather_mx_rows(const uint8_t* __restric
                                                         int K, int k_top, const int* __restrict__ perm,
                                                         const MTile* __restrict__ tiles, const int* __restrict__ num_tiles,
                                                         int win, int rows16, uint8_t* __restrict__ q_out,
-                                                        uint32_t* __restrict__ sf_out) {
+                                                        uint32_t* __restrict__ sf_out, int n_assign,
+                                                        int* __restrict__ status) {
   const int r0 = blockIdx.x * GR;
   if (r0 >= *num_tiles * win) return;
   const MTile t = tiles[r0 / win];
@@ -145,7 +146,9 @@ __global__ void __launch_bounds__(128) k_gather_mx_rows(const uint8_t* __restric
 #pragma unroll
   for (int i = 0; i < GR; ++i) {
     const int m = r0 % win + i;
-    src[i] = m < t.rows ? perm[t.srow0 + m] / k_top : -1;
+    const int a = m < t.rows ? perm[t.srow0 + m] : -1;
+    if (m < t.rows && (a < 0 || a >= n_assign)) report_bad_index(status);
+    src[i] = (a >= 0 && a < n_assign) ? a / k_top : -1;  // out-of-range assignments read as zeros
   }
   const int cpr = K / 32;  // 16-byte chunks per row
   for (int c = threadIdx.x; c < cpr; c += blockDim.x) {
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- producer
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
     // grouped: each tile's MTile is loaded a tile ahead, off the stream's critical path
     auto mt_of = [&](int t) { return GROUPED && t < total ? g.mt[mti_of(g, t, num_mt)] : MTile{}; };
     MTile mn = mt_of(blockIdx.x);
@@ -323,6 +326,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
         uint8_t* sa = dsm + stage * SB;
         uint8_t* sb = sa + A_BYTES;
+        issued |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         tc::mbar_expect_tx(&full[stage], stage_tx(KIND));
         tc::tma_load_2d(sa, &mapA, ks * 128, a_row, &full[stage]);
         tc::tma_load_2d(sb, &mapB, ks * 128, b0, &full[stage]);
@@ -349,6 +354,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
     }
+    // no copy of this block may still be landing in its shared memory when it
+    // exits (after an abort the consumer may not have waited for them): wait,
+    // bounded but regardless of the abort flag, for the last copy of each stage
+    const int never = 0;
+    for (int s2 = 0; s2 < STAGES; ++s2)
+      if ((issued >> s2 & 1) && !tc::mbar_wait(&full[s2], last_parity >> s2 & 1, g.limit_ns, &never)) fail();
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
     uint32_t stage = 0, phase = 0, acc_phase = 0;
@@ -404,9 +415,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc::mma_commit(&acc_full);
       acc_phase ^= 1;
     }
-    // wait (bounded) for every MMA this thread issued before TMEM is released
+    // wait (bounded, regardless of the abort flag) for every MMA this thread
+    // issued before TMEM is released
+    const int never = 0;
     tc::mma_commit(&drain);
-    if (!tc::mbar_wait(&drain, 0, g.limit_ns, &abort_flag)) fail();
+    if (!tc::mbar_wait(&drain, 0, g.limit_ns, &never)) fail();
   } else if (warp >= 2) {
     // ---------------- epilogue: thread <-> accumulator row m, column quarter cq
     const int q = warp & 3;          // TMEM lane quadrant this warp may read
@@ -633,7 +646,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- producer
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
     MTile mn = (int)blockIdx.x < total ? g.mt[blockIdx.x / g.n_tiles] : MTile{};
     for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
       const int nt = t % g.n_tiles;
@@ -649,6 +662,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int ks = 0; ks < nks; ++ks) {
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, g.limit_ns, &abort_flag)) { fail(); break; }
         uint8_t* st = dsm + stage * SB;
+        issued |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         tc::mbar_expect_tx(&full[stage], bytes);
         tc::tma_load_2d(st, &mapW, ks * 128, wr0, &full[stage]);
         if (SWIGLU) tc::tma_load_2d(st + A_BYTES, &mapW, ks * 128, wr0 + g.b_up_off, &full[stage]);
@@ -660,6 +675,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (++stage == NS) { stage = 0; phase ^= 1; }
       }
     }
+    // the last copy of each stage has landed before the block may exit
+    const int never = 0;
+    for (int s2 = 0; s2 < NS; ++s2)
+      if ((issued >> s2 & 1) && !tc::mbar_wait(&full[s2], last_parity >> s2 & 1, g.limit_ns, &never)) fail();
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
     uint32_t stage = 0, phase = 0;
@@ -705,8 +724,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (!ok) break;
       tc::mma_commit(&acc_full[buf]);
     }
+    const int never = 0;
     tc::mma_commit(&drain);
-    if (!tc::mbar_wait(&drain, 0, g.limit_ns, &abort_flag)) fail();
+    if (!tc::mbar_wait(&drain, 0, g.limit_ns, &never)) fail();
   } else if (warp >= 2) {
     // ---------------- epilogue: lane <-> weight row 32q + lane, token columns 16cq .. 16cq + 15
     const int q = warp & 3;
@@ -902,7 +922,7 @@ cudaError_t launch_expert_ffn_tc(const Shape& sh, const ExpertsDev& ex, const Tc
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   count_launch(), k_gather_mx_rows<<<rmax / GR, 128, 0, s>>>(xq, xs, H, sh.k, perm, reinterpret_cast<const MTile*>(w.mtiles),
                                              w.num_mt, win, wa ? 1 : 0, w.xq_perm,
-                                             reinterpret_cast<uint32_t*>(w.xs_mma));
+                                             reinterpret_cast<uint32_t*>(w.xs_mma), n, status);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const uint8_t* w13s_mma = ex.w13s_mma;
   const uint8_t* w2s_mma = ex.w2s_mma;

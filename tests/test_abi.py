@@ -37,6 +37,16 @@ def test_every_declared_symbol_is_exported(lib):
     assert declared == set(M.EXPORTED)
 
 
+def test_checked_build_exports_the_same_entry_points():
+    """The checked variant (MOEFP4_CHECKED=1) builds and exports exactly the
+    entry points of the header."""
+    path = B.build(checked=True)
+    assert path == M.CHECKED_LIB_PATH and os.path.exists(path)
+    chk = ctypes.CDLL(path)
+    for name in _declared():
+        assert hasattr(chk, name), name
+
+
 def test_status_strings(lib):
     for code, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARG"), (2, "MOE_ERR_UNSUPPORTED"),
                        (3, "MOE_ERR_CUDA"), (4, "MOE_ERR_TIMEOUT"), (5, "MOE_ERR_WORKSPACE")]:
