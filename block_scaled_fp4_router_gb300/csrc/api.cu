@@ -216,7 +216,8 @@ moe_status_t run_forward(const moe_layer_desc_t* desc, const ExpertsDev& ex, con
   int* ids = fold ? at<int>(ws, L.ids) : ids_r;  // [T][table k]
   float* w = fold ? at<float>(ws, L.wts) : w_r;
   MOE_CUDA(launch_router_logits(xb, w_router, logit_bias(desc, bias), at<float>(ws, L.logits), desc->T, desc->H,
-                                desc->E, at<float>(ws, L.rt_part), s));
+                                desc->E, at<float>(ws, L.rt_part), s, at<uint16_t>(ws, L.rt_wsplit),
+                                at<int>(ws, L.counters) + C_STATUS, g_wait_limit_ns.load()));
   MOE_CUDA(launch_topk(at<float>(ws, L.logits), desc->T, desc->E, desc->top_k, desc->score_func,
                        select_bias(desc, bias), ids_r, w_r, s, fold ? ids : nullptr, fold ? w : nullptr));
   MOE_CUDA(launch_quant_mxfp4(xb, sh.T, sh.H, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs), s));
@@ -432,7 +433,8 @@ moe_status_t moe_router_topk(const moe_layer_desc_t* desc, const void* x, const 
   const WsLayout L = ws_layout(desc->T, desc->H, desc->I, desc->E, desc->top_k);
   float* lg = logits ? logits : at<float>(ws, L.logits);
   MOE_CUDA(launch_router_logits(static_cast<const uint16_t*>(x), w_router, logit_bias(desc, bias), lg, desc->T,
-                                desc->H, desc->E, at<float>(ws, L.rt_part), s));
+                                desc->H, desc->E, at<float>(ws, L.rt_part), s, at<uint16_t>(ws, L.rt_wsplit),
+                                at<int>(ws, L.counters) + C_STATUS, g_wait_limit_ns.load()));
   return cuda_status(launch_topk(lg, desc->T, desc->E, desc->top_k, desc->score_func, select_bias(desc, bias),
                                  topk_ids, topk_w, s));
 }

@@ -43,9 +43,16 @@ cudaError_t launch_quant_mxfp4(const uint16_t* x, int rows, int K, uint8_t* code
 // A4 for the MXFP8 shared expert: E4M3 codes [rows][K], E8M0 scales [rows][K/32].
 cudaError_t launch_quant_mxfp8(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t s);
-// A1
+// A1.  part: [router_splits][T][E].  With wsplit ([3][E][H] BF16 scratch) and
+// a shape router_tc_supported accepts, the products run on tensor cores
+// (three BF16 terms of the weights, 64-element K chunks summed in FP32).
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
-                                 int T, int H, int E, float* part, cudaStream_t s);  // part: [router_splits][T][E]
+                                 int T, int H, int E, float* part, cudaStream_t s, uint16_t* wsplit = nullptr,
+                                 int* status = nullptr, uint64_t limit_ns = 0);
+bool router_tc_supported(int T, int H, int E);
+int router_tc_splits(int T, int H, int E);
+cudaError_t launch_router_tc(const uint16_t* x, const float* wr, const float* bias, float* out, int T, int H,
+                             int E, int S, uint16_t* wsplit, int* status, uint64_t limit_ns, cudaStream_t s);
 // A2.  score: SCORE_SOFTMAX (logits hold the bias) or SCORE_SIGMOID (raw
 // logits; sel_bias, may be null, corrects the choice only).
 // ids_ext / w_ext (optional): [T][k + 1], the last column the shared expert

@@ -145,6 +145,7 @@ struct WsLayout {
   size_t zero_end;     // end of the part that must start zero-filled
   size_t logits;       // float [T, E]
   size_t rt_part;      // float [splits, T, E]: split-K parts of the batched router
+  size_t rt_wsplit;    // bf16 [3][E][H]: the tensor-core router's three terms of the weights (T > 512)
   size_t ids;          // int [T, k]       (when the caller passes no output)
   size_t wts;          // float [T, k]
   size_t ids_r;        // int [T, k]: the router's top-k when the shared expert is folded into the table
@@ -216,6 +217,7 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.logits = take(sizeof(float) * (size_t)T * E);
   const size_t rparts = (size_t)imax(router_splits(T, E, H) * E, router_splits(T, Er, H) * Er);
   L.rt_part = take(rparts > (size_t)E || (T > 16 && T <= 512) ? sizeof(float) * rparts * (size_t)T : 0);
+  L.rt_wsplit = take(T > 512 ? (size_t)6 * E * H : 0);
   L.ids = take(sizeof(int) * n);
   L.wts = take(sizeof(float) * n);
   L.ids_r = take(sizeof(int) * n);

@@ -322,13 +322,23 @@ __global__ void __launch_bounds__(256) k_router_sum(const float* __restrict__ pa
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const float* bias, float* logits,
-                                 int T, int H, int E, float* part, cudaStream_t s) {
+                                 int T, int H, int E, float* part, cudaStream_t s, uint16_t* wsplit, int* status,
+                                 uint64_t limit_ns) {
   if (T == 0) return cudaSuccess;
   // Up to 16 tokens one block per expert row; up to 512 split-K 64 x 64
-  // tiles; beyond that the 128 x 128 tiled GEMM, split along K to balance
-  // the SMs.
-  const int S = router_splits(T, E, H);
+  // tiles; beyond that the tensor cores (E = 64 or 128) or the 128 x 128
+  // tiled FP32 GEMM, split along K to balance the SMs.
+  int S = router_splits(T, E, H);
   cudaError_t err;
+  if (wsplit && status && router_tc_supported(T, H, E)) {
+    S = router_tc_splits(T, H, E);
+    if ((err = launch_router_tc(x, wr, bias, S == 1 ? logits : part, T, H, E, S, wsplit, status, limit_ns, s)) !=
+        cudaSuccess || S == 1)
+      return err;
+    const size_t n = (size_t)T * E;
+    count_launch(), k_router_sum<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(part, bias, logits, T, E, S);
+    return cudaGetLastError();
+  }
   if (T <= 16) {
     dim3 grid(E, (T + 15) / 16);
     count_launch(), k_router_gemv<<<grid, 256, 0, s>>>(x, wr, bias, logits, T, H, E);
