@@ -7,8 +7,10 @@ epilogue, the shared expert, weighted combine) over one batch of synthetic
 tokens.  The headline workload is the 8192-token prefill layer (H=4096,
 I=1536, 128 MXFP4 experts, top-4 under a Zipf(1.1) router bias, BF16 shared
 expert) through moe_layer_forward; the other layer workloads (tiny, 1-token
-decode, 16-token NVFP4 decode uniform and Zipf(1.2), 128-token batched
-decode) are measured in the same run under "per_config".
+decode, 16-token NVFP4 decode uniform and Zipf(1.2), the 128-token batch
+through moe_layer_forward and, as "batch128@decode", through the
+single-launch moe_layer_decode, the prefill with an MXFP8 shared expert) are
+measured in the same run under "per_config".
 
 Timing (every workload): S steps are captured in a CUDA graph and replayed R
 times, so that one timed region is exactly K = R * S steps; the region is
@@ -47,7 +49,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill FP4 TFLOPS vs peak"
 N_LAYERS = 8
-PER_CONFIG = ["tiny", "decode1", "decode16", "decode16z", "batch128", "prefill8k_s8"]
+# "name@decode": the workload through moe_layer_decode (one launch) whatever its size
+PER_CONFIG = ["tiny", "decode1", "decode16", "decode16z", "batch128", "batch128@decode", "prefill8k_s8"]
 # nominal dense GB300 tensor rates (PFLOP/s): FP4 13.5, BF16 2.25
 FP4_PER_BF16 = 13.5 / 2.25
 MIN_REGION_S = 1.0
@@ -252,7 +255,7 @@ def replica_throughput(ms: float, world: int, T: int, K: int) -> float:
     return world * T * K / (ms * 1e-3)
 
 
-def measure(wl, args, dev, rank, world, pk, headline: bool):
+def measure(wl, args, dev, rank, world, pk, headline: bool, entry=None):
     """One workload: timed regions of exactly K steps, per-step durations,
     roofline, end to end through the C ABI from host buffers, clocks."""
     import numpy as np
@@ -263,7 +266,7 @@ def measure(wl, args, dev, rank, world, pk, headline: bool):
     from block_scaled_fp4_router_gb300 import workloads as W
     from block_scaled_fp4_router_gb300.device import DeviceLayer
 
-    fused = wl.T <= 16
+    fused = entry == "decode" if entry else wl.T <= 16
     T, K, Wm = wl.T, max(1, args.steps), max(3, args.warmup)
     # a graph of S steps replayed R times; S divides K and the S steps' token
     # rows and outputs stay within about 2 GB
@@ -380,7 +383,7 @@ def measure(wl, args, dev, rank, world, pk, headline: bool):
     hbm["frac"] = hbm["achieved"] / hbm["peak"]
     if fused:
         prep = layers[0].prepared and wl.H % 256 == 0 and wl.I % 256 == 0
-        hbm["kernel"] = "k_decode_tc" if prep else "k_fused_decode"
+        hbm["kernel"] = ("k_decode_tc (wide step)" if wl.T > 16 else "k_decode_tc") if prep else "k_fused_decode"
         res["roofline"] = hbm
     else:
         hbm["kernel"] = "the layer's launch sequence"
@@ -492,13 +495,18 @@ def run_ours(args):
     head = measure(wl, args, dev, rank, world, pk, headline=True)
     per = {}
     for name in [c for c in args.configs.split(",") if c and c != args.workload]:
-        per[name] = measure(W.WORKLOADS[name], args, dev, rank, world, pk, headline=False)
+        base, _, entry = name.partition("@")
+        per[name] = measure(W.WORKLOADS[base], args, dev, rank, world, pk, headline=False, entry=entry or None)
 
     # the oracle runs after every GPU measurement, on this process's host cores
     if rank == 0 and not args.no_cpu_baseline:
         head["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+        done = {}  # one oracle timing per workload, whatever the entry point
         for name in per:
-            per[name]["cpu_baseline"] = cpu_baseline(W.WORKLOADS[name], args.cpu_budget_s / 2)
+            base = name.partition("@")[0]
+            if base not in done:
+                done[base] = cpu_baseline(W.WORKLOADS[base], args.cpu_budget_s / 2)
+            per[name]["cpu_baseline"] = done[base]
     if rank != 0:
         return
     K = head["steps"]

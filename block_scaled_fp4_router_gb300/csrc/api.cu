@@ -584,7 +584,7 @@ moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t*
                               size_t ws_bytes, moe_stream_t stream) {
   MOE_RANGE();
   MOE_TRY(check_desc(desc));
-  if (desc->T > MAX_DECODE_T) return MOE_ERR_UNSUPPORTED;
+  if (desc->T > MAX_WIDE_T) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(desc, ws, ws_bytes));
   const moe_layer_desc_t dt = table_desc(desc);
   ExpertsDev ex;
@@ -599,8 +599,9 @@ moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t*
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   uint16_t* ob = static_cast<uint16_t*>(out);
-  // Prepared scales (moe_prepare_weights) select the tensor-core launch; a
-  // folded shared expert without them takes the batched path.
+  // Prepared scales (moe_prepare_weights) select the tensor-core launch (1-128
+  // tokens); without them, steps of more than 16 tokens and a folded shared
+  // expert take the batched path.
   if (fused_decode_tc_supported(sh, ex))
     return cuda_status(launch_fused_decode_tc(sh, ex, shd, w_router, bias, xb, ob, topk_ids, topk_w, ws,
                                               g_wait_limit_ns.load(), s, desc->shared_in_table, desc->score_func));

@@ -2,7 +2,8 @@
 // one launch, every contraction on tcgen05 (AMD technical article
 // "MiniMax-M3.1 on AMD Instinct GPUs", section "What we Optimized": the "mono
 // decode" path runs a pure decode step of at most 16 tokens as one fused MoE
-// launch).
+// launch), and the same launch for wider steps of 17-128 tokens (the
+// article's section "What's next": wider mono steps).
 //
 // A decode step streams every touched weight byte once, so the layer is
 // bound by HBM.  The weights are the MMA's A operand (128 weight rows per
@@ -34,6 +35,17 @@
 // producer and MMA warps onto the routed units.  There is no L2 prefetch
 // beyond the stage ring: extra traffic measurably slows the latency-bound
 // hand-offs more than it saves in streaming.
+//
+// Wide steps (17-128 tokens, the W instantiations) keep the 16-row B
+// operand: the shared expert runs per 16-token chunk (SGU / SDN units per
+// chunk), and the routed experts per slot, a run of at most 16 sorted
+// assignments of one expert.  Each block computes the top-k of its own
+// tokens and publishes it tagged with the launch number; every block then
+// sorts all T k assignments by expert (per-warp histograms and scans) in
+// shared memory.  x is quantised after the routing, straight into sorted
+// order, so a slot's activation rows are one 16-row TMA box; the routed
+// gate/up units stream their weight tiles into the ring while they wait for
+// it.
 //
 // Every wait is bounded (MOE_DEV_TIMEOUT in the status word); the last block
 // out resets the counters, and each finishing block resets its ticket.
@@ -74,7 +86,13 @@ constexpr uint32_t A_TILE = 16384, B_TILE = 2048;
 constexpr int NACC = 4;
 template <bool NV> __host__ __device__ constexpr uint32_t tmem_cols() { return NV ? 512u : 256u; }
 constexpr uint32_t TM_SF = 32 * NACC;
-constexpr int MAXN = MAX_DECODE_T * MAX_TOPK;
+// assignments and expert slots of a step (W: wide steps of up to 128 tokens)
+template <bool W> __host__ __device__ constexpr int maxn() { return (W ? MAX_WIDE_T : MAX_DECODE_T) * MAX_TOPK; }
+template <bool W> __host__ __device__ constexpr int maxslot() {
+  return W ? MAX_E + 1 + MAX_WIDE_T * MAX_TOPK / 16 : MAX_DECODE_T * MAX_TOPK;
+}
+template <bool W> __host__ __device__ constexpr int maxt() { return W ? MAX_WIDE_T : MAX_DECODE_T; }
+constexpr int EH = MAX_E + 2;  // per-expert table stride (the table holds up to MAX_E + 1 experts)
 
 enum UnitKind { U_SGU = 0, U_RGU = 1, U_SDN = 2, U_RDN = 3 };
 
@@ -85,7 +103,10 @@ struct DcArgs {
   int G;                     // blocks in the launch
   int s_sgu, s_rgu, s_sdn;   // split-K parts
   int n_sgu, n_sdn;          // unit counts that do not depend on the routing
-  int nslot_max;             // min(T k, E): ticket slots
+  int nslot_max;             // slots a step can have (dc_nslot_max)
+  int nck;                   // 16-token chunks of the shared expert's units (1 up to 16 tokens)
+  int tk_rgu, tk_nv, tk_slot;  // ticket offsets: routed gate/up tiles, NVFP4 per-slot scale blocks,
+                               // per-slot counters of finished routed h
   int shared;
   int nv;                    // NVFP4 experts (UE4M3 scales per 16, FP32 tensor scales)
   int score;                 // SCORE_SOFTMAX (the bias is part of the logit) or SCORE_SIGMOID
@@ -101,9 +122,14 @@ struct DcArgs {
   int* ctr;
   int* tickets;
   unsigned long long* logit64;  // [T, E]: (launch number << 32) | FP32 bits
-  uint8_t* xq;               // [T, H/2]
-  uint8_t* xs_mma;           // [H/128][512] E8M0 (MXFP4) or [H/64][512] UE4M3 (NVFP4)
-  int* xshift;               // NVFP4: [16] per-row power of two of the UE4M3 x scales
+  uint8_t* xq;               // [T, H/2]; wide steps: [T k, H/2] in sorted-assignment order
+  uint8_t* xs_mma;           // [H/128][512] E8M0 (MXFP4) or [H/64][512] UE4M3 (NVFP4); wide steps:
+                             // one such set per slot
+  int* xshift;               // NVFP4: [16] per-row power of two of the UE4M3 x scales; wide steps: [T k]
+  unsigned long long* topk64;  // wide steps: [2][T kr] (launch number << 32) | expert id, | weight bits
+  float* rpart;              // wide steps: [H/256][T][Er] router partial sums
+  uint8_t* xq_tok;           // wide steps: [T, H/2] x codes in token order (before the routing)
+  uint8_t* xe_tok;           // wide steps: [T, H/32] their E8M0 exponent bytes
   unsigned long long* rowmax;  // NVFP4: [T k] (launch << 32) | (largest h scale exponent + 256)
   uint8_t* hq;               // [T k, I/2] sorted-assignment rows
   uint8_t* hs_mma;           // [slots][I/128][512] E8M0 (MXFP4) or [slots][I/64][512] UE4M3 (NVFP4)
@@ -122,17 +148,24 @@ struct DcMaps {
   CUtensorMap xq, x, hsh, hq;        // activations: boxes of 16 rows x 128 B
 };
 
-// Routing of the step, built by the epilogue warps of every block.
-struct DcRouting {
-  int ids[MAXN];
-  float w[MAXN];
-  int inv[MAXN];          // assignment t*k+j -> sorted position
-  int tok[MAXN];          // sorted position -> token
-  int sorted_e[MAXN];     // sorted position -> expert
-  int slot_e[MAXN];       // slot -> expert (distinct experts, ascending)
-  int slot_beg[MAXN + 1]; // slot -> first sorted position
+// Routing of the step, built by the epilogue warps of every block (16-byte
+// aligned: before it is built, wide steps stage x in its storage as float4).
+template <bool W>
+struct __align__(16) DcRouting {
+  int ids[maxn<W>()];
+  float w[maxn<W>()];
+  int inv[maxn<W>()];          // assignment t*k+j -> sorted position
+  int tok[maxn<W>()];          // sorted position -> token
+  int sorted_e[maxn<W>()];     // sorted position -> expert
+  int slot_e[maxslot<W>()];    // slot -> expert (ascending)
+  int slot_beg[maxslot<W>() + 1];  // slot -> first sorted position
   int wcount[EPI_THREADS / 32];
   int n_slots;
+  // wide steps: per-warp expert histograms (then bases), expert offsets and
+  // first slots in the sorted order
+  int whist[W ? 4 * EH : 1];
+  int eoff[W ? EH : 1];
+  int soff[W ? EH : 1];
 };
 
 struct Unit {
@@ -140,6 +173,7 @@ struct Unit {
   int tile;   // 128-row tile: of I (gate/up) or of H (down)
   int part;   // split-K part
   int slot;   // routed units
+  int chunk;  // shared units: 16-token chunk
   int st0, st1;
 };
 
@@ -153,22 +187,28 @@ __device__ __forceinline__ void part_range(int stages, int s, int p, int& st0, i
   st1 = (p + 1) * stages / s;
 }
 
-// v-th shared down unit: 128-row tile of H, K part over stages of two chunks.
+// v-th shared down unit: 128-row tile of H, K part over stages of two
+// chunks, 16-token chunk (the chunks of one tile and part are neighbours in
+// the list, so their weight tiles are read from HBM about once).
 __device__ __forceinline__ Unit sdn_unit(const DcArgs& a, int v) {
   Unit U{};
   U.kind = U_SDN;
+  U.chunk = v % a.nck;
+  v /= a.nck;
   U.tile = v / a.s_sdn;
   U.part = v % a.s_sdn;
   part_range((a.I / 64 + 1) / 2, a.s_sdn, U.part, U.st0, U.st1);
   return U;
 }
 
-// v-th routed down unit: 128-row tile of H x expert slot, whole K.
+// v-th routed down unit: 128-row tile of H x expert slot, whole K, in slot
+// order (slots finish their gate/up in about that order, and each down unit
+// waits only for its own slot's h).
 __device__ __forceinline__ Unit rdn_unit(const DcArgs& a, int n_slots, int v) {
   Unit U{};
   U.kind = U_RDN;
-  U.tile = v / n_slots;
-  U.slot = v % n_slots;
+  U.slot = v / (a.H / 128);
+  U.tile = v % (a.H / 128);
   U.st0 = 0;
   U.st1 = (a.I / 256 + 1) / 2;
   return U;
@@ -179,6 +219,8 @@ __device__ Unit unit_at(const DcArgs& a, int n_slots, int u) {
   const int nbI = a.I / 128;
   if (u < a.n_sgu) {
     U.kind = U_SGU;
+    U.chunk = u % a.nck;
+    u /= a.nck;
     U.tile = u / a.s_sgu;
     U.part = u % a.s_sgu;
     part_range(a.H / 64, a.s_sgu, U.part, U.st0, U.st1);
@@ -238,7 +280,8 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 // Tokens go in groups of 8; within a group every load of a pass (4 x 8
 // elements per thread) is in flight before the FMAs, since these loads
 // compete with the weight streams for HBM.
-__device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DECODE_T], uint32_t epoch) {
+template <int MT>
+__device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MT], uint32_t epoch) {
   const int T = a.T, H = a.H;
   const int w = et >> 5, lane = et & 31;
   constexpr int PASS = EPI_THREADS * 8;
@@ -301,45 +344,127 @@ __device__ void router_row(const DcArgs& a, int e, int et, float (*red_s)[MAX_DE
   epi_sync();
 }
 
+// Wide steps: the router as split-K items (16-token group g, 256-element K
+// part q), so that no block streams more than one group's x.  The epilogue
+// warps stage x[16g .. 16g+15][256q .. 256q+255] in shared memory (xs, 16 KB
+// as FP32) and thread et computes experts et, et + 128, ... over the part,
+// each logit part four FP32 chains of 64 products added pairwise, stored to
+// rpart[q][t][e].  Every block counts itself on C_DC_RT once its items are
+// stored; the top-k adds a token's parts in q order.
+__device__ void router_w(const DcArgs& a, int et, float* xs) {
+  const int T = a.T, H = a.H, Er = a.Er, KP = H / 256, items = (T + 15) / 16 * KP;
+  for (int item = blockIdx.x; item < items; item += a.G) {
+    const int g = item / KP, q = item % KP;
+    for (int i = et; i < 16 * 32; i += EPI_THREADS) {  // 16 rows x 32 groups of 8 BF16
+      const int r = i >> 5, c = i & 31, t = 16 * g + r;
+      const uint4 v = t < T ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H + 256 * q) + c)
+                            : make_uint4(0, 0, 0, 0);
+      float4* d = reinterpret_cast<float4*>(xs + r * 256 + 8 * c);
+      d[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      d[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+    }
+    epi_sync();
+    for (int e = et; e < Er; e += EPI_THREADS) {
+      // four FP32 chains per token (k = 0, 1, 2, 3 mod 4), 64 products each,
+      // added pairwise at the end: the accuracy of the batched router's
+      // 128-element chains or better
+      float4 acc[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) acc[t] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const float4* wrow = reinterpret_cast<const float4*>(a.wr + (size_t)e * H + 256 * q);
+#pragma unroll 1
+      for (int k0 = 0; k0 < 64; k0 += 16) {
+        float4 wv[16];  // 64 weights in flight, then 16 tokens x 64 FMAs
+#pragma unroll
+        for (int j = 0; j < 16; ++j) wv[j] = __ldg(wrow + k0 + j);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float4 xv = *reinterpret_cast<const float4*>(xs + t * 256 + 4 * (k0 + j));
+            acc[t].x = fmaf(xv.x, wv[j].x, acc[t].x);
+            acc[t].y = fmaf(xv.y, wv[j].y, acc[t].y);
+            acc[t].z = fmaf(xv.z, wv[j].z, acc[t].z);
+            acc[t].w = fmaf(xv.w, wv[j].w, acc[t].w);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 16; ++t)
+        if (16 * g + t < T)
+          a.rpart[((size_t)q * T + 16 * g + t) * Er + e] = (acc[t].x + acc[t].y) + (acc[t].z + acc[t].w);
+    }
+    epi_sync();  // xs is restaged by the next item
+  }
+  if (et == 0) red_release_add(a.ctr + C_DC_RT, 1);  // after the barrier: every thread's parts
+}
+
+// Wide steps: token t's logits to lg[e] (thread et: experts et, et + 128),
+// the parts added in q order (up to 32 parts' loads in flight), the softmax
+// bias added last.
+__device__ void logits_w(const DcArgs& a, int t, int et, float* lg) {
+  const int KP = a.H / 256;
+  const size_t stride = (size_t)a.T * a.Er;
+  for (int e = et; e < a.Er; e += EPI_THREADS) {
+    const float* src = a.rpart + (size_t)t * a.Er + e;
+    float v = 0.0f;
+    for (int q0 = 0; q0 < KP; q0 += 32) {
+      float p[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) p[q] = q0 + q < KP ? __ldcg(src + (q0 + q) * stride) : 0.0f;
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        if (q0 + q < KP) v += p[q];
+    }
+    if (a.bias && a.score == SCORE_SOFTMAX) v += __ldg(a.bias + e);
+    lg[e] = v;
+  }
+}
+
+// MXFP4 codes of one 32-element BF16 block (16 bytes to dq) and its E8M0
+// byte.  Same arithmetic as the standalone quantiser.
+__device__ __forceinline__ uint8_t quant32(const uint16_t* xb, uint8_t* dq) {
+  const uint4* src = reinterpret_cast<const uint4*>(xb);
+  uint4 raw[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) raw[j] = __ldg(src + j);
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+  }
+  const int ex = mx_scale_exp(amax);
+  const float inv = pow2_neg(ex);
+  uint32_t c[4];
+#pragma unroll 1
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+    uint32_t word = 0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      word |= e2m1_rne(bf16_lo(w4[h]) * inv) << (8 * h);
+      word |= e2m1_rne(bf16_hi(w4[h]) * inv) << (8 * h + 4);
+    }
+    c[j] = word;
+  }
+  *reinterpret_cast<uint4*>(dq) = make_uint4(c[0], c[1], c[2], c[3]);
+  return (uint8_t)(ex + 127);
+}
+
 // MXFP4 quantisation of one 32-element block i = (token row t < 16, block b
 // of H/32): 16 code bytes of xq and byte b % 4 of the MMA-layout scale word
 // of row t in group b / 4 (word 4t of that group's 512-byte block).  Rows
-// t >= T get a zero scale byte.  Same arithmetic as the standalone quantiser.
+// t >= T get a zero scale byte.
 __device__ void quant_block(const DcArgs& a, int i) {
   const int nb = a.H / 32;
   const int t = i / nb, b = i % nb;
   uint8_t sb = 0;
-  if (t < a.T) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + b * 32);
-    uint4 raw[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) raw[j] = __ldg(src + j);
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
-    }
-    const int ex = mx_scale_exp(amax);
-    const float inv = pow2_neg(ex);
-    uint32_t c[4];
-#pragma unroll 1
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-      uint32_t word = 0;
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        word |= e2m1_rne(bf16_lo(w4[h]) * inv) << (8 * h);
-        word |= e2m1_rne(bf16_hi(w4[h]) * inv) << (8 * h + 4);
-      }
-      c[j] = word;
-    }
-    *reinterpret_cast<uint4*>(a.xq + (size_t)t * (a.H / 2) + b * 16) = make_uint4(c[0], c[1], c[2], c[3]);
-    sb = (uint8_t)(ex + 127);
-  }
+  if (t < a.T) sb = quant32(a.x + (size_t)t * a.H + b * 32, a.xq + (size_t)t * (a.H / 2) + b * 16);
   a.xs_mma[(size_t)(b / 4) * 512 + t * 16 + (b % 4)] = sb;
 }
+
 
 // One warp reads token t's E logits once every one carries this launch's
 // number (bounded wait; false on timeout).  Lane l gets experts l, l+32, ...
@@ -378,20 +503,17 @@ __device__ __forceinline__ float pow2f(int c) {
   return c >= -126 ? __uint_as_float((uint32_t)(c + 127) << 23) : __uint_as_float(1u << (c + 149));
 }
 
-// NVFP4 experts: one warp quantises token row t < 16 to MXFP4 (the same codes
-// and E8M0 exponents as the standalone quantiser) and writes the scales for
-// the UE4M3 MMA: each 32-block's 2^e twice (two 16-blocks) as 2^(e - c_t),
-// c_t = (largest e of the row) - 8, and c_t to xshift[t]; the epilogue
-// multiplies the row's products by 2^c_t.  A block more than 2^17 below the
-// row's largest block scale falls under UE4M3's range and is dropped.  Rows
-// t >= T get zero scale words.  Lane l takes blocks l, l+32, ... in batches
+// NVFP4 experts: one warp quantises token row t to MXFP4 (the same codes and
+// E8M0 exponents as the standalone quantiser), the codes to xrow, and writes
+// row `row` of the scale blocks at xs for the UE4M3 MMA: each 32-block's 2^e
+// twice (two 16-blocks) as 2^(e - c_t), c_t = (largest e of the row) - 8, and
+// c_t to *shift; the epilogue multiplies the row's products by 2^c_t.  A
+// block more than 2^17 below the row's largest block scale falls under
+// UE4M3's range and is dropped.  Lane l takes blocks l, l+32, ... in batches
 // of 4 with all their loads in flight; the exponents wait in e_s (H <= 8192).
-__device__ void quant_row_nv(const DcArgs& a, int t, uint8_t* e_s) {
+__device__ void quant_row_nv_to(const DcArgs& a, int t, uint8_t* xrow, uint8_t* xs, int row, int* shift,
+                                uint8_t* e_s, uint8_t* e8_out = nullptr) {
   const int lane = threadIdx.x & 31, nb = a.H / 32;
-  if (t >= a.T) {
-    for (int kb = lane; kb < a.H / 64; kb += 32) *reinterpret_cast<uint32_t*>(a.xs_mma + (size_t)kb * 512 + t * 16) = 0u;
-    return;
-  }
   const uint16_t* xr = a.x + (size_t)t * a.H;
   int emax = -127;
   for (int b0 = lane; b0 < nb; b0 += 4 * 32) {
@@ -415,7 +537,7 @@ __device__ void quant_row_nv(const DcArgs& a, int t, uint8_t* e_s) {
       }
       const int ex = mx_scale_exp(amax);
       const float inv = pow2_neg(ex);
-      uint32_t* dst = reinterpret_cast<uint32_t*>(a.xq + (size_t)t * (a.H / 2) + b * 16);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(xrow + b * 16);
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         const uint4 w = raw[4 * j + q];
@@ -429,18 +551,76 @@ __device__ void quant_row_nv(const DcArgs& a, int t, uint8_t* e_s) {
         dst[q] = word;
       }
       e_s[b] = (uint8_t)(ex + 127);
+      if (e8_out) e8_out[b] = (uint8_t)(ex + 127);
       emax = max(emax, ex);
     }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) emax = max(emax, __shfl_xor_sync(FULL, emax, o));
   const int c = emax - 8;
-  if (lane == 0) a.xshift[t] = c;
+  if (lane == 0) *shift = c;
   __syncwarp();
-  // bytes 2(b&1), 2(b&1)+1 of the word of row t in 64-element chunk b/2
+  if (!xs) return;
+  // bytes 2(b&1), 2(b&1)+1 of the word of the row in 64-element chunk b/2
   for (int b = lane; b < nb; b += 32) {
     const uint32_t u = ue4m3_pow2((int)e_s[b] - 127 - c);
-    *reinterpret_cast<uint16_t*>(a.xs_mma + (size_t)(b / 2) * 512 + t * 16 + 2 * (b & 1)) = (uint16_t)(u | (u << 8));
+    *reinterpret_cast<uint16_t*>(xs + (size_t)(b / 2) * 512 + row * 16 + 2 * (b & 1)) = (uint16_t)(u | (u << 8));
+  }
+}
+
+// Token row t < 16 of a step of up to 16 tokens (rows t >= T get zero scale
+// words).
+__device__ void quant_row_nv(const DcArgs& a, int t, uint8_t* e_s) {
+  const int lane = threadIdx.x & 31;
+  if (t >= a.T) {
+    for (int kb = lane; kb < a.H / 64; kb += 32) *reinterpret_cast<uint32_t*>(a.xs_mma + (size_t)kb * 512 + t * 16) = 0u;
+    return;
+  }
+  quant_row_nv_to(a, t, a.xq + (size_t)t * (a.H / 2), a.xs_mma, t, a.xshift + t, e_s);
+}
+
+// Wide steps, before the routing: x in token order, MXFP4 codes to xq_tok and
+// E8M0 bytes to xe_tok (NVFP4 also the row shift c_t to xshift[t]); the
+// epilogue warps of every block take a share while the router parts land.
+template <bool NV>
+__device__ void quant_tokens_w(const DcArgs& a, int et, uint8_t* e_s) {
+  const int T = a.T, H = a.H, nb = H / 32;
+  if (NV) {
+    for (int t = blockIdx.x * (EPI_THREADS / 32) + (et >> 5); t < T; t += a.G * (EPI_THREADS / 32))
+      quant_row_nv_to(a, t, a.xq_tok + (size_t)t * (H / 2), nullptr, 0, a.xshift + t, e_s, a.xe_tok + (size_t)t * nb);
+  } else {
+    for (int i = blockIdx.x * EPI_THREADS + et; i < T * nb; i += a.G * EPI_THREADS)
+      a.xe_tok[i] = quant32(a.x + (size_t)i * 32, a.xq_tok + (size_t)i * 16);
+  }
+}
+
+// Wide steps, after the routing: item i = (sorted row p, 32-element block b)
+// copies token tok[p]'s 16 code bytes to xq row p and writes its scale into
+// row c (p's row in its slot) of the slot's MMA-layout scale blocks: the
+// E8M0 byte (MXFP4), or the UE4M3 pair 2^(e - c_t) (NVFP4).  The slot's first
+// row also zeroes the scale words of the rows the slot leaves empty (its B
+// tile's other rows belong to the next slot or lie past T k).
+template <bool NV>
+__device__ void sort_x_w(const DcArgs& a, const DcRouting<true>& R, int i) {
+  const int H = a.H, nb = H / 32;
+  const int p = i / nb, b = i % nb;
+  const int e = R.sorted_e[p], r = p - R.eoff[e];
+  const int slot = R.soff[e] + (r >> 4), c = r & 15, t = R.tok[p];
+  *reinterpret_cast<uint4*>(a.xq + (size_t)p * (H / 2) + b * 16) =
+      __ldcg(reinterpret_cast<const uint4*>(a.xq_tok + (size_t)t * (H / 2) + b * 16));
+  const int e8 = __ldcg(a.xe_tok + (size_t)t * nb + b);
+  const int cnt = imin(16, R.eoff[e + 1] - (p - c));
+  if (NV) {
+    uint8_t* blk = a.xs_mma + ((size_t)slot * (H / 64) + b / 2) * 512;
+    const uint32_t u = ue4m3_pow2(e8 - 127 - __ldcg(a.xshift + t));
+    *reinterpret_cast<uint16_t*>(blk + c * 16 + 2 * (b & 1)) = (uint16_t)(u | (u << 8));
+    if (c == 0 && (b & 1) == 0)
+      for (int rr = cnt; rr < 16; ++rr) *reinterpret_cast<uint32_t*>(blk + rr * 16) = 0u;
+  } else {
+    uint8_t* blk = a.xs_mma + ((size_t)slot * (H / 128) + b / 4) * 512 + (b % 4);
+    blk[c * 16] = (uint8_t)e8;
+    if (c == 0)
+      for (int rr = cnt; rr < 16; ++rr) blk[rr * 16] = 0;
   }
 }
 
@@ -449,7 +629,7 @@ __device__ void quant_row_nv(const DcArgs& a, int t, uint8_t* e_s) {
 // that precede it) and the distinct-expert slots (runs of one expert in the
 // sorted order, numbered with a ballot).  128 epilogue threads, et = 0..127.
 // *failed is set (by some thread) when a logit row never arrived.
-__device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t epoch, int* failed) {
+__device__ void build_routing(const DcArgs& a, DcRouting<false>& R, int et, uint32_t epoch, int* failed) {
   const int T = a.T, k = a.k, kr = a.kr, n = T * k;
   const int w = et >> 5, lane = et & 31;
   for (int t = w; t < T; t += EPI_THREADS / 32) {
@@ -503,6 +683,155 @@ __device__ void build_routing(const DcArgs& a, DcRouting& R, int et, uint32_t ep
     R.n_slots = total;
     R.slot_beg[total] = n;
   }
+  epi_sync();
+}
+
+// Wide steps (T k <= 1024 assignments).  Once every block's router parts are
+// in, each block takes tokens blockIdx.x + G i one at a time: its epilogue
+// threads add the token's logit parts, warp 0 picks the top-k and publishes
+// it with the launch number in the high word, so a reader that sees the
+// number has the value; every
+// block then reads all T kr entries (bounded wait), adds the folded shared
+// expert, and sorts the assignments by expert, stably: warp w counts its
+// contiguous quarter of the assignments per expert (__match_any_sync), one
+// warp scans the counts into expert offsets, per-warp bases and first slots,
+// and each warp places its quarter.  Slot s is a run of at most 16 sorted
+// positions of one expert; an expert's runs are consecutive slots.
+__device__ void build_routing_w(const DcArgs& a, DcRouting<true>& R, int et, uint32_t epoch, int* failed) {
+  const int T = a.T, k = a.k, kr = a.kr, n = T * k, E = a.E, nr = T * kr;
+  const int w = et >> 5, lane = et & 31;
+  if ((int)blockIdx.x < T) {  // this block has tokens: every block's router parts must be in
+    if (et == 0 && !wait_at_least(a.ctr + C_DC_RT, a.G, a.ctr + C_STATUS, a.limit_ns)) *failed = 1;
+    epi_sync();
+  }
+  float* lg = reinterpret_cast<float*>(R.sorted_e);  // a token's logits (the sort comes later)
+  for (int t = blockIdx.x; t < T && !*failed; t += a.G) {
+    logits_w(a, t, et, lg);
+    epi_sync();
+    if (w != 0) {
+      epi_sync();
+      continue;
+    }
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = lane + 32 * i < a.Er ? lg[lane + 32 * i] : 0.0f;
+    int sel[MAX_TOPK];
+    float wt[MAX_TOPK];
+    route_row(v, a.Er, kr, a.score, a.bias, sel, wt);
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j == lane && j < kr) {
+        st_relaxed_u64(a.topk64 + t * kr + j, ((unsigned long long)epoch << 32) | (uint32_t)sel[j]);
+        st_relaxed_u64(a.topk64 + nr + t * kr + j, ((unsigned long long)epoch << 32) | __float_as_uint(wt[j]));
+      }
+    epi_sync();  // lg is rewritten for the next token
+  }
+  const uint64_t t0 = globaltimer_ns();
+  for (int i = et; i < nr; i += EPI_THREADS) {
+    unsigned long long vi = 0, vw = 0;
+    for (uint32_t it = 0;; ++it) {
+      vi = ld_relaxed_u64(a.topk64 + i);
+      vw = ld_relaxed_u64(a.topk64 + nr + i);
+      if ((uint32_t)(vi >> 32) == epoch && (uint32_t)(vw >> 32) == epoch) break;
+      if (globaltimer_ns() - t0 > a.limit_ns || it > (1u << 26)) {
+        *failed = 1;
+        vi = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    const int t = i / kr, j = i % kr;
+    const int id = (int)(uint32_t)vi;
+    R.ids[t * k + j] = id >= 0 && id < a.Er ? id : 0;  // a failed wait leaves a valid index
+    R.w[t * k + j] = __uint_as_float((uint32_t)vw);
+  }
+  if (kr < k)  // the shared expert folded into the table: expert Er, weight 1
+    for (int t = et; t < T; t += EPI_THREADS) {
+      R.ids[t * k + kr] = a.Er;
+      R.w[t * k + kr] = 1.0f;
+    }
+  int* wh = R.whist + w * EH;
+  for (int e = lane; e < E; e += 32) wh[e] = 0;
+  epi_sync();
+  if (*failed) return;  // the same answer in every thread after the barrier
+  const int per = (n + 3) / 4, lo = imin(n, w * per), hi = imin(n, lo + per);
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const int e = i < hi ? R.ids[i] : -1;
+    const unsigned peers = __match_any_sync(FULL, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
+    __syncwarp();
+  }
+  epi_sync();
+  if (w == 0) {
+    constexpr int EPL = (EH + 31) / 32;  // experts per lane
+    int cnt[EPL], tot = 0, stot = 0;
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int e = lane * EPL + q;
+      int c = 0;
+      if (e < E)
+        for (int ww = 0; ww < EPI_THREADS / 32; ++ww) c += R.whist[ww * EH + e];
+      cnt[q] = c;
+      tot += c;
+      stot += (c + 15) >> 4;
+    }
+    int it = tot, is = stot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x1 = __shfl_up_sync(FULL, it, o), x2 = __shfl_up_sync(FULL, is, o);
+      if (lane >= o) {
+        it += x1;
+        is += x2;
+      }
+    }
+    int eo = it - tot, so = is - stot;
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int e = lane * EPL + q;
+      if (e < E) {
+        R.eoff[e] = eo;
+        R.soff[e] = so;
+        int b = eo;
+        for (int ww = 0; ww < EPI_THREADS / 32; ++ww) {
+          const int c = R.whist[ww * EH + e];
+          R.whist[ww * EH + e] = b;
+          b += c;
+        }
+      }
+      eo += cnt[q];
+      so += (cnt[q] + 15) >> 4;
+    }
+    if (lane == 31) {
+      R.eoff[E] = eo;
+      R.soff[E] = so;
+      R.n_slots = so;
+    }
+  }
+  epi_sync();
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const int e = i < hi ? R.ids[i] : -1;
+    const unsigned peers = __match_any_sync(FULL, e);
+    const int pos = e >= 0 ? wh[e] + __popc(peers & ((1u << lane) - 1u)) : 0;
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
+    __syncwarp();
+    if (e >= 0) {
+      R.inv[i] = pos;
+      R.tok[pos] = i / k;
+      R.sorted_e[pos] = e;
+    }
+  }
+  epi_sync();
+  for (int p = et; p < n; p += EPI_THREADS) {
+    const int e = R.sorted_e[p], r = p - R.eoff[e];
+    if ((r & 15) == 0) {
+      R.slot_e[R.soff[e] + (r >> 4)] = e;
+      R.slot_beg[R.soff[e] + (r >> 4)] = p;
+    }
+  }
+  if (et == 0) R.slot_beg[R.n_slots] = n;
   epi_sync();
 }
 
@@ -561,17 +890,21 @@ __device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, 
 }
 
 // TMA / bulk copies of the activation tiles (and their scales) of stage st.
-template <bool NV>
+// Shared units take the 16 token rows of their chunk; routed gate/up units
+// every token row (steps of up to 16 tokens) or their slot's 16 sorted rows
+// (wide steps).
+template <bool NV, bool W>
 __device__ __forceinline__ void issue_acts(const DcArgs& a, const DcMaps& m, const Unit& U, int st, int beg,
                                            uint8_t* sp, uint64_t* fb) {
   if (U.kind == U_SGU) {
-    tc::tma_load_2d(sp + ST_B0, &m.x, st * 128, 0, fb);
+    tc::tma_load_2d(sp + ST_B0, &m.x, st * 128, 16 * U.chunk, fb);
   } else if (U.kind == U_RGU) {
-    tc::tma_load_2d(sp + ST_B0, &m.xq, st * 128, 0, fb);
-    tc::bulk_load(sp + st_sfb<NV>(), a.xs_mma + (size_t)st * sf_chunk<NV>(), sf_chunk<NV>(), fb);
+    tc::tma_load_2d(sp + ST_B0, &m.xq, st * 128, W ? beg : 0, fb);
+    const size_t set = W ? (size_t)U.slot * (a.H / 256) * sf_chunk<NV>() : 0;  // the slot's scale blocks
+    tc::bulk_load(sp + st_sfb<NV>(), a.xs_mma + set + (size_t)st * sf_chunk<NV>(), sf_chunk<NV>(), fb);
   } else if (U.kind == U_SDN) {
     for (int h = 0; h < stage_halves(a, U, st); ++h)
-      tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hsh, (2 * st + h) * 128, 0, fb);
+      tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hsh, (2 * st + h) * 128, 16 * U.chunk, fb);
   } else {
     const int halves = stage_halves(a, U, st);
     for (int h = 0; h < halves; ++h)
@@ -629,18 +962,21 @@ __device__ __forceinline__ void fp4_mma(uint32_t d, uint64_t ad, uint64_t bd, in
 
 // ------------------------------------------------------------------ kernel
 
-template <bool NV>
+template <bool NV, bool W>
 __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcMaps maps, const DcArgs a) {
   constexpr uint32_t STAGE_BYTES = stage_bytes<NV>();
   constexpr uint32_t ST_SFB = st_sfb<NV>();
   constexpr int NB = nblk<NV>();
   extern __shared__ __align__(1024) uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full[DSTAGES], empty[DSTAGES], acc_full[NACC], acc_empty[NACC], drain, routing_ready;
+  __shared__ uint64_t full[DSTAGES], empty[DSTAGES], acc_full[NACC], acc_empty[NACC], drain, routing_ready, comb;
+  __shared__ int never_s;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag, s_ok, s_last, s_fail;
   __shared__ uint32_t s_epoch;
-  __shared__ DcRouting R;
+  __shared__ DcRouting<W> R;
+  static_assert(!W || sizeof(DcRouting<W>) >= 16 * 256 * sizeof(float), "the wide router stages x in R");
+  static_assert(alignof(DcRouting<W>) >= 16, "float4 accesses to the staged x");
   __shared__ float red_s[EPI_THREADS / 32][MAX_DECODE_T];
   __shared__ __align__(4) uint8_t s_hsb[MAX_DECODE_T * 4];
   __shared__ uint8_t s_qe[EPI_THREADS / 32][256];  // NVFP4 quantiser: a row's block exponents
@@ -659,6 +995,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     }
     tc::mbar_init(&drain, 1);
     tc::mbar_init(&routing_ready, 1);
+    tc::mbar_init(&comb, 1);
+    never_s = 0;
     tc::mbar_fence_init();
     abort_flag = 0;
     s_fail = 0;
@@ -690,7 +1028,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         return tc::mbar_wait(&empty[j % DSTAGES], (j / DSTAGES) & 1, a.limit_ns, &abort_flag);
       };
       int n_slots = -1;
-      bool hsh_ok = false, hr_ok = false;
+      bool hsh_ok = false, xr_ok = false;
       tc::prefetch_tensormap(&maps.w13r);
       tc::prefetch_tensormap(&maps.w2r);
       tc::prefetch_tensormap(&maps.xq);
@@ -705,9 +1043,12 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         if (u >= a.n_sgu && n_slots < 0) {
           if (!tc::mbar_wait(&routing_ready, 0, a.limit_ns, &abort_flag)) { fail(); break; }
           n_slots = R.n_slots;
-          // x was quantised by plain stores of other blocks
-          if (!wait_at_least(a.ctr + C_DC_READY, a.G, status, a.limit_ns)) { fail(); break; }
-          tc::fence_proxy_async_global();
+          // x was quantised by plain stores of other blocks (wide steps: a
+          // dependency of the routed gate/up units, below)
+          if (!W) {
+            if (!wait_at_least(a.ctr + C_DC_READY, a.G, status, a.limit_ns)) { fail(); break; }
+            tc::fence_proxy_async_global();
+          }
         }
         if (u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
         const Unit U = unit_at(a, n_slots < 0 ? 0 : n_slots, u);
@@ -716,15 +1057,17 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           e = R.slot_e[U.slot];
           beg = R.slot_beg[U.slot];
         }
-        // Down units read h that other blocks write.  While it is not there
+        // Down units read h that other blocks write (and, in wide steps,
+        // routed gate/up units the sorted x rows).  While it is not there
         // yet, the unit's weight tiles already go into the ring (up to its
-        // depth); their h tiles follow once the dependency is met.
+        // depth); their activation tiles follow once the dependency is met.
         int npre = 0;
         uint32_t pre_stage[DSTAGES];
-        const bool dep_sdn = U.kind == U_SDN && !hsh_ok, dep_rdn = U.kind == U_RDN && !hr_ok;
-        if (dep_sdn || dep_rdn) {
-          int* cnt = a.ctr + (dep_sdn ? C_DC_HSH : C_DC_HR);
-          const int target = dep_sdn ? nbI : (NV ? n_slots : n_slots * nbI);
+        const bool dep_sdn = U.kind == U_SDN && !hsh_ok, dep_rdn = U.kind == U_RDN;
+        const bool dep_rgu = W && U.kind == U_RGU && !xr_ok;
+        if (dep_sdn || dep_rdn || dep_rgu) {
+          int* cnt = dep_sdn ? a.ctr + C_DC_HSH : dep_rdn ? a.tickets + a.tk_slot + U.slot : a.ctr + C_DC_READY;
+          const int target = dep_sdn ? nbI * a.nck : dep_rdn ? (NV ? 1 : nbI) : a.G;
           if (ld_acquire(cnt) < target) {
             npre = imin(U.st1 - U.st0, a.depth);
             bool ok = true;
@@ -744,18 +1087,19 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             if (!ok) break;
             if (!wait_at_least(cnt, target, status, a.limit_ns)) { fail(); break; }
           }
-          if (dep_sdn) hsh_ok = true; else hr_ok = true;
+          if (dep_sdn) hsh_ok = true;
+          else if (dep_rgu) xr_ok = true;
           tc::fence_proxy_async_global();
         }
         for (int j = 0; j < npre; ++j)
-          issue_acts<NV>(a, maps, U, U.st0 + j, beg, dsm + pre_stage[j] * STAGE_BYTES, &full[pre_stage[j]]);
+          issue_acts<NV, W>(a, maps, U, U.st0 + j, beg, dsm + pre_stage[j] * STAGE_BYTES, &full[pre_stage[j]]);
         bool ok = true;
         for (int st = U.st0 + npre; st < U.st1; ++st) {
           if (!claim()) { fail(); ok = false; break; }
           uint8_t* sp = dsm + stage * STAGE_BYTES;
           tc::mbar_expect_tx(&full[stage], stage_tx<NV>(a, U, st));
           issue_weights<NV>(a, maps, U, st, e, sp, &full[stage]);
-          issue_acts<NV>(a, maps, U, st, beg, sp, &full[stage]);
+          issue_acts<NV, W>(a, maps, U, st, beg, sp, &full[stage]);
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           ++gi;
@@ -868,31 +1212,50 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     const int T = a.T, H = a.H, I = a.I, k = a.k, n = T * k;
 
     const uint32_t epoch = s_epoch;
-    for (int e = blockIdx.x; e < a.Er; e += a.G) router_row(a, e, et, red_s, epoch);
-    // the router rows go to the first E blocks, the quantisation to the last ones
-    if (NV) {
-      const int t = (a.G - 1 - blockIdx.x) * (EPI_THREADS / 32) + (et >> 5);
-      if (t < MAX_DECODE_T) quant_row_nv(a, t, s_qe[et >> 5]);
+    if constexpr (W) {
+      // the routing table is not built yet: its storage stages x for the router
+      router_w(a, et, reinterpret_cast<float*>(&R));
+      quant_tokens_w<NV>(a, et, s_qe[et >> 5]);
     } else {
-      const int nqb = MAX_DECODE_T * (H / 32);
-      for (int i = (a.G - 1 - blockIdx.x) * EPI_THREADS + et; i < nqb; i += a.G * EPI_THREADS) quant_block(a, i);
+      for (int e = blockIdx.x; e < a.Er; e += a.G) router_row(a, e, et, red_s, epoch);
     }
-    tc::fence_proxy_async_global();
-    epi_sync();  // orders every thread's stores before thread 0's release
-    if (et == 0) red_release_add(a.ctr + C_DC_READY, 1);
-    build_routing(a, R, et, epoch, &s_fail);
+    if constexpr (!W) {
+      // the router rows go to the first E blocks, the quantisation to the last ones
+      if (NV) {
+        const int t = (a.G - 1 - blockIdx.x) * (EPI_THREADS / 32) + (et >> 5);
+        if (t < MAX_DECODE_T) quant_row_nv(a, t, s_qe[et >> 5]);
+      } else {
+        const int nqb = MAX_DECODE_T * (H / 32);
+        for (int i = (a.G - 1 - blockIdx.x) * EPI_THREADS + et; i < nqb; i += a.G * EPI_THREADS) quant_block(a, i);
+      }
+      tc::fence_proxy_async_global();
+      epi_sync();  // orders every thread's stores before thread 0's release
+      if (et == 0) red_release_add(a.ctr + C_DC_READY, 1);
+      build_routing(a, R, et, epoch, &s_fail);
+    } else {
+      build_routing_w(a, R, et, epoch, &s_fail);
+    }
     if (s_fail) {
       if (et == 0) fail();
     } else {
       if (et == 0) tc::mbar_arrive(&routing_ready);
-      if (blockIdx.x == 0 && et < n && et % a.k < a.kr) {  // the router's top-k, [T][kr]
-        const int o = et / a.k * a.kr + et % a.k;
-        if (a.ids_out) a.ids_out[o] = R.ids[et];
-        if (a.w_out) a.w_out[o] = R.w[et];
+      if constexpr (W) {
+        // x into sorted order, this block's share, then counted
+        for (int i = blockIdx.x * EPI_THREADS + et; i < n * (H / 32); i += a.G * EPI_THREADS) sort_x_w<NV>(a, R, i);
+        tc::fence_proxy_async_global();
+        epi_sync();
+        if (et == 0) red_release_add(a.ctr + C_DC_READY, 1);
       }
+      if (blockIdx.x == 0)  // the router's top-k, [T][kr]
+        for (int i = et; i < n; i += EPI_THREADS)
+          if (i % a.k < a.kr) {
+            const int o = i / a.k * a.kr + i % a.k;
+            if (a.ids_out) a.ids_out[o] = R.ids[i];
+            if (a.w_out) a.w_out[o] = R.w[i];
+          }
       const int n_slots = R.n_slots;
       const int total = units_total(a, n_slots);
-      const int dn_total = nbH * ((a.shared ? a.s_sdn : 0) + n_slots);  // down parts over all tiles
+      const int dn_total = nbH * ((a.shared ? a.s_sdn * a.nck : 0) + n_slots);  // down parts over all tiles
       int i = 0;
       for (int u = blockIdx.x; u < total; u += a.G, ++i) {
         const Unit U = unit_at(a, n_slots, u);
@@ -917,14 +1280,16 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         }
         int ticket, target;
         if (U.kind == U_SGU) {
-          float* dst = a.gu_sh + (size_t)U.part * T * 2 * I + 128 * U.tile + m;
+          // column c is token 16 chunk + c
+          float* dst = a.gu_sh + ((size_t)U.part * T + 16 * U.chunk) * 2 * I + 128 * U.tile + m;
+          const int nt = imin(16, T - 16 * U.chunk);
 #pragma unroll
-          for (int t = 0; t < MAX_DECODE_T; ++t)
-            if (t < T) {
-              dst[(size_t)t * 2 * I] = v[t];
-              dst[(size_t)t * 2 * I + I] = v[16 + t];
+          for (int c = 0; c < 16; ++c)
+            if (c < nt) {
+              dst[(size_t)c * 2 * I] = v[c];
+              dst[(size_t)c * 2 * I + I] = v[16 + c];
             }
-          ticket = U.tile;
+          ticket = U.tile * a.nck + U.chunk;
           target = a.s_sgu;
         } else if (U.kind == U_RGU) {
           // B held every token row: slot row c is the column of its token
@@ -936,19 +1301,31 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             sg = __ldg(a.tscale + 3 * e);
             su = __ldg(a.tscale + 3 * e + 1);
           }
-          for (int c = 0; c < cnt; ++c) {
-            const int t = R.tok[beg + c];
-            const float f = NV ? pow2f(__ldcg(a.xshift + t)) : 1.0f;
-            dst[(size_t)c * 2 * I] = pick16(v, 0, t) * (sg * f);
-            dst[(size_t)c * 2 * I + I] = pick16(v, 16, t) * (su * f);
+          if constexpr (W) {
+            // wide steps: B held the slot's sorted rows, column c is position beg + c
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              if (c < cnt) {
+                const float f = NV ? pow2f(__ldcg(a.xshift + R.tok[beg + c])) : 1.0f;
+                dst[(size_t)c * 2 * I] = v[c] * (sg * f);
+                dst[(size_t)c * 2 * I + I] = v[16 + c] * (su * f);
+              }
+          } else {
+            for (int c = 0; c < cnt; ++c) {
+              const int t = R.tok[beg + c];
+              const float f = NV ? pow2f(__ldcg(a.xshift + t)) : 1.0f;
+              dst[(size_t)c * 2 * I] = pick16(v, 0, t) * (sg * f);
+              dst[(size_t)c * 2 * I + I] = pick16(v, 16, t) * (su * f);
+            }
           }
-          ticket = nbI + U.slot * nbI + U.tile;
+          ticket = a.tk_rgu + U.slot * nbI + U.tile;
           target = a.s_rgu;
         } else if (U.kind == U_SDN) {
-          float* dst = a.ys + (size_t)U.part * T * H + 128 * U.tile + m;
+          float* dst = a.ys + ((size_t)U.part * T + 16 * U.chunk) * H + 128 * U.tile + m;
+          const int nt = imin(16, T - 16 * U.chunk);
 #pragma unroll
-          for (int t = 0; t < MAX_DECODE_T; ++t)
-            if (t < T) dst[(size_t)t * H] = v[t];
+          for (int c = 0; c < 16; ++c)
+            if (c < nt) dst[(size_t)c * H] = v[c];
           ticket = -1;
           target = 0;
         } else {
@@ -987,17 +1364,18 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         if (U.kind == U_SGU) {
           const float* src = a.gu_sh + 128 * U.tile + m;
           const size_t stride = (size_t)T * 2 * I;
-          for (int t0 = 0; t0 < T; t0 += 2) {  // two tokens' loads in flight together
+          const int tb = 16 * U.chunk, te = imin(T, tb + 16);  // the chunk's tokens
+          for (int t0 = tb; t0 < te; t0 += 2) {  // two tokens' loads in flight together
             float g[2], up[2];
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
-              const int t = imin(t0 + tt, T - 1);
+              const int t = imin(t0 + tt, te - 1);
               g[tt] = sum_parts(src + (size_t)t * 2 * I, stride, a.s_sgu);
               up[tt] = sum_parts(src + (size_t)t * 2 * I + I, stride, a.s_sgu);
             }
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
-              if (t0 + tt < T) a.h_shared[(size_t)(t0 + tt) * I + 128 * U.tile + m] = f32_to_bf16_rn(silu(g[tt]) * up[tt]);
+              if (t0 + tt < te) a.h_shared[(size_t)(t0 + tt) * I + 128 * U.tile + m] = f32_to_bf16_rn(silu(g[tt]) * up[tt]);
           }
           tc::fence_proxy_async_global();
           epi_sync();
@@ -1035,16 +1413,16 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             reinterpret_cast<uint32_t*>(a.hs_mma)[((size_t)U.slot * nbI + U.tile) * 128 + et] = word;
             tc::fence_proxy_async_global();
             epi_sync();
-            if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
+            if (et == 0) red_release_add(a.tickets + a.tk_slot + U.slot, 1);
           } else {
             // NVFP4: the slot's last finished tile knows every row's largest
             // exponent and writes the slot's UE4M3 scale blocks for the down MMA
             if (et == 0) {
               __threadfence();
-              const int old = atomicAdd(a.tickets + nbI * (1 + a.nslot_max) + nbH + U.slot, 1);
+              const int old = atomicAdd(a.tickets + a.tk_nv + U.slot, 1);
               s_last = old == nbI - 1;
               if (s_last) {
-                a.tickets[nbI * (1 + a.nslot_max) + nbH + U.slot] = 0;
+                a.tickets[a.tk_nv + U.slot] = 0;
                 __threadfence();
               }
             }
@@ -1053,16 +1431,21 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               convert_h_scales_nv(a, U.slot, beg, cnt, et);
               tc::fence_proxy_async_global();
               epi_sync();
-              if (et == 0) red_release_add(a.ctr + C_DC_HR, 1);
+              if (et == 0) red_release_add(a.tickets + a.tk_slot + U.slot, 1);
             }
           }
         }
       }
       // out = BF16(ys + sum_j w_j y_j), summed in a fixed order, once every
-      // down part is stored.  Items (128 columns of H x 4 tokens) are spread
-      // over all blocks, so a block's items cost one load round trip each
-      // (on 32 blocks a 16-token step took four in a row).
-      const int n_items = nbH * ((T + 3) / 4);
+      // down part is stored.  Items (128 columns of H x CT tokens) are spread
+      // over all blocks.  The rows an item reads (per token its k y rows and
+      // the shared expert's down parts, 512 B each) come into the idle stage
+      // ring by bulk copies, all in flight at once, and are summed from
+      // shared memory, so an item costs one load round trip and the code,
+      // which runs once per launch, stays compact.
+      constexpr int CT = W ? 16 : 4;
+      const int n_items = nbH * ((T + CT - 1) / CT);
+      const int nsp = a.shared ? a.s_sdn : 0, rpt = k + nsp;  // rows per token
       if ((int)blockIdx.x < n_items) {
         if (et == 0) {
           s_ok = wait_at_least(a.ctr + C_DC_DN, dn_total, status, a.limit_ns);
@@ -1070,30 +1453,30 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         }
         epi_sync();
       }
-      for (int item = blockIdx.x; item < n_items && s_ok; item += a.G) {
-        const int col = 128 * (item % nbH) + m;
-        {
-          const int t0 = 4 * (item / nbH);  // four tokens' loads in flight together
-          float y[4][MAX_TOPK], ysh[4];
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            const int t = imin(t0 + tt, T - 1);
-#pragma unroll
-            for (int j = 0; j < MAX_TOPK; ++j)
-              y[tt][j] = j < k ? __ldcg(a.y_assign + (size_t)R.inv[t * k + j] * H + col) : 0.0f;
-            ysh[tt] = a.shared ? sum_parts<4>(a.ys + (size_t)t * H + col, (size_t)T * H, a.s_sdn) : 0.0f;
-          }
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            const int t = t0 + tt;
-            if (t < T) {
-              float acc = ysh[tt];
-#pragma unroll
-              for (int j = 0; j < MAX_TOPK; ++j)
-                if (j < k) acc = fmaf(R.w[t * k + j], y[tt][j], acc);
-              a.out[(size_t)t * H + col] = f32_to_bf16_rn(acc);
-            }
-          }
+      float* cbuf = reinterpret_cast<float*>(dsm);  // [CT][rpt][128]: the ring's consumers are done
+      uint32_t it = 0;
+      for (int item = blockIdx.x; item < n_items && s_ok; item += a.G, ++it) {
+        const int cg = item % nbH, t0 = CT * (item / nbH), nt = imin(CT, T - t0), nrows = nt * rpt;
+        if (et == 0) tc::mbar_expect_tx(&comb, (uint32_t)nrows * 512u);
+        epi_sync();  // the expected bytes precede every copy; the last item's reads are done
+        for (int r = et; r < nrows; r += EPI_THREADS) {
+          const int tt = r / rpt, j = r % rpt, t = t0 + tt;
+          const float* src = j < k ? a.y_assign + (size_t)R.inv[t * k + j] * H + 128 * cg
+                                   : a.ys + ((size_t)(j - k) * T + t) * H + 128 * cg;
+          tc::bulk_load(cbuf + (size_t)r * 128, src, 512, &comb);
+        }
+        if (!tc::mbar_wait(&comb, it & 1, a.limit_ns, &abort_flag)) {
+          fail();
+          tc::mbar_wait(&comb, it & 1, a.limit_ns, &never_s);  // the copies land before the block exits
+          break;
+        }
+        for (int tt = 0; tt < nt; ++tt) {
+          const int t = t0 + tt;
+          const float* row = cbuf + (size_t)tt * rpt * 128 + m;
+          float acc = 0.0f;
+          for (int p = 0; p < nsp; ++p) acc += row[(k + p) * 128];
+          for (int j = 0; j < k; ++j) acc = fmaf(R.w[t * k + j], row[j * 128], acc);
+          a.out[(size_t)t * H + 128 * cg + m] = f32_to_bf16_rn(acc);
         }
       }
     }
@@ -1115,13 +1498,15 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
   __syncthreads();
   if (s_last) {
     if (a.nv)
-      for (int i = threadIdx.x; i < MAXN; i += blockDim.x) a.rowmax[i] = 0ull;
+      for (int i = threadIdx.x; i < a.T * a.k; i += blockDim.x) a.rowmax[i] = 0ull;
+    for (int i = threadIdx.x; i < a.nslot_max; i += blockDim.x) a.tickets[a.tk_slot + i] = 0;
     if (threadIdx.x == 0) {
       a.ctr[C_DC_READY] = 0;
       a.ctr[C_DC_HSH] = 0;
       a.ctr[C_DC_HR] = 0;
       a.ctr[C_DC_EXIT] = 0;
       a.ctr[C_DC_DN] = 0;
+      a.ctr[C_DC_RT] = 0;
       a.ctr[C_DC_EPOCH] = (int)s_epoch;
     }
     __threadfence();
@@ -1131,7 +1516,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
 }  // namespace
 
 bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex) {
-  return ex.w13s_mma && ex.w2s_mma && sh.T >= 1 && sh.T <= MAX_DECODE_T && sh.H % 256 == 0 && sh.I % 256 == 0 &&
+  return ex.w13s_mma && ex.w2s_mma && sh.T >= 1 && sh.T <= MAX_WIDE_T && sh.H % 256 == 0 && sh.I % 256 == 0 &&
          (!ex.nv || sh.H <= 8192);  // the NVFP4 quantiser keeps a row's 32-block exponents in shared memory
 }
 
@@ -1148,7 +1533,9 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   // whose TMA stream would share the SM's copy engine.
   const size_t smem = (size_t)DSTAGES * (nv ? stage_bytes<true>() : stage_bytes<false>()) + 1024;
   static_assert(DSTAGES * stage_bytes<false>() + 1024 > 114 * 1024, "the ring must keep one block per SM");
-  auto kern = nv ? k_decode_tc<true> : k_decode_tc<false>;
+  const bool wide = T > MAX_DECODE_T;
+  auto kern = nv ? (wide ? k_decode_tc<true, true> : k_decode_tc<true, false>)
+                 : (wide ? k_decode_tc<false, true> : k_decode_tc<false, false>);
   cudaError_t err = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int per_sm = 0;
@@ -1171,9 +1558,13 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.s_sgu = sp.sgu;
   a.s_rgu = sp.rgu;
   a.s_sdn = sp.sdn;
-  a.n_sgu = shared ? (I / 128) * sp.sgu : 0;
-  a.n_sdn = shared ? (H / 128) * sp.sdn : 0;
-  a.nslot_max = imin(n, E);
+  a.nck = dc_nck(T);
+  a.n_sgu = shared ? (I / 128) * sp.sgu * a.nck : 0;
+  a.n_sdn = shared ? (H / 128) * sp.sdn * a.nck : 0;
+  a.nslot_max = dc_nslot_max(T, k, E);
+  a.tk_rgu = (I / 128) * a.nck;
+  a.tk_nv = a.tk_rgu + a.nslot_max * (I / 128) + H / 128;
+  a.tk_slot = a.tk_nv + a.nslot_max;
   a.shared = shared ? 1 : 0;
   a.nv = ex.nv;
   a.score = score;
@@ -1189,11 +1580,15 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.ctr = reinterpret_cast<int*>(base + L.counters);
   a.tickets = reinterpret_cast<int*>(base + L.dc_tickets);
   a.logit64 = reinterpret_cast<unsigned long long*>(base + L.dc_logit64);
-  a.xq = base + L.xq;
+  a.xq = wide ? base + L.dc_xqs : base + L.xq;
+  a.topk64 = reinterpret_cast<unsigned long long*>(base + L.dc_topk64);
+  a.rpart = reinterpret_cast<float*>(base + L.dc_rpart);
+  a.xq_tok = base + L.xq;  // [T, H/2]
+  a.xe_tok = base + L.xs;  // [T, H/32]
   a.xs_mma = base + L.dc_xs;
   a.xshift = reinterpret_cast<int*>(base + L.dc_xshift);
   a.hsc = base + L.dc_hsc;
-  a.depth = a.nslot_max >= 16 ? 4 : 2;
+  a.depth = imin(n, E) >= 16 ? 4 : 2;
   a.rowmax = reinterpret_cast<unsigned long long*>(base + L.dc_rowmax);
   a.hq = base + L.hq;
   a.hs_mma = base + L.dc_hs;
@@ -1208,7 +1603,7 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   memset(&m, 0, sizeof(m));
   if ((err = make_map(&m.w13r, ex.w13, (uint64_t)E * 2 * I, H / 2)) != cudaSuccess) return err;
   if ((err = make_map(&m.w2r, ex.w2, (uint64_t)E * H, I / 2)) != cudaSuccess) return err;
-  if ((err = make_map(&m.xq, a.xq, T, H / 2, 16)) != cudaSuccess) return err;
+  if ((err = make_map(&m.xq, a.xq, wide ? n : T, H / 2, 16)) != cudaSuccess) return err;
   if ((err = make_map(&m.hq, a.hq, n, I / 2, 16)) != cudaSuccess) return err;
   if (shared) {
     if ((err = make_map(&m.w13s, shd.w13, (uint64_t)2 * I, (uint64_t)2 * H)) != cudaSuccess) return err;

@@ -14,13 +14,14 @@ namespace moefp4 {
 
 constexpr int MAX_TOPK = 8;
 constexpr int MAX_E = 256;
-constexpr int MAX_DECODE_T = 16;   // fused single-launch decode range
+constexpr int MAX_DECODE_T = 16;   // fused single-launch decode range (both engines)
+constexpr int MAX_WIDE_T = 128;    // single-launch range of the tensor-core engine (17..128: wide steps)
 constexpr int PERM_CHUNK = 1024;   // assignments ranked per block in the permutation
 constexpr int TC_MIN_ASSIGN = 256; // routed experts on tensor cores from this many assignments
 constexpr int TC_MIN_T_SHARED = 128; // shared expert on tensor cores from this many tokens
 constexpr int SPLIT_SMS = 152;        // SMs the split-K counts are balanced for
 
-// Tensor-core decode (T <= MAX_DECODE_T): one block per SM, at most this many.
+// Tensor-core decode (T <= MAX_WIDE_T): one block per SM, at most this many.
 constexpr int DC_MAX_GRID = 256;
 constexpr int DC_MAX_SPLIT = 16;
 
@@ -35,6 +36,25 @@ MOE_HD inline int dc_split(int tiles, int stages, int grid) {
   return s < 1 ? 1 : s;
 }
 
+// The tensor-core decode's B operand holds 16 token rows.  Steps of up to 16
+// tokens have one such chunk; wider steps (17..MAX_WIDE_T tokens) run the
+// shared expert per 16-token chunk and the routed experts per slot, a run of
+// at most 16 sorted assignments of one expert.
+MOE_HD inline int dc_nck(int T) { return T <= MAX_DECODE_T ? 1 : (T + 15) / 16; }
+// Expert slots a step can have: one per distinct expert, plus (wide steps)
+// one more per 16 assignments of an expert.
+MOE_HD inline int dc_nslot_max(int T, int k, int E) {
+  const int n = T * k;
+  return T <= MAX_DECODE_T ? imin(n, E) : imin(n, E) + (n + 15) / 16;
+}
+// Arrival tickets: shared gate/up tiles per chunk, routed gate/up tiles per
+// slot, (unused) H tiles, NVFP4 per-slot scale tickets, then per-slot
+// counters of finished routed h (the down units' dependency).
+MOE_HD inline int dc_ticket_count(int T, int H, int I, int E, int k) {
+  const int ns = dc_nslot_max(T, k, E);
+  return (I / 128) * dc_nck(T) + ns * (I / 128) + H / 128 + 2 * ns;
+}
+
 // Split factors of the tensor-core decode: shared gate/up (K = H in 64-element
 // BF16 stages), routed gate/up (K = H in 256-element FP4 stages) and shared
 // down (K = I in stages of two 64-element chunks; four parts make a part the
@@ -44,10 +64,12 @@ struct DcSplits {
 };
 MOE_HD inline DcSplits dc_splits(int T, int H, int I, int E, int k, int grid) {
   const int nslot = imin(T * k, E);
+  const int nck = dc_nck(T);
   DcSplits d;
-  d.sgu = dc_split(I / 128, H / 64, grid);
+  d.sgu = dc_split(I / 128 * nck, H / 64, grid);
   d.rgu = dc_split((nslot > 0 ? nslot : 1) * (I / 128), H / 256 > 0 ? H / 256 : 1, grid);
   d.sdn = imin(4, (I / 64 + 1) / 2);
+  if (nck > 1) d.sdn = imin(d.sdn, dc_split(H / 128 * nck, (I / 64 + 1) / 2, grid));
   return d;
 }
 
@@ -131,6 +153,7 @@ enum Counter : int {
   C_DC_EXIT = 11,  // tensor-core decode: blocks finished
   C_DC_EPOCH = 12, // tensor-core decode: launches completed on this workspace (tags the logits)
   C_DC_DN = 13,    // tensor-core decode: down-projection parts stored
+  C_DC_RT = 14,    // tensor-core decode, wide steps: blocks done with their router parts
   N_COUNTERS = 16
 };
 
@@ -142,6 +165,7 @@ struct WsLayout {
   size_t dc_tickets;   // int: split-K arrival tickets of the tensor-core decode
   size_t dc_logit64;   // uint64 [T, E]: tensor-core decode logits tagged with the launch number
   size_t dc_rowmax;    // uint64 [T*k]: NVFP4 h row exponents tagged with the launch number
+  size_t dc_topk64;    // uint64 [2][T*k]: wide steps' router top-k (ids, weights) tagged with the launch number
   size_t zero_end;     // end of the part that must start zero-filled
   size_t logits;       // float [T, E]
   size_t rt_part;      // float [splits, T, E]: split-K parts of the batched router
@@ -176,9 +200,12 @@ struct WsLayout {
   size_t tc_hs;        // scale blocks [padded rows/128][I/128][512 B]
   size_t tc_w13s;      // weight scale blocks [E][2I/128][H/128][512 B]
   size_t tc_w2s;       // weight scale blocks [E][H/128][I/128][512 B]
-  // tensor-core decode (T <= MAX_DECODE_T)
-  size_t dc_xs;        // x scales, MMA layout [H/128][512 B] (E8M0) or [H/64][512 B] (UE4M3), 16 token rows
-  size_t dc_xshift;    // int [16]: NVFP4 per-row power of two of the x scales
+  // tensor-core decode (T <= MAX_WIDE_T)
+  size_t dc_xs;        // x scales, MMA layout [H/128][512 B] (E8M0) or [H/64][512 B] (UE4M3), 16 token
+                       // rows; wide steps: one such set per slot
+  size_t dc_xshift;    // int [16] (wide steps: [T*k]): NVFP4 per-row power of two of the x scales
+  size_t dc_xqs;       // wide steps: uint8 [T*k, H/2] x codes in sorted-assignment order
+  size_t dc_rpart;     // wide steps: float [H/256][T][E] router partial sums (256-element K parts)
   size_t dc_hs;        // routed h scales, MMA layout [slots][I/128][512 B] (E8M0) or [slots][I/64][512 B] (UE4M3)
   size_t dc_hsc;       // NVFP4: E8M0 bytes of h [T*k][I/32] before the per-row UE4M3 conversion
   size_t dc_gu_sh;     // float [splits][T][2I]  shared gate/up partial sums
@@ -202,17 +229,18 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
     o = align256(o + (bytes ? bytes : 1));
     return at;
   };
-  const bool dc = T <= MAX_DECODE_T;
-  const int nslot = imin(T * k, E);
+  const bool dc = T <= MAX_WIDE_T;
+  const bool wide = T > MAX_DECODE_T;
+  const int nslot = dc_nslot_max(T, k, E);
   const DcSplits sp = dc_splits(T, H, I, E, k, DC_MAX_GRID);
   // The regions the tensor-core decode needs zeroed (or tagged) across calls
-  // sit at the same offsets, sized for the whole decode range, in the layout
-  // of every T: no call of any size writes anything else there.
-  const int nslot_cap = imin(MAX_DECODE_T * k, E);
+  // sit at the same offsets, sized for the whole single-launch range, in the
+  // layout of every T: no call of any size writes anything else there.
   L.counters = take(sizeof(int) * N_COUNTERS);
-  L.dc_tickets = take(sizeof(int) * ((size_t)(1 + nslot_cap) * (I / 128) + H / 128 + nslot_cap));
-  L.dc_logit64 = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * E);
-  L.dc_rowmax = take(sizeof(uint64_t) * (size_t)MAX_DECODE_T * MAX_TOPK);
+  L.dc_tickets = take(sizeof(int) * (size_t)dc_ticket_count(MAX_WIDE_T, H, I, E, k));
+  L.dc_logit64 = take(sizeof(uint64_t) * (size_t)MAX_WIDE_T * E);
+  L.dc_rowmax = take(sizeof(uint64_t) * (size_t)MAX_WIDE_T * MAX_TOPK);
+  L.dc_topk64 = take(sizeof(uint64_t) * 2 * (size_t)MAX_WIDE_T * MAX_TOPK);
   L.zero_end = o;
   L.logits = take(sizeof(float) * (size_t)T * E);
   const size_t rparts = (size_t)imax(router_splits(T, E, H) * E, router_splits(T, Er, H) * Er);
@@ -259,8 +287,10 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.tc_hs = take(tiles * (I / 128) * 512);
   L.tc_w13s = take(tc ? (size_t)E * 2 * I * H / 32 : 0);
   L.tc_w2s = take(tc ? (size_t)E * H * I / 32 : 0);
-  L.dc_xs = take(dc ? (size_t)H / 64 * 512 : 0);
-  L.dc_xshift = take(dc ? sizeof(int) * MAX_DECODE_T : 0);
+  L.dc_xs = take(dc ? (size_t)(wide ? nslot : 1) * (H / 64) * 512 : 0);
+  L.dc_xshift = take(dc ? sizeof(int) * (wide ? n : (size_t)MAX_DECODE_T) : 0);
+  L.dc_xqs = take(wide ? n * H / 2 : 0);
+  L.dc_rpart = take(wide ? sizeof(float) * (size_t)(H / 256 > 0 ? H / 256 : 1) * T * E : 0);
   L.dc_hs = take(dc ? (size_t)nslot * (I / 64) * 512 : 0);
   L.dc_hsc = take(dc ? n * (I / 32) : 0);
   L.dc_gu_sh = take(dc ? sizeof(float) * sp.sgu * T * 2 * (size_t)I : 0);

@@ -99,9 +99,9 @@ def test_shapes_in_whole_mxfp4_blocks_accepted(lib, H, I):
 def test_decode_range_and_workspace_checks(lib):
     ex = M.Experts(M.MOE_W_MXFP4, 4096, 4096, 4096, 4096, None)
     sh = M.SharedBF16(None, None)
-    d17 = M.desc(17, 512, 256, 16, 4)
-    # more than 16 tokens is outside the fused decode range
-    assert lib.moe_layer_decode(ctypes.byref(d17), ctypes.byref(ex), ctypes.byref(sh), 4096, None, 4096,
+    d129 = M.desc(129, 512, 256, 16, 4)
+    # more than 128 tokens is outside the single-launch range
+    assert lib.moe_layer_decode(ctypes.byref(d129), ctypes.byref(ex), ctypes.byref(sh), 4096, None, 4096,
                                 4096, None, None, 4096, 1 << 30, None) == M.MOE_ERR_UNSUPPORTED
     d4 = M.desc(4, 512, 256, 16, 4)
     need = M.moe_workspace_size(d4)

@@ -435,15 +435,61 @@ def test_decode_token_counts(T, prepared):
     out, ids, _ = dev.decode(bf16_tensor(sub["x"]))
     torch.cuda.synchronize()
     _compare_layer(wl.with_tokens(T), sub, cache, out, ids)
-    # 17 tokens is past the fused decode range: rejected before any launch
-    d17 = M.desc(17, wl.H, wl.I, wl.E, wl.top_k)
-    ws17 = torch.zeros(M.moe_workspace_size(d17), dtype=torch.uint8, device="cuda")
-    x17 = bf16_tensor(np.zeros((17, wl.H), np.uint16))
-    o17 = torch.empty((17, wl.H), dtype=torch.int16, device="cuda")
-    with pytest.raises(M.MoeError) as e:
-        M.moe_layer_decode(d17, dev.ex, dev.sh, dev.w_router, dev.bias, x17, o17, None, None, ws17)
-    assert e.value.status == M.MOE_ERR_UNSUPPORTED
     dev.set_prepared(True)
+
+
+@pytest.mark.parametrize("shape", [
+    (17, 512, 256, 16, 4, W.MXFP4, {}),
+    (33, 512, 512, 32, 4, W.NVFP4, {}),
+    (64, 768, 256, 64, 6, W.MXFP4, dict(shared=False)),
+    (100, 256, 512, 255, 8, W.MXFP4, {}),
+    (128, 512, 256, 16, 7, W.NVFP4, dict(shared=False, shared_fp4=True)),
+    (128, 256, 256, 8, 8, W.MXFP4, {}),
+    (96, 512, 256, 32, 4, W.MXFP4, dict(score="sigmoid", zipf=0.05)),
+], ids=["T17", "T33_nvfp4", "T64_k6_noshared", "T100_E255_k8", "T128_nvfp4_fold_n1024", "T128_dense",
+        "T96_sigmoid"])
+def test_wide_single_launch_shapes(shape):
+    """Steps of 17-128 tokens through moe_layer_decode, one launch: a ragged
+    last 16-token chunk (17, 33, 100), E = 255 with k = 8 (800 assignments),
+    the folded shared expert at the largest table step (128 tokens x 8 = 1024
+    assignments, every expert split over several 16-row slots), a dense
+    mixture (E == k: 128 rows per expert, 8 slots each), NVFP4 with distinct
+    tensor scales, sigmoid scoring.  Every token against the oracle; the
+    launch is bit-reproducible and agrees with the batched path."""
+    T, H, I, E, k, fmt, kw = shape
+    # router weights of std 0.08: logits of std ~1-2 (the workloads' regime),
+    # where the FP32 router's rounding stays far below the weights' rtol
+    wl = W.Workload("wide", T, H, I, E, k, fmt, 27, 0.08, **kw)
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, H, I, E, k, wl.fmt, T_max=T)
+    assert dev.prepared
+    x = bf16_tensor(lay["x"])
+    n0 = M.moe_debug_launch_count()
+    out, ids, w = dev.decode(x)
+    torch.cuda.synchronize()
+    assert M.moe_debug_launch_count() == n0 + 1
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, {}, out, ids, w=w)
+    out2, ids2, _ = dev.decode(x)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(ids, ids2)
+    out_f, ids_f, _ = dev.forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_f)
+    assert normwise(bits_to_float(out), bits_to_float(out_f)) <= 1e-2
+
+
+@pytest.mark.parametrize("name", ["batch128", "batch128_sfp4", "batch128_sig"])
+def test_batch128_single_launch_every_token(name):
+    """The 128-token step at full size (H = 4096, I = 1536, E = 128, top-4)
+    in one launch of the tensor-core decode, every token against the oracle."""
+    wl, lay, dev, cache = _workload(name)
+    n0 = M.moe_debug_launch_count()
+    out, ids, w = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_debug_launch_count() == n0 + 1
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, cache, out, ids, w=w)
 
 
 @pytest.fixture
@@ -691,7 +737,7 @@ def test_tensor_core_decode_shapes(shape):
 
 
 def test_decode_after_large_forward_on_one_workspace():
-    """A workspace sized for a 300-token forward also serves decode steps:
+    """A workspace sized for a 300-token forward also serves single-launch steps:
     the forward's scratch never lands where the decode expects its zeroed
     tickets and launch-tagged logits."""
     H, I, E, k = 512, 256, 16, 4
@@ -702,7 +748,7 @@ def test_decode_after_large_forward_on_one_workspace():
     for _ in range(2):
         out, ids, _ = dev.forward(bf16_tensor(lay["x"]))
         torch.cuda.synchronize()
-        for T in (1, 5, 16):
+        for T in (1, 5, 16, 40):
             sub = dict(lay)
             sub["x"] = lay["x"][:T]
             o, i, _ = dev.decode(bf16_tensor(sub["x"]))
