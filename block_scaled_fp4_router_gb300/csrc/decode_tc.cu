@@ -872,20 +872,23 @@ __device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, 
     const uint32_t sfc = sf_chunk<NV>();
     const size_t bpr = (size_t)a.H / 256 * (sfc / 512);  // scale blocks per 128-row tile
     const size_t rt = (size_t)e * (2 * nbI) + U.tile;    // gate row tile; the up tile is nbI further
-    tc::tma_load_2d(sp + ST_A0, &m.w13r, st * 128, row, fb);
-    tc::tma_load_2d(sp + ST_A1, &m.w13r, st * 128, row + a.I, fb);
-    tc::bulk_load(sp + ST_SFA, a.w13s_mma + rt * bpr * 512 + (size_t)st * sfc, sfc, fb);
-    tc::bulk_load(sp + ST_SFA + sfc, a.w13s_mma + (rt + nbI) * bpr * 512 + (size_t)st * sfc, sfc, fb);
+    const uint64_t pol = tc::l2_evict_first();  // routed weights are read once per step
+    tc::tma_load_2d_hint(sp + ST_A0, &m.w13r, st * 128, row, fb, pol);
+    tc::tma_load_2d_hint(sp + ST_A1, &m.w13r, st * 128, row + a.I, fb, pol);
+    tc::bulk_load_hint(sp + ST_SFA, a.w13s_mma + rt * bpr * 512 + (size_t)st * sfc, sfc, fb, pol);
+    tc::bulk_load_hint(sp + ST_SFA + sfc, a.w13s_mma + (rt + nbI) * bpr * 512 + (size_t)st * sfc, sfc, fb, pol);
   } else if (U.kind == U_SDN) {
     for (int h = 0; h < stage_halves(a, U, st); ++h)
       tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &m.w2s, (2 * st + h) * 128, 128 * U.tile, fb);
   } else {
     const int halves = stage_halves(a, U, st);
+    const uint64_t pol = tc::l2_evict_first();
     for (int h = 0; h < halves; ++h)
-      tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &m.w2r, (2 * st + h) * 128, e * a.H + 128 * U.tile, fb);
+      tc::tma_load_2d_hint(sp + (h ? ST_A1 : ST_A0), &m.w2r, (2 * st + h) * 128, e * a.H + 128 * U.tile, fb, pol);
     const uint32_t sfc = sf_chunk<NV>();
     const size_t bpr = (size_t)a.I / 256 * (sfc / 512);
-    tc::bulk_load(sp + ST_SFA, a.w2s_mma + ((size_t)e * nbH + U.tile) * bpr * 512 + (size_t)2 * st * sfc, halves * sfc, fb);
+    tc::bulk_load_hint(sp + ST_SFA, a.w2s_mma + ((size_t)e * nbH + U.tile) * bpr * 512 + (size_t)2 * st * sfc,
+                       halves * sfc, fb, pol);
   }
 }
 
@@ -1068,7 +1071,9 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         if (dep_sdn || dep_rdn || dep_rgu) {
           int* cnt = dep_sdn ? a.ctr + C_DC_HSH : dep_rdn ? a.tickets + a.tk_slot + U.slot : a.ctr + C_DC_READY;
           const int target = dep_sdn ? nbI * a.nck : dep_rdn ? (NV ? 1 : nbI) : a.G;
-          if (ld_acquire(cnt) < target) {
+          // a routed down unit's weights go into the ring before its slot's
+          // counter is read, so that load overlaps the weight copies
+          if (dep_rdn || ld_acquire(cnt) < target) {
             npre = imin(U.st1 - U.st0, a.depth);
             bool ok = true;
             for (int j = 0; j < npre; ++j) {
