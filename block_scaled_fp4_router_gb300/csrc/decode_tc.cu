@@ -93,6 +93,7 @@ template <bool W> __host__ __device__ constexpr int maxslot() {
 }
 template <bool W> __host__ __device__ constexpr int maxt() { return W ? MAX_WIDE_T : MAX_DECODE_T; }
 constexpr int EH = MAX_E + 2;  // per-expert table stride (the table holds up to MAX_E + 1 experts)
+constexpr int DC_SDN_MAX = 4;  // shared down parts (dc_splits caps them at 4)
 
 enum UnitKind { U_SGU = 0, U_RGU = 1, U_SDN = 2, U_RDN = 3 };
 
@@ -128,6 +129,7 @@ struct DcArgs {
   int* xshift;               // NVFP4: [16] per-row power of two of the UE4M3 x scales; wide steps: [T k]
   unsigned long long* topk64;  // wide steps: [2][T kr] (launch number << 32) | expert id, | weight bits
   float* rpart;              // wide steps: [H/256][T][Er] router partial sums
+  int pf_experts;            // wide steps: experts whose gate/up weights go to L2 during the routing
   uint8_t* xq_tok;           // wide steps: [T, H/2] x codes in token order (before the routing)
   uint8_t* xe_tok;           // wide steps: [T, H/32] their E8M0 exponent bytes
   unsigned long long* rowmax;  // NVFP4: [T k] (launch << 32) | (largest h scale exponent + 256)
@@ -1031,7 +1033,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         return tc::mbar_wait(&empty[j % DSTAGES], (j / DSTAGES) & 1, a.limit_ns, &abort_flag);
       };
       int n_slots = -1;
-      bool hsh_ok = false, xr_ok = false;
+      bool hsh_ok = false, xr_ok = false, all_h = false;
       tc::prefetch_tensormap(&maps.w13r);
       tc::prefetch_tensormap(&maps.w2r);
       tc::prefetch_tensormap(&maps.xq);
@@ -1041,6 +1043,20 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         tc::prefetch_tensormap(&maps.w2s);
         tc::prefetch_tensormap(&maps.x);
         tc::prefetch_tensormap(&maps.hsh);
+      }
+      if (W && a.pf_experts > 0) {
+        // A wide step that touches about every expert: while the routing is
+        // computed (HBM is otherwise nearly idle then), the gate/up weights
+        // and scales of the first experts go to L2, so the first routed
+        // units (slots in ascending expert order) start from L2.
+        const int kb = a.H / 256, nbox = (2 * a.I / 128) * kb;  // 128-row x 128-byte boxes per expert
+        for (int b = blockIdx.x; b < a.pf_experts * nbox; b += a.G) {
+          const int e = b / nbox, r = b % nbox;
+          tc::tma_prefetch_2d(&maps.w13r, (r % kb) * 128, e * 2 * a.I + 128 * (r / kb));
+        }
+        const size_t sbytes = (size_t)a.pf_experts * 2 * a.I * (a.H / (NV ? 16 : 32));
+        for (size_t o = (size_t)blockIdx.x * 16384; o < sbytes; o += (size_t)a.G * 16384)
+          tc::bulk_prefetch_l2(a.w13s_mma + o, (uint32_t)(sbytes - o < 16384 ? sbytes - o : 16384));
       }
       for (int u = blockIdx.x;; u += a.G) {
         if (u >= a.n_sgu && n_slots < 0) {
@@ -1066,9 +1082,12 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         // depth); their activation tiles follow once the dependency is met.
         int npre = 0;
         uint32_t pre_stage[DSTAGES];
-        const bool dep_sdn = U.kind == U_SDN && !hsh_ok, dep_rdn = U.kind == U_RDN;
+        const bool dep_sdn = U.kind == U_SDN && !hsh_ok, dep_rdn = U.kind == U_RDN && !all_h;
         const bool dep_rgu = W && U.kind == U_RGU && !xr_ok;
         if (dep_sdn || dep_rdn || dep_rgu) {
+          // every slot's h finished (relaxed load, read with the unit's own
+          // dependency below): later down units need no check at all
+          const int h_done = dep_rdn ? ld_relaxed(a.ctr + C_DC_HR) : 0;
           int* cnt = dep_sdn ? a.ctr + C_DC_HSH : dep_rdn ? a.tickets + a.tk_slot + U.slot : a.ctr + C_DC_READY;
           const int target = dep_sdn ? nbI * a.nck : dep_rdn ? (NV ? 1 : nbI) : a.G;
           // a routed down unit's weights go into the ring before its slot's
@@ -1094,6 +1113,10 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           }
           if (dep_sdn) hsh_ok = true;
           else if (dep_rgu) xr_ok = true;
+          else if (h_done >= (NV ? n_slots : n_slots * nbI)) {
+            __threadfence();  // with the relaxed load above: acquires every slot's h
+            all_h = true;
+          }
           tc::fence_proxy_async_global();
         }
         for (int j = 0; j < npre; ++j)
@@ -1418,7 +1441,10 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             reinterpret_cast<uint32_t*>(a.hs_mma)[((size_t)U.slot * nbI + U.tile) * 128 + et] = word;
             tc::fence_proxy_async_global();
             epi_sync();
-            if (et == 0) red_release_add(a.tickets + a.tk_slot + U.slot, 1);
+            if (et == 0) {
+              red_release_add(a.tickets + a.tk_slot + U.slot, 1);
+              red_release_add(a.ctr + C_DC_HR, 1);
+            }
           } else {
             // NVFP4: the slot's last finished tile knows every row's largest
             // exponent and writes the slot's UE4M3 scale blocks for the down MMA
@@ -1436,7 +1462,10 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               convert_h_scales_nv(a, U.slot, beg, cnt, et);
               tc::fence_proxy_async_global();
               epi_sync();
-              if (et == 0) red_release_add(a.tickets + a.tk_slot + U.slot, 1);
+              if (et == 0) {
+                red_release_add(a.tickets + a.tk_slot + U.slot, 1);
+                red_release_add(a.ctr + C_DC_HR, 1);
+              }
             }
           }
         }
@@ -1478,9 +1507,21 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         for (int tt = 0; tt < nt; ++tt) {
           const int t = t0 + tt;
           const float* row = cbuf + (size_t)tt * rpt * 128 + m;
+          float yv[MAX_TOPK], wv[MAX_TOPK], pv[DC_SDN_MAX];  // a token's loads issued together
+#pragma unroll
+          for (int j = 0; j < MAX_TOPK; ++j) {
+            yv[j] = j < k ? row[j * 128] : 0.0f;
+            wv[j] = j < k ? R.w[t * k + j] : 0.0f;
+          }
+#pragma unroll
+          for (int p = 0; p < DC_SDN_MAX; ++p) pv[p] = p < nsp ? row[(k + p) * 128] : 0.0f;
           float acc = 0.0f;
-          for (int p = 0; p < nsp; ++p) acc += row[(k + p) * 128];
-          for (int j = 0; j < k; ++j) acc = fmaf(R.w[t * k + j], row[j * 128], acc);
+#pragma unroll
+          for (int p = 0; p < DC_SDN_MAX; ++p)
+            if (p < nsp) acc += pv[p];
+#pragma unroll
+          for (int j = 0; j < MAX_TOPK; ++j)
+            if (j < k) acc = fmaf(wv[j], yv[j], acc);
           a.out[(size_t)t * H + 128 * cg + m] = f32_to_bf16_rn(acc);
         }
       }
@@ -1588,6 +1629,10 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.xq = wide ? base + L.dc_xqs : base + L.xq;
   a.topk64 = reinterpret_cast<unsigned long long*>(base + L.dc_topk64);
   a.rpart = reinterpret_cast<float*>(base + L.dc_rpart);
+  {  // wide steps with about as many assignments as experts: ~80 MB of the first experts' W13 to L2
+    const double per = (double)2 * I * (H / 2) * (1.0 + (nv ? 1.0 / 8 : 1.0 / 16));
+    a.pf_experts = wide && n >= E ? imin(E - fold, (int)(80e6 / per)) : 0;
+  }
   a.xq_tok = base + L.xq;  // [T, H/2]
   a.xe_tok = base + L.xs;  // [T, H/32]
   a.xs_mma = base + L.dc_xs;

@@ -132,6 +132,11 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
                : "memory");
 }
 
+// Pulls `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Orders this thread's generic-proxy global accesses with async-proxy (TMA)
 // accesses: after plain stores that a TMA load elsewhere will read, and
 // before TMA loads of data that plain stores elsewhere produced.
