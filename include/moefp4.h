@@ -320,14 +320,18 @@ MOE_API moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_as
 
 /* A10: the whole layer in one launch for decode steps of 1 to 16 tokens
  * (AMD article, section "What we Optimized": one fused launch per MoE layer
- * for pure decode steps of at most 16 tokens).  T > 16 returns
- * MOE_ERR_UNSUPPORTED (use moe_layer_forward).
+ * for pure decode steps of at most 16 tokens), and for wider steps of 17 to
+ * 128 tokens (the article's section "What's next": wider mono steps).
+ * T > 128 returns MOE_ERR_UNSUPPORTED (use moe_layer_forward).
  *   x          BF16 [T, H];  out BF16 [T, H]
  *   topk_ids   int32 [T, top_k] out or NULL;  topk_w FP32 [T, top_k] out or NULL
- * The launch is persistent (one block per SM slot); its dependency waits are
- * bounded and report MOE_ERR_TIMEOUT through moe_get_status.  Shapes whose H
- * or I is not a multiple of 64 run as the per-step sequence of
- * moe_layer_forward instead (same arithmetic, several launches). */
+ * The launch is persistent (one block per SM); its dependency waits are
+ * bounded and report MOE_ERR_TIMEOUT through moe_get_status.  One launch
+ * needs the routed experts' prepared scales (moe_prepare_weights) and H, I
+ * multiples of 256 for 17-128 tokens; up to 16 tokens, H and I multiples of
+ * 64 also run in one launch on CUDA cores.  Other cases run as the per-step
+ * sequence of moe_layer_forward (same arithmetic, several launches).  The
+ * output is bit-reproducible run to run on the one-launch paths. */
 MOE_API moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_experts_t* experts,
                               const moe_shared_bf16_t* shared, const float* w_router,
                               const float* bias, const void* x, void* out, int32_t* topk_ids,
