@@ -9,7 +9,8 @@ I=1536, 128 MXFP4 experts, top-4 under a Zipf(1.1) router bias, BF16 shared
 expert) through moe_layer_forward; the other layer workloads (tiny, 1-token
 decode, 16-token NVFP4 decode uniform and Zipf(1.2), the 128-token batch
 through moe_layer_forward and, as "batch128@decode", through the
-single-launch moe_layer_decode, the prefill with an MXFP8 shared expert) are
+single-launch moe_layer_decode (also with an MXFP8 shared expert), the
+prefill with an MXFP8 shared expert) are
 measured in the same run under "per_config".
 
 Timing (every workload): S steps are captured in a CUDA graph and replayed R
@@ -50,7 +51,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s; decode expert-weight HBM GB/s; prefill FP4 TFLOPS vs peak"
 N_LAYERS = 8
 # "name@decode": the workload through moe_layer_decode (one launch) whatever its size
-PER_CONFIG = ["tiny", "decode1", "decode16", "decode16z", "batch128", "batch128@decode", "prefill8k_s8"]
+PER_CONFIG = ["tiny", "decode1", "decode16", "decode16z", "batch128", "batch128@decode", "batch128_s8@decode",
+              "prefill8k_s8"]
 # nominal dense GB300 tensor rates (PFLOP/s): FP4 13.5, BF16 2.25
 FP4_PER_BF16 = 13.5 / 2.25
 MIN_REGION_S = 1.0
@@ -365,7 +367,9 @@ def measure(wl, args, dev, rank, world, pk, headline: bool, entry=None):
     byts = np.array([step_bytes(wl, int(n)) for n in distinct], dtype=np.float64)
     ms_step = ms / K
     res = {
-        "workload": describe(wl), "entry_point": "moe_layer_decode" if fused else "moe_layer_forward",
+        "workload": describe(wl),
+        "entry_point": ("moe_layer_decode" if fused else "moe_layer_forward")
+        + ("_shared_mxfp8" if wl.shared and wl.shared_fmt == "mxfp8" else ""),
         "tokens_per_step": T, "value": replica_throughput(ms, world, T, K), "unit": "tokens/s",
         "ms_per_step": ms_step, "steps": K,
         "timing": {"regions": len(regions), "region_ms_median": statistics.median(regions),

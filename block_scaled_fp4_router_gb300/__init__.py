@@ -34,6 +34,7 @@ EXPORTED = [
     "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8", "moe_shared_expert_mxfp8",
     "moe_noalloc_get_status", "moe_debug_wait_probe_noalloc", "moe_debug_launch_count", "moe_set_timing_events",
     "moe_dequant_mxfp8_to_bf16", "moe_prepare_shared_mxfp8", "moe_layer_forward_shared_mxfp8",
+    "moe_layer_decode_shared_mxfp8",
     "moe_debug_shared_mxfp8_h",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -116,6 +117,7 @@ def load(path: str = None) -> ctypes.CDLL:
         "moe_dequant_mxfp8_to_bf16": ([I32, I32, P, P, P, P], ctypes.c_int),
         "moe_prepare_shared_mxfp8": ([P, P, P, P, P], ctypes.c_int),
         "moe_layer_forward_shared_mxfp8": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
+        "moe_layer_decode_shared_mxfp8": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
         "moe_debug_shared_mxfp8_h": ([P, P, S, P, P, P], ctypes.c_int),
         "moe_set_timing_events": ([P, P], None),
         "moe_debug_requantized_h": ([P, P, S, P, P, P], ctypes.c_int),
@@ -260,6 +262,12 @@ def moe_layer_forward_shared_mxfp8(d, ex, sh8, w_router, bias, x, out, topk_ids,
     _check(load().moe_layer_forward_shared_mxfp8(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh8), _p(w_router),
                                                  _p(bias), _p(x), _p(out), _p(topk_ids), _p(topk_w), _p(ws),
                                                  _nbytes(ws), _stream(stream)), "moe_layer_forward_shared_mxfp8")
+
+
+def moe_layer_decode_shared_mxfp8(d, ex, sh8, w_router, bias, x, out, topk_ids, topk_w, ws, stream=None):
+    _check(load().moe_layer_decode_shared_mxfp8(ctypes.byref(d), ctypes.byref(ex), ctypes.byref(sh8), _p(w_router),
+                                                 _p(bias), _p(x), _p(out), _p(topk_ids), _p(topk_w), _p(ws),
+                                                 _nbytes(ws), _stream(stream)), "moe_layer_decode_shared_mxfp8")
 
 
 def moe_debug_shared_mxfp8_h(d, ws, hq, hs, stream=None):

@@ -545,6 +545,33 @@ moe_status_t moe_layer_forward_shared_mxfp8(const moe_layer_desc_t* desc, const 
                      static_cast<uint16_t*>(out), topk_ids, topk_w, ws, reinterpret_cast<cudaStream_t>(stream), &sh8);
 }
 
+moe_status_t moe_layer_decode_shared_mxfp8(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                           const moe_shared_mxfp8_t* shared, const float* w_router,
+                                           const float* bias, const void* x, void* out, int32_t* topk_ids,
+                                           float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_RANGE();
+  MOE_TRY(check_desc(desc));
+  if (desc->T > MAX_WIDE_T) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_ws(desc, ws, ws_bytes));
+  ExpertsDev ex;
+  Shared8Dev sh8;
+  MOE_TRY(check_experts(desc, experts, &ex));
+  MOE_TRY(check_shared8(desc, shared, &sh8));
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !out || !w_router || !aligned(x, 16) || !aligned(out, 16) || !aligned(w_router, 16))
+    return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  uint16_t* ob = static_cast<uint16_t*>(out);
+  // One launch needs the routed experts' and the shared expert's prepared
+  // scales; otherwise the batched path with the same arithmetic.
+  if (fused_decode_tc_supported(shape_of(desc), ex) && sh8.w13s_mma && sh8.w2s_mma)
+    return cuda_status(launch_fused_decode_tc(shape_of(desc), ex, SharedDev{nullptr, nullptr}, w_router, bias, xb,
+                                              ob, topk_ids, topk_w, ws, g_wait_limit_ns.load(), s, 0,
+                                              desc->score_func, &sh8));
+  return run_forward(desc, ex, SharedDev{nullptr, nullptr}, w_router, bias, xb, ob, topk_ids, topk_w, ws, s, &sh8);
+}
+
 moe_status_t moe_combine(const moe_layer_desc_t* desc, const float* y_assign, const int32_t* inv_perm,
                          const float* topk_w, const float* y_shared, void* out, moe_stream_t stream) {
   MOE_RANGE();

@@ -137,6 +137,24 @@ __device__ __forceinline__ uint2 e4m3x8_rne(const float (&v)[8], float inv) {
   return make_uint2(clear_neg_zero(lo), clear_neg_zero(hi));
 }
 
+// One E4M3 code of v (the hardware's nearest-even conversion, saturating at
+// +-448); a code of magnitude 0 is +0.
+__device__ __forceinline__ uint32_t e4m3_rne1(float v) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 h;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n\tcvt.u32.u16 %0, h;\n\t}"
+      : "=r"(w)
+      : "f"(v), "f"(0.0f));
+  w &= 0xFFu;
+  return (w & 0x7Fu) ? w : 0u;
+}
+
+// MXFP8 scale exponent of a 32-element block: X = 2^(floor(log2 amax) - 8),
+// -127 for an all-zero block (or a subnormal amax).
+__device__ __forceinline__ int mx8_scale_exp(float amax) {
+  const int ef = (int)((__float_as_uint(amax) >> 23) & 0xff);
+  return ef == 0 ? -127 : max(ef - 127 - 8, -127);
+}
+
 // One thread quantises 8 consecutive BF16 values x[8g .. 8g+7] to MXFP8
 // (E4M3, one E8M0 scale per 32: X = 2^(floor(log2 amax) - 8)); the 4 threads
 // of a block share their maxima with two shuffles, as in quant8_values.

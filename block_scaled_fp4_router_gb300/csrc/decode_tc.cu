@@ -130,6 +130,12 @@ struct DcArgs {
   unsigned long long* topk64;  // wide steps: [2][T kr] (launch number << 32) | expert id, | weight bits
   float* rpart;              // wide steps: [H/256][T][Er] router partial sums
   int pf_experts;            // wide steps: experts whose gate/up weights go to L2 during the routing
+  int sh8;                   // the shared expert in MXFP8 (E4M3 codes, UE8M0 scales per 32)
+  const uint8_t* w13s8_mma;  // its prepared scales: [2I/128][H/128][512 B], [H/128][I/128][512 B]
+  const uint8_t* w2s8_mma;
+  uint8_t* x8;               // MXFP8 shared expert: x codes [T, H]; scales [16-token chunks][H/128][512 B]
+  uint8_t* x8s;
+  uint8_t* h8s;              // h's scales [16-token chunks][I/128][512 B] (codes [T, I] in h_shared)
   uint8_t* xq_tok;           // wide steps: [T, H/2] x codes in token order (before the routing)
   uint8_t* xe_tok;           // wide steps: [T, H/32] their E8M0 exponent bytes
   unsigned long long* rowmax;  // NVFP4: [T k] (launch << 32) | (largest h scale exponent + 256)
@@ -199,7 +205,7 @@ __device__ __forceinline__ Unit sdn_unit(const DcArgs& a, int v) {
   v /= a.nck;
   U.tile = v / a.s_sdn;
   U.part = v % a.s_sdn;
-  part_range((a.I / 64 + 1) / 2, a.s_sdn, U.part, U.st0, U.st1);
+  part_range((a.I / (a.sh8 ? 128 : 64) + 1) / 2, a.s_sdn, U.part, U.st0, U.st1);
   return U;
 }
 
@@ -225,7 +231,7 @@ __device__ Unit unit_at(const DcArgs& a, int n_slots, int u) {
     u /= a.nck;
     U.tile = u / a.s_sgu;
     U.part = u % a.s_sgu;
-    part_range(a.H / 64, a.s_sgu, U.part, U.st0, U.st1);
+    part_range(a.H / (a.sh8 ? 128 : 64), a.s_sgu, U.part, U.st0, U.st1);  // K stages of 128 bytes per row
     return U;
   }
   u -= a.n_sgu;
@@ -453,6 +459,44 @@ __device__ __forceinline__ uint8_t quant32(const uint16_t* xb, uint8_t* dq) {
   }
   *reinterpret_cast<uint4*>(dq) = make_uint4(c[0], c[1], c[2], c[3]);
   return (uint8_t)(ex + 127);
+}
+
+// MXFP8 codes of one 32-element BF16 block (32 bytes to dq) and its E8M0
+// byte, the rule of the standalone MXFP8 quantiser.
+__device__ __forceinline__ uint8_t quant32_mx8(const uint16_t* xb, uint8_t* dq) {
+  const uint4* src = reinterpret_cast<const uint4*>(xb);
+  uint4 raw[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) raw[j] = __ldg(src + j);
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+  }
+  const int ex = mx8_scale_exp(amax);
+  const float inv = pow2_neg(ex);
+#pragma unroll 1
+  for (int j = 0; j < 4; ++j) {
+    const float v[8] = {bf16_lo(raw[j].x), bf16_hi(raw[j].x), bf16_lo(raw[j].y), bf16_hi(raw[j].y),
+                        bf16_lo(raw[j].z), bf16_hi(raw[j].z), bf16_lo(raw[j].w), bf16_hi(raw[j].w)};
+    reinterpret_cast<uint2*>(dq)[j] = e4m3x8_rne(v, inv);
+  }
+  return (uint8_t)(ex + 127);
+}
+
+// MXFP8 shared expert: x to x8 (token rows, 32-element block per item) and
+// its scale bytes in the MMA layout of the 16-row B tiles, [chunk][H/128]
+// [512 B], row t % 16; the rows past T of the last chunk get zero scales.
+__device__ void quant_x8(const DcArgs& a, int et) {
+  const int nb = a.H / 32, rows = 16 * a.nck;
+  for (int i = blockIdx.x * EPI_THREADS + et; i < rows * nb; i += a.G * EPI_THREADS) {
+    const int t = i / nb, b = i % nb;
+    uint8_t sb = 0;
+    if (t < a.T) sb = quant32_mx8(a.x + (size_t)t * a.H + b * 32, a.x8 + (size_t)t * a.H + b * 32);
+    a.x8s[((size_t)(t >> 4) * (a.H / 128) + b / 4) * 512 + (t & 15) * 16 + (b % 4)] = sb;
+  }
 }
 
 // MXFP4 quantisation of one 32-element block i = (token row t < 16, block b
@@ -841,7 +885,7 @@ __device__ void build_routing_w(const DcArgs& a, DcRouting<true>& R, int et, uin
 // tiles, one activation tile), down units two K chunks (the second may be
 // past the end of K).
 __device__ __forceinline__ int stage_halves(const DcArgs& a, const Unit& U, int st) {
-  if (U.kind == U_SDN) return 2 * st + 1 < a.I / 64 ? 2 : 1;
+  if (U.kind == U_SDN) return 2 * st + 1 < a.I / (a.sh8 ? 128 : 64) ? 2 : 1;
   if (U.kind == U_RDN) return 2 * st + 1 < a.I / 256 ? 2 : 1;
   return 2;
 }
@@ -854,9 +898,9 @@ template <bool NV>
 __device__ __forceinline__ uint32_t stage_tx(const DcArgs& a, const Unit& U, int st) {
   const uint32_t h = stage_halves(a, U, st);
   switch (U.kind) {
-    case U_SGU: return 2 * A_TILE + B_TILE;
+    case U_SGU: return 2 * A_TILE + B_TILE + (a.sh8 ? 3 * 512 : 0);
     case U_RGU: return 2 * A_TILE + B_TILE + 3 * sf_chunk<NV>();
-    case U_SDN: return h * (A_TILE + B_TILE);
+    case U_SDN: return h * (A_TILE + B_TILE + (a.sh8 ? 2 * 512 : 0));
     default: return h * (A_TILE + B_TILE + 2 * sf_chunk<NV>());
   }
 }
@@ -869,6 +913,11 @@ __device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, 
   if (U.kind == U_SGU) {
     tc::tma_load_2d(sp + ST_A0, &m.w13s, st * 128, 128 * U.tile, fb);
     tc::tma_load_2d(sp + ST_A1, &m.w13s, st * 128, a.I + 128 * U.tile, fb);
+    if (a.sh8) {  // the gate and up tiles' scale blocks for this 128-element K chunk
+      const size_t kb = a.H / 128;
+      tc::bulk_load(sp + ST_SFA, a.w13s8_mma + ((size_t)U.tile * kb + st) * 512, 512, fb);
+      tc::bulk_load(sp + ST_SFA + 512, a.w13s8_mma + ((size_t)(nbI + U.tile) * kb + st) * 512, 512, fb);
+    }
   } else if (U.kind == U_RGU) {
     const int row = e * 2 * a.I + 128 * U.tile;
     const uint32_t sfc = sf_chunk<NV>();
@@ -880,8 +929,11 @@ __device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, 
     tc::bulk_load_hint(sp + ST_SFA, a.w13s_mma + rt * bpr * 512 + (size_t)st * sfc, sfc, fb, pol);
     tc::bulk_load_hint(sp + ST_SFA + sfc, a.w13s_mma + (rt + nbI) * bpr * 512 + (size_t)st * sfc, sfc, fb, pol);
   } else if (U.kind == U_SDN) {
-    for (int h = 0; h < stage_halves(a, U, st); ++h)
+    const int halves = stage_halves(a, U, st);
+    for (int h = 0; h < halves; ++h)
       tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &m.w2s, (2 * st + h) * 128, 128 * U.tile, fb);
+    if (a.sh8)
+      tc::bulk_load(sp + ST_SFA, a.w2s8_mma + ((size_t)U.tile * (a.I / 128) + 2 * st) * 512, halves * 512, fb);
   } else {
     const int halves = stage_halves(a, U, st);
     const uint64_t pol = tc::l2_evict_first();
@@ -903,13 +955,17 @@ __device__ __forceinline__ void issue_acts(const DcArgs& a, const DcMaps& m, con
                                            uint8_t* sp, uint64_t* fb) {
   if (U.kind == U_SGU) {
     tc::tma_load_2d(sp + ST_B0, &m.x, st * 128, 16 * U.chunk, fb);
+    if (a.sh8) tc::bulk_load(sp + st_sfb<NV>(), a.x8s + ((size_t)U.chunk * (a.H / 128) + st) * 512, 512, fb);
   } else if (U.kind == U_RGU) {
     tc::tma_load_2d(sp + ST_B0, &m.xq, st * 128, W ? beg : 0, fb);
     const size_t set = W ? (size_t)U.slot * (a.H / 256) * sf_chunk<NV>() : 0;  // the slot's scale blocks
     tc::bulk_load(sp + st_sfb<NV>(), a.xs_mma + set + (size_t)st * sf_chunk<NV>(), sf_chunk<NV>(), fb);
   } else if (U.kind == U_SDN) {
-    for (int h = 0; h < stage_halves(a, U, st); ++h)
+    const int halves = stage_halves(a, U, st);
+    for (int h = 0; h < halves; ++h)
       tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hsh, (2 * st + h) * 128, 16 * U.chunk, fb);
+    if (a.sh8)
+      tc::bulk_load(sp + st_sfb<NV>(), a.h8s + ((size_t)U.chunk * (a.I / 128) + 2 * st) * 512, halves * 512, fb);
   } else {
     const int halves = stage_halves(a, U, st);
     for (int h = 0; h < halves; ++h)
@@ -1033,7 +1089,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         return tc::mbar_wait(&empty[j % DSTAGES], (j / DSTAGES) & 1, a.limit_ns, &abort_flag);
       };
       int n_slots = -1;
-      bool hsh_ok = false, xr_ok = false, all_h = false;
+      bool hsh_ok = false, xr_ok = false, all_h = false, x8_ok = false;
       tc::prefetch_tensormap(&maps.w13r);
       tc::prefetch_tensormap(&maps.w2r);
       tc::prefetch_tensormap(&maps.xq);
@@ -1084,11 +1140,15 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         uint32_t pre_stage[DSTAGES];
         const bool dep_sdn = U.kind == U_SDN && !hsh_ok, dep_rdn = U.kind == U_RDN && !all_h;
         const bool dep_rgu = W && U.kind == U_RGU && !xr_ok;
-        if (dep_sdn || dep_rdn || dep_rgu) {
+        const bool dep_sgu = U.kind == U_SGU && a.sh8 && !x8_ok;
+        if (dep_sdn || dep_rdn || dep_rgu || dep_sgu) {
           // every slot's h finished (relaxed load, read with the unit's own
           // dependency below): later down units need no check at all
           const int h_done = dep_rdn ? ld_relaxed(a.ctr + C_DC_HR) : 0;
-          int* cnt = dep_sdn ? a.ctr + C_DC_HSH : dep_rdn ? a.tickets + a.tk_slot + U.slot : a.ctr + C_DC_READY;
+          int* cnt = dep_sdn ? a.ctr + C_DC_HSH
+                     : dep_rdn ? a.tickets + a.tk_slot + U.slot
+                     : dep_rgu ? a.ctr + C_DC_READY
+                               : a.ctr + C_DC_X8;
           const int target = dep_sdn ? nbI * a.nck : dep_rdn ? (NV ? 1 : nbI) : a.G;
           // a routed down unit's weights go into the ring before its slot's
           // counter is read, so that load overlaps the weight copies
@@ -1113,6 +1173,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           }
           if (dep_sdn) hsh_ok = true;
           else if (dep_rgu) xr_ok = true;
+          else if (dep_sgu) x8_ok = true;
           else if (h_done >= (NV ? n_slots : n_slots * nbI)) {
             __threadfence();  // with the relaxed load above: acquires every slot's h
             all_h = true;
@@ -1168,7 +1229,20 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           const uint32_t sa = tc::smem_u32(dsm + stage * STAGE_BYTES);
           const uint32_t tsf = tmem + TM_SF + 16 * NB * stage;
           const bool first = st == U.st0;
-          if (U.kind == U_SGU) {
+          if (U.kind == U_SGU && a.sh8) {
+            // MXFP8: 128 K per stage, an MMA of K = 32 reads scale byte kk
+            tc::sf_copy(tsf, tc::desc_sf(sa + ST_SFA));
+            tc::sf_copy(tsf + 4, tc::desc_sf(sa + ST_SFA + 512));
+            tc::sf_copy(tsf + 8, tc::desc_sf(sa + ST_SFB));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = tc::desc_sw128(sa + ST_B0 + 32 * kk);
+              const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+              const uint32_t id8 = tc::idesc_mxf8(128, 16, kk, kk);
+              tc::mma_mxf8(acc, tc::desc_sw128(sa + ST_A0 + 32 * kk), bd, id8, tsf, tsf + 8, accum);
+              tc::mma_mxf8(acc + 16, tc::desc_sw128(sa + ST_A1 + 32 * kk), bd, id8, tsf + 4, tsf + 8, accum);
+            }
+          } else if (U.kind == U_SGU) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t bd = tc::desc_sw128(sa + ST_B0 + 32 * kk);
@@ -1189,6 +1263,21 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               const uint32_t accum = (first && kk == 0) ? 0u : 1u;
               fp4_mma<NV>(acc, tc::desc_sw128(sa + ST_A0 + 32 * kk), bd, kk, tsf, tsf + 8 * NB, accum);
               fp4_mma<NV>(acc + 16, tc::desc_sw128(sa + ST_A1 + 32 * kk), bd, kk, tsf + 4 * NB, tsf + 8 * NB, accum);
+            }
+          } else if (U.kind == U_SDN && a.sh8) {
+            const int halves = stage_halves(a, U, st);
+            for (int h = 0; h < halves; ++h) {
+              tc::sf_copy(tsf + 4 * h, tc::desc_sf(sa + ST_SFA + 512 * h));
+              tc::sf_copy(tsf + 8 + 4 * h, tc::desc_sf(sa + ST_SFB + 512 * h));
+            }
+            for (int h = 0; h < halves; ++h) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t accum = (first && h == 0 && kk == 0) ? 0u : 1u;
+                tc::mma_mxf8(acc, tc::desc_sw128(sa + (h ? ST_A1 : ST_A0) + 32 * kk),
+                             tc::desc_sw128(sa + (h ? ST_B1 : ST_B0) + 32 * kk), tc::idesc_mxf8(128, 16, kk, kk),
+                             tsf + 4 * h, tsf + 8 + 4 * h, accum);
+              }
             }
           } else if (U.kind == U_SDN) {
             const int halves = stage_halves(a, U, st);
@@ -1240,6 +1329,12 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     const int T = a.T, H = a.H, I = a.I, k = a.k, n = T * k;
 
     const uint32_t epoch = s_epoch;
+    if (a.sh8) {  // the MXFP8 shared expert's units wait for x8 (and start before the routing)
+      quant_x8(a, et);
+      tc::fence_proxy_async_global();
+      epi_sync();
+      if (et == 0) red_release_add(a.ctr + C_DC_X8, 1);
+    }
     if constexpr (W) {
       // the routing table is not built yet: its storage stages x for the router
       router_w(a, et, reinterpret_cast<float*>(&R));
@@ -1403,8 +1498,22 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             }
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
-              if (t0 + tt < te) a.h_shared[(size_t)(t0 + tt) * I + 128 * U.tile + m] = f32_to_bf16_rn(silu(g[tt]) * up[tt]);
+              if (t0 + tt < te) {
+                const float hv = silu(g[tt]) * up[tt];
+                if (a.sh8) {
+                  // MXFP8 per 32 along I: warp q holds one block of the row
+                  const int ex = mx8_scale_exp(warp_max(fabsf(hv)));
+                  reinterpret_cast<uint8_t*>(a.h_shared)[(size_t)(t0 + tt) * I + 128 * U.tile + m] =
+                      (uint8_t)e4m3_rne1(hv * pow2_neg(ex));
+                  if (lane == 0)
+                    a.h8s[((size_t)U.chunk * nbI + U.tile) * 512 + ((t0 + tt) & 15) * 16 + q] = (uint8_t)(ex + 127);
+                } else {
+                  a.h_shared[(size_t)(t0 + tt) * I + 128 * U.tile + m] = f32_to_bf16_rn(hv);
+                }
+              }
           }
+          if (a.sh8 && lane == 0)  // rows of the chunk past T: zero scales in the B tile
+            for (int r = te - tb; r < 16; ++r) a.h8s[((size_t)U.chunk * nbI + U.tile) * 512 + r * 16 + q] = 0;
           tc::fence_proxy_async_global();
           epi_sync();
           if (et == 0) red_release_add(a.ctr + C_DC_HSH, 1);
@@ -1553,6 +1662,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       a.ctr[C_DC_EXIT] = 0;
       a.ctr[C_DC_DN] = 0;
       a.ctr[C_DC_RT] = 0;
+      a.ctr[C_DC_X8] = 0;
       a.ctr[C_DC_EPOCH] = (int)s_epoch;
     }
     __threadfence();
@@ -1568,9 +1678,11 @@ bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex) {
 
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
                                    const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
-                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold, int score) {
+                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold, int score,
+                                   const Shared8Dev* sh8) {
   if (sh.T == 0) return cudaSuccess;
   if (!fused_decode_tc_supported(sh, ex)) return cudaErrorInvalidValue;
+  if (sh8 && (!sh8->w13s_mma || !sh8->w2s_mma || shd.w13 || fold)) return cudaErrorInvalidValue;
   const int T = sh.T, H = sh.H, I = sh.I, E = sh.E, k = sh.k, n = T * k;
   const WsLayout L = ws_layout(T, H, I, E, k);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -1589,8 +1701,12 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // one block per SM: every block holds a 200 KB stage ring and a TMEM allocation
   const int G = imin(sm_count(), DC_MAX_GRID);
-  const bool shared = shd.w13 != nullptr;
-  const DcSplits sp = dc_splits(T, H, I, E, k, G);
+  const bool shared = shd.w13 != nullptr || sh8 != nullptr;
+  DcSplits sp = dc_splits(T, H, I, E, k, G);
+  if (sh8) {  // MXFP8 stages hold 128 K elements: no more parts than stages
+    sp.sgu = imin(sp.sgu, H / 128);
+    sp.sdn = imin(sp.sdn, (I / 128 + 1) / 2);
+  }
 
   DcArgs a{};
   a.T = T;
@@ -1613,6 +1729,14 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   a.tk_slot = a.tk_nv + a.nslot_max;
   a.shared = shared ? 1 : 0;
   a.nv = ex.nv;
+  a.sh8 = sh8 ? 1 : 0;
+  if (sh8) {
+    a.w13s8_mma = sh8->w13s_mma;
+    a.w2s8_mma = sh8->w2s_mma;
+    a.x8 = base + L.dc_x8;
+    a.x8s = base + L.dc_x8s;
+    a.h8s = base + L.dc_h8s;
+  }
   a.score = score;
   a.w13s_mma = ex.w13s_mma;
   a.w2s_mma = ex.w2s_mma;
@@ -1655,7 +1779,12 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   if ((err = make_map(&m.w2r, ex.w2, (uint64_t)E * H, I / 2)) != cudaSuccess) return err;
   if ((err = make_map(&m.xq, a.xq, wide ? n : T, H / 2, 16)) != cudaSuccess) return err;
   if ((err = make_map(&m.hq, a.hq, n, I / 2, 16)) != cudaSuccess) return err;
-  if (shared) {
+  if (sh8) {  // E4M3 rows: one byte per element
+    if ((err = make_map(&m.w13s, sh8->w13, (uint64_t)2 * I, (uint64_t)H)) != cudaSuccess) return err;
+    if ((err = make_map(&m.w2s, sh8->w2, H, (uint64_t)I)) != cudaSuccess) return err;
+    if ((err = make_map(&m.x, a.x8, T, (uint64_t)H, 16)) != cudaSuccess) return err;
+    if ((err = make_map(&m.hsh, a.h_shared, T, (uint64_t)I, 16)) != cudaSuccess) return err;
+  } else if (shared) {
     if ((err = make_map(&m.w13s, shd.w13, (uint64_t)2 * I, (uint64_t)2 * H)) != cudaSuccess) return err;
     if ((err = make_map(&m.w2s, shd.w2, H, (uint64_t)2 * I)) != cudaSuccess) return err;
     if ((err = make_map(&m.x, x, T, (uint64_t)2 * H, 16)) != cudaSuccess) return err;

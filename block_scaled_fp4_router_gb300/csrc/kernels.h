@@ -156,7 +156,8 @@ bool fused_decode_tc_supported(const Shape& sh, const ExpertsDev& ex);
 // k - 1 experts; ids_out / w_out are [T][k - fold].
 cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const SharedDev& shd, const float* wr,
                                    const float* bias, const uint16_t* x, uint16_t* out, int* ids_out, float* w_out,
-                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold = 0, int score = 0);
+                                   void* ws, uint64_t wait_limit_ns, cudaStream_t s, int fold = 0, int score = 0,
+                                   const Shared8Dev* sh8 = nullptr);
 // bytes (a multiple of 16) from src to dst, both 16-byte aligned, device or
 // GPU-addressable pinned host memory, by SM loads and stores.
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t s);

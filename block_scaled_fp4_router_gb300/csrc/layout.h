@@ -154,6 +154,7 @@ enum Counter : int {
   C_DC_EPOCH = 12, // tensor-core decode: launches completed on this workspace (tags the logits)
   C_DC_DN = 13,    // tensor-core decode: down-projection parts stored
   C_DC_RT = 14,    // tensor-core decode, wide steps: blocks done with their router parts
+  C_DC_X8 = 15,    // tensor-core decode, MXFP8 shared expert: blocks done quantising x to MXFP8
   N_COUNTERS = 16
 };
 
@@ -206,6 +207,9 @@ struct WsLayout {
   size_t dc_xshift;    // int [16] (wide steps: [T*k]): NVFP4 per-row power of two of the x scales
   size_t dc_xqs;       // wide steps: uint8 [T*k, H/2] x codes in sorted-assignment order
   size_t dc_rpart;     // wide steps: float [H/256][T][E] router partial sums (256-element K parts)
+  size_t dc_x8;        // MXFP8 shared expert: uint8 [T, H] E4M3 codes of x (h's codes go to h_shared)
+  size_t dc_x8s;       // their scales, MMA layout [16-token chunks][H/128][512 B]
+  size_t dc_h8s;       // h's scales, MMA layout [16-token chunks][I/128][512 B]
   size_t dc_hs;        // routed h scales, MMA layout [slots][I/128][512 B] (E8M0) or [slots][I/64][512 B] (UE4M3)
   size_t dc_hsc;       // NVFP4: E8M0 bytes of h [T*k][I/32] before the per-row UE4M3 conversion
   size_t dc_gu_sh;     // float [splits][T][2I]  shared gate/up partial sums
@@ -291,6 +295,9 @@ MOE_HD inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.dc_xshift = take(dc ? sizeof(int) * (wide ? n : (size_t)MAX_DECODE_T) : 0);
   L.dc_xqs = take(wide ? n * H / 2 : 0);
   L.dc_rpart = take(wide ? sizeof(float) * (size_t)(H / 256 > 0 ? H / 256 : 1) * T * E : 0);
+  L.dc_x8 = take(dc ? (size_t)T * H : 0);
+  L.dc_x8s = take(dc ? (size_t)dc_nck(T) * (H / 128) * 512 : 0);
+  L.dc_h8s = take(dc ? (size_t)dc_nck(T) * (I / 128) * 512 : 0);
   L.dc_hs = take(dc ? (size_t)nslot * (I / 64) * 512 : 0);
   L.dc_hsc = take(dc ? n * (I / 32) : 0);
   L.dc_gu_sh = take(dc ? sizeof(float) * sp.sgu * T * 2 * (size_t)I : 0);

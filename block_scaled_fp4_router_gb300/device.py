@@ -8,9 +8,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (MOE_W_MXFP4, MOE_W_NVFP4, desc, experts, moe_layer_decode, moe_layer_forward,
-               moe_layer_forward_shared_mxfp8, moe_prepare_shared_mxfp8, moe_prepare_weights, moe_workspace_size,
-               shared_bf16, shared_mxfp8)
+from . import (MOE_W_MXFP4, MOE_W_NVFP4, desc, experts, moe_layer_decode, moe_layer_decode_shared_mxfp8,
+               moe_layer_forward, moe_layer_forward_shared_mxfp8, moe_prepare_shared_mxfp8, moe_prepare_weights,
+               moe_workspace_size, shared_bf16, shared_mxfp8)
 
 
 def _to_dev(a, device, dtype=None):
@@ -101,13 +101,15 @@ class DeviceLayer:
                 torch.empty((T, self.k), dtype=torch.float32, device=d))
 
     def decode(self, x: torch.Tensor, out=None, ids=None, w=None, stream=None):
-        if self.sh8 is not None:
-            raise NotImplementedError("the single-launch decode takes a BF16 or folded shared expert")
         T = x.shape[0]
         if out is None:
             out, ids, w = self.outputs(T)
-        moe_layer_decode(self.desc(T), self.ex, self.sh, self.w_router, self.bias, x, out, ids, w, self.ws,
-                         stream)
+        if self.sh8 is not None:
+            moe_layer_decode_shared_mxfp8(self.desc(T), self.ex, self.sh8, self.w_router, self.bias, x, out, ids, w,
+                                          self.ws, stream)
+        else:
+            moe_layer_decode(self.desc(T), self.ex, self.sh, self.w_router, self.bias, x, out, ids, w, self.ws,
+                             stream)
         return out, ids, w
 
     def forward(self, x: torch.Tensor, out=None, ids=None, w=None, stream=None):

@@ -337,6 +337,20 @@ MOE_API moe_status_t moe_layer_decode(const moe_layer_desc_t* desc, const moe_ex
                               const float* bias, const void* x, void* out, int32_t* topk_ids,
                               float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_layer_decode with the shared expert in MXFP8 (AMD article, section
+ * "What we Optimized": the fused decode runs the shared expert in MXFP8),
+ * 1 to 128 tokens.  The shared expert's arithmetic is moe_shared_expert_mxfp8's
+ * (x and h quantised to MXFP8 per 32, E4M3 x E4M3 on kind::mxf8f6f4 tensor
+ * cores).  One launch when the routed experts' scales and shared->w13_scale_mma
+ * / w2_scale_mma are prepared (moe_prepare_weights, moe_prepare_shared_mxfp8),
+ * else the batched path of moe_layer_forward_shared_mxfp8.  H and I multiples
+ * of 256 (else MOE_ERR_UNSUPPORTED); desc->shared_in_table must be 0; T > 128
+ * returns MOE_ERR_UNSUPPORTED.  Arguments and errors as moe_layer_decode. */
+MOE_API moe_status_t moe_layer_decode_shared_mxfp8(const moe_layer_desc_t* desc, const moe_experts_t* experts,
+                                                   const moe_shared_mxfp8_t* shared, const float* w_router,
+                                                   const float* bias, const void* x, void* out, int32_t* topk_ids,
+                                                   float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* The whole layer for any T, as the sequence router -> quantise -> permute ->
  * expert FFNs -> combine: the standard path the pages run outside the fused
  * decode range, i.e. prefill and decode steps of more than 16 tokens (AMD

@@ -920,6 +920,47 @@ def test_layer_forward_with_mxfp8_shared_expert(name, T, gemm, routed_gemm):
                    F.dequantize_mxfp8(lay["s8_w13"], lay["s8_w13_scale"]))
 
 
+@pytest.mark.parametrize("T", [1, 16, 40, None], ids=["T1", "T16", "T40", "T128"])
+def test_layer_decode_with_mxfp8_shared_expert(T):
+    """moe_layer_decode_shared_mxfp8 in one launch (the tensor-core decode
+    with kind::mxf8f6f4 shared units: x quantised to MXFP8 in the launch, h
+    requantised to MXFP8 by the shared gate/up finisher) on the full-size
+    layer: 1 token, one 16-token chunk, a ragged third chunk (40) and 128
+    tokens.  Every token against the oracle; the launch is bit-reproducible
+    and agrees with the batched moe_layer_forward_shared_mxfp8."""
+    wl, lay, dev, cache = _workload("batch128_s8", T)
+    assert dev.sh8 is not None and dev.prepared
+    x = bf16_tensor(lay["x"])
+    n0 = M.moe_debug_launch_count()
+    out, ids, w = dev.decode(x)
+    torch.cuda.synchronize()
+    assert M.moe_debug_launch_count() == n0 + 1
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, cache, out, ids, w=w)
+    out2, _, _ = dev.decode(x)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+    out_f, ids_f, _ = dev.forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_f)
+    assert normwise(bits_to_float(out), bits_to_float(out_f)) <= 1e-2
+
+
+@pytest.mark.parametrize("T", [5, 33])
+def test_layer_decode_mxfp8_shared_nvfp4_experts(T):
+    """The MXFP8 shared expert beside NVFP4 routed experts (distinct tensor
+    scales), one launch, small shape (H = 512, I = 256), every token."""
+    wl = W.Workload("s8nv", T, 512, 256, 16, 4, W.NVFP4, 28, 0.08, shared_fmt="mxfp8")
+    lay = W.generate(wl)
+    dev = DeviceLayer(lay, wl.H, wl.I, wl.E, wl.top_k, wl.fmt, T_max=T)
+    n0 = M.moe_debug_launch_count()
+    out, ids, w = dev.decode(bf16_tensor(lay["x"]))
+    torch.cuda.synchronize()
+    assert M.moe_debug_launch_count() == n0 + 1
+    assert M.moe_get_status(dev.ws) == M.MOE_OK
+    _compare_layer(wl, lay, {}, out, ids, w=w)
+
+
 def test_mxfp8_to_bf16_dequant_bitexact():
     """The MXFP8 -> BF16 copy against the oracle's exact dequantisation
     rounded once to BF16: every E4M3 code under scales across the E8M0 range
