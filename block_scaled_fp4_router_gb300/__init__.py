@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoefp4.so")
 # the checked build (out-of-range caller indices recorded in the status word)
 CHECKED_LIB_PATH = os.path.join(_HERE, "libmoefp4_checked.so")
+TRACE_LIB_PATH = os.path.join(_HERE, "libmoefp4_trace.so")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -33,6 +34,7 @@ EXPORTED = [
     "moe_layer_decode_noalloc", "moe_debug_requantized_h", "moe_prepare_weights", "moe_convert_nvfp4_to_mxfp4",
     "moe_set_routed_gemm", "moe_copy_rows", "moe_quant_act_mxfp8", "moe_shared_expert_mxfp8",
     "moe_noalloc_get_status", "moe_debug_wait_probe_noalloc", "moe_debug_launch_count", "moe_set_timing_events",
+    "moe_debug_decode_trace",
     "moe_dequant_mxfp8_to_bf16", "moe_prepare_shared_mxfp8", "moe_layer_forward_shared_mxfp8",
     "moe_layer_decode_shared_mxfp8",
     "moe_debug_shared_mxfp8_h",
@@ -81,12 +83,14 @@ _lib = None
 
 def load(path: str = None) -> ctypes.CDLL:
     """Load libmoefp4.so (raises if it has not been built); with
-    MOEFP4_CHECKED=1 in the environment, the checked build instead."""
+    MOEFP4_CHECKED=1 in the environment, the checked build instead, and with
+    MOEFP4_TRACE=1 the trace build."""
     global _lib
     if _lib is not None:
         return _lib
     if path is None:
-        path = CHECKED_LIB_PATH if os.environ.get("MOEFP4_CHECKED") == "1" else LIB_PATH
+        path = (CHECKED_LIB_PATH if os.environ.get("MOEFP4_CHECKED") == "1"
+                else TRACE_LIB_PATH if os.environ.get("MOEFP4_TRACE") == "1" else LIB_PATH)
     if not os.path.exists(path):
         raise RuntimeError(
             "libmoefp4.so is not built (expected at %s); run "
@@ -114,6 +118,7 @@ def load(path: str = None) -> ctypes.CDLL:
         "moe_noalloc_get_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
         "moe_debug_wait_probe_noalloc": ([U64, P], ctypes.c_int),
         "moe_debug_launch_count": ([ctypes.POINTER(ctypes.c_uint64)], None),
+        "moe_debug_decode_trace": ([P, S], ctypes.c_int),
         "moe_dequant_mxfp8_to_bf16": ([I32, I32, P, P, P, P], ctypes.c_int),
         "moe_prepare_shared_mxfp8": ([P, P, P, P, P], ctypes.c_int),
         "moe_layer_forward_shared_mxfp8": ([P, P, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
@@ -337,6 +342,19 @@ def moe_debug_launch_count() -> int:
     n = ctypes.c_uint64(0)
     load().moe_debug_launch_count(ctypes.byref(n))
     return n.value
+
+
+def moe_debug_decode_trace(clear: bool = False):
+    """Trace builds: the last single-launch decode's per-block %globaltimer
+    stamps as a numpy uint64 array [256 blocks, 16 events] (clear=True zeroes
+    them and returns None)."""
+    import numpy as np
+    if clear:
+        _check(load().moe_debug_decode_trace(None, 0), "moe_debug_decode_trace")
+        return None
+    out = np.zeros((256, 16), np.uint64)
+    _check(load().moe_debug_decode_trace(ctypes.c_void_p(out.ctypes.data), out.nbytes), "moe_debug_decode_trace")
+    return out
 
 
 def moe_set_timing_events(begin=None, end=None) -> None:

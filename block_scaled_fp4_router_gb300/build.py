@@ -7,7 +7,9 @@ An up-to-date library is left alone unless force=True.
 build(checked=True) makes the checked variant, libmoefp4_checked.so
 (MOEFP4_CHECKED=1: caller-given indices that are out of range are recorded as
 MOE_ERR_INVALID_ARG in the workspace status word), from objects under
-_build/checked/.
+_build/checked/.  build(trace=True) makes libmoefp4_trace.so (MOEFP4_TRACE=1:
+the single-launch decode stamps %globaltimer at its phase boundaries, read
+back by moe_debug_decode_trace), from objects under _build/trace/.
 """
 from __future__ import annotations
 
@@ -23,6 +25,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoefp4.so")
 LIB_CHECKED = os.path.join(PKG, "libmoefp4_checked.so")
+LIB_TRACE = os.path.join(PKG, "libmoefp4_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -52,14 +55,14 @@ def up_to_date(lib: str = LIB) -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
-    lib = LIB_CHECKED if checked else LIB
+def build(force: bool = False, verbose: bool = False, checked: bool = False, trace: bool = False) -> str:
+    lib = LIB_CHECKED if checked else LIB_TRACE if trace else LIB
     if not force and up_to_date(lib):
         return lib
     nvcc = _nvcc()
-    objdir = os.path.join(BUILD, "checked") if checked else BUILD
+    objdir = os.path.join(BUILD, "checked") if checked else os.path.join(BUILD, "trace") if trace else BUILD
     os.makedirs(objdir, exist_ok=True)
-    defs = ["-DMOEFP4_CHECKED=1"] if checked else []
+    defs = ["-DMOEFP4_CHECKED=1"] if checked else ["-DMOEFP4_TRACE=1"] if trace else []
 
     def compile_one(src):
         obj = os.path.join(objdir, os.path.basename(src) + ".o")

@@ -53,12 +53,37 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "moefp4.h"
 #include "routing.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
 namespace moefp4 {
 namespace {
+
+// Trace builds (MOEFP4_TRACE=1): each block stamps %globaltimer at its phase
+// boundaries of the last launch, read back by moe_debug_decode_trace.
+enum DcTraceEvent {
+  TR_START = 0,        // the block's TMEM is allocated
+  TR_ROUTER = 1,       // router rows or parts (wide steps: and x in token order) done
+  TR_ROUTING = 2,      // routing table built
+  TR_X = 3,            // x quantised (steps up to 16 tokens) or copied into sorted order (wide steps)
+  TR_X_SEEN = 4,       // producer: the quantised x of every block seen (wide steps)
+  TR_HSH_SEEN = 5,     // producer: the shared expert's h seen
+  TR_H_SEEN = 6,       // producer: every slot's routed h seen
+  TR_PRODUCER = 7,     // producer: every copy issued
+  TR_UNITS = 8,        // epilogue: every unit of the block done
+  TR_DOWN_SEEN = 9,    // epilogue: every down part stored
+  TR_END = 10,         // epilogue: combine done
+  TR_LAST_UNIT = 11,   // + unit kind: the block's last unit of that kind finished
+};
+#if MOEFP4_TRACE
+constexpr int DC_TRACE_EVENTS = 16;
+__device__ unsigned long long g_dc_trace[DC_MAX_GRID][DC_TRACE_EVENTS];
+#define DC_TRACE(ev) (g_dc_trace[blockIdx.x][(ev)] = globaltimer_ns())
+#else
+#define DC_TRACE(ev) ((void)0)
+#endif
 
 constexpr int DT = 192;                 // threads: TMA warp, MMA warp, 4 epilogue warps
 constexpr int EPI_THREADS = 128;
@@ -670,6 +695,50 @@ __device__ void sort_x_w(const DcArgs& a, const DcRouting<true>& R, int i) {
   }
 }
 
+// Token t's top-k (lane j holds choice j) published with the launch number in
+// the high word: [T kr] ids, then [T kr] weights.
+__device__ __forceinline__ void publish_topk(const DcArgs& a, int t, const int (&sel)[MAX_TOPK],
+                                             const float (&wt)[MAX_TOPK], uint32_t epoch) {
+  const int lane = threadIdx.x & 31, kr = a.kr, nr = a.T * kr;
+#pragma unroll
+  for (int j = 0; j < MAX_TOPK; ++j)
+    if (j == lane && j < kr) {
+      st_relaxed_u64(a.topk64 + t * kr + j, ((unsigned long long)epoch << 32) | (uint32_t)sel[j]);
+      st_relaxed_u64(a.topk64 + nr + t * kr + j, ((unsigned long long)epoch << 32) | __float_as_uint(wt[j]));
+    }
+}
+
+// Every token's published top-k into R.ids / R.w (bounded wait for this
+// launch's number), plus the folded shared expert (expert Er, weight 1).
+template <bool W>
+__device__ void gather_topk(const DcArgs& a, DcRouting<W>& R, int et, uint32_t epoch, int* failed) {
+  const int T = a.T, k = a.k, kr = a.kr, nr = T * kr;
+  const uint64_t t0 = globaltimer_ns();
+  for (int i = et; i < nr; i += EPI_THREADS) {
+    unsigned long long vi = 0, vw = 0;
+    for (uint32_t it = 0;; ++it) {
+      vi = ld_relaxed_u64(a.topk64 + i);
+      vw = ld_relaxed_u64(a.topk64 + nr + i);
+      if ((uint32_t)(vi >> 32) == epoch && (uint32_t)(vw >> 32) == epoch) break;
+      if (globaltimer_ns() - t0 > a.limit_ns || it > (1u << 26)) {
+        *failed = 1;
+        vi = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    const int t = i / kr, j = i % kr;
+    const int id = (int)(uint32_t)vi;
+    R.ids[t * k + j] = id >= 0 && id < a.Er ? id : 0;  // a failed wait leaves a valid index
+    R.w[t * k + j] = __uint_as_float((uint32_t)vw);
+  }
+  if (kr < k)  // the shared expert folded into the table: expert Er, weight 1
+    for (int t = et; t < T; t += EPI_THREADS) {
+      R.ids[t * k + kr] = a.Er;
+      R.w[t * k + kr] = 1.0f;
+    }
+}
+
 // Top-k of every token (one epilogue warp per token), then the stable sort
 // of the T*k <= 128 assignments by expert (each assignment counts the ones
 // that precede it) and the distinct-expert slots (runs of one expert in the
@@ -678,7 +747,12 @@ __device__ void sort_x_w(const DcArgs& a, const DcRouting<true>& R, int i) {
 __device__ void build_routing(const DcArgs& a, DcRouting<false>& R, int et, uint32_t epoch, int* failed) {
   const int T = a.T, k = a.k, kr = a.kr, n = T * k;
   const int w = et >> 5, lane = et & 31;
-  for (int t = w; t < T; t += EPI_THREADS / 32) {
+  // Up to 4 tokens every block picks them itself (one token per warp).  More
+  // tokens would queue on the warps: block b picks tokens b, b + G, ... (warp 0) and
+  // publishes it, and every block gathers them (one more round trip instead
+  // of up to four top-k passes in a row).
+  const bool spread = T > EPI_THREADS / 32;
+  for (int t = spread ? (w == 0 ? (int)blockIdx.x : T) : w; t < T; t += spread ? a.G : EPI_THREADS / 32) {
     float v[8];
     if (!wait_logit_row(a, t, epoch, v)) {
       if (lane == 0) *failed = 1;
@@ -687,6 +761,10 @@ __device__ void build_routing(const DcArgs& a, DcRouting<false>& R, int et, uint
     int sel[MAX_TOPK];
     float wt[MAX_TOPK];
     route_row(v, a.Er, kr, a.score, a.bias, sel, wt);
+    if (spread) {
+      publish_topk(a, t, sel, wt, epoch);
+      continue;
+    }
 #pragma unroll
     for (int j = 0; j < MAX_TOPK; ++j)
       if (j == lane && j < kr) {
@@ -698,6 +776,7 @@ __device__ void build_routing(const DcArgs& a, DcRouting<false>& R, int et, uint
       R.w[t * k + kr] = 1.0f;
     }
   }
+  if (spread) gather_topk(a, R, et, epoch, failed);
   epi_sync();
   if (*failed) return;  // the same answer in every thread after the barrier
   if (et < n) {
@@ -744,7 +823,7 @@ __device__ void build_routing(const DcArgs& a, DcRouting<false>& R, int et, uint
 // and each warp places its quarter.  Slot s is a run of at most 16 sorted
 // positions of one expert; an expert's runs are consecutive slots.
 __device__ void build_routing_w(const DcArgs& a, DcRouting<true>& R, int et, uint32_t epoch, int* failed) {
-  const int T = a.T, k = a.k, kr = a.kr, n = T * k, E = a.E, nr = T * kr;
+  const int T = a.T, k = a.k, kr = a.kr, n = T * k, E = a.E;
   const int w = et >> 5, lane = et & 31;
   if ((int)blockIdx.x < T) {  // this block has tokens: every block's router parts must be in
     if (et == 0 && !wait_at_least(a.ctr + C_DC_RT, a.G, a.ctr + C_STATUS, a.limit_ns)) *failed = 1;
@@ -764,38 +843,10 @@ __device__ void build_routing_w(const DcArgs& a, DcRouting<true>& R, int et, uin
     int sel[MAX_TOPK];
     float wt[MAX_TOPK];
     route_row(v, a.Er, kr, a.score, a.bias, sel, wt);
-#pragma unroll
-    for (int j = 0; j < MAX_TOPK; ++j)
-      if (j == lane && j < kr) {
-        st_relaxed_u64(a.topk64 + t * kr + j, ((unsigned long long)epoch << 32) | (uint32_t)sel[j]);
-        st_relaxed_u64(a.topk64 + nr + t * kr + j, ((unsigned long long)epoch << 32) | __float_as_uint(wt[j]));
-      }
+    publish_topk(a, t, sel, wt, epoch);
     epi_sync();  // lg is rewritten for the next token
   }
-  const uint64_t t0 = globaltimer_ns();
-  for (int i = et; i < nr; i += EPI_THREADS) {
-    unsigned long long vi = 0, vw = 0;
-    for (uint32_t it = 0;; ++it) {
-      vi = ld_relaxed_u64(a.topk64 + i);
-      vw = ld_relaxed_u64(a.topk64 + nr + i);
-      if ((uint32_t)(vi >> 32) == epoch && (uint32_t)(vw >> 32) == epoch) break;
-      if (globaltimer_ns() - t0 > a.limit_ns || it > (1u << 26)) {
-        *failed = 1;
-        vi = 0;
-        break;
-      }
-      __nanosleep(64);
-    }
-    const int t = i / kr, j = i % kr;
-    const int id = (int)(uint32_t)vi;
-    R.ids[t * k + j] = id >= 0 && id < a.Er ? id : 0;  // a failed wait leaves a valid index
-    R.w[t * k + j] = __uint_as_float((uint32_t)vw);
-  }
-  if (kr < k)  // the shared expert folded into the table: expert Er, weight 1
-    for (int t = et; t < T; t += EPI_THREADS) {
-      R.ids[t * k + kr] = a.Er;
-      R.w[t * k + kr] = 1.0f;
-    }
+  gather_topk(a, R, et, epoch, failed);
   int* wh = R.whist + w * EH;
   for (int e = lane; e < E; e += 32) wh[e] = 0;
   epi_sync();
@@ -1067,6 +1118,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     s_epoch = ep == 0u ? 1u : ep;
   }
   if (warp == 1) tc::tmem_alloc(&tmem_base, tmem_cols<NV>());
+  if (threadIdx.x == 0) DC_TRACE(TR_START);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -1171,12 +1223,18 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             if (!ok) break;
             if (!wait_at_least(cnt, target, status, a.limit_ns)) { fail(); break; }
           }
-          if (dep_sdn) hsh_ok = true;
-          else if (dep_rgu) xr_ok = true;
-          else if (dep_sgu) x8_ok = true;
-          else if (h_done >= (NV ? n_slots : n_slots * nbI)) {
+          if (dep_sdn) {
+            hsh_ok = true;
+            DC_TRACE(TR_HSH_SEEN);
+          } else if (dep_rgu) {
+            xr_ok = true;
+            DC_TRACE(TR_X_SEEN);
+          } else if (dep_sgu) {
+            x8_ok = true;
+          } else if (h_done >= (NV ? n_slots : n_slots * nbI)) {
             __threadfence();  // with the relaxed load above: acquires every slot's h
             all_h = true;
+            DC_TRACE(TR_H_SEEN);
           }
           tc::fence_proxy_async_global();
         }
@@ -1199,6 +1257,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         }
         if (!ok) break;
       }
+      DC_TRACE(TR_PRODUCER);
       // copies still in flight must land before the block's shared memory goes away
       for (int s = 0; s < DSTAGES; ++s)
         if ((issued >> s & 1) && !tc::mbar_wait(&full[s], last_parity >> s & 1, a.limit_ns, &never)) fail();
@@ -1342,6 +1401,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     } else {
       for (int e = blockIdx.x; e < a.Er; e += a.G) router_row(a, e, et, red_s, epoch);
     }
+    if (et == 0) DC_TRACE(TR_ROUTER);
     if constexpr (!W) {
       // the router rows go to the first E blocks, the quantisation to the last ones
       if (NV) {
@@ -1353,11 +1413,15 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       }
       tc::fence_proxy_async_global();
       epi_sync();  // orders every thread's stores before thread 0's release
-      if (et == 0) red_release_add(a.ctr + C_DC_READY, 1);
+      if (et == 0) {
+        red_release_add(a.ctr + C_DC_READY, 1);
+        DC_TRACE(TR_X);
+      }
       build_routing(a, R, et, epoch, &s_fail);
     } else {
       build_routing_w(a, R, et, epoch, &s_fail);
     }
+    if (et == 0) DC_TRACE(TR_ROUTING);
     if (s_fail) {
       if (et == 0) fail();
     } else {
@@ -1367,7 +1431,10 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         for (int i = blockIdx.x * EPI_THREADS + et; i < n * (H / 32); i += a.G * EPI_THREADS) sort_x_w<NV>(a, R, i);
         tc::fence_proxy_async_global();
         epi_sync();
-        if (et == 0) red_release_add(a.ctr + C_DC_READY, 1);
+        if (et == 0) {
+          red_release_add(a.ctr + C_DC_READY, 1);
+          DC_TRACE(TR_X);
+        }
       }
       if (blockIdx.x == 0)  // the router's top-k, [T][kr]
         for (int i = et; i < n; i += EPI_THREADS)
@@ -1462,6 +1529,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           ticket = -1;
           target = 0;
         }
+        if (et == 0) DC_TRACE(TR_LAST_UNIT + U.kind);
         if (ticket < 0) {
           // a down part: counted without waiting; the combine runs after the unit list
           epi_sync();
@@ -1579,6 +1647,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           }
         }
       }
+      if (et == 0) DC_TRACE(TR_UNITS);
       // out = BF16(ys + sum_j w_j y_j), summed in a fixed order, once every
       // down part is stored.  Items (128 columns of H x CT tokens) are spread
       // over all blocks.  The rows an item reads (per token its k y rows and
@@ -1596,6 +1665,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         }
         epi_sync();
       }
+      if (et == 0) DC_TRACE(TR_DOWN_SEEN);
       float* cbuf = reinterpret_cast<float*>(dsm);  // [CT][rpt][128]: the ring's consumers are done
       uint32_t it = 0;
       for (int item = blockIdx.x; item < n_items && s_ok; item += a.G, ++it) {
@@ -1637,6 +1707,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     }
   }
 
+  if (threadIdx.x == 64) DC_TRACE(TR_END);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {
@@ -1804,3 +1875,18 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
 }
 
 }  // namespace moefp4
+
+extern "C" MOE_API moe_status_t moe_debug_decode_trace(uint64_t* dst, size_t bytes) {
+#if MOEFP4_TRACE
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, moefp4::g_dc_trace) != cudaSuccess) return MOE_ERR_CUDA;
+  const size_t all = sizeof(moefp4::g_dc_trace);
+  const cudaError_t e = dst ? cudaMemcpy(dst, p, bytes < all ? bytes : all, cudaMemcpyDeviceToHost)
+                            : cudaMemset(p, 0, all);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+#else
+  (void)dst;
+  (void)bytes;
+  return MOE_ERR_UNSUPPORTED;
+#endif
+}

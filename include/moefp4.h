@@ -351,6 +351,15 @@ MOE_API moe_status_t moe_layer_decode_shared_mxfp8(const moe_layer_desc_t* desc,
                                                    const float* bias, const void* x, void* out, int32_t* topk_ids,
                                                    float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Trace builds only (libmoefp4_trace.so, compiled with MOEFP4_TRACE=1): the
+ * per-block %globaltimer stamps (ns) of the last single-launch decode,
+ * uint64 [256 blocks][16 events], events in the order start, router done,
+ * routing built, x quantised, x seen, shared h seen, routed h seen, producer
+ * done, units done, down parts seen, end, last SGU / RGU / SDN / RDN unit.
+ * Copies min(bytes, 32768) bytes to host memory dst; dst NULL clears the
+ * stamps.  Other builds return MOE_ERR_UNSUPPORTED. */
+MOE_API moe_status_t moe_debug_decode_trace(uint64_t* dst, size_t bytes);
+
 /* The whole layer for any T, as the sequence router -> quantise -> permute ->
  * expert FFNs -> combine: the standard path the pages run outside the fused
  * decode range, i.e. prefill and decode steps of more than 16 tokens (AMD

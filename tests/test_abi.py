@@ -47,6 +47,11 @@ def test_checked_build_exports_the_same_entry_points():
         assert hasattr(chk, name), name
 
 
+def test_decode_trace_needs_the_trace_build(lib):
+    """moe_debug_decode_trace answers only in the trace build."""
+    assert lib.moe_debug_decode_trace(None, 0) == M.MOE_ERR_UNSUPPORTED
+
+
 def test_status_strings(lib):
     for code, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARG"), (2, "MOE_ERR_UNSUPPORTED"),
                        (3, "MOE_ERR_CUDA"), (4, "MOE_ERR_TIMEOUT"), (5, "MOE_ERR_WORKSPACE")]:
