@@ -88,10 +88,11 @@ __device__ unsigned long long g_dc_trace[DC_MAX_GRID][DC_TRACE_EVENTS];
 constexpr int DT = 192;                 // threads: TMA warp, MMA warp, 4 epilogue warps
 constexpr int EPI_THREADS = 128;
 // A 4-stage ring, of which the host lets `depth` stages be in flight: two
-// (~70-90 KB per SM, ~10-13 MB over the GPU) cover HBM's bandwidth-latency
-// product for a 1-4 token step, where a deeper queue would only slow the
-// latency-bound hand-offs between the steps; four for the larger steps,
-// which stream hundreds of MB.
+// for a step of up to 15 assignments (its shared units stream while the
+// routing is computed, and a deeper queue slows the latency-bound hand-offs),
+// four for the larger steps.  Routed down units always put all their weight
+// copies (at most three stages at I = 1536) into the ring before they wait
+// for their slot's h.
 constexpr int DSTAGES = 4;
 // byte offsets inside one stage (swizzled tiles on 1024-byte boundaries)
 constexpr uint32_t ST_A0 = 0, ST_A1 = 16384;       // 128 rows x 128 B each
@@ -1133,11 +1134,11 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       // ------------------------------------------------ TMA producer
       const int never = 0;
       uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0, gi = 0;
-      // Stage gi may be issued once stage gi - depth has been consumed (which
-      // also frees slot gi % DSTAGES: depth <= DSTAGES, consumption in order).
-      auto claim = [&]() -> bool {
-        if (gi < (uint32_t)a.depth) return true;
-        const uint32_t j = gi - (uint32_t)a.depth;
+      // Stage gi may be issued once stage gi - d is consumed (d <= DSTAGES:
+      // consumption in order, so slot gi % DSTAGES is free then).
+      auto claim = [&](int d) -> bool {
+        if (gi < (uint32_t)d) return true;
+        const uint32_t j = gi - (uint32_t)d;
         return tc::mbar_wait(&empty[j % DSTAGES], (j / DSTAGES) & 1, a.limit_ns, &abort_flag);
       };
       int n_slots = -1;
@@ -1179,6 +1180,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         }
         if (u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
         const Unit U = unit_at(a, n_slots < 0 ? 0 : n_slots, u);
+        const int ud = U.kind == U_RDN ? DSTAGES : a.depth;
         int e = 0, beg = 0;
         if (U.kind == U_RGU || U.kind == U_RDN) {
           e = R.slot_e[U.slot];
@@ -1205,10 +1207,10 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           // a routed down unit's weights go into the ring before its slot's
           // counter is read, so that load overlaps the weight copies
           if (dep_rdn || ld_acquire(cnt) < target) {
-            npre = imin(U.st1 - U.st0, a.depth);
+            npre = imin(U.st1 - U.st0, ud);
             bool ok = true;
             for (int j = 0; j < npre; ++j) {
-              if (!claim()) { fail(); ok = false; break; }
+              if (!claim(ud)) { fail(); ok = false; break; }
               tc::mbar_expect_tx(&full[stage], stage_tx<NV>(a, U, U.st0 + j));
               issue_weights<NV>(a, maps, U, U.st0 + j, e, dsm + stage * STAGE_BYTES, &full[stage]);
               pre_stage[j] = stage;
@@ -1242,7 +1244,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           issue_acts<NV, W>(a, maps, U, U.st0 + j, beg, dsm + pre_stage[j] * STAGE_BYTES, &full[pre_stage[j]]);
         bool ok = true;
         for (int st = U.st0 + npre; st < U.st1; ++st) {
-          if (!claim()) { fail(); ok = false; break; }
+          if (!claim(ud)) { fail(); ok = false; break; }
           uint8_t* sp = dsm + stage * STAGE_BYTES;
           tc::mbar_expect_tx(&full[stage], stage_tx<NV>(a, U, st));
           issue_weights<NV>(a, maps, U, st, e, sp, &full[stage]);
@@ -1469,16 +1471,19 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           cnt = R.slot_beg[U.slot + 1] - beg;
         }
         int ticket, target;
+        float rg_sg = 1.0f, rg_su = 1.0f;  // one-part routed tiles: the gate / up factors
         if (U.kind == U_SGU) {
           // column c is token 16 chunk + c
+          // (a tile of one part keeps its sums in registers for the finisher)
           float* dst = a.gu_sh + ((size_t)U.part * T + 16 * U.chunk) * 2 * I + 128 * U.tile + m;
           const int nt = imin(16, T - 16 * U.chunk);
+          if (a.s_sgu > 1)
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            if (c < nt) {
-              dst[(size_t)c * 2 * I] = v[c];
-              dst[(size_t)c * 2 * I + I] = v[16 + c];
-            }
+            for (int c = 0; c < 16; ++c)
+              if (c < nt) {
+                dst[(size_t)c * 2 * I] = v[c];
+                dst[(size_t)c * 2 * I + I] = v[16 + c];
+              }
           ticket = U.tile * a.nck + U.chunk;
           target = a.s_sgu;
         } else if (U.kind == U_RGU) {
@@ -1491,7 +1496,11 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             sg = __ldg(a.tscale + 3 * e);
             su = __ldg(a.tscale + 3 * e + 1);
           }
-          if constexpr (W) {
+          if (a.s_rgu == 1) {
+            // the tile's only part: the finisher takes the sums from v
+            rg_sg = sg;
+            rg_su = su;
+          } else if constexpr (W) {
             // wide steps: B held the slot's sorted rows, column c is position beg + c
 #pragma unroll
             for (int c = 0; c < 16; ++c)
@@ -1561,8 +1570,13 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
               const int t = imin(t0 + tt, te - 1);
-              g[tt] = sum_parts(src + (size_t)t * 2 * I, stride, a.s_sgu);
-              up[tt] = sum_parts(src + (size_t)t * 2 * I + I, stride, a.s_sgu);
+              if (a.s_sgu == 1) {
+                g[tt] = pick16(v, 0, t - tb);
+                up[tt] = pick16(v, 16, t - tb);
+              } else {
+                g[tt] = sum_parts(src + (size_t)t * 2 * I, stride, a.s_sgu);
+                up[tt] = sum_parts(src + (size_t)t * 2 * I + I, stride, a.s_sgu);
+              }
             }
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
@@ -1590,8 +1604,16 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           const float* src = a.gu_r + (size_t)beg * 2 * I + 128 * U.tile + m;
           const size_t stride = (size_t)n * 2 * I;
           for (int c = 0; c < cnt; ++c) {
-            const float g = sum_parts(src + (size_t)c * 2 * I, stride, a.s_rgu);
-            const float up = sum_parts(src + (size_t)c * 2 * I + I, stride, a.s_rgu);
+            float g, up;
+            if (a.s_rgu == 1) {  // the same products the part store would hold
+              const int col = W ? c : R.tok[beg + c];
+              const float f = NV ? pow2f(__ldcg(a.xshift + R.tok[beg + c])) : 1.0f;
+              g = pick16(v, 0, col) * (rg_sg * f);
+              up = pick16(v, 16, col) * (rg_su * f);
+            } else {
+              g = sum_parts(src + (size_t)c * 2 * I, stride, a.s_rgu);
+              up = sum_parts(src + (size_t)c * 2 * I + I, stride, a.s_rgu);
+            }
             const float h = silu(g) * up;
             const int ex = mx_scale_exp(warp_max(fabsf(h)));
             uint32_t wv = e2m1_rne(h * pow2_neg(ex)) << (4 * (lane & 7));
