@@ -64,7 +64,8 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="prefill8k", help="the headline workload")
+    p.add_argument("--workload", default="prefill8k",
+                   help="the headline workload (name@decode: through moe_layer_decode, one launch)")
     p.add_argument("--configs", default=",".join(PER_CONFIG),
                    help="workloads measured under per_config (comma list, '' for none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -218,7 +219,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    wl = W.WORKLOADS[args.workload]
+    wl = W.WORKLOADS[args.workload.partition("@")[0]]
     budget = max(10.0, min(120.0, 12.0 * max(1, args.steps) ** 0.5))
     rate, steps, toks, dt, what = oracle_rate(wl, budget, args.steps)
     cores = os.cpu_count()
@@ -495,8 +496,9 @@ def run_ours(args):
     pkg.load()
     pk = peaks()
 
-    wl = W.WORKLOADS[args.workload]
-    head = measure(wl, args, dev, rank, world, pk, headline=True)
+    head_name, _, head_entry = args.workload.partition("@")
+    wl = W.WORKLOADS[head_name]
+    head = measure(wl, args, dev, rank, world, pk, headline=True, entry=head_entry or None)
     per = {}
     for name in [c for c in args.configs.split(",") if c and c != args.workload]:
         base, _, entry = name.partition("@")
