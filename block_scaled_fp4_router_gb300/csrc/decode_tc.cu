@@ -110,6 +110,17 @@ constexpr uint32_t A_TILE = 16384, B_TILE = 2048;
 // TMEM: NACC 32-column accumulators (the MMA runs up to NACC units ahead of
 // the epilogue), then 16 NBLK scale columns per stage.
 constexpr int NACC = 4;
+// Units go round-robin (unit u to block u mod G), or, in steps of up to 16
+// tokens whose routed gate/up units fill more than one round of blocks (the
+// DYN instantiations), dynamically: each block's first
+// unit is blockIdx.x, the later ones come from a launch-wide counter in
+// increasing order, and the producer passes them to the MMA and epilogue
+// warps through a ring of UQ entries.  Measured on GB300: dynamic 130-133 us
+// against 137-141 us round-robin for 16 NVFP4 tokens (the four-versus-three
+// gate/up units per block no longer decide the end), but slower for one
+// token, for the 16-token small layer and for 128 tokens, where the
+// round-robin list is already balanced and the hand-off costs.
+constexpr int UQ = 16;
 template <bool NV> __host__ __device__ constexpr uint32_t tmem_cols() { return NV ? 512u : 256u; }
 constexpr uint32_t TM_SF = 32 * NACC;
 // assignments and expert slots of a step (W: wide steps of up to 128 tokens)
@@ -1075,7 +1086,7 @@ __device__ __forceinline__ void fp4_mma(uint32_t d, uint64_t ad, uint64_t bd, in
 
 // ------------------------------------------------------------------ kernel
 
-template <bool NV, bool W>
+template <bool NV, bool W, bool DYN>
 __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcMaps maps, const DcArgs a) {
   constexpr uint32_t STAGE_BYTES = stage_bytes<NV>();
   constexpr uint32_t ST_SFB = st_sfb<NV>();
@@ -1083,6 +1094,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
   extern __shared__ __align__(1024) uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[DSTAGES], empty[DSTAGES], acc_full[NACC], acc_empty[NACC], drain, routing_ready, comb;
+  __shared__ uint64_t uq_full[DYN ? UQ : 1], uq_empty[DYN ? UQ : 1];
+  __shared__ int s_uq[DYN ? UQ : 1], s_unit[2];
   __shared__ int never_s;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag, s_ok, s_last, s_fail;
@@ -1109,6 +1122,11 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
     tc::mbar_init(&drain, 1);
     tc::mbar_init(&routing_ready, 1);
     tc::mbar_init(&comb, 1);
+    if (DYN)
+      for (int q = 0; q < UQ; ++q) {
+        tc::mbar_init(&uq_full[q], 1);
+        tc::mbar_init(&uq_empty[q], 2);  // the MMA issuer and epilogue thread 0
+      }
     never_s = 0;
     tc::mbar_fence_init();
     abort_flag = 0;
@@ -1167,7 +1185,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         for (size_t o = (size_t)blockIdx.x * 16384; o < sbytes; o += (size_t)a.G * 16384)
           tc::bulk_prefetch_l2(a.w13s_mma + o, (uint32_t)(sbytes - o < 16384 ? sbytes - o : 16384));
       }
-      for (int u = blockIdx.x;; u += a.G) {
+      int u = blockIdx.x;
+      for (int i = 0;; ++i) {
         if (u >= a.n_sgu && n_slots < 0) {
           if (!tc::mbar_wait(&routing_ready, 0, a.limit_ns, &abort_flag)) { fail(); break; }
           n_slots = R.n_slots;
@@ -1178,7 +1197,16 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             tc::fence_proxy_async_global();
           }
         }
-        if (u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
+        const bool done = u >= units_total(a, n_slots < 0 ? 0 : n_slots);
+        if constexpr (DYN) {  // hand the unit number (or the end, -1) to the MMA and epilogue warps
+          const int q = i % UQ;
+          if (i >= UQ && !tc::mbar_wait(&uq_empty[q], (i / UQ - 1) & 1, a.limit_ns, &abort_flag)) { fail(); break; }
+          s_uq[q] = done ? -1 : u;
+          tc::mbar_arrive(&uq_full[q]);
+        }
+        if (done) break;
+        // the next unit's number (dynamic: read while this unit's copies are issued)
+        const int next = DYN ? a.G + atomicAdd(a.ctr + C_DC_QUEUE, 1) : u + a.G;
         const Unit U = unit_at(a, n_slots < 0 ? 0 : n_slots, u);
         const int ud = U.kind == U_RDN ? DSTAGES : a.depth;
         int e = 0, beg = 0;
@@ -1258,6 +1286,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           }
         }
         if (!ok) break;
+        u = next;
       }
       DC_TRACE(TR_PRODUCER);
       // copies still in flight must land before the block's shared memory goes away
@@ -1270,13 +1299,21 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       const int never = 0;
       const uint32_t id_bf = tc::idesc_bf16(128, 16);
       uint32_t stage = 0, phase = 0;
-      int n_slots = -1, i = 0;
-      for (int u = blockIdx.x;; u += a.G, ++i) {
+      int n_slots = -1;
+      for (int i = 0;; ++i) {
+        int u = blockIdx.x + i * a.G;
+        if constexpr (DYN) {
+          const int q = i % UQ;
+          if (!tc::mbar_wait(&uq_full[q], (i / UQ) & 1, a.limit_ns, &abort_flag)) { fail(); break; }
+          u = s_uq[q];
+          tc::mbar_arrive(&uq_empty[q]);
+          if (u < 0) break;
+        }
         if (u >= a.n_sgu && n_slots < 0) {
           if (!tc::mbar_wait(&routing_ready, 0, a.limit_ns, &abort_flag)) { fail(); break; }
           n_slots = R.n_slots;
         }
-        if (u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
+        if (!DYN && u >= units_total(a, n_slots < 0 ? 0 : n_slots)) break;
         const Unit U = unit_at(a, n_slots < 0 ? 0 : n_slots, u);
         const int buf = i % NACC;
         const uint32_t use = (uint32_t)(i / NACC);
@@ -1446,19 +1483,32 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             if (a.w_out) a.w_out[o] = R.w[i];
           }
       const int n_slots = R.n_slots;
-      const int total = units_total(a, n_slots);
+
       const int dn_total = nbH * ((a.shared ? a.s_sdn * a.nck : 0) + n_slots);  // down parts over all tiles
-      int i = 0;
-      for (int u = blockIdx.x; u < total; u += a.G, ++i) {
-        const Unit U = unit_at(a, n_slots, u);
+      for (int i = 0;; ++i) {
         const int buf = i % NACC;
         const uint32_t use = (uint32_t)(i / NACC);
+        if (!DYN && (int)blockIdx.x + i * a.G >= units_total(a, n_slots)) break;
         if (et == 0) {
-          s_ok = tc::mbar_wait(&acc_full[buf], use & 1, a.limit_ns, &abort_flag);
+          int uu = blockIdx.x + i * a.G;
+          s_ok = true;
+          if constexpr (DYN) {
+            const int q = i % UQ;
+            s_ok = tc::mbar_wait(&uq_full[q], (i / UQ) & 1, a.limit_ns, &abort_flag);
+            uu = -1;
+            if (s_ok) {
+              uu = s_uq[q];
+              tc::mbar_arrive(&uq_empty[q]);
+            }
+          }
+          if (s_ok && uu >= 0) s_ok = tc::mbar_wait(&acc_full[buf], use & 1, a.limit_ns, &abort_flag);
           if (!s_ok) fail();
+          s_unit[i & 1] = uu;
         }
         epi_sync();
-        if (!s_ok) break;
+        const int u = s_unit[i & 1];
+        if (!s_ok || u < 0) break;
+        const Unit U = unit_at(a, n_slots, u);
         tc::fence_after_sync();
         float v[32];
         tc::tmem_ld32(trow + 32 * buf, v);
@@ -1756,6 +1806,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       a.ctr[C_DC_DN] = 0;
       a.ctr[C_DC_RT] = 0;
       a.ctr[C_DC_X8] = 0;
+      a.ctr[C_DC_QUEUE] = 0;
       a.ctr[C_DC_EPOCH] = (int)s_epoch;
     }
     __threadfence();
@@ -1785,15 +1836,18 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
   const size_t smem = (size_t)DSTAGES * (nv ? stage_bytes<true>() : stage_bytes<false>()) + 1024;
   static_assert(DSTAGES * stage_bytes<false>() + 1024 > 114 * 1024, "the ring must keep one block per SM");
   const bool wide = T > MAX_DECODE_T;
-  auto kern = nv ? (wide ? k_decode_tc<true, true> : k_decode_tc<true, false>)
-                 : (wide ? k_decode_tc<false, true> : k_decode_tc<false, false>);
+  // one block per SM: every block holds a 200 KB stage ring and a TMEM allocation
+  const int G = imin(sm_count(), DC_MAX_GRID);
+  // dynamic hand-out where the routed gate/up units take more than one round
+  const bool dyn = !wide && imin(n, E) * (I / 128) >= G;
+  auto kern = nv ? (wide ? k_decode_tc<true, true, false> : dyn ? k_decode_tc<true, false, true> : k_decode_tc<true, false, false>)
+                 : (wide ? k_decode_tc<false, true, false>
+                         : dyn ? k_decode_tc<false, false, true> : k_decode_tc<false, false, false>);
   cudaError_t err = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int per_sm = 0;
   if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DT, smem)) != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  // one block per SM: every block holds a 200 KB stage ring and a TMEM allocation
-  const int G = imin(sm_count(), DC_MAX_GRID);
   const bool shared = shd.w13 != nullptr || sh8 != nullptr;
   DcSplits sp = dc_splits(T, H, I, E, k, G);
   if (sh8) {  // MXFP8 stages hold 128 K elements: no more parts than stages

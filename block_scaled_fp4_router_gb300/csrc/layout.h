@@ -155,7 +155,8 @@ enum Counter : int {
   C_DC_DN = 13,    // tensor-core decode: down-projection parts stored
   C_DC_RT = 14,    // tensor-core decode, wide steps: blocks done with their router parts
   C_DC_X8 = 15,    // tensor-core decode, MXFP8 shared expert: blocks done quantising x to MXFP8
-  N_COUNTERS = 16
+  C_DC_QUEUE = 16, // tensor-core decode: units handed out after each block's first
+  N_COUNTERS = 32
 };
 
 MOE_HD inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
