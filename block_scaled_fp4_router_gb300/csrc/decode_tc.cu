@@ -11,41 +11,49 @@
 // a 16-row B operand, so every SM keeps weights in flight without spending
 // CUDA-core issue slots on FP4 decoding.
 //
-// Work units (one block per SM, cooperative launch, the same static
-// round-robin list in every block):
-//   SGU  shared gate/up:  128 gate + 128 up rows x a K part (BF16, kind::f16)
+// Work units (one block per SM, cooperative launch; one unit list, the same
+// in every block, handed out round-robin or, for 16-token-class steps,
+// dynamically in increasing order -- see UQ):
+//   SGU  shared gate/up:  128 gate + 128 up rows x a K part (BF16 kind::f16,
+//                         or MXFP8 kind::mxf8f6f4)
 //   RGU  routed gate/up:  expert slot x 128 gate + 128 up rows x a K part (FP4)
-//   SDN  shared down:     128 rows of H x a K part (BF16)
+//   SDN  shared down:     128 rows of H x a K part (BF16 or MXFP8)
 //   RDN  routed down:     128 rows of H x one expert slot (FP4, whole K)
 // Split-K gate/up parts write FP32 partial sums; the block that delivers the
-// last part of a tile (an atomic ticket) sums the parts in a fixed order and
-// runs the tile's epilogue: SwiGLU to BF16 h (shared) or SwiGLU + MXFP4
-// requantise (routed).  Down parts are counted; once all are stored, the
-// weighted combine out = BF16(ys + sum_j w_j y_j), summed in a fixed order,
-// runs as items of 128 columns x 4 tokens spread over all blocks.  Results
-// are therefore bit-reproducible run to run.  With the shared expert folded
-// into the FP4 table, every token has one more slot (the table's last
-// expert, weight 1) and there are no SGU / SDN units.
+// last part of a tile (an atomic ticket) sums the parts in a fixed order (a
+// tile of one part takes them from its registers) and runs the tile's
+// epilogue: SwiGLU to BF16 h, or MXFP8 h (shared), or SwiGLU + MXFP4
+// requantise (routed).  A routed down unit waits only for its own slot's h.
+// Down parts are counted; once all are stored, the weighted combine
+// out = BF16(ys + sum_j w_j y_j), summed in a fixed order, runs as items of
+// 128 columns x 4 (wide steps 16) tokens spread over all blocks, their rows
+// brought into the idle ring by bulk copies.  Results are therefore
+// bit-reproducible run to run.  With the shared expert folded into the FP4
+// table, every token has one more slot (the table's last expert, weight 1)
+// and there are no SGU / SDN units.
 //
 // Warp roles: warp 0 issues TMA, warp 1 issues tcgen05.cp / tcgen05.mma,
 // warps 2-5 are the epilogue (one TMEM lane = one weight row each).  Before
 // their first unit the epilogue warps compute this block's router rows and
 // its slice of the MXFP4 quantisation of x; once every block has done so they
 // build the routing (top-k, sort by expert) in shared memory and release the
-// producer and MMA warps onto the routed units.  There is no L2 prefetch
-// beyond the stage ring: extra traffic measurably slows the latency-bound
-// hand-offs more than it saves in streaming.
+// producer and MMA warps onto the routed units.  Routed weights load with an
+// evict-first L2 policy, so the small hand-off data (partials, h, y) stays in
+// L2; steps of up to 16 tokens prefetch nothing beyond the stage ring (extra
+// traffic measurably slows their latency-bound hand-offs).
 //
 // Wide steps (17-128 tokens, the W instantiations) keep the 16-row B
 // operand: the shared expert runs per 16-token chunk (SGU / SDN units per
 // chunk), and the routed experts per slot, a run of at most 16 sorted
-// assignments of one expert.  Each block computes the top-k of its own
-// tokens and publishes it tagged with the launch number; every block then
-// sorts all T k assignments by expert (per-warp histograms and scans) in
-// shared memory.  x is quantised after the routing, straight into sorted
-// order, so a slot's activation rows are one 16-row TMA box; the routed
-// gate/up units stream their weight tiles into the ring while they wait for
-// it.
+// assignments of one expert.  The router runs as split-K items, each block
+// computes the top-k of its own tokens and publishes it tagged with the
+// launch number, and every block then sorts all T k assignments by expert
+// (per-warp histograms and scans) in shared memory.  x is quantised in token
+// order while the router parts land and copied into sorted order once the
+// routing is known, so a slot's activation rows are one 16-row TMA box; the
+// routed gate/up units stream their weight tiles into the ring while they
+// wait for it, and the first experts' gate/up weights are prefetched into L2
+// during the routing when the step touches about every expert.
 //
 // Every wait is bounded (MOE_DEV_TIMEOUT in the status word); the last block
 // out resets the counters, and each finishing block resets its ticket.
@@ -159,7 +167,7 @@ struct DcArgs {
   float* w_out;
   int* ctr;
   int* tickets;
-  unsigned long long* logit64;  // [T, E]: (launch number << 32) | FP32 bits
+  unsigned long long* logit64;  // steps of up to 16 tokens: [T, Er] (launch number << 32) | FP32 bits
   uint8_t* xq;               // [T, H/2]; wide steps: [T k, H/2] in sorted-assignment order
   uint8_t* xs_mma;           // [H/128][512] E8M0 (MXFP4) or [H/64][512] UE4M3 (NVFP4); wide steps:
                              // one such set per slot
@@ -249,7 +257,7 @@ __device__ __forceinline__ Unit sdn_unit(const DcArgs& a, int v) {
 // v-th routed down unit: 128-row tile of H x expert slot, whole K, in slot
 // order (slots finish their gate/up in about that order, and each down unit
 // waits only for its own slot's h).
-__device__ __forceinline__ Unit rdn_unit(const DcArgs& a, int n_slots, int v) {
+__device__ __forceinline__ Unit rdn_unit(const DcArgs& a, int v) {
   Unit U{};
   U.kind = U_RDN;
   U.slot = v / (a.H / 128);
@@ -283,7 +291,7 @@ __device__ Unit unit_at(const DcArgs& a, int n_slots, int u) {
   }
   u -= n_rgu;
   if (u < a.n_sdn) return sdn_unit(a, u);
-  return rdn_unit(a, n_slots, u - a.n_sdn);
+  return rdn_unit(a, u - a.n_sdn);
 }
 
 __device__ __forceinline__ void epi_sync() { tc::named_sync(1, EPI_THREADS); }
