@@ -155,6 +155,39 @@ __device__ __forceinline__ int mx8_scale_exp(float amax) {
   return ef == 0 ? -127 : max(ef - 127 - 8, -127);
 }
 
+// MXFP4 codes of one 32-element BF16 block (16 bytes to dq, 16-byte aligned;
+// xb 16-byte aligned) and its E8M0 byte, by one thread.  The same codes and
+// scales as the standalone quantiser (mx_scale_exp, e2m1_rne).
+__device__ __forceinline__ uint8_t quant32(const uint16_t* xb, uint8_t* dq) {
+  const uint4* src = reinterpret_cast<const uint4*>(xb);
+  uint4 raw[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) raw[j] = __ldg(src + j);
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[h])), fabsf(bf16_hi(w4[h]))));
+  }
+  const int ex = mx_scale_exp(amax);
+  const float inv = pow2_neg(ex);
+  uint32_t c[4];
+#pragma unroll 1
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+    uint32_t word = 0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      word |= e2m1_rne(bf16_lo(w4[h]) * inv) << (8 * h);
+      word |= e2m1_rne(bf16_hi(w4[h]) * inv) << (8 * h + 4);
+    }
+    c[j] = word;
+  }
+  *reinterpret_cast<uint4*>(dq) = make_uint4(c[0], c[1], c[2], c[3]);
+  return (uint8_t)(ex + 127);
+}
+
 // One thread quantises 8 consecutive BF16 values x[8g .. 8g+7] to MXFP8
 // (E4M3, one E8M0 scale per 32: X = 2^(floor(log2 amax) - 8)); the 4 threads
 // of a block share their maxima with two shuffles, as in quant8_values.
