@@ -446,16 +446,20 @@ def test_decode_token_counts(T, prepared):
     (128, 512, 256, 16, 7, W.NVFP4, dict(shared=False, shared_fp4=True)),
     (128, 256, 256, 8, 8, W.MXFP4, {}),
     (96, 512, 256, 32, 4, W.MXFP4, dict(score="sigmoid", zipf=0.05)),
+    (128, 256, 256, 256, 8, W.MXFP4, dict(shared=False)),
+    (100, 512, 256, 64, 4, W.NVFP4, dict(shared_fmt="mxfp8")),
 ], ids=["T17", "T33_nvfp4", "T64_k6_noshared", "T100_E255_k8", "T128_nvfp4_fold_n1024", "T128_dense",
-        "T96_sigmoid"])
+        "T96_sigmoid", "T128_E256_k8_n1024", "T100_nvfp4_mxfp8_shared"])
 def test_wide_single_launch_shapes(shape):
     """Steps of 17-128 tokens through moe_layer_decode, one launch: a ragged
     last 16-token chunk (17, 33, 100), E = 255 with k = 8 (800 assignments),
     the folded shared expert at the largest table step (128 tokens x 8 = 1024
     assignments, every expert split over several 16-row slots), a dense
-    mixture (E == k: 128 rows per expert, 8 slots each), NVFP4 with distinct
-    tensor scales, sigmoid scoring.  Every token against the oracle; the
-    launch is bit-reproducible and agrees with the batched path."""
+    mixture (E == k: 128 rows per expert, 8 slots each), 1024 assignments over
+    256 experts (up to 320 slots, the shared-memory table's bound), NVFP4
+    with distinct tensor scales and an MXFP8 shared expert, sigmoid scoring.
+    Every token against the oracle; the launch is bit-reproducible and agrees
+    with the batched path."""
     T, H, I, E, k, fmt, kw = shape
     # router weights of std 0.08: logits of std ~1-2 (the workloads' regime),
     # where the FP32 router's rounding stays far below the weights' rtol
