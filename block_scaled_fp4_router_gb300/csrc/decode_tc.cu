@@ -18,7 +18,8 @@
 //                         or MXFP8 kind::mxf8f6f4)
 //   RGU  routed gate/up:  expert slot x 128 gate + 128 up rows x a K part (FP4)
 //   SDN  shared down:     128 rows of H x a K part (BF16 or MXFP8)
-//   RDN  routed down:     128 rows of H x one expert slot (FP4, whole K)
+//   RDN  routed down:     2 x 128 rows of H x one expert slot (FP4, whole
+//                         K; both tiles share the slot's h tile)
 // Split-K gate/up parts write FP32 partial sums; the block that delivers the
 // last part of a tile (an atomic ticket) sums the parts in a fixed order (a
 // tile of one part takes them from its registers) and runs the tile's
@@ -231,7 +232,7 @@ struct Unit {
 };
 
 __device__ __forceinline__ int units_total(const DcArgs& a, int n_slots) {
-  return a.n_sgu + n_slots * (a.I / 128) * a.s_rgu + a.n_sdn + n_slots * (a.H / 128);
+  return a.n_sgu + n_slots * (a.I / 128) * a.s_rgu + a.n_sdn + n_slots * (a.H / 256);
 }
 
 // Part p of `stages` stages split into s near-equal parts.
@@ -254,16 +255,18 @@ __device__ __forceinline__ Unit sdn_unit(const DcArgs& a, int v) {
   return U;
 }
 
-// v-th routed down unit: 128-row tile of H x expert slot, whole K, in slot
-// order (slots finish their gate/up in about that order, and each down unit
-// waits only for its own slot's h).
+// v-th routed down unit: a pair of 128-row tiles of H (rows 256 tile ..
+// 256 tile + 255) x expert slot, whole K, one 256-element K chunk per stage,
+// in slot order (slots finish their gate/up in about that order, and each
+// down unit waits only for its own slot's h).  The pair shares one h tile
+// per stage, as the gate/up units share their x tile.
 __device__ __forceinline__ Unit rdn_unit(const DcArgs& a, int v) {
   Unit U{};
   U.kind = U_RDN;
-  U.slot = v / (a.H / 128);
-  U.tile = v % (a.H / 128);
+  U.slot = v / (a.H / 256);
+  U.tile = v % (a.H / 256);
   U.st0 = 0;
-  U.st1 = (a.I / 256 + 1) / 2;
+  U.st1 = a.I / 256;
   return U;
 }
 
@@ -921,12 +924,11 @@ __device__ void build_routing_w(const DcArgs& a, DcRouting<true>& R, int et, uin
   epi_sync();
 }
 
-// Halves of a stage that a unit uses: gate/up units one K chunk (two weight
-// tiles, one activation tile), down units two K chunks (the second may be
-// past the end of K).
+// Halves of a stage that a unit uses: gate/up and routed down units one K
+// chunk (two weight tiles, one activation tile), shared down units two K
+// chunks (the second may be past the end of K).
 __device__ __forceinline__ int stage_halves(const DcArgs& a, const Unit& U, int st) {
   if (U.kind == U_SDN) return 2 * st + 1 < a.I / (a.sh8 ? 128 : 64) ? 2 : 1;
-  if (U.kind == U_RDN) return 2 * st + 1 < a.I / 256 ? 2 : 1;
   return 2;
 }
 
@@ -939,9 +941,8 @@ __device__ __forceinline__ uint32_t stage_tx(const DcArgs& a, const Unit& U, int
   const uint32_t h = stage_halves(a, U, st);
   switch (U.kind) {
     case U_SGU: return 2 * A_TILE + B_TILE + (a.sh8 ? 3 * 512 : 0);
-    case U_RGU: return 2 * A_TILE + B_TILE + 3 * sf_chunk<NV>();
     case U_SDN: return h * (A_TILE + B_TILE + (a.sh8 ? 2 * 512 : 0));
-    default: return h * (A_TILE + B_TILE + 2 * sf_chunk<NV>());
+    default: return 2 * A_TILE + B_TILE + 3 * sf_chunk<NV>();  // routed gate/up and down
   }
 }
 
@@ -974,15 +975,16 @@ __device__ __forceinline__ void issue_weights(const DcArgs& a, const DcMaps& m, 
       tc::tma_load_2d(sp + (h ? ST_A1 : ST_A0), &m.w2s, (2 * st + h) * 128, 128 * U.tile, fb);
     if (a.sh8)
       tc::bulk_load(sp + ST_SFA, a.w2s8_mma + ((size_t)U.tile * (a.I / 128) + 2 * st) * 512, halves * 512, fb);
-  } else {
-    const int halves = stage_halves(a, U, st);
+  } else {  // routed down: two 128-row tiles of H, one K chunk
     const uint64_t pol = tc::l2_evict_first();
-    for (int h = 0; h < halves; ++h)
-      tc::tma_load_2d_hint(sp + (h ? ST_A1 : ST_A0), &m.w2r, (2 * st + h) * 128, e * a.H + 128 * U.tile, fb, pol);
+    const int row = e * a.H + 256 * U.tile;
+    tc::tma_load_2d_hint(sp + ST_A0, &m.w2r, st * 128, row, fb, pol);
+    tc::tma_load_2d_hint(sp + ST_A1, &m.w2r, st * 128, row + 128, fb, pol);
     const uint32_t sfc = sf_chunk<NV>();
     const size_t bpr = (size_t)a.I / 256 * (sfc / 512);
-    tc::bulk_load_hint(sp + ST_SFA, a.w2s_mma + ((size_t)e * nbH + U.tile) * bpr * 512 + (size_t)2 * st * sfc,
-                       halves * sfc, fb, pol);
+    const size_t rt = (size_t)e * nbH + 2 * U.tile;
+    tc::bulk_load_hint(sp + ST_SFA, a.w2s_mma + rt * bpr * 512 + (size_t)st * sfc, sfc, fb, pol);
+    tc::bulk_load_hint(sp + ST_SFA + sfc, a.w2s_mma + (rt + 1) * bpr * 512 + (size_t)st * sfc, sfc, fb, pol);
   }
 }
 
@@ -1007,12 +1009,10 @@ __device__ __forceinline__ void issue_acts(const DcArgs& a, const DcMaps& m, con
     if (a.sh8)
       tc::bulk_load(sp + st_sfb<NV>(), a.h8s + ((size_t)U.chunk * (a.I / 128) + 2 * st) * 512, halves * 512, fb);
   } else {
-    const int halves = stage_halves(a, U, st);
-    for (int h = 0; h < halves; ++h)
-      tc::tma_load_2d(sp + (h ? ST_B1 : ST_B0), &m.hq, (2 * st + h) * 128, beg, fb);
     const size_t bpr = (size_t)a.I / 256 * nblk<NV>();  // scale blocks of one slot
-    tc::bulk_load(sp + st_sfb<NV>(), a.hs_mma + (size_t)U.slot * bpr * 512 + (size_t)2 * st * sf_chunk<NV>(),
-                  halves * sf_chunk<NV>(), fb);
+    tc::tma_load_2d(sp + ST_B0, &m.hq, st * 128, beg, fb);
+    tc::bulk_load(sp + st_sfb<NV>(), a.hs_mma + (size_t)U.slot * bpr * 512 + (size_t)st * sf_chunk<NV>(),
+                  sf_chunk<NV>(), fb);
   }
 }
 
@@ -1325,7 +1325,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               tc::mma_bf16(acc, tc::desc_sw128(sa + ST_A0 + 32 * kk), bd, id_bf, accum);
               tc::mma_bf16(acc + 16, tc::desc_sw128(sa + ST_A1 + 32 * kk), bd, id_bf, accum);
             }
-          } else if (U.kind == U_RGU) {
+          } else if (U.kind == U_RGU || U.kind == U_RDN) {
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
               tc::sf_copy(tsf + 4 * b, tc::desc_sf(sa + ST_SFA + 512 * b));
@@ -1362,23 +1362,6 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
                 const uint32_t accum = (first && h == 0 && kk == 0) ? 0u : 1u;
                 tc::mma_bf16(acc, tc::desc_sw128(sa + (h ? ST_A1 : ST_A0) + 32 * kk),
                              tc::desc_sw128(sa + (h ? ST_B1 : ST_B0) + 32 * kk), id_bf, accum);
-              }
-            }
-          } else {
-            const int halves = stage_halves(a, U, st);
-            for (int h = 0; h < halves; ++h)
-#pragma unroll
-              for (int b = 0; b < NB; ++b) {
-                tc::sf_copy(tsf + 4 * NB * h + 4 * b, tc::desc_sf(sa + ST_SFA + 512 * (NB * h + b)));
-                tc::sf_copy(tsf + 4 * NB * (2 + h) + 4 * b, tc::desc_sf(sa + ST_SFB + 512 * (NB * h + b)));
-              }
-            for (int h = 0; h < halves; ++h) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t accum = (first && h == 0 && kk == 0) ? 0u : 1u;
-                fp4_mma<NV>(acc, tc::desc_sw128(sa + (h ? ST_A1 : ST_A0) + 32 * kk),
-                            tc::desc_sw128(sa + (h ? ST_B1 : ST_B0) + 32 * kk), kk, tsf + 4 * NB * h,
-                            tsf + 4 * NB * (2 + h), accum);
               }
             }
           }
@@ -1557,11 +1540,16 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         } else {
           // B held the slot's sorted rows: column c is sorted position beg + c
           // (NVFP4: times the expert's down tensor scale and 2^c of the h row)
-          float* dst = a.y_assign + (size_t)beg * H + 128 * U.tile + m;
+          // columns 0-15: the pair's first 128 rows of H, 16-31: its second
+          float* dst = a.y_assign + (size_t)beg * H + 256 * U.tile + m;
           const float sd = NV ? __ldg(a.tscale + 3 * R.slot_e[U.slot] + 2) : 1.0f;
 #pragma unroll
           for (int c = 0; c < MAX_DECODE_T; ++c)
-            if (c < cnt) dst[(size_t)c * H] = NV ? v[c] * (sd * pow2f(h_row_shift(a, beg + c))) : v[c];
+            if (c < cnt) {
+              const float f = NV ? sd * pow2f(h_row_shift(a, beg + c)) : 1.0f;
+              dst[(size_t)c * H] = NV ? v[c] * f : v[c];
+              dst[(size_t)c * H + 128] = NV ? v[16 + c] * f : v[16 + c];
+            }
           ticket = -1;
           target = 0;
         }
@@ -1569,7 +1557,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         if (ticket < 0) {
           // a down part: counted without waiting; the combine runs after the unit list
           epi_sync();
-          if (et == 0) red_release_add(a.ctr + C_DC_DN, 1);
+          if (et == 0) red_release_add(a.ctr + C_DC_DN, U.kind == U_RDN ? 2 : 1);
           continue;
         }
         // split-K arrival: the block that brings the last part finishes the
