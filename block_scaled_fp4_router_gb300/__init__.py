@@ -344,17 +344,19 @@ def moe_debug_launch_count() -> int:
     return n.value
 
 
-def moe_debug_decode_trace(clear: bool = False):
+def moe_debug_decode_trace(clear: bool = False, slots: bool = False):
     """Trace builds: the last single-launch decode's per-block %globaltimer
-    stamps as a numpy uint64 array [256 blocks, 16 events] (clear=True zeroes
-    them and returns None)."""
+    stamps as a numpy uint64 array [256 blocks, 16 events]; with slots=True
+    also the per-slot stamps [320 slots, 8] (a pair).  clear=True zeroes both
+    and returns None."""
     import numpy as np
     if clear:
         _check(load().moe_debug_decode_trace(None, 0), "moe_debug_decode_trace")
         return None
-    out = np.zeros((256, 16), np.uint64)
+    out = np.zeros((256 * 16 + (320 * 8 if slots else 0),), np.uint64)
     _check(load().moe_debug_decode_trace(ctypes.c_void_p(out.ctypes.data), out.nbytes), "moe_debug_decode_trace")
-    return out
+    blocks = out[:256 * 16].reshape(256, 16)
+    return (blocks, out[256 * 16:].reshape(320, 8)) if slots else blocks
 
 
 def moe_set_timing_events(begin=None, end=None) -> None:

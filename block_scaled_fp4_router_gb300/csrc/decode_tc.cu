@@ -86,12 +86,28 @@ enum DcTraceEvent {
   TR_END = 10,         // epilogue: combine done
   TR_LAST_UNIT = 11,   // + unit kind: the block's last unit of that kind finished
 };
+// Per expert slot (the first DC_TRACE_SLOTS): earliest and latest hand-out
+// of its routed gate/up units, latest gate/up unit done, h ready, earliest
+// and latest hand-out of its down units, latest down unit stored, and
+// (expert << 8 | rows).  Earliest times are kept as ~t under atomicMax, so
+// that zeroed entries mean "not reached".
+enum DcSlotEvent { TS_RGU_FIRST = 0, TS_RGU_LAST, TS_RGU_DONE, TS_H, TS_RDN_FIRST, TS_RDN_LAST, TS_RDN_DONE, TS_INFO };
 #if MOEFP4_TRACE
 constexpr int DC_TRACE_EVENTS = 16;
+constexpr int DC_TRACE_SLOTS = 320;
 __device__ unsigned long long g_dc_trace[DC_MAX_GRID][DC_TRACE_EVENTS];
+__device__ unsigned long long g_dc_slot_trace[DC_TRACE_SLOTS][8];
 #define DC_TRACE(ev) (g_dc_trace[blockIdx.x][(ev)] = globaltimer_ns())
+#define DC_SLOT_FIRST(s, ev) \
+  ((s) < DC_TRACE_SLOTS ? (void)atomicMax(&g_dc_slot_trace[(s)][(ev)], ~globaltimer_ns()) : (void)0)
+#define DC_SLOT_LAST(s, ev) \
+  ((s) < DC_TRACE_SLOTS ? (void)atomicMax(&g_dc_slot_trace[(s)][(ev)], globaltimer_ns()) : (void)0)
+#define DC_SLOT_SET(s, ev, v) ((s) < DC_TRACE_SLOTS ? (void)(g_dc_slot_trace[(s)][(ev)] = (v)) : (void)0)
 #else
 #define DC_TRACE(ev) ((void)0)
+#define DC_SLOT_FIRST(s, ev) ((void)0)
+#define DC_SLOT_LAST(s, ev) ((void)0)
+#define DC_SLOT_SET(s, ev, v) ((void)0)
 #endif
 
 constexpr int DT = 192;                 // threads: TMA warp, MMA warp, 4 epilogue warps
@@ -1023,20 +1039,33 @@ __device__ __forceinline__ int h_row_shift(const DcArgs& a, int p);
 // beg+cnt-1) for the down MMA, [I/64][512 B], from their E8M0 bytes and the
 // row shift 2^c (c = the row's largest exponent - 8).  128 threads; thread
 // et writes word et of every block (row et/4 when et % 4 == 0, else zero).
+// A row's bytes (I/32, a multiple of 8) are loaded 64 at a time by eight
+// 8-byte loads in flight together: one round trip, not one per block.
 __device__ void convert_h_scales_nv(const DcArgs& a, int slot, int beg, int cnt, int et) {
-  const int nb = a.I / 32, r = et >> 2;
+  const int nb = a.I / 32, ng = a.I / 64, r = et >> 2;
   const bool real = (et & 3) == 0 && r < cnt;
-  const int c = real ? h_row_shift(a, beg + r) : 0;
-  const uint8_t* hsr = a.hsc + (size_t)(beg + (real ? r : 0)) * nb;
-  uint32_t* dst = reinterpret_cast<uint32_t*>(a.hs_mma) + (size_t)slot * (a.I / 64) * 128 + et;
-  for (int g = 0; g < a.I / 64; ++g) {
-    uint32_t word = 0;
-    if (real) {
-      const uint32_t u0 = ue4m3_pow2((int)__ldcg(hsr + 2 * g) - 127 - c);
-      const uint32_t u1 = ue4m3_pow2((int)__ldcg(hsr + 2 * g + 1) - 127 - c);
-      word = u0 | (u0 << 8) | (u1 << 16) | (u1 << 24);
-    }
-    dst[(size_t)g * 128] = word;
+  const uint2* hsr = reinterpret_cast<const uint2*>(a.hsc + (size_t)(beg + (real ? r : 0)) * nb);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(a.hs_mma) + (size_t)slot * ng * 128 + et;
+  int c = 0;
+  for (int g0 = 0; g0 < ng; g0 += 32) {  // blocks g0 .. g0 + 31: bytes 2 g0 .. 2 g0 + 63
+    uint2 b[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = real && 2 * g0 + 8 * j < nb ? __ldcg(hsr + g0 / 4 + j) : make_uint2(0, 0);
+    if (g0 == 0 && real) c = h_row_shift(a, beg + r);  // after the first bytes' loads: both in flight
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (g0 + j < ng) {
+        uint32_t word = 0;
+        if (real) {
+          // block g0 + j: bytes 2j and 2j + 1 of the chunk
+          const uint32_t w32 = (j & 2) ? b[j / 4].y : b[j / 4].x;
+          const int sh = 16 * (j & 1);
+          const uint32_t u0 = ue4m3_pow2((int)((w32 >> sh) & 0xffu) - 127 - c);
+          const uint32_t u1 = ue4m3_pow2((int)((w32 >> (sh + 8)) & 0xffu) - 127 - c);
+          word = u0 | (u0 << 8) | (u1 << 16) | (u1 << 24);
+        }
+        dst[(size_t)(g0 + j) * 128] = word;
+      }
   }
 }
 
@@ -1082,6 +1111,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
   static_assert(alignof(DcRouting<W>) >= 16, "float4 accesses to the staged x");
   __shared__ float red_s[EPI_THREADS / 32][MAX_DECODE_T];
   __shared__ __align__(4) uint8_t s_hsb[MAX_DECODE_T * 4];
+  __shared__ int s_rows[MAX_DECODE_T];  // NVFP4: the current slot's per-row exponent shifts
   __shared__ uint8_t s_qe[EPI_THREADS / 32][256];  // NVFP4 quantiser: a row's block exponents
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nbI = a.I / 128, nbH = a.H / 128;
@@ -1190,6 +1220,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         if (U.kind == U_RGU || U.kind == U_RDN) {
           e = R.slot_e[U.slot];
           beg = R.slot_beg[U.slot];
+          DC_SLOT_FIRST(U.slot, U.kind == U_RGU ? TS_RGU_FIRST : TS_RDN_FIRST);
+          DC_SLOT_LAST(U.slot, U.kind == U_RGU ? TS_RGU_LAST : TS_RDN_LAST);
         }
         // Down units read h that other blocks write (and, in wide steps,
         // routed gate/up units the sorted x rows).  While it is not there
@@ -1505,6 +1537,9 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             const int e = R.slot_e[U.slot];
             sg = __ldg(a.tscale + 3 * e);
             su = __ldg(a.tscale + 3 * e + 1);
+            // the rows' x shifts 2^c_t, loaded together (one round trip)
+            if (et < cnt) s_rows[et] = __ldcg(a.xshift + R.tok[beg + et]);
+            epi_sync();
           }
           if (a.s_rgu == 1) {
             // the tile's only part: the finisher takes the sums from v
@@ -1515,14 +1550,14 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
 #pragma unroll
             for (int c = 0; c < 16; ++c)
               if (c < cnt) {
-                const float f = NV ? pow2f(__ldcg(a.xshift + R.tok[beg + c])) : 1.0f;
+                const float f = NV ? pow2f(s_rows[c]) : 1.0f;
                 dst[(size_t)c * 2 * I] = v[c] * (sg * f);
                 dst[(size_t)c * 2 * I + I] = v[16 + c] * (su * f);
               }
           } else {
             for (int c = 0; c < cnt; ++c) {
               const int t = R.tok[beg + c];
-              const float f = NV ? pow2f(__ldcg(a.xshift + t)) : 1.0f;
+              const float f = NV ? pow2f(s_rows[c]) : 1.0f;
               dst[(size_t)c * 2 * I] = pick16(v, 0, t) * (sg * f);
               dst[(size_t)c * 2 * I + I] = pick16(v, 16, t) * (su * f);
             }
@@ -1543,10 +1578,14 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           // columns 0-15: the pair's first 128 rows of H, 16-31: its second
           float* dst = a.y_assign + (size_t)beg * H + 256 * U.tile + m;
           const float sd = NV ? __ldg(a.tscale + 3 * R.slot_e[U.slot] + 2) : 1.0f;
+          if (NV) {  // the rows' shifts, loaded together (one round trip, not one per row)
+            if (et < cnt) s_rows[et] = h_row_shift(a, beg + et);
+            epi_sync();
+          }
 #pragma unroll
           for (int c = 0; c < MAX_DECODE_T; ++c)
             if (c < cnt) {
-              const float f = NV ? sd * pow2f(h_row_shift(a, beg + c)) : 1.0f;
+              const float f = NV ? sd * pow2f(s_rows[c]) : 1.0f;
               dst[(size_t)c * H] = NV ? v[c] * f : v[c];
               dst[(size_t)c * H + 128] = NV ? v[16 + c] * f : v[16 + c];
             }
@@ -1554,10 +1593,12 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
           target = 0;
         }
         if (et == 0) DC_TRACE(TR_LAST_UNIT + U.kind);
+        if (et == 0 && U.kind == U_RGU) DC_SLOT_LAST(U.slot, TS_RGU_DONE);
         if (ticket < 0) {
           // a down part: counted without waiting; the combine runs after the unit list
           epi_sync();
           if (et == 0) red_release_add(a.ctr + C_DC_DN, U.kind == U_RDN ? 2 : 1);
+          if (et == 0 && U.kind == U_RDN) DC_SLOT_LAST(U.slot, TS_RDN_DONE);
           continue;
         }
         // split-K arrival: the block that brings the last part finishes the
@@ -1622,7 +1663,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             float g, up;
             if (a.s_rgu == 1) {  // the same products the part store would hold
               const int col = W ? c : R.tok[beg + c];
-              const float f = NV ? pow2f(__ldcg(a.xshift + R.tok[beg + c])) : 1.0f;
+              const float f = NV ? pow2f(s_rows[c]) : 1.0f;  // loaded at the unit's start
               g = pick16(v, 0, col) * (rg_sg * f);
               up = pick16(v, 16, col) * (rg_su * f);
             } else {
@@ -1658,6 +1699,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             if (et == 0) {
               red_release_add(a.tickets + a.tk_slot + U.slot, 1);
               red_release_add(a.ctr + C_DC_HR, 1);
+              DC_SLOT_LAST(U.slot, TS_H);
+              DC_SLOT_SET(U.slot, TS_INFO, ((unsigned long long)R.slot_e[U.slot] << 8) | (unsigned)cnt);
             }
           } else {
             // NVFP4: the slot's last finished tile knows every row's largest
@@ -1679,6 +1722,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               if (et == 0) {
                 red_release_add(a.tickets + a.tk_slot + U.slot, 1);
                 red_release_add(a.ctr + C_DC_HR, 1);
+                DC_SLOT_LAST(U.slot, TS_H);
+                DC_SLOT_SET(U.slot, TS_INFO, ((unsigned long long)R.slot_e[U.slot] << 8) | (unsigned)cnt);
               }
             }
           }
@@ -1920,10 +1965,20 @@ cudaError_t launch_fused_decode_tc(const Shape& sh, const ExpertsDev& ex, const 
 extern "C" MOE_API moe_status_t moe_debug_decode_trace(uint64_t* dst, size_t bytes) {
 #if MOEFP4_TRACE
   void* p = nullptr;
+  void* q = nullptr;
   if (cudaGetSymbolAddress(&p, moefp4::g_dc_trace) != cudaSuccess) return MOE_ERR_CUDA;
-  const size_t all = sizeof(moefp4::g_dc_trace);
-  const cudaError_t e = dst ? cudaMemcpy(dst, p, bytes < all ? bytes : all, cudaMemcpyDeviceToHost)
-                            : cudaMemset(p, 0, all);
+  if (cudaGetSymbolAddress(&q, moefp4::g_dc_slot_trace) != cudaSuccess) return MOE_ERR_CUDA;
+  const size_t nb = sizeof(moefp4::g_dc_trace), ns = sizeof(moefp4::g_dc_slot_trace);
+  cudaError_t e;
+  if (!dst) {
+    e = cudaMemset(p, 0, nb);
+    if (e == cudaSuccess) e = cudaMemset(q, 0, ns);
+  } else {
+    e = cudaMemcpy(dst, p, bytes < nb ? bytes : nb, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && bytes > nb)
+      e = cudaMemcpy(reinterpret_cast<uint8_t*>(dst) + nb, q, bytes - nb < ns ? bytes - nb : ns,
+                     cudaMemcpyDeviceToHost);
+  }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 #else
   (void)dst;

@@ -6,7 +6,9 @@ Builds and loads the trace variant of the library (libmoefp4_trace.so,
 MOEFP4_TRACE=1), runs a few steps of each workload on one random layer, and
 prints, for the last step, when each phase boundary was reached: minimum,
 median and maximum over the blocks, in microseconds after the earliest block
-started.  The trace stamps are plain stores of %globaltimer, so the timeline
+started.  With --slots it also prints, per expert slot, when its routed
+gate/up and down units were handed out and done and when its h was ready.
+The trace stamps are plain stores (per-slot ones: atomics) of %globaltimer, so the timeline
 costs the launch a few hundred nanoseconds at most; step times printed here
 are host-timed around single launches (no CUDA graph) and are not bench
 values.
@@ -36,7 +38,32 @@ EVENTS = [
 ]
 
 
-def timeline(name: str, steps: int = 12, device: int = 0) -> str:
+SLOT_COLUMNS = ["gate/up first out", "gate/up last out", "gate/up last done", "h ready", "down first out",
+                "down last out", "down last done"]
+
+
+def slot_table(sl, t0) -> list:
+    """Per expert slot: the stamps of its units (us after t0), in slot order."""
+    lines = ["| slot | expert | rows | " + " | ".join(SLOT_COLUMNS) + " |", "|---" * (3 + len(SLOT_COLUMNS)) + "|"]
+    mask = (1 << 64) - 1
+    for s in range(sl.shape[0]):
+        info = int(sl[s, 7])
+        if info == 0:
+            continue
+        cells = []
+        for c in range(7):
+            v = int(sl[s, c])
+            if v == 0:
+                cells.append("-")
+                continue
+            if c in (0, 4):  # earliest times are stored complemented
+                v = ~v & mask
+            cells.append("%.1f" % ((v - t0) / 1e3))
+        lines.append("| %d | %d | %d | %s |" % (s, info >> 8, info & 0xFF, " | ".join(cells)))
+    return lines
+
+
+def timeline(name: str, steps: int = 12, device: int = 0, slots: bool = False) -> str:
     import numpy as np
     import torch
 
@@ -63,7 +90,8 @@ def timeline(name: str, steps: int = 12, device: int = 0) -> str:
         torch.cuda.synchronize(dev)
         us.append(b.elapsed_time(e) * 1e3)
     status = M.moe_get_status(lay.ws)
-    tr = M.moe_debug_decode_trace().astype(np.int64)
+    tr, sl = M.moe_debug_decode_trace(slots=True)
+    tr = tr.astype(np.int64)
     started = tr[:, 0] > 0
     t0 = tr[started, 0].min()
     lines = ["%s: T=%d, %d blocks, host-timed step %.1f us (median of %d), status %d"
@@ -76,6 +104,9 @@ def timeline(name: str, steps: int = 12, device: int = 0) -> str:
             continue
         d = (v - t0) / 1e3
         lines.append("| %s | %d | %.1f | %.1f | %.1f |" % (label, v.size, d.min(), np.median(d), d.max()))
+    if slots:
+        lines.append("")
+        lines += slot_table(sl, int(t0))
     del lay
     torch.cuda.empty_cache()
     return "\n".join(lines)
@@ -85,6 +116,7 @@ def main() -> None:
     p = argparse.ArgumentParser()
     p.add_argument("workloads", nargs="+")
     p.add_argument("--steps", type=int, default=12)
+    p.add_argument("--slots", action="store_true", help="also a per-slot table of the routed units")
     args = p.parse_args()
     from block_scaled_fp4_router_gb300 import build as B
 
@@ -94,7 +126,7 @@ def main() -> None:
 
     M.load(M.TRACE_LIB_PATH)
     for name in args.workloads:
-        print(timeline(name, args.steps))
+        print(timeline(name, args.steps, slots=args.slots))
         print()
 
 

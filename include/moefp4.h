@@ -355,9 +355,13 @@ MOE_API moe_status_t moe_layer_decode_shared_mxfp8(const moe_layer_desc_t* desc,
  * per-block %globaltimer stamps (ns) of the last single-launch decode,
  * uint64 [256 blocks][16 events], events in the order start, router done,
  * routing built, x quantised, x seen, shared h seen, routed h seen, producer
- * done, units done, down parts seen, end, last SGU / RGU / SDN / RDN unit.
- * Copies min(bytes, 32768) bytes to host memory dst; dst NULL clears the
- * stamps.  Other builds return MOE_ERR_UNSUPPORTED. */
+ * done, units done, down parts seen, end, last SGU / RGU / SDN / RDN unit;
+ * then uint64 [320 expert slots][8]: first (stored as ~t) and last hand-out
+ * of the slot's routed gate/up units, last gate/up unit done, h ready, first
+ * (~t) and last hand-out of its down units, last down unit stored, and
+ * expert << 8 | rows (0: slot not reached).  Copies min(bytes, 53248) bytes
+ * to host memory dst; dst NULL clears both.  Other builds return
+ * MOE_ERR_UNSUPPORTED. */
 MOE_API moe_status_t moe_debug_decode_trace(uint64_t* dst, size_t bytes);
 
 /* The whole layer for any T, as the sequence router -> quantise -> permute ->

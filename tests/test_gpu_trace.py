@@ -1,7 +1,7 @@
 """The trace build (MOEFP4_TRACE=1) on the GPU: the single-launch decode
-stamps every block's phase boundaries, in order, and computes the same
-output as the product build.  Runs in a child process (the binding loads one
-library per process)."""
+stamps every block's phase boundaries and every expert slot's unit
+hand-outs, in order, and computes the same output as the product build.
+Runs in a child process (the binding loads one library per process)."""
 import os
 import subprocess
 import sys
@@ -28,7 +28,19 @@ for T in (5, 40):
     out, ids, _ = dev.decode(x)
     torch.cuda.synchronize()
     assert M.moe_get_status(dev.ws) == M.MOE_OK
-    tr = M.moe_debug_decode_trace().astype(np.int64)
+    tr, sl = M.moe_debug_decode_trace(slots=True)
+    tr = tr.astype(np.int64)
+    # per-slot stamps: every assignment in one reached slot; each slot's gate/up
+    # handed out, then done, then its h ready, then its down units stored
+    info = sl[:, 7].astype(np.int64)
+    reached = info > 0
+    assert int((info[reached] & 0xFF).sum()) == T * wl.top_k
+    st = sl[reached].copy()
+    st[:, 0] = np.invert(st[:, 0])
+    st[:, 4] = np.invert(st[:, 4])
+    st = st.astype(np.int64)
+    assert np.all(st[:, 0] <= st[:, 1]) and np.all(st[:, 1] <= st[:, 2]) and np.all(st[:, 2] <= st[:, 3])
+    assert np.all(st[:, 4] <= st[:, 5]) and np.all(st[:, 5] <= st[:, 6]) and np.all(st[:, 3] <= st[:, 6])
     blocks = tr[:, 0] > 0
     nb = int(blocks.sum())
     assert nb >= 1 and np.all(tr[nb:, 0] == 0)
