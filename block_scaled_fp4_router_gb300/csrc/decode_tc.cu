@@ -1606,13 +1606,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
         if (target > 1) {
           epi_sync();
           if (et == 0) {
-            __threadfence();
-            const int old = atomicAdd(a.tickets + ticket, 1);
-            s_last = old == target - 1;
-            if (s_last) {
-              a.tickets[ticket] = 0;
-              __threadfence();
-            }
+            s_last = atom_add_acq_rel(a.tickets + ticket, 1) == target - 1;
+            if (s_last) a.tickets[ticket] = 0;  // no other arrival follows in this launch
           }
           epi_sync();
           if (!s_last) continue;
@@ -1706,13 +1701,8 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
             // NVFP4: the slot's last finished tile knows every row's largest
             // exponent and writes the slot's UE4M3 scale blocks for the down MMA
             if (et == 0) {
-              __threadfence();
-              const int old = atomicAdd(a.tickets + a.tk_nv + U.slot, 1);
-              s_last = old == nbI - 1;
-              if (s_last) {
-                a.tickets[a.tk_nv + U.slot] = 0;
-                __threadfence();
-              }
+              s_last = atom_add_acq_rel(a.tickets + a.tk_nv + U.slot, 1) == nbI - 1;
+              if (s_last) a.tickets[a.tk_nv + U.slot] = 0;
             }
             epi_sync();
             if (s_last) {
