@@ -1666,7 +1666,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
               up = sum_parts(src + (size_t)c * 2 * I + I, stride, a.s_rgu);
             }
             const float h = silu(g) * up;
-            const int ex = mx_scale_exp(warp_max(fabsf(h)));
+            const int ex = mx_scale_exp(warp_max_nonneg(fabsf(h)));
             uint32_t wv = e2m1_rne(h * pow2_neg(ex)) << (4 * (lane & 7));
             wv |= __shfl_xor_sync(FULL, wv, 1);
             wv |= __shfl_xor_sync(FULL, wv, 2);
@@ -1789,10 +1789,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
   // The last block out resets the launch's counters for the next call and
   // clears the NVFP4 row exponents (atomicMax words: a word tagged with an
   // older launch number than the next launch's would otherwise win it).
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(a.ctr + C_DC_EXIT, 1) == a.G - 1;
-  }
+  if (threadIdx.x == 0) s_last = atom_add_acq_rel(a.ctr + C_DC_EXIT, 1) == a.G - 1;
   __syncthreads();
   if (s_last) {
     if (a.nv)
@@ -1809,7 +1806,7 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       a.ctr[C_DC_QUEUE] = 0;
       a.ctr[C_DC_EPOCH] = (int)s_epoch;
     }
-    __threadfence();
+    // (the launch's end makes these stores visible to the next launch)
   }
 }
 
