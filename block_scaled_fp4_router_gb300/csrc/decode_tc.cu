@@ -115,9 +115,9 @@ constexpr int EPI_THREADS = 128;
 // A 4-stage ring, of which the host lets `depth` stages be in flight: two
 // for a step of up to 15 assignments (its shared units stream while the
 // routing is computed, and a deeper queue slows the latency-bound hand-offs),
-// four for the larger steps.  Routed down units always put all their weight
-// copies (at most three stages at I = 1536) into the ring before they wait
-// for their slot's h.
+// four for the larger steps.  Routed down units put up to four of their
+// weight stages (of six at I = 1536) into the ring before they wait for
+// their slot's h.
 constexpr int DSTAGES = 4;
 // byte offsets inside one stage (swizzled tiles on 1024-byte boundaries)
 constexpr uint32_t ST_A0 = 0, ST_A1 = 16384;       // 128 rows x 128 B each
