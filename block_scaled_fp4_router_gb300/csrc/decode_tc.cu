@@ -27,8 +27,8 @@
 // requantise (routed).  A routed down unit waits only for its own slot's h.
 // Down parts are counted; once all are stored, the weighted combine
 // out = BF16(ys + sum_j w_j y_j), summed in a fixed order, runs as items of
-// 128 columns x 4 (wide steps 16) tokens spread over all blocks, their rows
-// brought into the idle ring by bulk copies.  Results are therefore
+// 128 columns x 4 (wide steps 32 or 16) tokens spread over all blocks, their
+// rows brought into the idle ring by bulk copies.  Results are therefore
 // bit-reproducible run to run.  With the shared expert folded into the FP4
 // table, every token has one more slot (the table's last expert, weight 1)
 // and there are no SGU / SDN units.
@@ -1727,9 +1727,11 @@ __global__ void __launch_bounds__(DT, 1) k_decode_tc(const __grid_constant__ DcM
       // ring by bulk copies, all in flight at once, and are summed from
       // shared memory, so an item costs one load round trip and the code,
       // which runs once per launch, stays compact.
-      constexpr int CT = W ? 16 : 4;
-      const int n_items = nbH * ((T + CT - 1) / CT);
       const int nsp = a.shared ? a.s_sdn : 0, rpt = k + nsp;  // rows per token
+      // wide steps: 32 tokens per item (one round of items at 128 tokens)
+      // where their rows fit the ring, else 16; narrow steps 4
+      const int CT = W ? (32 * rpt * 512 <= DSTAGES * (int)STAGE_BYTES ? 32 : 16) : 4;
+      const int n_items = nbH * ((T + CT - 1) / CT);
       if ((int)blockIdx.x < n_items) {
         if (et == 0) {
           s_ok = wait_at_least(a.ctr + C_DC_DN, dn_total, status, a.limit_ns);
