@@ -719,11 +719,13 @@ def test_small_and_degenerate_shapes(shape):
 
 @pytest.mark.parametrize("shape", [(5, 256, 256, 256, 8, W.MXFP4), (16, 256, 512, 4, 4, W.MXFP4),
                                    (1, 768, 768, 8, 2, W.MXFP4), (11, 1024, 256, 64, 6, W.MXFP4),
-                                   (6, 768, 512, 24, 4, W.NVFP4), (16, 256, 256, 256, 8, W.NVFP4)])
+                                   (6, 768, 512, 24, 4, W.NVFP4), (16, 256, 256, 256, 8, W.NVFP4),
+                                   (3, 512, 2560, 8, 4, W.NVFP4)])
 def test_tensor_core_decode_shapes(shape):
     """The tcgen05 decode on E = 256 with k = 8, a dense mixture (E == k) at
-    16 tokens, odd numbers of K chunks (H = I = 768), a mid-size case and two
-    NVFP4 layers; the CUDA-core decode on the same layer agrees."""
+    16 tokens, odd numbers of K chunks (H = I = 768), a mid-size case and
+    three NVFP4 layers, one with I = 2560 (h's UE4M3 scale blocks converted
+    in two chunks of 32); the CUDA-core decode on the same layer agrees."""
     T, H, I, E, k, fmt = shape
     wl = W.Workload("dcedge", T, H, I, E, k, fmt, 24, 0.5)
     lay = W.generate(wl)
